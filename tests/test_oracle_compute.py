@@ -1,0 +1,347 @@
+"""Pins of the oracle's arithmetic against what the mathematics and the pages fix.
+
+  - integer sub-block dots: brute force over unpacked codes;
+  - Q4_K x Q8_1 GEMV: the algebraic identity with dequantise-then-f64-dot (exact
+    when the stored s equals d*sum(q), bounded by the s rounding otherwise);
+  - zero padding 896 -> 1024 leaves the GEMV bit-identical (forward_utils.rs,
+    pad_and_upload_input);
+  - Q4_0 GEMV: exact integer sums with d = 1, linearity;
+  - RMSNorm: closed form on constant input, unit RMS, padding zeros
+    (using.rs, rms_norm_inplace);
+  - SiLU, RoPE and attention invariants; the first-token case of the attention
+    (clone_layer_weights.rs, forward_single_full_cuda_with_cache);
+  - layer / stack: identities that hold with zero weights.
+"""
+import numpy as np
+import pytest
+
+import rz_synth as S
+
+
+def _unpack_rows(orc, w, nsb):
+    """-> d, dmin (f64 [R, nsb]), sc, m ([R, nsb, 8]), q ([R, nsb, 256])"""
+    R = w.shape[0]
+    d = np.zeros((R, nsb))
+    dm = np.zeros((R, nsb))
+    sc = np.zeros((R, nsb, 8), np.int64)
+    mn = np.zeros((R, nsb, 8), np.int64)
+    q = np.zeros((R, nsb, 256), np.int64)
+    for r in range(R):
+        for b in range(nsb):
+            db, dmb, s_, m_, q_ = orc.q4k_unpack(w[r, b * 144:(b + 1) * 144])
+            d[r, b], dm[r, b] = orc.f16_to_f64(np.array([db, dmb], np.uint16))
+            sc[r, b], mn[r, b], q[r, b] = s_, m_, q_
+    return d, dm, sc, mn, q
+
+
+def test_subblock_dots_brute_force(orc):
+    out_dim, in_dim = 5, 768
+    w = S.q4k_weight("pin.dots.w", out_dim, in_dim)
+    x8 = orc.q8_1_quantize(S.normal("pin.dots.x", (1, in_dim)))
+    I = orc.q4k_q8_subblock_dots(w, x8, out_dim, in_dim)
+    _, _, q8 = orc.q8_1_fields(x8, 1, in_dim)          # [1, in/32, 32]
+    _, _, _, _, q = _unpack_rows(orc, w, in_dim // 256)
+    q4 = q.reshape(out_dim, in_dim // 32, 32)
+    brute = (q4 * q8[0].astype(np.int64)[None]).sum(axis=-1)
+    assert np.array_equal(I, brute)
+
+
+def test_gemv_identity_exact_case(orc):
+    """When every stored s equals d8*sum(q8) exactly, the factored integer dot equals
+    the dequantise-then-f64-dot up to f64 rounding."""
+    g = np.random.default_rng(11)
+    out_dim, in_dim, m = 6, 1024, 3
+    w = S.q4k_weight("pin.exact.w", out_dim, in_dim)
+    k = g.integers(-127, 128, (m, in_dim))
+    k[:, ::32] = 127                     # amax 127 in every block -> d8 = 1/8 exactly
+    k[:, 1::32] = -127                   # keeps |sum q| small so s = sum/8 is exact in fp16
+    x = (k * 0.125).astype(np.float32)
+    x8 = orc.q8_1_quantize(x)
+    d8, s8, q8 = orc.q8_1_fields(x8, m, in_dim)
+    assert np.all(d8 == 0.125)
+    assert np.array_equal(s8.astype(np.float64), 0.125 * q8.astype(np.int64).sum(-1))
+    y = orc.q4k_q8_gemv(w, x8, m, out_dim, in_dim).astype(np.float64)
+    W = orc.q4k_dequantize(w)                # f64 [out, in]
+    X = orc.q8_1_dequantize(x8, m, in_dim)   # f64 [m, in]
+    ref = X @ W.T
+    scale = np.abs(X) @ np.abs(W).T
+    # the oracle returns f32: allow the f32 rounding of the result plus f64 noise
+    assert np.all(np.abs(y - ref) <= np.abs(ref) * 2 ** -24 + 1e-12 * scale)
+
+
+def test_gemv_identity_random_bounded_by_s_rounding(orc):
+    out_dim, in_dim, m = 8, 1024, 2
+    w = S.q4k_weight("pin.ident.w", out_dim, in_dim)
+    x8 = orc.q8_1_quantize(S.normal("pin.ident.x", (m, in_dim)))
+    y = orc.q4k_q8_gemv(w, x8, m, out_dim, in_dim).astype(np.float64)
+    W = orc.q4k_dequantize(w)
+    X = orc.q8_1_dequantize(x8, m, in_dim)
+    ref = X @ W.T
+    d8, s8, q8 = orc.q8_1_fields(x8, m, in_dim)
+    s_true = d8.astype(np.float64) * q8.astype(np.int64).sum(-1)
+    s_err = np.abs(s8.astype(np.float64) - s_true)               # [m, in/32]
+    d, dm, sc, mn, q = _unpack_rows(orc, w, in_dim // 256)
+    coef = (dm[..., None] * mn).reshape(out_dim, in_dim // 32)   # dmin_b * m_bj
+    bound = s_err @ coef.T                                       # [m, out]
+    scale = np.abs(X) @ np.abs(W).T
+    diff = np.abs(y - ref)
+    assert np.all(diff <= bound + np.abs(ref) * 2 ** -24 + 1e-12 * scale)
+    assert bound.max() > 0     # the bound is live, not vacuous-zero
+
+
+def test_gemv_catches_dropped_min_term(orc):
+    """A variant without the -dmin*m*s term would be far outside the bound above."""
+    out_dim, in_dim = 4, 512
+    w = S.q4k_weight("pin.min.w", out_dim, in_dim)
+    x8 = orc.q8_1_quantize(S.normal("pin.min.x", (1, in_dim)))
+    y = orc.q4k_q8_gemv(w, x8, 1, out_dim, in_dim)[0].astype(np.float64)
+    W = orc.q4k_dequantize(w)
+    X = orc.q8_1_dequantize(x8, 1, in_dim)[0]
+    d, dm, sc, mn, q = _unpack_rows(orc, w, in_dim // 256)
+    no_min = ((d[..., None, None] * sc[..., None] *
+               q.reshape(out_dim, -1, 8, 32)).reshape(out_dim, in_dim)) @ X
+    assert np.max(np.abs(y - W @ X)) < 1e-3 * np.max(np.abs(y - no_min))
+
+
+def test_padding_invariance_896_to_1024(orc):
+    """Zero-padded activations make the padded weight columns irrelevant: random or
+    zero weights there give bit-identical outputs."""
+    out_dim = 64
+    w = S.q4k_weight("pin.pad.w", out_dim, 1024)
+    x = S.hidden_input("pin.pad.x", 2, 896, 1024)
+    x8 = orc.q8_1_quantize(x)
+    y_rand = orc.q4k_q8_gemv(w, x8, 2, out_dim, 1024)
+    # zero the codes of elements 896..1023 (super-block 3, sub-blocks 4..7)
+    w0 = w.copy()
+    for r in range(out_dim):
+        blk = w0[r, 3 * 144:4 * 144]
+        d, dm, sc, mn, q = orc.q4k_unpack(blk)
+        q[128:] = 0
+        sc[4:] = 0
+        mn[4:] = 0
+        w0[r, 3 * 144:4 * 144] = orc.q4k_pack(d, dm, sc, mn, q)
+    y_zero = orc.q4k_q8_gemv(w0, x8, 2, out_dim, 1024)
+    assert np.array_equal(y_rand.view(np.uint32), y_zero.view(np.uint32))
+    d8, s8, q8 = orc.q8_1_fields(x8, 2, 1024)
+    assert not d8[:, 28:].any() and not s8[:, 28:].any() and not q8[:, 28:].any()
+
+
+def test_q4_0_gemv_exact_integers(orc):
+    g = np.random.default_rng(2)
+    out_dim, in_dim = 7, 320
+    w = S.q4_0_weight("pin.q40.w", out_dim, in_dim).reshape(out_dim, in_dim // 32, 18)
+    w[:, :, 0], w[:, :, 1] = 0x00, 0x3C        # d = 1.0
+    w = w.reshape(out_dim, -1)
+    x = g.integers(-50, 51, (2, in_dim)).astype(np.float32)
+    y = orc.q4_0_gemv(w, x, out_dim, in_dim)
+    codes = np.zeros((out_dim, in_dim), np.int64)
+    for r in range(out_dim):
+        for b in range(in_dim // 32):
+            _, q = orc.q4_0_unpack(w[r, b * 18:(b + 1) * 18])
+            codes[r, b * 32:(b + 1) * 32] = q.astype(np.int64) - 8
+    assert np.array_equal(y.astype(np.int64), x.astype(np.int64) @ codes.T)
+
+
+def test_q4_0_gemv_linear(orc):
+    out_dim, in_dim = 16, 256
+    w = S.q4_0_weight("pin.q40lin.w", out_dim, in_dim)
+    x = S.normal("pin.q40lin.x", (1, in_dim))
+    z = S.normal("pin.q40lin.z", (1, in_dim))
+    W = orc.q4_0_dequantize(w)
+    y = lambda v: orc.q4_0_gemv(w, v, out_dim, in_dim).astype(np.float64)
+    lhs = y((0.5 * x + 2.0 * z).astype(np.float32))      # exact in f32 (power-of-2 scales)
+    rhs = 0.5 * y(x) + 2.0 * y(z)
+    scale = np.abs(W) @ (np.abs(x) + np.abs(z)).T
+    assert np.all(np.abs(lhs - rhs) <= 4 * 2 ** -24 * scale.T)
+
+
+def test_rmsnorm_constant_closed_form(orc):
+    for c, eps in [(0.01, 1e-6), (3.0, 1e-6), (-0.2, 1e-5)]:
+        n, n_pad = 896, 1024
+        x = np.zeros((1, n_pad), np.float32)
+        x[0, :n] = c
+        y = orc.rmsnorm(x, np.ones(n, np.float32), n, n_pad, eps)
+        expect = np.float32(np.float32(c) / np.sqrt(np.float64(np.float32(c)) ** 2 + np.float32(eps)))
+        assert np.allclose(y[0, :n], expect, rtol=2 ** -23, atol=0)
+        assert not y[0, n:].any()
+
+
+def test_rmsnorm_unit_rms_and_gamma(orc):
+    x = S.hidden_input("pin.rms.x", 3, 896, 1024) * 7.0
+    gam = S.uniform("pin.rms.g", 896, 0.5, 1.5)
+    y = orc.rmsnorm(x, gam, 896, 1024, 0.0).astype(np.float64)
+    rms = np.sqrt(np.mean((y[:, :896] / gam) ** 2, axis=1))
+    assert np.allclose(rms, 1.0, rtol=1e-6)
+    y2 = orc.rmsnorm(x * 0.25, gam, 896, 1024, 0.0)     # scale invariance at eps = 0
+    assert np.allclose(y2, y, rtol=1e-6, atol=1e-7)
+
+
+def test_silu_identities(orc):
+    assert orc.silu(0.0) == 0.0
+    for v in [0.1, 1.0, 3.3, 12.0]:
+        assert abs((orc.silu(v) - orc.silu(-v)) - v) < 1e-14 * max(1, v)
+    assert abs(orc.silu(40.0) - 40.0) < 1e-14 * 40
+    assert abs(orc.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) < 1e-16
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_invariants(orc, mode):
+    hd, H = 64, 3
+    v = S.normal(f"pin.rope.v{mode}", H * hd)
+    assert np.array_equal(orc.rope(v, H, hd, 0, 1e4, mode), v)          # position 0
+    r = orc.rope(v, H, hd, 37, 1e4, mode).astype(np.float64)
+    assert np.allclose(np.linalg.norm(r.reshape(H, hd), axis=1),
+                       np.linalg.norm(v.reshape(H, hd).astype(np.float64), axis=1), rtol=1e-6)
+    # group property: rope(rope(v, 20), 17) = rope(v, 37)
+    rr = orc.rope(orc.rope(v, H, hd, 20, 1e4, mode), H, hd, 17, 1e4, mode)
+    assert np.allclose(rr, r, atol=1e-5)
+    # relative position: <rope(q,p), rope(k,p')> depends on p - p' only
+    q = S.normal(f"pin.rope.q{mode}", hd)
+    k = S.normal(f"pin.rope.k{mode}", hd)
+    a = np.dot(orc.rope(q, 1, hd, 50, 1e4, mode), orc.rope(k, 1, hd, 45, 1e4, mode))
+    b = np.dot(orc.rope(q, 1, hd, 1005, 1e4, mode), orc.rope(k, 1, hd, 1000, 1e4, mode))
+    assert abs(a - b) < 1e-4 * (1 + abs(a))
+
+
+def test_rope_pairing_and_frequency_closed_form(orc):
+    hd = 8
+    p = 3
+    theta = 1e4
+    for mode, partner in [(0, {0: 1, 2: 3, 4: 5, 6: 7}), (1, {0: 4, 1: 5, 2: 6, 3: 7})]:
+        for i, (a, b) in enumerate(partner.items()):
+            v = np.zeros(hd, np.float32)
+            v[a] = 1.0
+            r = orc.rope(v, 1, hd, p, theta, mode)
+            ang = p * theta ** (-2.0 * i / hd)
+            assert abs(r[a] - np.cos(ang)) < 1e-6 and abs(r[b] - np.sin(ang)) < 1e-6
+            others = [j for j in range(hd) if j not in (a, b)]
+            assert not r[others].any()
+
+
+def test_attention_first_token_is_v_expanded(orc):
+    """Position 0 (empty cache before the token): the output is v, each q head taking
+    its kv head q_head / (n_heads / n_kv_heads)."""
+    H, Hkv, hd = 8, 2, 16
+    q = S.normal("pin.att0.q", H * hd)
+    kc = S.normal("pin.att0.k", (4, Hkv * hd))
+    vc = S.normal("pin.att0.v", (4, Hkv * hd))
+    out = orc.attention(q, kc, vc, 0, H, Hkv, hd)
+    for h in range(H):
+        kvh = h // (H // Hkv)
+        assert np.array_equal(out[h * hd:(h + 1) * hd], vc[0, kvh * hd:(kvh + 1) * hd])
+
+
+def test_attention_brute_force_and_uniform(orc):
+    H, Hkv, hd, pos = 4, 2, 8, 9
+    q = S.normal("pin.att.q", H * hd)
+    kc = S.normal("pin.att.k", (12, Hkv * hd))
+    vc = S.normal("pin.att.v", (12, Hkv * hd))
+    out = orc.attention(q, kc, vc, pos, H, Hkv, hd)
+    for h in range(H):
+        kvh = h // 2
+        K = kc[:pos + 1, kvh * hd:(kvh + 1) * hd].astype(np.float64)
+        V = vc[:pos + 1, kvh * hd:(kvh + 1) * hd].astype(np.float64)
+        s = K @ q[h * hd:(h + 1) * hd].astype(np.float64) / np.sqrt(hd)
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        assert np.allclose(out[h * hd:(h + 1) * hd], p @ V, rtol=1e-6, atol=1e-6)
+    # identical keys -> uniform weights -> mean of the values
+    kc_same = np.repeat(kc[:1], 12, axis=0)
+    out = orc.attention(q, kc_same, vc, pos, H, Hkv, hd)
+    for h in range(H):
+        kvh = h // 2
+        assert np.allclose(out[h * hd:(h + 1) * hd],
+                           vc[:pos + 1, kvh * hd:(kvh + 1) * hd].mean(axis=0), atol=1e-6)
+
+
+def _tiny_shape():
+    return S.LayerShape(hidden=448, inter=512, n_heads=7, n_kv_heads=1, head_dim=64,
+                        rope_theta=1e6, rope_mode=1)
+
+
+def _orc_layer(orc, L):
+    sh = L.shape
+    return orc.LayerWeights(**L.w, attn_gamma=L.attn_gamma, ffn_gamma=L.ffn_gamma,
+                            hidden=sh.hidden, hidden_pad=sh.hidden_pad, n_heads=sh.n_heads,
+                            n_kv_heads=sh.n_kv_heads, head_dim=sh.head_dim, inter=sh.inter,
+                            eps=sh.eps, rope_theta=sh.rope_theta, rope_mode=sh.rope_mode)
+
+
+def test_layer_zero_weights_is_identity(orc):
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.zero")
+    for k in L.w:
+        L.w[k] = np.zeros_like(L.w[k])        # d = dmin = 0: every weight is 0
+    lw = _orc_layer(orc, L)
+    x = S.hidden_input("pin.zero.x", 1, sh.hidden, sh.hidden_pad)[0]
+    kc, vc = S.kv_prefill(sh, "pin.zero", 16, 5)
+    out = orc.decode_layer(x, lw, kc[0], vc[0], 5)
+    assert np.array_equal(out, x)
+    assert not kc[0, 5].any() and not vc[0, 5].any()   # k = v = 0 written at pos
+
+
+def test_ffn_zero_down_or_gate_is_identity(orc):
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.ffn0")
+    x = S.hidden_input("pin.ffn0.x", 1, sh.hidden, sh.hidden_pad)[0]
+    for zero in ("wdown", "wgate"):
+        w = dict(L.w)
+        w[zero] = np.zeros_like(w[zero])
+        out = orc.swiglu_ffn(x, L.ffn_gamma, w["wgate"], w["wup"], w["wdown"],
+                             sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
+        assert np.array_equal(out, x)
+
+
+def test_layer_first_token_composition(orc):
+    """At position 0 the layer equals: x + O(q8(v expanded)) followed by the FFN, with
+    v = V(q8(norm x)) -- the first-token case of forward_single_full_cuda_with_cache."""
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.first")
+    lw = _orc_layer(orc, L)
+    x = S.hidden_input("pin.first.x", 1, sh.hidden, sh.hidden_pad)[0]
+    kc, vc = S.kv_prefill(sh, "pin.first", 8, 0)
+    out = orc.decode_layer(x, lw, kc[0], vc[0], 0)
+    n = orc.rmsnorm(x, L.attn_gamma, sh.hidden, sh.hidden_pad, sh.eps)
+    x8 = orc.q8_1_quantize(n)
+    v = orc.q4k_q8_gemv(L.w["wv"], x8, 1, sh.kv_dim, sh.hidden_pad)[0]
+    att = np.zeros(sh.q_pad, np.float32)
+    for h in range(sh.n_heads):
+        kvh = h // (sh.n_heads // sh.n_kv_heads)
+        att[h * sh.head_dim:(h + 1) * sh.head_dim] = v[kvh * sh.head_dim:(kvh + 1) * sh.head_dim]
+    o = orc.q4k_q8_gemv(L.w["wo"], orc.q8_1_quantize(att), 1, sh.hidden, sh.q_pad)[0]
+    r1 = np.zeros(sh.hidden_pad, np.float32)
+    r1[:sh.hidden] = x[:sh.hidden] + o
+    expect = orc.swiglu_ffn(r1, L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
+                            sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
+    assert np.array_equal(out, expect)
+    assert np.array_equal(vc[0, 0], v)
+
+
+def test_stack_zero_layers_is_norm_then_head(orc):
+    hidden, hp, vocab = 896, 1024, 100
+    x = S.hidden_input("pin.stack0.x", 1, hidden, hp)[0]
+    g = S.uniform("pin.stack0.g", hidden, 0.5, 1.5)
+    lm = S.q4_0_weight("pin.stack0.lm", vocab, hidden)
+    hid, logits = orc.decode_stack(x, [], [], [], 0, g, lm, vocab, hidden, hp, 1e-6)
+    assert np.array_equal(hid, x)
+    n = orc.rmsnorm(x, g, hidden, hp, 1e-6)[0, :hidden]
+    assert np.array_equal(logits, orc.q4_0_gemv(lm, n, vocab, hidden)[0])
+
+
+def test_ffn_gates_with_silu_of_gate_times_up(orc):
+    """cuda_swiglu_ffn: SiLU is applied to the gate projection, then multiplied by up;
+    both read the same quantised normed input; h is quantised again before down."""
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.ffnorder")
+    x = S.hidden_input("pin.ffnorder.x", 1, sh.hidden, sh.hidden_pad)[0]
+    out = orc.swiglu_ffn(x, L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
+                         sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
+    x8 = orc.q8_1_quantize(orc.rmsnorm(x, L.ffn_gamma, sh.hidden, sh.hidden_pad, sh.eps))
+    g = orc.q4k_q8_gemv(L.w["wgate"], x8, 1, sh.inter, sh.hidden_pad)[0].astype(np.float64)
+    u = orc.q4k_q8_gemv(L.w["wup"], x8, 1, sh.inter, sh.hidden_pad)[0].astype(np.float64)
+    h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+    dn = orc.q4k_q8_gemv(L.w["wdown"], orc.q8_1_quantize(h), 1, sh.hidden, sh.inter)[0]
+    assert np.allclose(out[:sh.hidden], x[:sh.hidden] + dn, rtol=0, atol=1e-6 * np.abs(dn).max())
+    h_swapped = (u / (1.0 + np.exp(-u)) * g).astype(np.float32)
+    dn_sw = orc.q4k_q8_gemv(L.w["wdown"], orc.q8_1_quantize(h_swapped), 1, sh.hidden, sh.inter)[0]
+    assert np.abs(dn_sw - dn).max() > 1e-2 * np.abs(dn).max()
