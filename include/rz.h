@@ -1,0 +1,163 @@
+/*
+ * rz.h -- C ABI of librz, the GB300 (sm_103a) Q4_K x Q8_1 single-token decode path.
+ *
+ * The operations follow the dp4a decode layer of realizar 0.8.5
+ * src/cuda/executor/cached.rs (transformer_layer_gpu_true_dp4a), the Q4_0 model
+ * forward of realizar 0.8.4 src/gpu/adapters/using.rs (GpuModelQ4::forward,
+ * q4_0_gemv_into, rms_norm_inplace), the GPU-resident stack of realizar 0.8.5
+ * src/cuda/executor/layers/forward_utils.rs (forward_all_layers_gpu_to_logits)
+ * and the single-token semantics of realizar 0.8.4
+ * src/gguf/cuda/clone_layer_weights.rs (forward_single_full_cuda_with_cache).
+ *
+ * Conventions for every entry point
+ *   - Pointers named w, x, y, q8, gamma, out, input, output, workspace, k, v are
+ *     DEVICE pointers owned by the caller.  librz never allocates device memory,
+ *     never synchronises the stream and never copies between host and device
+ *     (except rz_check_device_error, which reads one word back).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and returns immediately.  Launches are stream-ordered and can be captured
+ *     into a CUDA graph.
+ *   - Every shape, alignment and range check runs on the host before anything is
+ *     launched.  A failed check returns a non-zero rz_status, launches nothing and
+ *     sets a message readable with rz_last_error() (thread-local).
+ *   - Weights must be 16-byte aligned; f32 and Q8_1 buffers 16-byte aligned.
+ *   - Device-side conditions that the host cannot see (a position read from device
+ *     memory outside the cache, a bounded wait that ran out) never trap: the kernel
+ *     records a code in a device error word and skips the access; the host reads
+ *     and clears it with rz_check_device_error().
+ *
+ * Data formats (GGML convention for the weights; the pages name the types but do
+ * not print their layouts):
+ *   Q4_K  super-block of 256 weights in 144 bytes: f16 d | f16 dmin | 12 bytes of
+ *         eight 6-bit scales and eight 6-bit mins | 128 bytes of 4-bit quants.
+ *         weight = d * sc_j * q - dmin * m_j for sub-block j = e / 32; weight e is
+ *         nibble (e % 64 < 32 ? low : high) of qs[32 * (e / 64) + e % 32].
+ *         A matrix [out_dim][in_dim] is row-major: out_dim rows of in_dim / 256
+ *         consecutive super-blocks.
+ *   Q4_0  block of 32 weights in 18 bytes: f16 d | 16 bytes of 4-bit quants;
+ *         weight i = d * (q_i - 8), q_i the low nibble of byte i (i < 16) or the
+ *         high nibble of byte i - 16.  Row-major like Q4_K.
+ *   Q8_1  activations quantised in blocks of 32: d = max|x| / 127 (f32 division),
+ *         q = round-half-away(x / d) clamped to [-127, 127] (0 when d == 0),
+ *         s = d * sum(q).  A buffer for m rows of n values (n % 32 == 0) holds
+ *         int8 q[m][n], then f32 d[m][n/32], then f32 s[m][n/32]:
+ *         RZ_Q8_1_BYTES(m, n) bytes.  (d and s are f32 so that s stays finite for
+ *         block maxima beyond fp16 range / 32.)
+ */
+#ifndef RZ_H
+#define RZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RZ_OK = 0,
+    RZ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad enum */
+    RZ_ERR_SHAPE = 2,       /* dimension not a multiple of the block size, m > RZ_MAX_BATCH, ... */
+    RZ_ERR_ALIGN = 3,       /* pointer not 16-byte aligned */
+    RZ_ERR_CUDA = 4,        /* a CUDA runtime call failed (message has the CUDA error) */
+    RZ_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (rz_check_device_error) */
+    RZ_ERR_UNSUPPORTED = 6, /* no sm_103a device, or a configuration this build does not handle */
+    RZ_ERR_DEVICE = 7       /* a device-side range check failed (rz_check_device_error) */
+} rz_status;
+
+typedef void *rz_stream; /* cudaStream_t */
+
+#define RZ_Q4K_BLOCK_BYTES 144
+#define RZ_Q4K_BLOCK_WEIGHTS 256
+#define RZ_Q4_0_BLOCK_BYTES 18
+#define RZ_Q4_0_BLOCK_WEIGHTS 32
+#define RZ_Q8_1_BLOCK 32
+#define RZ_Q8_1_BYTES(m, n) ((m) * (n) + 8 * (m) * ((n) / 32))
+#define RZ_MAX_BATCH 16
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *rz_last_error(void);
+/* Library version string. */
+const char *rz_version(void);
+
+/*
+ * rz_q8_1_quantize -- Q8_1 quantisation of activations (q8_quantize_async in
+ * transformer_layer_gpu_true_dp4a, steps 2 and 5).
+ *   x    f32 [m][n], row-major.            q8  RZ_Q8_1_BYTES(m, n) bytes (output).
+ *   1 <= m, n % 32 == 0.  Bit-exact with the format definition above.
+ */
+rz_status rz_q8_1_quantize(const float *x, void *q8, int64_t m, int64_t n, rz_stream stream);
+
+/*
+ * rz_q4k_q8_gemv -- y = W x for Q4_K weights and Q8_1 activations, the integer
+ * GEMV behind every Q/K/V/O and FFN projection (q4k_q8_gemv_async in
+ * transformer_layer_gpu_true_dp4a, steps 3 and 6).
+ *   For token t < m and row r:
+ *     y[t][r] = sum_b d_b * sum_j sc_bj * d8_tbj * I_tbrj - dmin_b * sum_j m_bj * s_tbj
+ *   with I the exact int32 dot of the 32 codes of sub-block j.
+ *   w   Q4_K [out_dim][in_dim]     q8  Q8_1 of m rows of in_dim     y  f32 [m][out_dim]
+ *   1 <= m <= RZ_MAX_BATCH, in_dim % 256 == 0, out_dim >= 1.  Weights are read once
+ *   for all m tokens.  f32 combination order differs from a sequential sum
+ *   (deterministic run to run).
+ */
+rz_status rz_q4k_q8_gemv(const void *w, const void *q8, float *y, int64_t m, int64_t out_dim,
+                         int64_t in_dim, rz_stream stream);
+
+/*
+ * rz_q4k_q8_subblock_dots -- the integer sub-block dots alone, for exact checks:
+ *   I[r][k] = sum_{i<32} q4[r][32k + i] * q8[32k + i]   (one activation row)
+ *   I  int32 [out_dim][in_dim/32] (output).  in_dim % 256 == 0.
+ */
+rz_status rz_q4k_q8_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,
+                                  int64_t in_dim, rz_stream stream);
+
+/*
+ * rz_q4_0_gemv -- y = W x for Q4_0 weights and f32 activations (the LM head of
+ * GpuModelQ4::forward, q4_0_gemv_into; step 5 of that function).
+ *   w  Q4_0 [out_dim][in_dim]   x  f32 [m][in_dim]   y  f32 [m][out_dim]
+ *   in_dim % 32 == 0, 1 <= m <= RZ_MAX_BATCH.  Only w needs 16-byte alignment of
+ *   its base; rows of 18-byte blocks may start anywhere.
+ */
+rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
+                       int64_t in_dim, rz_stream stream);
+
+/*
+ * rz_rmsnorm -- RMSNorm with optional fused Q8_1 quantisation (rms_norm_inplace in
+ * using.rs; rmsnorm_gpu + q8_quantize_async in transformer_layer_gpu_true_dp4a):
+ *   rms = sqrt(sum_{i<n} x_i^2 / n + eps);  y_i = x_i / rms * gamma_i (i < n),
+ *   y_i = 0 for n <= i < n_pad (the zero padding of pad_and_upload_input).
+ *   x      f32 [m][n_pad] (only the first n of each row are read)
+ *   gamma  f32 [n]
+ *   y      f32 [m][n_pad] output, or NULL
+ *   q8     Q8_1 of m rows of n_pad (output), or NULL.  When given, it is exactly
+ *          the Q8_1 quantisation of the f32 y this call computes.
+ *   At least one of y, q8 non-NULL.  n >= 1, n_pad >= n, n_pad % 32 == 0 when q8.
+ */
+rz_status rz_rmsnorm(const float *x, const float *gamma, float *y, void *q8, int64_t m, int64_t n,
+                     int64_t n_pad, float eps, rz_stream stream);
+
+/*
+ * rz_residual_add -- out = a + b elementwise in f32 (residual_add_gpu, steps 7 and
+ * 10 of transformer_layer_gpu_true_dp4a).  out may alias a or b.  Bit-exact.
+ */
+rz_status rz_residual_add(const float *a, const float *b, float *out, int64_t n, rz_stream stream);
+
+/*
+ * rz_check_device_error -- synchronise `stream`, read the device error word of the
+ * current device and clear it.  *code_out (nullable) receives the raw code (0 = none).
+ * Returns RZ_OK, RZ_ERR_TIMEOUT (a bounded wait ran out) or RZ_ERR_DEVICE (a
+ * device-side range check failed and the access was skipped).
+ */
+rz_status rz_check_device_error(rz_stream stream, uint32_t *code_out);
+
+/*
+ * rz_set_pdl -- enable (default) or disable programmatic dependent launch between
+ * consecutive librz kernels in a stream.  With it a GEMV starts streaming its
+ * weights while the previous kernel finishes; results are identical either way.
+ */
+rz_status rz_set_pdl(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RZ_H */

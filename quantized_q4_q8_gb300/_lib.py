@@ -1,0 +1,84 @@
+"""ctypes binding of librz (argument marshalling only).
+
+Every function here forwards to the C entry point of the same name in
+include/rz.h.  Tensors are passed as raw device pointers (``tensor.data_ptr()``)
+and the stream as ``torch.cuda.current_stream().cuda_stream`` unless given.
+All computation happens in the CUDA kernels of librz; there is no fallback: if
+the shared library is missing or fails to load, importing raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librz.so")
+
+RZ_OK = 0
+STATUS_NAMES = {
+    0: "RZ_OK", 1: "RZ_ERR_INVALID_ARG", 2: "RZ_ERR_SHAPE", 3: "RZ_ERR_ALIGN",
+    4: "RZ_ERR_CUDA", 5: "RZ_ERR_TIMEOUT", 6: "RZ_ERR_UNSUPPORTED", 7: "RZ_ERR_DEVICE",
+}
+
+
+class RzError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_vp = C.c_void_p
+_i64 = C.c_int64
+_f32 = C.c_float
+
+# name -> argtypes (restype is rz_status = int unless listed in _RESTYPES)
+SIGNATURES = {
+    "rz_q8_1_quantize": [_vp, _vp, _i64, _i64, _vp],
+    "rz_q4k_q8_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "rz_q4k_q8_subblock_dots": [_vp, _vp, _vp, _i64, _i64, _vp],
+    "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "rz_rmsnorm": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _vp],
+    "rz_residual_add": [_vp, _vp, _vp, _i64, _vp],
+    "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
+    "rz_set_pdl": [C.c_int],
+    "rz_last_error": [],
+    "rz_version": [],
+}
+_RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load librz.so; raises if it is missing (build it with the package build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"librz is not built ({path} missing): run __graft_entry__.build() "
+                          "or python quantized_q4_q8_gb300/build.py")
+    lib = C.CDLL(path)
+    for name, args in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _RESTYPES.get(name, C.c_int)
+    _lib = lib
+    return lib
+
+
+def call(name: str, *args):
+    """Call a status-returning entry point; raise RzError on failure."""
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != RZ_OK:
+        raise RzError(name, st, lib.rz_last_error().decode())
+    return st
+
+
+def status(name: str, *args) -> int:
+    """Call an entry point and return its raw status (no raise)."""
+    return getattr(load(), name)(*args)
+
+
+def last_error() -> str:
+    return load().rz_last_error().decode()

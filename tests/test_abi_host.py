@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+librz builds here (nvcc cross-compiles for sm_103a), loads without a GPU, and
+exports every entry point include/rz.h declares.  Calls that need no launch
+(argument validation, version) are exercised too: a rejected call must return
+its error status before touching the device.
+"""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(rz_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import quantized_q4_q8_gb300 as rz
+    path = rz.build()
+    return C.CDLL(path), path
+
+
+def test_header_declares_the_path(lib):
+    names = _declared_symbols()
+    for required in ("rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4_0_gemv", "rz_rmsnorm",
+                     "rz_residual_add"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    L, path = lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(rz_[a-z0-9_]+)$", out, flags=re.M))
+    missing = _declared_symbols() - exported
+    assert not missing, f"declared but not exported: {sorted(missing)}"
+    for name in _declared_symbols():
+        getattr(L, name)
+
+
+def test_binding_signatures_cover_header(lib):
+    from quantized_q4_q8_gb300 import _lib
+    assert _declared_symbols() <= set(_lib.SIGNATURES), \
+        sorted(_declared_symbols() - set(_lib.SIGNATURES))
+
+
+def test_version_and_no_error(lib):
+    from quantized_q4_q8_gb300 import _lib
+    L = _lib.load()
+    assert b"sm_103a" in L.rz_version()
+    assert L.rz_last_error() == b""
+
+
+@pytest.mark.parametrize("call,args,status", [
+    ("rz_q8_1_quantize", (0, 16, 1, 32, None), 1),            # null x
+    ("rz_q8_1_quantize", (16, 16, 1, 33, None), 2),           # n % 32
+    ("rz_q8_1_quantize", (16, 17, 1, 32, None), 3),           # misaligned q8
+    ("rz_q4k_q8_gemv", (16, 16, 16, 17, 4, 256, None), 2),    # m > 16
+    ("rz_q4k_q8_gemv", (16, 16, 16, 1, 4, 300, None), 2),     # in_dim % 256
+    ("rz_q4k_q8_gemv", (16, 16, 16, 0, 4, 256, None), 1),     # m = 0
+    ("rz_q4k_q8_gemv", (24, 16, 16, 1, 4, 256, None), 3),     # misaligned w
+    ("rz_q4_0_gemv", (16, 16, 16, 1, 4, 48, None), 2),        # in_dim % 32
+    ("rz_rmsnorm", (16, 16, 0, 0, 1, 8, 8, 1e-6, None), 1),   # no output
+    ("rz_rmsnorm", (16, 16, 16, 16, 1, 8, 40, 1e-6, None), 2),  # n_pad % 32 with q8
+    ("rz_rmsnorm", (16, 16, 16, 0, 1, 9, 8, 1e-6, None), 1),  # n_pad < n
+    ("rz_residual_add", (16, 16, 16, 0, None), 1),            # n = 0
+])
+def test_argument_checks_fail_before_launch(lib, call, args, status):
+    """Rejected calls return their status and a message without any device work
+    (these pointers are not device memory and there is no GPU here)."""
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    st = _lib.status(call, *args)
+    assert st == status, (st, _lib.last_error())
+    assert _lib.last_error()
+
+
+def test_package_fails_loudly_without_library(tmp_path):
+    from quantized_q4_q8_gb300 import _lib
+    with pytest.raises(ImportError):
+        _lib._lib_backup = _lib._lib
+        try:
+            _lib._lib = None
+            _lib.load(str(tmp_path / "missing.so"))
+        finally:
+            _lib._lib = _lib._lib_backup

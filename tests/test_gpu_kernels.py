@@ -1,0 +1,183 @@
+"""GPU parity: each librz kernel against the CPU oracle on the same seeded inputs.
+
+Bars: Q8_1 codes, d, s and the integer sub-block dots bit-exact; f32 GEMV
+outputs within 1e-5 relative plus 1e-6 * ||row|| absolute; residual add
+bit-exact; RMSNorm's fused Q8_1 bit-exact against the oracle's quantisation of
+the GPU's own f32 output.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import rz_synth as S
+
+from gpu_common import (assert_gemv_close, check_no_device_error, row_norms_q4_0,
+                        row_norms_q4k, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rz():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_q4_q8_gb300 as rz
+    rz.load()
+    return rz
+
+
+# ----------------------------------------------------------------------------- Q8_1
+@pytest.mark.parametrize("m,n", [(1, 32), (1, 1024), (3, 896), (16, 4096), (1, 14336), (2, 4864)])
+def test_q8_1_bit_exact(rz, m, n):
+    x = S.normal(f"gq8.{m}.{n}", (m, n)) * np.float32(3.0)
+    x[0, :32] = 0.0                       # an all-zero block
+    if n >= 64:
+        x[0, 32:64] = 0.0
+        x[0, 40] = -7.25                  # one-hot block
+    q8 = rz.q8_1_quantize(to_dev(x)).cpu().numpy()
+    check_no_device_error()
+    assert np.array_equal(q8, oracle.q8_1_quantize(x))
+
+
+def test_q8_1_large_magnitudes_bit_exact(rz):
+    x = S.normal("gq8.big", (2, 512)) * np.float32(4.0e4)
+    q8 = rz.q8_1_quantize(to_dev(x)).cpu().numpy()
+    assert np.array_equal(q8, oracle.q8_1_quantize(x))
+
+
+# ----------------------------------------------------------------------------- Q4_K x Q8_1
+@pytest.mark.parametrize("out_dim,in_dim", [(256, 1024), (7, 256), (33, 512), (129, 768),
+                                            (64, 2048), (40, 1280), (17, 4864), (9, 11008),
+                                            (5, 14336)])
+def test_q4k_subblock_dots_bit_exact(rz, out_dim, in_dim):
+    w = S.q4k_weight(f"gdots.{out_dim}.{in_dim}", out_dim, in_dim)
+    x8 = oracle.q8_1_quantize(S.normal(f"gdots.x.{in_dim}", (1, in_dim)))
+    I = rz.q4k_q8_subblock_dots(to_dev(w), to_dev(x8), out_dim, in_dim).cpu().numpy()
+    assert np.array_equal(I, oracle.q4k_q8_subblock_dots(w, x8, out_dim, in_dim))
+
+
+GEMV_CASES = [
+    (256, 1024, 1),            # the small single-GEMV workload (4 super-blocks per row)
+    (1, 256, 1), (3, 512, 1), (129, 768, 1), (37, 1280, 1), (61, 1792, 1),
+    (300, 2048, 1), (1000, 4096, 1), (23, 4864, 1), (45, 11008, 1), (19, 14336, 1),
+    (256, 1024, 2), (100, 1024, 3), (77, 4096, 4), (50, 2304, 5), (33, 4096, 8),
+    (65, 1024, 16), (40, 4864, 16), (9, 14336, 16), (2000, 256, 7),
+]
+
+
+@pytest.mark.parametrize("out_dim,in_dim,m", GEMV_CASES)
+def test_q4k_gemv_parity(rz, out_dim, in_dim, m):
+    w = S.q4k_weight(f"ggemv.{out_dim}.{in_dim}", out_dim, in_dim)
+    x = S.normal(f"ggemv.x.{in_dim}.{m}", (m, in_dim))
+    x8 = oracle.q8_1_quantize(x)
+    y = rz.q4k_q8_gemv(to_dev(w), to_dev(x8), m, out_dim, in_dim).cpu().numpy()
+    check_no_device_error()
+    y_ref = oracle.q4k_q8_gemv(w, x8, m, out_dim, in_dim)
+    assert_gemv_close(y, y_ref, row_norms_q4k(w)[None, :], f"{out_dim}x{in_dim} m={m}")
+
+
+def test_q4k_gemv_deterministic(rz):
+    out_dim, in_dim, m = 512, 4096, 4
+    w = to_dev(S.q4k_weight("gdet.w", out_dim, in_dim))
+    x8 = to_dev(oracle.q8_1_quantize(S.normal("gdet.x", (m, in_dim))))
+    a = rz.q4k_q8_gemv(w, x8, m, out_dim, in_dim).cpu().numpy()
+    b = rz.q4k_q8_gemv(w, x8, m, out_dim, in_dim).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("out_dim,in_dim", S.LLAMA_SWEEP)
+@pytest.mark.parametrize("m", [1, 16])
+def test_q4k_gemv_full_size_sampled(rz, out_dim, in_dim, m):
+    """Full Llama-shaped sweep in the launch configuration the benchmark times;
+    the oracle recomputes a sample of rows (first, last, random)."""
+    w = S.q4k_weight(f"sweep.{out_dim}.{in_dim}", out_dim, in_dim)
+    x = S.normal(f"sweep.x.{in_dim}.{m}", (m, in_dim))
+    x8 = oracle.q8_1_quantize(x)
+    y = rz.q4k_q8_gemv(to_dev(w), to_dev(x8), m, out_dim, in_dim).cpu().numpy()
+    check_no_device_error()
+    g = np.random.default_rng(out_dim + in_dim + m)
+    rows = np.unique(np.concatenate([[0, 1, out_dim // 2, out_dim - 1],
+                                     g.integers(0, out_dim, 60)]))
+    y_ref = oracle.q4k_q8_gemv(w[rows], x8, m, len(rows), in_dim)
+    assert_gemv_close(y[:, rows], y_ref, row_norms_q4k(w[rows])[None, :], f"sweep {out_dim}x{in_dim}")
+    assert np.isfinite(y).all()
+
+
+def test_q4k_gemv_padding_invariance(rz):
+    """896 -> 1024: zero-padded activations make the padded weight columns
+    irrelevant on the GPU too (bit-identical outputs)."""
+    out_dim = 896
+    w = S.q4k_weight("gpad.w", out_dim, 1024)
+    x = S.hidden_input("gpad.x", 1, 896, 1024)
+    x8 = to_dev(oracle.q8_1_quantize(x))
+    y_rand = rz.q4k_q8_gemv(to_dev(w), x8, 1, out_dim, 1024).cpu().numpy()
+    w0 = w.copy()
+    w0[:, 3 * 144 + 16 + 64:4 * 144] = 0   # chunks 2, 3 of super-block 3: elements 896..1023
+    y_zero = rz.q4k_q8_gemv(to_dev(w0), x8, 1, out_dim, 1024).cpu().numpy()
+    assert np.array_equal(y_rand.view(np.uint32), y_zero.view(np.uint32))
+
+
+# ----------------------------------------------------------------------------- Q4_0
+@pytest.mark.parametrize("out_dim,in_dim,m", [(100, 896, 1), (33, 4096, 1), (7, 32, 1),
+                                              (50, 1000 // 32 * 32, 1), (64, 8192, 1),
+                                              (40, 896, 3), (17, 4096, 16), (300, 9216, 2)])
+def test_q4_0_gemv_parity(rz, out_dim, in_dim, m):
+    w = S.q4_0_weight(f"gq40.{out_dim}.{in_dim}", out_dim, in_dim)
+    x = S.normal(f"gq40.x.{in_dim}.{m}", (m, in_dim))
+    y = rz.q4_0_gemv(to_dev(w), to_dev(x), out_dim, in_dim).cpu().numpy()
+    check_no_device_error()
+    y_ref = oracle.q4_0_gemv(w, x, out_dim, in_dim)
+    assert_gemv_close(y, y_ref, row_norms_q4_0(w)[None, :], f"q4_0 {out_dim}x{in_dim} m={m}")
+
+
+@pytest.mark.parametrize("vocab,hidden", S.LM_HEADS)
+def test_q4_0_lm_head_full_size_sampled(rz, vocab, hidden):
+    w = S.q4_0_weight(f"lm.{vocab}.{hidden}", vocab, hidden)
+    x = S.normal(f"lm.x.{hidden}", (1, hidden))
+    y = rz.q4_0_gemv(to_dev(w), to_dev(x), vocab, hidden).cpu().numpy()
+    check_no_device_error()
+    g = np.random.default_rng(vocab)
+    rows = np.unique(np.concatenate([[0, vocab - 1], g.integers(0, vocab, 200)]))
+    y_ref = oracle.q4_0_gemv(w[rows], x, len(rows), hidden)
+    assert_gemv_close(y[:, rows], y_ref, row_norms_q4_0(w[rows])[None, :], f"lm head {vocab}")
+
+
+# ----------------------------------------------------------------------------- RMSNorm / residual
+@pytest.mark.parametrize("m,n,n_pad", [(1, 896, 1024), (1, 4096, 4096), (4, 896, 1024),
+                                       (16, 4096, 4096), (1, 100, 128), (2, 5, 32)])
+def test_rmsnorm_parity_and_fused_q8(rz, m, n, n_pad):
+    x = S.hidden_input(f"gnorm.{m}.{n}", m, n, n_pad) * np.float32(5.0)
+    g = S.uniform(f"gnorm.g.{n}", n, 0.5, 1.5)
+    y, q8 = rz.rmsnorm(to_dev(x), to_dev(g), n, n_pad, 1e-6)
+    y = y.cpu().numpy()
+    q8 = q8.cpu().numpy()
+    y_ref = oracle.rmsnorm(x, g, n, n_pad, 1e-6)
+    assert np.allclose(y, y_ref, rtol=2e-6, atol=1e-6 * np.abs(y_ref).max())
+    assert not y[:, n:].any()
+    # the fused quantisation is exactly Q8_1 of the GPU's own f32 output
+    assert np.array_equal(q8, oracle.q8_1_quantize(y))
+    # against the fully-oracle path: codes differ by at most one step
+    d1, s1, c1 = oracle.q8_1_fields(q8, m, n_pad)
+    d2, s2, c2 = oracle.q8_1_fields(oracle.q8_1_quantize(y_ref), m, n_pad)
+    assert np.abs(c1.astype(int) - c2.astype(int)).max() <= 1
+
+
+def test_rmsnorm_y_only_and_q8_only(rz):
+    x = S.hidden_input("gnorm2", 2, 896, 1024)
+    g = S.uniform("gnorm2.g", 896, 0.5, 1.5)
+    y, _ = rz.rmsnorm(to_dev(x), to_dev(g), 896, 1024, 1e-6, want_q8=False)
+    _, q8 = rz.rmsnorm(to_dev(x), to_dev(g), 896, 1024, 1e-6, want_y=False)
+    assert np.array_equal(q8.cpu().numpy(), oracle.q8_1_quantize(y.cpu().numpy()))
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 896, 4097])
+def test_residual_add_bit_exact(rz, n):
+    a = S.normal(f"gres.a.{n}", n)
+    b = S.normal(f"gres.b.{n}", n) * np.float32(1e3)
+    out = rz.residual_add(to_dev(a), to_dev(b)).cpu().numpy()
+    assert np.array_equal(out, oracle.residual_add(a, b))
+
+
+def test_device_errors_none_after_suite(rz):
+    check_no_device_error()
