@@ -1,0 +1,595 @@
+"""Benchmark of the Q4_K x Q8_1 decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rz|reference]
+                    [--workload stack|gemv] [--batch M] [--position P]
+
+Workloads (synthetic, seeded; rz_synth):
+  stack  one decode step of the 32-layer Llama-7B-shaped Q4_K stack (hidden 4096,
+         intermediate 11008, 32 heads, head_dim 128, f32 KV cache at position P,
+         M tokens) plus output RMSNorm and the Q4_0 LM head 32000 x 4096.
+  gemv   one Q4_K x Q8_1 GEMV 4096 x 14336 (M tokens), weights rotated through
+         copies larger than twice the L2.
+
+One JSON line on stdout (rank 0).  `value` is the achieved HBM bandwidth of the
+whole step: algorithmic bytes (quantised weights + activations + KV cache read
++ outputs) / device time, summed over ranks.  Multi-GPU runs are independent
+replicas (the path has no exchange step): `scaling` is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import rz_synth as S  # noqa: E402
+
+METRIC = "Q4_K×Q8_1 GEMV achieved HBM GB/s (% of GB300 peak); decode tokens/s/layer stack"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_file: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (sha256 of the .cu file), else None."""
+    src = os.path.join(ROOT, "quantized_q4_q8_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for fn in sorted(os.listdir(os.path.join(ROOT, "profiles"))) if os.path.isdir(
+            os.path.join(ROOT, "profiles")) else []:
+        if not fn.endswith((".md", ".txt")):
+            continue
+        txt = open(os.path.join(ROOT, "profiles", fn)).read()
+        m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", txt)
+        m_wl = re.search(r"workload:\s*(\S+)", txt)
+        m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+        if m_sha and m_tr and m_wl and m_sha.group(1) == sha and m_wl.group(1) == workload:
+            return int(m_tr.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, v: float, device) -> float:
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workloads
+class GemvWorkload:
+    """Q4_K x Q8_1 GEMV, out 4096 x in 14336 (the largest shape of the Llama sweep)."""
+    out_dim, in_dim = 4096, 14336
+    kernel_file = "gemv_q4k.cu"
+
+    def __init__(self, m: int):
+        self.m = m
+        self.name = f"q4k_q8_gemv_{self.out_dim}x{self.in_dim}_m{m}"
+
+    def setup(self, dev):
+        import torch
+        import quantized_q4_q8_gb300 as rz
+        self.rz = rz
+        self.w_host = S.q4k_weight(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim, self.in_dim)
+        self.wbytes = self.w_host.size
+        ncopies = max(2, int(np.ceil(2 * L2_BYTES / self.wbytes)) + 1)
+        w0 = torch.from_numpy(self.w_host).to(dev)
+        self.ws = [w0] + [w0.clone() for _ in range(ncopies - 1)]
+        self.x_host = S.normal(f"sweep.x.{self.in_dim}.{self.m}", (self.m, self.in_dim))
+        self.x = torch.from_numpy(self.x_host).to(dev)
+        self.q8 = rz.q8_1_quantize(self.x)
+        self.y = torch.empty((self.m, self.out_dim), dtype=torch.float32, device=dev)
+        self.i = 0
+        # pinned host buffers for the end-to-end leg
+        self.x_pin = torch.from_numpy(self.x_host).pin_memory()
+        self.y_pin = torch.empty((self.m, self.out_dim), dtype=torch.float32).pin_memory()
+
+    def bytes_per_step(self):
+        return self.wbytes + S.Q4K_BYTES * 0 + self.m * self.in_dim * 5 // 4 + self.m * self.out_dim * 4
+
+    def launches_per_step(self):
+        return 1
+
+    def step(self, stream):
+        w = self.ws[self.i % len(self.ws)]
+        self.i += 1
+        self.rz.rz_q4k_q8_gemv(w, self.q8, self.y, self.m, self.out_dim, self.in_dim, stream=stream)
+
+    def e2e_step(self, stream):
+        """host x -> device, quantise, GEMV, device y -> host (through the C ABI)."""
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.rz.rz_q8_1_quantize(self.x, self.q8, self.m, self.in_dim, stream=stream)
+        self.step(stream)
+        self.y_pin.copy_(self.y, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.m * self.in_dim * 4, self.m * self.out_dim * 4
+
+    def e2e_launches(self):
+        return 2
+
+    def dominant(self):
+        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.bytes_per_step(),
+                "launches_per_step": 1}
+
+    def cpu_sample(self):
+        """The oracle on a bounded sample: rows of the same matrix."""
+        import oracle
+        if not hasattr(self, "w_host"):
+            self.w_host = S.q4k_weight(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim,
+                                       self.in_dim)
+            self.x_host = S.normal(f"sweep.x.{self.in_dim}.{self.m}", (self.m, self.in_dim))
+            self.wbytes = self.w_host.size
+        rows = 96
+        x8 = oracle.q8_1_quantize(self.x_host)
+        w = np.ascontiguousarray(self.w_host[:rows])
+        t0 = time.perf_counter()
+        oracle.q4k_q8_gemv(w, x8, self.m, rows, self.in_dim)
+        dt = time.perf_counter() - t0
+        frac = rows / self.out_dim
+        return {"value": self.bytes_per_step() * frac / dt / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle", "sample": f"{rows} of {self.out_dim} rows of the {self.out_dim}x"
+                f"{self.in_dim} GEMV (m={self.m}), single-threaded C oracle, {dt:.1f} s"}
+
+    def config(self):
+        return {"workload": self.name, "out_dim": self.out_dim, "in_dim": self.in_dim,
+                "batch_tokens": self.m, "weight_copies": len(self.ws),
+                "l2": "weights rotated through copies > 2x L2"}
+
+    def config_ref(self):
+        return {"workload": self.name, "out_dim": self.out_dim, "in_dim": self.in_dim,
+                "batch_tokens": self.m}
+
+    def cpu_baseline(self):
+        return self.cpu_sample()
+
+    def dominant_time(self, stream):
+        return None
+
+
+class StackWorkload:
+    """One decode step of the 32-layer Llama-7B-shaped Q4_K stack + Q4_0 LM head."""
+    kernel_file = "gemv_q4k.cu"
+    n_layers = S.LLAMA_LAYERS
+    vocab = S.LLAMA_VOCAB
+    max_seq = S.LLAMA_MAX_SEQ
+
+    def __init__(self, m: int, position: int):
+        self.m = m
+        self.position = position
+        self.shape = S.LLAMA7B
+        self.name = f"llama7b_q4k_decode_stack_l{self.n_layers}_m{m}_pos{position}"
+
+    # ---- algorithmic bytes of one step
+    def weight_bytes(self):
+        sh = self.shape
+        return self.n_layers * (sh.weight_bytes() + 2 * sh.hidden * 4) + sh.hidden * 4 + \
+            self.vocab * (sh.hidden // 32) * S.Q4_0_BYTES
+
+    def bytes_per_step(self):
+        sh, m, p = self.shape, self.m, self.position
+        act = 0
+        for o, i in sh.weight_shapes().values():          # Q8_1 in, f32 out per GEMV
+            act += m * i * 5 // 4 + m * o * 4
+        kv = m * (p + 1) * sh.kv_dim * 4 * 2 + m * sh.kv_dim * 4 * 2   # read rows 0..p, write row p
+        per_layer = act + kv + 2 * m * sh.hidden_pad * 4                # layer input and output
+        head = m * sh.hidden * 4 + m * self.vocab * 4
+        return self.weight_bytes() + self.n_layers * per_layer + head
+
+    def gemv_bytes(self):
+        sh, m = self.shape, self.m
+        return self.n_layers * sum(o * (i // 256) * S.Q4K_BYTES + m * i * 5 // 4 + m * o * 4
+                                   for o, i in sh.weight_shapes().values())
+
+    def launches_per_step(self):
+        return self.n_layers * 9 + 2
+
+    def setup(self, dev):
+        import torch
+        import quantized_q4_q8_gb300 as rz
+        self.rz = rz
+        sh = self.shape
+        self.dls = []
+        for i in range(self.n_layers):
+            w = S.layer_device(sh, f"stack.l{i}", dev)
+            self.dls.append(rz.DeviceLayer(w, sh.hidden, sh.hidden_pad, sh.n_heads, sh.n_kv_heads,
+                                           sh.head_dim, sh.inter, sh.eps, sh.rope_theta,
+                                           sh.rope_mode))
+        self.kvs = [rz.DeviceKV(*S.kv_prefill_device(sh, f"stack.kv{i}", self.max_seq,
+                                                     self.position, self.m, dev))
+                    for i in range(self.n_layers)]
+        g = S.torch_gen("stack.out_gamma", dev)
+        self.out_gamma = torch.rand(sh.hidden, device=dev, generator=g) + 0.5
+        self.lm = S.q4_0_weight_device("stack.lm_head", self.vocab, sh.hidden, dev)
+        self.stack = rz.DeviceStack(self.dls, self.kvs, self.out_gamma, self.lm, self.vocab)
+        self.x = torch.zeros((self.m, sh.hidden_pad), dtype=torch.float32, device=dev)
+        self.x[:, :sh.hidden] = torch.randn((self.m, sh.hidden), device=dev,
+                                            generator=S.torch_gen("stack.x", dev))
+        self.ws = rz.workspace(self.stack.workspace_bytes(self.m), dev)
+        self.hid = torch.empty((self.m, sh.hidden_pad), dtype=torch.float32, device=dev)
+        self.logits = torch.empty((self.m, self.vocab), dtype=torch.float32, device=dev)
+        self.x_pin = self.x.cpu().pin_memory()
+        self.logits_pin = torch.empty((self.m, self.vocab), dtype=torch.float32).pin_memory()
+        self.graph = None
+        self.gemv_graph = None
+
+    def _launch(self, stream):
+        self.rz.rz_decode_stack(self.x, self.stack, None, self.position, self.m, self.hid,
+                                self.logits, self.ws, stream=stream)
+
+    def capture(self, stream):
+        import torch
+        self._launch(stream)          # eager warm-up outside the graph (sets attributes)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self._launch(stream)
+        torch.cuda.synchronize()
+
+    def step(self, stream):
+        if self.graph is None:
+            self.capture(stream)
+        self.graph.replay()
+
+    def e2e_step(self, stream):
+        """host hidden -> device, the whole stack, device logits -> host."""
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.graph.replay()
+        self.logits_pin.copy_(self.logits, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.m * self.shape.hidden_pad * 4, self.m * self.vocab * 4
+
+    def e2e_launches(self):
+        return self.launches_per_step()
+
+    def dominant(self):
+        n = self.n_layers * 7
+        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.gemv_bytes() / n,
+                "launches_per_step": n}
+
+    def dominant_time(self, stream, reps=5):
+        """Average duration of the Q4_K GEMV launches of one step: the 224 weight
+        matrices of the 32 layers launched back to back (CUDA graph) against the
+        layer's Q8_1 activation, timed with CUDA events on the stream."""
+        import torch
+        rz = self.rz
+        sh = self.shape
+        if self.gemv_graph is None:
+            dev = self.x.device
+            self.gx = {i: rz.q8_1_quantize(torch.randn((self.m, i), device=dev,
+                                                        generator=S.torch_gen(f"gx{i}", dev)))
+                       for i in {i for _, i in sh.weight_shapes().values()}}
+            self.gy = torch.empty((self.m, max(o for o, _ in sh.weight_shapes().values())),
+                                  device=dev)
+            def launch():
+                for dl in self.dls:
+                    for nm, (o, i) in sh.weight_shapes().items():
+                        rz.rz_q4k_q8_gemv(dl.t[nm], self.gx[i], self.gy, self.m, o, i,
+                                          stream=stream)
+            launch()
+            torch.cuda.synchronize()
+            self.gemv_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.gemv_graph, stream=stream):
+                launch()
+            torch.cuda.synchronize()
+        self.gemv_graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                self.gemv_graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * self.n_layers * 7)
+
+    def cpu_sample(self, n_sample_layers: int = 1):
+        """The oracle on n_sample_layers layers of the same shape plus the LM head, one
+        token, timed on this host; the step time is extrapolated from the mean layer time."""
+        import oracle
+        sh = self.shape
+        kc, vc = S.kv_prefill(sh, "cpu.kv", self.position + 1, self.position, 1)
+        x = S.hidden_input("cpu.x", 1, sh.hidden, sh.hidden_pad)[0]
+        t_layers = []
+        for li in range(n_sample_layers):
+            L = S.layer(sh, f"cpu.l{li}")
+            ol = oracle.LayerWeights(**L.w, attn_gamma=L.attn_gamma, ffn_gamma=L.ffn_gamma,
+                                     hidden=sh.hidden, hidden_pad=sh.hidden_pad,
+                                     n_heads=sh.n_heads, n_kv_heads=sh.n_kv_heads,
+                                     head_dim=sh.head_dim, inter=sh.inter, eps=sh.eps,
+                                     rope_theta=sh.rope_theta, rope_mode=sh.rope_mode)
+            t0 = time.perf_counter()
+            x = oracle.decode_layer(x, ol, kc[0], vc[0], self.position)
+            t_layers.append(time.perf_counter() - t0)
+        lm = S.q4_0_weight("cpu.lm", self.vocab, sh.hidden)
+        t0 = time.perf_counter()
+        oracle.q4_0_gemv(lm, x[:sh.hidden], self.vocab, sh.hidden)
+        t_head = time.perf_counter() - t0
+        t_layer = sum(t_layers) / len(t_layers)
+        t_step = (self.n_layers * t_layer + t_head) * self.m
+        one_token = StackWorkload(1, self.position)
+        return {"value": one_token.bytes_per_step() * self.m / t_step / 1e9, "unit": "GB/s",
+                "cores": 1, "kind": "oracle",
+                "tokens_per_s": self.m / t_step,
+                "sample": f"{n_sample_layers} of {self.n_layers} layers (single-threaded C "
+                          f"oracle, mean {t_layer:.2f} s per layer) + the Q4_0 LM head "
+                          f"({t_head:.2f} s), one token at position {self.position}; step time "
+                          f"extrapolated as {self.n_layers} x layer + head per token"}
+
+    def cpu_baseline(self):
+        return self.cpu_sample(n_sample_layers=16)
+
+    def config(self):
+        return {"workload": self.name, "layers": self.n_layers, "hidden": self.shape.hidden,
+                "intermediate": self.shape.inter, "heads": self.shape.n_heads,
+                "kv_heads": self.shape.n_kv_heads, "head_dim": self.shape.head_dim,
+                "vocab": self.vocab, "batch_tokens": self.m, "position": self.position,
+                "max_seq": self.max_seq,
+                "weights_bytes": self.weight_bytes(),
+                "l2": "inputs larger than L2 (3.7 GB of weights per step)",
+                "launch": "one CUDA graph per step (PDL edges between kernels)"}
+
+    def config_ref(self):
+        return self.config()
+
+
+WORKLOADS = {"gemv": GemvWorkload, "stack": StackWorkload}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_rz(args, world, rank, local, pg):
+    import torch
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import quantized_q4_q8_gb300 as rz
+    rz.load()
+    wl = WORKLOADS[args.workload](args.batch) if args.workload == "gemv" else \
+        WORKLOADS[args.workload](args.batch, args.position)
+    wl.setup(dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_line = wl.cpu_baseline()   # before any timing: the host is idle here
+    else:
+        cpu_line = None
+    stream = torch.cuda.Stream(device=dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wl.step(stream)
+    torch.cuda.synchronize()
+    st, code = rz.check_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error word after warm-up: 0x{code:x}")
+
+    # ---- device-timed region
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            wl.step(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop() if rank == 0 else None
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(pg, ms, dev)
+
+    # ---- dominant kernel: average launch duration over back-to-back launches
+    dom = wl.dominant()
+    dom_ms = wl.dominant_time(stream)
+    if dom_ms is None:   # the step is one launch of the dominant kernel
+        dom_ms = ms / dom["launches_per_step"]
+
+    # ---- end to end through the C ABI with host buffers
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wl.e2e_step(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            wl.e2e_step(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps, dev)
+    st, code = rz.check_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error word after timing: 0x{code:x}")
+
+    bytes_step = wl.bytes_per_step()
+    value = world * bytes_step / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = dom["bytes_per_launch"] / (dom_ms * 1e-3) / 1e9
+    traffic = profile_traffic(wl.kernel_file, wl.name)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "q4k_x_q8_1_int8dot_f32",
+        "data": "synthetic (seeded, distributions of the workload definition)",
+        "config": wl.config(),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "tokens_per_s": round(world * wl.m / (ms * 1e-3), 2),
+        "tokens_per_s_per_layer_stack": round(world * wl.m / (ms * 1e-3), 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": dom["kernel"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": wl.e2e_bytes()[0], "d2h_bytes_per_step": wl.e2e_bytes()[1],
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": args.steps * wl.launches_per_step(),
+        "clocks": clk,
+    }
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload](args.batch) if args.workload == "gemv" else \
+        WORKLOADS[args.workload](args.batch, args.position)
+    samples = []
+    for _ in range(args.steps):
+        samples.append(wl.cpu_sample())
+    v = statistics.median(s["value"] for s in samples)
+    cb = dict(samples[0])
+    cb["value"] = v
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": cb["unit"],
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 oracle", "data": "synthetic", "config": wl.config_ref(),
+        "cpu_baseline": cb,
+        "e2e": {"value": round(v, 4), "unit": cb["unit"], "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="rz", choices=["rz", "reference"])
+    ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--position", type=int, default=1024)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks have no work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local, pg = dist_setup(args.gpus)
+    run_rz(args, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -143,6 +143,108 @@ rz_status rz_rmsnorm(const float *x, const float *gamma, float *y, void *q8, int
 rz_status rz_residual_add(const float *a, const float *b, float *out, int64_t n, rz_stream stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Layer-level entry points.  They launch several kernels in stream order and
+ * use a caller-provided device workspace (size from the *_workspace_bytes
+ * function, base 16-byte aligned).  The workspace holds intermediates only; the
+ * attention counters inside it must be zero before the first call (fill the
+ * workspace with zeros once after allocating it); every completed call leaves
+ * them zero again.  Calls that share a workspace must not overlap on the GPU.
+ * ---------------------------------------------------------------------------
+ */
+
+/* One Q4_K decode layer (the weights of transformer_layer_gpu_true_dp4a).
+ * Matrices (Q4_K, row-major [out][in]):
+ *   wq [n_heads*head_dim][hidden_pad]   wk, wv [n_kv_heads*head_dim][hidden_pad]
+ *   wo [hidden][q_pad]                  q_pad = n_heads*head_dim rounded up to 256
+ *   wgate, wup [inter][hidden_pad]      wdown [hidden][inter]
+ * attn_gamma, ffn_gamma: f32 [hidden].  hidden_pad % 256 == 0 (the zero padding of
+ * pad_and_upload_input), inter % 256 == 0, head_dim % 32 == 0 and <= 256,
+ * n_heads % n_kv_heads == 0 with at most 16 query heads per kv head.
+ * rope_mode 0 rotates adjacent pairs (2i, 2i+1), 1 rotates (i, i + head_dim/2);
+ * the angle of pair i at position p is p * rope_theta^(-2i/head_dim). */
+typedef struct {
+    const void *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
+    const float *attn_gamma, *ffn_gamma;
+    int32_t hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter;
+    float eps, rope_theta;
+    int32_t rope_mode;
+} rz_layer_weights;
+
+/* f32 KV cache of one layer.  Row p of sequence t (token t of a batch) is at
+ * k + t*seq_stride + p*kv_dim (same for v), kv_dim = n_kv_heads*head_dim.
+ * seq_stride is ignored when m == 1; otherwise >= max_seq*kv_dim. */
+typedef struct {
+    float *k, *v;
+    int64_t seq_stride;
+    int32_t max_seq;
+} rz_kv_cache;
+
+/*
+ * rz_swiglu_ffn -- out = x + W_down q8( silu(W_gate q8(n)) * (W_up q8(n)) ),
+ * n = RMSNorm(x; gamma) (steps 8-10 of transformer_layer_gpu_true_dp4a;
+ * fused_ffn_swiglu_gpu_true_dp4a; SiLU of the gate times up as in cuda_swiglu_ffn
+ * of clone_layer_weights.rs).  x, out f32 [m][hidden_pad] (out may alias x;
+ * out[.][hidden..hidden_pad) is written as 0).
+ */
+size_t rz_swiglu_ffn_workspace_bytes(int64_t m, int64_t hidden_pad, int64_t inter);
+rz_status rz_swiglu_ffn(const float *x, const float *gamma, const void *w_gate, const void *w_up,
+                        const void *w_down, float *out, int64_t m, int64_t hidden,
+                        int64_t hidden_pad, int64_t inter, float eps, void *workspace,
+                        size_t ws_bytes, rz_stream stream);
+
+/*
+ * rz_attention_decode -- RoPE on q and k at each token's position, append k and v
+ * to the cache row `position`, then softmax(q k^T / sqrt(head_dim)) v over cache
+ * rows 0..position with the GQA map kv_head = q_head / (n_heads / n_kv_heads)
+ * (incremental_attention_async, step 4; first-token and GQA semantics of
+ * forward_single_full_cuda_with_cache).
+ *   q, k, v   f32 projections, token t at q + t*ld_qkv (same ld for k, v);
+ *             q [n_heads*head_dim], k, v [n_kv_heads*head_dim] per token.
+ *   positions device int32 [m] (each checked in the kernel against max_seq; a bad
+ *             one records RZ_ERR_DEVICE, skips its cache write and yields zeros),
+ *             or NULL to use `position` for every token (checked on the host).
+ *   att       f32 [m][n_heads*head_dim] output, or NULL.
+ *   att_q8    Q8_1 of m rows of q_pad (output, the O projection's input), or NULL.
+ */
+size_t rz_attention_workspace_bytes(int64_t m, int32_t n_heads, int32_t n_kv_heads,
+                                    int32_t head_dim, int32_t max_seq);
+rz_status rz_attention_decode(const float *q, const float *k, const float *v, int64_t ld_qkv,
+                              const rz_kv_cache *kv, const int32_t *positions, int32_t position,
+                              int64_t m, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                              float rope_theta, int32_t rope_mode, float *att, void *att_q8,
+                              void *workspace, size_t ws_bytes, rz_stream stream);
+
+/*
+ * rz_decode_layer -- one decode step of one layer for m tokens (m sequences),
+ * the step order of transformer_layer_gpu_true_dp4a.
+ *   input, output f32 [m][hidden_pad] (zero padding kept; output may alias input)
+ *   kv            this layer's cache, written at each token's position
+ *   positions     device int32 [m] or NULL for the host `position`
+ */
+size_t rz_decode_layer_workspace_bytes(const rz_layer_weights *w, int64_t m, int32_t max_seq);
+rz_status rz_decode_layer(const float *input, const rz_layer_weights *w, const rz_kv_cache *kv,
+                          const int32_t *positions, int32_t position, int64_t m, float *output,
+                          void *workspace, size_t ws_bytes, rz_stream stream);
+
+/*
+ * rz_decode_stack -- n_layers decode layers, then the output RMSNorm and the Q4_0
+ * LM head (forward_all_layers_gpu_to_logits; GpuModelQ4::forward steps 4-5).
+ *   layers, kvs   host arrays of n_layers descriptors (same hidden, hidden_pad,
+ *                 eps and kv max_seq for every layer)
+ *   out_gamma     f32 [hidden];  lm_head Q4_0 [vocab][hidden]
+ *   hidden_out    f32 [m][hidden_pad] final hidden state, or NULL
+ *   logits        f32 [m][vocab]
+ */
+size_t rz_decode_stack_workspace_bytes(const rz_layer_weights *layers, int32_t n_layers, int64_t m,
+                                       int32_t max_seq);
+rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
+                          int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
+                          const float *out_gamma, const void *lm_head, int64_t vocab,
+                          float *hidden_out, float *logits, void *workspace, size_t ws_bytes,
+                          rz_stream stream);
+
+/*
  * rz_check_device_error -- synchronise `stream`, read the device error word of the
  * current device and clear it.  *code_out (nullable) receives the raw code (0 = none).
  * Returns RZ_OK, RZ_ERR_TIMEOUT (a bounded wait ran out) or RZ_ERR_DEVICE (a

@@ -29,7 +29,30 @@ class RzError(RuntimeError):
 
 _vp = C.c_void_p
 _i64 = C.c_int64
+_i32 = C.c_int32
 _f32 = C.c_float
+_sz = C.c_size_t
+
+
+class LayerWeightsStruct(C.Structure):
+    """rz_layer_weights (device pointers and dims)."""
+    _fields_ = [
+        ("wq", _vp), ("wk", _vp), ("wv", _vp), ("wo", _vp),
+        ("wgate", _vp), ("wup", _vp), ("wdown", _vp),
+        ("attn_gamma", _vp), ("ffn_gamma", _vp),
+        ("hidden", _i32), ("hidden_pad", _i32), ("n_heads", _i32), ("n_kv_heads", _i32),
+        ("head_dim", _i32), ("inter", _i32),
+        ("eps", _f32), ("rope_theta", _f32), ("rope_mode", _i32),
+    ]
+
+
+class KvCacheStruct(C.Structure):
+    """rz_kv_cache."""
+    _fields_ = [("k", _vp), ("v", _vp), ("seq_stride", _i64), ("max_seq", _i32)]
+
+
+_LWP = C.POINTER(LayerWeightsStruct)
+_KVP = C.POINTER(KvCacheStruct)
 
 # name -> argtypes (restype is rz_status = int unless listed in _RESTYPES)
 SIGNATURES = {
@@ -39,12 +62,24 @@ SIGNATURES = {
     "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "rz_rmsnorm": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _vp],
     "rz_residual_add": [_vp, _vp, _vp, _i64, _vp],
+    "rz_swiglu_ffn_workspace_bytes": [_i64, _i64, _i64],
+    "rz_swiglu_ffn": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp, _sz, _vp],
+    "rz_attention_workspace_bytes": [_i64, _i32, _i32, _i32, _i32],
+    "rz_attention_decode": [_vp, _vp, _vp, _i64, _KVP, _vp, _i32, _i64, _i32, _i32, _i32, _f32,
+                            _i32, _vp, _vp, _vp, _sz, _vp],
+    "rz_decode_layer_workspace_bytes": [_LWP, _i64, _i32],
+    "rz_decode_layer": [_vp, _LWP, _KVP, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
+    "rz_decode_stack_workspace_bytes": [_LWP, _i32, _i64, _i32],
+    "rz_decode_stack": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
+                        _sz, _vp],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
     "rz_set_pdl": [C.c_int],
     "rz_last_error": [],
     "rz_version": [],
 }
-_RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p}
+_RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p,
+             "rz_swiglu_ffn_workspace_bytes": _sz, "rz_attention_workspace_bytes": _sz,
+             "rz_decode_layer_workspace_bytes": _sz, "rz_decode_stack_workspace_bytes": _sz}
 
 _lib = None
 

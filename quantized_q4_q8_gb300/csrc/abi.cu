@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/rz.h"
 #include "rz_common.cuh"
@@ -141,6 +142,8 @@ rz_status rz_q4k_q8_gemv(const void *w, const void *q8, float *y, int64_t m, int
     if (!aligned16(w) || !aligned16(q8) || !aligned16(y))
         return fail(RZ_ERR_ALIGN, "rz_q4k_q8_gemv: buffers must be 16-byte aligned");
     RZ_TRY(check_device());
+    if (!q4k_gemv_supported(m, in_dim, EPI_STORE))
+        return fail(RZ_ERR_UNSUPPORTED, "rz_q4k_q8_gemv: in_dim=%lld exceeds the shared-memory stage ring", (long long)in_dim);
     Q4kSegment seg{w, y, nullptr, out_dim};
     RZ_CUDA(launch_q4k_gemv(&seg, 1, EPI_STORE, q8, m, in_dim, static_cast<cudaStream_t>(stream)),
             "rz_q4k_q8_gemv launch");
@@ -231,6 +234,240 @@ rz_status rz_set_pdl(int enable)
 {
     t_last_error.clear();
     g_use_pdl = enable != 0;
+    return RZ_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- layer-level helpers
+namespace {
+
+rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, LayerDesc *out)
+{
+    if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
+    const void *ptrs[] = {w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma};
+    for (const void *p : ptrs) {
+        if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer", fn);
+        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
+    }
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld not in [1, %d]", fn, (long long)m, RZ_MAX_BATCH);
+    if (w->hidden < 1 || w->hidden_pad < w->hidden || w->hidden_pad % 256)
+        return fail(RZ_ERR_SHAPE, "%s: hidden=%d hidden_pad=%d (hidden_pad must be a multiple of 256 >= hidden)", fn,
+                    w->hidden, w->hidden_pad);
+    if (w->n_heads < 1 || w->n_kv_heads < 1 || w->n_heads % w->n_kv_heads)
+        return fail(RZ_ERR_SHAPE, "%s: n_heads=%d n_kv_heads=%d", fn, w->n_heads, w->n_kv_heads);
+    if (w->n_heads / w->n_kv_heads > 16) return fail(RZ_ERR_UNSUPPORTED, "%s: more than 16 query heads per kv head", fn);
+    if (w->head_dim < 32 || w->head_dim > 256 || w->head_dim % 32)
+        return fail(RZ_ERR_SHAPE, "%s: head_dim=%d (multiple of 32 in [32, 256])", fn, w->head_dim);
+    if (w->inter < 256 || w->inter % 256) return fail(RZ_ERR_SHAPE, "%s: inter=%d is not a multiple of 256", fn, w->inter);
+    if (!(w->eps >= 0.0f) || !(w->rope_theta > 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps/rope_theta", fn);
+    if (w->rope_mode != 0 && w->rope_mode != 1) return fail(RZ_ERR_INVALID_ARG, "%s: rope_mode=%d", fn, w->rope_mode);
+    const int q_dim = w->n_heads * w->head_dim;
+    const int q_pad = (q_dim + 255) / 256 * 256;
+    if (!q4k_gemv_supported(m, w->hidden_pad, EPI_SWIGLU) || !q4k_gemv_supported(m, q_pad, EPI_STORE) ||
+        !q4k_gemv_supported(m, w->inter, EPI_STORE))
+        return fail(RZ_ERR_UNSUPPORTED, "%s: a GEMV row is too wide for the shared-memory stage ring", fn);
+    LayerDesc d{w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma,
+                w->hidden, w->hidden_pad, w->n_heads, w->n_kv_heads, w->head_dim, w->inter,
+                w->eps, w->rope_theta, w->rope_mode};
+    *out = d;
+    return RZ_OK;
+}
+
+rz_status check_kv(const rz_kv_cache *kv, const char *fn, int64_t m, int kv_dim, KvDesc *out)
+{
+    if (!kv || !kv->k || !kv->v) return fail(RZ_ERR_INVALID_ARG, "%s: null KV cache", fn);
+    if (!aligned16(kv->k) || !aligned16(kv->v)) return fail(RZ_ERR_ALIGN, "%s: KV cache must be 16-byte aligned", fn);
+    if (kv->max_seq < 1) return fail(RZ_ERR_INVALID_ARG, "%s: max_seq=%d", fn, kv->max_seq);
+    if (m > 1 && kv->seq_stride < (int64_t)kv->max_seq * kv_dim)
+        return fail(RZ_ERR_SHAPE, "%s: seq_stride=%lld < max_seq*kv_dim", fn, (long long)kv->seq_stride);
+    *out = KvDesc{kv->k, kv->v, m > 1 ? kv->seq_stride : 0, kv->max_seq};
+    return RZ_OK;
+}
+
+rz_status check_position(const int32_t *positions, int32_t position, int max_seq, const char *fn)
+{
+    if (positions) {
+        if (!aligned16(positions) && (reinterpret_cast<uintptr_t>(positions) & 3u))
+            return fail(RZ_ERR_ALIGN, "%s: positions must be 4-byte aligned", fn);
+        return RZ_OK;
+    }
+    if (position < 0 || position >= max_seq)
+        return fail(RZ_ERR_INVALID_ARG, "%s: position=%d outside [0, %d)", fn, position, max_seq);
+    return RZ_OK;
+}
+
+rz_status check_ws(const void *ws, size_t have, size_t need, const char *fn)
+{
+    if (!ws) return fail(RZ_ERR_INVALID_ARG, "%s: null workspace", fn);
+    if (!aligned16(ws)) return fail(RZ_ERR_ALIGN, "%s: workspace must be 16-byte aligned", fn);
+    if (have < need) return fail(RZ_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, have, need);
+    return RZ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rz_swiglu_ffn_workspace_bytes(int64_t m, int64_t hidden_pad, int64_t inter)
+{
+    if (m < 1 || hidden_pad < 1 || inter < 1) return 0;
+    return ffn_workspace_bytes(m, hidden_pad, inter);
+}
+
+rz_status rz_swiglu_ffn(const float *x, const float *gamma, const void *w_gate, const void *w_up,
+                        const void *w_down, float *out, int64_t m, int64_t hidden, int64_t hidden_pad,
+                        int64_t inter, float eps, void *workspace, size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_swiglu_ffn";
+    t_last_error.clear();
+    if (!x || !gamma || !w_gate || !w_up || !w_down || !out) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    const void *ptrs[] = {x, gamma, w_gate, w_up, w_down, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld", fn, (long long)m);
+    if (hidden < 1 || hidden_pad < hidden || hidden_pad % 256 || inter < 256 || inter % 256)
+        return fail(RZ_ERR_SHAPE, "%s: hidden=%lld hidden_pad=%lld inter=%lld", fn, (long long)hidden,
+                    (long long)hidden_pad, (long long)inter);
+    if (!(eps >= 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps", fn);
+    RZ_TRY(check_ws(workspace, ws_bytes, ffn_workspace_bytes(m, hidden_pad, inter), fn));
+    RZ_TRY(check_device());
+    if (!q4k_gemv_supported(m, hidden_pad, EPI_SWIGLU) || !q4k_gemv_supported(m, inter, EPI_STORE))
+        return fail(RZ_ERR_UNSUPPORTED, "%s: a GEMV row is too wide for the shared-memory stage ring", fn);
+    RZ_CUDA(launch_swiglu_ffn(x, gamma, w_gate, w_up, w_down, out, m, hidden, hidden_pad, inter, eps, workspace,
+                              static_cast<cudaStream_t>(stream)),
+            "rz_swiglu_ffn launch");
+    return RZ_OK;
+}
+
+size_t rz_attention_workspace_bytes(int64_t m, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                    int32_t max_seq)
+{
+    if (m < 1 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1 || max_seq < 1) return 0;
+    if (check_device() != RZ_OK) return 0;
+    const int chunk = attention_chunk_len(max_seq, n_kv_heads, (int)m);
+    const int n_chunks = (max_seq + chunk - 1) / chunk;
+    const size_t group = (size_t)(n_heads / n_kv_heads);
+    auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+    return a256((size_t)m * n_heads * head_dim * 4) +
+           a256((size_t)m * n_kv_heads * n_chunks * group * (head_dim + 2) * 4) + a256((size_t)m * n_kv_heads * 4);
+}
+
+rz_status rz_attention_decode(const float *q, const float *k, const float *v, int64_t ld_qkv,
+                              const rz_kv_cache *kv, const int32_t *positions, int32_t position, int64_t m,
+                              int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float rope_theta,
+                              int32_t rope_mode, float *att, void *att_q8, void *workspace, size_t ws_bytes,
+                              rz_stream stream)
+{
+    const char *fn = "rz_attention_decode";
+    t_last_error.clear();
+    if (!q || !k || !v || (!att && !att_q8)) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld", fn, (long long)m);
+    if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || n_heads / n_kv_heads > 16)
+        return fail(RZ_ERR_SHAPE, "%s: n_heads=%d n_kv_heads=%d", fn, n_heads, n_kv_heads);
+    if (head_dim < 32 || head_dim > 256 || head_dim % 32) return fail(RZ_ERR_SHAPE, "%s: head_dim=%d", fn, head_dim);
+    if (rope_mode != 0 && rope_mode != 1) return fail(RZ_ERR_INVALID_ARG, "%s: rope_mode", fn);
+    if (!(rope_theta > 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: rope_theta", fn);
+    const int64_t q_dim = (int64_t)n_heads * head_dim, kv_dim = (int64_t)n_kv_heads * head_dim;
+    if (m > 1 && ld_qkv < q_dim) return fail(RZ_ERR_SHAPE, "%s: ld_qkv", fn);
+    if ((att && !aligned16(att)) || (att_q8 && !aligned16(att_q8)))
+        return fail(RZ_ERR_ALIGN, "%s: outputs must be 16-byte aligned", fn);
+    KvDesc kd;
+    RZ_TRY(check_kv(kv, fn, m, (int)kv_dim, &kd));
+    RZ_TRY(check_position(positions, position, kv->max_seq, fn));
+    const size_t need = rz_attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, kv->max_seq);
+    RZ_TRY(check_device());
+    RZ_TRY(check_ws(workspace, ws_bytes, need, fn));
+    LayerDesc L{};
+    L.n_heads = n_heads;
+    L.n_kv_heads = n_kv_heads;
+    L.head_dim = head_dim;
+    L.rope_theta = rope_theta;
+    L.rope_mode = rope_mode;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+    float *q_rot = reinterpret_cast<float *>(ws);
+    ws += a256((size_t)m * q_dim * 4);
+    const int chunk = attention_chunk_len(kv->max_seq, n_kv_heads, (int)m);
+    const int n_chunks = (kv->max_seq + chunk - 1) / chunk;
+    float *part = reinterpret_cast<float *>(ws);
+    ws += a256((size_t)m * n_kv_heads * n_chunks * (n_heads / n_kv_heads) * (head_dim + 2) * 4);
+    int *counters = reinterpret_cast<int *>(ws);
+    AttnArgs a = make_attn_args(L, m, kd, positions, position, q_rot, part, counters, q, k, v, ld_qkv, att, att_q8);
+    RZ_CUDA(launch_attention(a, static_cast<cudaStream_t>(stream)), "rz_attention_decode launch");
+    return RZ_OK;
+}
+
+size_t rz_decode_layer_workspace_bytes(const rz_layer_weights *w, int64_t m, int32_t max_seq)
+{
+    LayerDesc L;
+    if (max_seq < 1 || check_layer(w, "rz_decode_layer_workspace_bytes", m, &L) != RZ_OK) return 0;
+    if (check_device() != RZ_OK) return 0;
+    return layer_workspace_bytes(L, m, max_seq);
+}
+
+rz_status rz_decode_layer(const float *input, const rz_layer_weights *w, const rz_kv_cache *kv,
+                          const int32_t *positions, int32_t position, int64_t m, float *output, void *workspace,
+                          size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_decode_layer";
+    t_last_error.clear();
+    if (!input || !output) return fail(RZ_ERR_INVALID_ARG, "%s: null input/output", fn);
+    if (!aligned16(input) || !aligned16(output)) return fail(RZ_ERR_ALIGN, "%s: input/output alignment", fn);
+    LayerDesc L;
+    RZ_TRY(check_layer(w, fn, m, &L));
+    KvDesc kd;
+    RZ_TRY(check_kv(kv, fn, m, L.n_kv_heads * L.head_dim, &kd));
+    RZ_TRY(check_position(positions, position, kv->max_seq, fn));
+    RZ_TRY(check_device());
+    RZ_TRY(check_ws(workspace, ws_bytes, layer_workspace_bytes(L, m, kd.max_seq), fn));
+    RZ_CUDA(launch_decode_layer(input, L, kd, positions, position, m, output, workspace,
+                                static_cast<cudaStream_t>(stream)),
+            "rz_decode_layer launch");
+    return RZ_OK;
+}
+
+size_t rz_decode_stack_workspace_bytes(const rz_layer_weights *layers, int32_t n_layers, int64_t m, int32_t max_seq)
+{
+    LayerDesc L;
+    if (!layers || n_layers < 1 || max_seq < 1) return 0;
+    if (check_layer(&layers[0], "rz_decode_stack_workspace_bytes", m, &L) != RZ_OK) return 0;
+    if (check_device() != RZ_OK) return 0;
+    return stack_workspace_bytes(L, m, max_seq);
+}
+
+rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
+                          int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
+                          const float *out_gamma, const void *lm_head, int64_t vocab, float *hidden_out,
+                          float *logits, void *workspace, size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_decode_stack";
+    t_last_error.clear();
+    if (!input || !layers || !kvs || !out_gamma || !lm_head || !logits)
+        return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (n_layers < 1 || n_layers > 4096) return fail(RZ_ERR_INVALID_ARG, "%s: n_layers=%d", fn, n_layers);
+    if (vocab < 1) return fail(RZ_ERR_INVALID_ARG, "%s: vocab", fn);
+    const void *ptrs[] = {input, out_gamma, lm_head, logits};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
+    if (hidden_out && !aligned16(hidden_out)) return fail(RZ_ERR_ALIGN, "%s: hidden_out alignment", fn);
+    std::vector<LayerDesc> Ls((size_t)n_layers);
+    std::vector<KvDesc> Ks((size_t)n_layers);
+    for (int l = 0; l < n_layers; ++l) {
+        RZ_TRY(check_layer(&layers[l], fn, m, &Ls[l]));
+        RZ_TRY(check_kv(&kvs[l], fn, m, Ls[l].n_kv_heads * Ls[l].head_dim, &Ks[l]));
+        if (Ls[l].hidden != Ls[0].hidden || Ls[l].hidden_pad != Ls[0].hidden_pad || Ls[l].eps != Ls[0].eps ||
+            Ks[l].max_seq != Ks[0].max_seq || Ls[l].n_heads != Ls[0].n_heads ||
+            Ls[l].n_kv_heads != Ls[0].n_kv_heads || Ls[l].head_dim != Ls[0].head_dim || Ls[l].inter != Ls[0].inter)
+            return fail(RZ_ERR_SHAPE, "%s: layer %d differs in shape from layer 0", fn, l);
+    }
+    if (Ls[0].hidden % 32) return fail(RZ_ERR_SHAPE, "%s: hidden %% 32 != 0 (Q4_0 LM head blocks)", fn);
+    RZ_TRY(check_position(positions, position, Ks[0].max_seq, fn));
+    RZ_TRY(check_device());
+    RZ_TRY(check_ws(workspace, ws_bytes, stack_workspace_bytes(Ls[0], m, Ks[0].max_seq), fn));
+    RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, out_gamma, lm_head,
+                                vocab, hidden_out, logits, workspace, static_cast<cudaStream_t>(stream)),
+            "rz_decode_stack launch");
     return RZ_OK;
 }
 

@@ -33,6 +33,7 @@ struct Args {
     int wg;        // warps per row group
     int rp;        // row groups per CTA
     int m;
+    int64_t ldx;   // elements between tokens' activation rows
     int64_t rows_per_cta_max;
 };
 
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
                 float res[kRowUnroll][MT];
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    if (MT > 1 && t < a.m && active) load_x(a.x + t * a.in_dim + (int64_t)b * 32, xv);
+                    if (MT > 1 && t < a.m && active) load_x(a.x + t * a.ldx + (int64_t)b * 32, xv);
 #pragma unroll
                     for (int u = 0; u < kRowUnroll; ++u) {
                         const int64_t rr = r + (int64_t)u * a.rp;
@@ -166,7 +167,14 @@ cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t s)
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                              int64_t in_dim, cudaStream_t s)
 {
+    return launch_q4_0_gemv_ld(w, x, in_dim, y, m, out_dim, in_dim, s);
+}
+
+cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
+                                int64_t out_dim, int64_t in_dim, cudaStream_t s)
+{
     Args a = {};
+    a.ldx = ldx;
     a.w = static_cast<const uint8_t *>(w);
     a.x = x;
     a.y = y;

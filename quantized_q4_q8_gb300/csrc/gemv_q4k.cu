@@ -6,38 +6,52 @@
 // I_tbj the exact int32 dot of the 32 4-bit codes of sub-block j with the 32
 // int8 codes of the matching Q8_1 block.
 //
-// GB300 design.  The kernel is bound by streaming the 144-byte super-blocks
-// from HBM.  Each warp owns a contiguous range of output rows and runs its own
-// ring of shared-memory slots fed by the 1-D bulk copy engine (cp.async.bulk,
-// completion on an mbarrier): lane 0 keeps kSlots pieces of 8 super-blocks
-// (1152 bytes) in flight while the warp computes on the oldest one, so the
-// bytes in flight live in shared memory instead of registers.  Inside a piece
-// each group of 4 lanes takes one super-block and each lane one 32-byte chunk of
-// its quants (two sub-blocks: low and high nibbles), so the 32-element integer
-// dots are complete within a lane (dp4a on unsigned nibbles x signed int8) and
-// only the f32 combination crosses lanes, once per row, in a fixed order (the
-// result is deterministic).  Rows shorter than 8 super-blocks are packed
-// several to a piece.  Weights are read once for all m tokens.  Every wait on a
-// bulk copy is bounded; on expiry the warp records an error and drains.
+// GB300 design.  The kernel streams 144-byte super-blocks from HBM; compute is
+// a few dp4a per byte.  One CTA per SM owns a contiguous range of rows.  A
+// producer warp keeps a ring of ~16 KB shared-memory stages full with the 1-D
+// bulk copy engine (cp.async.bulk, completion counted on an mbarrier), so the
+// bytes in flight live in shared memory, not registers.  A stage holds whole
+// "packs" (one row, or 8/nsb rows when a row has fewer than 8 super-blocks);
+// sixteen consumer warps take packs round-robin, each waiting only on the stage
+// of its own pack and releasing it with one mbarrier arrival, so warps run ahead
+// of each other across stages and the ring stays full.  Within a pack each
+// group of 4 lanes takes a super-block (two at a time for independent work) and
+// each lane one 32-byte chunk of its quants (two sub-blocks: low and high
+// nibbles), so every 32-element integer dot completes inside one lane (dp4a of
+// unsigned nibbles with signed int8); only the f32 combination crosses lanes,
+// once per row, in a fixed order (deterministic results).  The Q8_1 codes are
+// staged in shared memory once per CTA when they fit, in padded 288-byte slots
+// per super-block so that the activation reads are free of bank conflicts.
+// The weight prologue is issued before waiting on the previous kernel
+// (programmatic dependent launch), so it overlaps that kernel's tail.  Every
+// wait is bounded; on expiry the kernel records an error code and drains its
+// outstanding copies instead of trapping.
+#include <algorithm>
+
 #include "rz_common.cuh"
 #include "rz_kernels.h"
 
 namespace rz {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 6;
-constexpr int kPieceSB = 8;
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSB = 144;
-constexpr int kPieceBytes = kPieceSB * kSB;
-constexpr int kWarpSmem = kSlots * kPieceBytes;
-constexpr int kSmemBytes = kWarps * kWarpSmem + kWarps * kSlots * 8;
+constexpr int kRingBudget = 160 * 1024;
+constexpr int kStageTarget = 16 * 1024;
+constexpr int kXSmemMax = 64 * 1024;
+constexpr int kMaxStages = 32;
+
+__host__ __device__ inline int64_t x_smem_bytes(int64_t m, int64_t in_dim)
+{
+    return m * (in_dim / 256) * 288 + 8 * m * (in_dim / 32);
+}
 
 struct Args {
     const uint8_t *w[3];
     float *y[3];
     const float *res[3];
+    int64_t ldy[3], ldr[3];
     int64_t seg_begin[4];  // first unit of segment k; seg_begin[nseg] == units
     int nseg;
     int64_t units;
@@ -48,42 +62,13 @@ struct Args {
     const float *xd;       // [m][in_dim/32]
     const float *xs;       // [m][in_dim/32]
     int64_t in_dim;
+    int rpp;               // rows per pack (8/nsb when nsb divides 8 and is < 8, else 1)
+    int PS;                // packs per stage
+    int NS;                // stages in the ring
+    int stage_bytes;       // PS * rpp * R * row_bytes
+    int x_smem;            // activations staged (swizzled) in shared memory
     unsigned *err;
 };
-
-struct Piece {
-    int64_t unit;  // first unit of the piece
-    int rows;      // whole rows in the piece (packed mode), else 1
-    int half;      // 0: gate / plain row, 1: up row (SwiGLU)
-    int sb0;       // first super-block of the row in this piece
-    int cnt;       // super-blocks per row in this piece
-    bool row_end;  // the piece ends its row
-};
-
-__device__ __forceinline__ Piece piece_of(int64_t p, int64_t u0, int64_t u1, int rpp, int ppr,
-                                          int R, int nsb)
-{
-    Piece pc;
-    if (rpp > 1) {
-        pc.unit = u0 + p * rpp;
-        pc.rows = (int)min((int64_t)rpp, u1 - pc.unit);
-        pc.half = 0;
-        pc.sb0 = 0;
-        pc.cnt = nsb;
-        pc.row_end = true;
-    } else {
-        int64_t per_unit = (int64_t)R * ppr;
-        pc.unit = u0 + p / per_unit;
-        int rem = (int)(p % per_unit);
-        pc.half = rem / ppr;
-        int pir = rem % ppr;
-        pc.sb0 = kPieceSB * pir;
-        pc.cnt = min(kPieceSB, nsb - pc.sb0);
-        pc.rows = 1;
-        pc.row_end = (pir == ppr - 1);
-    }
-    return pc;
-}
 
 __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
 {
@@ -92,112 +77,134 @@ __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
     return k;
 }
 
-template <int EPI>
-__device__ __forceinline__ const uint8_t *row_src(const Args &a, int64_t unit, int half)
+// Shared-memory copy of the Q8_1 codes.  Super-block sb of token t occupies a
+// 288-byte slot; the 64 bytes that lane chunk c reads (sub-blocks 2c, 2c+1) sit at
+// 64c + 16(c >> 1) inside it.  With this padding the 8 lanes of a shared-memory
+// phase (2 consecutive super-blocks x 4 chunks) hit 8 different bank groups, and
+// every address is a lane constant plus a multiple of the super-block index.
+constexpr int kXSlot = 288;
+
+__device__ __forceinline__ int x_chunk_off(int c) { return 64 * c + 16 * (c >> 1); }
+
+// Per-lane constants of the scale/min decode.  Lane chunk c owns sub-blocks
+// j0 = 2c and j1 = 2c + 1; the two 6-bit scales (and mins) are built for both
+// sub-blocks at once, one per byte, from the 16-bit windows A = s[k], s[k+1],
+// B = s[4+k], s[5+k], C = s[8+k], s[9+k] with k = j0 & 3:
+//   j < 4 : sc = A & 63,                    m = B & 63
+//   j >= 4: sc = (C & 15) | (A >> 6) << 4,  m = (C >> 4) | (B >> 6) << 4
+struct LaneConst {
+    uint32_t sh;       // 8 * k
+    uint32_t mask_lo;  // 0x3f3f for j < 4, else 0
+    uint32_t mask_c;   // 0x0f0f for j >= 4, else 0
+    uint32_t mask_hi;  // 0x3030 for j >= 4, else 0
+};
+
+__device__ __forceinline__ LaneConst lane_const(int c)
 {
-    if (EPI == EPI_SWIGLU) return a.w[half] + unit * a.row_bytes;
-    int k = seg_of(a, unit);
-    return a.w[k] + (unit - a.seg_begin[k]) * a.row_bytes;
+    LaneConst L;
+    L.sh = 8u * (uint32_t)((2 * c) & 3);
+    const bool hi = c >= 2;
+    L.mask_lo = hi ? 0u : 0x3f3fu;
+    L.mask_c = hi ? 0x0f0fu : 0u;
+    L.mask_hi = hi ? 0x3030u : 0u;
+    return L;
 }
 
-// lane 0: arm the slot barrier and start the copies of piece pc
-template <int EPI>
-__device__ __forceinline__ void issue_piece(const Args &a, const Piece &pc, uint8_t *slot,
-                                            uint64_t *bar)
+struct XSrc {
+    uint32_t q;        // shared-memory byte address of the codes (token 0) (smem copy)
+    uint32_t ds;       // shared-memory byte address of d (token 0); s follows at + m*nb*4
+    const int8_t *gq;  // global copies (when the activations stay in global memory)
+    const float *gd;
+    const float *gs;
+    int64_t in_dim, nb;
+    int m;
+};
+
+__device__ __forceinline__ int4 lds128(uint32_t addr)
 {
-    if (pc.rows > 1 || pc.cnt == a.nsb) {
-        // whole rows: one copy per run of rows contiguous in one segment
-        unsigned bytes = (unsigned)(pc.rows * a.row_bytes);
-        mbar_arrive_expect_tx(bar, bytes);
-        int r = 0;
-        while (r < pc.rows) {
-            int64_t u = pc.unit + r;
-            int run = 1;
-            if (EPI != EPI_SWIGLU) {
-                int k = seg_of(a, u);
-                int64_t left = a.seg_begin[k + 1] - u;
-                run = (int)min((int64_t)(pc.rows - r), left);
-            }
-            bulk_g2s(slot + (int64_t)r * a.row_bytes, row_src<EPI>(a, u, pc.half),
-                     (unsigned)(run * a.row_bytes), bar);
-            r += run;
-        }
-    } else {
-        unsigned bytes = (unsigned)(pc.cnt * kSB);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(slot, row_src<EPI>(a, pc.unit, pc.half) + (int64_t)pc.sb0 * kSB, bytes, bar);
-    }
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
-// Accumulate one super-block (shared memory at `blk`, row super-block index sb)
-// into acc[t] for every token; lane owns 32-byte quant chunk c = lane & 3.
-template <int MT>
-__device__ __forceinline__ void sb_accumulate(const Args &a, const uint8_t *blk, int sb, int c,
-                                              float (&acc)[MT])
+__device__ __forceinline__ float2 lds64f(uint32_t addr)
 {
-    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-    const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
-    const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
-    const float d = h2f((uint16_t)(hdr.x & 0xffffu));
-    const float dmin = h2f((uint16_t)(hdr.x >> 16));
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
 
-    // 6-bit scale and min of sub-blocks j0 = 2c and j1 = 2c + 1
-    const int k0 = (2 * c) & 3, k1 = (2 * c + 1) & 3;
-    const uint32_t a0 = (hdr.y >> (8 * k0)) & 0xffu, a1 = (hdr.y >> (8 * k1)) & 0xffu;
-    const uint32_t b0 = (hdr.z >> (8 * k0)) & 0xffu, b1 = (hdr.z >> (8 * k1)) & 0xffu;
-    uint32_t sc0, sc1, m0, m1;
-    if (c < 2) {
-        sc0 = a0 & 63u;
-        sc1 = a1 & 63u;
-        m0 = b0 & 63u;
-        m1 = b1 & 63u;
-    } else {
-        const uint32_t c0 = (hdr.w >> (8 * k0)) & 0xffu, c1 = (hdr.w >> (8 * k1)) & 0xffu;
-        sc0 = (c0 & 15u) | ((a0 >> 6) << 4);
-        sc1 = (c1 & 15u) | ((a1 >> 6) << 4);
-        m0 = (c0 >> 4) | ((b0 >> 6) << 4);
-        m1 = (c1 >> 4) | ((b1 >> 6) << 4);
-    }
-    const float dsc0 = d * (float)sc0, dsc1 = d * (float)sc1;
-    const float dm0 = dmin * (float)m0, dm1 = dmin * (float)m1;
+// Accumulate one super-block at shared address `blk`, super-block index sb of
+// its row, into acc[t]; the lane owns quant chunk c (sub-blocks 2c, 2c+1).
+template <int MT, bool XS>
+__device__ __forceinline__ void sb_accumulate(const XSrc &x, uint32_t blk, int sb, int c,
+                                              const LaneConst &L, float (&acc)[MT])
+{
+    const int4 hdr = lds128(blk);
+    const int4 qa = lds128(blk + 16 + 32 * c);
+    const int4 qb = lds128(blk + 32 + 32 * c);
+    const float d = h2f((uint16_t)((uint32_t)hdr.x & 0xffffu));
+    const float dmin = h2f((uint16_t)((uint32_t)hdr.x >> 16));
 
-    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t A = (uint32_t)hdr.y >> L.sh, B = (uint32_t)hdr.z >> L.sh, C = (uint32_t)hdr.w >> L.sh;
+    const uint32_t scp = (A & L.mask_lo) | (C & L.mask_c) | ((A >> 2) & L.mask_hi);
+    const uint32_t mnp = (B & L.mask_lo) | ((C >> 4) & L.mask_c) | ((B >> 2) & L.mask_hi);
+    const int sc0 = (int)(scp & 0xffu), sc1 = (int)((scp >> 8) & 0xffu);
+    const float dm0 = dmin * (float)(mnp & 0xffu), dm1 = dmin * (float)((mnp >> 8) & 0xffu);
+
+    const uint32_t q[8] = {(uint32_t)qa.x, (uint32_t)qa.y, (uint32_t)qa.z, (uint32_t)qa.w,
+                           (uint32_t)qb.x, (uint32_t)qb.y, (uint32_t)qb.z, (uint32_t)qb.w};
     int lo[8], hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         lo[i] = (int)(q[i] & 0x0f0f0f0fu);
         hi[i] = (int)((q[i] >> 4) & 0x0f0f0f0fu);
     }
-
-    const int64_t nb = a.in_dim / 32;
-    const int64_t jb = (int64_t)sb * 8 + 2 * c;  // Q8_1 block of sub-block j0
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-        if (t < a.m) {
-            const int4 *xp = reinterpret_cast<const int4 *>(a.xq + t * a.in_dim + jb * 32);
-            const int4 x0 = __ldg(xp), x1 = __ldg(xp + 1), x2 = __ldg(xp + 2), x3 = __ldg(xp + 3);
-            const float2 d8 = __ldg(reinterpret_cast<const float2 *>(a.xd + t * nb + jb));
-            const float2 s8 = __ldg(reinterpret_cast<const float2 *>(a.xs + t * nb + jb));
-            int i0 = 0, i1 = 0;
-            i0 = __dp4a(lo[0], x0.x, i0);
-            i0 = __dp4a(lo[1], x0.y, i0);
-            i0 = __dp4a(lo[2], x0.z, i0);
-            i0 = __dp4a(lo[3], x0.w, i0);
-            i0 = __dp4a(lo[4], x1.x, i0);
-            i0 = __dp4a(lo[5], x1.y, i0);
-            i0 = __dp4a(lo[6], x1.z, i0);
-            i0 = __dp4a(lo[7], x1.w, i0);
-            i1 = __dp4a(hi[0], x2.x, i1);
-            i1 = __dp4a(hi[1], x2.y, i1);
-            i1 = __dp4a(hi[2], x2.z, i1);
-            i1 = __dp4a(hi[3], x2.w, i1);
-            i1 = __dp4a(hi[4], x3.x, i1);
-            i1 = __dp4a(hi[5], x3.y, i1);
-            i1 = __dp4a(hi[6], x3.z, i1);
-            i1 = __dp4a(hi[7], x3.w, i1);
-            const float dot = dsc0 * (d8.x * (float)i0) + dsc1 * (d8.y * (float)i1);
-            const float mins = dm0 * s8.x + dm1 * s8.y;
-            acc[t] += dot - mins;
+        if (t < x.m) {
+            int4 x0, x1, x2, x3;
+            float2 d8, s8;
+            if (XS) {
+                const uint32_t xa = x.q + (uint32_t)(t * (x.in_dim / 256) + sb) * kXSlot + x_chunk_off(c);
+                x0 = lds128(xa);
+                x1 = lds128(xa + 16);
+                x2 = lds128(xa + 32);
+                x3 = lds128(xa + 48);
+                const uint32_t da = x.ds + (uint32_t)(t * x.nb + sb * 8 + 2 * c) * 4u;
+                d8 = lds64f(da);
+                s8 = lds64f(da + (uint32_t)(x.m * x.nb) * 4u);
+            } else {
+                const int64_t jb = (int64_t)sb * 8 + 2 * c;
+                const int4 *xp = reinterpret_cast<const int4 *>(x.gq + t * x.in_dim + jb * 32);
+                x0 = __ldg(xp);
+                x1 = __ldg(xp + 1);
+                x2 = __ldg(xp + 2);
+                x3 = __ldg(xp + 3);
+                d8 = __ldg(reinterpret_cast<const float2 *>(x.gd + t * x.nb + jb));
+                s8 = __ldg(reinterpret_cast<const float2 *>(x.gs + t * x.nb + jb));
+            }
+            // four independent dp4a chains (two per sub-block)
+            int a0 = __dp4a(lo[0], x0.x, 0), a1 = __dp4a(lo[4], x1.x, 0);
+            int b0 = __dp4a(hi[0], x2.x, 0), b1 = __dp4a(hi[4], x3.x, 0);
+            a0 = __dp4a(lo[1], x0.y, a0);
+            a1 = __dp4a(lo[5], x1.y, a1);
+            b0 = __dp4a(hi[1], x2.y, b0);
+            b1 = __dp4a(hi[5], x3.y, b1);
+            a0 = __dp4a(lo[2], x0.z, a0);
+            a1 = __dp4a(lo[6], x1.z, a1);
+            b0 = __dp4a(hi[2], x2.z, b0);
+            b1 = __dp4a(hi[6], x3.z, b1);
+            a0 = __dp4a(lo[3], x0.w, a0);
+            a1 = __dp4a(lo[7], x1.w, a1);
+            b0 = __dp4a(hi[3], x2.w, b0);
+            b1 = __dp4a(hi[7], x3.w, b1);
+            // sc * I is exact in int32; one conversion per sub-block
+            const float t0 = (float)(sc0 * (a0 + a1)) * d8.x;
+            const float t1 = (float)(sc1 * (b0 + b1)) * d8.y;
+            acc[t] = fmaf(d, t0 + t1, acc[t]) - (dm0 * s8.x + dm1 * s8.y);
         }
     }
 }
@@ -207,132 +214,175 @@ __device__ __forceinline__ float silu_mul(float g, float u)
     return g / (1.0f + expf(-g)) * u;
 }
 
-template <int MT, int EPI>
-__device__ __forceinline__ void write_unit(const Args &a, int64_t unit, const float (&v)[MT],
-                                           const float (&gate)[MT], int lane)
-{
-    int k = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
-    const int64_t rows = a.seg_begin[k + 1] - a.seg_begin[k];
-    const int64_t lr = unit - a.seg_begin[k];
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        if (t < a.m && lane == (t & 31)) {
-            float out = v[t];
-            if (EPI == EPI_RESID) out = a.res[k][t * rows + lr] + out;
-            if (EPI == EPI_SWIGLU) out = silu_mul(gate[t], v[t]);
-            a.y[k][t * rows + lr] = out;
-        }
-    }
-}
-
-template <int MT, int EPI>
-__global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const Args a)
+template <int MT, int EPI, bool XS>
+__global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    uint8_t *ring = smem + warp * kWarpSmem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * kWarpSmem) + warp * kSlots;
+    uint8_t *ring = smem;
+    uint8_t *xsm = smem + (int64_t)a.NS * a.stage_bytes;
+    const int64_t xbytes = XS ? x_smem_bytes(a.m, a.in_dim) : 0;
+    uint64_t *full = reinterpret_cast<uint64_t *>(xsm + xbytes);
+    uint64_t *empty = full + a.NS;
 
-    // units of this CTA, then of this warp (balanced contiguous ranges)
-    const int64_t G = gridDim.x;
-    const int64_t c0 = a.units * blockIdx.x / G, c1 = a.units * (blockIdx.x + 1) / G;
-    const int64_t u0 = c0 + (c1 - c0) * warp / kWarps;
-    const int64_t u1 = c0 + (c1 - c0) * (warp + 1) / kWarps;
-
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = (EPI == EPI_SWIGLU) ? 2 : 1;
-    const int rpp = (EPI != EPI_SWIGLU && a.nsb < kPieceSB && kPieceSB % a.nsb == 0)
-                        ? kPieceSB / a.nsb : 1;
-    const int ppr = (a.nsb + kPieceSB - 1) / kPieceSB;
-    const int64_t nu = u1 - u0;
-    const int64_t npieces = (rpp > 1) ? (nu + rpp - 1) / rpp : nu * R * ppr;
+    const int64_t G = gridDim.x;
+    const int64_t r0 = a.units * blockIdx.x / G, r1 = a.units * (blockIdx.x + 1) / G;
+    const int64_t npacks = (r1 - r0 + a.rpp - 1) / a.rpp;
+    const int64_t nstages = (npacks + a.PS - 1) / a.PS;
+    const int64_t pack_bytes = (int64_t)a.rpp * a.row_bytes;  // one half (gate or up)
 
-    if (lane == 0) {
-        for (int s = 0; s < kSlots; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.PS);  // one arrival per pack
+        }
         fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
-    // prologue: weights do not depend on the previous kernel
-    if (lane == 0) {
-        for (int64_t p = 0; p < npieces && p < kSlots; ++p)
-            issue_piece<EPI>(a, piece_of(p, u0, u1, rpp, ppr, R, a.nsb), ring + p * kPieceBytes,
-                             &bars[p]);
-    }
-    pdl_launch_dependents();
-    pdl_wait();  // activations come from the previous kernel
-
-    const int g = lane >> 2, c = lane & 3;
-    float acc[MT], gate[MT];
-#pragma unroll
-    for (int t = 0; t < MT; ++t) acc[t] = gate[t] = 0.0f;
-
-    for (int64_t p = 0; p < npieces; ++p) {
-        const int s = (int)(p % kSlots);
-        const unsigned parity = (unsigned)((p / kSlots) & 1);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[s], parity));
-        if (!ok) {
-            if (lane == 0) {
-                set_error(a.err, DEV_TIMEOUT_GEMV);
-                for (int64_t q = p; q < npieces && q < p + kSlots; ++q)
-                    if (!mbar_wait(&bars[q % kSlots], (unsigned)((q / kSlots) & 1)))
-                        set_error(a.err, DEV_TIMEOUT_DRAIN);
-            }
-            return;
-        }
-        const Piece pc = piece_of(p, u0, u1, rpp, ppr, R, a.nsb);
-        const uint8_t *slot = ring + s * kPieceBytes;
-
-        if (rpp > 1) {
-            // several whole rows: group g -> row g / nsb, super-block g % nsb
-            const int rip = g / a.nsb;
-            float pacc[MT];
-#pragma unroll
-            for (int t = 0; t < MT; ++t) pacc[t] = 0.0f;
-            if (rip < pc.rows) sb_accumulate<MT>(a, slot + g * kSB, g % a.nsb, c, pacc);
-            const int seg = 4 * a.nsb;  // lanes per row: 4, 8 or 16
-#pragma unroll
-            for (int t = 0; t < MT; ++t)
-                for (int o = 1; o < seg; o <<= 1) pacc[t] += __shfl_xor_sync(0xffffffffu, pacc[t], o);
-            if ((lane % seg) == 0 && rip < pc.rows) {
-                const int64_t unit = pc.unit + rip;
-                const int k = seg_of(a, unit);
-                const int64_t rows = a.seg_begin[k + 1] - a.seg_begin[k];
-                const int64_t lr = unit - a.seg_begin[k];
-#pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    if (t < a.m) {
-                        float out = pacc[t];
-                        if (EPI == EPI_RESID) out = a.res[k][t * rows + lr] + out;
-                        a.y[k][t * rows + lr] = out;
-                    }
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int64_t k = 0;
+            bool ok = true;
+            for (; k < nstages; ++k) {
+                const int s = (int)(k % a.NS);
+                if (k >= a.NS && !mbar_wait(&empty[s], (unsigned)(((k / a.NS) - 1) & 1))) {
+                    set_error(a.err, DEV_TIMEOUT_GEMV);
+                    ok = false;
+                    break;
                 }
-            }
-        } else {
-            if (g < pc.cnt) sb_accumulate<MT>(a, slot + g * kSB, pc.sb0 + g, c, acc);
-            if (pc.row_end) {
-#pragma unroll
-                for (int t = 0; t < MT; ++t) acc[t] = warp_sum(acc[t]);
-                if (EPI == EPI_SWIGLU && pc.half == 0) {
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        gate[t] = acc[t];
-                        acc[t] = 0.0f;
+                const int64_t u0 = r0 + k * a.PS * a.rpp;
+                const int n = (int)min((int64_t)a.PS * a.rpp, r1 - u0);  // rows in this stage
+                uint8_t *dst = ring + (int64_t)s * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], (unsigned)(R * n * a.row_bytes));
+                if (EPI == EPI_SWIGLU) {
+                    // stage layout: pack p -> [gate rows | up rows]
+                    for (int p = 0; p * a.rpp < n; ++p) {
+                        const int nr = min(a.rpp, n - p * a.rpp);
+                        const int64_t u = u0 + (int64_t)p * a.rpp;
+                        uint8_t *pd = dst + (int64_t)p * 2 * pack_bytes;
+                        bulk_g2s(pd, a.w[0] + u * a.row_bytes, (unsigned)(nr * a.row_bytes), &full[s]);
+                        bulk_g2s(pd + pack_bytes, a.w[1] + u * a.row_bytes, (unsigned)(nr * a.row_bytes),
+                                 &full[s]);
                     }
                 } else {
-                    write_unit<MT, EPI>(a, pc.unit, acc, gate, lane);
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+                    int r = 0;
+                    while (r < n) {
+                        const int64_t u = u0 + r;
+                        const int kseg = seg_of(a, u);
+                        const int run = (int)min((int64_t)(n - r), a.seg_begin[kseg + 1] - u);
+                        bulk_g2s(dst + (int64_t)r * a.row_bytes,
+                                 a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
+                                 (unsigned)(run * a.row_bytes), &full[s]);
+                        r += run;
+                    }
                 }
             }
+            // drain: stages issued but possibly not complete must land before exit
+            if (!ok) {
+                for (int64_t q = (k > a.NS ? k - a.NS : 0); q < k; ++q)
+                    if (!mbar_wait(&full[q % a.NS], (unsigned)((q / a.NS) & 1)))
+                        set_error(a.err, DEV_TIMEOUT_DRAIN);
+            }
         }
+        pdl_launch_dependents();
+        return;
+    }
 
-        // refill this slot with piece p + kSlots
+    // ---------------------------------------------------------------- consumers
+    pdl_wait();  // activations and the output buffers belong to the previous kernel
+    XSrc x;
+    x.in_dim = a.in_dim;
+    x.nb = a.in_dim / 32;
+    x.m = a.m;
+    x.gq = a.xq;
+    x.gd = a.xd;
+    x.gs = a.xs;
+    if (XS) {
+        // codes: 16-byte chunk i of super-block sbg (all tokens) -> padded slot layout
+        const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
+        const int4 *src = reinterpret_cast<const int4 *>(a.xq);
+        for (int64_t i = threadIdx.x; i < nsbx * 16; i += kConsumerWarps * 32) {
+            const int64_t sbg = i >> 4;
+            const int ch = (int)(i & 15), cc = ch >> 2;
+            *reinterpret_cast<int4 *>(xsm + sbg * kXSlot + x_chunk_off(cc) + 16 * (ch & 3)) = src[i];
+        }
+        // d and s, unchanged
+        const int64_t nds = 2LL * a.m * x.nb / 4;
+        const int4 *dsrc = reinterpret_cast<const int4 *>(a.xd);
+        int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
+        for (int64_t i = threadIdx.x; i < nds; i += kConsumerWarps * 32) ddst[i] = dsrc[i];
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        x.q = smem_u32(xsm);
+        x.ds = smem_u32(xsm + nsbx * kXSlot);
+    }
+
+    const int g = lane >> 2, c = lane & 3;
+    const LaneConst Lc = lane_const(c);
+    const int seg_lanes = (a.rpp > 1) ? 4 * a.nsb : 32;
+    const int rip = (a.rpp > 1) ? g / a.nsb : 0;  // row of the pack this group works on
+    const int leader = lane % seg_lanes == 0;
+    const uint32_t ring_s = smem_u32(ring);
+
+    for (int64_t i = warp; i < npacks; i += kConsumerWarps) {
+        const int64_t k = i / a.PS;
+        const int s = (int)(k % a.NS);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (unsigned)((k / a.NS) & 1)));
+        if (!ok) {
+            if (lane == 0) set_error(a.err, DEV_TIMEOUT_GEMV);
+            return;
+        }
+        const int64_t pack0 = r0 + i * a.rpp;
+        const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
+        const uint32_t pk = ring_s + (uint32_t)(s * a.stage_bytes + (i % a.PS) * R * pack_bytes);
+        float acc[2][MT], acc2[2][MT];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[h][t] = acc2[h][t] = 0.0f;
+#pragma unroll
+        for (int h = 0; h < R; ++h) {
+            const uint32_t half = pk + (uint32_t)(h * pack_bytes);
+            if (a.rpp > 1) {
+                if (rip < pack_rows)
+                    sb_accumulate<MT, XS>(x, half + g * kSB, g % a.nsb, c, Lc, acc[h]);
+            } else {
+                int sb = g;
+                if (MT <= 2) {
+                    for (; sb + 8 < a.nsb; sb += 16) {  // two independent super-blocks per step
+                        sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
+                        sb_accumulate<MT, XS>(x, half + (sb + 8) * kSB, sb + 8, c, Lc, acc2[h]);
+                    }
+                }
+                for (; sb < a.nsb; sb += 8) sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
+            }
+        }
         __syncwarp();
-        if (lane == 0 && p + kSlots < npieces) {
-            fence_proxy_async_smem();
-            issue_piece<EPI>(a, piece_of(p + kSlots, u0, u1, rpp, ppr, R, a.nsb),
-                             ring + s * kPieceBytes, &bars[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);  // the slot's bytes are no longer read
+        // reduce over the lanes of each row (fixed order)
+#pragma unroll
+        for (int h = 0; h < R; ++h)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                acc[h][t] += acc2[h][t];
+                for (int o = 1; o < seg_lanes; o <<= 1) acc[h][t] += __shfl_xor_sync(0xffffffffu, acc[h][t], o);
+            }
+        if (rip < pack_rows) {
+            const int64_t unit = pack0 + rip;
+            const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
+            const int64_t lr = unit - a.seg_begin[kseg];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                // spread the token stores over the lanes of the row
+                if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
+                    float out = acc[0][t];
+                    if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                    if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
+                    a.y[kseg][t * a.ldy[kseg] + lr] = out;
+                }
+            }
         }
     }
 }
@@ -359,38 +409,52 @@ __global__ void q4k_subblock_dots_kernel(const uint8_t *w, const int8_t *xq, int
     I[idx] = acc;
 }
 
-template <int MT, int EPI>
+size_t smem_bytes(const Args &a)
+{
+    const int64_t xbytes = a.x_smem ? x_smem_bytes(a.m, a.in_dim) : 0;
+    return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 2 * 8 * (size_t)a.NS;
+}
+
+template <int MT, int EPI, bool XS>
 cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
 {
     static bool attr_done[64] = {};
     const int dev = dev_info().device;
+    const size_t smem = smem_bytes(a);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI>, a);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS>, a);
+}
+
+template <int MT, int EPI>
+cudaError_t launch_x(const Args &a, int grid, cudaStream_t s)
+{
+    return a.x_smem ? launch_t<MT, EPI, true>(a, grid, s) : launch_t<MT, EPI, false>(a, grid, s);
 }
 
 template <int EPI>
 cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s)
 {
-    if (a.m <= 1) return launch_t<1, EPI>(a, grid, s);
-    if (a.m <= 2) return launch_t<2, EPI>(a, grid, s);
-    if (a.m <= 4) return launch_t<4, EPI>(a, grid, s);
-    if (a.m <= 8) return launch_t<8, EPI>(a, grid, s);
-    return launch_t<16, EPI>(a, grid, s);
+    if (a.m <= 1) return launch_x<1, EPI>(a, grid, s);
+    if (a.m <= 2) return launch_x<2, EPI>(a, grid, s);
+    if (a.m <= 4) return launch_x<4, EPI>(a, grid, s);
+    if (a.m <= 8) return launch_x<8, EPI>(a, grid, s);
+    return launch_x<16, EPI>(a, grid, s);
 }
 
 }  // namespace
@@ -399,22 +463,28 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
                             int64_t m, int64_t in_dim, cudaStream_t s)
 {
     Args a = {};
-    a.nseg = nseg;
     int64_t units = 0;
     for (int k = 0; k < nseg; ++k) {
         a.w[k] = static_cast<const uint8_t *>(seg[k].w);
         a.y[k] = seg[k].y;
         a.res[k] = seg[k].res;
-        a.seg_begin[k] = (epilogue == EPI_SWIGLU) ? 0 : units;
-        if (epilogue != EPI_SWIGLU) units += seg[k].rows;
+        a.ldy[k] = seg[k].ldy ? seg[k].ldy : seg[k].rows;
+        a.ldr[k] = seg[k].ldr ? seg[k].ldr : seg[k].rows;
+        if (epilogue != EPI_SWIGLU) {
+            a.seg_begin[k] = units;
+            units += seg[k].rows;
+        }
     }
     if (epilogue == EPI_SWIGLU) {
         units = seg[0].rows;
         a.nseg = 1;  // outputs indexed by unit through segment 0
+        a.seg_begin[0] = 0;
         a.seg_begin[1] = units;
     } else {
+        a.nseg = nseg;
         a.seg_begin[nseg] = units;
     }
+    const int R = (epilogue == EPI_SWIGLU) ? 2 : 1;
     a.units = units;
     a.nsb = (int)(in_dim / 256);
     a.row_bytes = (int64_t)a.nsb * kSB;
@@ -424,16 +494,39 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
     a.xd = reinterpret_cast<const float *>(static_cast<const uint8_t *>(q8) + m * in_dim);
     a.xs = a.xd + m * (in_dim / 32);
     a.err = dev_error_word();
+    a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
+    const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
+    a.PS = (int)std::max<int64_t>(1, kStageTarget / pack);
+    a.stage_bytes = (int)(a.PS * pack);
+    const int64_t xbytes = x_smem_bytes(m, in_dim);
+    a.x_smem = xbytes <= kXSmemMax ? 1 : 0;
+    const int64_t budget = (int64_t)dev_info().smem_optin - (a.x_smem ? xbytes : 0) - 1024;
+    int64_t ns = std::min<int64_t>(kRingBudget, budget) / a.stage_bytes;
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 2) return cudaErrorInvalidConfiguration;  // excluded by q4k_gemv_supported
+    a.NS = (int)ns;
+    if ((int64_t)smem_bytes(a) > (int64_t)dev_info().smem_optin) return cudaErrorInvalidConfiguration;
 
     const int sms = dev_info().sm_count;
-    int64_t grid = (units + kWarps - 1) / kWarps;
-    if (grid > 2 * sms) grid = 2 * sms;
+    int64_t grid = units < sms ? units : sms;
     if (grid < 1) grid = 1;
     switch (epilogue) {
     case EPI_STORE: return launch_epi<EPI_STORE>(a, (int)grid, s);
     case EPI_RESID: return launch_epi<EPI_RESID>(a, (int)grid, s);
     default: return launch_epi<EPI_SWIGLU>(a, (int)grid, s);
     }
+}
+
+bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue)
+{
+    const int R = (epilogue == EPI_SWIGLU) ? 2 : 1;
+    const int64_t nsb = in_dim / 256;
+    const int64_t rpp = (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1;
+    const int64_t pack = R * rpp * nsb * kSB;
+    const int64_t stage = std::max<int64_t>(1, kStageTarget / pack) * pack;
+    const int64_t xbytes = x_smem_bytes(m, in_dim);
+    const int64_t budget = (int64_t)dev_info().smem_optin - (xbytes <= kXSmemMax ? xbytes : 0) - 1024;
+    return std::min<int64_t>(kRingBudget, budget) / stage >= 2;
 }
 
 cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,

@@ -1,0 +1,207 @@
+// layer.cu -- the SwiGLU FFN, the decode layer and the decode stack as launch
+// sequences on one stream (no host synchronisation, no allocation).
+//
+// Step order of transformer_layer_gpu_true_dp4a (realizar 0.8.5
+// src/cuda/executor/cached.rs):
+//   1 RMSNorm(attn) -> 2 Q8_1 once for Q, K and V -> 3 Q/K/V GEMVs ->
+//   4 incremental attention -> 5 Q8_1 of the attention output -> 6 O GEMV ->
+//   7 residual -> 8 RMSNorm(ffn) -> 9 SwiGLU FFN (gate, up, silu(gate) * up, Q8_1,
+//   down) -> 10 residual.
+// Fusions here: 1+2 are one kernel (the norm writes the Q8_1 directly); Q, K and
+// V are one GEMV launch over the three matrices; RoPE and the KV append are one
+// small kernel; 4+5 are one split-sequence attention kernel whose merging CTA
+// quantises its heads; 6+7 and 9(down)+10 are GEMVs with a residual epilogue;
+// gate and up are one GEMV launch whose epilogue applies silu(gate) * up.
+// The stack (forward_all_layers_gpu_to_logits in realizar 0.8.5
+// src/cuda/executor/layers/forward_utils.rs) chains the layers through two
+// workspace buffers, then the output RMSNorm and the Q4_0 LM head.
+#include <algorithm>
+
+#include "rz_common.cuh"
+#include "rz_kernels.h"
+
+namespace rz {
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static size_t q8_bytes(int64_t m, int64_t n) { return (size_t)(m * n + 8 * m * (n / 32)); }
+
+size_t ffn_workspace_bytes(int64_t m, int64_t hidden_pad, int64_t inter)
+{
+    return align256(q8_bytes(m, hidden_pad)) + align256((size_t)m * inter * 4) +
+           align256(q8_bytes(m, inter));
+}
+
+cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_gate, const void *w_up,
+                              const void *w_down, float *out, int64_t m, int64_t hidden,
+                              int64_t hidden_pad, int64_t inter, float eps, void *workspace,
+                              cudaStream_t s)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *x8 = ws;
+    ws += align256(q8_bytes(m, hidden_pad));
+    float *h = reinterpret_cast<float *>(ws);
+    ws += align256((size_t)m * inter * 4);
+    void *h8 = ws;
+
+    cudaError_t e = launch_rmsnorm(x, gamma, nullptr, x8, m, hidden, hidden_pad, eps, s);
+    if (e != cudaSuccess) return e;
+    Q4kSegment gu[2] = {{w_gate, h, nullptr, inter, inter, 0}, {w_up, nullptr, nullptr, inter, 0, 0}};
+    e = launch_q4k_gemv(gu, 2, EPI_SWIGLU, x8, m, hidden_pad, s);
+    if (e != cudaSuccess) return e;
+    e = launch_q8_1_quantize(h, h8, m, inter, s);
+    if (e != cudaSuccess) return e;
+    Q4kSegment dn = {w_down, out, x, hidden, hidden_pad, hidden_pad};
+    e = launch_q4k_gemv(&dn, 1, EPI_RESID, h8, m, inter, s);
+    if (e != cudaSuccess) return e;
+    if (hidden_pad > hidden)
+        e = cudaMemset2DAsync(out + hidden, (size_t)hidden_pad * 4, 0, (size_t)(hidden_pad - hidden) * 4,
+                              (size_t)m, s);
+    return e;
+}
+
+// ---------------------------------------------------------------- decode layer
+struct LayerWs {
+    void *x8;
+    float *qkv, *q_rot, *part;
+    int *counters;
+    void *a8;
+    float *res1;
+    void *ffn;
+    size_t total;
+};
+
+static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *base)
+{
+    LayerWs w{};
+    const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
+    const int q_pad = (q_dim + 255) / 256 * 256;
+    const int group = L.n_heads / L.n_kv_heads;
+    const int chunk = attention_chunk_len(max_seq, L.n_kv_heads, (int)m);
+    const int n_chunks = (max_seq + chunk - 1) / chunk;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.x8 = take(q8_bytes(m, L.hidden_pad));
+    w.qkv = reinterpret_cast<float *>(take((size_t)m * (q_dim + 2 * kv_dim) * 4));
+    w.q_rot = reinterpret_cast<float *>(take((size_t)m * q_dim * 4));
+    w.part = reinterpret_cast<float *>(
+        take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4));
+    w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
+    w.a8 = take(q8_bytes(m, q_pad));
+    w.res1 = reinterpret_cast<float *>(take((size_t)m * L.hidden_pad * 4));
+    w.ffn = take(ffn_workspace_bytes(m, L.hidden_pad, L.inter));
+    w.total = off;
+    return w;
+}
+
+size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
+{
+    return layer_ws(L, m, max_seq, nullptr).total;
+}
+
+// Offset of the attention counters inside the layer workspace (they must be
+// zero before the first call; every completed call leaves them zero).
+size_t layer_counter_offset(const LayerDesc &L, int64_t m, int max_seq)
+{
+    uint8_t *base = reinterpret_cast<uint8_t *>(256);
+    return (size_t)(reinterpret_cast<uint8_t *>(layer_ws(L, m, max_seq, base).counters) - base);
+}
+
+AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
+                        int position, float *q_rot, float *part, int *counters, const float *q,
+                        const float *k, const float *v, int64_t ld_qkv, float *att, void *att_q8)
+{
+    AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.ld_qkv = ld_qkv;
+    a.q_rot = q_rot;
+    a.kc = kv.k;
+    a.vc = kv.v;
+    a.seq_stride = kv.seq_stride;
+    a.max_seq = kv.max_seq;
+    a.positions = positions;
+    a.position = position;
+    a.m = (int)m;
+    a.n_heads = L.n_heads;
+    a.n_kv_heads = L.n_kv_heads;
+    a.head_dim = L.head_dim;
+    a.group = L.n_heads / L.n_kv_heads;
+    a.q_dim = L.n_heads * L.head_dim;
+    a.q_pad = (a.q_dim + 255) / 256 * 256;
+    a.kv_dim = L.n_kv_heads * L.head_dim;
+    a.rope_theta = L.rope_theta;
+    a.rope_mode = L.rope_mode;
+    a.chunk_len = attention_chunk_len(kv.max_seq, L.n_kv_heads, (int)m);
+    a.n_chunks = (kv.max_seq + a.chunk_len - 1) / a.chunk_len;
+    a.part = part;
+    a.counters = counters;
+    a.att = att;
+    a.att_q8 = att_q8;
+    a.err = dev_error_word();
+    return a;
+}
+
+cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
+                                const int32_t *positions, int position, int64_t m, float *output,
+                                void *workspace, cudaStream_t s)
+{
+    LayerWs w = layer_ws(L, m, kv.max_seq, static_cast<uint8_t *>(workspace));
+    const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
+    const int q_pad = (q_dim + 255) / 256 * 256;
+    const int64_t ld_qkv = q_dim + 2 * kv_dim;
+
+    cudaError_t e = launch_rmsnorm(input, L.attn_gamma, nullptr, w.x8, m, L.hidden, L.hidden_pad, L.eps, s);
+    if (e != cudaSuccess) return e;
+    Q4kSegment qkv[3] = {{L.wq, w.qkv, nullptr, q_dim, ld_qkv, 0},
+                         {L.wk, w.qkv + q_dim, nullptr, kv_dim, ld_qkv, 0},
+                         {L.wv, w.qkv + q_dim + kv_dim, nullptr, kv_dim, ld_qkv, 0}};
+    e = launch_q4k_gemv(qkv, 3, EPI_STORE, w.x8, m, L.hidden_pad, s);
+    if (e != cudaSuccess) return e;
+    AttnArgs a = make_attn_args(L, m, kv, positions, position, w.q_rot, w.part, w.counters, w.qkv,
+                                w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, nullptr, w.a8);
+    e = launch_attention(a, s);
+    if (e != cudaSuccess) return e;
+    Q4kSegment o = {L.wo, w.res1, input, L.hidden, L.hidden_pad, L.hidden_pad};
+    e = launch_q4k_gemv(&o, 1, EPI_RESID, w.a8, m, q_pad, s);
+    if (e != cudaSuccess) return e;
+    return launch_swiglu_ffn(w.res1, L.ffn_gamma, L.wgate, L.wup, L.wdown, output, m, L.hidden,
+                             L.hidden_pad, L.inter, L.eps, w.ffn, s);
+}
+
+// ---------------------------------------------------------------- stack
+size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
+{
+    return 3 * align256((size_t)m * L.hidden_pad * 4) + layer_workspace_bytes(L, m, max_seq);
+}
+
+cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
+                                const KvDesc *kvs, const int32_t *positions, int position, int64_t m,
+                                const float *out_gamma, const void *lm_head, int64_t vocab,
+                                float *hidden_out, float *logits, void *workspace, cudaStream_t s)
+{
+    const LayerDesc &L0 = layers[0];
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t hbytes = align256((size_t)m * L0.hidden_pad * 4);
+    float *buf[2] = {reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes)};
+    float *normed = reinterpret_cast<float *>(ws + 2 * hbytes);
+    void *lws = ws + 3 * hbytes;
+    const float *cur = input;
+    cudaError_t e = cudaSuccess;
+    for (int l = 0; l < n_layers; ++l) {
+        float *out = (l == n_layers - 1 && hidden_out) ? hidden_out : buf[l & 1];
+        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s);
+        if (e != cudaSuccess) return e;
+        cur = out;
+    }
+    e = launch_rmsnorm(cur, out_gamma, normed, nullptr, m, L0.hidden, L0.hidden_pad, L0.eps, s);
+    if (e != cudaSuccess) return e;
+    return launch_q4_0_gemv_ld(lm_head, normed, L0.hidden_pad, logits, m, vocab, L0.hidden, s);
+}
+
+}  // namespace rz

@@ -37,9 +37,11 @@ enum Q4kEpilogue { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
 
 struct Q4kSegment {
     const void *w;     // Q4_K [rows][in_dim]
-    float *y;          // [m][rows]
-    const float *res;  // [m][rows] (EPI_RESID) or nullptr
+    float *y;          // [m][ldy], row r of token t at y[t * ldy + r]
+    const float *res;  // [m][ldr] (EPI_RESID) or nullptr
     int64_t rows;
+    int64_t ldy = 0;   // 0: rows
+    int64_t ldr = 0;   // 0: rows
 };
 
 // Up to three weight matrices with the same in_dim read against one Q8_1
@@ -48,11 +50,79 @@ struct Q4kSegment {
 cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
                             int64_t m, int64_t in_dim, cudaStream_t s);
 
+// Whether the stage ring of the GEMV fits in shared memory for this shape
+// (rows up to 23040 wide, 11520 for the paired gate/up launch).
+bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue);
+
 cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,
                                      int64_t in_dim, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+    const float *q, *k, *v;      // pre-RoPE projections of token t at + t * ld_qkv
+    int64_t ld_qkv;
+    float *q_rot;                // workspace f32 [m][q_dim]
+    float *kc, *vc;              // caches: token t at + t * seq_stride, row p at + p * kv_dim
+    int64_t seq_stride;
+    int max_seq;
+    const int32_t *positions;    // device int32 [m], or nullptr to use `position`
+    int position;
+    int m, n_heads, n_kv_heads, head_dim, group, q_dim, q_pad, kv_dim;
+    float rope_theta;
+    int rope_mode;
+    int chunk_len, n_chunks;
+    float *part;                 // workspace: [m][n_kv_heads][n_chunks][group][head_dim + 2]
+    int *counters;               // workspace: [m][n_kv_heads], zero before the first call
+    float *att;                  // f32 [m][q_dim] output, or nullptr
+    void *att_q8;                // Q8_1 of m rows of q_pad (output), or nullptr
+    unsigned *err;
+};
+
+int attention_chunk_len(int max_seq, int n_kv_heads, int m);
+size_t attention_smem_bytes(int group, int head_dim, int chunk_len);
+// RoPE + KV append, then split-sequence attention with the merge and the Q8_1 of
+// the output (two launches).
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- Q4_0 GEMV
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                              int64_t in_dim, cudaStream_t s);
+// as above with activation row stride ldx (elements) between tokens
+cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
+                                int64_t out_dim, int64_t in_dim, cudaStream_t s);
+
+// ---------------------------------------------------------------- layer / stack
+struct LayerDesc {
+    const void *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
+    const float *attn_gamma, *ffn_gamma;
+    int hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter;
+    float eps, rope_theta;
+    int rope_mode;
+};
+
+struct KvDesc {
+    float *k, *v;
+    int64_t seq_stride;
+    int max_seq;
+};
+
+size_t ffn_workspace_bytes(int64_t m, int64_t hidden_pad, int64_t inter);
+cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_gate, const void *w_up,
+                              const void *w_down, float *out, int64_t m, int64_t hidden,
+                              int64_t hidden_pad, int64_t inter, float eps, void *workspace,
+                              cudaStream_t s);
+size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
+size_t layer_counter_offset(const LayerDesc &L, int64_t m, int max_seq);
+AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
+                        int position, float *q_rot, float *part, int *counters, const float *q,
+                        const float *k, const float *v, int64_t ld_qkv, float *att, void *att_q8);
+cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
+                                const int32_t *positions, int position, int64_t m, float *output,
+                                void *workspace, cudaStream_t s);
+size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
+cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
+                                const KvDesc *kvs, const int32_t *positions, int position, int64_t m,
+                                const float *out_gamma, const void *lm_head, int64_t vocab,
+                                float *hidden_out, float *logits, void *workspace, cudaStream_t s);
 
 }  // namespace rz

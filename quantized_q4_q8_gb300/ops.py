@@ -11,6 +11,9 @@ __all__ = [
     "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
     "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
+    "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
+    "swiglu_ffn", "attention_workspace_bytes", "attention_decode",
+    "decode_layer_workspace_bytes", "decode_layer", "rz_decode_stack", "decode_stack",
 ]
 
 
@@ -163,3 +166,143 @@ def set_pdl(enable: bool):
 
 def version() -> str:
     return load().rz_version().decode()
+
+
+# ------------------------------------------------------------------ layer-level helpers
+class DeviceLayer:
+    """One Q4_K decode layer resident on the GPU (torch tensors) and its C descriptor.
+
+    weights: dict with uint8 CUDA tensors wq, wk, wv, wo, wgate, wup, wdown and f32
+    CUDA tensors attn_gamma, ffn_gamma.  Shapes follow include/rz.h."""
+
+    def __init__(self, weights: dict, hidden: int, hidden_pad: int, n_heads: int,
+                 n_kv_heads: int, head_dim: int, inter: int, eps: float, rope_theta: float,
+                 rope_mode: int):
+        from ._lib import LayerWeightsStruct
+        self.t = weights
+        self.hidden, self.hidden_pad, self.n_heads = hidden, hidden_pad, n_heads
+        self.n_kv_heads, self.head_dim, self.inter = n_kv_heads, head_dim, inter
+        self.eps, self.rope_theta, self.rope_mode = eps, rope_theta, rope_mode
+        self.struct = LayerWeightsStruct(
+            *[weights[k].data_ptr() for k in ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown",
+                                             "attn_gamma", "ffn_gamma")],
+            hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter, eps, rope_theta, rope_mode)
+
+    @property
+    def kv_dim(self):
+        return self.n_kv_heads * self.head_dim
+
+
+class DeviceKV:
+    """f32 K and V caches [m][max_seq][kv_dim] of one layer and their C descriptor."""
+
+    def __init__(self, k, v):
+        from ._lib import KvCacheStruct
+        import torch
+        assert k.dtype == torch.float32 and k.is_cuda and k.is_contiguous() and k.dim() == 3
+        self.k, self.v = k, v
+        m, max_seq, kv_dim = k.shape
+        self.max_seq = max_seq
+        self.struct = KvCacheStruct(k.data_ptr(), v.data_ptr(), max_seq * kv_dim, max_seq)
+
+
+def workspace(nbytes: int, device):
+    """Zero-filled device workspace (the attention counters start at zero)."""
+    import torch
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def swiglu_ffn_workspace_bytes(m, hidden_pad, inter):
+    return load().rz_swiglu_ffn_workspace_bytes(m, hidden_pad, inter)
+
+
+def swiglu_ffn(x, gamma, w_gate, w_up, w_down, hidden, hidden_pad, inter, eps, out=None,
+               ws=None, stream=None):
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    if out is None:
+        out = torch.empty((m, hidden_pad), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(swiglu_ffn_workspace_bytes(m, hidden_pad, inter), x.device)
+    call("rz_swiglu_ffn", _ptr(x), _ptr(gamma), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(out),
+         m, hidden, hidden_pad, inter, eps, _ptr(ws), ws.numel(), _stream(stream))
+    return out
+
+
+def attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, max_seq):
+    return load().rz_attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, max_seq)
+
+
+def attention_decode(q, k, v, ld_qkv, kv: "DeviceKV", n_heads, n_kv_heads, head_dim,
+                     rope_theta, rope_mode, position=0, positions=None, want_att=True,
+                     want_q8=True, ws=None, stream=None):
+    import ctypes as C
+    import torch
+    m = kv.k.shape[0]
+    q_dim = n_heads * head_dim
+    q_pad = (q_dim + 255) // 256 * 256
+    att = torch.empty((m, q_dim), dtype=torch.float32, device=q.device) if want_att else None
+    a8 = torch.empty(q8_1_size(m, q_pad), dtype=torch.uint8, device=q.device) if want_q8 else None
+    if ws is None:
+        ws = workspace(attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, kv.max_seq),
+                       q.device)
+    call("rz_attention_decode", _ptr(q), _ptr(k), _ptr(v), ld_qkv, C.byref(kv.struct),
+         _ptr(positions), position, m, n_heads, n_kv_heads, head_dim, rope_theta, rope_mode,
+         _ptr(att), _ptr(a8), _ptr(ws), ws.numel(), _stream(stream))
+    return att, a8
+
+
+def decode_layer_workspace_bytes(layer: "DeviceLayer", m, max_seq):
+    import ctypes as C
+    return load().rz_decode_layer_workspace_bytes(C.byref(layer.struct), m, max_seq)
+
+
+def decode_layer(x, layer: "DeviceLayer", kv: "DeviceKV", position=0, positions=None, out=None,
+                 ws=None, stream=None):
+    import ctypes as C
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    if out is None:
+        out = torch.empty((m, layer.hidden_pad), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(decode_layer_workspace_bytes(layer, m, kv.max_seq), x.device)
+    call("rz_decode_layer", _ptr(x), C.byref(layer.struct), C.byref(kv.struct), _ptr(positions),
+         position, m, _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    return out
+
+
+class DeviceStack:
+    """Layers + per-layer KV caches + output norm + Q4_0 LM head, with the host
+    descriptor arrays the C ABI takes."""
+
+    def __init__(self, layers, kvs, out_gamma, lm_head, vocab):
+        from ._lib import KvCacheStruct, LayerWeightsStruct
+        self.layers, self.kvs = layers, kvs
+        self.out_gamma, self.lm_head, self.vocab = out_gamma, lm_head, vocab
+        n = len(layers)
+        self.lw = (LayerWeightsStruct * n)(*[l.struct for l in layers])
+        self.kv = (KvCacheStruct * n)(*[k.struct for k in kvs])
+
+    def workspace_bytes(self, m):
+        return load().rz_decode_stack_workspace_bytes(self.lw, len(self.layers), m,
+                                                      self.kvs[0].max_seq)
+
+
+def rz_decode_stack(x, stack: "DeviceStack", positions, position, m, hidden_out, logits, ws,
+                    stream=None):
+    return call("rz_decode_stack", _ptr(x), stack.lw, stack.kv, len(stack.layers),
+                _ptr(positions), position, m, _ptr(stack.out_gamma), _ptr(stack.lm_head),
+                stack.vocab, _ptr(hidden_out), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def decode_stack(x, stack: "DeviceStack", position=0, positions=None, ws=None, stream=None,
+                 want_hidden=True):
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    hp = stack.layers[0].hidden_pad
+    hid = torch.empty((m, hp), dtype=torch.float32, device=x.device) if want_hidden else None
+    logits = torch.empty((m, stack.vocab), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(stack.workspace_bytes(m), x.device)
+    rz_decode_stack(x, stack, positions, position, m, hid, logits, ws, stream)
+    return hid, logits

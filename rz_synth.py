@@ -174,3 +174,57 @@ def kv_prefill(shape: LayerShape, tag: str, max_seq: int, filled: int, m: int = 
         k[:, :filled] = normal(f"{tag}.k", (m, filled, shape.kv_dim), seed)
         v[:, :filled] = normal(f"{tag}.v", (m, filled, shape.kv_dim), seed)
     return k, v
+
+
+# ----------------------------------------------------------------------------- device-side
+# The same distributions drawn with torch's generator directly in device memory,
+# for workloads too large to generate on the host (the 32-layer stack and its KV
+# caches).  Used by the benchmark; the parity tests use the host generators above.
+def torch_gen(name: str, device, seed: int = SEED):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((seed << 32) ^ zlib.crc32(name.encode()))
+    return g
+
+
+def q4k_weight_device(name: str, out_dim: int, in_dim: int, device, seed: int = SEED):
+    import torch
+    g = torch_gen(name, device, seed)
+    nsb = out_dim * (in_dim // 256)
+    blk = torch.randint(0, 256, (nsb, Q4K_BYTES), dtype=torch.uint8, device=device, generator=g)
+    dd = (torch.rand((nsb, 2), device=device, generator=g) * 9e-3 + 1e-3).to(torch.float16)
+    blk[:, 0:4] = dd.view(torch.uint8).view(nsb, 4)
+    return blk.view(out_dim, (in_dim // 256) * Q4K_BYTES)
+
+
+def q4_0_weight_device(name: str, out_dim: int, in_dim: int, device, seed: int = SEED):
+    import torch
+    g = torch_gen(name, device, seed)
+    nb = out_dim * (in_dim // 32)
+    blk = torch.randint(0, 256, (nb, Q4_0_BYTES), dtype=torch.uint8, device=device, generator=g)
+    d = (torch.rand((nb, 1), device=device, generator=g) * 9e-3 + 1e-3).to(torch.float16)
+    blk[:, 0:2] = d.view(torch.uint8).view(nb, 2)
+    return blk.view(out_dim, (in_dim // 32) * Q4_0_BYTES)
+
+
+def layer_device(shape: LayerShape, tag: str, device, seed: int = SEED) -> dict:
+    import torch
+    out = {nm: q4k_weight_device(f"{tag}.{nm}", o, i, device, seed)
+           for nm, (o, i) in shape.weight_shapes().items()}
+    for nm in ("attn_gamma", "ffn_gamma"):
+        g = torch_gen(f"{tag}.{nm}", device, seed)
+        out[nm] = torch.rand(shape.hidden, device=device, generator=g) + 0.5
+    return out
+
+
+def kv_prefill_device(shape: LayerShape, tag: str, max_seq: int, filled: int, m: int, device,
+                      seed: int = SEED):
+    import torch
+    k = torch.zeros((m, max_seq, shape.kv_dim), dtype=torch.float32, device=device)
+    v = torch.zeros_like(k)
+    if filled > 0:
+        k[:, :filled] = torch.randn((m, filled, shape.kv_dim), device=device,
+                                    generator=torch_gen(f"{tag}.k", device, seed))
+        v[:, :filled] = torch.randn((m, filled, shape.kv_dim), device=device,
+                                    generator=torch_gen(f"{tag}.v", device, seed))
+    return k, v

@@ -1,0 +1,259 @@
+"""GPU parity of the composite steps: attention, SwiGLU FFN, decode layer, stack.
+
+Bars.  Attention (f32 in, f32 out): |gpu - oracle| <= 1e-5 |ref| + 1e-5 max|ref|;
+the cache row written bit-exact for v and within 1e-6 relative for the rotated k;
+the attention output's Q8_1 bit-exact against the oracle's quantisation of the
+GPU's own f32 output.  Composite outputs that pass through Q8_1 re-quantisation
+of values the GPU computes in f32 (FFN, layer, stack): within 1e-3 relative, as
+max|gpu - ref| <= 1e-3 max|ref| and ||gpu - ref||_2 <= 1e-3 ||ref||_2.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import rz_synth as S
+
+from gpu_common import check_no_device_error, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rz():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_q4_q8_gb300 as rz
+    rz.load()
+    return rz
+
+
+def assert_rel(gpu, ref, tol=1e-3, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.isfinite(gpu).all(), f"{what}: non-finite output"
+    dmax = np.abs(gpu - ref).max()
+    d2 = np.linalg.norm(gpu - ref)
+    assert dmax <= tol * np.abs(ref).max(), f"{what}: max err {dmax:.3e} vs {tol} * {np.abs(ref).max():.3e}"
+    assert d2 <= tol * np.linalg.norm(ref), f"{what}: l2 err {d2:.3e} vs {tol} * {np.linalg.norm(ref):.3e}"
+    return dmax / np.abs(ref).max()
+
+
+def dev_layer(rz, L):
+    sh = L.shape
+    w = {k: to_dev(v) for k, v in L.w.items()}
+    w["attn_gamma"] = to_dev(L.attn_gamma)
+    w["ffn_gamma"] = to_dev(L.ffn_gamma)
+    return rz.DeviceLayer(w, sh.hidden, sh.hidden_pad, sh.n_heads, sh.n_kv_heads, sh.head_dim,
+                          sh.inter, sh.eps, sh.rope_theta, sh.rope_mode)
+
+
+def orc_layer(L):
+    sh = L.shape
+    return oracle.LayerWeights(**L.w, attn_gamma=L.attn_gamma, ffn_gamma=L.ffn_gamma,
+                               hidden=sh.hidden, hidden_pad=sh.hidden_pad, n_heads=sh.n_heads,
+                               n_kv_heads=sh.n_kv_heads, head_dim=sh.head_dim, inter=sh.inter,
+                               eps=sh.eps, rope_theta=sh.rope_theta, rope_mode=sh.rope_mode)
+
+
+# ----------------------------------------------------------------------------- attention
+ATT_CASES = [
+    # n_heads, n_kv_heads, head_dim, theta, mode, max_seq, positions
+    (14, 2, 64, 1e6, 1, 160, [127]),
+    (14, 2, 64, 1e6, 1, 160, [0]),
+    (8, 8, 128, 1e4, 0, 300, [257]),
+    (4, 1, 32, 1e4, 0, 50, [49]),
+    (8, 2, 64, 1e4, 1, 2056, [2048]),
+    (8, 4, 64, 1e4, 0, 100, [5, 0, 99]),
+]
+
+
+@pytest.mark.parametrize("H,Hkv,hd,theta,mode,max_seq,positions", ATT_CASES)
+def test_attention_decode_parity(rz, H, Hkv, hd, theta, mode, max_seq, positions):
+    import torch
+    m = len(positions)
+    kv_dim, q_dim = Hkv * hd, H * hd
+    sh = S.LayerShape(hidden=q_dim, inter=256, n_heads=H, n_kv_heads=Hkv, head_dim=hd,
+                      rope_theta=theta, rope_mode=mode)
+    kc, vc = S.kv_prefill(sh, f"gatt.{H}.{hd}.{m}", max_seq, max(positions), m)
+    kc *= np.float32(0.5)
+    q = S.normal(f"gatt.q.{H}.{hd}.{m}", (m, q_dim)) * np.float32(0.7)
+    k = S.normal(f"gatt.k.{H}.{hd}.{m}", (m, kv_dim)) * np.float32(0.7)
+    v = S.normal(f"gatt.v.{H}.{hd}.{m}", (m, kv_dim))
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    pos_d = to_dev(np.array(positions, np.int32)) if m > 1 else None
+    qkv = to_dev(np.concatenate([q, k, v], axis=1))      # one row per token: q | k | v
+    ld = q_dim + 2 * kv_dim
+    att, a8 = rz.attention_decode(qkv, qkv[:, q_dim:], qkv[:, q_dim + kv_dim:], ld, kv, H, Hkv, hd,
+                                  theta, mode, position=positions[0], positions=pos_d)
+    att = att.cpu().numpy()
+    a8 = a8.cpu().numpy()
+    check_no_device_error()
+    kc_after = kv.k.cpu().numpy()
+    vc_after = kv.v.cpu().numpy()
+    q_pad = (q_dim + 255) // 256 * 256
+    for t, p in enumerate(positions):
+        qr = oracle.rope(q[t], H, hd, p, theta, mode)
+        kr = oracle.rope(k[t], Hkv, hd, p, theta, mode)
+        assert np.array_equal(vc_after[t, p], v[t])
+        assert np.allclose(kc_after[t, p], kr, rtol=1e-6, atol=1e-6 * np.abs(kr).max())
+        kct = kc[t].copy()
+        vct = vc[t].copy()
+        kct[p] = kr
+        vct[p] = v[t]
+        ref = oracle.attention(qr, kct, vct, p, H, Hkv, hd).astype(np.float64)
+        err = np.abs(att[t] - ref)
+        assert np.all(err <= 1e-5 * np.abs(ref) + 1e-5 * np.abs(ref).max()), (t, err.max())
+    # the fused Q8_1 of the output is exactly the format applied to the f32 output
+    padded = np.zeros((m, q_pad), np.float32)
+    padded[:, :q_dim] = att
+    assert np.array_equal(a8, oracle.q8_1_quantize(padded))
+    # the other cache rows are untouched
+    for t, p in enumerate(positions):
+        mask = np.ones(max_seq, bool)
+        mask[p] = False
+        assert np.array_equal(kc_after[t][mask], kc[t][mask])
+
+
+def test_attention_first_token_is_v(rz):
+    """Position 0: every query head returns the value of its kv head (the first-token
+    case of forward_single_full_cuda_with_cache), to f32 rounding of the weights."""
+    H, Hkv, hd = 14, 2, 64
+    kc = np.zeros((1, 8, Hkv * hd), np.float32)
+    vc = np.zeros_like(kc)
+    q = S.normal("gfirst.q", (1, H * hd))
+    k = S.normal("gfirst.k", (1, Hkv * hd))
+    v = S.normal("gfirst.v", (1, Hkv * hd))
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    att, _ = rz.attention_decode(to_dev(q), to_dev(k), to_dev(v), H * hd, kv, H, Hkv, hd, 1e6, 1,
+                                 position=0)
+    att = att.cpu().numpy()[0]
+    for h in range(H):
+        kvh = h // (H // Hkv)
+        assert np.array_equal(att[h * hd:(h + 1) * hd], v[0, kvh * hd:(kvh + 1) * hd])
+
+
+def test_attention_bad_device_position_is_reported(rz):
+    """A device-resident position outside the cache is caught in the kernel: the
+    error word reports it, the cache is not written, the output is zeros."""
+    H, Hkv, hd, max_seq = 4, 2, 32, 16
+    kc = S.normal("gbad.k", (2, max_seq, Hkv * hd))
+    vc = S.normal("gbad.v", (2, max_seq, Hkv * hd))
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    qkv = to_dev(S.normal("gbad.qkv", (2, H * hd + 2 * Hkv * hd)))
+    ld = H * hd + 2 * Hkv * hd
+    pos = to_dev(np.array([3, max_seq + 5], np.int32))
+    att, _ = rz.attention_decode(qkv, qkv[:, H * hd:], qkv[:, H * hd + Hkv * hd:], ld, kv, H, Hkv, hd,
+                                 1e4, 0, positions=pos)
+    st, code = rz.check_device_error()
+    assert st == 7 and code == 0x201
+    assert np.array_equal(kv.k.cpu().numpy()[1], kc[1])
+    assert not att.cpu().numpy()[1].any()
+    check_no_device_error()   # the word was cleared
+
+
+# ----------------------------------------------------------------------------- SwiGLU FFN
+@pytest.mark.parametrize("shape,m", [(S.QWEN2, 1), (S.QWEN2, 3), (S.LLAMA7B, 1), (S.LLAMA7B, 2)])
+def test_swiglu_ffn_parity(rz, shape, m):
+    L = S.layer(shape, f"gffn.{shape.hidden}")
+    x = S.hidden_input(f"gffn.x.{shape.hidden}.{m}", m, shape.hidden, shape.hidden_pad)
+    out = rz.swiglu_ffn(to_dev(x), to_dev(L.ffn_gamma), to_dev(L.w["wgate"]), to_dev(L.w["wup"]),
+                        to_dev(L.w["wdown"]), shape.hidden, shape.hidden_pad, shape.inter,
+                        shape.eps).cpu().numpy()
+    check_no_device_error()
+    for t in range(m):
+        ref = oracle.swiglu_ffn(x[t], L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
+                                shape.hidden, shape.hidden_pad, shape.inter, shape.eps)
+        assert_rel(out[t], ref, what=f"ffn token {t}")
+        assert not out[t, shape.hidden:].any()
+
+
+# ----------------------------------------------------------------------------- decode layer
+@pytest.mark.parametrize("pos", [127, 0])
+def test_decode_layer_qwen2_parity(rz, pos):
+    """The Qwen2-0.5B-shaped layer at position 127 (and the first token)."""
+    sh = S.QWEN2
+    L = S.layer(sh, "qwen2.l0")
+    max_seq = 160
+    x = S.hidden_input("qwen2.x", 1, sh.hidden, sh.hidden_pad)
+    kc, vc = S.kv_prefill(sh, "qwen2.kv", max_seq, pos)
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    out = rz.decode_layer(to_dev(x), dev_layer(rz, L), kv, position=pos).cpu().numpy()
+    check_no_device_error()
+    kc_r, vc_r = kc[0].copy(), vc[0].copy()
+    ref = oracle.decode_layer(x[0], orc_layer(L), kc_r, vc_r, pos)
+    assert_rel(out[0], ref, what="qwen2 layer")
+    assert not out[0, sh.hidden:].any()
+    assert_rel(kv.k.cpu().numpy()[0, pos], kc_r[pos], tol=1e-4, what="k row")
+    assert_rel(kv.v.cpu().numpy()[0, pos], vc_r[pos], tol=1e-4, what="v row")
+
+
+def test_decode_layer_batched_positions(rz):
+    """m = 4 sequences at different positions through one launch sequence; each
+    matches the oracle run alone."""
+    import torch
+    sh = S.QWEN2
+    L = S.layer(sh, "qwen2.b")
+    positions = [5, 127, 0, 63]
+    m, max_seq = len(positions), 128
+    x = S.hidden_input("qwen2.bx", m, sh.hidden, sh.hidden_pad)
+    kc, vc = S.kv_prefill(sh, "qwen2.bkv", max_seq, max(positions), m)
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    out = rz.decode_layer(to_dev(x), dev_layer(rz, L), kv,
+                          positions=to_dev(np.array(positions, np.int32))).cpu().numpy()
+    check_no_device_error()
+    ol = orc_layer(L)
+    for t, p in enumerate(positions):
+        kt, vt = kc[t].copy(), vc[t].copy()
+        ref = oracle.decode_layer(x[t], ol, kt, vt, p)
+        assert_rel(out[t], ref, what=f"token {t} at {p}")
+
+
+def test_decode_layer_llama_parity(rz):
+    sh = S.LLAMA7B
+    L = S.layer(sh, "llama.l0")
+    pos, max_seq = 128, 256
+    x = S.hidden_input("llama.x", 1, sh.hidden, sh.hidden_pad)
+    kc, vc = S.kv_prefill(sh, "llama.kv", max_seq, pos)
+    kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+    out = rz.decode_layer(to_dev(x), dev_layer(rz, L), kv, position=pos).cpu().numpy()
+    check_no_device_error()
+    ref = oracle.decode_layer(x[0], orc_layer(L), kc[0].copy(), vc[0].copy(), pos)
+    assert_rel(out[0], ref, what="llama layer")
+
+
+def test_decode_layer_in_place(rz):
+    import torch
+    sh = S.QWEN2
+    L = S.layer(sh, "qwen2.ip")
+    x = S.hidden_input("qwen2.ipx", 1, sh.hidden, sh.hidden_pad)
+    kc, vc = S.kv_prefill(sh, "qwen2.ipkv", 64, 10)
+    dl = dev_layer(rz, L)
+    a = rz.decode_layer(to_dev(x), dl, rz.DeviceKV(to_dev(kc), to_dev(vc)), position=10).cpu().numpy()
+    xd = to_dev(x)
+    rz.decode_layer(xd, dl, rz.DeviceKV(to_dev(kc), to_dev(vc)), position=10, out=xd)
+    assert np.array_equal(xd.cpu().numpy(), a)
+
+
+# ----------------------------------------------------------------------------- stack
+def test_decode_stack_qwen2_two_layers_and_lm_head(rz):
+    """Two Qwen2-shaped layers, output norm and the 151936 x 896 Q4_0 LM head."""
+    sh = S.QWEN2
+    vocab = 151936
+    layers = [S.layer(sh, f"qs.l{i}") for i in range(2)]
+    out_gamma = S.uniform("qs.og", sh.hidden, 0.5, 1.5)
+    lm = S.q4_0_weight("qs.lm", vocab, sh.hidden)
+    pos, max_seq = 127, 128
+    x = S.hidden_input("qs.x", 1, sh.hidden, sh.hidden_pad)
+    kvs_h = [S.kv_prefill(sh, f"qs.kv{i}", max_seq, pos) for i in range(2)]
+    kvs = [rz.DeviceKV(to_dev(k), to_dev(v)) for k, v in kvs_h]
+    stack = rz.DeviceStack([dev_layer(rz, L) for L in layers], kvs, to_dev(out_gamma), to_dev(lm), vocab)
+    hid, logits = rz.decode_stack(to_dev(x), stack, position=pos)
+    hid = hid.cpu().numpy()
+    logits = logits.cpu().numpy()
+    check_no_device_error()
+    hid_r, log_r = oracle.decode_stack(x[0], [orc_layer(L) for L in layers],
+                                       [k[0].copy() for k, _ in kvs_h], [v[0].copy() for _, v in kvs_h],
+                                       pos, out_gamma, lm, vocab)
+    assert_rel(hid[0], hid_r, what="stack hidden")
+    assert_rel(logits[0], log_r, what="stack logits")
