@@ -569,8 +569,9 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000 for the stack, 2000 for the GEMV)")
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="rz", choices=["rz", "reference"])
     ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -579,6 +580,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.steps is None:
+        args.steps = 1000 if args.workload == "stack" else 2000
+        if args.impl == "reference":
+            args.steps = 20
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks have no work
         world = int(os.environ.get("WORLD_SIZE", "1"))
