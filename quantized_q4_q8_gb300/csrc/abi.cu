@@ -245,6 +245,8 @@ namespace {
 rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, LayerDesc *out)
 {
     if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
+    // the shape limits below depend on the device's shared memory
+    RZ_TRY(check_device());
     const void *ptrs[] = {w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma};
     for (const void *p : ptrs) {
         if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer", fn);
@@ -349,7 +351,7 @@ size_t rz_attention_workspace_bytes(int64_t m, int32_t n_heads, int32_t n_kv_hea
     const int n_chunks = (max_seq + chunk - 1) / chunk;
     const size_t group = (size_t)(n_heads / n_kv_heads);
     auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
-    return a256((size_t)m * n_heads * head_dim * 4) +
+    return a256((size_t)m * head_dim * 4) +
            a256((size_t)m * n_kv_heads * n_chunks * group * (head_dim + 2) * 4) + a256((size_t)m * n_kv_heads * 4);
 }
 
@@ -386,14 +388,15 @@ rz_status rz_attention_decode(const float *q, const float *k, const float *v, in
     L.rope_mode = rope_mode;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
-    float *q_rot = reinterpret_cast<float *>(ws);
-    ws += a256((size_t)m * q_dim * 4);
+    float *rope_tab = reinterpret_cast<float *>(ws);
+    ws += a256((size_t)m * head_dim * 4);
     const int chunk = attention_chunk_len(kv->max_seq, n_kv_heads, (int)m);
     const int n_chunks = (kv->max_seq + chunk - 1) / chunk;
     float *part = reinterpret_cast<float *>(ws);
     ws += a256((size_t)m * n_kv_heads * n_chunks * (n_heads / n_kv_heads) * (head_dim + 2) * 4);
     int *counters = reinterpret_cast<int *>(ws);
-    AttnArgs a = make_attn_args(L, m, kd, positions, position, q_rot, part, counters, q, k, v, ld_qkv, att, att_q8);
+    AttnArgs a = make_attn_args(L, m, kd, positions, position, rope_tab, 1, part, counters, q, k, v, ld_qkv, att,
+                                att_q8);
     RZ_CUDA(launch_attention(a, static_cast<cudaStream_t>(stream)), "rz_attention_decode launch");
     return RZ_OK;
 }

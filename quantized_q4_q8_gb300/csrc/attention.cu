@@ -7,18 +7,25 @@
 // row `position`, and every query head h attends over cache rows 0..position of
 // kv head h / (n_heads / n_kv_heads) with softmax(q.k / sqrt(head_dim)).
 //
-// RoPE pairs (i, i + 1) for mode 0 and (i, i + head_dim/2) for mode 1 turn by
-// position * theta^(-2i/head_dim).  The angle is formed and reduced modulo 2*pi
-// in double precision (positions reach thousands of radians), then rotated with
-// single-precision sin/cos of the reduced angle.
+// RoPE pairs (2i, 2i + 1) for mode 0 and (i, i + head_dim/2) for mode 1 turn by
+// position * theta^(-2i/head_dim).  A small kernel builds, per token, the cosine
+// and sine of every pair's angle: the angle is formed and reduced modulo 2*pi in
+// double precision (positions reach thousands of radians), then sin/cos are taken
+// in single precision.  The table depends only on the positions, so the layer
+// stack builds it once per step and every layer reuses it.
 //
-// Attention is split over the sequence (flash-decoding style): CTA (token, kv
-// head, chunk) scores its chunk of cache rows for all query heads of the group,
-// keeps the chunk max, the exp-sum and the unnormalised weighted sum of values,
-// and the last CTA of each (token, kv head) -- found with an atomic counter, no
-// spinning -- merges the chunks with the log-sum-exp rule, writes the f32 output
-// and its Q8_1 quantisation (head_dim is a multiple of 32, so Q8_1 blocks never
-// straddle heads) for the O projection.  The counter is reset by the merging CTA.
+// Attention is split over the sequence in chunks of 64 cache rows (flash-
+// decoding style).  CTA (chunk, kv head, token) rotates its query heads, and the
+// CTA whose chunk holds the token's own row rotates k, writes k and v to the
+// cache and uses them from shared memory.  The scores and the weighted values are
+// computed with every load of the chunk issued before it is used (32 KB of K,
+// then 32 KB of V in flight per CTA at head_dim 128), so HBM rather than latency
+// bounds the kernel.  Each CTA leaves its chunk max, exp-sum and unnormalised
+// weighted values; the last CTA of each (token, kv head) -- found with an atomic
+// counter, no spinning -- merges the chunks with the log-sum-exp rule and writes
+// the f32 output and its Q8_1 quantisation (head_dim is a multiple of 32, so Q8_1
+// blocks never straddle heads) for the O projection.  The counter is reset by the
+// merging CTA.
 #include <math.h>
 
 #include "rz_common.cuh"
@@ -27,7 +34,8 @@
 namespace rz {
 namespace {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
+constexpr int kChunk = 64;  // cache rows per CTA
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
 __device__ __forceinline__ int token_position(const AttnArgs &a, int t)
@@ -35,56 +43,38 @@ __device__ __forceinline__ int token_position(const AttnArgs &a, int t)
     return a.positions ? a.positions[t] : a.position;
 }
 
-// rotate pair (x0, x1) of dimension index i at position pos
-__device__ __forceinline__ void rope_pair(float &x0, float &x1, int i, int head_dim, int pos,
-                                          double log2_theta)
+// cos/sin of every pair angle, per token: tab[t][i] = (cos, sin)
+__global__ void rope_table_kernel(const AttnArgs a)
 {
-    const double inv_freq = exp2(-(2.0 * i / head_dim) * log2_theta);
-    const double ang = (double)pos * inv_freq;
-    const double red = ang - kTwoPi * rint(ang / kTwoPi);
-    float sn, cs;
-    sincosf((float)red, &sn, &cs);
-    const float a = x0, b = x1;
-    x0 = a * cs - b * sn;
-    x1 = a * sn + b * cs;
-}
-
-// One CTA per (token, head) of q and of k: rotate; k and v go to the cache row.
-__global__ void rope_append_kernel(const AttnArgs a)
-{
+    pdl_launch_dependents();
     pdl_wait();
-    const int t = blockIdx.y;
-    const int head = blockIdx.x;  // [0, n_heads) q heads, then kv heads
+    const int t = blockIdx.x;
+    const int half = a.head_dim / 2;
     const int pos = token_position(a, t);
-    const int hd = a.head_dim, half = hd / 2;
-    if (pos < 0 || pos >= a.max_seq) {
-        if (threadIdx.x == 0) set_error(a.err, DEV_BAD_POSITION);
-        return;
-    }
     const double l2t = log2((double)a.rope_theta);
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const int ia = a.rope_mode == 0 ? 2 * i : i;
-        const int ib = a.rope_mode == 0 ? 2 * i + 1 : i + half;
-        if (head < a.n_heads) {
-            const float *src = a.q + (int64_t)t * a.ld_qkv + (int64_t)head * hd;
-            float *dst = a.q_rot + (int64_t)t * a.q_dim + (int64_t)head * hd;
-            float x0 = src[ia], x1 = src[ib];
-            rope_pair(x0, x1, i, hd, pos, l2t);
-            dst[ia] = x0;
-            dst[ib] = x1;
-        } else {
-            const int kh = head - a.n_heads;
-            const float *ks = a.k + (int64_t)t * a.ld_qkv + (int64_t)kh * hd;
-            const float *vs = a.v + (int64_t)t * a.ld_qkv + (int64_t)kh * hd;
-            float *kd = a.kc + (int64_t)t * a.seq_stride + (int64_t)pos * a.kv_dim + (int64_t)kh * hd;
-            float *vd = a.vc + (int64_t)t * a.seq_stride + (int64_t)pos * a.kv_dim + (int64_t)kh * hd;
-            float x0 = ks[ia], x1 = ks[ib];
-            rope_pair(x0, x1, i, hd, pos, l2t);
-            kd[ia] = x0;
-            kd[ib] = x1;
-            vd[ia] = vs[ia];
-            vd[ib] = vs[ib];
-        }
+        const double inv_freq = exp2(-(2.0 * i / a.head_dim) * l2t);
+        const double ang = (double)pos * inv_freq;
+        const double red = ang - kTwoPi * rint(ang / kTwoPi);
+        float sn, cs;
+        sincosf((float)red, &sn, &cs);
+        a.rope_tab[((int64_t)t * half + i) * 2] = cs;
+        a.rope_tab[((int64_t)t * half + i) * 2 + 1] = sn;
+    }
+}
+
+// rotate one head (hd values at src) into dst using the token's table
+__device__ __forceinline__ void rope_head(const float *src, float *dst, const float *tab, int hd,
+                                          int mode, int tid, int nthreads)
+{
+    const int half = hd / 2;
+    for (int i = tid; i < half; i += nthreads) {
+        const int ia = mode == 0 ? 2 * i : i;
+        const int ib = mode == 0 ? 2 * i + 1 : i + half;
+        const float cs = tab[2 * i], sn = tab[2 * i + 1];
+        const float x0 = src[ia], x1 = src[ib];
+        dst[ia] = x0 * cs - x1 * sn;
+        dst[ib] = x0 * sn + x1 * cs;
     }
 }
 
@@ -95,90 +85,153 @@ __device__ __forceinline__ float *part_rec(const AttnArgs &a, int t, int kvh, in
     return a.part + idx * (a.head_dim + 2);
 }
 
-// grid (n_chunks, n_kv_heads, m); dynamic smem: q [group][hd] + p [group][chunk_len]
+// `cnt` consecutive floats at p (16-byte aligned when cnt >= 4) into r
+template <int CNT>
+__device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
+{
+    if (CNT % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < CNT; e += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(p + e);
+            r[e] = v.x;
+            r[e + 1] = v.y;
+            r[e + 2] = v.z;
+            r[e + 3] = v.w;
+        }
+    } else if (CNT == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        r[0] = v.x;
+        r[1] = v.y;
+    } else {
+        r[0] = p[0];
+    }
+}
+
+// grid (n_chunks, n_kv_heads, m), 256 threads; CPT = head_dim / 32.
+// shared memory: qs [G][hd] | kn [hd] | vn [hd] | ps [G][64] | stat [G][2] | red [8][G][hd] | flag
+template <int CPT>
 __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const AttnArgs a)
 {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int chunk = blockIdx.x, kvh = blockIdx.y, t = blockIdx.z;
-    const int hd = a.head_dim, G = a.group, L = a.chunk_len;
-    float *qs = sm;                 // [G][hd]
-    float *ps = sm + G * hd;        // [G][L]
-    float *stat = ps + G * L;       // [G][2] and a flag
+    const int hd = a.head_dim, G = a.group;
+    float *qs = sm;
+    float *kn = qs + G * hd;
+    float *vn = kn + hd;
+    float *ps = vn + hd;
+    float *stat = ps + G * kChunk;
+    float *red = stat + 2 * G + 2;  // keeps 8-byte alignment for the float2 reads below
+    int *flag = reinterpret_cast<int *>(red + 8 * G * hd);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = kAttnThreads / 32;
+    pdl_launch_dependents();
     pdl_wait();
 
     const int pos = token_position(a, t);
     const bool pos_ok = pos >= 0 && pos < a.max_seq;
-    const int c0 = chunk * L;
-    const int c1 = pos_ok ? min(c0 + L, pos + 1) : c0;
-    const int n = max(0, c1 - c0);
+    const int c0 = chunk * kChunk;
+    const int n = pos_ok ? max(0, min(kChunk, pos + 1 - c0)) : 0;
+    const bool own = pos_ok && pos >= c0 && pos < c0 + kChunk;  // this chunk holds the new row
+    if (!pos_ok && chunk == 0 && kvh == 0 && tid == 0) set_error(a.err, DEV_BAD_POSITION);
+    const float *tab = a.rope_tab + (int64_t)t * (hd / 2) * 2;
     const float scale = 1.0f / sqrtf((float)hd);
+    const int64_t kv_base = (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
 
     if (n > 0) {
-        for (int i = tid; i < G * hd; i += kAttnThreads)
-            qs[i] = a.q_rot[(int64_t)t * a.q_dim + (int64_t)(kvh * G) * hd + i];
+        // rotated query heads of this kv head, and (owner) the new row
+        for (int g = 0; g < G; ++g)
+            rope_head(a.q + (int64_t)t * a.ld_qkv + (int64_t)(kvh * G + g) * hd, qs + g * hd, tab, hd,
+                      a.rope_mode, tid, kAttnThreads);
+        if (own) {
+            const float *ks = a.k + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
+            const float *vs = a.v + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
+            rope_head(ks, kn, tab, hd, a.rope_mode, tid, kAttnThreads);
+            for (int i = tid; i < hd; i += kAttnThreads) vn[i] = vs[i];
+        }
         __syncthreads();
-        const float *kbase = a.kc + (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
-        // scores: each warp takes 4 positions at a time (loads first, then the
-        // dot products), lanes over head_dim
-        const int per = hd / 32;  // 1..8 values per lane
-        for (int j0 = warp * 4; j0 < n; j0 += nwarps * 4) {
-            float kv[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float *kr = kbase + (int64_t)(c0 + j0 + u) * a.kv_dim;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    kv[u][e] = (e < per && j0 + u < n) ? kr[e * 32 + lane] : 0.0f;
+        if (own) {
+            float *kd = a.kc + kv_base + (int64_t)pos * a.kv_dim;
+            float *vd = a.vc + kv_base + (int64_t)pos * a.kv_dim;
+            for (int i = tid; i < hd; i += kAttnThreads) {
+                kd[i] = kn[i];
+                vd[i] = vn[i];
+            }
+        }
+
+        // ---- scores: 4 threads per cache row, hd/4 = 8*CPT values each, all loads first
+        {
+            const int j = tid >> 2, part = tid & 3;
+            constexpr int PER = 8 * CPT;
+            float kv[PER];
+            if (j < n) {
+                const float *kr = (c0 + j == pos) ? kn : a.kc + kv_base + (int64_t)(c0 + j) * a.kv_dim;
+                load_cols<PER>(kr + part * PER, kv);
             }
             for (int g = 0; g < G; ++g) {
+                float dot = 0.0f;
+                if (j < n) {
+                    const float *qg = qs + g * hd + part * PER;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float dot = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (e < per) dot = fmaf(qs[g * hd + e * 32 + lane], kv[u][e], dot);
-                    dot = warp_sum(dot);
-                    if (lane == 0 && j0 + u < n) ps[g * L + j0 + u] = dot * scale;
+                    for (int e = 0; e < PER; ++e) dot = fmaf(qg[e], kv[e], dot);
                 }
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                if (part == 0 && j < n) ps[g * kChunk + j] = dot * scale;
             }
         }
         __syncthreads();
-        // chunk softmax statistics per query head (warp per head)
-        for (int g = warp; g < G; g += nwarps) {
-            float mx = -INFINITY;
-            for (int j = lane; j < n; j += 32) mx = fmaxf(mx, ps[g * L + j]);
-            mx = warp_max(mx);
-            float sum = 0.0f;
-            for (int j = lane; j < n; j += 32) {
-                const float p = expf(ps[g * L + j] - mx);
-                ps[g * L + j] = p;
-                sum += p;
-            }
-            sum = warp_sum(sum);
+        // ---- chunk softmax statistics (warp per query head)
+        for (int g = warp; g < G; g += kAttnThreads / 32) {
+            const float v0 = lane < n ? ps[g * kChunk + lane] : -INFINITY;
+            const float v1 = lane + 32 < n ? ps[g * kChunk + lane + 32] : -INFINITY;
+            const float mx = warp_max(fmaxf(v0, v1));
+            const float p0 = lane < n ? expf(v0 - mx) : 0.0f;
+            const float p1 = lane + 32 < n ? expf(v1 - mx) : 0.0f;
+            ps[g * kChunk + lane] = p0;
+            ps[g * kChunk + lane + 32] = p1;
+            const float sum = warp_sum(p0 + p1);
             if (lane == 0) {
                 stat[2 * g] = mx;
                 stat[2 * g + 1] = sum;
             }
         }
         __syncthreads();
-        // weighted values: thread per head_dim element, loop over positions
-        const float *vbase = a.vc + (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
-        for (int dd = tid; dd < hd; dd += kAttnThreads) {
-            float o[16];
+        // ---- weighted values: 8 row groups x 32 column threads, all loads first
+        {
+            const int rg = warp, col = lane;
+            float v[8][CPT];
 #pragma unroll
-            for (int g = 0; g < 16; ++g) o[g] = 0.0f;
-#pragma unroll 4
-            for (int j = 0; j < n; ++j) {
-                const float v = vbase[(int64_t)(c0 + j) * a.kv_dim + dd];
+            for (int r = 0; r < 8; ++r) {
+                const int j = rg + 8 * r;
 #pragma unroll
-                for (int g = 0; g < 16; ++g)
-                    if (g < G) o[g] = fmaf(ps[g * L + j], v, o[g]);
+                for (int e = 0; e < CPT; ++e) v[r][e] = 0.0f;
+                if (j < n) {
+                    const float *vr = (c0 + j == pos) ? vn : a.vc + kv_base + (int64_t)(c0 + j) * a.kv_dim;
+                    load_cols<CPT>(vr + col * CPT, v[r]);
+                }
             }
+            for (int g = 0; g < G; ++g) {
+                float o[CPT];
 #pragma unroll
-            for (int g = 0; g < 16; ++g)
-                if (g < G) part_rec(a, t, kvh, chunk, g)[2 + dd] = o[g];
+                for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int j = rg + 8 * r;
+                    const float p = j < n ? ps[g * kChunk + j] : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) o[e] = fmaf(p, v[r][e], o[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) red[(rg * G + g) * hd + col * CPT + e] = o[e];
+            }
+        }
+        __syncthreads();
+        // fixed-order sum over the 8 row groups -> partial record
+        for (int i = tid; i < G * hd; i += kAttnThreads) {
+            const int g = i / hd, dd = i % hd;
+            float s = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) s += red[(r * G + g) * hd + dd];
+            part_rec(a, t, kvh, chunk, g)[2 + dd] = s;
         }
         for (int g = tid; g < G; g += kAttnThreads) {
             float *rec = part_rec(a, t, kvh, chunk, g);
@@ -196,7 +249,6 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     // ---- arrive; the last chunk of (t, kvh) merges
     __threadfence();
     __syncthreads();
-    int *flag = reinterpret_cast<int *>(stat + 2 * G);
     if (tid == 0) {
         int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
         const int prev = atomicAdd(cnt, 1);
@@ -208,25 +260,20 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     if (!*flag) return;
     __threadfence();
 
-    float *outv = qs;  // reuse: merged output [G][hd]
-    for (int g = 0; g < G; ++g) {
+    const int nc = pos_ok ? min(a.n_chunks, pos / kChunk + 1) : 0;  // chunks holding rows
+    float *outv = red;  // merged output [G][hd]
+    for (int i = tid; i < G * hd; i += kAttnThreads) {
+        const int g = i / hd, dd = i % hd;
         float M = -INFINITY;
-        for (int c = 0; c < a.n_chunks; ++c) M = fmaxf(M, __ldcg(part_rec(a, t, kvh, c, g)));
-        float Lsum = 0.0f;
-        for (int c = 0; c < a.n_chunks; ++c) {
+        for (int c = 0; c < nc; ++c) M = fmaxf(M, __ldcg(part_rec(a, t, kvh, c, g)));
+        float Lsum = 0.0f, acc = 0.0f;
+        for (int c = 0; c < nc; ++c) {
             const float *rec = part_rec(a, t, kvh, c, g);
-            const float l = __ldcg(rec + 1);
-            if (l > 0.0f) Lsum += l * expf(__ldcg(rec) - M);
+            const float w = expf(__ldcg(rec) - M);
+            Lsum += __ldcg(rec + 1) * w;
+            acc += __ldcg(rec + 2 + dd) * w;
         }
-        for (int dd = tid; dd < hd; dd += kAttnThreads) {
-            float acc = 0.0f;
-            for (int c = 0; c < a.n_chunks; ++c) {
-                const float *rec = part_rec(a, t, kvh, c, g);
-                const float l = __ldcg(rec + 1);
-                if (l > 0.0f) acc += __ldcg(rec + 2 + dd) * expf(__ldcg(rec) - M);
-            }
-            outv[g * hd + dd] = (Lsum > 0.0f) ? acc / Lsum : 0.0f;  // 0 only after a bad position
-        }
+        outv[g * hd + dd] = (Lsum > 0.0f) ? acc / Lsum : 0.0f;  // 0 only after a bad position
     }
     __syncthreads();
     const int64_t col0 = (int64_t)kvh * G * hd;
@@ -239,7 +286,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
         float *qd = reinterpret_cast<float *>(q + (int64_t)a.m * a.q_pad);
         float *qsum = qd + (int64_t)a.m * (a.q_pad / 32);
         const int nblk = G * hd / 32;
-        for (int b = warp; b < nblk; b += nwarps) {
+        for (int b = warp; b < nblk; b += kAttnThreads / 32) {
             const float v = outv[b * 32 + lane];
             const float amax = warp_max(fabsf(v));
             const float dq = __fdiv_rn(amax, 127.0f);
@@ -280,32 +327,42 @@ cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem, cudaSt
 
 }  // namespace
 
-int attention_chunk_len(int max_seq, int n_kv_heads, int m)
+int attention_chunk_len(int, int, int) { return kChunk; }
+
+size_t attention_smem_bytes(int group, int head_dim, int)
 {
-    // enough CTAs to cover the GPU about twice at the longest sequence
-    const int sms = dev_info().sm_count;
-    int L = 64;
-    while (L > 16 && (int64_t)((max_seq + L - 1) / L) * n_kv_heads * m < 2 * sms) L /= 2;
-    return L;
+    return ((size_t)group * head_dim + 2 * (size_t)head_dim + (size_t)group * kChunk + 2 * (size_t)group + 2 +
+            8 * (size_t)group * head_dim + 4) *
+           sizeof(float);
 }
 
-size_t attention_smem_bytes(int group, int head_dim, int chunk_len)
+cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s)
 {
-    return ((size_t)group * head_dim + (size_t)group * chunk_len + 2 * (size_t)group + 4) * sizeof(float);
+    AttnArgs args = a;
+    void *kargs[] = {&args};
+    return launch_ex((const void *)rope_table_kernel, dim3((unsigned)a.m), dim3(64), 0, s, kargs);
 }
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
 {
     AttnArgs args = a;
     void *kargs[] = {&args};
-    cudaError_t e = launch_ex((const void *)rope_append_kernel,
-                              dim3((unsigned)(a.n_heads + a.n_kv_heads), (unsigned)a.m),
-                              dim3(64), 0, s, kargs);
-    if (e != cudaSuccess) return e;
-    const size_t smem = attention_smem_bytes(a.group, a.head_dim, a.chunk_len);
-    return launch_ex((const void *)attention_chunk_kernel,
-                     dim3((unsigned)a.n_chunks, (unsigned)a.n_kv_heads, (unsigned)a.m),
-                     dim3(kAttnThreads), smem, s, kargs);
+    if (a.make_table) {
+        cudaError_t e = launch_rope_table(a, s);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t smem = attention_smem_bytes(a.group, a.head_dim, kChunk);
+    const void *fn = a.head_dim == 32    ? (const void *)attention_chunk_kernel<1>
+                     : a.head_dim == 64  ? (const void *)attention_chunk_kernel<2>
+                     : a.head_dim == 128 ? (const void *)attention_chunk_kernel<4>
+                                         : (const void *)attention_chunk_kernel<8>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)dev_info().smem_optin);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_ex(fn, dim3((unsigned)a.n_chunks, (unsigned)a.n_kv_heads, (unsigned)a.m), dim3(kAttnThreads),
+                     smem, s, kargs);
 }
 
 }  // namespace rz

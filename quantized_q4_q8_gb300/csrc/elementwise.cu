@@ -39,42 +39,29 @@ __global__ void q8_1_quantize_kernel(const float *__restrict__ x, int8_t *__rest
 {
     const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     if (blk >= nblocks) return;
     // blocks of consecutive rows are consecutive: block blk covers x[32 blk, 32 blk + 32)
     const float v = x[blk * 32 + lane];
     q8_block_store(v, lane, q + blk * 32, qd + blk, qs + blk);
 }
 
-constexpr int kNormThreads = 256;
+constexpr int kNormThreads = 1024;
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
     const float *__restrict__ x, const float *__restrict__ gamma, float *__restrict__ y,
     int8_t *__restrict__ q, float *__restrict__ qd, float *__restrict__ qs, int64_t n,
     int64_t n_pad, float eps)
 {
-    __shared__ float red[kNormThreads / 32 + 1];
+    __shared__ float red[9];
     const int64_t row = blockIdx.x;
     const float *xr = x + row * n_pad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
-
-    float ss = 0.0f;
-    for (int64_t i = tid; i < n; i += kNormThreads) {
-        const float v = xr[i];
-        ss = fmaf(v, v, ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (warp == 0) {
-        float v = (lane < kNormThreads / 32) ? red[lane] : 0.0f;
-        v = warp_sum(v);
-        if (lane == 0) red[kNormThreads / 32] = v;
-    }
-    __syncthreads();
-    const float total = red[kNormThreads / 32];
-    const float scale = 1.0f / sqrtf(total / (float)n + eps);
     pdl_launch_dependents();
+    pdl_wait();
+    const float total = fixed_order_sumsq(xr, n, tid, red, [] { __syncthreads(); });
+    const float scale = rms_scale(total, n, eps);
 
     if (q != nullptr) {
         // n_pad % 32 == 0: warps take whole Q8_1 blocks
@@ -93,6 +80,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
 
 __global__ void residual_add_kernel(const float *a, const float *b, float *out, int64_t n)
 {
+    pdl_launch_dependents();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t n4 = n / 4;
@@ -119,8 +107,16 @@ cudaError_t launch_q8_1_quantize(const float *x, void *q8, int64_t m, int64_t n,
     const int64_t nblocks = m * (n / 32);
     const int warps = 8;
     const int64_t grid = (nblocks + warps - 1) / warps;
-    q8_1_quantize_kernel<<<(unsigned)grid, warps * 32, 0, s>>>(x, q, qd, qs, nblocks);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, q8_1_quantize_kernel, x, q, qd, qs, nblocks);
 }
 
 cudaError_t launch_rmsnorm(const float *x, const float *gamma, float *y, void *q8, int64_t m,

@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
     const int rg = warp / a.wg, wc = warp % a.wg;
     const int64_t row_bytes = (int64_t)a.nb * 18;
     const bool direct = (a.wg == 1 && a.cw == 1);
+    pdl_launch_dependents();
     pdl_wait();
 
     if (rg < a.rp) {

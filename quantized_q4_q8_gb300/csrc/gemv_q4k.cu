@@ -10,9 +10,10 @@
 // a few dp4a per byte.  One CTA per SM owns a contiguous range of rows.  A
 // producer warp keeps a ring of ~16 KB shared-memory stages full with the 1-D
 // bulk copy engine (cp.async.bulk, completion counted on an mbarrier), so the
-// bytes in flight live in shared memory, not registers.  A stage holds whole
-// "packs" (one row, or 8/nsb rows when a row has fewer than 8 super-blocks);
-// sixteen consumer warps take packs round-robin, each waiting only on the stage
+// bytes in flight live in shared memory, not registers, and it prefetches the
+// rest of the CTA's rows into L2 (cp.async.bulk.prefetch.L2) at once.  A stage
+// holds whole "packs" (one row, or 8/nsb rows when a row has fewer than 8
+// super-blocks); sixteen consumer warps take packs round-robin, each waiting only on the stage
 // of its own pack and releasing it with one mbarrier arrival, so warps run ahead
 // of each other across stages and the ring stays full.  Within a pack each
 // group of 4 lanes takes a super-block (two at a time for independent work) and
@@ -37,10 +38,10 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSB = 144;
-constexpr int kRingBudget = 160 * 1024;
+constexpr int kCtaSmem = 200 * 1024;
 constexpr int kStageTarget = 16 * 1024;
-constexpr int kXSmemMax = 64 * 1024;
-constexpr int kMaxStages = 32;
+constexpr int kXSmemMax = 48 * 1024;
+constexpr int kMaxStages = 16;
 
 __host__ __device__ inline int64_t x_smem_bytes(int64_t m, int64_t in_dim)
 {
@@ -67,8 +68,16 @@ struct Args {
     int NS;                // stages in the ring
     int stage_bytes;       // PS * rpp * R * row_bytes
     int x_smem;            // activations staged (swizzled) in shared memory
+    // f32 input quantised in the kernel (XIN_NORM / XIN_F32)
+    const float *xf;
+    int64_t ldxf;
+    const float *gamma;
+    int64_t norm_n;
+    float eps;
     unsigned *err;
 };
+
+enum XIn { XIN_Q8 = 0, XIN_NORM = 1, XIN_F32 = 2 };
 
 __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
 {
@@ -214,14 +223,19 @@ __device__ __forceinline__ float silu_mul(float g, float u)
     return g / (1.0f + expf(-g)) * u;
 }
 
-template <int MT, int EPI, bool XS>
+__device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+template <int MT, int EPI, bool XS, int XIN>
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint8_t *xsm = smem + (int64_t)a.NS * a.stage_bytes;
     const int64_t xbytes = XS ? x_smem_bytes(a.m, a.in_dim) : 0;
-    uint64_t *full = reinterpret_cast<uint64_t *>(xsm + xbytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(xsm + xbytes + 64);  // 64 B: norm reduction
     uint64_t *empty = full + a.NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,10 +254,32 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
         fence_mbar_init();
     }
     __syncthreads();
+    // the next kernel may become resident now: its weights stream while we drain
+    pdl_launch_dependents();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // everything beyond the first NS stages goes to L2 right away, so HBM
+            // stays busy even while the ring is full
+            for (int64_t k = a.NS; k < nstages; ++k) {
+                const int64_t u0 = r0 + k * a.PS * a.rpp;
+                const int n = (int)min((int64_t)a.PS * a.rpp, r1 - u0);
+                if (EPI == EPI_SWIGLU) {
+                    prefetch_l2(a.w[0] + u0 * a.row_bytes, (unsigned)(n * a.row_bytes));
+                    prefetch_l2(a.w[1] + u0 * a.row_bytes, (unsigned)(n * a.row_bytes));
+                } else {
+                    int r = 0;
+                    while (r < n) {
+                        const int64_t u = u0 + r;
+                        const int kseg = seg_of(a, u);
+                        const int run = (int)min((int64_t)(n - r), a.seg_begin[kseg + 1] - u);
+                        prefetch_l2(a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
+                                    (unsigned)(run * a.row_bytes));
+                        r += run;
+                    }
+                }
+            }
             int64_t k = 0;
             bool ok = true;
             for (; k < nstages; ++k) {
@@ -287,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                         set_error(a.err, DEV_TIMEOUT_DRAIN);
             }
         }
-        pdl_launch_dependents();
         return;
     }
 
@@ -300,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     x.gq = a.xq;
     x.gd = a.xd;
     x.gs = a.xs;
-    if (XS) {
+    if (XS && XIN == XIN_Q8) {
         // codes: 16-byte chunk i of super-block sbg (all tokens) -> padded slot layout
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
         const int4 *src = reinterpret_cast<const int4 *>(a.xq);
@@ -315,6 +350,44 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
         int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
         for (int64_t i = threadIdx.x; i < nds; i += kConsumerWarps * 32) ddst[i] = dsrc[i];
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    }
+    if (XS && XIN != XIN_Q8) {
+        // quantise the f32 input (RMS-normalised first for XIN_NORM) straight into
+        // the padded slot layout: warp per Q8_1 block, as the standalone kernels do
+        const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
+        float *dsm = reinterpret_cast<float *>(xsm + nsbx * kXSlot);
+        float *ssm = dsm + (int64_t)a.m * x.nb;
+        float *red = reinterpret_cast<float *>(full) - 16;  // 9 floats below the barriers
+        auto sync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
+        for (int t = 0; t < a.m; ++t) {
+            const float *xr = a.xf + t * a.ldxf;
+            float scale = 1.0f;
+            if (XIN == XIN_NORM) scale = rms_scale(fixed_order_sumsq(xr, a.norm_n, threadIdx.x, red, sync), a.norm_n, a.eps);
+            for (int64_t b = warp; b < x.nb; b += kConsumerWarps) {
+                const int64_t i = b * 32 + lane;
+                float v;
+                if (XIN == XIN_NORM)
+                    v = (i < a.norm_n) ? __fmul_rn(__fmul_rn(xr[i], scale), a.gamma[i]) : 0.0f;
+                else
+                    v = xr[i];
+                const float amax = warp_max(fabsf(v));
+                const float dq = __fdiv_rn(amax, 127.0f);
+                const int qi = q8_code(v, dq);
+                const int sum = warp_sum_int(qi);
+                const int64_t sb = b >> 3;
+                const int j = (int)(b & 7);
+                xsm[(t * (a.in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
+                    (uint8_t)(int8_t)qi;
+                if (lane == 0) {
+                    dsm[t * x.nb + b] = dq;
+                    ssm[t * x.nb + b] = __fmul_rn(dq, (float)sum);
+                }
+            }
+            sync();  // the reduction buffer is reused by the next token
+        }
+    }
+    if (XS) {
+        const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
         x.q = smem_u32(xsm);
         x.ds = smem_u32(xsm + nsbx * kXSlot);
     }
@@ -412,17 +485,17 @@ __global__ void q4k_subblock_dots_kernel(const uint8_t *w, const int8_t *xq, int
 size_t smem_bytes(const Args &a)
 {
     const int64_t xbytes = a.x_smem ? x_smem_bytes(a.m, a.in_dim) : 0;
-    return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 2 * 8 * (size_t)a.NS;
+    return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 64 + 2 * 8 * (size_t)a.NS;
 }
 
-template <int MT, int EPI, bool XS>
+template <int MT, int EPI, bool XS, int XIN>
 cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
 {
     static bool attr_done[64] = {};
     const int dev = dev_info().device;
     const size_t smem = smem_bytes(a);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS>,
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS, XIN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
@@ -438,29 +511,35 @@ cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS>, a);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS, XIN>, a);
 }
 
 template <int MT, int EPI>
-cudaError_t launch_x(const Args &a, int grid, cudaStream_t s)
+cudaError_t launch_x(const Args &a, int grid, cudaStream_t s, int xin)
 {
-    return a.x_smem ? launch_t<MT, EPI, true>(a, grid, s) : launch_t<MT, EPI, false>(a, grid, s);
+    if (xin == XIN_NORM) {
+        if constexpr (EPI != EPI_RESID) return launch_t<MT, EPI, true, XIN_NORM>(a, grid, s);
+        return cudaErrorInvalidValue;
+    }
+    if (xin == XIN_F32) {
+        if constexpr (EPI == EPI_RESID) return launch_t<MT, EPI, true, XIN_F32>(a, grid, s);
+        return cudaErrorInvalidValue;
+    }
+    return a.x_smem ? launch_t<MT, EPI, true, XIN_Q8>(a, grid, s) : launch_t<MT, EPI, false, XIN_Q8>(a, grid, s);
 }
 
 template <int EPI>
-cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s)
+cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
 {
-    if (a.m <= 1) return launch_x<1, EPI>(a, grid, s);
-    if (a.m <= 2) return launch_x<2, EPI>(a, grid, s);
-    if (a.m <= 4) return launch_x<4, EPI>(a, grid, s);
-    if (a.m <= 8) return launch_x<8, EPI>(a, grid, s);
-    return launch_x<16, EPI>(a, grid, s);
+    if (a.m <= 1) return launch_x<1, EPI>(a, grid, s, xin);
+    if (a.m <= 2) return launch_x<2, EPI>(a, grid, s, xin);
+    if (a.m <= 4) return launch_x<4, EPI>(a, grid, s, xin);
+    if (a.m <= 8) return launch_x<8, EPI>(a, grid, s, xin);
+    return launch_x<16, EPI>(a, grid, s, xin);
 }
 
-}  // namespace
-
-cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
-                            int64_t m, int64_t in_dim, cudaStream_t s)
+static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
+                                 const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
 {
     Args a = {};
     int64_t units = 0;
@@ -490,19 +569,36 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
     a.row_bytes = (int64_t)a.nsb * kSB;
     a.m = (int)m;
     a.in_dim = in_dim;
-    a.xq = static_cast<const int8_t *>(q8);
-    a.xd = reinterpret_cast<const float *>(static_cast<const uint8_t *>(q8) + m * in_dim);
-    a.xs = a.xd + m * (in_dim / 32);
+    if (q8) {
+        a.xq = static_cast<const int8_t *>(q8);
+        a.xd = reinterpret_cast<const float *>(static_cast<const uint8_t *>(q8) + m * in_dim);
+        a.xs = a.xd + m * (in_dim / 32);
+    }
+    int xin = XIN_Q8;
+    if (f32in) {
+        a.xf = f32in->x;
+        a.ldxf = f32in->ldx;
+        a.gamma = f32in->gamma;
+        a.norm_n = f32in->norm_n;
+        a.eps = f32in->eps;
+        xin = f32in->gamma ? XIN_NORM : XIN_F32;
+    }
     a.err = dev_error_word();
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
     a.PS = (int)std::max<int64_t>(1, kStageTarget / pack);
     a.stage_bytes = (int)(a.PS * pack);
     const int64_t xbytes = x_smem_bytes(m, in_dim);
-    a.x_smem = xbytes <= kXSmemMax ? 1 : 0;
-    const int64_t budget = (int64_t)dev_info().smem_optin - (a.x_smem ? xbytes : 0) - 1024;
-    int64_t ns = std::min<int64_t>(kRingBudget, budget) / a.stage_bytes;
+    a.x_smem = (xbytes <= kXSmemMax || f32in) ? 1 : 0;
+    const int64_t budget = (int64_t)kCtaSmem - (a.x_smem ? xbytes : 0) - 1024;
+    int64_t ns = budget / a.stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 2) {
+        // wide rows: fall back to stages of one pack
+        a.PS = 1;
+        a.stage_bytes = (int)pack;
+        ns = std::min<int64_t>(kMaxStages, budget / a.stage_bytes);
+    }
     if (ns < 2) return cudaErrorInvalidConfiguration;  // excluded by q4k_gemv_supported
     a.NS = (int)ns;
     if ((int64_t)smem_bytes(a) > (int64_t)dev_info().smem_optin) return cudaErrorInvalidConfiguration;
@@ -511,11 +607,34 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
     int64_t grid = units < sms ? units : sms;
     if (grid < 1) grid = 1;
     switch (epilogue) {
-    case EPI_STORE: return launch_epi<EPI_STORE>(a, (int)grid, s);
-    case EPI_RESID: return launch_epi<EPI_RESID>(a, (int)grid, s);
-    default: return launch_epi<EPI_SWIGLU>(a, (int)grid, s);
+    case EPI_STORE: return launch_epi<EPI_STORE>(a, (int)grid, s, xin);
+    case EPI_RESID: return launch_epi<EPI_RESID>(a, (int)grid, s, xin);
+    default: return launch_epi<EPI_SWIGLU>(a, (int)grid, s, xin);
     }
 }
+
+}  // namespace
+
+cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
+                            int64_t m, int64_t in_dim, cudaStream_t s)
+{
+    return launch_common(seg, nseg, epilogue, q8, nullptr, m, in_dim, s);
+}
+
+bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)
+{
+    return x_smem_bytes(m, in_dim) <= kXSmemMax;
+}
+
+cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
+                                int64_t m, int64_t in_dim, cudaStream_t s)
+{
+    if (!q4k_gemv_f32_input_ok(m, in_dim)) return cudaErrorInvalidValue;
+    return launch_common(seg, nseg, epilogue, nullptr, &in, m, in_dim, s);
+}
+
+
+
 
 bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue)
 {
@@ -523,10 +642,9 @@ bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue)
     const int64_t nsb = in_dim / 256;
     const int64_t rpp = (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1;
     const int64_t pack = R * rpp * nsb * kSB;
-    const int64_t stage = std::max<int64_t>(1, kStageTarget / pack) * pack;
     const int64_t xbytes = x_smem_bytes(m, in_dim);
-    const int64_t budget = (int64_t)dev_info().smem_optin - (xbytes <= kXSmemMax ? xbytes : 0) - 1024;
-    return std::min<int64_t>(kRingBudget, budget) / stage >= 2;
+    const int64_t budget = (int64_t)kCtaSmem - (xbytes <= kXSmemMax ? xbytes : 0) - 1024;
+    return budget / pack >= 2;
 }
 
 cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,

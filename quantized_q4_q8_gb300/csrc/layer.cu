@@ -7,11 +7,16 @@
 //   4 incremental attention -> 5 Q8_1 of the attention output -> 6 O GEMV ->
 //   7 residual -> 8 RMSNorm(ffn) -> 9 SwiGLU FFN (gate, up, silu(gate) * up, Q8_1,
 //   down) -> 10 residual.
-// Fusions here: 1+2 are one kernel (the norm writes the Q8_1 directly); Q, K and
-// V are one GEMV launch over the three matrices; RoPE and the KV append are one
-// small kernel; 4+5 are one split-sequence attention kernel whose merging CTA
-// quantises its heads; 6+7 and 9(down)+10 are GEMVs with a residual epilogue;
-// gate and up are one GEMV launch whose epilogue applies silu(gate) * up.
+// Fusions here: 1+2+3 are one launch: every CTA of the Q|K|V GEMV normalises
+// and quantises the layer input into its shared memory, and the three matrices
+// are one GEMV; 4+5 are one split-sequence attention kernel that also applies
+// RoPE (from a cos/sin table built once per step), appends k and v to the cache,
+// and whose merging CTA quantises its heads; 6+7 are one GEMV with a residual
+// epilogue; in 9 the norm + Q8_1 live in the gate/up GEMV, whose epilogue
+// applies silu(gate) * up, and the Q8_1 of h lives in the down GEMV, whose
+// epilogue adds the residual (10).  Five launches per layer.  When the batch is
+// too large for the activations to sit in shared memory, the norm and the
+// quantisation run as their own kernels instead.
 // The stack (forward_all_layers_gpu_to_logits in realizar 0.8.5
 // src/cuda/executor/layers/forward_utils.rs) chains the layers through two
 // workspace buffers, then the output RMSNorm and the Q4_0 LM head.
@@ -44,15 +49,26 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
     ws += align256((size_t)m * inter * 4);
     void *h8 = ws;
 
-    cudaError_t e = launch_rmsnorm(x, gamma, nullptr, x8, m, hidden, hidden_pad, eps, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     Q4kSegment gu[2] = {{w_gate, h, nullptr, inter, inter, 0}, {w_up, nullptr, nullptr, inter, 0, 0}};
-    e = launch_q4k_gemv(gu, 2, EPI_SWIGLU, x8, m, hidden_pad, s);
-    if (e != cudaSuccess) return e;
-    e = launch_q8_1_quantize(h, h8, m, inter, s);
+    if (q4k_gemv_f32_input_ok(m, hidden_pad)) {
+        // RMSNorm -> Q8_1 inside the gate/up GEMV (every CTA normalises the input)
+        e = launch_q4k_gemv_f32(gu, 2, EPI_SWIGLU, F32Input{x, hidden_pad, gamma, hidden, eps}, m, hidden_pad, s);
+    } else {
+        e = launch_rmsnorm(x, gamma, nullptr, x8, m, hidden, hidden_pad, eps, s);
+        if (e != cudaSuccess) return e;
+        e = launch_q4k_gemv(gu, 2, EPI_SWIGLU, x8, m, hidden_pad, s);
+    }
     if (e != cudaSuccess) return e;
     Q4kSegment dn = {w_down, out, x, hidden, hidden_pad, hidden_pad};
-    e = launch_q4k_gemv(&dn, 1, EPI_RESID, h8, m, inter, s);
+    if (q4k_gemv_f32_input_ok(m, inter)) {
+        // Q8_1 of h inside the down GEMV
+        e = launch_q4k_gemv_f32(&dn, 1, EPI_RESID, F32Input{h, inter, nullptr, 0, 0.0f}, m, inter, s);
+    } else {
+        e = launch_q8_1_quantize(h, h8, m, inter, s);
+        if (e != cudaSuccess) return e;
+        e = launch_q4k_gemv(&dn, 1, EPI_RESID, h8, m, inter, s);
+    }
     if (e != cudaSuccess) return e;
     if (hidden_pad > hidden)
         e = cudaMemset2DAsync(out + hidden, (size_t)hidden_pad * 4, 0, (size_t)(hidden_pad - hidden) * 4,
@@ -63,7 +79,7 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
 // ---------------------------------------------------------------- decode layer
 struct LayerWs {
     void *x8;
-    float *qkv, *q_rot, *part;
+    float *qkv, *rope_tab, *part;
     int *counters;
     void *a8;
     float *res1;
@@ -87,7 +103,7 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
     };
     w.x8 = take(q8_bytes(m, L.hidden_pad));
     w.qkv = reinterpret_cast<float *>(take((size_t)m * (q_dim + 2 * kv_dim) * 4));
-    w.q_rot = reinterpret_cast<float *>(take((size_t)m * q_dim * 4));
+    w.rope_tab = reinterpret_cast<float *>(take((size_t)m * L.head_dim * 4));
     w.part = reinterpret_cast<float *>(
         take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4));
     w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
@@ -112,15 +128,17 @@ size_t layer_counter_offset(const LayerDesc &L, int64_t m, int max_seq)
 }
 
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
-                        int position, float *q_rot, float *part, int *counters, const float *q,
-                        const float *k, const float *v, int64_t ld_qkv, float *att, void *att_q8)
+                        int position, float *rope_tab, int make_table, float *part, int *counters,
+                        const float *q, const float *k, const float *v, int64_t ld_qkv, float *att,
+                        void *att_q8)
 {
     AttnArgs a{};
     a.q = q;
     a.k = k;
     a.v = v;
     a.ld_qkv = ld_qkv;
-    a.q_rot = q_rot;
+    a.rope_tab = rope_tab;
+    a.make_table = make_table;
     a.kc = kv.k;
     a.vc = kv.v;
     a.seq_stride = kv.seq_stride;
@@ -149,22 +167,29 @@ AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const i
 
 cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
                                 const int32_t *positions, int position, int64_t m, float *output,
-                                void *workspace, cudaStream_t s)
+                                void *workspace, cudaStream_t s, int make_table)
 {
     LayerWs w = layer_ws(L, m, kv.max_seq, static_cast<uint8_t *>(workspace));
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int q_pad = (q_dim + 255) / 256 * 256;
     const int64_t ld_qkv = q_dim + 2 * kv_dim;
 
-    cudaError_t e = launch_rmsnorm(input, L.attn_gamma, nullptr, w.x8, m, L.hidden, L.hidden_pad, L.eps, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     Q4kSegment qkv[3] = {{L.wq, w.qkv, nullptr, q_dim, ld_qkv, 0},
                          {L.wk, w.qkv + q_dim, nullptr, kv_dim, ld_qkv, 0},
                          {L.wv, w.qkv + q_dim + kv_dim, nullptr, kv_dim, ld_qkv, 0}};
-    e = launch_q4k_gemv(qkv, 3, EPI_STORE, w.x8, m, L.hidden_pad, s);
+    if (q4k_gemv_f32_input_ok(m, L.hidden_pad)) {
+        // RMSNorm -> Q8_1 inside the Q|K|V GEMV
+        e = launch_q4k_gemv_f32(qkv, 3, EPI_STORE,
+                                F32Input{input, L.hidden_pad, L.attn_gamma, L.hidden, L.eps}, m, L.hidden_pad, s);
+    } else {
+        e = launch_rmsnorm(input, L.attn_gamma, nullptr, w.x8, m, L.hidden, L.hidden_pad, L.eps, s);
+        if (e != cudaSuccess) return e;
+        e = launch_q4k_gemv(qkv, 3, EPI_STORE, w.x8, m, L.hidden_pad, s);
+    }
     if (e != cudaSuccess) return e;
-    AttnArgs a = make_attn_args(L, m, kv, positions, position, w.q_rot, w.part, w.counters, w.qkv,
-                                w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, nullptr, w.a8);
+    AttnArgs a = make_attn_args(L, m, kv, positions, position, w.rope_tab, make_table, w.part, w.counters,
+                                w.qkv, w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, nullptr, w.a8);
     e = launch_attention(a, s);
     if (e != cudaSuccess) return e;
     Q4kSegment o = {L.wo, w.res1, input, L.hidden, L.hidden_pad, L.hidden_pad};
@@ -195,7 +220,8 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
     cudaError_t e = cudaSuccess;
     for (int l = 0; l < n_layers; ++l) {
         float *out = (l == n_layers - 1 && hidden_out) ? hidden_out : buf[l & 1];
-        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s);
+        // the RoPE table depends only on the positions: built by the first layer
+        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s, l == 0);
         if (e != cudaSuccess) return e;
         cur = out;
     }

@@ -146,4 +146,40 @@ __device__ __forceinline__ int q8_code(float x, float d)
     return static_cast<int>(r);
 }
 
+// Sum of squares of x[0, n) in a fixed order that does not depend on the launch
+// shape: 256 partial sums p_L = fma-accumulated x_i^2 over i = L mod 256 in
+// ascending i, a butterfly within each warp of 32 partials, then a butterfly over
+// the 8 warp sums.  Threads 0..255 of the block take part (tid = thread index
+// among the participating threads, nthreads >= 256, a multiple of 32);
+// `red` holds 9 floats of shared memory; `sync` synchronises the participating
+// threads.  Every participating thread returns the same total.
+template <typename Sync>
+__device__ __forceinline__ float fixed_order_sumsq(const float *x, int64_t n, int tid, float *red,
+                                                   Sync sync)
+{
+    const int lane = tid & 31, warp = tid >> 5;
+    float ss = 0.0f;
+    if (tid < 256)
+        for (int64_t i = tid; i < n; i += 256) {
+            const float v = x[i];
+            ss = fmaf(v, v, ss);
+        }
+    ss = warp_sum(ss);
+    if (lane == 0 && warp < 8) red[warp] = ss;
+    sync();
+    if (warp == 0) {
+        float v = (lane < 8) ? red[lane] : 0.0f;
+        v = warp_sum(v);
+        if (lane == 0) red[8] = v;
+    }
+    sync();
+    return red[8];
+}
+
+// RMSNorm scale 1 / sqrt(sum x^2 / n + eps) (rms_norm_inplace)
+__device__ __forceinline__ float rms_scale(float sumsq, int64_t n, float eps)
+{
+    return 1.0f / sqrtf(sumsq / (float)n + eps);
+}
+
 }  // namespace rz

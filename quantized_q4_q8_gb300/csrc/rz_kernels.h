@@ -50,8 +50,25 @@ struct Q4kSegment {
 cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
                             int64_t m, int64_t in_dim, cudaStream_t s);
 
+// The same GEMV with f32 activations quantised inside the kernel (every CTA
+// quantises the whole input into its shared memory): with gamma != nullptr the
+// input is first RMS-normalised over its first norm_n values (the fused
+// RMSNorm -> Q8_1 of the decode layer), else quantised as it is (the Q8_1 of the
+// FFN intermediate).  x: f32 [m][ldx].  Bit-identical to rz_rmsnorm / the Q8_1
+// kernel followed by launch_q4k_gemv.
+struct F32Input {
+    const float *x;
+    int64_t ldx;
+    const float *gamma;  // nullptr: no norm
+    int64_t norm_n;
+    float eps;
+};
+bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim);
+cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
+                                int64_t m, int64_t in_dim, cudaStream_t s);
+
 // Whether the stage ring of the GEMV fits in shared memory for this shape
-// (rows up to 23040 wide, 11520 for the paired gate/up launch).
+// (two stages of one pack: rows up to about 47000 wide at m = 1).
 bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue);
 
 cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,
@@ -61,7 +78,8 @@ cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, 
 struct AttnArgs {
     const float *q, *k, *v;      // pre-RoPE projections of token t at + t * ld_qkv
     int64_t ld_qkv;
-    float *q_rot;                // workspace f32 [m][q_dim]
+    float *rope_tab;             // workspace f32 [m][head_dim/2][2]: cos, sin of each pair angle
+    int make_table;              // 1: build rope_tab first (else it holds this step's table)
     float *kc, *vc;              // caches: token t at + t * seq_stride, row p at + p * kv_dim
     int64_t seq_stride;
     int max_seq;
@@ -80,8 +98,10 @@ struct AttnArgs {
 
 int attention_chunk_len(int max_seq, int n_kv_heads, int m);
 size_t attention_smem_bytes(int group, int head_dim, int chunk_len);
-// RoPE + KV append, then split-sequence attention with the merge and the Q8_1 of
-// the output (two launches).
+// the RoPE cos/sin table of every token (one small launch)
+cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s);
+// (table,) then split-sequence attention with RoPE, the KV append, the merge and
+// the Q8_1 of the output.
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- Q4_0 GEMV
@@ -114,11 +134,12 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
 size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
 size_t layer_counter_offset(const LayerDesc &L, int64_t m, int max_seq);
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
-                        int position, float *q_rot, float *part, int *counters, const float *q,
-                        const float *k, const float *v, int64_t ld_qkv, float *att, void *att_q8);
+                        int position, float *rope_tab, int make_table, float *part, int *counters,
+                        const float *q, const float *k, const float *v, int64_t ld_qkv, float *att,
+                        void *att_q8);
 cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
                                 const int32_t *positions, int position, int64_t m, float *output,
-                                void *workspace, cudaStream_t s);
+                                void *workspace, cudaStream_t s, int make_table = 1);
 size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
 cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
                                 const KvDesc *kvs, const int32_t *positions, int position, int64_t m,

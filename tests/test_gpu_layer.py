@@ -257,3 +257,29 @@ def test_decode_stack_qwen2_two_layers_and_lm_head(rz):
                                        pos, out_gamma, lm, vocab)
     assert_rel(hid[0], hid_r, what="stack hidden")
     assert_rel(logits[0], log_r, what="stack logits")
+
+
+def test_stack_as_first_call_in_a_fresh_process(rz, tmp_path):
+    """A process whose first librz call is the layer-level entry point (no earlier
+    kernel call) gets through the host-side shape checks."""
+    import subprocess
+    import sys
+    code = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, %r)
+import quantized_q4_q8_gb300 as rz, rz_synth as S
+sh = S.QWEN2
+dev = torch.device("cuda:0")
+w = S.layer_device(sh, "fresh", dev)
+L = rz.DeviceLayer(w, sh.hidden, sh.hidden_pad, sh.n_heads, sh.n_kv_heads, sh.head_dim, sh.inter,
+                   sh.eps, sh.rope_theta, sh.rope_mode)
+kv = rz.DeviceKV(*S.kv_prefill_device(sh, "fresh.kv", 16, 3, 1, dev))
+stack = rz.DeviceStack([L], [kv], torch.ones(sh.hidden, device=dev), S.q4_0_weight_device("fresh.lm", 64, sh.hidden, dev), 64)
+x = torch.zeros((1, sh.hidden_pad), device=dev); x[:, :sh.hidden] = 1.0
+hid, logits = rz.decode_stack(x, stack, position=3)
+torch.cuda.synchronize()
+assert torch.isfinite(logits).all()
+print("fresh ok")
+""" % (str(__import__("os").path.dirname(__import__("os").path.dirname(__file__))),)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "fresh ok" in r.stdout, r.stderr[-3000:]
