@@ -107,13 +107,14 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
     }
 }
 
-// grid (n_chunks, n_kv_heads, m), 256 threads; CPT = head_dim / 32.
+// grid (n_kv_heads, m, launch_chunks), chunk-major so that low chunks (needed by
+// every token) are scheduled first; 256 threads; CPT = head_dim / 32.
 // shared memory: qs [G][hd] | kn [hd] | vn [hd] | ps [G][64] | stat [G][2] | red [8][G][hd] | flag
 template <int CPT>
 __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const AttnArgs a)
 {
     extern __shared__ __align__(16) float sm[];
-    const int chunk = blockIdx.x, kvh = blockIdx.y, t = blockIdx.z;
+    const int kvh = blockIdx.x, t = blockIdx.y, chunk = blockIdx.z;
     const int hd = a.head_dim, G = a.group;
     float *qs = sm;
     float *kn = qs + G * hd;
@@ -128,6 +129,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
 
     const int pos = token_position(a, t);
     const bool pos_ok = pos >= 0 && pos < a.max_seq;
+    // chunks holding rows of this token; after a bad position chunk 0 alone takes
+    // part and the merge writes zeros
+    const int nc = pos_ok ? min(a.n_chunks, pos / kChunk + 1) : 1;
+    if (chunk >= nc) return;
     const int c0 = chunk * kChunk;
     const int n = pos_ok ? max(0, min(kChunk, pos + 1 - c0)) : 0;
     const bool own = pos_ok && pos >= c0 && pos < c0 + kChunk;  // this chunk holds the new row
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     if (tid == 0) {
         int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
         const int prev = atomicAdd(cnt, 1);
-        const int last = (prev == a.n_chunks - 1);
+        const int last = (prev == nc - 1);
         if (last) *cnt = 0;  // ready for the next call
         *flag = last;
     }
@@ -260,20 +265,39 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     if (!*flag) return;
     __threadfence();
 
-    const int nc = pos_ok ? min(a.n_chunks, pos / kChunk + 1) : 0;  // chunks holding rows
+    // chunk statistics in parallel (thread per (head, chunk)), then the weights
+    float *wts = ps;  // [G][kChunk] reused: chunk weights exp(m_c - M)
+    for (int g = warp; g < G; g += kAttnThreads / 32) {
+        float mc[2], lc[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = lane + 32 * h;
+            mc[h] = c < nc ? __ldcg(part_rec(a, t, kvh, c, g)) : -INFINITY;
+            lc[h] = c < nc ? __ldcg(part_rec(a, t, kvh, c, g) + 1) : 0.0f;
+        }
+        const float M = warp_max(fmaxf(mc[0], mc[1]));
+        float lsum = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = lane + 32 * h;
+            const float w = (c < nc && lc[h] > 0.0f) ? expf(mc[h] - M) : 0.0f;
+            if (c < kChunk) wts[g * kChunk + c] = w;
+            lsum += w * lc[h];
+        }
+        lsum = warp_sum(lsum);
+        if (lane == 0) stat[2 * g] = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;  // 0 only after a bad position
+    }
+    __syncthreads();
     float *outv = red;  // merged output [G][hd]
     for (int i = tid; i < G * hd; i += kAttnThreads) {
         const int g = i / hd, dd = i % hd;
-        float M = -INFINITY;
-        for (int c = 0; c < nc; ++c) M = fmaxf(M, __ldcg(part_rec(a, t, kvh, c, g)));
-        float Lsum = 0.0f, acc = 0.0f;
+        float acc = 0.0f;
+#pragma unroll 8
         for (int c = 0; c < nc; ++c) {
-            const float *rec = part_rec(a, t, kvh, c, g);
-            const float w = expf(__ldcg(rec) - M);
-            Lsum += __ldcg(rec + 1) * w;
-            acc += __ldcg(rec + 2 + dd) * w;
+            const float w = wts[g * kChunk + c];
+            if (w != 0.0f) acc = fmaf(__ldcg(part_rec(a, t, kvh, c, g) + 2 + dd), w, acc);
         }
-        outv[g * hd + dd] = (Lsum > 0.0f) ? acc / Lsum : 0.0f;  // 0 only after a bad position
+        outv[g * hd + dd] = acc * stat[2 * g];
     }
     __syncthreads();
     const int64_t col0 = (int64_t)kvh * G * hd;
@@ -361,8 +385,8 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
     }
-    return launch_ex(fn, dim3((unsigned)a.n_chunks, (unsigned)a.n_kv_heads, (unsigned)a.m), dim3(kAttnThreads),
-                     smem, s, kargs);
+    return launch_ex(fn, dim3((unsigned)a.n_kv_heads, (unsigned)a.m, (unsigned)a.launch_chunks),
+                     dim3(kAttnThreads), smem, s, kargs);
 }
 
 }  // namespace rz

@@ -47,34 +47,38 @@ __global__ void q8_1_quantize_kernel(const float *__restrict__ x, int8_t *__rest
     q8_block_store(v, lane, q + blk * 32, qd + blk, qs + blk);
 }
 
-constexpr int kNormThreads = 1024;
+constexpr int kNormThreads = 32 * kRowWarps;  // 512: the register-row layout
 
+// Rows up to kRowWarps * kRowBlocksPerWarp * 32 values, reduced in the same
+// fixed order as the GEMV prologue, so the fused and the separate paths give
+// identical bits.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
     const float *__restrict__ x, const float *__restrict__ gamma, float *__restrict__ y,
     int8_t *__restrict__ q, float *__restrict__ qd, float *__restrict__ qs, int64_t n,
     int64_t n_pad, float eps)
 {
-    __shared__ float red[9];
+    __shared__ float red[kRowWarps + 1];
     const int64_t row = blockIdx.x;
     const float *xr = x + row * n_pad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
     pdl_wait();
-    const float total = fixed_order_sumsq(xr, n, tid, red, [] { __syncthreads(); });
-    const float scale = rms_scale(total, n, eps);
-
-    if (q != nullptr) {
-        // n_pad % 32 == 0: warps take whole Q8_1 blocks
-        const int64_t nb = n_pad / 32;
-        for (int64_t b = warp; b < nb; b += kNormThreads / 32) {
+    const int64_t nb = (n_pad + 31) / 32;
+    const float scale = rms_scale(row_sumsq(xr, nb, n, warp, lane, red, [] { __syncthreads(); }), n, eps);
+    for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
+        if (warp + (int64_t)kRowWarps * k0 >= nb) break;
+        RowBatch rb;
+        row_batch(xr, gamma, nb, n, warp, lane, k0, rb);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
+            if (b >= nb) break;
             const int64_t i = b * 32 + lane;
-            const float v = (i < n) ? __fmul_rn(__fmul_rn(xr[i], scale), gamma[i]) : 0.0f;
-            if (y) y[row * n_pad + i] = v;
-            q8_block_store(v, lane, q + row * n_pad + b * 32, qd + row * nb + b, qs + row * nb + b);
+            const float v = (i < n) ? __fmul_rn(__fmul_rn(rb.v[u], scale), rb.g[u]) : 0.0f;
+            if (y && i < n_pad) y[row * n_pad + i] = v;
+            if (q) q8_block_store(v, lane, q + row * n_pad + b * 32, qd + row * (n_pad / 32) + b,
+                                  qs + row * (n_pad / 32) + b);
         }
-    } else {
-        for (int64_t i = tid; i < n_pad; i += kNormThreads)
-            y[row * n_pad + i] = (i < n) ? __fmul_rn(__fmul_rn(xr[i], scale), gamma[i]) : 0.0f;
     }
 }
 

@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     uint8_t *ring = smem;
     uint8_t *xsm = smem + (int64_t)a.NS * a.stage_bytes;
     const int64_t xbytes = XS ? x_smem_bytes(a.m, a.in_dim) : 0;
-    uint64_t *full = reinterpret_cast<uint64_t *>(xsm + xbytes + 64);  // 64 B: norm reduction
+    uint64_t *full = reinterpret_cast<uint64_t *>(xsm + xbytes + 96);  // 96 B: norm reduction
     uint64_t *empty = full + a.NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -357,34 +357,41 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
         float *dsm = reinterpret_cast<float *>(xsm + nsbx * kXSlot);
         float *ssm = dsm + (int64_t)a.m * x.nb;
-        float *red = reinterpret_cast<float *>(full) - 16;  // 9 floats below the barriers
+        float *red = reinterpret_cast<float *>(full) - 24;  // 17 floats below the barriers
         auto sync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
         for (int t = 0; t < a.m; ++t) {
-            const float *xr = a.xf + t * a.ldxf;
+            // loads unrolled eight blocks at a time, so they are in flight together
+            const float *xrow = a.xf + t * a.ldxf;
+            const int64_t nval = XIN == XIN_NORM ? a.norm_n : a.in_dim;
             float scale = 1.0f;
-            if (XIN == XIN_NORM) scale = rms_scale(fixed_order_sumsq(xr, a.norm_n, threadIdx.x, red, sync), a.norm_n, a.eps);
-            for (int64_t b = warp; b < x.nb; b += kConsumerWarps) {
-                const int64_t i = b * 32 + lane;
-                float v;
-                if (XIN == XIN_NORM)
-                    v = (i < a.norm_n) ? __fmul_rn(__fmul_rn(xr[i], scale), a.gamma[i]) : 0.0f;
-                else
-                    v = xr[i];
-                const float amax = warp_max(fabsf(v));
-                const float dq = __fdiv_rn(amax, 127.0f);
-                const int qi = q8_code(v, dq);
-                const int sum = warp_sum_int(qi);
-                const int64_t sb = b >> 3;
-                const int j = (int)(b & 7);
-                xsm[(t * (a.in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
-                    (uint8_t)(int8_t)qi;
-                if (lane == 0) {
-                    dsm[t * x.nb + b] = dq;
-                    ssm[t * x.nb + b] = __fmul_rn(dq, (float)sum);
+            if (XIN == XIN_NORM) scale = rms_scale(row_sumsq(xrow, x.nb, nval, warp, lane, red, sync), a.norm_n, a.eps);
+            for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
+                if (warp + (int64_t)kRowWarps * k0 >= x.nb) break;
+                RowBatch rb;
+                row_batch(xrow, XIN == XIN_NORM ? a.gamma : nullptr, x.nb, nval, warp, lane, k0, rb);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
+                    if (b >= x.nb) break;
+                    const int64_t i = b * 32 + lane;
+                    float v = rb.v[u];
+                    if (XIN == XIN_NORM) v = (i < a.norm_n) ? __fmul_rn(__fmul_rn(v, scale), rb.g[u]) : 0.0f;
+                    const float amax = warp_max(fabsf(v));
+                    const float dq = __fdiv_rn(amax, 127.0f);
+                    const int qi = q8_code(v, dq);
+                    const int sum = warp_sum_int(qi);
+                    const int64_t sb = b >> 3;
+                    const int j = (int)(b & 7);
+                    xsm[(t * (a.in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
+                        (uint8_t)(int8_t)qi;
+                    if (lane == 0) {
+                        dsm[t * x.nb + b] = dq;
+                        ssm[t * x.nb + b] = __fmul_rn(dq, (float)sum);
+                    }
                 }
             }
-            sync();  // the reduction buffer is reused by the next token
         }
+        sync();
     }
     if (XS) {
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
@@ -485,7 +492,7 @@ __global__ void q4k_subblock_dots_kernel(const uint8_t *w, const int8_t *xq, int
 size_t smem_bytes(const Args &a)
 {
     const int64_t xbytes = a.x_smem ? x_smem_bytes(a.m, a.in_dim) : 0;
-    return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 64 + 2 * 8 * (size_t)a.NS;
+    return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 96 + 2 * 8 * (size_t)a.NS;
 }
 
 template <int MT, int EPI, bool XS, int XIN>
@@ -623,7 +630,7 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
 
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)
 {
-    return x_smem_bytes(m, in_dim) <= kXSmemMax;
+    return x_smem_bytes(m, in_dim) <= kXSmemMax && in_dim <= 32LL * kRowWarps * kRowBlocksPerWarp;
 }
 
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,

@@ -157,6 +157,7 @@ AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const i
     a.rope_mode = L.rope_mode;
     a.chunk_len = attention_chunk_len(kv.max_seq, L.n_kv_heads, (int)m);
     a.n_chunks = (kv.max_seq + a.chunk_len - 1) / a.chunk_len;
+    a.launch_chunks = positions ? a.n_chunks : position / a.chunk_len + 1;
     a.part = part;
     a.counters = counters;
     a.att = att;

@@ -146,34 +146,67 @@ __device__ __forceinline__ int q8_code(float x, float d)
     return static_cast<int>(r);
 }
 
-// Sum of squares of x[0, n) in a fixed order that does not depend on the launch
-// shape: 256 partial sums p_L = fma-accumulated x_i^2 over i = L mod 256 in
-// ascending i, a butterfly within each warp of 32 partials, then a butterfly over
-// the 8 warp sums.  Threads 0..255 of the block take part (tid = thread index
-// among the participating threads, nthreads >= 256, a multiple of 32);
-// `red` holds 9 floats of shared memory; `sync` synchronises the participating
-// threads.  Every participating thread returns the same total.
-template <typename Sync>
-__device__ __forceinline__ float fixed_order_sumsq(const float *x, int64_t n, int tid, float *red,
-                                                   Sync sync)
+// One activation row walked by 16 warps (512 threads): warp w owns the Q8_1
+// blocks b = w, w + 16, w + 32, ... (at most kRowBlocksPerWarp of them) and lane l
+// element 32 b + l of each.  Values at or beyond `n_valid` count as 0.  Loads are
+// unrolled eight at a time so they are in flight together.
+constexpr int kRowWarps = 16;
+constexpr int kRowBlocksPerWarp = 32;  // rows up to 16384 values
+
+__device__ __forceinline__ float row_value(const float *x, int64_t nb, int64_t n_valid, int warp, int lane,
+                                           int k)
 {
-    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t b = warp + (int64_t)kRowWarps * k;
+    const int64_t i = b * 32 + lane;
+    return (b < nb && i < n_valid) ? __ldg(x + i) : 0.0f;
+}
+
+// The values (and gammas, when given) of 8 consecutive blocks k0 .. k0+7 of this
+// warp, loaded before any use through the read-only path so that stores to
+// shared memory between them cannot hold the loads back.
+struct RowBatch {
+    float v[8], g[8];
+};
+
+__device__ __forceinline__ void row_batch(const float *x, const float *gamma, int64_t nb, int64_t n_valid,
+                                          int warp, int lane, int k0, RowBatch &r)
+{
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
+        const int64_t i = b * 32 + lane;
+        const bool in = b < nb && i < n_valid;
+        r.v[u] = in ? __ldg(x + i) : 0.0f;
+        r.g[u] = (in && gamma) ? __ldg(gamma + i) : 0.0f;
+    }
+}
+
+// Sum of squares of the row in a fixed order: per thread over its blocks in
+// ascending block order, then the xor butterfly of each warp, then the butterfly
+// over the 16 warp sums.  `red` holds 17 floats of shared memory; `sync`
+// synchronises the 512 participating threads.  Every thread returns the total.
+template <typename Sync>
+__device__ __forceinline__ float row_sumsq(const float *x, int64_t nb, int64_t n_valid, int warp, int lane,
+                                           float *red, Sync sync)
+{
     float ss = 0.0f;
-    if (tid < 256)
-        for (int64_t i = tid; i < n; i += 256) {
-            const float v = x[i];
-            ss = fmaf(v, v, ss);
-        }
+#pragma unroll 8
+    for (int k = 0; k < kRowBlocksPerWarp; ++k) {
+        const float v = row_value(x, nb, n_valid, warp, lane, k);
+        ss = fmaf(v, v, ss);
+    }
     ss = warp_sum(ss);
-    if (lane == 0 && warp < 8) red[warp] = ss;
+    if (lane == 0) red[warp] = ss;
     sync();
     if (warp == 0) {
-        float v = (lane < 8) ? red[lane] : 0.0f;
+        float v = (lane < kRowWarps) ? red[lane] : 0.0f;
         v = warp_sum(v);
-        if (lane == 0) red[8] = v;
+        if (lane == 0) red[kRowWarps] = v;
     }
     sync();
-    return red[8];
+    const float total = red[kRowWarps];
+    sync();  // red may be reused right after
+    return total;
 }
 
 // RMSNorm scale 1 / sqrt(sum x^2 / n + eps) (rms_norm_inplace)

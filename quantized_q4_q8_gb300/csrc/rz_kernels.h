@@ -88,7 +88,8 @@ struct AttnArgs {
     int m, n_heads, n_kv_heads, head_dim, group, q_dim, q_pad, kv_dim;
     float rope_theta;
     int rope_mode;
-    int chunk_len, n_chunks;
+    int chunk_len, n_chunks;     // n_chunks covers max_seq (workspace layout)
+    int launch_chunks;           // chunks launched: enough for the host position, else n_chunks
     float *part;                 // workspace: [m][n_kv_heads][n_chunks][group][head_dim + 2]
     int *counters;               // workspace: [m][n_kv_heads], zero before the first call
     float *att;                  // f32 [m][q_dim] output, or nullptr
