@@ -188,6 +188,7 @@ rz_status rz_rmsnorm(const float *x, const float *gamma, float *y, void *q8, int
     if (!x || !gamma || (!y && !q8)) return fail(RZ_ERR_INVALID_ARG, "rz_rmsnorm: null pointer");
     if (m < 1 || n < 1 || n_pad < n) return fail(RZ_ERR_INVALID_ARG, "rz_rmsnorm: bad sizes");
     if (m > (1 << 30)) return fail(RZ_ERR_SHAPE, "rz_rmsnorm: m too large");
+    if (n_pad > 16384) return fail(RZ_ERR_UNSUPPORTED, "rz_rmsnorm: rows longer than 16384 values");
     if (q8 && (n_pad % 32)) return fail(RZ_ERR_SHAPE, "rz_rmsnorm: n_pad %% 32 != 0 with a Q8_1 output");
     if (!(eps >= 0.0f)) return fail(RZ_ERR_INVALID_ARG, "rz_rmsnorm: eps must be >= 0");
     if (!aligned16(x) || !aligned16(gamma) || (y && !aligned16(y)) || (q8 && !aligned16(q8)))
@@ -281,6 +282,7 @@ rz_status check_kv(const rz_kv_cache *kv, const char *fn, int64_t m, int kv_dim,
     if (!kv || !kv->k || !kv->v) return fail(RZ_ERR_INVALID_ARG, "%s: null KV cache", fn);
     if (!aligned16(kv->k) || !aligned16(kv->v)) return fail(RZ_ERR_ALIGN, "%s: KV cache must be 16-byte aligned", fn);
     if (kv->max_seq < 1) return fail(RZ_ERR_INVALID_ARG, "%s: max_seq=%d", fn, kv->max_seq);
+    if (kv->max_seq > 4096) return fail(RZ_ERR_UNSUPPORTED, "%s: max_seq=%d > 4096", fn, kv->max_seq);
     if (m > 1 && kv->seq_stride < (int64_t)kv->max_seq * kv_dim)
         return fail(RZ_ERR_SHAPE, "%s: seq_stride=%lld < max_seq*kv_dim", fn, (long long)kv->seq_stride);
     *out = KvDesc{kv->k, kv->v, m > 1 ? kv->seq_stride : 0, kv->max_seq};
