@@ -245,6 +245,22 @@ rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, co
                           rz_stream stream);
 
 /*
+ * rz_swiglu_ffn_static -- the same computation as rz_swiglu_ffn, for callers that
+ * cannot allocate device memory or pass a workspace (the paper has no
+ * counterpart: this is a packaging variant of rz_swiglu_ffn).  Its intermediates
+ * live in a fixed 512 KiB device array inside the library (every GPU that loads
+ * the library holds one until the process exits); shapes whose scratch
+ * (rz_swiglu_ffn_workspace_bytes) exceeds 512 KiB are rejected with
+ * RZ_ERR_UNSUPPORTED.  It calls no allocator.  The first call on a device looks
+ * up the array's device address (a runtime query), so make that first call before
+ * any stream capture.  All calls share the array: calls that overlap on the GPU
+ * race and must be ordered by the caller.  Arguments as for rz_swiglu_ffn.
+ */
+rz_status rz_swiglu_ffn_static(const float *x, const float *gamma, const void *w_gate, const void *w_up,
+                               const void *w_down, float *out, int64_t m, int64_t hidden,
+                               int64_t hidden_pad, int64_t inter, float eps, rz_stream stream);
+
+/*
  * rz_check_device_error -- synchronise `stream`, read the device error word of the
  * current device and clear it.  *code_out (nullable) receives the raw code (0 = none).
  * Returns RZ_OK, RZ_ERR_TIMEOUT (a bounded wait ran out) or RZ_ERR_DEVICE (a

@@ -64,6 +64,7 @@ SIGNATURES = {
     "rz_residual_add": [_vp, _vp, _vp, _i64, _vp],
     "rz_swiglu_ffn_workspace_bytes": [_i64, _i64, _i64],
     "rz_swiglu_ffn": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp, _sz, _vp],
+    "rz_swiglu_ffn_static": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _vp],
     "rz_attention_workspace_bytes": [_i64, _i32, _i32, _i32, _i32],
     "rz_attention_decode": [_vp, _vp, _vp, _i64, _KVP, _vp, _i32, _i64, _i32, _i32, _i32, _f32,
                             _i32, _vp, _vp, _vp, _sz, _vp],

@@ -92,6 +92,16 @@ rz_status check_device()
 
 }  // namespace
 
+// Shared with entry points defined in other files: set this thread's last-error
+// message, and run the device check (and the per-device set-up) of this file.
+rz_status record_error(rz_status st, const char *msg)
+{
+    t_last_error = msg;
+    return st;
+}
+
+rz_status ensure_device() { return check_device(); }
+
 const DevInfo &dev_info()
 {
     int dev = 0;

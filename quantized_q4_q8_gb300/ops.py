@@ -12,7 +12,7 @@ __all__ = [
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
     "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
     "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
-    "swiglu_ffn", "attention_workspace_bytes", "attention_decode",
+    "swiglu_ffn", "rz_swiglu_ffn_static", "attention_workspace_bytes", "attention_decode",
     "decode_layer_workspace_bytes", "decode_layer", "rz_decode_stack", "decode_stack",
 ]
 
@@ -227,6 +227,13 @@ def swiglu_ffn(x, gamma, w_gate, w_up, w_down, hidden, hidden_pad, inter, eps, o
     call("rz_swiglu_ffn", _ptr(x), _ptr(gamma), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(out),
          m, hidden, hidden_pad, inter, eps, _ptr(ws), ws.numel(), _stream(stream))
     return out
+
+
+def rz_swiglu_ffn_static(x, gamma, w_gate, w_up, w_down, out, m, hidden, hidden_pad, inter, eps,
+                         stream=None):
+    """The SwiGLU FFN with the library's static scratch (no workspace argument)."""
+    return call("rz_swiglu_ffn_static", _ptr(x), _ptr(gamma), _ptr(w_gate), _ptr(w_up),
+                _ptr(w_down), _ptr(out), m, hidden, hidden_pad, inter, eps, _stream(stream))
 
 
 def attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, max_seq):
