@@ -260,9 +260,10 @@ class StackWorkload:
     vocab = S.LLAMA_VOCAB
     max_seq = S.LLAMA_MAX_SEQ
 
-    def __init__(self, m: int, position: int):
+    def __init__(self, m: int, position: int, n_layers: int = S.LLAMA_LAYERS):
         self.m = m
         self.position = position
+        self.n_layers = n_layers
         self.shape = S.LLAMA7B
         self.name = f"llama7b_q4k_decode_stack_l{self.n_layers}_m{m}_pos{position}"
 
@@ -417,7 +418,7 @@ class StackWorkload:
         t_head = time.perf_counter() - t0
         t_layer = sum(t_layers) / len(t_layers)
         t_step = (self.n_layers * t_layer + t_head) * self.m
-        one_token = StackWorkload(1, self.position)
+        one_token = StackWorkload(1, self.position, self.n_layers)
         return {"value": one_token.bytes_per_step() * self.m / t_step / 1e9, "unit": "GB/s",
                 "cores": 1, "kind": "oracle",
                 "tokens_per_s": self.m / t_step,
@@ -446,6 +447,12 @@ class StackWorkload:
 WORKLOADS = {"gemv": GemvWorkload, "stack": StackWorkload}
 
 
+def make_workload(args):
+    if args.workload == "gemv":
+        return GemvWorkload(args.batch)
+    return StackWorkload(args.batch, args.position, args.layers)
+
+
 # ----------------------------------------------------------------------------- arms
 def run_rz(args, world, rank, local, pg):
     import torch
@@ -453,8 +460,7 @@ def run_rz(args, world, rank, local, pg):
     torch.cuda.set_device(dev)
     import quantized_q4_q8_gb300 as rz
     rz.load()
-    wl = WORKLOADS[args.workload](args.batch) if args.workload == "gemv" else \
-        WORKLOADS[args.workload](args.batch, args.position)
+    wl = make_workload(args)
     wl.setup(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_line = wl.cpu_baseline()   # before any timing: the host is idle here
@@ -549,8 +555,7 @@ def run_reference(args, world, rank):
     """The oracle timed on the host cores on a bounded sample of the same workload."""
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload](args.batch) if args.workload == "gemv" else \
-        WORKLOADS[args.workload](args.batch, args.position)
+    wl = make_workload(args)
     samples = []
     for _ in range(args.steps):
         samples.append(wl.cpu_sample())
@@ -580,6 +585,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--position", type=int, default=1024)
+    ap.add_argument("--layers", type=int, default=S.LLAMA_LAYERS,
+                    help="layers of the stack (32 for the benchmark; fewer for small profiles)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
