@@ -255,7 +255,6 @@ class GemvWorkload:
 
 class StackWorkload:
     """One decode step of the 32-layer Llama-7B-shaped Q4_K stack + Q4_0 LM head."""
-    kernel_file = "gemv_q4k.cu"
     n_layers = S.LLAMA_LAYERS
     vocab = S.LLAMA_VOCAB
     max_seq = S.LLAMA_MAX_SEQ
@@ -288,10 +287,23 @@ class StackWorkload:
         return self.n_layers * sum(o * (i // 256) * S.Q4K_BYTES + m * i * 5 // 4 + m * o * 4
                                    for o, i in sh.weight_shapes().values())
 
+    def head_bytes(self):
+        sh, m = self.shape, self.m
+        return self.vocab * (sh.hidden // 32) * S.Q4_0_BYTES + sh.hidden * 4 + m * sh.hidden * 4 + \
+            m * self.vocab * 4
+
     def launches_per_step(self):
-        # RoPE table; per layer: Q|K|V GEMV (fused norm), attention, O GEMV, gate/up GEMV
-        # (fused norm), down GEMV (fused Q8_1 of h); output norm; LM head
-        return 1 + self.n_layers * 5 + 2
+        # the library's own count: the persistent kernel (one per 32 layers) + output
+        # norm + LM head, or RoPE table + 5 per layer + output norm + LM head
+        return self.stack.launches(self.m, with_head=True)
+
+    @property
+    def persistent(self):
+        return self.stack.launches(self.m, with_head=False) == (self.n_layers + 31) // 32
+
+    @property
+    def kernel_file(self):
+        return "decode_persistent.cu" if self.persistent else "gemv_q4k.cu"
 
     def setup(self, dev):
         import torch
@@ -321,6 +333,7 @@ class StackWorkload:
         self.logits_pin = torch.empty((self.m, self.vocab), dtype=torch.float32).pin_memory()
         self.graph = None
         self.gemv_graph = None
+        self.layers_graph = None
 
     def _launch(self, stream):
         self.rz.rz_decode_stack(self.x, self.stack, None, self.position, self.m, self.hid,
@@ -353,17 +366,52 @@ class StackWorkload:
         return self.launches_per_step()
 
     def dominant(self):
+        if self.persistent:
+            n = (self.n_layers + 31) // 32
+            return {"kernel": "decode_persistent_kernel",
+                    "bytes_per_launch": (self.bytes_per_step() - self.head_bytes()) / n,
+                    "launches_per_step": n}
         n = self.n_layers * 7
         return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.gemv_bytes() / n,
                 "launches_per_step": n}
 
-    def dominant_time(self, stream, reps=5):
-        """Average duration of the Q4_K GEMV launches of one step: the 224 weight
-        matrices of the 32 layers launched back to back (CUDA graph) against the
-        layer's Q8_1 activation, timed with CUDA events on the stream."""
+    def _time_graph(self, graph, stream, reps):
+        import torch
+        graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def dominant_time(self, stream, reps=20):
+        """Average launch duration of the dominant kernel, CUDA events on the stream.
+        Persistent path: the step's layers alone (rz_decode_layers: the persistent
+        kernel, after a memset of its 8 barrier bytes) replayed as a graph.  Launch
+        sequence: the 224 weight matrices of the 32 layers launched back to back
+        (CUDA graph) against the layer's Q8_1 activation."""
         import torch
         rz = self.rz
         sh = self.shape
+        if self.persistent:
+            if self.layers_graph is None:
+                self.layers_out = torch.empty((self.m, sh.hidden_pad), dtype=torch.float32,
+                                              device=self.x.device)
+                def launch():
+                    rz.rz_decode_layers(self.x, self.stack, None, self.position, self.m,
+                                        self.layers_out, self.ws, stream=stream)
+                launch()
+                torch.cuda.synchronize()
+                self.layers_graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(self.layers_graph, stream=stream):
+                    launch()
+                torch.cuda.synchronize()
+            return self._time_graph(self.layers_graph, stream, reps) / self.dominant()["launches_per_step"]
         if self.gemv_graph is None:
             dev = self.x.device
             self.gx = {i: rz.q8_1_quantize(torch.randn((self.m, i), device=dev,
@@ -382,17 +430,7 @@ class StackWorkload:
             with torch.cuda.graph(self.gemv_graph, stream=stream):
                 launch()
             torch.cuda.synchronize()
-        self.gemv_graph.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                self.gemv_graph.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / (reps * self.n_layers * 7)
+        return self._time_graph(self.gemv_graph, stream, 5) / (self.n_layers * 7)
 
     def cpu_sample(self, n_sample_layers: int = 1):
         """The oracle on n_sample_layers layers of the same shape plus the LM head, one
@@ -430,18 +468,21 @@ class StackWorkload:
     def cpu_baseline(self):
         return self.cpu_sample(n_sample_layers=16)
 
-    def config(self):
+    def config_ref(self):
         return {"workload": self.name, "layers": self.n_layers, "hidden": self.shape.hidden,
                 "intermediate": self.shape.inter, "heads": self.shape.n_heads,
                 "kv_heads": self.shape.n_kv_heads, "head_dim": self.shape.head_dim,
                 "vocab": self.vocab, "batch_tokens": self.m, "position": self.position,
                 "max_seq": self.max_seq,
                 "weights_bytes": self.weight_bytes(),
-                "l2": "inputs larger than L2 (3.7 GB of weights per step)",
-                "launch": "one CUDA graph per step (PDL edges between kernels)"}
+                "l2": "inputs larger than L2 (3.7 GB of weights per step)"}
 
-    def config_ref(self):
-        return self.config()
+    def config(self):
+        c = self.config_ref()
+        c["launch"] = ("one CUDA graph per step: the persistent decode kernel (cooperative, one CTA "
+                       "per SM, all layers) + output RMSNorm + LM head") if self.persistent else \
+            "one CUDA graph per step (PDL edges between kernels)"
+        return c
 
 
 WORKLOADS = {"gemv": GemvWorkload, "stack": StackWorkload}
@@ -460,6 +501,7 @@ def run_rz(args, world, rank, local, pg):
     torch.cuda.set_device(dev)
     import quantized_q4_q8_gb300 as rz
     rz.load()
+    rz.set_persistent(args.persistent)
     wl = make_workload(args)
     wl.setup(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -583,6 +625,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="rz", choices=["rz", "reference"])
     ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--persistent", action="store_true",
+                    help="run the decode step as the persistent kernel instead of the launch sequence")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--position", type=int, default=1024)
     ap.add_argument("--layers", type=int, default=S.LLAMA_LAYERS,

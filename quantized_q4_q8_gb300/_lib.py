@@ -73,14 +73,18 @@ SIGNATURES = {
     "rz_decode_stack_workspace_bytes": [_LWP, _i32, _i64, _i32],
     "rz_decode_stack": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
                         _sz, _vp],
+    "rz_decode_layers": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
+    "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
     "rz_set_pdl": [C.c_int],
+    "rz_set_persistent": [C.c_int],
     "rz_last_error": [],
     "rz_version": [],
 }
 _RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p,
              "rz_swiglu_ffn_workspace_bytes": _sz, "rz_attention_workspace_bytes": _sz,
-             "rz_decode_layer_workspace_bytes": _sz, "rz_decode_stack_workspace_bytes": _sz}
+             "rz_decode_layer_workspace_bytes": _sz, "rz_decode_stack_workspace_bytes": _sz,
+             "rz_decode_stack_launches": C.c_int32}
 
 _lib = None
 

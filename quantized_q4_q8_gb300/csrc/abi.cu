@@ -236,7 +236,7 @@ rz_status rz_check_device_error(rz_stream stream, uint32_t *code_out)
     RZ_CUDA(cudaMemcpyToSymbolAsync(g_dev_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s),
             "clear device error word");
     RZ_CUDA(cudaStreamSynchronize(s), "synchronize");
-    if ((code & 0xf00u) == 0x100u)
+    if ((code & 0xf00u) == 0x100u || (code & 0xf00u) == 0x300u)
         return fail(RZ_ERR_TIMEOUT, "device error 0x%x: a bounded wait ran out", code);
     return fail(RZ_ERR_DEVICE, "device error 0x%x: a device-side range check failed", code);
 }
@@ -245,6 +245,13 @@ rz_status rz_set_pdl(int enable)
 {
     t_last_error.clear();
     g_use_pdl = enable != 0;
+    return RZ_OK;
+}
+
+rz_status rz_set_persistent(int enable)
+{
+    t_last_error.clear();
+    g_use_persistent = enable != 0;
     return RZ_OK;
 }
 
@@ -451,23 +458,16 @@ size_t rz_decode_stack_workspace_bytes(const rz_layer_weights *layers, int32_t n
     return stack_workspace_bytes(L, m, max_seq);
 }
 
-rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
-                          int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
-                          const float *out_gamma, const void *lm_head, int64_t vocab, float *hidden_out,
-                          float *logits, void *workspace, size_t ws_bytes, rz_stream stream)
+// Checks shared by rz_decode_stack and rz_decode_layers.
+static rz_status check_stack(const char *fn, const float *input, const rz_layer_weights *layers,
+                             const rz_kv_cache *kvs, int32_t n_layers, const int32_t *positions, int32_t position,
+                             int64_t m, std::vector<LayerDesc> &Ls, std::vector<KvDesc> &Ks)
 {
-    const char *fn = "rz_decode_stack";
-    t_last_error.clear();
-    if (!input || !layers || !kvs || !out_gamma || !lm_head || !logits)
-        return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!input || !layers || !kvs) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (n_layers < 1 || n_layers > 4096) return fail(RZ_ERR_INVALID_ARG, "%s: n_layers=%d", fn, n_layers);
-    if (vocab < 1) return fail(RZ_ERR_INVALID_ARG, "%s: vocab", fn);
-    const void *ptrs[] = {input, out_gamma, lm_head, logits};
-    for (const void *p : ptrs)
-        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
-    if (hidden_out && !aligned16(hidden_out)) return fail(RZ_ERR_ALIGN, "%s: hidden_out alignment", fn);
-    std::vector<LayerDesc> Ls((size_t)n_layers);
-    std::vector<KvDesc> Ks((size_t)n_layers);
+    if (!aligned16(input)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
+    Ls.resize((size_t)n_layers);
+    Ks.resize((size_t)n_layers);
     for (int l = 0; l < n_layers; ++l) {
         RZ_TRY(check_layer(&layers[l], fn, m, &Ls[l]));
         RZ_TRY(check_kv(&kvs[l], fn, m, Ls[l].n_kv_heads * Ls[l].head_dim, &Ks[l]));
@@ -476,14 +476,61 @@ rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, co
             Ls[l].n_kv_heads != Ls[0].n_kv_heads || Ls[l].head_dim != Ls[0].head_dim || Ls[l].inter != Ls[0].inter)
             return fail(RZ_ERR_SHAPE, "%s: layer %d differs in shape from layer 0", fn, l);
     }
-    if (Ls[0].hidden % 32) return fail(RZ_ERR_SHAPE, "%s: hidden %% 32 != 0 (Q4_0 LM head blocks)", fn);
     RZ_TRY(check_position(positions, position, Ks[0].max_seq, fn));
-    RZ_TRY(check_device());
+    return check_device();
+}
+
+rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
+                          int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
+                          const float *out_gamma, const void *lm_head, int64_t vocab, float *hidden_out,
+                          float *logits, void *workspace, size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_decode_stack";
+    t_last_error.clear();
+    if (!out_gamma || !lm_head || !logits) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (vocab < 1) return fail(RZ_ERR_INVALID_ARG, "%s: vocab", fn);
+    const void *ptrs[] = {out_gamma, lm_head, logits};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
+    if (hidden_out && !aligned16(hidden_out)) return fail(RZ_ERR_ALIGN, "%s: hidden_out alignment", fn);
+    std::vector<LayerDesc> Ls;
+    std::vector<KvDesc> Ks;
+    RZ_TRY(check_stack(fn, input, layers, kvs, n_layers, positions, position, m, Ls, Ks));
+    if (Ls[0].hidden % 32) return fail(RZ_ERR_SHAPE, "%s: hidden %% 32 != 0 (Q4_0 LM head blocks)", fn);
     RZ_TRY(check_ws(workspace, ws_bytes, stack_workspace_bytes(Ls[0], m, Ks[0].max_seq), fn));
     RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, out_gamma, lm_head,
                                 vocab, hidden_out, logits, workspace, static_cast<cudaStream_t>(stream)),
             "rz_decode_stack launch");
     return RZ_OK;
+}
+
+rz_status rz_decode_layers(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
+                           int32_t n_layers, const int32_t *positions, int32_t position, int64_t m, float *output,
+                           void *workspace, size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_decode_layers";
+    t_last_error.clear();
+    if (!output) return fail(RZ_ERR_INVALID_ARG, "%s: null output", fn);
+    if (!aligned16(output)) return fail(RZ_ERR_ALIGN, "%s: output alignment", fn);
+    std::vector<LayerDesc> Ls;
+    std::vector<KvDesc> Ks;
+    RZ_TRY(check_stack(fn, input, layers, kvs, n_layers, positions, position, m, Ls, Ks));
+    RZ_TRY(check_ws(workspace, ws_bytes, stack_workspace_bytes(Ls[0], m, Ks[0].max_seq), fn));
+    RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, nullptr, nullptr, 0,
+                                output, nullptr, workspace, static_cast<cudaStream_t>(stream)),
+            "rz_decode_layers launch");
+    return RZ_OK;
+}
+
+int32_t rz_decode_stack_launches(const rz_layer_weights *layers, int32_t n_layers, int64_t m, int32_t max_seq,
+                                 int32_t with_head)
+{
+    if (!layers || n_layers < 1 || n_layers > 4096 || max_seq < 1) return 0;
+    std::vector<LayerDesc> Ls((size_t)n_layers);
+    for (int l = 0; l < n_layers; ++l)
+        if (check_layer(&layers[l], "rz_decode_stack_launches", m, &Ls[l]) != RZ_OK) return 0;
+    if (check_device() != RZ_OK) return 0;
+    return stack_kernel_launches(Ls.data(), n_layers, m, max_seq, with_head != 0);
 }
 
 }  // extern "C"

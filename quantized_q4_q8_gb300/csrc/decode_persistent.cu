@@ -1,0 +1,995 @@
+// decode_persistent.cu -- the decode step of a stack of Q4_K layers (m = 1) as
+// ONE persistent kernel: one CTA per SM for the whole step.
+//
+// Same operations and order as the launch sequence in layer.cu (the layer of
+// transformer_layer_gpu_true_dp4a, realizar 0.8.5 src/cuda/executor/cached.rs):
+// per layer, RMSNorm -> Q8_1 -> fused Q|K|V GEMV; RoPE, KV append and split-
+// sequence attention with the Q8_1 of its output; O GEMV + residual; RMSNorm ->
+// Q8_1 -> gate/up GEMV with silu(gate) * up; Q8_1 of h -> down GEMV + residual.
+//
+// Why one kernel.  A decode step streams every weight byte once, and at batch 1
+// the work per byte is a few integer dot instructions, so the step is bound by
+// HBM -- but only if HBM never idles.  As separate launches each GEMV pays a ramp
+// (CTAs start, compute the activation prologue, fill their pipeline) and a tail
+// (the last CTAs finish alone), and with 9-51 MB per matrix those fixed costs are
+// as long as the transfer itself.  Here the weights never stop flowing: in every
+// CTA a producer warp walks the whole step's list of byte ranges -- the CTA's
+// share of each layer's Q|K|V rows, its attention units' K and V cache rows, its
+// O rows, gate/up rows and down rows, layer after layer -- and keeps a ring of
+// shared-memory slots full with the 1-D bulk copy engine (cp.async.bulk on
+// mbarriers), plus an L2 prefetch window further ahead.  None of those bytes
+// depend on the step's activations (the cache rows read are those of earlier
+// tokens), so the producer never waits for anything but a free slot.  Sixteen
+// consumer warps follow the same list.  Between dependent phases (Q|K|V ->
+// attention -> O -> gate/up -> down -> next layer) the consumers meet at a grid
+// barrier; meanwhile the ring and the L2 window keep filling with the next
+// phase's weights, so the barrier and the activation prologue hide behind HBM
+// traffic instead of adding to it.
+//
+// Grid barriers need every CTA resident: the kernel is launched cooperatively
+// (the launch fails rather than run with CTAs missing).  Every wait is bounded
+// and also gives up as soon as any CTA has recorded an error, so a failure
+// ends the kernel with an error code instead of hanging the GPU.
+//
+// Attention runs one warp per unit (token, kv head, chunk of CL cache rows);
+// the unit's K and V rows arrive in one ring slot.  The warp rotates the query
+// heads of its kv head with a per-CTA RoPE table, scores the chunk, applies the
+// chunk softmax and the weighted values, and leaves a partial record; the last
+// warp to finish a (token, kv head) -- an atomic counter, no spinning -- merges
+// the chunks (log-sum-exp rule) and writes the Q8_1 of the merged heads.  The
+// warp whose chunk holds the token's own row rotates k, appends k and v to the
+// cache and uses them from registers.  Lane l holds elements 32 e + l of a head.
+#include <math.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "q4k_dot.cuh"
+#include "rz_common.cuh"
+#include "rz_kernels.h"
+
+namespace rz {
+
+bool g_use_persistent = false;
+
+namespace {
+
+constexpr int kPWarps = kRowWarps;             // consumer warps
+constexpr int kPThreads = (kPWarps + 1) * 32;  // + the producer warp
+constexpr int kPMaxLayers = 32;                // layers per launch (kernel parameter space)
+constexpr int kMaxSlots = 32;
+constexpr int kAttnUnitBytes = 16384;          // K rows + V rows of one attention unit
+constexpr int kMaxG = 8;                       // query heads per kv head
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+enum Kind { K_QKV = 0, K_O = 1, K_GU = 2, K_DN = 3, K_ATT = 4 };
+constexpr int kPhases = 5;
+__device__ __forceinline__ int phase_kind(int p)
+{
+    return p == 0 ? K_QKV : p == 1 ? K_ATT : p == 2 ? K_O : p == 3 ? K_GU : K_DN;
+}
+
+struct PLayer {
+    const uint8_t *w[7];  // q, k, v, o, gate, up, down
+    const float *attn_gamma, *ffn_gamma;
+    float *kc, *vc;
+};
+
+struct PArgs {
+    PLayer L[kPMaxLayers];
+    int n_layers, m;
+    int hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter, group, q_dim, q_pad, kv_dim;
+    float eps, rope_theta;
+    int rope_mode;
+    int64_t seq_stride;
+    int max_seq;
+    const int32_t *positions;
+    int position;
+    int chunk_len, n_chunks;  // attention rows per unit; chunks covering max_seq
+    int slot_bytes, n_slots, pf_stages;
+    int x_region;
+    int ps[4];  // packs per stage of each GEMV kind
+    const float *input;
+    float *output;
+    float *xbuf[2];
+    float *qkv, *part, *res1, *h;
+    int8_t *a8;
+    int *counters;
+    unsigned *gbar;
+    unsigned *err;
+};
+
+// ---------------------------------------------------------------- per-CTA plan
+struct GemvShape {
+    int64_t units, in_dim, row_bytes;
+    int nsb, R, rpp, ps;
+};
+
+__host__ __device__ inline void gemv_dims(int kind, int q_dim, int kv_dim, int hidden, int hidden_pad, int q_pad,
+                                          int inter, int64_t &units, int64_t &in_dim, int &R)
+{
+    R = 1;
+    if (kind == K_QKV) {
+        units = q_dim + 2 * (int64_t)kv_dim;
+        in_dim = hidden_pad;
+    } else if (kind == K_O) {
+        units = hidden;
+        in_dim = q_pad;
+    } else if (kind == K_GU) {
+        units = inter;
+        in_dim = hidden_pad;
+        R = 2;
+    } else {
+        units = hidden;
+        in_dim = inter;
+    }
+}
+
+__device__ __forceinline__ GemvShape gemv_shape(const PArgs &a, int kind)
+{
+    GemvShape g;
+    gemv_dims(kind, a.q_dim, a.kv_dim, a.hidden, a.hidden_pad, a.q_pad, a.inter, g.units, g.in_dim, g.R);
+    g.nsb = (int)(g.in_dim / 256);
+    g.row_bytes = (int64_t)g.nsb * kSB;
+    g.rpp = pack_rows_for(g.nsb);
+    g.ps = a.ps[kind];
+    return g;
+}
+
+struct Plan {
+    int64_t r0[4], r1[4];    // this CTA's rows of each GEMV kind
+    int64_t nst[kPhases];    // stages of each kind (indexed by Kind)
+    int64_t au0, au1;        // this CTA's attention units
+    int pos[4];              // positions of the tokens (m <= 4)
+    int nc[4];               // chunks of each token
+};
+
+__device__ __forceinline__ int token_pos(const PArgs &a, int t)
+{
+    return a.positions ? a.positions[t] : a.position;
+}
+
+__device__ __forceinline__ bool pos_valid(const PArgs &a, int p) { return p >= 0 && p < a.max_seq; }
+
+__device__ __forceinline__ void make_plan(const PArgs &a, Plan &p)
+{
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    for (int k = 0; k < 4; ++k) {
+        const GemvShape g = gemv_shape(a, k);
+        p.r0[k] = g.units * b / G;
+        p.r1[k] = g.units * (b + 1) / G;
+        const int64_t npacks = (p.r1[k] - p.r0[k] + g.rpp - 1) / g.rpp;
+        p.nst[k] = (npacks + g.ps - 1) / g.ps;
+    }
+    int64_t U = 0;
+    for (int t = 0; t < a.m; ++t) {
+        p.pos[t] = token_pos(a, t);
+        p.nc[t] = pos_valid(a, p.pos[t]) ? min(a.n_chunks, p.pos[t] / a.chunk_len + 1) : 1;
+        U += (int64_t)a.n_kv_heads * p.nc[t];
+    }
+    p.au0 = U * b / G;
+    p.au1 = U * (b + 1) / G;
+    p.nst[K_ATT] = p.au1 - p.au0;
+}
+
+// attention unit u -> (token, kv head, chunk)
+__device__ __forceinline__ void unit_coords(const PArgs &a, const Plan &p, int64_t u, int &t, int &kvh, int &chunk)
+{
+    t = 0;
+    while (t + 1 < a.m && u >= (int64_t)a.n_kv_heads * p.nc[t]) {
+        u -= (int64_t)a.n_kv_heads * p.nc[t];
+        ++t;
+    }
+    kvh = (int)(u / p.nc[t]);
+    chunk = (int)(u % p.nc[t]);
+}
+
+__device__ __forceinline__ int unit_rows(const PArgs &a, const Plan &p, int t, int chunk)
+{
+    const int pos = p.pos[t];
+    if (!pos_valid(a, pos)) return 0;
+    return max(0, min(a.chunk_len, pos + 1 - chunk * a.chunk_len));
+}
+
+__device__ __forceinline__ const uint8_t *seg_weight(const PArgs &a, int l, int kind, int seg)
+{
+    const PLayer &L = a.L[l];
+    switch (kind) {
+    case K_QKV: return L.w[seg];
+    case K_O: return L.w[3];
+    case K_GU: return L.w[4 + seg];
+    default: return L.w[6];
+    }
+}
+
+// Q|K|V: rows [0, q_dim) of wq, then wk, then wv; every other kind has one matrix.
+__device__ __forceinline__ int qkv_seg(const PArgs &a, int64_t unit, int64_t &local)
+{
+    if (unit < a.q_dim) {
+        local = unit;
+        return 0;
+    }
+    if (unit < a.q_dim + a.kv_dim) {
+        local = unit - a.q_dim;
+        return 1;
+    }
+    local = unit - a.q_dim - a.kv_dim;
+    return 2;
+}
+
+// Every byte range of stage k of phase `kind` of layer l for this CTA:
+// f(piece index, dst offset in the slot, source, bytes).  Returns the bytes of
+// the stage.
+template <typename F>
+__device__ __forceinline__ unsigned stage_ranges(const PArgs &a, const Plan &p, int l, int kind, int64_t k, F f)
+{
+    if (kind == K_ATT) {
+        int t, kvh, chunk;
+        unit_coords(a, p, p.au0 + k, t, kvh, chunk);
+        const int n = unit_rows(a, p, t, chunk);
+        const unsigned rb = (unsigned)a.head_dim * 4u;
+        const int64_t base = (int64_t)t * a.seq_stride + (int64_t)chunk * a.chunk_len * a.kv_dim +
+                             (int64_t)kvh * a.head_dim;
+        for (int j = 0; j < n; ++j) {
+            f(2 * j, (unsigned)j * rb, a.L[l].kc + base + (int64_t)j * a.kv_dim, rb);
+            f(2 * j + 1, (unsigned)(a.chunk_len + j) * rb, a.L[l].vc + base + (int64_t)j * a.kv_dim, rb);
+        }
+        return 2u * (unsigned)n * rb;
+    }
+    const GemvShape g = gemv_shape(a, kind);
+    const int64_t u0 = p.r0[kind] + k * g.ps * g.rpp;
+    const int n = (int)min((int64_t)g.ps * g.rpp, p.r1[kind] - u0);  // rows in this stage
+    const int64_t pack_bytes = (int64_t)g.rpp * g.row_bytes;
+    if (g.R == 2) {
+        for (int q = 0; q * g.rpp < n; ++q) {
+            const int nr = min(g.rpp, n - q * g.rpp);
+            const int64_t u = u0 + (int64_t)q * g.rpp;
+            f(2 * q, (unsigned)(q * 2 * pack_bytes), seg_weight(a, l, kind, 0) + u * g.row_bytes,
+              (unsigned)(nr * g.row_bytes));
+            f(2 * q + 1, (unsigned)(q * 2 * pack_bytes + pack_bytes), seg_weight(a, l, kind, 1) + u * g.row_bytes,
+              (unsigned)(nr * g.row_bytes));
+        }
+    } else if (kind == K_QKV) {
+        int r = 0, piece = 0;
+        while (r < n) {
+            int64_t local;
+            const int seg = qkv_seg(a, u0 + r, local);
+            const int64_t seg_end = seg == 0 ? a.q_dim : a.kv_dim;
+            const int run = (int)min((int64_t)(n - r), seg_end - local);
+            f(piece++, (unsigned)(r * g.row_bytes), seg_weight(a, l, kind, seg) + local * g.row_bytes,
+              (unsigned)(run * g.row_bytes));
+            r += run;
+        }
+    } else {
+        f(0, 0u, seg_weight(a, l, kind, 0) + u0 * g.row_bytes, (unsigned)(n * g.row_bytes));
+    }
+    return (unsigned)(g.R * n * g.row_bytes);
+}
+
+// Position in the step's list of stages (layer, phase, stage of the phase).
+struct StageIter {
+    int l, ph;
+    int64_t k;
+};
+
+__device__ __forceinline__ void iter_skip_empty(const PArgs &a, const Plan &p, StageIter &it)
+{
+    while (it.l < a.n_layers && it.k >= p.nst[phase_kind(it.ph)]) {
+        it.k = 0;
+        if (++it.ph == kPhases) {
+            it.ph = 0;
+            ++it.l;
+        }
+    }
+}
+
+__device__ __forceinline__ void iter_next(const PArgs &a, const Plan &p, StageIter &it)
+{
+    ++it.k;
+    iter_skip_empty(a, p, it);
+}
+
+// ---------------------------------------------------------------- producer
+// The whole producer warp walks the list; lane 0 waits for free slots and arms
+// the full barrier, and the byte ranges of a stage are spread over the lanes
+// (an attention unit is 2 x CL cache rows, one copy each).  A copy may land
+// before the barrier is armed: the transaction count goes negative and the
+// phase still cannot complete before lane 0's arrival.
+__device__ void producer(const PArgs &a, const Plan &p, uint8_t *ring, uint64_t *full, uint64_t *empty, int lane)
+{
+    const int NS = a.n_slots;
+    StageIter it{0, 0, 0}, pf{0, 0, 0};
+    iter_skip_empty(a, p, it);
+    iter_skip_empty(a, p, pf);
+    int64_t P = 0;  // stage index of the prefetch cursor
+    // the first NS stages are copied at once: the prefetch window starts after them
+    while (P < NS && pf.l < a.n_layers) {
+        iter_next(a, p, pf);
+        ++P;
+    }
+    int64_t K = 0;
+    bool ok = true;
+    for (; it.l < a.n_layers; iter_next(a, p, it), ++K) {
+        // L2 prefetch window: stages [K + NS, K + NS + pf_stages)
+        while (pf.l < a.n_layers && P < K + NS + a.pf_stages) {
+            stage_ranges(a, p, pf.l, phase_kind(pf.ph), pf.k, [&](int i, unsigned, const void *src, unsigned bytes) {
+                if ((i & 31) == lane) prefetch_l2(src, bytes);
+            });
+            iter_next(a, p, pf);
+            ++P;
+        }
+        const int s = (int)(K % NS);
+        if (K >= NS) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait_abortable(&empty[s], (unsigned)(((K / NS) - 1) & 1),
+                                                                         a.err, DEV_TIMEOUT_STEP));
+            if (!got) {
+                ok = false;
+                break;
+            }
+        }
+        uint8_t *dst = ring + (int64_t)s * a.slot_bytes;
+        const int kind = phase_kind(it.ph);
+        if (lane == 0) {
+            const unsigned bytes = stage_ranges(a, p, it.l, kind, it.k, [](int, unsigned, const void *, unsigned) {});
+            mbar_arrive_expect_tx(&full[s], bytes);
+        }
+        stage_ranges(a, p, it.l, kind, it.k, [&](int i, unsigned off, const void *src, unsigned nbytes) {
+            if ((i & 31) == lane) bulk_g2s(dst + off, src, nbytes, &full[s]);
+        });
+    }
+    // stages issued but perhaps not landed must land before the CTA exits
+    if (!ok && lane == 0) {
+        for (int64_t q = (K > NS ? K - NS : 0); q < K; ++q)
+            if (!mbar_wait(&full[q % NS], (unsigned)((q / NS) & 1))) set_error(a.err, DEV_TIMEOUT_DRAIN);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------- consumers
+struct CCtx {
+    const PArgs *a;
+    const Plan *p;
+    uint32_t ring_s;
+    uint64_t *full, *empty;
+    uint8_t *xsm;
+    float *red;
+    const float *rope;  // [m][head_dim / 2][2] cos, sin
+    int warp, lane, tid;
+};
+
+__device__ __forceinline__ void csync()
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(kPWarps * 32) : "memory");
+}
+
+// All consumer warps of every CTA: after it, every global write made by any CTA
+// before it is visible.  `idx`: barriers passed so far in this launch.
+__device__ __forceinline__ void grid_barrier(const CCtx &c, unsigned idx)
+{
+    csync();
+    if (c.warp == 0) {
+        if (c.lane == 0) {
+            unsigned *ctr = c.a->gbar;
+            const unsigned target = gridDim.x * (idx + 1);
+            __threadfence();
+            atomicAdd(ctr, 1u);
+            bool done = false;
+            for (uint32_t i = 0; i < kWaitLimit; ++i) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+                if (v >= target) {
+                    done = true;
+                    break;
+                }
+                if ((i & 15u) == 15u && *reinterpret_cast<volatile unsigned *>(c.a->err) != 0u) break;
+                __nanosleep(64);
+            }
+            if (!done && *reinterpret_cast<volatile unsigned *>(c.a->err) == 0u) set_error(c.a->err, DEV_TIMEOUT_GRID);
+            __threadfence();
+        }
+        __syncwarp();
+    }
+    csync();
+}
+
+// One GEMV phase: the CTA's packs, warp w taking packs w, w + 16, ...
+template <int MT, int EPI, int R>
+__device__ __forceinline__ void gemv_phase(const CCtx &c, int l, int kind, int64_t K0, const float *res,
+                                           float *y)
+{
+    const PArgs &a = *c.a;
+    const Plan &p = *c.p;
+    const GemvShape g = gemv_shape(a, kind);
+    const int64_t r0 = p.r0[kind], r1 = p.r1[kind];
+    const int64_t npacks = (r1 - r0 + g.rpp - 1) / g.rpp;
+    const uint32_t pack_bytes = (uint32_t)(g.rpp * g.row_bytes);
+    XSrc x;
+    x.in_dim = g.in_dim;
+    x.nb = g.in_dim / 32;
+    x.m = a.m;
+    x.q = smem_u32(c.xsm);
+    x.ds = smem_u32(c.xsm + (int64_t)a.m * (g.in_dim / 256) * kXSlot);
+    x.gq = nullptr;
+    x.gd = x.gs = nullptr;
+    const int gl = c.lane >> 2;
+    const int seg_lanes = (g.rpp > 1) ? 4 * g.nsb : 32;
+    const int rip = (g.rpp > 1) ? gl / g.nsb : 0;
+    const int leader = c.lane % seg_lanes == 0;
+    int64_t ldy = a.hidden_pad, ldr = a.hidden_pad;
+    if (kind == K_QKV) ldy = a.q_dim + 2 * (int64_t)a.kv_dim;
+    if (kind == K_GU) ldy = a.inter;
+
+    // Every warp passes every stage of the phase in order (waits for it, takes its
+    // own packs in it, releases it), so no warp can run a ring length ahead of a
+    // stage that is not filled yet: the parity waits stay unambiguous.
+    const int64_t nst = p.nst[kind];
+    for (int64_t k = 0; k < nst; ++k) {
+        const int64_t K = K0 + k;
+        const int s = (int)(K % a.n_slots);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], (unsigned)((K / a.n_slots) & 1),
+                                                                    a.err, DEV_TIMEOUT_STEP));
+        if (!ok) continue;
+        const int64_t first = k * g.ps, end = min(first + g.ps, npacks);
+        for (int64_t i = first + ((c.warp - first % kPWarps) + kPWarps) % kPWarps; i < end; i += kPWarps) {
+            const int64_t pack0 = r0 + i * g.rpp;
+            const int pack_rows = (int)min((int64_t)g.rpp, r1 - pack0);
+            const uint32_t pk = c.ring_s + (uint32_t)(s * a.slot_bytes) + (uint32_t)(i % g.ps) * R * pack_bytes;
+            float acc[2][MT];
+            pack_accumulate<MT, R, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
+            if (rip < pack_rows) {
+                const int64_t unit = pack0 + rip;
+                int64_t lr = unit;
+                float *yk = y;
+                if (kind == K_QKV) {
+                    const int seg = qkv_seg(a, unit, lr);
+                    yk = y + (seg == 0 ? 0 : seg == 1 ? a.q_dim : a.q_dim + a.kv_dim);
+                }
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t < a.m && ((seg_lanes == 32) ? c.lane == (t & 31) : leader)) {
+                        float out = acc[0][t];
+                        if (EPI == EPI_RESID) out = __ldcg(res + t * ldr + lr) + out;
+                        if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
+                        yk[t * ldy + lr] = out;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(&c.empty[s]);  // this warp is done with the slot
+    }
+}
+
+// RoPE of one head held lane-strided (v[e] = element 32 e + lane) with the
+// token's table.  Mode 0 pairs (2i, 2i + 1): partner in lane ^ 1, same e.
+// Mode 1 pairs (i, i + hd/2): partner in the same lane, e +- CPT/2.
+template <int CPT>
+__device__ __forceinline__ void rope_lanes(float (&v)[CPT], const float *tab, int mode, int lane)
+{
+    if (mode == 0) {
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) {
+            const int d = 32 * e + lane;
+            const float cs = tab[2 * (d >> 1)], sn = tab[2 * (d >> 1) + 1];
+            const float other = __shfl_xor_sync(0xffffffffu, v[e], 1);
+            v[e] = (lane & 1) ? other * sn + v[e] * cs : v[e] * cs - other * sn;
+        }
+    } else {
+        constexpr int H = CPT / 2;
+#pragma unroll
+        for (int e = 0; e < H; ++e) {
+            const int i = 32 * e + lane;
+            const float cs = tab[2 * i], sn = tab[2 * i + 1];
+            const float x0 = v[e], x1 = v[e + H];
+            v[e] = x0 * cs - x1 * sn;
+            v[e + H] = x0 * sn + x1 * cs;
+        }
+    }
+}
+
+// Partial record of one chunk for one query head: [max, sum, o[head_dim]]
+__device__ __forceinline__ float *part_rec(const PArgs &a, int t, int kvh, int chunk, int g)
+{
+    const int64_t idx = (((int64_t)t * a.n_kv_heads + kvh) * a.n_chunks + chunk) * a.group + g;
+    return a.part + idx * (a.head_dim + 2);
+}
+
+// Merge the chunks of (t, kvh) and write the Q8_1 of its query heads.
+template <int CPT>
+__device__ __forceinline__ void attn_merge(const PArgs &a, int t, int kvh, int nc, int lane)
+{
+    const int hd = a.head_dim;
+    int8_t *q = a.a8;
+    float *qd = reinterpret_cast<float *>(q + (int64_t)a.m * a.q_pad);
+    float *qsum = qd + (int64_t)a.m * (a.q_pad / 32);
+    for (int g = 0; g < a.group; ++g) {
+        const float *r0 = part_rec(a, t, kvh, 0, g);
+        const int64_t cstride = (int64_t)a.group * (hd + 2);
+        float M = -INFINITY;
+        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(r0 + c * cstride));
+        M = warp_max(M);
+        float L = 0.0f;
+        for (int c = lane; c < nc; c += 32) {
+            const float mc = __ldcg(r0 + c * cstride), lc = __ldcg(r0 + c * cstride + 1);
+            L += (lc > 0.0f) ? expf(mc - M) * lc : 0.0f;
+        }
+        L = warp_sum(L);
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;  // 0 only after a bad position
+        float o[CPT];
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
+#pragma unroll 4
+        for (int c = 0; c < nc; ++c) {
+            const float *rc = r0 + c * cstride;
+            const float mc = __ldcg(rc), lc = __ldcg(rc + 1);
+            const float w = (lc > 0.0f) ? expf(mc - M) : 0.0f;
+            if (w != 0.0f) {
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) o[e] = fmaf(__ldcg(rc + 2 + 32 * e + lane), w, o[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) {
+            const float v = o[e] * inv;
+            const float amax = warp_max(fabsf(v));
+            const float dq = __fdiv_rn(amax, 127.0f);
+            const int qi = q8_code(v, dq);
+            const int sum = warp_sum_int(qi);
+            const int64_t blk = ((int64_t)(kvh * a.group + g) * hd) / 32 + e;
+            q[(int64_t)t * a.q_pad + blk * 32 + lane] = (int8_t)qi;
+            if (lane == 0) {
+                qd[(int64_t)t * (a.q_pad / 32) + blk] = dq;
+                qsum[(int64_t)t * (a.q_pad / 32) + blk] = __fmul_rn(dq, (float)sum);
+            }
+        }
+    }
+}
+
+template <int CPT, int GM>
+__device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0)
+{
+    const PArgs &a = *c.a;
+    const Plan &p = *c.p;
+    const int hd = a.head_dim, G = a.group, lane = c.lane;
+    const int64_t ld_qkv = a.q_dim + 2 * (int64_t)a.kv_dim;
+    const float scale = 1.0f / sqrtf((float)hd);
+    // Q8_1 padding columns q_dim .. q_pad of the attention output are zero
+    if (blockIdx.x == 0 && c.warp == 0 && a.q_pad > a.q_dim) {
+        float *qd = reinterpret_cast<float *>(a.a8 + (int64_t)a.m * a.q_pad);
+        float *qsum = qd + (int64_t)a.m * (a.q_pad / 32);
+        for (int t = 0; t < a.m; ++t) {
+            for (int i = a.q_dim + lane; i < a.q_pad; i += 32) a.a8[(int64_t)t * a.q_pad + i] = 0;
+            for (int b = a.q_dim / 32 + lane; b < a.q_pad / 32; b += 32) {
+                qd[(int64_t)t * (a.q_pad / 32) + b] = 0.0f;
+                qsum[(int64_t)t * (a.q_pad / 32) + b] = 0.0f;
+            }
+        }
+    }
+    const int64_t nunits = p.au1 - p.au0;
+    // every warp passes every unit's stage in order; unit i is worked by warp i % 16
+    for (int64_t i = 0; i < nunits; ++i) {
+        const int64_t K = K0 + i;
+        const int s = (int)(K % a.n_slots);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], (unsigned)((K / a.n_slots) & 1),
+                                                                    a.err, DEV_TIMEOUT_STEP));
+        if (!ok) continue;
+        if (i % kPWarps != c.warp) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.empty[s]);
+            continue;
+        }
+        int t, kvh, chunk;
+        unit_coords(a, p, p.au0 + i, t, kvh, chunk);
+        const int pos = p.pos[t];
+        const bool pos_ok = pos_valid(a, pos);
+        const int n = unit_rows(a, p, t, chunk);
+        const int c0 = chunk * a.chunk_len;
+        const bool own = pos_ok && pos >= c0 && pos < c0 + a.chunk_len;
+        if (!pos_ok && chunk == 0 && kvh == 0 && lane == 0) set_error(a.err, DEV_BAD_POSITION);
+        const float *tab = c.rope + (int64_t)t * hd;  // hd / 2 pairs of (cos, sin)
+
+        // rotated query heads of this kv head
+        float qv[GM][CPT];
+        const float *qrow = a.qkv + (int64_t)t * ld_qkv + (int64_t)kvh * G * hd;
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            if (g < G) {
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) qv[g][e] = __ldcg(qrow + g * hd + 32 * e + lane);
+                rope_lanes<CPT>(qv[g], tab, a.rope_mode, lane);
+            }
+        }
+        // the token's own k (rotated) and v, appended to the cache
+        float kn[CPT], vn[CPT];
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) kn[e] = vn[e] = 0.0f;
+        if (own) {
+            const float *kr = a.qkv + (int64_t)t * ld_qkv + a.q_dim + (int64_t)kvh * hd;
+            const float *vr = kr + a.kv_dim;
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                kn[e] = __ldcg(kr + 32 * e + lane);
+                vn[e] = __ldcg(vr + 32 * e + lane);
+            }
+            rope_lanes<CPT>(kn, tab, a.rope_mode, lane);
+            const int64_t row = (int64_t)t * a.seq_stride + (int64_t)pos * a.kv_dim + (int64_t)kvh * hd;
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                a.L[l].kc[row + 32 * e + lane] = kn[e];
+                a.L[l].vc[row + 32 * e + lane] = vn[e];
+            }
+        }
+        // scores: lane j keeps row j's score of each head
+        const uint32_t ks = c.ring_s + (uint32_t)(s * a.slot_bytes);
+        const uint32_t vs = ks + (uint32_t)(a.chunk_len * hd * 4);
+        float sc[GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g) sc[g] = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            float kj[CPT];
+            const bool mine = (c0 + j == pos);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                float v;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(ks + (uint32_t)((j * hd + 32 * e + lane) * 4)));
+                kj[e] = mine ? kn[e] : v;
+            }
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                if (g < G) {
+                    float dot = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) dot = fmaf(qv[g][e], kj[e], dot);
+                    dot = warp_sum(dot);
+                    if (lane == j) sc[g] = dot * scale;
+                }
+            }
+        }
+        // chunk softmax per head
+        float pr[GM], mx[GM], sm[GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            if (g < G) {
+                mx[g] = warp_max(sc[g]);
+                pr[g] = lane < n ? expf(sc[g] - mx[g]) : 0.0f;
+                sm[g] = warp_sum(pr[g]);
+            }
+        }
+        // weighted values
+        float o[GM][CPT];
+#pragma unroll
+        for (int g = 0; g < GM; ++g)
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) o[g][e] = 0.0f;
+        for (int j = 0; j < n; ++j) {
+            float vj[CPT];
+            const bool mine = (c0 + j == pos);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                float v;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(vs + (uint32_t)((j * hd + 32 * e + lane) * 4)));
+                vj[e] = mine ? vn[e] : v;
+            }
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                if (g < G) {
+                    const float pj = __shfl_sync(0xffffffffu, pr[g], j);
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) o[g][e] = fmaf(pj, vj[e], o[g][e]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.empty[s]);  // this warp is done with the slot
+        // partial records
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            if (g < G) {
+                float *rec = part_rec(a, t, kvh, chunk, g);
+                if (lane == 0) {
+                    rec[0] = n > 0 ? mx[g] : -INFINITY;
+                    rec[1] = n > 0 ? sm[g] : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) rec[2 + 32 * e + lane] = o[g][e];
+            }
+        }
+        // arrive; the last chunk of (t, kvh) merges
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
+            const int prev = atomicAdd(cnt, 1);
+            last = (prev == p.nc[t] - 1);
+            if (last) *cnt = 0;  // ready for the next layer
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence();
+            attn_merge<CPT>(a, t, kvh, p.nc[t], lane);
+        }
+    }
+}
+
+template <int CPT, int GM>
+__global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const __grid_constant__ PArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    uint8_t *xsm = smem + (int64_t)a.n_slots * a.slot_bytes;
+    float *rope = reinterpret_cast<float *>(xsm + a.x_region);
+    float *red = rope + a.m * a.head_dim;
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + 32);
+    uint64_t *empty = full + a.n_slots;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    Plan p;
+    make_plan(a, p);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.n_slots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kPWarps);  // every consumer warp releases every stage
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kPWarps) {
+        producer(a, p, ring, full, empty, lane);
+    } else {
+        // RoPE table of every token: angle reduced modulo 2 pi in double precision
+        const int half = a.head_dim / 2;
+        const double l2t = log2((double)a.rope_theta);
+        for (int idx = threadIdx.x; idx < a.m * half; idx += kPWarps * 32) {
+            const int t = idx / half, i = idx % half;
+            const int pos = pos_valid(a, p.pos[t]) ? p.pos[t] : 0;
+            const double inv_freq = exp2(-(2.0 * i / a.head_dim) * l2t);
+            const double ang = (double)pos * inv_freq;
+            const double rd = ang - kTwoPi * rint(ang / kTwoPi);
+            float sn, cs;
+            sincosf((float)rd, &sn, &cs);
+            rope[(t * half + i) * 2] = cs;
+            rope[(t * half + i) * 2 + 1] = sn;
+        }
+        CCtx c;
+        c.a = &a;
+        c.p = &p;
+        c.ring_s = smem_u32(ring);
+        c.full = full;
+        c.empty = empty;
+        c.xsm = xsm;
+        c.red = red;
+        c.rope = rope;
+        c.warp = warp;
+        c.lane = lane;
+        c.tid = threadIdx.x;
+        csync();
+
+        unsigned nbar = 0;
+        int64_t K = 0;
+        auto sync = [] { csync(); };
+        for (int l = 0; l < a.n_layers; ++l) {
+            const PLayer &L = a.L[l];
+            const float *x_in = l == 0 ? a.input : a.xbuf[(l - 1) & 1];
+            float *x_out = l == a.n_layers - 1 ? a.output : a.xbuf[l & 1];
+            // 1-3: RMSNorm -> Q8_1 -> Q|K|V
+            stage_x_f32<true, true>(xsm, x_in, a.hidden_pad, L.attn_gamma, a.hidden, a.eps, a.m, a.hidden_pad, red,
+                                    warp, lane, sync);
+            gemv_phase<1, EPI_STORE, 1>(c, l, K_QKV, K, nullptr, a.qkv);
+            K += p.nst[K_QKV];
+            grid_barrier(c, nbar++);
+            // 4-5: attention, Q8_1 of its output
+            attention_phase<CPT, GM>(c, l, K);
+            K += p.nst[K_ATT];
+            grid_barrier(c, nbar++);
+            // 6-7: O + residual
+            stage_x_q8<true>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + (int64_t)a.m * a.q_pad), a.m,
+                             a.q_pad, threadIdx.x, sync);
+            gemv_phase<1, EPI_RESID, 1>(c, l, K_O, K, x_in, a.res1);
+            K += p.nst[K_O];
+            grid_barrier(c, nbar++);
+            // 8-9: RMSNorm -> Q8_1 -> gate/up, silu(gate) * up
+            stage_x_f32<true, true>(xsm, a.res1, a.hidden_pad, L.ffn_gamma, a.hidden, a.eps, a.m, a.hidden_pad,
+                                    red, warp, lane, sync);
+            gemv_phase<1, EPI_SWIGLU, 2>(c, l, K_GU, K, nullptr, a.h);
+            K += p.nst[K_GU];
+            grid_barrier(c, nbar++);
+            // 9-10: Q8_1 of h -> down + residual
+            stage_x_f32<true, false>(xsm, a.h, a.inter, nullptr, 0, 0.0f, a.m, a.inter, red, warp, lane, sync);
+            gemv_phase<1, EPI_RESID, 1>(c, l, K_DN, K, a.res1, x_out);
+            K += p.nst[K_DN];
+            if (blockIdx.x == 0 && a.hidden_pad > a.hidden) {
+                for (int t = 0; t < a.m; ++t)
+                    for (int i = a.hidden + threadIdx.x; i < a.hidden_pad; i += kPWarps * 32)
+                        x_out[(int64_t)t * a.hidden_pad + i] = 0.0f;
+            }
+            if (l + 1 < a.n_layers) grid_barrier(c, nbar++);
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- host planning
+struct HostPlan {
+    bool ok;
+    int slot_bytes, n_slots, ps[4], x_region, chunk_len, n_chunks;
+    size_t smem;
+};
+
+int env_int(const char *name, int dflt)
+{
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+
+HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin)
+{
+    HostPlan h{};
+    h.ok = false;
+    const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
+    const int q_pad = (q_dim + 255) / 256 * 256;
+    int64_t pack[4];
+    int64_t xr = 0;
+    for (int k = 0; k < 4; ++k) {
+        int64_t units, in_dim;
+        int R;
+        gemv_dims(k, q_dim, kv_dim, L.hidden, L.hidden_pad, q_pad, L.inter, units, in_dim, R);
+        const int nsb = (int)(in_dim / 256);
+        pack[k] = (int64_t)R * pack_rows_for(nsb) * nsb * kSB;
+        xr = std::max(xr, x_smem_bytes(m, in_dim));
+    }
+    h.x_region = (int)((xr + 127) / 128 * 128);
+    h.chunk_len = kAttnUnitBytes / (2 * L.head_dim * 4);
+    h.n_chunks = (max_seq + h.chunk_len - 1) / h.chunk_len;
+    const int64_t fixed = h.x_region + (int64_t)m * L.head_dim * 4 + 32 * 4 + 2 * 8 * kMaxSlots;
+    const int64_t budget = (int64_t)smem_optin - fixed;
+    double best = 0.0;
+    for (int S = kAttnUnitBytes; S <= 32768; S += 128) {
+        const int ns = (int)std::min<int64_t>(kMaxSlots, budget / S);
+        if (ns < 4) continue;
+        double fill = 1.0;
+        bool fits = true;
+        for (int k = 0; k < 4; ++k) {
+            if (pack[k] > S) {
+                fits = false;
+                break;
+            }
+            fill = std::min(fill, (double)(S / pack[k] * pack[k]) / S);
+        }
+        if (!fits) continue;
+        const double score = (double)ns * S * fill;
+        if (score > best) {
+            best = score;
+            h.slot_bytes = S;
+            h.n_slots = ns;
+        }
+    }
+    if (best <= 0.0) return h;
+    for (int k = 0; k < 4; ++k) h.ps[k] = (int)(h.slot_bytes / pack[k]);
+    h.smem = (size_t)h.n_slots * h.slot_bytes + (size_t)fixed;
+    h.ok = h.smem <= smem_optin;
+    return h;
+}
+
+const void *kernel_for(int head_dim, int group)
+{
+    if (head_dim == 128) return group == 1 ? (const void *)decode_persistent_kernel<4, 1>
+                                           : (const void *)decode_persistent_kernel<4, 8>;
+    return (const void *)decode_persistent_kernel<2, 8>;
+}
+
+}  // namespace
+
+int persistent_chunk_len(int head_dim) { return kAttnUnitBytes / (2 * head_dim * 4); }
+
+bool persistent_decode_ok(const LayerDesc &L, int64_t m, int max_seq)
+{
+    if (!g_use_persistent || m != 1) return false;
+    if (L.head_dim != 64 && L.head_dim != 128) return false;
+    if (L.n_heads % L.n_kv_heads != 0 || L.n_heads / L.n_kv_heads > kMaxG) return false;
+    // activation rows walked by the 16-warp row helpers
+    if (L.hidden_pad > 32 * kRowWarps * kRowBlocksPerWarp || L.inter > 32 * kRowWarps * kRowBlocksPerWarp)
+        return false;
+    const DevInfo &d = dev_info();
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, d.device) != cudaSuccess || !coop) return false;
+    return host_plan(L, m, max_seq, d.smem_optin).ok;
+}
+
+cudaError_t launch_decode_persistent(const float *input, const LayerDesc *layers, const KvDesc *kvs, int n_layers,
+                                     const int32_t *positions, int position, int64_t m, float *output,
+                                     const PersistentWs &ws, cudaStream_t s)
+{
+    const LayerDesc &L0 = layers[0];
+    const DevInfo &d = dev_info();
+    const HostPlan hp = host_plan(L0, m, kvs[0].max_seq, d.smem_optin);
+    if (!hp.ok) return cudaErrorInvalidConfiguration;
+    const void *fn = kernel_for(L0.head_dim, L0.n_heads / L0.n_kv_heads);
+    {
+        static std::mutex mu;
+        static bool attr_done[64][3] = {};
+        std::lock_guard<std::mutex> lk(mu);
+        const int which = L0.head_dim == 128 ? (L0.n_heads == L0.n_kv_heads ? 0 : 1) : 2;
+        if (d.device < 64 && !attr_done[d.device][which]) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem_optin);
+            if (e != cudaSuccess) return e;
+            attr_done[d.device][which] = true;
+        }
+    }
+    const int pf_kb = env_int("RZ_L2_PREFETCH_KB", 192);
+    const float *cur = input;
+    for (int g0 = 0; g0 < n_layers; g0 += kPMaxLayers) {
+        const int nl = std::min(kPMaxLayers, n_layers - g0);
+        PArgs a{};
+        for (int i = 0; i < nl; ++i) {
+            const LayerDesc &L = layers[g0 + i];
+            const void *w[7] = {L.wq, L.wk, L.wv, L.wo, L.wgate, L.wup, L.wdown};
+            for (int k = 0; k < 7; ++k) a.L[i].w[k] = static_cast<const uint8_t *>(w[k]);
+            a.L[i].attn_gamma = L.attn_gamma;
+            a.L[i].ffn_gamma = L.ffn_gamma;
+            a.L[i].kc = kvs[g0 + i].k;
+            a.L[i].vc = kvs[g0 + i].v;
+        }
+        a.n_layers = nl;
+        a.m = (int)m;
+        a.hidden = L0.hidden;
+        a.hidden_pad = L0.hidden_pad;
+        a.n_heads = L0.n_heads;
+        a.n_kv_heads = L0.n_kv_heads;
+        a.head_dim = L0.head_dim;
+        a.inter = L0.inter;
+        a.group = L0.n_heads / L0.n_kv_heads;
+        a.q_dim = L0.n_heads * L0.head_dim;
+        a.q_pad = (a.q_dim + 255) / 256 * 256;
+        a.kv_dim = L0.n_kv_heads * L0.head_dim;
+        a.eps = L0.eps;
+        a.rope_theta = L0.rope_theta;
+        a.rope_mode = L0.rope_mode;
+        a.seq_stride = kvs[0].seq_stride;
+        a.max_seq = kvs[0].max_seq;
+        a.positions = positions;
+        a.position = position;
+        a.chunk_len = hp.chunk_len;
+        a.n_chunks = hp.n_chunks;
+        a.slot_bytes = hp.slot_bytes;
+        a.n_slots = hp.n_slots;
+        a.pf_stages = std::max(0, pf_kb * 1024 / hp.slot_bytes);
+        a.x_region = hp.x_region;
+        for (int k = 0; k < 4; ++k) a.ps[k] = hp.ps[k];
+        a.input = cur;
+        const bool last_group = g0 + nl == n_layers;
+        a.output = last_group ? output : ws.gbuf[(g0 / kPMaxLayers) & 1];
+        a.xbuf[0] = ws.xbuf[0];
+        a.xbuf[1] = ws.xbuf[1];
+        a.qkv = ws.qkv;
+        a.part = ws.part;
+        a.res1 = ws.res1;
+        a.h = ws.h;
+        a.a8 = static_cast<int8_t *>(ws.a8);
+        a.counters = ws.counters;
+        a.gbar = ws.gbar;
+        a.err = dev_error_word();
+        // grid-barrier words and merge counters start at zero in every launch
+        cudaError_t e = cudaMemsetAsync(ws.counters, 0, ((size_t)m * L0.n_kv_heads + 2) * sizeof(int), s);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)d.sm_count);
+        cfg.blockDim = dim3(kPThreads);
+        cfg.dynamicSmemBytes = hp.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *args[] = {&a};
+        e = cudaLaunchKernelExC(&cfg, fn, args);
+        if (e != cudaSuccess) return e;
+        cur = a.output;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace rz

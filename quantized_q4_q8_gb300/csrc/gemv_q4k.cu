@@ -13,9 +13,11 @@
 // bytes in flight live in shared memory, not registers, and it prefetches the
 // rest of the CTA's rows into L2 (cp.async.bulk.prefetch.L2) at once.  A stage
 // holds whole "packs" (one row, or 8/nsb rows when a row has fewer than 8
-// super-blocks); sixteen consumer warps take packs round-robin, each waiting only on the stage
-// of its own pack and releasing it with one mbarrier arrival, so warps run ahead
-// of each other across stages and the ring stays full.  Within a pack each
+// super-blocks); pack i goes to consumer warp i % 16.  Every consumer warp
+// passes every stage in order -- waits for it, works its own packs in it,
+// releases the slot with one arrival -- so no warp can get a ring length ahead
+// of a stage that has not been filled (the parity waits stay unambiguous), and
+// a stage is refilled once all sixteen have passed it.  Within a pack each
 // group of 4 lanes takes a super-block (two at a time for independent work) and
 // each lane one 32-byte chunk of its quants (two sub-blocks: low and high
 // nibbles), so every 32-element integer dot completes inside one lane (dp4a of
@@ -29,6 +31,7 @@
 // outstanding copies instead of trapping.
 #include <algorithm>
 
+#include "q4k_dot.cuh"
 #include "rz_common.cuh"
 #include "rz_kernels.h"
 
@@ -37,16 +40,10 @@ namespace {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kSB = 144;
 constexpr int kCtaSmem = 200 * 1024;
 constexpr int kStageTarget = 16 * 1024;
 constexpr int kXSmemMax = 48 * 1024;
 constexpr int kMaxStages = 16;
-
-__host__ __device__ inline int64_t x_smem_bytes(int64_t m, int64_t in_dim)
-{
-    return m * (in_dim / 256) * 288 + 8 * m * (in_dim / 32);
-}
 
 struct Args {
     const uint8_t *w[3];
@@ -86,148 +83,6 @@ __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
     return k;
 }
 
-// Shared-memory copy of the Q8_1 codes.  Super-block sb of token t occupies a
-// 288-byte slot; the 64 bytes that lane chunk c reads (sub-blocks 2c, 2c+1) sit at
-// 64c + 16(c >> 1) inside it.  With this padding the 8 lanes of a shared-memory
-// phase (2 consecutive super-blocks x 4 chunks) hit 8 different bank groups, and
-// every address is a lane constant plus a multiple of the super-block index.
-constexpr int kXSlot = 288;
-
-__device__ __forceinline__ int x_chunk_off(int c) { return 64 * c + 16 * (c >> 1); }
-
-// Per-lane constants of the scale/min decode.  Lane chunk c owns sub-blocks
-// j0 = 2c and j1 = 2c + 1; the two 6-bit scales (and mins) are built for both
-// sub-blocks at once, one per byte, from the 16-bit windows A = s[k], s[k+1],
-// B = s[4+k], s[5+k], C = s[8+k], s[9+k] with k = j0 & 3:
-//   j < 4 : sc = A & 63,                    m = B & 63
-//   j >= 4: sc = (C & 15) | (A >> 6) << 4,  m = (C >> 4) | (B >> 6) << 4
-struct LaneConst {
-    uint32_t sh;       // 8 * k
-    uint32_t mask_lo;  // 0x3f3f for j < 4, else 0
-    uint32_t mask_c;   // 0x0f0f for j >= 4, else 0
-    uint32_t mask_hi;  // 0x3030 for j >= 4, else 0
-};
-
-__device__ __forceinline__ LaneConst lane_const(int c)
-{
-    LaneConst L;
-    L.sh = 8u * (uint32_t)((2 * c) & 3);
-    const bool hi = c >= 2;
-    L.mask_lo = hi ? 0u : 0x3f3fu;
-    L.mask_c = hi ? 0x0f0fu : 0u;
-    L.mask_hi = hi ? 0x3030u : 0u;
-    return L;
-}
-
-struct XSrc {
-    uint32_t q;        // shared-memory byte address of the codes (token 0) (smem copy)
-    uint32_t ds;       // shared-memory byte address of d (token 0); s follows at + m*nb*4
-    const int8_t *gq;  // global copies (when the activations stay in global memory)
-    const float *gd;
-    const float *gs;
-    int64_t in_dim, nb;
-    int m;
-};
-
-__device__ __forceinline__ int4 lds128(uint32_t addr)
-{
-    int4 v;
-    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float2 lds64f(uint32_t addr)
-{
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-    return v;
-}
-
-// Accumulate one super-block at shared address `blk`, super-block index sb of
-// its row, into acc[t]; the lane owns quant chunk c (sub-blocks 2c, 2c+1).
-template <int MT, bool XS>
-__device__ __forceinline__ void sb_accumulate(const XSrc &x, uint32_t blk, int sb, int c,
-                                              const LaneConst &L, float (&acc)[MT])
-{
-    const int4 hdr = lds128(blk);
-    const int4 qa = lds128(blk + 16 + 32 * c);
-    const int4 qb = lds128(blk + 32 + 32 * c);
-    const float d = h2f((uint16_t)((uint32_t)hdr.x & 0xffffu));
-    const float dmin = h2f((uint16_t)((uint32_t)hdr.x >> 16));
-
-    const uint32_t A = (uint32_t)hdr.y >> L.sh, B = (uint32_t)hdr.z >> L.sh, C = (uint32_t)hdr.w >> L.sh;
-    const uint32_t scp = (A & L.mask_lo) | (C & L.mask_c) | ((A >> 2) & L.mask_hi);
-    const uint32_t mnp = (B & L.mask_lo) | ((C >> 4) & L.mask_c) | ((B >> 2) & L.mask_hi);
-    const int sc0 = (int)(scp & 0xffu), sc1 = (int)((scp >> 8) & 0xffu);
-    const float dm0 = dmin * (float)(mnp & 0xffu), dm1 = dmin * (float)((mnp >> 8) & 0xffu);
-
-    const uint32_t q[8] = {(uint32_t)qa.x, (uint32_t)qa.y, (uint32_t)qa.z, (uint32_t)qa.w,
-                           (uint32_t)qb.x, (uint32_t)qb.y, (uint32_t)qb.z, (uint32_t)qb.w};
-    int lo[8], hi[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        lo[i] = (int)(q[i] & 0x0f0f0f0fu);
-        hi[i] = (int)((q[i] >> 4) & 0x0f0f0f0fu);
-    }
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-        if (t < x.m) {
-            int4 x0, x1, x2, x3;
-            float2 d8, s8;
-            if (XS) {
-                const uint32_t xa = x.q + (uint32_t)(t * (x.in_dim / 256) + sb) * kXSlot + x_chunk_off(c);
-                x0 = lds128(xa);
-                x1 = lds128(xa + 16);
-                x2 = lds128(xa + 32);
-                x3 = lds128(xa + 48);
-                const uint32_t da = x.ds + (uint32_t)(t * x.nb + sb * 8 + 2 * c) * 4u;
-                d8 = lds64f(da);
-                s8 = lds64f(da + (uint32_t)(x.m * x.nb) * 4u);
-            } else {
-                const int64_t jb = (int64_t)sb * 8 + 2 * c;
-                const int4 *xp = reinterpret_cast<const int4 *>(x.gq + t * x.in_dim + jb * 32);
-                x0 = __ldg(xp);
-                x1 = __ldg(xp + 1);
-                x2 = __ldg(xp + 2);
-                x3 = __ldg(xp + 3);
-                d8 = __ldg(reinterpret_cast<const float2 *>(x.gd + t * x.nb + jb));
-                s8 = __ldg(reinterpret_cast<const float2 *>(x.gs + t * x.nb + jb));
-            }
-            // four independent dp4a chains (two per sub-block)
-            int a0 = __dp4a(lo[0], x0.x, 0), a1 = __dp4a(lo[4], x1.x, 0);
-            int b0 = __dp4a(hi[0], x2.x, 0), b1 = __dp4a(hi[4], x3.x, 0);
-            a0 = __dp4a(lo[1], x0.y, a0);
-            a1 = __dp4a(lo[5], x1.y, a1);
-            b0 = __dp4a(hi[1], x2.y, b0);
-            b1 = __dp4a(hi[5], x3.y, b1);
-            a0 = __dp4a(lo[2], x0.z, a0);
-            a1 = __dp4a(lo[6], x1.z, a1);
-            b0 = __dp4a(hi[2], x2.z, b0);
-            b1 = __dp4a(hi[6], x3.z, b1);
-            a0 = __dp4a(lo[3], x0.w, a0);
-            a1 = __dp4a(lo[7], x1.w, a1);
-            b0 = __dp4a(hi[3], x2.w, b0);
-            b1 = __dp4a(hi[7], x3.w, b1);
-            // sc * I is exact in int32; one conversion per sub-block
-            const float t0 = (float)(sc0 * (a0 + a1)) * d8.x;
-            const float t1 = (float)(sc1 * (b0 + b1)) * d8.y;
-            acc[t] = fmaf(d, t0 + t1, acc[t]) - (dm0 * s8.x + dm1 * s8.y);
-        }
-    }
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u)
-{
-    return g / (1.0f + expf(-g)) * u;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 template <int MT, int EPI, bool XS, int XIN>
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
 {
@@ -249,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], a.PS);  // one arrival per pack
+            mbar_init(&empty[s], kConsumerWarps);  // one arrival per consumer warp
         }
         fence_mbar_init();
     }
@@ -335,63 +190,14 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     x.gq = a.xq;
     x.gd = a.xd;
     x.gs = a.xs;
-    if (XS && XIN == XIN_Q8) {
-        // codes: 16-byte chunk i of super-block sbg (all tokens) -> padded slot layout
-        const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
-        const int4 *src = reinterpret_cast<const int4 *>(a.xq);
-        for (int64_t i = threadIdx.x; i < nsbx * 16; i += kConsumerWarps * 32) {
-            const int64_t sbg = i >> 4;
-            const int ch = (int)(i & 15), cc = ch >> 2;
-            *reinterpret_cast<int4 *>(xsm + sbg * kXSlot + x_chunk_off(cc) + 16 * (ch & 3)) = src[i];
-        }
-        // d and s, unchanged
-        const int64_t nds = 2LL * a.m * x.nb / 4;
-        const int4 *dsrc = reinterpret_cast<const int4 *>(a.xd);
-        int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
-        for (int64_t i = threadIdx.x; i < nds; i += kConsumerWarps * 32) ddst[i] = dsrc[i];
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-    }
+    auto csync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
+    if (XS && XIN == XIN_Q8) stage_x_q8<false>(xsm, a.xq, a.xd, a.m, a.in_dim, threadIdx.x, csync);
     if (XS && XIN != XIN_Q8) {
         // quantise the f32 input (RMS-normalised first for XIN_NORM) straight into
-        // the padded slot layout: warp per Q8_1 block, as the standalone kernels do
-        const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
-        float *dsm = reinterpret_cast<float *>(xsm + nsbx * kXSlot);
-        float *ssm = dsm + (int64_t)a.m * x.nb;
+        // the padded slot layout
         float *red = reinterpret_cast<float *>(full) - 24;  // 17 floats below the barriers
-        auto sync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
-        for (int t = 0; t < a.m; ++t) {
-            // loads unrolled eight blocks at a time, so they are in flight together
-            const float *xrow = a.xf + t * a.ldxf;
-            const int64_t nval = XIN == XIN_NORM ? a.norm_n : a.in_dim;
-            float scale = 1.0f;
-            if (XIN == XIN_NORM) scale = rms_scale(row_sumsq(xrow, x.nb, nval, warp, lane, red, sync), a.norm_n, a.eps);
-            for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
-                if (warp + (int64_t)kRowWarps * k0 >= x.nb) break;
-                RowBatch rb;
-                row_batch(xrow, XIN == XIN_NORM ? a.gamma : nullptr, x.nb, nval, warp, lane, k0, rb);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
-                    if (b >= x.nb) break;
-                    const int64_t i = b * 32 + lane;
-                    float v = rb.v[u];
-                    if (XIN == XIN_NORM) v = (i < a.norm_n) ? __fmul_rn(__fmul_rn(v, scale), rb.g[u]) : 0.0f;
-                    const float amax = warp_max(fabsf(v));
-                    const float dq = __fdiv_rn(amax, 127.0f);
-                    const int qi = q8_code(v, dq);
-                    const int sum = warp_sum_int(qi);
-                    const int64_t sb = b >> 3;
-                    const int j = (int)(b & 7);
-                    xsm[(t * (a.in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
-                        (uint8_t)(int8_t)qi;
-                    if (lane == 0) {
-                        dsm[t * x.nb + b] = dq;
-                        ssm[t * x.nb + b] = __fmul_rn(dq, (float)sum);
-                    }
-                }
-            }
-        }
-        sync();
+        stage_x_f32<false, XIN == XIN_NORM>(xsm, a.xf, a.ldxf, a.gamma, a.norm_n, a.eps, a.m, a.in_dim, red,
+                                            warp, lane, csync);
     }
     if (XS) {
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
@@ -399,71 +205,49 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
         x.ds = smem_u32(xsm + nsbx * kXSlot);
     }
 
-    const int g = lane >> 2, c = lane & 3;
-    const LaneConst Lc = lane_const(c);
+    const int g = lane >> 2;
     const int seg_lanes = (a.rpp > 1) ? 4 * a.nsb : 32;
     const int rip = (a.rpp > 1) ? g / a.nsb : 0;  // row of the pack this group works on
     const int leader = lane % seg_lanes == 0;
     const uint32_t ring_s = smem_u32(ring);
 
-    for (int64_t i = warp; i < npacks; i += kConsumerWarps) {
-        const int64_t k = i / a.PS;
+    // Every consumer warp passes every stage in order (waits for it, takes its own
+    // packs -- pack i goes to warp i % 16 -- and releases the slot once), so no
+    // warp can run a ring length ahead of a stage that is not filled yet and the
+    // parity waits stay unambiguous.
+    for (int64_t k = 0; k < nstages; ++k) {
         const int s = (int)(k % a.NS);
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (unsigned)((k / a.NS) & 1)));
         if (!ok) {
             if (lane == 0) set_error(a.err, DEV_TIMEOUT_GEMV);
             return;
         }
-        const int64_t pack0 = r0 + i * a.rpp;
-        const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
-        const uint32_t pk = ring_s + (uint32_t)(s * a.stage_bytes + (i % a.PS) * R * pack_bytes);
-        float acc[2][MT], acc2[2][MT];
+        const int64_t first = k * a.PS, end = min(first + a.PS, npacks);
+        for (int64_t i = first + ((warp - first % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; i < end;
+             i += kConsumerWarps) {
+            const int64_t pack0 = r0 + i * a.rpp;
+            const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
+            const uint32_t pk = ring_s + (uint32_t)(s * a.stage_bytes + (i % a.PS) * R * pack_bytes);
+            float acc[2][MT];
+            pack_accumulate<MT, R, XS>(x, pk, (uint32_t)pack_bytes, a.nsb, a.rpp, rip, pack_rows, lane, acc);
+            if (rip < pack_rows) {
+                const int64_t unit = pack0 + rip;
+                const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
+                const int64_t lr = unit - a.seg_begin[kseg];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int t = 0; t < MT; ++t) acc[h][t] = acc2[h][t] = 0.0f;
-#pragma unroll
-        for (int h = 0; h < R; ++h) {
-            const uint32_t half = pk + (uint32_t)(h * pack_bytes);
-            if (a.rpp > 1) {
-                if (rip < pack_rows)
-                    sb_accumulate<MT, XS>(x, half + g * kSB, g % a.nsb, c, Lc, acc[h]);
-            } else {
-                int sb = g;
-                if (MT <= 2) {
-                    for (; sb + 8 < a.nsb; sb += 16) {  // two independent super-blocks per step
-                        sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
-                        sb_accumulate<MT, XS>(x, half + (sb + 8) * kSB, sb + 8, c, Lc, acc2[h]);
+                for (int t = 0; t < MT; ++t) {
+                    // spread the token stores over the lanes of the row
+                    if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
+                        float out = acc[0][t];
+                        if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                        if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
+                        a.y[kseg][t * a.ldy[kseg] + lr] = out;
                     }
                 }
-                for (; sb < a.nsb; sb += 8) sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // the slot's bytes are no longer read
-        // reduce over the lanes of each row (fixed order)
-#pragma unroll
-        for (int h = 0; h < R; ++h)
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                acc[h][t] += acc2[h][t];
-                for (int o = 1; o < seg_lanes; o <<= 1) acc[h][t] += __shfl_xor_sync(0xffffffffu, acc[h][t], o);
-            }
-        if (rip < pack_rows) {
-            const int64_t unit = pack0 + rip;
-            const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
-            const int64_t lr = unit - a.seg_begin[kseg];
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                // spread the token stores over the lanes of the row
-                if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
-                    float out = acc[0][t];
-                    if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
-                    if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
-                    a.y[kseg][t * a.ldy[kseg] + lr] = out;
-                }
-            }
-        }
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the slot
     }
 }
 

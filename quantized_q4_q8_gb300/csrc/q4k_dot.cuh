@@ -1,0 +1,289 @@
+// q4k_dot.cuh -- the Q4_K x Q8_1 dot-product core shared by the stand-alone GEMV
+// kernel and the persistent decode kernel: the padded shared-memory layout of
+// the Q8_1 activations, the super-block accumulation of one lane, the packing of
+// rows into ring stages, and the staging of activations (copy of Q8_1 codes, or
+// quantisation of f32 values, optionally RMS-normalised first) into that layout.
+//
+// Super-block layout (block_q4_K of GGML's k-quants): f16 d, f16 dmin, 12 bytes
+// of packed 6-bit scales and mins, 128 bytes of 4-bit codes; element e sits in
+// byte 32 (e / 64) + e % 32, low nibble when e % 64 < 32.  Value of element e of
+// sub-block j: d * sc_j * q - dmin * m_j.
+#pragma once
+
+#include "rz_common.cuh"
+
+namespace rz {
+namespace {
+
+constexpr int kSB = 144;
+
+// Shared-memory copy of the Q8_1 codes.  Super-block sb of token t occupies a
+// 288-byte slot; the 64 bytes that lane chunk c reads (sub-blocks 2c, 2c+1) sit at
+// 64c + 16(c >> 1) inside it.  With this padding the 8 lanes of a shared-memory
+// phase (2 consecutive super-blocks x 4 chunks) hit 8 different bank groups, and
+// every address is a lane constant plus a multiple of the super-block index.
+// The f32 scales d then the f32 sums s of all tokens follow the slots.
+constexpr int kXSlot = 288;
+
+__device__ __forceinline__ int x_chunk_off(int c) { return 64 * c + 16 * (c >> 1); }
+
+__host__ __device__ inline int64_t x_smem_bytes(int64_t m, int64_t in_dim)
+{
+    return m * (in_dim / 256) * kXSlot + 8 * m * (in_dim / 32);
+}
+
+// Per-lane constants of the scale/min decode.  Lane chunk c owns sub-blocks
+// j0 = 2c and j1 = 2c + 1; the two 6-bit scales (and mins) are built for both
+// sub-blocks at once, one per byte, from the 16-bit windows A = s[k], s[k+1],
+// B = s[4+k], s[5+k], C = s[8+k], s[9+k] with k = j0 & 3:
+//   j < 4 : sc = A & 63,                    m = B & 63
+//   j >= 4: sc = (C & 15) | (A >> 6) << 4,  m = (C >> 4) | (B >> 6) << 4
+struct LaneConst {
+    uint32_t sh;       // 8 * k
+    uint32_t mask_lo;  // 0x3f3f for j < 4, else 0
+    uint32_t mask_c;   // 0x0f0f for j >= 4, else 0
+    uint32_t mask_hi;  // 0x3030 for j >= 4, else 0
+};
+
+__device__ __forceinline__ LaneConst lane_const(int c)
+{
+    LaneConst L;
+    L.sh = 8u * (uint32_t)((2 * c) & 3);
+    const bool hi = c >= 2;
+    L.mask_lo = hi ? 0u : 0x3f3fu;
+    L.mask_c = hi ? 0x0f0fu : 0u;
+    L.mask_hi = hi ? 0x3030u : 0u;
+    return L;
+}
+
+struct XSrc {
+    uint32_t q;        // shared-memory byte address of the codes (token 0) (smem copy)
+    uint32_t ds;       // shared-memory byte address of d (token 0); s follows at + m*nb*4
+    const int8_t *gq;  // global copies (when the activations stay in global memory)
+    const float *gd;
+    const float *gs;
+    int64_t in_dim, nb;
+    int m;
+};
+
+__device__ __forceinline__ int4 lds128(uint32_t addr)
+{
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+// Accumulate one super-block at shared address `blk`, super-block index sb of
+// its row, into acc[t]; the lane owns quant chunk c (sub-blocks 2c, 2c+1).
+template <int MT, bool XS>
+__device__ __forceinline__ void sb_accumulate(const XSrc &x, uint32_t blk, int sb, int c,
+                                              const LaneConst &L, float (&acc)[MT])
+{
+    const int4 hdr = lds128(blk);
+    const int4 qa = lds128(blk + 16 + 32 * c);
+    const int4 qb = lds128(blk + 32 + 32 * c);
+    const float d = h2f((uint16_t)((uint32_t)hdr.x & 0xffffu));
+    const float dmin = h2f((uint16_t)((uint32_t)hdr.x >> 16));
+
+    const uint32_t A = (uint32_t)hdr.y >> L.sh, B = (uint32_t)hdr.z >> L.sh, C = (uint32_t)hdr.w >> L.sh;
+    const uint32_t scp = (A & L.mask_lo) | (C & L.mask_c) | ((A >> 2) & L.mask_hi);
+    const uint32_t mnp = (B & L.mask_lo) | ((C >> 4) & L.mask_c) | ((B >> 2) & L.mask_hi);
+    const int sc0 = (int)(scp & 0xffu), sc1 = (int)((scp >> 8) & 0xffu);
+    const float dm0 = dmin * (float)(mnp & 0xffu), dm1 = dmin * (float)((mnp >> 8) & 0xffu);
+
+    const uint32_t q[8] = {(uint32_t)qa.x, (uint32_t)qa.y, (uint32_t)qa.z, (uint32_t)qa.w,
+                           (uint32_t)qb.x, (uint32_t)qb.y, (uint32_t)qb.z, (uint32_t)qb.w};
+    int lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        lo[i] = (int)(q[i] & 0x0f0f0f0fu);
+        hi[i] = (int)((q[i] >> 4) & 0x0f0f0f0fu);
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t < x.m) {
+            int4 x0, x1, x2, x3;
+            float2 d8, s8;
+            if (XS) {
+                const uint32_t xa = x.q + (uint32_t)(t * (x.in_dim / 256) + sb) * kXSlot + x_chunk_off(c);
+                x0 = lds128(xa);
+                x1 = lds128(xa + 16);
+                x2 = lds128(xa + 32);
+                x3 = lds128(xa + 48);
+                const uint32_t da = x.ds + (uint32_t)(t * x.nb + sb * 8 + 2 * c) * 4u;
+                d8 = lds64f(da);
+                s8 = lds64f(da + (uint32_t)(x.m * x.nb) * 4u);
+            } else {
+                const int64_t jb = (int64_t)sb * 8 + 2 * c;
+                const int4 *xp = reinterpret_cast<const int4 *>(x.gq + t * x.in_dim + jb * 32);
+                x0 = __ldg(xp);
+                x1 = __ldg(xp + 1);
+                x2 = __ldg(xp + 2);
+                x3 = __ldg(xp + 3);
+                d8 = __ldg(reinterpret_cast<const float2 *>(x.gd + t * x.nb + jb));
+                s8 = __ldg(reinterpret_cast<const float2 *>(x.gs + t * x.nb + jb));
+            }
+            // four independent dp4a chains (two per sub-block)
+            int a0 = __dp4a(lo[0], x0.x, 0), a1 = __dp4a(lo[4], x1.x, 0);
+            int b0 = __dp4a(hi[0], x2.x, 0), b1 = __dp4a(hi[4], x3.x, 0);
+            a0 = __dp4a(lo[1], x0.y, a0);
+            a1 = __dp4a(lo[5], x1.y, a1);
+            b0 = __dp4a(hi[1], x2.y, b0);
+            b1 = __dp4a(hi[5], x3.y, b1);
+            a0 = __dp4a(lo[2], x0.z, a0);
+            a1 = __dp4a(lo[6], x1.z, a1);
+            b0 = __dp4a(hi[2], x2.z, b0);
+            b1 = __dp4a(hi[6], x3.z, b1);
+            a0 = __dp4a(lo[3], x0.w, a0);
+            a1 = __dp4a(lo[7], x1.w, a1);
+            b0 = __dp4a(hi[3], x2.w, b0);
+            b1 = __dp4a(hi[7], x3.w, b1);
+            // sc * I is exact in int32; one conversion per sub-block
+            const float t0 = (float)(sc0 * (a0 + a1)) * d8.x;
+            const float t1 = (float)(sc1 * (b0 + b1)) * d8.y;
+            acc[t] = fmaf(d, t0 + t1, acc[t]) - (dm0 * s8.x + dm1 * s8.y);
+        }
+    }
+}
+
+// Rows per pack: a warp takes a whole pack; rows with fewer than 8 super-blocks
+// are packed 8 / nsb to a warp so that every lane group has a super-block.
+__host__ __device__ inline int pack_rows_for(int nsb) { return (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1; }
+
+// One pack at shared address pk (R halves of pack_bytes each: gate then up for
+// the SwiGLU pair) against the staged activations; the per-row results end up
+// reduced over the lanes of the row in acc[h][t] (fixed order: deterministic).
+// Lane layout: group g = lane / 4 takes super-blocks g, g + 8, ... of its row
+// (row rip = g / nsb of the pack when rows are packed), lane c = lane % 4 one
+// 32-byte quant chunk of each.
+template <int MT, int R, bool XS>
+__device__ __forceinline__ void pack_accumulate(const XSrc &x, uint32_t pk, uint32_t pack_bytes, int nsb,
+                                                int rpp, int rip, int pack_rows, int lane,
+                                                float (&acc)[2][MT])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const LaneConst Lc = lane_const(c);
+    float acc2[2][MT];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[h][t] = acc2[h][t] = 0.0f;
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+        const uint32_t half = pk + (uint32_t)h * pack_bytes;
+        if (rpp > 1) {
+            if (rip < pack_rows) sb_accumulate<MT, XS>(x, half + g * kSB, g % nsb, c, Lc, acc[h]);
+        } else {
+            int sb = g;
+            if (MT <= 2) {
+                for (; sb + 8 < nsb; sb += 16) {  // two independent super-blocks per step
+                    sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
+                    sb_accumulate<MT, XS>(x, half + (sb + 8) * kSB, sb + 8, c, Lc, acc2[h]);
+                }
+            }
+            for (; sb < nsb; sb += 8) sb_accumulate<MT, XS>(x, half + sb * kSB, sb, c, Lc, acc[h]);
+        }
+    }
+    const int seg_lanes = (rpp > 1) ? 4 * nsb : 32;
+#pragma unroll
+    for (int h = 0; h < R; ++h)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            acc[h][t] += acc2[h][t];
+            for (int o = 1; o < seg_lanes; o <<= 1) acc[h][t] += __shfl_xor_sync(0xffffffffu, acc[h][t], o);
+        }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return g / (1.0f + expf(-g)) * u;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------- activation staging
+// Both helpers run on the 512 threads of 16 warps (thread index tid, warp, lane)
+// and end with `sync` over them.
+
+// Q8_1 codes of m rows of in_dim (SoA: codes, then d, then s) -> slot layout.
+template <bool CG, typename Sync>
+__device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const float *xd, int m,
+                                           int64_t in_dim, int tid, Sync sync)
+{
+    const int64_t nsbx = (int64_t)m * (in_dim / 256);
+    const int4 *src = reinterpret_cast<const int4 *>(xq);
+    for (int64_t i = tid; i < nsbx * 16; i += kRowWarps * 32) {
+        const int64_t sbg = i >> 4;
+        const int ch = (int)(i & 15), cc = ch >> 2;
+        const int4 v = CG ? __ldcg(src + i) : src[i];
+        *reinterpret_cast<int4 *>(xsm + sbg * kXSlot + x_chunk_off(cc) + 16 * (ch & 3)) = v;
+    }
+    // d and s, unchanged
+    const int64_t nds = 2LL * m * (in_dim / 32) / 4;
+    const int4 *dsrc = reinterpret_cast<const int4 *>(xd);
+    int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
+    for (int64_t i = tid; i < nds; i += kRowWarps * 32) ddst[i] = CG ? __ldcg(dsrc + i) : dsrc[i];
+    sync();
+}
+
+// f32 rows x[t * ldx + i] quantised into the slot layout: RMS-normalised over
+// their first norm_n values with gamma first when NORM, else as they are.  Warp
+// per Q8_1 block, the same order of operations as the stand-alone RMSNorm and
+// Q8_1 kernels, so the codes are bit-identical to theirs.  `red`: 17 floats.
+template <bool CG, bool NORM, typename Sync>
+__device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
+                                            int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
+                                            int warp, int lane, Sync sync)
+{
+    const int64_t nb = in_dim / 32;
+    const int64_t nsbx = (int64_t)m * (in_dim / 256);
+    float *dsm = reinterpret_cast<float *>(xsm + nsbx * kXSlot);
+    float *ssm = dsm + (int64_t)m * nb;
+    for (int t = 0; t < m; ++t) {
+        const float *xrow = xf + t * ldx;
+        const int64_t nval = NORM ? norm_n : in_dim;
+        float scale = 1.0f;
+        if (NORM) scale = rms_scale(row_sumsq<CG>(xrow, nb, nval, warp, lane, red, sync), norm_n, eps);
+        for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
+            if (warp + (int64_t)kRowWarps * k0 >= nb) break;
+            RowBatch rb;
+            row_batch<CG>(xrow, NORM ? gamma : nullptr, nb, nval, warp, lane, k0, rb);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
+                if (b >= nb) break;
+                const int64_t i = b * 32 + lane;
+                float v = rb.v[u];
+                if (NORM) v = (i < norm_n) ? __fmul_rn(__fmul_rn(v, scale), rb.g[u]) : 0.0f;
+                const float amax = warp_max(fabsf(v));
+                const float dq = __fdiv_rn(amax, 127.0f);
+                const int qi = q8_code(v, dq);
+                const int sum = warp_sum_int(qi);
+                const int64_t sb = b >> 3;
+                const int j = (int)(b & 7);
+                xsm[(t * (in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
+                    (uint8_t)(int8_t)qi;
+                if (lane == 0) {
+                    dsm[t * nb + b] = dq;
+                    ssm[t * nb + b] = __fmul_rn(dq, (float)sum);
+                }
+            }
+        }
+    }
+    sync();
+}
+
+}  // namespace
+}  // namespace rz

@@ -17,8 +17,10 @@ enum DevErr : unsigned {
     DEV_OK = 0,
     DEV_TIMEOUT_GEMV = 0x101,   // bulk-copy wait in a GEMV gave up
     DEV_TIMEOUT_Q40 = 0x102,
+    DEV_TIMEOUT_STEP = 0x103,   // a stage-ring wait of the persistent decode kernel gave up
     DEV_TIMEOUT_DRAIN = 0x1ff,  // draining outstanding copies gave up
     DEV_BAD_POSITION = 0x201,   // a device-resident position outside [0, max_seq)
+    DEV_TIMEOUT_GRID = 0x301,   // a grid barrier of the persistent decode kernel gave up
 };
 
 __device__ __forceinline__ void set_error(unsigned *err, unsigned code)
@@ -63,6 +65,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrival that counts `count` times (the phase completes when the arrivals of
+// the phase add up to the count given at initialisation).
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
 {
     uint32_t ok;
@@ -83,6 +93,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
 {
     for (uint32_t i = 0; i < kWaitLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Bounded wait that also gives up as soon as the error word is set by any CTA
+// (so that one failure ends every waiting CTA quickly instead of each running
+// into its own bound).  On running out of the bound it records `code`.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, unsigned parity, unsigned *err,
+                                                    unsigned code)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *reinterpret_cast<volatile unsigned *>(err) != 0u) return false;
+    }
+    set_error(err, code);
     return false;
 }
 
@@ -153,21 +177,35 @@ __device__ __forceinline__ int q8_code(float x, float d)
 constexpr int kRowWarps = 16;
 constexpr int kRowBlocksPerWarp = 32;  // rows up to 16384 values
 
+// Activation loads.  CG = false takes the read-only path (data written before the
+// kernel started); CG = true reads through L2 only, for data that other CTAs of
+// the same kernel wrote (a persistent kernel after a grid barrier).
+template <bool CG>
+__device__ __forceinline__ float ld_act(const float *p)
+{
+    if constexpr (CG)
+        return __ldcg(p);
+    else
+        return __ldg(p);
+}
+
+template <bool CG = false>
 __device__ __forceinline__ float row_value(const float *x, int64_t nb, int64_t n_valid, int warp, int lane,
                                            int k)
 {
     const int64_t b = warp + (int64_t)kRowWarps * k;
     const int64_t i = b * 32 + lane;
-    return (b < nb && i < n_valid) ? __ldg(x + i) : 0.0f;
+    return (b < nb && i < n_valid) ? ld_act<CG>(x + i) : 0.0f;
 }
 
 // The values (and gammas, when given) of 8 consecutive blocks k0 .. k0+7 of this
-// warp, loaded before any use through the read-only path so that stores to
-// shared memory between them cannot hold the loads back.
+// warp, loaded before any use so that stores to shared memory between them
+// cannot hold the loads back.  Gammas are weights: always the read-only path.
 struct RowBatch {
     float v[8], g[8];
 };
 
+template <bool CG = false>
 __device__ __forceinline__ void row_batch(const float *x, const float *gamma, int64_t nb, int64_t n_valid,
                                           int warp, int lane, int k0, RowBatch &r)
 {
@@ -176,7 +214,7 @@ __device__ __forceinline__ void row_batch(const float *x, const float *gamma, in
         const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
         const int64_t i = b * 32 + lane;
         const bool in = b < nb && i < n_valid;
-        r.v[u] = in ? __ldg(x + i) : 0.0f;
+        r.v[u] = in ? ld_act<CG>(x + i) : 0.0f;
         r.g[u] = (in && gamma) ? __ldg(gamma + i) : 0.0f;
     }
 }
@@ -185,14 +223,14 @@ __device__ __forceinline__ void row_batch(const float *x, const float *gamma, in
 // ascending block order, then the xor butterfly of each warp, then the butterfly
 // over the 16 warp sums.  `red` holds 17 floats of shared memory; `sync`
 // synchronises the 512 participating threads.  Every thread returns the total.
-template <typename Sync>
+template <bool CG = false, typename Sync>
 __device__ __forceinline__ float row_sumsq(const float *x, int64_t nb, int64_t n_valid, int warp, int lane,
                                            float *red, Sync sync)
 {
     float ss = 0.0f;
 #pragma unroll 8
     for (int k = 0; k < kRowBlocksPerWarp; ++k) {
-        const float v = row_value(x, nb, n_valid, warp, lane, k);
+        const float v = row_value<CG>(x, nb, n_valid, warp, lane, k);
         ss = fmaf(v, v, ss);
     }
     ss = warp_sum(ss);

@@ -133,7 +133,6 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
                               int64_t hidden_pad, int64_t inter, float eps, void *workspace,
                               cudaStream_t s);
 size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
-size_t layer_counter_offset(const LayerDesc &L, int64_t m, int max_seq);
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
                         int position, float *rope_tab, int make_table, float *part, int *counters,
                         const float *q, const float *k, const float *v, int64_t ld_qkv, float *att,
@@ -142,9 +141,34 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
                                 const int32_t *positions, int position, int64_t m, float *output,
                                 void *workspace, cudaStream_t s, int make_table = 1);
 size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
+// logits == nullptr: the layers only, the final hidden state in hidden_out.
 cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
                                 const KvDesc *kvs, const int32_t *positions, int position, int64_t m,
                                 const float *out_gamma, const void *lm_head, int64_t vocab,
                                 float *hidden_out, float *logits, void *workspace, cudaStream_t s);
+// kernels launched by one launch_decode_stack (with or without the head)
+int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head);
+
+// ---------------------------------------------------------------- persistent decode step
+// The decode step of a stack of identical layers as one cooperative kernel per
+// (up to) 32 layers (decode_persistent.cu).  Used by launch_decode_layer and
+// launch_decode_stack when persistent_decode_ok; the launch sequence above
+// serves every other case.
+extern bool g_use_persistent;
+
+struct PersistentWs {
+    float *xbuf[2];  // layer outputs inside one launch (ping-pong)
+    float *gbuf[2];  // outputs of the launches before the last one (ping-pong)
+    float *qkv, *part, *res1, *h;
+    void *a8;
+    int *counters;   // [m][n_kv_heads] merge counters, directly followed by
+    unsigned *gbar;  // the 2 grid-barrier words (zeroed before every launch)
+};
+
+int persistent_chunk_len(int head_dim);
+bool persistent_decode_ok(const LayerDesc &L, int64_t m, int max_seq);
+cudaError_t launch_decode_persistent(const float *input, const LayerDesc *layers, const KvDesc *kvs, int n_layers,
+                                     const int32_t *positions, int position, int64_t m, float *output,
+                                     const PersistentWs &ws, cudaStream_t s);
 
 }  // namespace rz

@@ -8,12 +8,13 @@ from ._lib import call, load, status
 __all__ = [
     "q8_1_size", "q4k_bytes", "q4_0_bytes",
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
-    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl",
+    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_set_persistent",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
-    "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
+    "rmsnorm", "residual_add", "check_device_error", "set_pdl", "set_persistent", "version",
     "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
     "swiglu_ffn", "rz_swiglu_ffn_static", "attention_workspace_bytes", "attention_decode",
     "decode_layer_workspace_bytes", "decode_layer", "rz_decode_stack", "decode_stack",
+    "rz_decode_layers", "decode_layers",
 ]
 
 
@@ -83,6 +84,10 @@ def rz_check_device_error(stream=None):
 
 def rz_set_pdl(enable: bool):
     return call("rz_set_pdl", 1 if enable else 0)
+
+
+def rz_set_persistent(enable: bool):
+    return call("rz_set_persistent", 1 if enable else 0)
 
 
 # ------------------------------------------------------------------ tensor helpers
@@ -162,6 +167,10 @@ def check_device_error(stream=None):
 
 def set_pdl(enable: bool):
     rz_set_pdl(enable)
+
+
+def set_persistent(enable: bool):
+    rz_set_persistent(enable)
 
 
 def version() -> str:
@@ -294,12 +303,33 @@ class DeviceStack:
         return load().rz_decode_stack_workspace_bytes(self.lw, len(self.layers), m,
                                                       self.kvs[0].max_seq)
 
+    def launches(self, m, with_head=True):
+        """librz kernels one rz_decode_stack (or rz_decode_layers) call launches."""
+        return load().rz_decode_stack_launches(self.lw, len(self.layers), m, self.kvs[0].max_seq,
+                                               1 if with_head else 0)
+
 
 def rz_decode_stack(x, stack: "DeviceStack", positions, position, m, hidden_out, logits, ws,
                     stream=None):
     return call("rz_decode_stack", _ptr(x), stack.lw, stack.kv, len(stack.layers),
                 _ptr(positions), position, m, _ptr(stack.out_gamma), _ptr(stack.lm_head),
                 stack.vocab, _ptr(hidden_out), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def rz_decode_layers(x, stack: "DeviceStack", positions, position, m, out, ws, stream=None):
+    return call("rz_decode_layers", _ptr(x), stack.lw, stack.kv, len(stack.layers), _ptr(positions),
+                position, m, _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def decode_layers(x, stack: "DeviceStack", position=0, positions=None, ws=None, stream=None):
+    """The stack's layers without the output norm and LM head; returns the hidden state."""
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    out = torch.empty((m, stack.layers[0].hidden_pad), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(stack.workspace_bytes(m), x.device)
+    rz_decode_layers(x, stack, positions, position, m, out, ws, stream)
+    return out
 
 
 def decode_stack(x, stack: "DeviceStack", position=0, positions=None, ws=None, stream=None,
