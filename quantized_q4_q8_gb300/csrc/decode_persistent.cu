@@ -55,8 +55,11 @@ bool g_use_persistent = false;
 
 namespace {
 
-constexpr int kPWarps = kRowWarps;             // consumer warps
+// 15 consumer warps + 1 producer warp: 16 warps, 4 per SM sub-partition, which
+// leaves 128 registers per thread (a 17th warp would cut that to 96).
+constexpr int kPWarps = 15;                    // consumer warps
 constexpr int kPThreads = (kPWarps + 1) * 32;  // + the producer warp
+constexpr int kPMaxRow = kPWarps * 32 * 32;    // activation rows the staging helpers take
 constexpr int kPMaxLayers = 32;                // layers per launch (kernel parameter space)
 constexpr int kMaxSlots = 32;
 constexpr int kAttnUnitBytes = 16384;          // K rows + V rows of one attention unit
@@ -144,6 +147,8 @@ struct Plan {
     int pos[4];              // positions of the tokens (m <= 4)
     int nc[4];               // chunks of each token
 };
+constexpr int kPlanBytes = 256;
+static_assert(sizeof(Plan) <= kPlanBytes, "plan");
 
 __device__ __forceinline__ int token_pos(const PArgs &a, int t)
 {
@@ -174,15 +179,18 @@ __device__ __forceinline__ void make_plan(const PArgs &a, Plan &p)
 }
 
 // attention unit u -> (token, kv head, chunk)
-__device__ __forceinline__ void unit_coords(const PArgs &a, const Plan &p, int64_t u, int &t, int &kvh, int &chunk)
+// (32-bit: at most m * n_kv_heads * 4096 units)
+__device__ __forceinline__ void unit_coords(const PArgs &a, const Plan &p, int64_t u64, int &t, int &kvh, int &chunk)
 {
+    int u = (int)u64;
     t = 0;
-    while (t + 1 < a.m && u >= (int64_t)a.n_kv_heads * p.nc[t]) {
-        u -= (int64_t)a.n_kv_heads * p.nc[t];
+    while (t + 1 < a.m && u >= a.n_kv_heads * p.nc[t]) {
+        u -= a.n_kv_heads * p.nc[t];
         ++t;
     }
-    kvh = (int)(u / p.nc[t]);
-    chunk = (int)(u % p.nc[t]);
+    const int nc = p.nc[t];
+    kvh = u / nc;
+    chunk = u - kvh * nc;
 }
 
 __device__ __forceinline__ int unit_rows(const PArgs &a, const Plan &p, int t, int chunk)
@@ -218,125 +226,162 @@ __device__ __forceinline__ int qkv_seg(const PArgs &a, int64_t unit, int64_t &lo
     return 2;
 }
 
-// Every byte range of stage k of phase `kind` of layer l for this CTA:
-// f(piece index, dst offset in the slot, source, bytes).  Returns the bytes of
-// the stage.
-template <typename F>
-__device__ __forceinline__ unsigned stage_ranges(const PArgs &a, const Plan &p, int l, int kind, int64_t k, F f)
+// ---------------------------------------------------------------- producer
+// The whole producer warp walks the step phase by phase.  Per phase it works out
+// the phase's geometry once; per stage it then needs a few additions: lane 0
+// waits for the slot, arms the full barrier with the stage's byte count, and the
+// stage's byte ranges (one run per Q|K|V matrix, a gate and an up range per pack,
+// a K and a V row per cache row) are spread over the lanes.  A copy may land
+// before the barrier is armed: the transaction count goes negative and the phase
+// still cannot complete before lane 0's arrival.  When a phase starts, the next
+// phase's byte ranges are prefetched into L2 (64 KB pieces over the lanes), so
+// the ring's copies mostly read L2.
+
+// Byte ranges of this CTA's share of phase (l, kind), for the L2 prefetch.
+__device__ __forceinline__ void prefetch_phase(const PArgs &a, const Plan &p, int l, int kind, int lane)
 {
     if (kind == K_ATT) {
-        int t, kvh, chunk;
-        unit_coords(a, p, p.au0 + k, t, kvh, chunk);
-        const int n = unit_rows(a, p, t, chunk);
         const unsigned rb = (unsigned)a.head_dim * 4u;
-        const int64_t base = (int64_t)t * a.seq_stride + (int64_t)chunk * a.chunk_len * a.kv_dim +
-                             (int64_t)kvh * a.head_dim;
-        for (int j = 0; j < n; ++j) {
-            f(2 * j, (unsigned)j * rb, a.L[l].kc + base + (int64_t)j * a.kv_dim, rb);
-            f(2 * j + 1, (unsigned)(a.chunk_len + j) * rb, a.L[l].vc + base + (int64_t)j * a.kv_dim, rb);
-        }
-        return 2u * (unsigned)n * rb;
-    }
-    const GemvShape g = gemv_shape(a, kind);
-    const int64_t u0 = p.r0[kind] + k * g.ps * g.rpp;
-    const int n = (int)min((int64_t)g.ps * g.rpp, p.r1[kind] - u0);  // rows in this stage
-    const int64_t pack_bytes = (int64_t)g.rpp * g.row_bytes;
-    if (g.R == 2) {
-        for (int q = 0; q * g.rpp < n; ++q) {
-            const int nr = min(g.rpp, n - q * g.rpp);
-            const int64_t u = u0 + (int64_t)q * g.rpp;
-            f(2 * q, (unsigned)(q * 2 * pack_bytes), seg_weight(a, l, kind, 0) + u * g.row_bytes,
-              (unsigned)(nr * g.row_bytes));
-            f(2 * q + 1, (unsigned)(q * 2 * pack_bytes + pack_bytes), seg_weight(a, l, kind, 1) + u * g.row_bytes,
-              (unsigned)(nr * g.row_bytes));
-        }
-    } else if (kind == K_QKV) {
-        int r = 0, piece = 0;
-        while (r < n) {
-            int64_t local;
-            const int seg = qkv_seg(a, u0 + r, local);
-            const int64_t seg_end = seg == 0 ? a.q_dim : a.kv_dim;
-            const int run = (int)min((int64_t)(n - r), seg_end - local);
-            f(piece++, (unsigned)(r * g.row_bytes), seg_weight(a, l, kind, seg) + local * g.row_bytes,
-              (unsigned)(run * g.row_bytes));
-            r += run;
-        }
-    } else {
-        f(0, 0u, seg_weight(a, l, kind, 0) + u0 * g.row_bytes, (unsigned)(n * g.row_bytes));
-    }
-    return (unsigned)(g.R * n * g.row_bytes);
-}
-
-// Position in the step's list of stages (layer, phase, stage of the phase).
-struct StageIter {
-    int l, ph;
-    int64_t k;
-};
-
-__device__ __forceinline__ void iter_skip_empty(const PArgs &a, const Plan &p, StageIter &it)
-{
-    while (it.l < a.n_layers && it.k >= p.nst[phase_kind(it.ph)]) {
-        it.k = 0;
-        if (++it.ph == kPhases) {
-            it.ph = 0;
-            ++it.l;
-        }
-    }
-}
-
-__device__ __forceinline__ void iter_next(const PArgs &a, const Plan &p, StageIter &it)
-{
-    ++it.k;
-    iter_skip_empty(a, p, it);
-}
-
-// ---------------------------------------------------------------- producer
-// The whole producer warp walks the list; lane 0 waits for free slots and arms
-// the full barrier, and the byte ranges of a stage are spread over the lanes
-// (an attention unit is 2 x CL cache rows, one copy each).  A copy may land
-// before the barrier is armed: the transaction count goes negative and the
-// phase still cannot complete before lane 0's arrival.
-__device__ void producer(const PArgs &a, const Plan &p, uint8_t *ring, uint64_t *full, uint64_t *empty, int lane)
-{
-    const int NS = a.n_slots;
-    StageIter it{0, 0, 0}, pf{0, 0, 0};
-    iter_skip_empty(a, p, it);
-    iter_skip_empty(a, p, pf);
-    int64_t P = 0;  // stage index of the prefetch cursor
-    // the first NS stages are copied at once: the prefetch window starts after them
-    while (P < NS && pf.l < a.n_layers) {
-        iter_next(a, p, pf);
-        ++P;
-    }
-    int64_t K = 0;
-    bool ok = true;
-    for (; it.l < a.n_layers; iter_next(a, p, it), ++K) {
-        // L2 prefetch window: stages [K + NS, K + NS + pf_stages)
-        while (pf.l < a.n_layers && P < K + NS + a.pf_stages) {
-            stage_ranges(a, p, pf.l, phase_kind(pf.ph), pf.k, [&](int i, unsigned, const void *src, unsigned bytes) {
-                if ((i & 31) == lane) prefetch_l2(src, bytes);
-            });
-            iter_next(a, p, pf);
-            ++P;
-        }
-        const int s = (int)(K % NS);
-        if (K >= NS) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait_abortable(&empty[s], (unsigned)(((K / NS) - 1) & 1),
-                                                                         a.err, DEV_TIMEOUT_STEP));
-            if (!got) {
-                ok = false;
-                break;
+        const int nunits = (int)(p.au1 - p.au0);
+        const int rows = nunits * a.chunk_len;
+        for (int j = lane; j < rows; j += 32) {
+            const int i = j / a.chunk_len, r = j - i * a.chunk_len;
+            int t, kvh, chunk;
+            unit_coords(a, p, p.au0 + i, t, kvh, chunk);
+            if (r < unit_rows(a, p, t, chunk)) {
+                const int64_t off = (int64_t)t * a.seq_stride + ((int64_t)chunk * a.chunk_len + r) * a.kv_dim +
+                                    (int64_t)kvh * a.head_dim;
+                prefetch_l2(a.L[l].kc + off, rb);
+                prefetch_l2(a.L[l].vc + off, rb);
             }
         }
-        uint8_t *dst = ring + (int64_t)s * a.slot_bytes;
-        const int kind = phase_kind(it.ph);
-        if (lane == 0) {
-            const unsigned bytes = stage_ranges(a, p, it.l, kind, it.k, [](int, unsigned, const void *, unsigned) {});
-            mbar_arrive_expect_tx(&full[s], bytes);
+        return;
+    }
+    const GemvShape g = gemv_shape(a, kind);
+    const int64_t r0 = p.r0[kind], r1 = p.r1[kind];
+    if (r1 <= r0) return;
+    // up to three contiguous row ranges (Q|K|V: one per matrix; gate/up: two)
+    const uint8_t *src[3];
+    int64_t len[3];
+    int nr = 0;
+    if (kind == K_QKV) {
+        const int64_t bnd[4] = {0, a.q_dim, a.q_dim + (int64_t)a.kv_dim, a.q_dim + 2 * (int64_t)a.kv_dim};
+        for (int sgi = 0; sgi < 3; ++sgi) {
+            const int64_t lo = max(r0, bnd[sgi]), hi = min(r1, bnd[sgi + 1]);
+            if (hi > lo) {
+                src[nr] = a.L[l].w[sgi] + (lo - bnd[sgi]) * g.row_bytes;
+                len[nr++] = (hi - lo) * g.row_bytes;
+            }
         }
-        stage_ranges(a, p, it.l, kind, it.k, [&](int i, unsigned off, const void *src, unsigned nbytes) {
-            if ((i & 31) == lane) bulk_g2s(dst + off, src, nbytes, &full[s]);
-        });
+    } else {
+        for (int h = 0; h < g.R; ++h) {
+            src[nr] = seg_weight(a, l, kind, h) + r0 * g.row_bytes;
+            len[nr++] = (r1 - r0) * g.row_bytes;
+        }
+    }
+    constexpr int64_t kPiece = 64 * 1024;
+    int piece = 0;
+    for (int q = 0; q < nr; ++q)
+        for (int64_t off = 0; off < len[q]; off += kPiece, ++piece)
+            if ((piece & 31) == lane) prefetch_l2(src[q] + off, (unsigned)min(kPiece, len[q] - off));
+}
+
+__device__ __forceinline__ void producer(const PArgs &a, const Plan &p, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                         int lane)
+{
+    const int NS = a.n_slots;
+    const uint32_t ring_s = smem_u32(ring);
+    // The RMSNorm gammas are read by every CTA right after a grid barrier, when
+    // HBM is busiest: each CTA brings a 1 KB slice of the next one into L2 a phase
+    // ahead (attention gamma of layer l + 1 with layer l's down rows, FFN gamma of
+    // layer l with its O rows).
+    const unsigned gbytes = (unsigned)a.hidden * 4u & ~15u, goff = blockIdx.x * 1024u;
+    auto prefetch_gamma = [&](const float *gm) {
+        if (lane == 0 && goff < gbytes) prefetch_l2(reinterpret_cast<const uint8_t *>(gm) + goff, min(1024u, gbytes - goff));
+    };
+    prefetch_gamma(a.L[0].attn_gamma);
+    prefetch_phase(a, p, 0, K_QKV, lane);
+    int64_t K = 0;
+    bool ok = true;
+    for (int l = 0; l < a.n_layers && ok; ++l) {
+        for (int ph = 0; ph < kPhases && ok; ++ph) {
+            const int kind = phase_kind(ph);
+            if (ph == 2) prefetch_gamma(a.L[l].ffn_gamma);
+            if (ph == 4 && l + 1 < a.n_layers) prefetch_gamma(a.L[l + 1].attn_gamma);
+            if (ph + 1 < kPhases)
+                prefetch_phase(a, p, l, phase_kind(ph + 1), lane);
+            else if (l + 1 < a.n_layers)
+                prefetch_phase(a, p, l + 1, K_QKV, lane);
+            const int64_t nst = p.nst[kind];
+            // phase geometry
+            GemvShape g{};
+            const uint8_t *w0 = nullptr, *w1 = nullptr, *w2 = nullptr;
+            int64_t r0 = 0, r1 = 0, stage_rows = 0, pack_bytes = 0;
+            if (kind != K_ATT) {
+                g = gemv_shape(a, kind);
+                r0 = p.r0[kind];
+                r1 = p.r1[kind];
+                stage_rows = (int64_t)g.ps * g.rpp;
+                pack_bytes = (int64_t)g.rpp * g.row_bytes;
+                w0 = seg_weight(a, l, kind, 0);
+                w1 = seg_weight(a, l, kind, 1);
+                w2 = seg_weight(a, l, kind, 2);
+            }
+            for (int64_t k = 0; k < nst; ++k, ++K) {
+                const int s = (int)(K % NS);
+                if (K >= NS) {
+                    const bool got = __all_sync(0xffffffffu, mbar_wait_abortable(&empty[s], (unsigned)(((K / NS) - 1) & 1),
+                                                                                 a.err, DEV_TIMEOUT_STEP));
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                }
+                const uint32_t dst = ring_s + (uint32_t)s * (uint32_t)a.slot_bytes;
+                unsigned bytes = 0;
+                if (kind == K_ATT) {
+                    int t, kvh, chunk;
+                    unit_coords(a, p, p.au0 + k, t, kvh, chunk);
+                    const int n = unit_rows(a, p, t, chunk);
+                    const unsigned rb = (unsigned)a.head_dim * 4u;
+                    bytes = 2u * (unsigned)n * rb;
+                    const int64_t base = (int64_t)t * a.seq_stride + (int64_t)chunk * a.chunk_len * a.kv_dim +
+                                         (int64_t)kvh * a.head_dim;
+                    for (int j = lane; j < 2 * n; j += 32) {
+                        const int r = j >> 1;
+                        const float *src = ((j & 1) ? a.L[l].vc : a.L[l].kc) + base + (int64_t)r * a.kv_dim;
+                        bulk_g2s_u32(dst + (uint32_t)((j & 1) * a.chunk_len + r) * rb, src, rb, &full[s]);
+                    }
+                } else {
+                    const int64_t u0 = r0 + k * stage_rows;
+                    const int n = (int)min(stage_rows, r1 - u0);
+                    bytes = (unsigned)(g.R * n * g.row_bytes);
+                    if (g.R == 2) {
+                        const int npk = (n + g.rpp - 1) / g.rpp;
+                        for (int j = lane; j < 2 * npk; j += 32) {
+                            const int q = j >> 1, h = j & 1;
+                            const int nr = min(g.rpp, n - q * g.rpp);
+                            const uint8_t *src = (h ? w1 : w0) + (u0 + (int64_t)q * g.rpp) * g.row_bytes;
+                            bulk_g2s_u32(dst + (uint32_t)((2 * q + h) * pack_bytes), src, (unsigned)(nr * g.row_bytes),
+                                         &full[s]);
+                        }
+                    } else if (kind == K_QKV) {
+                        if (lane < 3) {
+                            const int64_t bnd[4] = {0, a.q_dim, a.q_dim + (int64_t)a.kv_dim,
+                                                    a.q_dim + 2 * (int64_t)a.kv_dim};
+                            const int64_t lo = max(u0, bnd[lane]), hi = min(u0 + n, bnd[lane + 1]);
+                            if (hi > lo)
+                                bulk_g2s_u32(dst + (uint32_t)((lo - u0) * g.row_bytes),
+                                             (lane == 0 ? w0 : lane == 1 ? w1 : w2) + (lo - bnd[lane]) * g.row_bytes,
+                                             (unsigned)((hi - lo) * g.row_bytes), &full[s]);
+                        }
+                    } else if (lane == 0) {
+                        bulk_g2s_u32(dst, w0 + u0 * g.row_bytes, bytes, &full[s]);
+                    }
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+            }
+        }
     }
     // stages issued but perhaps not landed must land before the CTA exits
     if (!ok && lane == 0) {
@@ -348,8 +393,6 @@ __device__ void producer(const PArgs &a, const Plan &p, uint8_t *ring, uint64_t 
 
 // ---------------------------------------------------------------- consumers
 struct CCtx {
-    const PArgs *a;
-    const Plan *p;
     uint32_t ring_s;
     uint64_t *full, *empty;
     uint8_t *xsm;
@@ -365,12 +408,12 @@ __device__ __forceinline__ void csync()
 
 // All consumer warps of every CTA: after it, every global write made by any CTA
 // before it is visible.  `idx`: barriers passed so far in this launch.
-__device__ __forceinline__ void grid_barrier(const CCtx &c, unsigned idx)
+__device__ __forceinline__ void grid_barrier(const PArgs &a, const CCtx &c, unsigned idx)
 {
     csync();
     if (c.warp == 0) {
         if (c.lane == 0) {
-            unsigned *ctr = c.a->gbar;
+            unsigned *ctr = a.gbar;
             const unsigned target = gridDim.x * (idx + 1);
             __threadfence();
             atomicAdd(ctr, 1u);
@@ -382,10 +425,10 @@ __device__ __forceinline__ void grid_barrier(const CCtx &c, unsigned idx)
                     done = true;
                     break;
                 }
-                if ((i & 15u) == 15u && *reinterpret_cast<volatile unsigned *>(c.a->err) != 0u) break;
+                if ((i & 15u) == 15u && *reinterpret_cast<volatile unsigned *>(a.err) != 0u) break;
                 __nanosleep(64);
             }
-            if (!done && *reinterpret_cast<volatile unsigned *>(c.a->err) == 0u) set_error(c.a->err, DEV_TIMEOUT_GRID);
+            if (!done && *reinterpret_cast<volatile unsigned *>(a.err) == 0u) set_error(a.err, DEV_TIMEOUT_GRID);
             __threadfence();
         }
         __syncwarp();
@@ -395,11 +438,9 @@ __device__ __forceinline__ void grid_barrier(const CCtx &c, unsigned idx)
 
 // One GEMV phase: the CTA's packs, warp w taking packs w, w + 16, ...
 template <int MT, int EPI, int R>
-__device__ __forceinline__ void gemv_phase(const CCtx &c, int l, int kind, int64_t K0, const float *res,
-                                           float *y)
+__device__ __forceinline__ void gemv_phase(const PArgs &a, const Plan &p, const CCtx &c, int l, int kind, int64_t K0,
+                                           const float *res, float *y)
 {
-    const PArgs &a = *c.a;
-    const Plan &p = *c.p;
     const GemvShape g = gemv_shape(a, kind);
     const int64_t r0 = p.r0[kind], r1 = p.r1[kind];
     const int64_t npacks = (r1 - r0 + g.rpp - 1) / g.rpp;
@@ -416,10 +457,21 @@ __device__ __forceinline__ void gemv_phase(const CCtx &c, int l, int kind, int64
     const int seg_lanes = (g.rpp > 1) ? 4 * g.nsb : 32;
     const int rip = (g.rpp > 1) ? gl / g.nsb : 0;
     const int leader = c.lane % seg_lanes == 0;
-    int64_t ldy = a.hidden_pad, ldr = a.hidden_pad;
-    if (kind == K_QKV) ldy = a.q_dim + 2 * (int64_t)a.kv_dim;
-    if (kind == K_GU) ldy = a.inter;
 
+    static_assert(MT == 1, "the persistent kernel decodes one token");
+    // epilogue of one output row
+    auto store_row = [&](int64_t unit, float v0, float v1) {
+        int64_t lr = unit;
+        float *yk = y;
+        if (kind == K_QKV) {
+            const int seg = qkv_seg(a, unit, lr);
+            yk = y + (seg == 0 ? 0 : seg == 1 ? a.q_dim : a.q_dim + a.kv_dim);
+        }
+        float out = v0;
+        if (EPI == EPI_RESID) out = __ldcg(res + lr) + out;
+        if (EPI == EPI_SWIGLU) out = silu_mul(v0, v1);
+        yk[lr] = out;
+    };
     // Every warp passes every stage of the phase in order (waits for it, takes its
     // own packs in it, releases it), so no warp can run a ring length ahead of a
     // stage that is not filled yet: the parity waits stay unambiguous.
@@ -431,29 +483,29 @@ __device__ __forceinline__ void gemv_phase(const CCtx &c, int l, int kind, int64
                                                                     a.err, DEV_TIMEOUT_STEP));
         if (!ok) continue;
         const int64_t first = k * g.ps, end = min(first + g.ps, npacks);
-        for (int64_t i = first + ((c.warp - first % kPWarps) + kPWarps) % kPWarps; i < end; i += kPWarps) {
-            const int64_t pack0 = r0 + i * g.rpp;
-            const int pack_rows = (int)min((int64_t)g.rpp, r1 - pack0);
-            const uint32_t pk = c.ring_s + (uint32_t)(s * a.slot_bytes) + (uint32_t)(i % g.ps) * R * pack_bytes;
-            float acc[2][MT];
-            pack_accumulate<MT, R, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
-            if (rip < pack_rows) {
-                const int64_t unit = pack0 + rip;
-                int64_t lr = unit;
-                float *yk = y;
-                if (kind == K_QKV) {
-                    const int seg = qkv_seg(a, unit, lr);
-                    yk = y + (seg == 0 ? 0 : seg == 1 ? a.q_dim : a.q_dim + a.kv_dim);
-                }
-#pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    if (t < a.m && ((seg_lanes == 32) ? c.lane == (t & 31) : leader)) {
-                        float out = acc[0][t];
-                        if (EPI == EPI_RESID) out = __ldcg(res + t * ldr + lr) + out;
-                        if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
-                        yk[t * ldy + lr] = out;
-                    }
-                }
+        const uint32_t slot = c.ring_s + (uint32_t)(s * a.slot_bytes);
+        if (MT == 1 && g.rpp == 1) {
+            // rows in pairs: pair q of the stage (packs first + 2q, first + 2q + 1)
+            // goes to warp (pairs of earlier stages + q) % 15
+            const int64_t npair = (end - first + 1) / 2;
+            const int64_t pair0 = k * ((g.ps + 1) / 2);
+            for (int64_t q = ((c.warp - pair0 % kPWarps) + kPWarps) % kPWarps; q < npair; q += kPWarps) {
+                const int64_t iA = first + 2 * q;
+                const bool hasB = iA + 1 < end;
+                const uint32_t pkA = slot + (uint32_t)(iA % g.ps) * R * pack_bytes;
+                float acc[2][2];
+                pack_pair_accumulate<R>(x, pkA, pkA + R * pack_bytes, hasB, pack_bytes, g.nsb, c.lane, acc);
+                if (c.lane == 0 || (c.lane == 16 && hasB))
+                    store_row(r0 + iA + (c.lane >> 4), acc[0][0], acc[1][0]);
+            }
+        } else {
+            for (int64_t i = first + ((c.warp - first % kPWarps) + kPWarps) % kPWarps; i < end; i += kPWarps) {
+                const int64_t pack0 = r0 + i * g.rpp;
+                const int pack_rows = (int)min((int64_t)g.rpp, r1 - pack0);
+                const uint32_t pk = slot + (uint32_t)(i % g.ps) * R * pack_bytes;
+                float acc[2][MT];
+                pack_accumulate<MT, R, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
+                if (rip < pack_rows && leader) store_row(pack0 + rip, acc[0][0], acc[1][0]);
             }
         }
         __syncwarp();
@@ -488,71 +540,172 @@ __device__ __forceinline__ void rope_lanes(float (&v)[CPT], const float *tab, in
     }
 }
 
-// Partial record of one chunk for one query head: [max, sum, o[head_dim]]
+// Partial record [max, sum, o[head_dim]] of one query head: first for one
+// chunk, then (at the run's first chunk) for a run of chunks one CTA worked.
 __device__ __forceinline__ float *part_rec(const PArgs &a, int t, int kvh, int chunk, int g)
 {
     const int64_t idx = (((int64_t)t * a.n_kv_heads + kvh) * a.n_chunks + chunk) * a.group + g;
     return a.part + idx * (a.head_dim + 2);
 }
 
-// Merge the chunks of (t, kvh) and write the Q8_1 of its query heads.
-template <int CPT>
-__device__ __forceinline__ void attn_merge(const PArgs &a, int t, int kvh, int nc, int lane)
+// Log-sum-exp combination of records [m_k, l_k, o_k] in the order given, as a
+// running (M, L, O): for each non-empty record, M' = max(M, m_k) and
+// L, O <- L, O * exp(M - M') + l_k, o_k * exp(m_k - M').  Four records' loads are
+// in flight at a time.  GLOBAL: the records are in global memory, written by
+// other CTAs (read through L2); else in shared memory.  Lane-strided o.
+template <int CPT, bool GLOBAL, typename Rec>
+__device__ __forceinline__ void lse_combine(int n, Rec rec, int lane, float &M, float &L, float (&O)[CPT])
 {
-    const int hd = a.head_dim;
-    int8_t *q = a.a8;
-    float *qd = reinterpret_cast<float *>(q + (int64_t)a.m * a.q_pad);
-    float *qsum = qd + (int64_t)a.m * (a.q_pad / 32);
-    for (int g = 0; g < a.group; ++g) {
-        const float *r0 = part_rec(a, t, kvh, 0, g);
-        const int64_t cstride = (int64_t)a.group * (hd + 2);
-        float M = -INFINITY;
-        for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(r0 + c * cstride));
-        M = warp_max(M);
-        float L = 0.0f;
-        for (int c = lane; c < nc; c += 32) {
-            const float mc = __ldcg(r0 + c * cstride), lc = __ldcg(r0 + c * cstride + 1);
-            L += (lc > 0.0f) ? expf(mc - M) * lc : 0.0f;
-        }
-        L = warp_sum(L);
-        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;  // 0 only after a bad position
-        float o[CPT];
+    auto ld = [](const float *q) { return GLOBAL ? __ldcg(q) : *q; };
+    M = -INFINITY;
+    L = 0.0f;
 #pragma unroll
-        for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
-#pragma unroll 4
-        for (int c = 0; c < nc; ++c) {
-            const float *rc = r0 + c * cstride;
-            const float mc = __ldcg(rc), lc = __ldcg(rc + 1);
-            const float w = (lc > 0.0f) ? expf(mc - M) : 0.0f;
-            if (w != 0.0f) {
+    for (int e = 0; e < CPT; ++e) O[e] = 0.0f;
+    for (int k0 = 0; k0 < n; k0 += 4) {
+        float mk[4], lk[4], ov[4][CPT];
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) o[e] = fmaf(__ldcg(rc + 2 + 32 * e + lane), w, o[e]);
+        for (int u = 0; u < 4; ++u) {
+            lk[u] = 0.0f;
+            mk[u] = -INFINITY;
+            if (k0 + u < n) {
+                const float *r = rec(k0 + u);
+                mk[u] = ld(r);
+                lk[u] = ld(r + 1);
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) ov[u][e] = ld(r + 2 + 32 * e + lane);
             }
         }
 #pragma unroll
-        for (int e = 0; e < CPT; ++e) {
-            const float v = o[e] * inv;
-            const float amax = warp_max(fabsf(v));
-            const float dq = __fdiv_rn(amax, 127.0f);
-            const int qi = q8_code(v, dq);
-            const int sum = warp_sum_int(qi);
-            const int64_t blk = ((int64_t)(kvh * a.group + g) * hd) / 32 + e;
-            q[(int64_t)t * a.q_pad + blk * 32 + lane] = (int8_t)qi;
-            if (lane == 0) {
-                qd[(int64_t)t * (a.q_pad / 32) + blk] = dq;
-                qsum[(int64_t)t * (a.q_pad / 32) + blk] = __fmul_rn(dq, (float)sum);
+        for (int u = 0; u < 4; ++u) {
+            if (lk[u] > 0.0f) {
+                const float Mn = fmaxf(M, mk[u]);
+                const float sa = (L > 0.0f) ? expf(M - Mn) : 0.0f;
+                const float sb = expf(mk[u] - Mn);
+                L = fmaf(L, sa, lk[u] * sb);
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) O[e] = fmaf(O[e], sa, ov[u][e] * sb);
+                M = Mn;
             }
         }
     }
 }
 
-template <int CPT, int GM>
-__device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0)
+// CTA owning attention unit u (the units are split evenly over the grid)
+__device__ __forceinline__ int unit_owner(int u, int U, int G)
 {
-    const PArgs &a = *c.a;
-    const Plan &p = *c.p;
-    const int hd = a.head_dim, G = a.group, lane = c.lane;
+    int b = (int)((int64_t)u * G / U);
+    while (b + 1 < G && (int64_t)U * (b + 1) / G <= u) ++b;
+    while (b > 0 && (int64_t)U * b / G > u) --b;
+    return b;
+}
+
+// Query heads of kv head kvh for token t, lane-strided (not yet rotated).
+template <int CPT, int GM>
+__device__ __forceinline__ void load_q(const PArgs &a, int t, int kvh, int lane, float (&qv)[GM][CPT])
+{
     const int64_t ld_qkv = a.q_dim + 2 * (int64_t)a.kv_dim;
+    const float *qrow = a.qkv + (int64_t)t * ld_qkv + (int64_t)kvh * a.group * a.head_dim;
+#pragma unroll
+    for (int g = 0; g < GM; ++g)
+        if (g < a.group)
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) qv[g][e] = __ldcg(qrow + g * a.head_dim + 32 * e + lane);
+}
+
+// Step 2 of the attention phase, after every chunk record of the CTA is
+// written: the CTA's consecutive units of one (token, kv head) are combined into
+// one record at the run's first chunk (warp r % 16 takes run r); the run then
+// arrives on the head's counter with its chunk count, and the run that completes
+// the head merges the runs of all CTAs in chunk order and writes the Q8_1 of the
+// head's output.  srec: the chunk records in shared memory, or nullptr.
+template <int CPT>
+__device__ __forceinline__ void attention_runs(const PArgs &a, const Plan &p, const float *srec, int warp, int lane)
+{
+    const int hd = a.head_dim, G = a.group;
+    int U = 0, ubase[4];
+    for (int t = 0; t < a.m; ++t) {
+        ubase[t] = U;
+        U += a.n_kv_heads * p.nc[t];
+    }
+    const int au0 = (int)p.au0, au1 = (int)p.au1;
+    int r = 0;
+    for (int u = au0; u < au1; ++r) {
+        int t, kvh, chunk;
+        unit_coords(a, p, u, t, kvh, chunk);
+        const int nc = p.nc[t];
+        const int head0 = ubase[t] + kvh * nc;  // unit of chunk 0
+        const int run_end = min(au1, head0 + nc);
+        const int len = run_end - u;
+        if (r % kPWarps == warp) {
+            for (int g = 0; g < G; ++g) {
+                float M, L, O[CPT];
+                if (srec)
+                    lse_combine<CPT, false>(len, [&](int k) { return srec + ((int64_t)(u - au0 + k) * G + g) * (hd + 2); },
+                                            lane, M, L, O);
+                else
+                    lse_combine<CPT, true>(len, [&](int k) { return part_rec(a, t, kvh, chunk + k, g); }, lane, M,
+                                           L, O);
+                __syncwarp();  // every lane has read the first record before it is overwritten
+                float *rec = part_rec(a, t, kvh, chunk, g);
+                if (lane == 0) {
+                    rec[0] = M;
+                    rec[1] = L;
+                }
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) rec[2 + 32 * e + lane] = O[e];
+            }
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
+                const int prev = atomicAdd(cnt, len);
+                last = (prev + len == nc);
+                if (last) *cnt = 0;  // ready for the next layer
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                int8_t *q = a.a8;
+                float *qd = reinterpret_cast<float *>(q + (int64_t)a.m * a.q_pad);
+                float *qsum = qd + (int64_t)a.m * (a.q_pad / 32);
+                const int Gd = gridDim.x;
+                for (int g = 0; g < G; ++g) {
+                    // run starts of this head in chunk order: run k starts at the first
+                    // unit of the k-th CTA that holds units of the head
+                    const int b0 = unit_owner(head0, U, Gd);
+                    const int nrun = unit_owner(head0 + nc - 1, U, Gd) - b0 + 1;
+                    float M, L, O[CPT];
+                    lse_combine<CPT, true>(nrun, [&](int k) {
+                        const int first = k == 0 ? head0 : (int)((int64_t)U * (b0 + k) / Gd);
+                        return part_rec(a, t, kvh, first - head0, g);
+                    }, lane, M, L, O);
+                    const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;  // 0 only after a bad position
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) {
+                        const float v = O[e] * inv;
+                        const float amax = warp_max(fabsf(v));
+                        const float dq = __fdiv_rn(amax, 127.0f);
+                        const int qi = q8_code(v, dq, __frcp_rn(dq));
+                        const int sum = warp_sum_int(qi);
+                        const int64_t blk = ((int64_t)(kvh * G + g) * hd) / 32 + e;
+                        q[(int64_t)t * a.q_pad + blk * 32 + lane] = (int8_t)qi;
+                        if (lane == 0) {
+                            qd[(int64_t)t * (a.q_pad / 32) + blk] = dq;
+                            qsum[(int64_t)t * (a.q_pad / 32) + blk] = __fmul_rn(dq, (float)sum);
+                        }
+                    }
+                }
+            }
+        }
+        u = run_end;
+    }
+}
+
+template <int CPT, int GM>
+__device__ __forceinline__ void attention_phase(const PArgs &a, const Plan &p, const CCtx &c, int l, int64_t K0)
+{
+    const int hd = a.head_dim, G = a.group, lane = c.lane;
     const float scale = 1.0f / sqrtf((float)hd);
     // Q8_1 padding columns q_dim .. q_pad of the attention output are zero
     if (blockIdx.x == 0 && c.warp == 0 && a.q_pad > a.q_dim) {
@@ -566,15 +719,27 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
             }
         }
     }
-    const int64_t nunits = p.au1 - p.au0;
-    // every warp passes every unit's stage in order; unit i is worked by warp i % 16
-    for (int64_t i = 0; i < nunits; ++i) {
+    const int nunits = (int)(p.au1 - p.au0);
+    // chunk records in the (idle) activation region when they fit
+    const int rec_floats = G * (hd + 2);
+    float *srec = ((int64_t)nunits * rec_floats * 4 <= a.x_region) ? reinterpret_cast<float *>(c.xsm) : nullptr;
+
+    // 1. chunks: every warp passes every unit's stage in order; unit i is worked by
+    //    warp i % 16, which loads its query heads before it waits for the stage
+    int mine = c.warp;
+    float qv[GM][CPT];
+    if (mine < nunits) {
+        int t, kvh, chunk;
+        unit_coords(a, p, p.au0 + mine, t, kvh, chunk);
+        load_q<CPT, GM>(a, t, kvh, lane, qv);
+    }
+    for (int i = 0; i < nunits; ++i) {
         const int64_t K = K0 + i;
         const int s = (int)(K % a.n_slots);
         const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], (unsigned)((K / a.n_slots) & 1),
                                                                     a.err, DEV_TIMEOUT_STEP));
         if (!ok) continue;
-        if (i % kPWarps != c.warp) {
+        if (i != mine) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.empty[s]);
             continue;
@@ -588,23 +753,15 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
         const bool own = pos_ok && pos >= c0 && pos < c0 + a.chunk_len;
         if (!pos_ok && chunk == 0 && kvh == 0 && lane == 0) set_error(a.err, DEV_BAD_POSITION);
         const float *tab = c.rope + (int64_t)t * hd;  // hd / 2 pairs of (cos, sin)
-
-        // rotated query heads of this kv head
-        float qv[GM][CPT];
-        const float *qrow = a.qkv + (int64_t)t * ld_qkv + (int64_t)kvh * G * hd;
 #pragma unroll
-        for (int g = 0; g < GM; ++g) {
-            if (g < G) {
-#pragma unroll
-                for (int e = 0; e < CPT; ++e) qv[g][e] = __ldcg(qrow + g * hd + 32 * e + lane);
-                rope_lanes<CPT>(qv[g], tab, a.rope_mode, lane);
-            }
-        }
+        for (int g = 0; g < GM; ++g)
+            if (g < G) rope_lanes<CPT>(qv[g], tab, a.rope_mode, lane);
         // the token's own k (rotated) and v, appended to the cache
         float kn[CPT], vn[CPT];
 #pragma unroll
         for (int e = 0; e < CPT; ++e) kn[e] = vn[e] = 0.0f;
         if (own) {
+            const int64_t ld_qkv = a.q_dim + 2 * (int64_t)a.kv_dim;
             const float *kr = a.qkv + (int64_t)t * ld_qkv + a.q_dim + (int64_t)kvh * hd;
             const float *vr = kr + a.kv_dim;
 #pragma unroll
@@ -620,29 +777,47 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
                 a.L[l].vc[row + 32 * e + lane] = vn[e];
             }
         }
-        // scores: lane j keeps row j's score of each head
+        // scores, RJ rows at a time (independent reductions in flight); lane j
+        // keeps row j's score of each head
         const uint32_t ks = c.ring_s + (uint32_t)(s * a.slot_bytes);
         const uint32_t vs = ks + (uint32_t)(a.chunk_len * hd * 4);
+        constexpr int RJ = GM == 1 ? 4 : 2;
         float sc[GM];
 #pragma unroll
         for (int g = 0; g < GM; ++g) sc[g] = -INFINITY;
-        for (int j = 0; j < n; ++j) {
-            float kj[CPT];
-            const bool mine = (c0 + j == pos);
+        for (int j0 = 0; j0 < n; j0 += RJ) {
+            float kj[RJ][CPT];
 #pragma unroll
-            for (int e = 0; e < CPT; ++e) {
-                float v;
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(ks + (uint32_t)((j * hd + 32 * e + lane) * 4)));
-                kj[e] = mine ? kn[e] : v;
+            for (int r = 0; r < RJ; ++r) {
+                const int j = j0 + r;
+                const bool me = (c0 + j == pos);
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) {
+                    float v = 0.0f;
+                    if (j < n)
+                        asm volatile("ld.shared.f32 %0, [%1];"
+                                     : "=f"(v)
+                                     : "r"(ks + (uint32_t)((j * hd + 32 * e + lane) * 4)));
+                    kj[r][e] = me ? kn[e] : v;
+                }
             }
 #pragma unroll
             for (int g = 0; g < GM; ++g) {
                 if (g < G) {
-                    float dot = 0.0f;
+                    float dot[RJ];
 #pragma unroll
-                    for (int e = 0; e < CPT; ++e) dot = fmaf(qv[g][e], kj[e], dot);
-                    dot = warp_sum(dot);
-                    if (lane == j) sc[g] = dot * scale;
+                    for (int r = 0; r < RJ; ++r) {
+                        dot[r] = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) dot[r] = fmaf(qv[g][e], kj[r][e], dot[r]);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int r = 0; r < RJ; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+#pragma unroll
+                    for (int r = 0; r < RJ; ++r)
+                        if (lane == j0 + r && j0 + r < n) sc[g] = dot[r] * scale;
                 }
             }
         }
@@ -662,14 +837,15 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
         for (int g = 0; g < GM; ++g)
 #pragma unroll
             for (int e = 0; e < CPT; ++e) o[g][e] = 0.0f;
+#pragma unroll 4
         for (int j = 0; j < n; ++j) {
             float vj[CPT];
-            const bool mine = (c0 + j == pos);
+            const bool me = (c0 + j == pos);
 #pragma unroll
             for (int e = 0; e < CPT; ++e) {
                 float v;
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(vs + (uint32_t)((j * hd + 32 * e + lane) * 4)));
-                vj[e] = mine ? vn[e] : v;
+                vj[e] = me ? vn[e] : v;
             }
 #pragma unroll
             for (int g = 0; g < GM; ++g) {
@@ -682,11 +858,17 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.empty[s]);  // this warp is done with the slot
-        // partial records
+        // the next unit's query heads are on their way while this record is written
+        mine += kPWarps;
+        if (mine < nunits) {
+            int t2, kvh2, chunk2;
+            unit_coords(a, p, p.au0 + mine, t2, kvh2, chunk2);
+            load_q<CPT, GM>(a, t2, kvh2, lane, qv);
+        }
 #pragma unroll
         for (int g = 0; g < GM; ++g) {
             if (g < G) {
-                float *rec = part_rec(a, t, kvh, chunk, g);
+                float *rec = srec ? srec + ((int64_t)i * G + g) * (hd + 2) : part_rec(a, t, kvh, chunk, g);
                 if (lane == 0) {
                     rec[0] = n > 0 ? mx[g] : -INFINITY;
                     rec[1] = n > 0 ? sm[g] : 0.0f;
@@ -695,22 +877,9 @@ __device__ __forceinline__ void attention_phase(const CCtx &c, int l, int64_t K0
                 for (int e = 0; e < CPT; ++e) rec[2 + 32 * e + lane] = o[g][e];
             }
         }
-        // arrive; the last chunk of (t, kvh) merges
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
-            const int prev = atomicAdd(cnt, 1);
-            last = (prev == p.nc[t] - 1);
-            if (last) *cnt = 0;  // ready for the next layer
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence();
-            attn_merge<CPT>(a, t, kvh, p.nc[t], lane);
-        }
     }
+    csync();  // every chunk record of this CTA is written
+    attention_runs<CPT>(a, p, srec, c.warp, lane);
 }
 
 template <int CPT, int GM>
@@ -723,11 +892,11 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const _
     float *red = rope + a.m * a.head_dim;
     uint64_t *full = reinterpret_cast<uint64_t *>(red + 32);
     uint64_t *empty = full + a.n_slots;
+    Plan &p = *reinterpret_cast<Plan *>(empty + a.n_slots);  // in shared memory: read often, indexed
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    Plan p;
-    make_plan(a, p);
     if (threadIdx.x == 0) {
+        make_plan(a, p);
         for (int s = 0; s < a.n_slots; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kPWarps);  // every consumer warp releases every stage
@@ -754,8 +923,6 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const _
             rope[(t * half + i) * 2 + 1] = sn;
         }
         CCtx c;
-        c.a = &a;
-        c.p = &p;
         c.ring_s = smem_u32(ring);
         c.full = full;
         c.empty = empty;
@@ -775,37 +942,37 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const _
             const float *x_in = l == 0 ? a.input : a.xbuf[(l - 1) & 1];
             float *x_out = l == a.n_layers - 1 ? a.output : a.xbuf[l & 1];
             // 1-3: RMSNorm -> Q8_1 -> Q|K|V
-            stage_x_f32<true, true>(xsm, x_in, a.hidden_pad, L.attn_gamma, a.hidden, a.eps, a.m, a.hidden_pad, red,
+            stage_x_f32<true, true, kPWarps>(xsm, x_in, a.hidden_pad, L.attn_gamma, a.hidden, a.eps, a.m, a.hidden_pad, red,
                                     warp, lane, sync);
-            gemv_phase<1, EPI_STORE, 1>(c, l, K_QKV, K, nullptr, a.qkv);
+            gemv_phase<1, EPI_STORE, 1>(a, p, c, l, K_QKV, K, nullptr, a.qkv);
             K += p.nst[K_QKV];
-            grid_barrier(c, nbar++);
+            grid_barrier(a, c, nbar++);
             // 4-5: attention, Q8_1 of its output
-            attention_phase<CPT, GM>(c, l, K);
+            attention_phase<CPT, GM>(a, p, c, l, K);
             K += p.nst[K_ATT];
-            grid_barrier(c, nbar++);
+            grid_barrier(a, c, nbar++);
             // 6-7: O + residual
-            stage_x_q8<true>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + (int64_t)a.m * a.q_pad), a.m,
+            stage_x_q8<true, kPWarps>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + (int64_t)a.m * a.q_pad), a.m,
                              a.q_pad, threadIdx.x, sync);
-            gemv_phase<1, EPI_RESID, 1>(c, l, K_O, K, x_in, a.res1);
+            gemv_phase<1, EPI_RESID, 1>(a, p, c, l, K_O, K, x_in, a.res1);
             K += p.nst[K_O];
-            grid_barrier(c, nbar++);
+            grid_barrier(a, c, nbar++);
             // 8-9: RMSNorm -> Q8_1 -> gate/up, silu(gate) * up
-            stage_x_f32<true, true>(xsm, a.res1, a.hidden_pad, L.ffn_gamma, a.hidden, a.eps, a.m, a.hidden_pad,
+            stage_x_f32<true, true, kPWarps>(xsm, a.res1, a.hidden_pad, L.ffn_gamma, a.hidden, a.eps, a.m, a.hidden_pad,
                                     red, warp, lane, sync);
-            gemv_phase<1, EPI_SWIGLU, 2>(c, l, K_GU, K, nullptr, a.h);
+            gemv_phase<1, EPI_SWIGLU, 2>(a, p, c, l, K_GU, K, nullptr, a.h);
             K += p.nst[K_GU];
-            grid_barrier(c, nbar++);
+            grid_barrier(a, c, nbar++);
             // 9-10: Q8_1 of h -> down + residual
-            stage_x_f32<true, false>(xsm, a.h, a.inter, nullptr, 0, 0.0f, a.m, a.inter, red, warp, lane, sync);
-            gemv_phase<1, EPI_RESID, 1>(c, l, K_DN, K, a.res1, x_out);
+            stage_x_f32<true, false, kPWarps>(xsm, a.h, a.inter, nullptr, 0, 0.0f, a.m, a.inter, red, warp, lane, sync);
+            gemv_phase<1, EPI_RESID, 1>(a, p, c, l, K_DN, K, a.res1, x_out);
             K += p.nst[K_DN];
             if (blockIdx.x == 0 && a.hidden_pad > a.hidden) {
                 for (int t = 0; t < a.m; ++t)
                     for (int i = a.hidden + threadIdx.x; i < a.hidden_pad; i += kPWarps * 32)
                         x_out[(int64_t)t * a.hidden_pad + i] = 0.0f;
             }
-            if (l + 1 < a.n_layers) grid_barrier(c, nbar++);
+            if (l + 1 < a.n_layers) grid_barrier(a, c, nbar++);
         }
     }
     __syncthreads();
@@ -843,7 +1010,7 @@ HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin
     h.x_region = (int)((xr + 127) / 128 * 128);
     h.chunk_len = kAttnUnitBytes / (2 * L.head_dim * 4);
     h.n_chunks = (max_seq + h.chunk_len - 1) / h.chunk_len;
-    const int64_t fixed = h.x_region + (int64_t)m * L.head_dim * 4 + 32 * 4 + 2 * 8 * kMaxSlots;
+    const int64_t fixed = h.x_region + (int64_t)m * L.head_dim * 4 + 32 * 4 + 2 * 8 * kMaxSlots + kPlanBytes;
     const int64_t budget = (int64_t)smem_optin - fixed;
     double best = 0.0;
     for (int S = kAttnUnitBytes; S <= 32768; S += 128) {
@@ -889,9 +1056,8 @@ bool persistent_decode_ok(const LayerDesc &L, int64_t m, int max_seq)
     if (!g_use_persistent || m != 1) return false;
     if (L.head_dim != 64 && L.head_dim != 128) return false;
     if (L.n_heads % L.n_kv_heads != 0 || L.n_heads / L.n_kv_heads > kMaxG) return false;
-    // activation rows walked by the 16-warp row helpers
-    if (L.hidden_pad > 32 * kRowWarps * kRowBlocksPerWarp || L.inter > 32 * kRowWarps * kRowBlocksPerWarp)
-        return false;
+    // activation rows walked by the staging helpers
+    if (L.hidden_pad > kPMaxRow || L.inter > kPMaxRow) return false;
     const DevInfo &d = dev_info();
     int coop = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, d.device) != cudaSuccess || !coop) return false;
@@ -918,7 +1084,7 @@ cudaError_t launch_decode_persistent(const float *input, const LayerDesc *layers
             attr_done[d.device][which] = true;
         }
     }
-    const int pf_kb = env_int("RZ_L2_PREFETCH_KB", 192);
+    const int pf_kb = env_int("RZ_L2_PREFETCH_KB", 384);
     const float *cur = input;
     for (int g0 = 0; g0 < n_layers; g0 += kPMaxLayers) {
         const int nl = std::min(kPMaxLayers, n_layers - g0);

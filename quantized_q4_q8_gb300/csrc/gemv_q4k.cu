@@ -223,25 +223,51 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
             return;
         }
         const int64_t first = k * a.PS, end = min(first + a.PS, npacks);
-        for (int64_t i = first + ((warp - first % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; i < end;
-             i += kConsumerWarps) {
-            const int64_t pack0 = r0 + i * a.rpp;
-            const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
-            const uint32_t pk = ring_s + (uint32_t)(s * a.stage_bytes + (i % a.PS) * R * pack_bytes);
-            float acc[2][MT];
-            pack_accumulate<MT, R, XS>(x, pk, (uint32_t)pack_bytes, a.nsb, a.rpp, rip, pack_rows, lane, acc);
-            if (rip < pack_rows) {
-                const int64_t unit = pack0 + rip;
-                const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
-                const int64_t lr = unit - a.seg_begin[kseg];
+        const uint32_t slot = ring_s + (uint32_t)(s * a.stage_bytes);
+        if (MT == 1 && XS && a.rpp == 1) {
+            // rows in pairs: pair q of the stage (packs first + 2q, first + 2q + 1)
+            // goes to warp (pairs of earlier stages + q) % 16
+            const int64_t npair = (end - first + 1) / 2;
+            const int64_t pair0 = k * ((a.PS + 1) / 2);
+            for (int64_t q = ((warp - pair0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; q < npair;
+                 q += kConsumerWarps) {
+                const int64_t iA = first + 2 * q;
+                const bool hasB = iA + 1 < end;
+                const uint32_t pkA = slot + (uint32_t)((iA % a.PS) * R * pack_bytes);
+                float acc[2][2];
+                pack_pair_accumulate<R>(x, pkA, pkA + (uint32_t)(R * pack_bytes), hasB, (uint32_t)pack_bytes, a.nsb,
+                                        lane, acc);
+                if (lane == 0 || (lane == 16 && hasB)) {
+                    const int64_t unit = r0 + iA + (lane >> 4);
+                    const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
+                    const int64_t lr = unit - a.seg_begin[kseg];
+                    float out = acc[0][0];
+                    if (EPI == EPI_RESID) out = a.res[kseg][lr] + out;
+                    if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][0], acc[1][0]);
+                    a.y[kseg][lr] = out;
+                }
+            }
+        } else {
+            for (int64_t i = first + ((warp - first % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; i < end;
+                 i += kConsumerWarps) {
+                const int64_t pack0 = r0 + i * a.rpp;
+                const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
+                const uint32_t pk = slot + (uint32_t)((i % a.PS) * R * pack_bytes);
+                float acc[2][MT];
+                pack_accumulate<MT, R, XS>(x, pk, (uint32_t)pack_bytes, a.nsb, a.rpp, rip, pack_rows, lane, acc);
+                if (rip < pack_rows) {
+                    const int64_t unit = pack0 + rip;
+                    const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
+                    const int64_t lr = unit - a.seg_begin[kseg];
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    // spread the token stores over the lanes of the row
-                    if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
-                        float out = acc[0][t];
-                        if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
-                        if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
-                        a.y[kseg][t * a.ldy[kseg] + lr] = out;
+                    for (int t = 0; t < MT; ++t) {
+                        // spread the token stores over the lanes of the row
+                        if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
+                            float out = acc[0][t];
+                            if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                            if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
+                            a.y[kseg][t * a.ldy[kseg] + lr] = out;
+                        }
                     }
                 }
             }

@@ -155,6 +155,121 @@ __device__ __forceinline__ void sb_accumulate(const XSrc &x, uint32_t blk, int s
     }
 }
 
+// Weight super-block fields a lane needs: d, dmin, its two 6-bit scales and
+// mins (as products), and its 32 quant bytes: the low nibbles masked down
+// (0..15) and the high nibbles masked in place (16 x 0..15).
+struct SbLane {
+    float d, dm0, dm1;
+    int sc0, sc1;
+    uint32_t lo[8], hi16[8];
+};
+
+// dot of four unsigned bytes with four signed bytes, plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ void sb_lane_load(uint32_t blk, int c, const LaneConst &L, SbLane &w)
+{
+    const int4 hdr = lds128(blk);
+    const int4 qa = lds128(blk + 16 + 32 * c);
+    const int4 qb = lds128(blk + 32 + 32 * c);
+    w.d = h2f((uint16_t)((uint32_t)hdr.x & 0xffffu));
+    const float dmin = h2f((uint16_t)((uint32_t)hdr.x >> 16));
+    const uint32_t A = (uint32_t)hdr.y >> L.sh, B = (uint32_t)hdr.z >> L.sh, C = (uint32_t)hdr.w >> L.sh;
+    const uint32_t scp = (A & L.mask_lo) | (C & L.mask_c) | ((A >> 2) & L.mask_hi);
+    const uint32_t mnp = (B & L.mask_lo) | ((C >> 4) & L.mask_c) | ((B >> 2) & L.mask_hi);
+    w.sc0 = (int)(scp & 0xffu);
+    w.sc1 = (int)((scp >> 8) & 0xffu);
+    w.dm0 = dmin * (float)(mnp & 0xffu);
+    w.dm1 = dmin * (float)((mnp >> 8) & 0xffu);
+    const uint32_t q[8] = {(uint32_t)qa.x, (uint32_t)qa.y, (uint32_t)qa.z, (uint32_t)qa.w,
+                           (uint32_t)qb.x, (uint32_t)qb.y, (uint32_t)qb.z, (uint32_t)qb.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w.lo[i] = q[i] & 0x0f0f0f0fu;
+        w.hi16[i] = q[i] & 0xf0f0f0f0u;
+    }
+}
+
+// acc += the lane's share of one super-block (same value as sb_accumulate: the
+// high-nibble dot comes out 16 times too large, exactly, and is shifted back)
+__device__ __forceinline__ void sb_lane_dot(const SbLane &w, const int4 &x0, const int4 &x1, const int4 &x2,
+                                            const int4 &x3, const float2 &d8, const float2 &s8, float &acc)
+{
+    int a0 = dp4a_us(w.lo[0], x0.x, 0), a1 = dp4a_us(w.lo[4], x1.x, 0);
+    int b0 = dp4a_us(w.hi16[0], x2.x, 0), b1 = dp4a_us(w.hi16[4], x3.x, 0);
+    a0 = dp4a_us(w.lo[1], x0.y, a0);
+    a1 = dp4a_us(w.lo[5], x1.y, a1);
+    b0 = dp4a_us(w.hi16[1], x2.y, b0);
+    b1 = dp4a_us(w.hi16[5], x3.y, b1);
+    a0 = dp4a_us(w.lo[2], x0.z, a0);
+    a1 = dp4a_us(w.lo[6], x1.z, a1);
+    b0 = dp4a_us(w.hi16[2], x2.z, b0);
+    b1 = dp4a_us(w.hi16[6], x3.z, b1);
+    a0 = dp4a_us(w.lo[3], x0.w, a0);
+    a1 = dp4a_us(w.lo[7], x1.w, a1);
+    b0 = dp4a_us(w.hi16[3], x2.w, b0);
+    b1 = dp4a_us(w.hi16[7], x3.w, b1);
+    const float t0 = (float)(w.sc0 * (a0 + a1)) * d8.x;
+    const float t1 = (float)(w.sc1 * ((b0 + b1) >> 4)) * d8.y;  // |16 I| < 2^31: exact
+    acc = fmaf(w.d, t0 + t1, acc) - (w.dm0 * s8.x + w.dm1 * s8.y);
+}
+
+// Two rows at once (one token, activations in shared memory): super-block sb of
+// row A at blkA and of row B at blkB share one load of the activations.  No
+// branch between the rows, so their dependency chains interleave (a missing row
+// B is passed as a copy of row A and its result dropped by the caller).
+__device__ __forceinline__ void sb_accumulate_pair(const XSrc &x, uint32_t blkA, uint32_t blkB, int sb, int c,
+                                                   const LaneConst &L, float &accA, float &accB)
+{
+    const uint32_t xa = x.q + (uint32_t)sb * kXSlot + x_chunk_off(c);
+    const int4 x0 = lds128(xa), x1 = lds128(xa + 16), x2 = lds128(xa + 32), x3 = lds128(xa + 48);
+    const uint32_t da = x.ds + (uint32_t)(sb * 8 + 2 * c) * 4u;
+    const float2 d8 = lds64f(da), s8 = lds64f(da + (uint32_t)x.nb * 4u);
+    SbLane wa, wb;
+    sb_lane_load(blkA, c, L, wa);
+    sb_lane_load(blkB, c, L, wb);
+    sb_lane_dot(wa, x0, x1, x2, x3, d8, s8, accA);
+    sb_lane_dot(wb, x0, x1, x2, x3, d8, s8, accB);
+}
+
+// Two packs of one row each (rows with 8 or more super-blocks), one token.  On
+// return the totals of row A are in lane 0 (acc[h][0]) and those of row B in
+// lane 16 (acc[h][1]).  Reduction: one exchange across the half-warps (lanes
+// below 16 keep row A, the others row B), then the xor butterfly 8, 4, 2, 1 within
+// each half: a fixed order, so the result is deterministic.
+template <int R>
+__device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA, uint32_t pkB, bool hasB,
+                                                     uint32_t pack_bytes, int nsb, int lane, float (&acc)[2][2])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const LaneConst Lc = lane_const(c);
+    float a[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) a[h][0] = a[h][1] = 0.0f;
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+        const uint32_t hA = pkA + (uint32_t)h * pack_bytes;
+        const uint32_t hB = (hasB ? pkB : pkA) + (uint32_t)h * pack_bytes;
+        for (int sb = g; sb < nsb; sb += 8)
+            sb_accumulate_pair(x, hA + sb * kSB, hB + sb * kSB, sb, c, Lc, a[h][0], a[h][1]);
+    }
+    const bool upper = lane & 16;
+#pragma unroll
+    for (int h = 0; h < R; ++h) {
+        const float rA = a[h][0], rB = a[h][1];
+        const float keep = upper ? rB : rA, send = upper ? rA : rB;
+        float v = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[h][0] = acc[h][1] = v;  // row A in lanes 0-15, row B in lanes 16-31
+    }
+}
+
 // Rows per pack: a warp takes a whole pack; rows with fewer than 8 super-blocks
 // are packed 8 / nsb to a warp so that every lane group has a super-block.
 __host__ __device__ inline int pack_rows_for(int nsb) { return (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1; }
@@ -214,17 +329,17 @@ __device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
 }
 
 // ---------------------------------------------------------------- activation staging
-// Both helpers run on the 512 threads of 16 warps (thread index tid, warp, lane)
-// and end with `sync` over them.
+// Both helpers run on the 32 * NW threads of NW warps (thread index tid, warp,
+// lane) and end with `sync` over them.
 
 // Q8_1 codes of m rows of in_dim (SoA: codes, then d, then s) -> slot layout.
-template <bool CG, typename Sync>
+template <bool CG, int NW = kRowWarps, typename Sync>
 __device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const float *xd, int m,
                                            int64_t in_dim, int tid, Sync sync)
 {
     const int64_t nsbx = (int64_t)m * (in_dim / 256);
     const int4 *src = reinterpret_cast<const int4 *>(xq);
-    for (int64_t i = tid; i < nsbx * 16; i += kRowWarps * 32) {
+    for (int64_t i = tid; i < nsbx * 16; i += NW * 32) {
         const int64_t sbg = i >> 4;
         const int ch = (int)(i & 15), cc = ch >> 2;
         const int4 v = CG ? __ldcg(src + i) : src[i];
@@ -234,55 +349,150 @@ __device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const
     const int64_t nds = 2LL * m * (in_dim / 32) / 4;
     const int4 *dsrc = reinterpret_cast<const int4 *>(xd);
     int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
-    for (int64_t i = tid; i < nds; i += kRowWarps * 32) ddst[i] = CG ? __ldcg(dsrc + i) : dsrc[i];
+    for (int64_t i = tid; i < nds; i += NW * 32) ddst[i] = CG ? __ldcg(dsrc + i) : dsrc[i];
     sync();
 }
 
 // f32 rows x[t * ldx + i] quantised into the slot layout: RMS-normalised over
-// their first norm_n values with gamma first when NORM, else as they are.  Warp
-// per Q8_1 block, the same order of operations as the stand-alone RMSNorm and
-// Q8_1 kernels, so the codes are bit-identical to theirs.  `red`: 17 floats.
-template <bool CG, bool NORM, typename Sync>
-__device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
-                                            int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
-                                            int warp, int lane, Sync sync)
+// their first norm_n values with gamma first when NORM, else as they are.
+// Layout: thread j of the NT = 32 NW threads takes float4 number j, j + NT, ...
+// (KF of them at most), so the 32 float4s of a warp are 128 consecutive values,
+// four Q8_1 blocks of eight lanes each.  All loads are issued at once (one round
+// trip to memory); a block's max |x| and code sum take three shuffles within its
+// eight lanes, and each lane stores its four codes as one word.  The sum of
+// squares runs in a fixed order (per thread over its float4s in order, then the
+// xor butterfly of each warp, then the warp sums in order), so every CTA
+// computes the same bits.  `red`: NW + 1 floats of shared memory.
+template <bool CG, bool NORM, int KF, int NW, typename Sync>
+__device__ __forceinline__ void stage_x_f32_kf(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
+                                               int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
+                                               int warp, int lane, Sync sync)
 {
-    const int64_t nb = in_dim / 32;
-    const int64_t nsbx = (int64_t)m * (in_dim / 256);
-    float *dsm = reinterpret_cast<float *>(xsm + nsbx * kXSlot);
+    constexpr int NT = 32 * NW;
+    const int64_t nb = in_dim / 32, n4 = in_dim / 4, nsb = in_dim / 256;
+    float *dsm = reinterpret_cast<float *>(xsm + (int64_t)m * nsb * kXSlot);
     float *ssm = dsm + (int64_t)m * nb;
+    const int tid = warp * 32 + lane;
     for (int t = 0; t < m; ++t) {
-        const float *xrow = xf + t * ldx;
-        const int64_t nval = NORM ? norm_n : in_dim;
-        float scale = 1.0f;
-        if (NORM) scale = rms_scale(row_sumsq<CG>(xrow, nb, nval, warp, lane, red, sync), norm_n, eps);
-        for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
-            if (warp + (int64_t)kRowWarps * k0 >= nb) break;
-            RowBatch rb;
-            row_batch<CG>(xrow, NORM ? gamma : nullptr, nb, nval, warp, lane, k0, rb);
+        const float4 *xrow = reinterpret_cast<const float4 *>(xf + t * ldx);
+        // gammas ride along with the values for short rows; for long rows they
+        // are fetched after the reduction (registers)
+        constexpr bool kEarly = NORM && KF <= 4;
+        auto load_gamma = [&](int64_t f) {
+            // gamma holds norm_n values (not padded): no read past them
+            const int64_t i0 = f * 4;
+            float4 g;
+            if (i0 + 3 < norm_n) {
+                g = __ldg(reinterpret_cast<const float4 *>(gamma) + f);
+            } else {
+                g.x = i0 < norm_n ? __ldg(gamma + i0) : 0.f;
+                g.y = i0 + 1 < norm_n ? __ldg(gamma + i0 + 1) : 0.f;
+                g.z = i0 + 2 < norm_n ? __ldg(gamma + i0 + 2) : 0.f;
+                g.w = 0.f;
+            }
+            return g;
+        };
+        float4 v[KF], gm[kEarly ? KF : 1];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
-                if (b >= nb) break;
-                const int64_t i = b * 32 + lane;
-                float v = rb.v[u];
-                if (NORM) v = (i < norm_n) ? __fmul_rn(__fmul_rn(v, scale), rb.g[u]) : 0.0f;
-                const float amax = warp_max(fabsf(v));
-                const float dq = __fdiv_rn(amax, 127.0f);
-                const int qi = q8_code(v, dq);
-                const int sum = warp_sum_int(qi);
-                const int64_t sb = b >> 3;
-                const int j = (int)(b & 7);
-                xsm[(t * (in_dim / 256) + sb) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + lane] =
-                    (uint8_t)(int8_t)qi;
-                if (lane == 0) {
-                    dsm[t * nb + b] = dq;
-                    ssm[t * nb + b] = __fmul_rn(dq, (float)sum);
-                }
+        for (int k = 0; k < KF; ++k) {
+            const int64_t f = (int64_t)k * NT + tid;  // validity is uniform over a warp
+            if (f < n4) {
+                if constexpr (CG)
+                    v[k] = __ldcg(xrow + f);
+                else
+                    v[k] = __ldg(xrow + f);
+                if constexpr (kEarly) gm[k] = load_gamma(f);
+            } else {
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (kEarly) gm[k] = v[k];
+            }
+        }
+        if constexpr (NORM) {
+            float ss = 0.0f;
+#pragma unroll
+            for (int k = 0; k < KF; ++k) {
+                const int64_t i0 = ((int64_t)k * NT + tid) * 4;
+                // values at or past norm_n are padding
+                const float x0 = i0 < norm_n ? v[k].x : 0.f, x1 = i0 + 1 < norm_n ? v[k].y : 0.f;
+                const float x2 = i0 + 2 < norm_n ? v[k].z : 0.f, x3 = i0 + 3 < norm_n ? v[k].w : 0.f;
+                v[k] = make_float4(x0, x1, x2, x3);
+                ss = fmaf(x0, x0, ss);
+                ss = fmaf(x1, x1, ss);
+                ss = fmaf(x2, x2, ss);
+                ss = fmaf(x3, x3, ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp] = ss;
+            sync();
+            if (warp == 0) {
+                float r = 0.0f;
+                for (int w = 0; w < NW; ++w) r += red[w];  // every lane, same order
+                if (lane == 0) red[NW] = r;
+            }
+            sync();
+            const float scale = rms_scale(red[NW], norm_n, eps);
+            sync();  // red is reused by the next token
+#pragma unroll
+            for (int k = 0; k < KF; ++k) {
+                const int64_t f = (int64_t)k * NT + tid;
+                float4 g;
+                if constexpr (kEarly)
+                    g = gm[k];
+                else
+                    g = (f < n4) ? load_gamma(f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[k].x = __fmul_rn(__fmul_rn(v[k].x, scale), g.x);
+                v[k].y = __fmul_rn(__fmul_rn(v[k].y, scale), g.y);
+                v[k].z = __fmul_rn(__fmul_rn(v[k].z, scale), g.z);
+                v[k].w = __fmul_rn(__fmul_rn(v[k].w, scale), g.w);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KF; ++k) {
+            const int64_t f = (int64_t)k * NT + tid;
+            if ((int64_t)k * NT + warp * 32 >= n4) break;  // warp-uniform
+            float am = fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w)));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            const float d = __fdiv_rn(am, 127.0f);
+            const float rd = __frcp_rn(d);
+            const int q0 = q8_code(v[k].x, d, rd), q1 = q8_code(v[k].y, d, rd);
+            const int q2 = q8_code(v[k].z, d, rd), q3 = q8_code(v[k].w, d, rd);
+            int sum = q0 + q1 + q2 + q3;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            const int64_t b = f >> 3;  // Q8_1 block
+            const int e0 = (int)(f & 7) * 4;
+            const int j = (int)(b & 7);
+            const uint32_t word = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                                  ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+            *reinterpret_cast<uint32_t *>(xsm + (t * nsb + (b >> 3)) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) +
+                                          e0) = word;
+            if ((lane & 7) == 0) {
+                dsm[t * nb + b] = d;
+                ssm[t * nb + b] = __fmul_rn(d, (float)sum);
             }
         }
     }
     sync();
+}
+
+// Dispatch on the float4s per thread the row needs (rows up to NW * 1024 values).
+template <bool CG, bool NORM, int NW = kRowWarps, typename Sync>
+__device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
+                                            int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
+                                            int warp, int lane, Sync sync)
+{
+    const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
+    if (kf <= 2)
+        stage_x_f32_kf<CG, NORM, 2, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else if (kf <= 4)
+        stage_x_f32_kf<CG, NORM, 4, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else if (kf <= 6)
+        stage_x_f32_kf<CG, NORM, 6, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else
+        stage_x_f32_kf<CG, NORM, 8, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
 }
 
 }  // namespace

@@ -121,6 +121,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
         : "memory");
 }
 
+// The same with the destination as a shared-memory address.
+__device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: wait for the preceding kernel in the stream
 // (no-op when launched without the attribute).
@@ -160,8 +169,31 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// Q8_1 code of one value given its block scale: round half away from zero of the
-// IEEE f32 quotient x / d, clamped to [-127, 127]; 0 when d == 0.
+// Q8_1 code of one value given its block scale d and rd, the correctly rounded
+// 1/d (one per block): round half away from zero of the IEEE f32 quotient x / d,
+// clamped to [-127, 127]; 0 when d == 0.
+// y = x * rd is within 2.3e-5 of the IEEE quotient here: |x / d| <= 127 (1 + 2^-24)
+// because d = max|x| / 127, and 1/d, the product and the quotient each carry at
+// most 2^-24 relative rounding error.  round() is constant between consecutive
+// half-integers, so unless y lies within 2^-10 of one, y and the quotient round
+// to the same integer; next to a half-integer (and for a non-finite y, after an
+// overflowing 1/d) the quotient itself is formed and decides.
+__device__ __forceinline__ int q8_code(float x, float d, float rd)
+{
+    if (d == 0.0f) return 0;
+    const float y = __fmul_rn(x, rd);
+    const float t = fabsf(y);
+    const float f = t - floorf(t);
+    float r;
+    if (fabsf(f - 0.5f) >= 0.0009765625f)  // false for NaN
+        r = roundf(y);
+    else
+        r = roundf(__fdiv_rn(x, d));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+// The same from the quotient alone (call sites that quantise one value per scale).
 __device__ __forceinline__ int q8_code(float x, float d)
 {
     if (d == 0.0f) return 0;

@@ -40,6 +40,25 @@ def test_q8_1_bit_exact(rz, m, n):
     assert np.array_equal(q8, oracle.q8_1_quantize(x))
 
 
+def test_q8_1_boundary_quotients_bit_exact(rz):
+    """Every element next to a rounding boundary of x / d ((k + 1/2) d, nudged by at
+    most an ulp): the kernels decide these with the IEEE quotient, as the format
+    does, so the codes still match the oracle bit for bit."""
+    g = np.random.default_rng(11)
+    nblk = 4096
+    amax = g.uniform(0.01, 100, nblk).astype(np.float32)
+    d = amax / np.float32(127)
+    k = g.integers(-126, 126, (nblk, 31)).astype(np.float32)
+    x = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    nudge = g.integers(-1, 2, x.shape)
+    x = np.where(nudge > 0, np.nextafter(x, np.float32(np.inf)),
+                 np.where(nudge < 0, np.nextafter(x, np.float32(-np.inf)), x))
+    x = np.concatenate([amax[:, None], x], axis=1).astype(np.float32).reshape(4, -1)
+    q8 = rz.q8_1_quantize(to_dev(x)).cpu().numpy()
+    check_no_device_error()
+    assert np.array_equal(q8, oracle.q8_1_quantize(x))
+
+
 def test_q8_1_large_magnitudes_bit_exact(rz):
     x = S.normal("gq8.big", (2, 512)) * np.float32(4.0e4)
     q8 = rz.q8_1_quantize(to_dev(x)).cpu().numpy()
