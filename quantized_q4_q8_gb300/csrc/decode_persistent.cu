@@ -211,21 +211,6 @@ __device__ __forceinline__ const uint8_t *seg_weight(const PArgs &a, int l, int 
     }
 }
 
-// Q|K|V: rows [0, q_dim) of wq, then wk, then wv; every other kind has one matrix.
-__device__ __forceinline__ int qkv_seg(const PArgs &a, int64_t unit, int64_t &local)
-{
-    if (unit < a.q_dim) {
-        local = unit;
-        return 0;
-    }
-    if (unit < a.q_dim + a.kv_dim) {
-        local = unit - a.q_dim;
-        return 1;
-    }
-    local = unit - a.q_dim - a.kv_dim;
-    return 2;
-}
-
 // ---------------------------------------------------------------- producer
 // The whole producer warp walks the step phase by phase.  Per phase it works out
 // the phase's geometry once; per stage it then needs a few additions: lane 0
@@ -302,6 +287,7 @@ __device__ __forceinline__ void producer(const PArgs &a, const Plan &p, uint8_t 
     prefetch_gamma(a.L[0].attn_gamma);
     prefetch_phase(a, p, 0, K_QKV, lane);
     int64_t K = 0;
+    RingPos rp{0, 0u};
     bool ok = true;
     for (int l = 0; l < a.n_layers && ok; ++l) {
         for (int ph = 0; ph < kPhases && ok; ++ph) {
@@ -327,11 +313,12 @@ __device__ __forceinline__ void producer(const PArgs &a, const Plan &p, uint8_t 
                 w1 = seg_weight(a, l, kind, 1);
                 w2 = seg_weight(a, l, kind, 2);
             }
-            for (int64_t k = 0; k < nst; ++k, ++K) {
-                const int s = (int)(K % NS);
+            for (int64_t k = 0; k < nst; ++k, ++K, ring_next(rp, NS)) {
+                const int s = rp.s;
                 if (K >= NS) {
-                    const bool got = __all_sync(0xffffffffu, mbar_wait_abortable(&empty[s], (unsigned)(((K / NS) - 1) & 1),
-                                                                                 a.err, DEV_TIMEOUT_STEP));
+                    // the slot's previous stage (one ring length back) is released
+                    const bool got = __all_sync(0xffffffffu, mbar_wait_abortable(&empty[s], rp.par ^ 1u, a.err,
+                                                                                 DEV_TIMEOUT_STEP));
                     if (!got) {
                         ok = false;
                         break;
@@ -437,20 +424,26 @@ __device__ __forceinline__ void grid_barrier(const PArgs &a, const CCtx &c, unsi
 }
 
 // One GEMV phase: the CTA's packs, warp w taking packs w, w + 16, ...
-template <int MT, int EPI, int R>
-__device__ __forceinline__ void gemv_phase(const PArgs &a, const Plan &p, const CCtx &c, int l, int kind, int64_t K0,
+// One GEMV phase of the consumers (kind K_QKV, K_O, K_GU or K_DN).  Called from
+// one place for all four kinds: with a copy per kind the kernel's code outgrew
+// the instruction caches and instruction fetch became the first stall.
+__device__ __forceinline__ void gemv_phase(const PArgs &a, const Plan &p, const CCtx &cc, int kind, int64_t K0,
                                            const float *res, float *y)
 {
+    const CCtx c = cc;
+    const int R = kind == K_GU ? 2 : 1;
     const GemvShape g = gemv_shape(a, kind);
     const int64_t r0 = p.r0[kind], r1 = p.r1[kind];
     const int64_t npacks = (r1 - r0 + g.rpp - 1) / g.rpp;
     const uint32_t pack_bytes = (uint32_t)(g.rpp * g.row_bytes);
+    const int n_slots = a.n_slots, slot_bytes = a.slot_bytes, q_dim = a.q_dim, kv_dim = a.kv_dim;
+    unsigned *const err = a.err;
     XSrc x;
     x.in_dim = g.in_dim;
     x.nb = g.in_dim / 32;
-    x.m = a.m;
+    x.m = 1;
     x.q = smem_u32(c.xsm);
-    x.ds = smem_u32(c.xsm + (int64_t)a.m * (g.in_dim / 256) * kXSlot);
+    x.ds = smem_u32(c.xsm + (g.in_dim / 256) * kXSlot);
     x.gq = nullptr;
     x.gd = x.gs = nullptr;
     const int gl = c.lane >> 2;
@@ -458,59 +451,78 @@ __device__ __forceinline__ void gemv_phase(const PArgs &a, const Plan &p, const 
     const int rip = (g.rpp > 1) ? gl / g.nsb : 0;
     const int leader = c.lane % seg_lanes == 0;
 
-    static_assert(MT == 1, "the persistent kernel decodes one token");
     // epilogue of one output row
     auto store_row = [&](int64_t unit, float v0, float v1) {
         int64_t lr = unit;
         float *yk = y;
         if (kind == K_QKV) {
-            const int seg = qkv_seg(a, unit, lr);
-            yk = y + (seg == 0 ? 0 : seg == 1 ? a.q_dim : a.q_dim + a.kv_dim);
+            const int seg = unit < q_dim ? 0 : unit < q_dim + kv_dim ? 1 : 2;
+            const int64_t base = seg == 0 ? 0 : seg == 1 ? q_dim : (int64_t)q_dim + kv_dim;
+            lr = unit - base;
+            yk = y + base;
         }
         float out = v0;
-        if (EPI == EPI_RESID) out = __ldcg(res + lr) + out;
-        if (EPI == EPI_SWIGLU) out = silu_mul(v0, v1);
+        if (kind == K_O || kind == K_DN) out = __ldcg(res + lr) + out;
+        if (kind == K_GU) out = silu_mul(v0, v1);
         yk[lr] = out;
     };
     // Every warp passes every stage of the phase in order (waits for it, takes its
     // own packs in it, releases it), so no warp can run a ring length ahead of a
     // stage that is not filled yet: the parity waits stay unambiguous.
-    const int64_t nst = p.nst[kind];
-    for (int64_t k = 0; k < nst; ++k) {
-        const int64_t K = K0 + k;
-        const int s = (int)(K % a.n_slots);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], (unsigned)((K / a.n_slots) & 1),
-                                                                    a.err, DEV_TIMEOUT_STEP));
-        if (!ok) continue;
-        const int64_t first = k * g.ps, end = min(first + g.ps, npacks);
-        const uint32_t slot = c.ring_s + (uint32_t)(s * a.slot_bytes);
-        if (MT == 1 && g.rpp == 1) {
+    const int nst = (int)p.nst[kind];
+    const int npk = (int)npacks, ps = g.ps, pps = (ps + 1) / 2;  // packs and pairs per stage
+    RingPos rp = ring_pos(K0, n_slots);
+    int prot = 0, rot = 0;  // pairs / packs of the earlier stages, modulo the warp count
+    for (int k = 0; k < nst; ++k, ring_next(rp, n_slots)) {
+        const int s = rp.s;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], rp.par, err, DEV_TIMEOUT_STEP));
+        const int first = k * ps, end = min(first + ps, npk);
+        const uint32_t slot = c.ring_s + (uint32_t)(s * slot_bytes);
+        if (ok && g.rpp == 1) {
             // rows in pairs: pair q of the stage (packs first + 2q, first + 2q + 1)
             // goes to warp (pairs of earlier stages + q) % 15
-            const int64_t npair = (end - first + 1) / 2;
-            const int64_t pair0 = k * ((g.ps + 1) / 2);
-            for (int64_t q = ((c.warp - pair0 % kPWarps) + kPWarps) % kPWarps; q < npair; q += kPWarps) {
-                const int64_t iA = first + 2 * q;
+            const int npair = (end - first + 1) / 2;
+            for (int q = (c.warp - prot + kPWarps) % kPWarps; q < npair; q += kPWarps) {
+                const int iA = first + 2 * q;
                 const bool hasB = iA + 1 < end;
-                const uint32_t pkA = slot + (uint32_t)(iA % g.ps) * R * pack_bytes;
+                const uint32_t pkA = slot + (uint32_t)(2 * q) * R * pack_bytes;
                 float acc[2][2];
-                pack_pair_accumulate<R>(x, pkA, pkA + R * pack_bytes, hasB, pack_bytes, g.nsb, c.lane, acc);
+                pack_pair_accumulate(x, pkA, pkA + R * pack_bytes, hasB, R, pack_bytes, g.nsb, c.lane, acc);
                 if (c.lane == 0 || (c.lane == 16 && hasB))
                     store_row(r0 + iA + (c.lane >> 4), acc[0][0], acc[1][0]);
             }
-        } else {
-            for (int64_t i = first + ((c.warp - first % kPWarps) + kPWarps) % kPWarps; i < end; i += kPWarps) {
-                const int64_t pack0 = r0 + i * g.rpp;
+        } else if (ok) {
+            for (int i = first + (c.warp - rot + kPWarps) % kPWarps; i < end; i += kPWarps) {
+                const int64_t pack0 = r0 + (int64_t)i * g.rpp;
                 const int pack_rows = (int)min((int64_t)g.rpp, r1 - pack0);
-                const uint32_t pk = slot + (uint32_t)(i % g.ps) * R * pack_bytes;
-                float acc[2][MT];
-                pack_accumulate<MT, R, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
+                const uint32_t pk = slot + (uint32_t)(i - first) * R * pack_bytes;
+                float acc[2][1];
+                if (R == 2)
+                    pack_accumulate<1, 2, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
+                else
+                    pack_accumulate<1, 1, true>(x, pk, pack_bytes, g.nsb, g.rpp, rip, pack_rows, c.lane, acc);
                 if (rip < pack_rows && leader) store_row(pack0 + rip, acc[0][0], acc[1][0]);
             }
         }
+        prot += pps;
+        while (prot >= kPWarps) prot -= kPWarps;
+        rot += ps;
+        while (rot >= kPWarps) rot -= kPWarps;
+        if (!ok) continue;
         __syncwarp();
         if (c.lane == 0) mbar_arrive(&c.empty[s]);  // this warp is done with the slot
     }
+}
+
+// Activation staging of the consumers (one call site for the same reason).
+__device__ __forceinline__ void stage_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
+                                          int64_t norm_n, float eps, int64_t in_dim, float *red, int warp, int lane)
+{
+    auto sync = [] { csync(); };
+    if (gamma)
+        stage_x_f32<true, true, kPWarps>(xsm, xf, ldx, gamma, norm_n, eps, 1, in_dim, red, warp, lane, sync);
+    else
+        stage_x_f32<true, false, kPWarps>(xsm, xf, ldx, nullptr, 0, 0.0f, 1, in_dim, red, warp, lane, sync);
 }
 
 // RoPE of one head held lane-strided (v[e] = element 32 e + lane) with the
@@ -628,15 +640,15 @@ __device__ __forceinline__ void attention_runs(const PArgs &a, const Plan &p, co
         U += a.n_kv_heads * p.nc[t];
     }
     const int au0 = (int)p.au0, au1 = (int)p.au1;
-    int r = 0;
-    for (int u = au0; u < au1; ++r) {
+    int rw = 0;  // warp of the current run
+    for (int u = au0; u < au1; rw = rw + 1 == kPWarps ? 0 : rw + 1) {
         int t, kvh, chunk;
         unit_coords(a, p, u, t, kvh, chunk);
         const int nc = p.nc[t];
         const int head0 = ubase[t] + kvh * nc;  // unit of chunk 0
         const int run_end = min(au1, head0 + nc);
         const int len = run_end - u;
-        if (r % kPWarps == warp) {
+        if (rw == warp) {
             for (int g = 0; g < G; ++g) {
                 float M, L, O[CPT];
                 if (srec)
@@ -686,7 +698,7 @@ __device__ __forceinline__ void attention_runs(const PArgs &a, const Plan &p, co
                         const float v = O[e] * inv;
                         const float amax = warp_max(fabsf(v));
                         const float dq = __fdiv_rn(amax, 127.0f);
-                        const int qi = q8_code(v, dq, __frcp_rn(dq));
+                        const int qi = q8_code(v, dq, rcp_approx(dq));
                         const int sum = warp_sum_int(qi);
                         const int64_t blk = ((int64_t)(kvh * G + g) * hd) / 32 + e;
                         q[(int64_t)t * a.q_pad + blk * 32 + lane] = (int8_t)qi;
@@ -733,11 +745,10 @@ __device__ __forceinline__ void attention_phase(const PArgs &a, const Plan &p, c
         unit_coords(a, p, p.au0 + mine, t, kvh, chunk);
         load_q<CPT, GM>(a, t, kvh, lane, qv);
     }
-    for (int i = 0; i < nunits; ++i) {
-        const int64_t K = K0 + i;
-        const int s = (int)(K % a.n_slots);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], (unsigned)((K / a.n_slots) & 1),
-                                                                    a.err, DEV_TIMEOUT_STEP));
+    RingPos rp = ring_pos(K0, a.n_slots);
+    for (int i = 0; i < nunits; ++i, ring_next(rp, a.n_slots)) {
+        const int s = rp.s;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_abortable(&c.full[s], rp.par, a.err, DEV_TIMEOUT_STEP));
         if (!ok) continue;
         if (i != mine) {
             __syncwarp();
@@ -937,42 +948,39 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const _
         unsigned nbar = 0;
         int64_t K = 0;
         auto sync = [] { csync(); };
+        // The five phases of a layer run through one call site each for the
+        // staging and the GEMV, so that their code exists once (see gemv_phase).
         for (int l = 0; l < a.n_layers; ++l) {
             const PLayer &L = a.L[l];
             const float *x_in = l == 0 ? a.input : a.xbuf[(l - 1) & 1];
             float *x_out = l == a.n_layers - 1 ? a.output : a.xbuf[l & 1];
-            // 1-3: RMSNorm -> Q8_1 -> Q|K|V
-            stage_x_f32<true, true, kPWarps>(xsm, x_in, a.hidden_pad, L.attn_gamma, a.hidden, a.eps, a.m, a.hidden_pad, red,
-                                    warp, lane, sync);
-            gemv_phase<1, EPI_STORE, 1>(a, p, c, l, K_QKV, K, nullptr, a.qkv);
-            K += p.nst[K_QKV];
-            grid_barrier(a, c, nbar++);
-            // 4-5: attention, Q8_1 of its output
-            attention_phase<CPT, GM>(a, p, c, l, K);
-            K += p.nst[K_ATT];
-            grid_barrier(a, c, nbar++);
-            // 6-7: O + residual
-            stage_x_q8<true, kPWarps>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + (int64_t)a.m * a.q_pad), a.m,
-                             a.q_pad, threadIdx.x, sync);
-            gemv_phase<1, EPI_RESID, 1>(a, p, c, l, K_O, K, x_in, a.res1);
-            K += p.nst[K_O];
-            grid_barrier(a, c, nbar++);
-            // 8-9: RMSNorm -> Q8_1 -> gate/up, silu(gate) * up
-            stage_x_f32<true, true, kPWarps>(xsm, a.res1, a.hidden_pad, L.ffn_gamma, a.hidden, a.eps, a.m, a.hidden_pad,
-                                    red, warp, lane, sync);
-            gemv_phase<1, EPI_SWIGLU, 2>(a, p, c, l, K_GU, K, nullptr, a.h);
-            K += p.nst[K_GU];
-            grid_barrier(a, c, nbar++);
-            // 9-10: Q8_1 of h -> down + residual
-            stage_x_f32<true, false, kPWarps>(xsm, a.h, a.inter, nullptr, 0, 0.0f, a.m, a.inter, red, warp, lane, sync);
-            gemv_phase<1, EPI_RESID, 1>(a, p, c, l, K_DN, K, a.res1, x_out);
-            K += p.nst[K_DN];
-            if (blockIdx.x == 0 && a.hidden_pad > a.hidden) {
-                for (int t = 0; t < a.m; ++t)
-                    for (int i = a.hidden + threadIdx.x; i < a.hidden_pad; i += kPWarps * 32)
-                        x_out[(int64_t)t * a.hidden_pad + i] = 0.0f;
+            for (int ph = 0; ph < kPhases; ++ph) {
+                const int kind = phase_kind(ph);
+                if (kind == K_ATT) {
+                    // 4-5: attention, Q8_1 of its output
+                    attention_phase<CPT, GM>(a, p, c, l, K);
+                } else {
+                    // 1-3: RMSNorm -> Q8_1 -> Q|K|V; 6-7: O + residual; 8-9: RMSNorm ->
+                    // Q8_1 -> gate/up, silu(gate) * up; 9-10: Q8_1 of h -> down + residual
+                    if (kind == K_O) {
+                        stage_x_q8<true, kPWarps>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + a.q_pad), 1,
+                                                  a.q_pad, threadIdx.x, sync);
+                    } else {
+                        const float *src = kind == K_QKV ? x_in : kind == K_GU ? a.res1 : a.h;
+                        const int64_t n = kind == K_DN ? a.inter : a.hidden_pad;
+                        const float *gamma = kind == K_QKV ? L.attn_gamma : kind == K_GU ? L.ffn_gamma : nullptr;
+                        stage_f32(xsm, src, n, gamma, gamma ? a.hidden : 0, a.eps, n, red, warp, lane);
+                    }
+                    const float *res = kind == K_O ? x_in : kind == K_DN ? a.res1 : nullptr;
+                    float *y = kind == K_QKV ? a.qkv : kind == K_O ? a.res1 : kind == K_GU ? a.h : x_out;
+                    gemv_phase(a, p, c, kind, K, res, y);
+                }
+                K += p.nst[kind];
+                if (kind == K_DN && blockIdx.x == 0 && a.hidden_pad > a.hidden) {
+                    for (int i = a.hidden + threadIdx.x; i < a.hidden_pad; i += kPWarps * 32) x_out[i] = 0.0f;
+                }
+                if (ph + 1 < kPhases || l + 1 < a.n_layers) grid_barrier(a, c, nbar++);
             }
-            if (l + 1 < a.n_layers) grid_barrier(a, c, nbar++);
         }
     }
     __syncthreads();

@@ -137,9 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
             }
             int64_t k = 0;
             bool ok = true;
-            for (; k < nstages; ++k) {
-                const int s = (int)(k % a.NS);
-                if (k >= a.NS && !mbar_wait(&empty[s], (unsigned)(((k / a.NS) - 1) & 1))) {
+            RingPos rp{0, 0u};
+            for (; k < nstages; ++k, ring_next(rp, a.NS)) {
+                const int s = rp.s;
+                if (k >= a.NS && !mbar_wait(&empty[s], rp.par ^ 1u)) {
                     set_error(a.err, DEV_TIMEOUT_GEMV);
                     ok = false;
                     break;
@@ -215,28 +216,34 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     // packs -- pack i goes to warp i % 16 -- and releases the slot once), so no
     // warp can run a ring length ahead of a stage that is not filled yet and the
     // parity waits stay unambiguous.
-    for (int64_t k = 0; k < nstages; ++k) {
-        const int s = (int)(k % a.NS);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (unsigned)((k / a.NS) & 1)));
+    RingPos rp{0, 0u};
+    const int npk = (int)npacks, PS = a.PS, pps = (PS + 1) / 2;  // packs and pairs per stage
+    int prot = 0, rot = 0;  // pairs / packs of the earlier stages, modulo the warp count
+    for (int k = 0; k < (int)nstages; ++k, ring_next(rp, a.NS)) {
+        const int s = rp.s;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], rp.par));
         if (!ok) {
             if (lane == 0) set_error(a.err, DEV_TIMEOUT_GEMV);
             return;
         }
-        const int64_t first = k * a.PS, end = min(first + a.PS, npacks);
+        const int first = k * PS, end = min(first + PS, npk);
         const uint32_t slot = ring_s + (uint32_t)(s * a.stage_bytes);
+        const int q0 = (warp - prot + kConsumerWarps) % kConsumerWarps, i0 = (warp - rot + kConsumerWarps) % kConsumerWarps;
+        prot += pps;
+        while (prot >= kConsumerWarps) prot -= kConsumerWarps;
+        rot += PS;
+        while (rot >= kConsumerWarps) rot -= kConsumerWarps;
         if (MT == 1 && XS && a.rpp == 1) {
             // rows in pairs: pair q of the stage (packs first + 2q, first + 2q + 1)
             // goes to warp (pairs of earlier stages + q) % 16
-            const int64_t npair = (end - first + 1) / 2;
-            const int64_t pair0 = k * ((a.PS + 1) / 2);
-            for (int64_t q = ((warp - pair0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; q < npair;
-                 q += kConsumerWarps) {
-                const int64_t iA = first + 2 * q;
+            const int npair = (end - first + 1) / 2;
+            for (int q = q0; q < npair; q += kConsumerWarps) {
+                const int iA = first + 2 * q;
                 const bool hasB = iA + 1 < end;
-                const uint32_t pkA = slot + (uint32_t)((iA % a.PS) * R * pack_bytes);
+                const uint32_t pkA = slot + (uint32_t)(2 * q * R * pack_bytes);
                 float acc[2][2];
-                pack_pair_accumulate<R>(x, pkA, pkA + (uint32_t)(R * pack_bytes), hasB, (uint32_t)pack_bytes, a.nsb,
-                                        lane, acc);
+                pack_pair_accumulate(x, pkA, pkA + (uint32_t)(R * pack_bytes), hasB, R, (uint32_t)pack_bytes, a.nsb,
+                                     lane, acc);
                 if (lane == 0 || (lane == 16 && hasB)) {
                     const int64_t unit = r0 + iA + (lane >> 4);
                     const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
@@ -248,11 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                 }
             }
         } else {
-            for (int64_t i = first + ((warp - first % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; i < end;
-                 i += kConsumerWarps) {
-                const int64_t pack0 = r0 + i * a.rpp;
+            for (int i = first + i0; i < end; i += kConsumerWarps) {
+                const int64_t pack0 = r0 + (int64_t)i * a.rpp;
                 const int pack_rows = (int)min((int64_t)a.rpp, r1 - pack0);
-                const uint32_t pk = slot + (uint32_t)((i % a.PS) * R * pack_bytes);
+                const uint32_t pk = slot + (uint32_t)((i - first) * R * pack_bytes);
                 float acc[2][MT];
                 pack_accumulate<MT, R, XS>(x, pk, (uint32_t)pack_bytes, a.nsb, a.rpp, rip, pack_rows, lane, acc);
                 if (rip < pack_rows) {

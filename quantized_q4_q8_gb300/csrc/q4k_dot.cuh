@@ -242,8 +242,7 @@ __device__ __forceinline__ void sb_accumulate_pair(const XSrc &x, uint32_t blkA,
 // lane 16 (acc[h][1]).  Reduction: one exchange across the half-warps (lanes
 // below 16 keep row A, the others row B), then the xor butterfly 8, 4, 2, 1 within
 // each half: a fixed order, so the result is deterministic.
-template <int R>
-__device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA, uint32_t pkB, bool hasB,
+__device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA, uint32_t pkB, bool hasB, int R,
                                                      uint32_t pack_bytes, int nsb, int lane, float (&acc)[2][2])
 {
     const int g = lane >> 2, c = lane & 3;
@@ -251,7 +250,7 @@ __device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA
     float a[2][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) a[h][0] = a[h][1] = 0.0f;
-#pragma unroll
+#pragma unroll 1
     for (int h = 0; h < R; ++h) {
         const uint32_t hA = pkA + (uint32_t)h * pack_bytes;
         const uint32_t hB = (hasB ? pkB : pkA) + (uint32_t)h * pack_bytes;
@@ -260,7 +259,7 @@ __device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA
     }
     const bool upper = lane & 16;
 #pragma unroll
-    for (int h = 0; h < R; ++h) {
+    for (int h = 0; h < 2; ++h) {
         const float rA = a[h][0], rB = a[h][1];
         const float keep = upper ? rB : rA, send = upper ? rA : rB;
         float v = keep + __shfl_xor_sync(0xffffffffu, send, 16);
@@ -455,7 +454,7 @@ __device__ __forceinline__ void stage_x_f32_kf(uint8_t *xsm, const float *xf, in
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
             const float d = __fdiv_rn(am, 127.0f);
-            const float rd = __frcp_rn(d);
+            const float rd = rcp_approx(d);
             const int q0 = q8_code(v[k].x, d, rd), q1 = q8_code(v[k].y, d, rd);
             const int q2 = q8_code(v[k].z, d, rd), q3 = q8_code(v[k].w, d, rd);
             int sum = q0 + q1 + q2 + q3;
@@ -485,12 +484,8 @@ __device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64
                                             int warp, int lane, Sync sync)
 {
     const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
-    if (kf <= 2)
-        stage_x_f32_kf<CG, NORM, 2, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
-    else if (kf <= 4)
+    if (kf <= 4)
         stage_x_f32_kf<CG, NORM, 4, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
-    else if (kf <= 6)
-        stage_x_f32_kf<CG, NORM, 6, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
     else
         stage_x_f32_kf<CG, NORM, 8, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
 }

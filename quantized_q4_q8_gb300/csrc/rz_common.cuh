@@ -130,6 +130,26 @@ __device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsi
         : "memory");
 }
 
+// Position in a ring of n slots, advanced one stage at a time: the slot and the
+// parity of the slot's current phase (no division in the loops that walk it).
+struct RingPos {
+    int s;
+    unsigned par;
+};
+
+__device__ __forceinline__ RingPos ring_pos(int64_t k, int n)
+{
+    return RingPos{(int)(k % n), (unsigned)((k / n) & 1)};
+}
+
+__device__ __forceinline__ void ring_next(RingPos &r, int n)
+{
+    if (++r.s == n) {
+        r.s = 0;
+        r.par ^= 1u;
+    }
+}
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: wait for the preceding kernel in the stream
 // (no-op when launched without the attribute).
@@ -169,26 +189,31 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// Q8_1 code of one value given its block scale d and rd, the correctly rounded
-// 1/d (one per block): round half away from zero of the IEEE f32 quotient x / d,
-// clamped to [-127, 127]; 0 when d == 0.
-// y = x * rd is within 2.3e-5 of the IEEE quotient here: |x / d| <= 127 (1 + 2^-24)
-// because d = max|x| / 127, and 1/d, the product and the quotient each carry at
-// most 2^-24 relative rounding error.  round() is constant between consecutive
-// half-integers, so unless y lies within 2^-10 of one, y and the quotient round
-// to the same integer; next to a half-integer (and for a non-finite y, after an
-// overflowing 1/d) the quotient itself is formed and decides.
+// Q8_1 code of one value given its block scale d and rd, an approximation of
+// 1/d with relative error below 2^-21 (rcp_approx): round half away from zero of
+// the IEEE f32 quotient x / d, clamped to [-127, 127]; 0 when d == 0.
+// y = x * rd is within 127 (2^-21 + 2^-23) < 8e-5 of the IEEE quotient (|x / d| <=
+// 127 (1 + 2^-24) because d = max|x| / 127; the product and the quotient each
+// carry at most 2^-24 relative rounding error).  Round-half-away is constant
+// between consecutive half-integers, so when y lies more than 2^-10 away from
+// one -- |y - rint(y)| < 1/2 - 2^-10 -- rint(y) is the code (no tie is near); next
+// to a half-integer (and for a non-finite y) the quotient itself is formed
+// (out of line: rare) and decides.
+static __device__ __noinline__ float q8_exact_quotient(float x, float d) { return __fdiv_rn(x, d); }
+
+__device__ __forceinline__ float rcp_approx(float d)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
 __device__ __forceinline__ int q8_code(float x, float d, float rd)
 {
     if (d == 0.0f) return 0;
     const float y = __fmul_rn(x, rd);
-    const float t = fabsf(y);
-    const float f = t - floorf(t);
-    float r;
-    if (fabsf(f - 0.5f) >= 0.0009765625f)  // false for NaN
-        r = roundf(y);
-    else
-        r = roundf(__fdiv_rn(x, d));
+    float r = rintf(y);
+    if (!(fabsf(y - r) < 0.4990234375f)) r = roundf(q8_exact_quotient(x, d));  // 1/2 - 2^-10; NaN too
     r = fminf(fmaxf(r, -127.0f), 127.0f);
     return static_cast<int>(r);
 }
