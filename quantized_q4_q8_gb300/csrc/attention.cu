@@ -109,20 +109,28 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
 
 // grid (n_kv_heads, m, launch_chunks), chunk-major so that low chunks (needed by
 // every token) are scheduled first; 256 threads; CPT = head_dim / 32.
-// shared memory: qs [G][hd] | kn [hd] | vn [hd] | ps [G][64] | stat [G][2] | red [8][G][hd] | flag
+// The chunk's V rows are bulk-copied into shared memory as soon as the CTA
+// starts, so they arrive while the K rows (loaded into registers) are scored;
+// 4 CTAs fit on an SM (the grid of a decode step at a few thousand positions is
+// one wave).
+// shared memory: vbuf [64][hd] | qs [G][4][PER + 4] | kn [hd] | vn [hd] |
+//                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | mbarrier
 template <int CPT>
-__global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const AttnArgs a)
 {
     extern __shared__ __align__(16) float sm[];
     const int kvh = blockIdx.x, t = blockIdx.y, chunk = blockIdx.z;
     const int hd = a.head_dim, G = a.group;
-    float *qs = sm;
-    float *kn = qs + G * hd;
+    constexpr int PER = 8 * CPT;  // K values per thread (4 threads per row)
+    float *vbuf = sm;
+    float *qs = vbuf + kChunk * hd;
+    float *kn = qs + G * 4 * (PER + 4);
     float *vn = kn + hd;
     float *ps = vn + hd;
     float *stat = ps + G * kChunk;
-    float *red = stat + 2 * G + 2;  // keeps 8-byte alignment for the float2 reads below
+    float *red = stat + ((2 * G + 2 + 3) & ~3);  // 16-byte aligned for the float4 stores
     int *flag = reinterpret_cast<int *>(red + 8 * G * hd);
+    uint64_t *vbar = reinterpret_cast<uint64_t *>(flag + 2);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
     pdl_wait();
@@ -142,10 +150,35 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     const int64_t kv_base = (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
 
     if (n > 0) {
-        // rotated query heads of this kv head, and (owner) the new row
-        for (int g = 0; g < G; ++g)
-            rope_head(a.q + (int64_t)t * a.ld_qkv + (int64_t)(kvh * G + g) * hd, qs + g * hd, tab, hd,
-                      a.rope_mode, tid, kAttnThreads);
+        // V rows on their way into shared memory (the token's own row is taken
+        // from vn below: its cache copy is written by this CTA)
+        if (tid == 0) {
+            mbar_init(vbar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) mbar_arrive_expect_tx(vbar, (unsigned)(n * hd * 4));
+        if (tid < n)
+            bulk_g2s(vbuf + tid * hd, a.vc + kv_base + (int64_t)(c0 + tid) * a.kv_dim, (unsigned)(hd * 4), vbar);
+        // K rows into registers: 4 threads per cache row, hd/4 values each
+        const int j = tid >> 2, part = tid & 3;
+        float kv[PER];
+        if (j < n && c0 + j != pos) load_cols<PER>(a.kc + kv_base + (int64_t)(c0 + j) * a.kv_dim + part * PER, kv);
+
+        // rotated query heads of this kv head (padded per part: conflict-free
+        // float4 reads below), and (owner) the new row
+        for (int g = 0; g < G; ++g) {
+            const float *src = a.q + (int64_t)t * a.ld_qkv + (int64_t)(kvh * G + g) * hd;
+            const int half = hd / 2;
+            for (int i = tid; i < half; i += kAttnThreads) {
+                const int ia = a.rope_mode == 0 ? 2 * i : i;
+                const int ib = a.rope_mode == 0 ? 2 * i + 1 : i + half;
+                const float cs = tab[2 * i], sn = tab[2 * i + 1];
+                const float x0 = src[ia], x1 = src[ib];
+                qs[g * 4 * (PER + 4) + (ia / PER) * (PER + 4) + ia % PER] = x0 * cs - x1 * sn;
+                qs[g * 4 * (PER + 4) + (ib / PER) * (PER + 4) + ib % PER] = x0 * sn + x1 * cs;
+            }
+        }
         if (own) {
             const float *ks = a.k + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
             const float *vs = a.v + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
@@ -160,28 +193,26 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
                 kd[i] = kn[i];
                 vd[i] = vn[i];
             }
+            if (j < n && c0 + j == pos) load_cols<PER>(kn + part * PER, kv);
         }
 
-        // ---- scores: 4 threads per cache row, hd/4 = 8*CPT values each, all loads first
-        {
-            const int j = tid >> 2, part = tid & 3;
-            constexpr int PER = 8 * CPT;
-            float kv[PER];
+        // ---- scores
+        for (int g = 0; g < G; ++g) {
+            float dot = 0.0f;
             if (j < n) {
-                const float *kr = (c0 + j == pos) ? kn : a.kc + kv_base + (int64_t)(c0 + j) * a.kv_dim;
-                load_cols<PER>(kr + part * PER, kv);
-            }
-            for (int g = 0; g < G; ++g) {
-                float dot = 0.0f;
-                if (j < n) {
-                    const float *qg = qs + g * hd + part * PER;
+                const float *qg = qs + g * 4 * (PER + 4) + part * (PER + 4);
 #pragma unroll
-                    for (int e = 0; e < PER; ++e) dot = fmaf(qg[e], kv[e], dot);
+                for (int e = 0; e < PER; e += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(qg + e);
+                    dot = fmaf(q4.x, kv[e], dot);
+                    dot = fmaf(q4.y, kv[e + 1], dot);
+                    dot = fmaf(q4.z, kv[e + 2], dot);
+                    dot = fmaf(q4.w, kv[e + 3], dot);
                 }
-                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                if (part == 0 && j < n) ps[g * kChunk + j] = dot * scale;
             }
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            if (part == 0 && j < n) ps[g * kChunk + j] = dot * scale;
         }
         __syncthreads();
         // ---- chunk softmax statistics (warp per query head)
@@ -199,44 +230,50 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
                 stat[2 * g + 1] = sum;
             }
         }
+        // the V rows have landed (bounded wait; on expiry the copies are waited
+        // out again before the CTA may leave)
+        if (!mbar_wait(vbar, 0)) {
+            if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
+            if (!mbar_wait(vbar, 0) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
+        }
         __syncthreads();
-        // ---- weighted values: 8 row groups x 32 column threads, all loads first
+        // ---- weighted values: 8 row groups x 32 column threads, CPT columns each
         {
             const int rg = warp, col = lane;
-            float v[8][CPT];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int j = rg + 8 * r;
-#pragma unroll
-                for (int e = 0; e < CPT; ++e) v[r][e] = 0.0f;
-                if (j < n) {
-                    const float *vr = (c0 + j == pos) ? vn : a.vc + kv_base + (int64_t)(c0 + j) * a.kv_dim;
-                    load_cols<CPT>(vr + col * CPT, v[r]);
-                }
-            }
             for (int g = 0; g < G; ++g) {
                 float o[CPT];
 #pragma unroll
                 for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int j = rg + 8 * r;
-                    const float p = j < n ? ps[g * kChunk + j] : 0.0f;
+                    const int jj = rg + 8 * r;
+                    if (jj < n) {
+                        float vv[CPT];
+                        load_cols<CPT>(((c0 + jj == pos) ? vn : vbuf + jj * hd) + col * CPT, vv);
+                        const float p = ps[g * kChunk + jj];
 #pragma unroll
-                    for (int e = 0; e < CPT; ++e) o[e] = fmaf(p, v[r][e], o[e]);
+                        for (int e = 0; e < CPT; ++e) o[e] = fmaf(p, vv[e], o[e]);
+                    }
                 }
+                float *rd = red + (rg * G + g) * hd + col * CPT;
+                if (CPT % 4 == 0) {
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) red[(rg * G + g) * hd + col * CPT + e] = o[e];
+                    for (int e = 0; e < CPT; e += 4)
+                        *reinterpret_cast<float4 *>(rd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) rd[e] = o[e];
+                }
             }
         }
         __syncthreads();
         // fixed-order sum over the 8 row groups -> partial record
         for (int i = tid; i < G * hd; i += kAttnThreads) {
             const int g = i / hd, dd = i % hd;
-            float s = 0.0f;
+            float s8 = 0.0f;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) s += red[(r * G + g) * hd + dd];
-            part_rec(a, t, kvh, chunk, g)[2 + dd] = s;
+            for (int r = 0; r < 8; ++r) s8 += red[(r * G + g) * hd + dd];
+            part_rec(a, t, kvh, chunk, g)[2 + dd] = s8;
         }
         for (int g = tid; g < G; g += kAttnThreads) {
             float *rec = part_rec(a, t, kvh, chunk, g);
@@ -355,9 +392,11 @@ int attention_chunk_len(int, int, int) { return kChunk; }
 
 size_t attention_smem_bytes(int group, int head_dim, int)
 {
-    return ((size_t)group * head_dim + 2 * (size_t)head_dim + (size_t)group * kChunk + 2 * (size_t)group + 2 +
-            8 * (size_t)group * head_dim + 4) *
-           sizeof(float);
+    const size_t per = (size_t)head_dim / 4;  // K values per thread
+    return ((size_t)kChunk * head_dim + (size_t)group * 4 * (per + 4) + 2 * (size_t)head_dim +
+            (size_t)group * kChunk + ((2 * (size_t)group + 2 + 3) & ~(size_t)3) + 8 * (size_t)group * head_dim) *
+               sizeof(float) +
+           16 + 16;  // flag (+ pad), mbarrier
 }
 
 cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s)
