@@ -279,6 +279,9 @@ rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, Laye
     if (w->n_heads / w->n_kv_heads > 16) return fail(RZ_ERR_UNSUPPORTED, "%s: more than 16 query heads per kv head", fn);
     if (w->head_dim < 32 || w->head_dim > 256 || w->head_dim % 32)
         return fail(RZ_ERR_SHAPE, "%s: head_dim=%d (multiple of 32 in [32, 256])", fn, w->head_dim);
+    if (attention_smem_bytes(w->n_heads / w->n_kv_heads, w->head_dim, 0) > dev_info().smem_optin)
+        return fail(RZ_ERR_UNSUPPORTED, "%s: head_dim=%d with %d query heads per kv head needs more shared memory "
+                    "than a CTA has", fn, w->head_dim, w->n_heads / w->n_kv_heads);
     if (w->inter < 256 || w->inter % 256) return fail(RZ_ERR_SHAPE, "%s: inter=%d is not a multiple of 256", fn, w->inter);
     if (!(w->eps >= 0.0f) || !(w->rope_theta > 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps/rope_theta", fn);
     if (w->rope_mode != 0 && w->rope_mode != 1) return fail(RZ_ERR_INVALID_ARG, "%s: rope_mode=%d", fn, w->rope_mode);
@@ -398,6 +401,9 @@ rz_status rz_attention_decode(const float *q, const float *k, const float *v, in
     RZ_TRY(check_position(positions, position, kv->max_seq, fn));
     const size_t need = rz_attention_workspace_bytes(m, n_heads, n_kv_heads, head_dim, kv->max_seq);
     RZ_TRY(check_device());
+    if (attention_smem_bytes(n_heads / n_kv_heads, head_dim, 0) > dev_info().smem_optin)
+        return fail(RZ_ERR_UNSUPPORTED, "%s: head_dim=%d with %d query heads per kv head needs more shared memory "
+                    "than a CTA has", fn, head_dim, n_heads / n_kv_heads);
     RZ_TRY(check_ws(workspace, ws_bytes, need, fn));
     LayerDesc L{};
     L.n_heads = n_heads;

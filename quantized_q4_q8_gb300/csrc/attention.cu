@@ -109,28 +109,31 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
 
 // grid (n_kv_heads, m, launch_chunks), chunk-major so that low chunks (needed by
 // every token) are scheduled first; 256 threads; CPT = head_dim / 32.
-// The chunk's V rows are bulk-copied into shared memory as soon as the CTA
-// starts, so they arrive while the K rows (loaded into registers) are scored;
-// 4 CTAs fit on an SM (the grid of a decode step at a few thousand positions is
-// one wave).
-// shared memory: vbuf [64][hd] | qs [G][4][PER + 4] | kn [hd] | vn [hd] |
-//                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | mbarrier
+// The chunk's K and V rows are bulk-copied into shared memory (one copy per row,
+// completion counted on two mbarriers) as soon as the CTA starts: the copy engine
+// keeps the whole chunk in flight, which per-thread loads cannot (the SM's limit
+// on outstanding misses held them near 2 TB/s).  Scores: warp w takes rows w,
+// w + 8, ..., lane l dims l + 32 e of each (conflict-free), with the rotated query
+// heads in shared memory.
+// shared memory: kbuf [64][hd] | vbuf [64][hd] | qs [G][hd] | kn [hd] | vn [hd] |
+//                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | 2 mbarriers
 template <int CPT>
-__global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const AttnArgs a)
 {
     extern __shared__ __align__(16) float sm[];
     const int kvh = blockIdx.x, t = blockIdx.y, chunk = blockIdx.z;
     const int hd = a.head_dim, G = a.group;
-    constexpr int PER = 8 * CPT;  // K values per thread (4 threads per row)
-    float *vbuf = sm;
+    float *kbuf = sm;
+    float *vbuf = kbuf + kChunk * hd;
     float *qs = vbuf + kChunk * hd;
-    float *kn = qs + G * 4 * (PER + 4);
+    float *kn = qs + G * hd;
     float *vn = kn + hd;
     float *ps = vn + hd;
     float *stat = ps + G * kChunk;
     float *red = stat + ((2 * G + 2 + 3) & ~3);  // 16-byte aligned for the float4 stores
     int *flag = reinterpret_cast<int *>(red + 8 * G * hd);
-    uint64_t *vbar = reinterpret_cast<uint64_t *>(flag + 2);
+    uint64_t *kbar = reinterpret_cast<uint64_t *>(flag + 2);
+    uint64_t *vbar = kbar + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
     pdl_wait();
@@ -150,35 +153,28 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
     const int64_t kv_base = (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
 
     if (n > 0) {
-        // V rows on their way into shared memory (the token's own row is taken
-        // from vn below: its cache copy is written by this CTA)
+        // K and V rows on their way into shared memory (the token's own row is taken
+        // from kn / vn below: its cache copy is written by this CTA)
         if (tid == 0) {
+            mbar_init(kbar, 1);
             mbar_init(vbar, 1);
             fence_mbar_init();
         }
         __syncthreads();
-        if (tid == 0) mbar_arrive_expect_tx(vbar, (unsigned)(n * hd * 4));
-        if (tid < n)
-            bulk_g2s(vbuf + tid * hd, a.vc + kv_base + (int64_t)(c0 + tid) * a.kv_dim, (unsigned)(hd * 4), vbar);
-        // K rows into registers: 4 threads per cache row, hd/4 values each
-        const int j = tid >> 2, part = tid & 3;
-        float kv[PER];
-        if (j < n && c0 + j != pos) load_cols<PER>(a.kc + kv_base + (int64_t)(c0 + j) * a.kv_dim + part * PER, kv);
-
-        // rotated query heads of this kv head (padded per part: conflict-free
-        // float4 reads below), and (owner) the new row
-        for (int g = 0; g < G; ++g) {
-            const float *src = a.q + (int64_t)t * a.ld_qkv + (int64_t)(kvh * G + g) * hd;
-            const int half = hd / 2;
-            for (int i = tid; i < half; i += kAttnThreads) {
-                const int ia = a.rope_mode == 0 ? 2 * i : i;
-                const int ib = a.rope_mode == 0 ? 2 * i + 1 : i + half;
-                const float cs = tab[2 * i], sn = tab[2 * i + 1];
-                const float x0 = src[ia], x1 = src[ib];
-                qs[g * 4 * (PER + 4) + (ia / PER) * (PER + 4) + ia % PER] = x0 * cs - x1 * sn;
-                qs[g * 4 * (PER + 4) + (ib / PER) * (PER + 4) + ib % PER] = x0 * sn + x1 * cs;
-            }
+        if (tid == 0) {
+            mbar_arrive_expect_tx(kbar, (unsigned)(n * hd * 4));
+            mbar_arrive_expect_tx(vbar, (unsigned)(n * hd * 4));
         }
+        if (tid < n)
+            bulk_g2s(kbuf + tid * hd, a.kc + kv_base + (int64_t)(c0 + tid) * a.kv_dim, (unsigned)(hd * 4), kbar);
+        else if (tid >= kChunk && tid - kChunk < n)
+            bulk_g2s(vbuf + (tid - kChunk) * hd, a.vc + kv_base + (int64_t)(c0 + tid - kChunk) * a.kv_dim,
+                     (unsigned)(hd * 4), vbar);
+
+        // rotated query heads of this kv head, and (owner) the new row
+        for (int g = 0; g < G; ++g)
+            rope_head(a.q + (int64_t)t * a.ld_qkv + (int64_t)(kvh * G + g) * hd, qs + g * hd, tab, hd, a.rope_mode,
+                      tid, kAttnThreads);
         if (own) {
             const float *ks = a.k + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
             const float *vs = a.v + (int64_t)t * a.ld_qkv + (int64_t)kvh * hd;
@@ -193,26 +189,39 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
                 kd[i] = kn[i];
                 vd[i] = vn[i];
             }
-            if (j < n && c0 + j == pos) load_cols<PER>(kn + part * PER, kv);
+        }
+        // the K rows have landed (bounded wait; on expiry the copies are waited
+        // out again before the CTA may leave)
+        if (!mbar_wait(kbar, 0)) {
+            if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
+            if (!mbar_wait(kbar, 0) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
         }
 
-        // ---- scores
+        // ---- scores: warp w rows w + 8 r, lane l dims l + 32 e
         for (int g = 0; g < G; ++g) {
-            float dot = 0.0f;
-            if (j < n) {
-                const float *qg = qs + g * 4 * (PER + 4) + part * (PER + 4);
+            float qv[CPT];
 #pragma unroll
-                for (int e = 0; e < PER; e += 4) {
-                    const float4 q4 = *reinterpret_cast<const float4 *>(qg + e);
-                    dot = fmaf(q4.x, kv[e], dot);
-                    dot = fmaf(q4.y, kv[e + 1], dot);
-                    dot = fmaf(q4.z, kv[e + 2], dot);
-                    dot = fmaf(q4.w, kv[e + 3], dot);
+            for (int e = 0; e < CPT; ++e) qv[e] = qs[g * hd + 32 * e + lane];
+            float dot[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int jj = warp + 8 * r;
+                const float *kr = (c0 + jj == pos) ? kn : kbuf + jj * hd;
+                dot[r] = 0.0f;
+                if (jj < n) {
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) dot[r] = fmaf(qv[e], kr[32 * e + lane], dot[r]);
                 }
             }
-            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-            if (part == 0 && j < n) ps[g * kChunk + j] = dot * scale;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (warp + 8 * r < n) ps[g * kChunk + warp + 8 * r] = dot[r] * scale;
+            }
         }
         __syncthreads();
         // ---- chunk softmax statistics (warp per query head)
@@ -230,8 +239,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
                 stat[2 * g + 1] = sum;
             }
         }
-        // the V rows have landed (bounded wait; on expiry the copies are waited
-        // out again before the CTA may leave)
+        // the V rows have landed
         if (!mbar_wait(vbar, 0)) {
             if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
             if (!mbar_wait(vbar, 0) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
@@ -329,11 +337,17 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
     for (int i = tid; i < G * hd; i += kAttnThreads) {
         const int g = i / hd, dd = i % hd;
         float acc = 0.0f;
-#pragma unroll 8
-        for (int c = 0; c < nc; ++c) {
-            const float w = wts[g * kChunk + c];
-            if (w != 0.0f) acc = fmaf(__ldcg(part_rec(a, t, kvh, c, g) + 2 + dd), w, acc);
+        // eight records' loads in flight at a time (every record c < nc is written and
+        // finite; a zero weight adds exactly nothing), summed in chunk order
+        int c = 0;
+        for (; c + 8 <= nc; c += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(part_rec(a, t, kvh, c + u, g) + 2 + dd);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc = fmaf(v[u], wts[g * kChunk + c + u], acc);
         }
+        for (; c < nc; ++c) acc = fmaf(__ldcg(part_rec(a, t, kvh, c, g) + 2 + dd), wts[g * kChunk + c], acc);
         outv[g * hd + dd] = acc * stat[2 * g];
     }
     __syncthreads();
@@ -392,11 +406,10 @@ int attention_chunk_len(int, int, int) { return kChunk; }
 
 size_t attention_smem_bytes(int group, int head_dim, int)
 {
-    const size_t per = (size_t)head_dim / 4;  // K values per thread
-    return ((size_t)kChunk * head_dim + (size_t)group * 4 * (per + 4) + 2 * (size_t)head_dim +
+    return (2 * (size_t)kChunk * head_dim + (size_t)group * head_dim + 2 * (size_t)head_dim +
             (size_t)group * kChunk + ((2 * (size_t)group + 2 + 3) & ~(size_t)3) + 8 * (size_t)group * head_dim) *
                sizeof(float) +
-           16 + 16;  // flag (+ pad), mbarrier
+           16 + 16;  // flag (+ pad), two mbarriers
 }
 
 cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s)
