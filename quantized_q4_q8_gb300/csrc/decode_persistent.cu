@@ -999,6 +999,14 @@ int env_int(const char *name, int dflt)
     return (v && *v) ? atoi(v) : dflt;
 }
 
+// Packs per slot.  With one row per pack the rows are worked in pairs, so an
+// odd count above one drops to the even count below it (an odd count leaves the
+// last pair with a single row, worked twice).
+int64_t even_packs(int64_t per, bool one_row)
+{
+    return (one_row && per > 1 && (per & 1)) ? per - 1 : per;
+}
+
 HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin)
 {
     HostPlan h{};
@@ -1006,12 +1014,14 @@ HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int q_pad = (q_dim + 255) / 256 * 256;
     int64_t pack[4];
+    bool rpp1[4];
     int64_t xr = 0;
     for (int k = 0; k < 4; ++k) {
         int64_t units, in_dim;
         int R;
         gemv_dims(k, q_dim, kv_dim, L.hidden, L.hidden_pad, q_pad, L.inter, units, in_dim, R);
         const int nsb = (int)(in_dim / 256);
+        rpp1[k] = pack_rows_for(nsb) == 1;
         pack[k] = (int64_t)R * pack_rows_for(nsb) * nsb * kSB;
         xr = std::max(xr, x_smem_bytes(m, in_dim));
     }
@@ -1031,7 +1041,7 @@ HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin
                 fits = false;
                 break;
             }
-            fill = std::min(fill, (double)(S / pack[k] * pack[k]) / S);
+            fill = std::min(fill, (double)(even_packs(S / pack[k], rpp1[k]) * pack[k]) / S);
         }
         if (!fits) continue;
         const double score = (double)ns * S * fill;
@@ -1042,7 +1052,7 @@ HostPlan host_plan(const LayerDesc &L, int64_t m, int max_seq, size_t smem_optin
         }
     }
     if (best <= 0.0) return h;
-    for (int k = 0; k < 4; ++k) h.ps[k] = (int)(h.slot_bytes / pack[k]);
+    for (int k = 0; k < 4; ++k) h.ps[k] = (int)even_packs(h.slot_bytes / pack[k], rpp1[k]);
     h.smem = (size_t)h.n_slots * h.slot_bytes + (size_t)fixed;
     h.ok = h.smem <= smem_optin;
     return h;

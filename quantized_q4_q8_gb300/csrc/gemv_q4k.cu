@@ -410,6 +410,11 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
     a.PS = (int)std::max<int64_t>(1, kStageTarget / pack);
+    if (m == 1 && a.rpp == 1 && (a.PS & 1)) {
+        // row pairs: an even pack count per stage, so that no pair is cut short
+        if ((a.PS + 1) * pack <= kStageTarget * 5 / 4) a.PS += 1;
+        else if (a.PS > 1) a.PS -= 1;
+    }
     a.stage_bytes = (int)(a.PS * pack);
     const int64_t xbytes = x_smem_bytes(m, in_dim);
     a.x_smem = (xbytes <= kXSmemMax || f32in) ? 1 : 0;
