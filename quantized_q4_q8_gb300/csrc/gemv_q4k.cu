@@ -8,10 +8,11 @@
 //
 // GB300 design.  The kernel streams 144-byte super-blocks from HBM; compute is
 // a few dp4a per byte.  One CTA per SM owns a contiguous range of rows.  A
-// producer warp keeps a ring of ~16 KB shared-memory stages full with the 1-D
+// producer warp keeps a ring of 16-32 KB shared-memory stages full with the 1-D
 // bulk copy engine (cp.async.bulk, completion counted on an mbarrier), so the
-// bytes in flight live in shared memory, not registers, and it prefetches the
-// rest of the CTA's rows into L2 (cp.async.bulk.prefetch.L2) at once.  A stage
+// bytes in flight live in shared memory, not registers.  (Prefetching the rest
+// of the CTA's rows into L2 up front was measured slower: it queues ahead of
+// the ring's own copies and of the activation loads.)  A stage
 // holds whole "packs" (one row, or 8/nsb rows when a row has fewer than 8
 // super-blocks); pack i goes to consumer warp i % 16.  Every consumer warp
 // passes every stage in order -- waits for it, works its own packs in it,
@@ -42,6 +43,7 @@ constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kCtaSmem = 200 * 1024;
 constexpr int kStageTarget = 16 * 1024;
+constexpr int kStageTargetFused = 32 * 1024;
 constexpr int kXSmemMax = 48 * 1024;
 constexpr int kMaxStages = 16;
 
@@ -115,26 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            // everything beyond the first NS stages goes to L2 right away, so HBM
-            // stays busy even while the ring is full
-            for (int64_t k = a.NS; k < nstages; ++k) {
-                const int64_t u0 = r0 + k * a.PS * a.rpp;
-                const int n = (int)min((int64_t)a.PS * a.rpp, r1 - u0);
-                if (EPI == EPI_SWIGLU) {
-                    prefetch_l2(a.w[0] + u0 * a.row_bytes, (unsigned)(n * a.row_bytes));
-                    prefetch_l2(a.w[1] + u0 * a.row_bytes, (unsigned)(n * a.row_bytes));
-                } else {
-                    int r = 0;
-                    while (r < n) {
-                        const int64_t u = u0 + r;
-                        const int kseg = seg_of(a, u);
-                        const int run = (int)min((int64_t)(n - r), a.seg_begin[kseg + 1] - u);
-                        prefetch_l2(a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
-                                    (unsigned)(run * a.row_bytes));
-                        r += run;
-                    }
-                }
-            }
             int64_t k = 0;
             bool ok = true;
             RingPos rp{0, 0u};
@@ -409,10 +391,15 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     a.err = dev_error_word();
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
-    a.PS = (int)std::max<int64_t>(1, kStageTarget / pack);
+    // Small stages for the plain GEMV (Q8_1 in, store out): its consumers start
+    // at once, so the first stage's arrival is on the critical path.  The fused
+    // kernels first wait for the previous kernel and stage their input, while the
+    // ring fills: larger stages there mean fewer barrier round trips.
+    const int64_t tgt = (f32in || epilogue != EPI_STORE) ? kStageTargetFused : kStageTarget;
+    a.PS = (int)std::max<int64_t>(1, tgt / pack);
     if (m == 1 && a.rpp == 1 && (a.PS & 1)) {
         // row pairs: an even pack count per stage, so that no pair is cut short
-        if ((a.PS + 1) * pack <= kStageTarget * 5 / 4) a.PS += 1;
+        if ((a.PS + 1) * pack <= tgt * 5 / 4) a.PS += 1;
         else if (a.PS > 1) a.PS -= 1;
     }
     a.stage_bytes = (int)(a.PS * pack);
