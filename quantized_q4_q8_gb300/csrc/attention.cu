@@ -15,18 +15,25 @@
 // stack builds it once per step and every layer reuses it.
 //
 // Attention is split over the sequence in chunks of 64 cache rows (flash-
-// decoding style).  CTA (chunk, kv head, token) rotates its query heads, and the
-// CTA whose chunk holds the token's own row rotates k, writes k and v to the
-// cache and uses them from shared memory.  The scores and the weighted values are
-// computed with every load of the chunk issued before it is used (32 KB of K,
-// then 32 KB of V in flight per CTA at head_dim 128), so HBM rather than latency
-// bounds the kernel.  Each CTA leaves its chunk max, exp-sum and unnormalised
-// weighted values; the last CTA of each (token, kv head) -- found with an atomic
+// decoding style).  The grid is one wave: CTA (z, kv head, token) works chunks
+// z, z + Z, ... in turn, Z sized so that every CTA is resident at once and the
+// chunks are spread evenly.  It rotates its query heads once, and the CTA that
+// works the chunk holding the token's own row rotates k, writes k and v to the
+// cache and uses them from shared memory.  A chunk's K and V rows are bulk-
+// copied into shared memory (32 KB each at head_dim 128), and each buffer is
+// refilled with the CTA's next chunk as soon as it has been read, so the copies
+// of the next chunk overlap the work on this one and HBM rather than latency or
+// a second wave of CTAs bounds the kernel.  Each CTA leaves per chunk the max,
+// exp-sum and unnormalised weighted values; the CTA that completes the last
+// chunks of a (token, kv head) -- found with an atomic
 // counter, no spinning -- merges the chunks with the log-sum-exp rule and writes
 // the f32 output and its Q8_1 quantisation (head_dim is a multiple of 32, so Q8_1
 // blocks never straddle heads) for the O projection.  The counter is reset by the
 // merging CTA.
 #include <math.h>
+
+#include <algorithm>
+#include <mutex>
 
 #include "rz_common.cuh"
 #include "rz_kernels.h"
@@ -107,10 +114,9 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
     }
 }
 
-// grid (n_kv_heads, m, launch_chunks), chunk-major so that low chunks (needed by
-// every token) are scheduled first; 256 threads; CPT = head_dim / 32.
-// The chunk's K and V rows are bulk-copied into shared memory (one copy per row,
-// completion counted on two mbarriers) as soon as the CTA starts: the copy engine
+// grid (n_kv_heads, m, Z), Z <= launch_chunks chunk slots; 256 threads; CPT =
+// head_dim / 32.  A chunk's K and V rows are bulk-copied into shared memory (one
+// copy per row, completion counted on two mbarriers, one phase per chunk): the copy engine
 // keeps the whole chunk in flight, which per-thread loads cannot (the SM's limit
 // on outstanding misses held them near 2 TB/s).  Scores: warp w takes rows w,
 // w + 8, ..., lane l dims l + 32 e of each (conflict-free), with the rotated query
@@ -143,33 +149,46 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     // chunks holding rows of this token; after a bad position chunk 0 alone takes
     // part and the merge writes zeros
     const int nc = pos_ok ? min(a.n_chunks, pos / kChunk + 1) : 1;
-    if (chunk >= nc) return;
-    const int c0 = chunk * kChunk;
-    const int n = pos_ok ? max(0, min(kChunk, pos + 1 - c0)) : 0;
-    const bool own = pos_ok && pos >= c0 && pos < c0 + kChunk;  // this chunk holds the new row
+    // this CTA works chunks chunk, chunk + Z, ... below nc, in that order
+    const int Z = gridDim.z;
+    const int mine = chunk < nc ? (nc - 1 - chunk) / Z + 1 : 0;
+    if (mine == 0) return;
     if (!pos_ok && chunk == 0 && kvh == 0 && tid == 0) set_error(a.err, DEV_BAD_POSITION);
     const float *tab = a.rope_tab + (int64_t)t * (hd / 2) * 2;
     const float scale = 1.0f / sqrtf((float)hd);
     const int64_t kv_base = (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
+    auto rows_of = [&](int c) { return pos_ok ? max(0, min(kChunk, pos + 1 - c * kChunk)) : 0; };
+    const int own_chunk = pos / kChunk;  // the chunk holding the new row
+    const bool own = pos_ok && own_chunk >= chunk && (own_chunk - chunk) % Z == 0;
 
-    if (n > 0) {
-        // K and V rows on their way into shared memory (the token's own row is taken
-        // from kn / vn below: its cache copy is written by this CTA)
+    if (rows_of(chunk) > 0) {
+        // K and V rows of chunk c on their way into kbuf / vbuf, one bulk copy per
+        // row (the token's own row is taken from kn / vn: its cache copy is written
+        // by this CTA).  A buffer is refilled for the CTA's next chunk as soon as
+        // every thread is done with it, so the next chunk streams in meanwhile.
+        auto issue_k = [&](int c) {
+            const int nr = rows_of(c);
+            if (tid == 0) mbar_arrive_expect_tx(kbar, (unsigned)(nr * hd * 4));
+            if (tid < nr)
+                bulk_g2s(kbuf + tid * hd, a.kc + kv_base + (int64_t)(c * kChunk + tid) * a.kv_dim,
+                         (unsigned)(hd * 4), kbar);
+        };
+        auto issue_v = [&](int c) {
+            const int nr = rows_of(c);
+            if (tid == 0) mbar_arrive_expect_tx(vbar, (unsigned)(nr * hd * 4));
+            if (tid >= kChunk && tid - kChunk < nr)
+                bulk_g2s(vbuf + (tid - kChunk) * hd,
+                         a.vc + kv_base + (int64_t)(c * kChunk + tid - kChunk) * a.kv_dim, (unsigned)(hd * 4),
+                         vbar);
+        };
         if (tid == 0) {
             mbar_init(kbar, 1);
             mbar_init(vbar, 1);
             fence_mbar_init();
         }
         __syncthreads();
-        if (tid == 0) {
-            mbar_arrive_expect_tx(kbar, (unsigned)(n * hd * 4));
-            mbar_arrive_expect_tx(vbar, (unsigned)(n * hd * 4));
-        }
-        if (tid < n)
-            bulk_g2s(kbuf + tid * hd, a.kc + kv_base + (int64_t)(c0 + tid) * a.kv_dim, (unsigned)(hd * 4), kbar);
-        else if (tid >= kChunk && tid - kChunk < n)
-            bulk_g2s(vbuf + (tid - kChunk) * hd, a.vc + kv_base + (int64_t)(c0 + tid - kChunk) * a.kv_dim,
-                     (unsigned)(hd * 4), vbar);
+        issue_k(chunk);
+        issue_v(chunk);
 
         // rotated query heads of this kv head, and (owner) the new row
         for (int g = 0; g < G; ++g)
@@ -190,103 +209,114 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
                 vd[i] = vn[i];
             }
         }
-        // the K rows have landed (bounded wait; on expiry the copies are waited
-        // out again before the CTA may leave)
-        if (!mbar_wait(kbar, 0)) {
-            if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
-            if (!mbar_wait(kbar, 0) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
-        }
 
-        // ---- scores: warp w rows w + 8 r, lane l dims l + 32 e
-        for (int g = 0; g < G; ++g) {
-            float qv[CPT];
-#pragma unroll
-            for (int e = 0; e < CPT; ++e) qv[e] = qs[g * hd + 32 * e + lane];
-            float dot[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int jj = warp + 8 * r;
-                const float *kr = (c0 + jj == pos) ? kn : kbuf + jj * hd;
-                dot[r] = 0.0f;
-                if (jj < n) {
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e) dot[r] = fmaf(qv[e], kr[32 * e + lane], dot[r]);
-                }
+        bool ok = true;
+        for (int it = 0, c = chunk; it < mine && ok; ++it, c += Z) {
+            const unsigned par = (unsigned)(it & 1);
+            const int c0 = c * kChunk, n = rows_of(c);
+            // the K rows have landed (bounded wait; on expiry the copies are waited
+            // out again before the CTA may leave, and no further chunk is started)
+            if (!mbar_wait(kbar, par)) {
+                if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
+                if (!mbar_wait(kbar, par) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
+                ok = false;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int r = 0; r < 8; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (warp + 8 * r < n) ps[g * kChunk + warp + 8 * r] = dot[r] * scale;
-            }
-        }
-        __syncthreads();
-        // ---- chunk softmax statistics (warp per query head)
-        for (int g = warp; g < G; g += kAttnThreads / 32) {
-            const float v0 = lane < n ? ps[g * kChunk + lane] : -INFINITY;
-            const float v1 = lane + 32 < n ? ps[g * kChunk + lane + 32] : -INFINITY;
-            const float mx = warp_max(fmaxf(v0, v1));
-            const float p0 = lane < n ? expf(v0 - mx) : 0.0f;
-            const float p1 = lane + 32 < n ? expf(v1 - mx) : 0.0f;
-            ps[g * kChunk + lane] = p0;
-            ps[g * kChunk + lane + 32] = p1;
-            const float sum = warp_sum(p0 + p1);
-            if (lane == 0) {
-                stat[2 * g] = mx;
-                stat[2 * g + 1] = sum;
-            }
-        }
-        // the V rows have landed
-        if (!mbar_wait(vbar, 0)) {
-            if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
-            if (!mbar_wait(vbar, 0) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
-        }
-        __syncthreads();
-        // ---- weighted values: 8 row groups x 32 column threads, CPT columns each
-        {
-            const int rg = warp, col = lane;
+
+            // ---- scores: warp w rows w + 8 r, lane l dims l + 32 e
             for (int g = 0; g < G; ++g) {
-                float o[CPT];
+                float qv[CPT];
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
+                for (int e = 0; e < CPT; ++e) qv[e] = qs[g * hd + 32 * e + lane];
+                float dot[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int jj = rg + 8 * r;
+                    const int jj = warp + 8 * r;
+                    const float *kr = (c0 + jj == pos) ? kn : kbuf + jj * hd;
+                    dot[r] = 0.0f;
                     if (jj < n) {
-                        float vv[CPT];
-                        load_cols<CPT>(((c0 + jj == pos) ? vn : vbuf + jj * hd) + col * CPT, vv);
-                        const float p = ps[g * kChunk + jj];
 #pragma unroll
-                        for (int e = 0; e < CPT; ++e) o[e] = fmaf(p, vv[e], o[e]);
+                        for (int e = 0; e < CPT; ++e) dot[r] = fmaf(qv[e], kr[32 * e + lane], dot[r]);
                     }
                 }
-                float *rd = red + (rg * G + g) * hd + col * CPT;
-                if (CPT % 4 == 0) {
 #pragma unroll
-                    for (int e = 0; e < CPT; e += 4)
-                        *reinterpret_cast<float4 *>(rd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                } else {
+                for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                    for (int e = 0; e < CPT; ++e) rd[e] = o[e];
+                    for (int r = 0; r < 8; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+                if (lane == 0) {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        if (warp + 8 * r < n) ps[g * kChunk + warp + 8 * r] = dot[r] * scale;
                 }
             }
-        }
-        __syncthreads();
-        // fixed-order sum over the 8 row groups -> partial record
-        for (int i = tid; i < G * hd; i += kAttnThreads) {
-            const int g = i / hd, dd = i % hd;
-            float s8 = 0.0f;
+            __syncthreads();
+            if (ok && it + 1 < mine) issue_k(c + Z);  // kbuf is free
+            // ---- chunk softmax statistics (warp per query head)
+            for (int g = warp; g < G; g += kAttnThreads / 32) {
+                const float v0 = lane < n ? ps[g * kChunk + lane] : -INFINITY;
+                const float v1 = lane + 32 < n ? ps[g * kChunk + lane + 32] : -INFINITY;
+                const float mx = warp_max(fmaxf(v0, v1));
+                const float p0 = lane < n ? expf(v0 - mx) : 0.0f;
+                const float p1 = lane + 32 < n ? expf(v1 - mx) : 0.0f;
+                ps[g * kChunk + lane] = p0;
+                ps[g * kChunk + lane + 32] = p1;
+                const float sum = warp_sum(p0 + p1);
+                if (lane == 0) {
+                    stat[2 * g] = mx;
+                    stat[2 * g + 1] = sum;
+                }
+            }
+            // the V rows have landed
+            if (!mbar_wait(vbar, par)) {
+                if (tid == 0) set_error(a.err, DEV_TIMEOUT_ATTN);
+                if (!mbar_wait(vbar, par) && tid == 0) set_error(a.err, DEV_TIMEOUT_DRAIN);
+                ok = false;
+            }
+            __syncthreads();
+            // ---- weighted values: 8 row groups x 32 column threads, CPT columns each
+            {
+                const int rg = warp, col = lane;
+                for (int g = 0; g < G; ++g) {
+                    float o[CPT];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) s8 += red[(r * G + g) * hd + dd];
-            part_rec(a, t, kvh, chunk, g)[2 + dd] = s8;
-        }
-        for (int g = tid; g < G; g += kAttnThreads) {
-            float *rec = part_rec(a, t, kvh, chunk, g);
-            rec[0] = stat[2 * g];
-            rec[1] = stat[2 * g + 1];
+                    for (int e = 0; e < CPT; ++e) o[e] = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int jj = rg + 8 * r;
+                        if (jj < n) {
+                            float vv[CPT];
+                            load_cols<CPT>(((c0 + jj == pos) ? vn : vbuf + jj * hd) + col * CPT, vv);
+                            const float p = ps[g * kChunk + jj];
+#pragma unroll
+                            for (int e = 0; e < CPT; ++e) o[e] = fmaf(p, vv[e], o[e]);
+                        }
+                    }
+                    float *rd = red + (rg * G + g) * hd + col * CPT;
+                    if (CPT % 4 == 0) {
+#pragma unroll
+                        for (int e = 0; e < CPT; e += 4)
+                            *reinterpret_cast<float4 *>(rd + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) rd[e] = o[e];
+                    }
+                }
+            }
+            __syncthreads();
+            if (ok && it + 1 < mine) issue_v(c + Z);  // vbuf is free
+            // fixed-order sum over the 8 row groups -> partial record of chunk c
+            for (int i = tid; i < G * hd; i += kAttnThreads) {
+                const int g = i / hd, dd = i % hd;
+                float s8 = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) s8 += red[(r * G + g) * hd + dd];
+                part_rec(a, t, kvh, c, g)[2 + dd] = s8;
+            }
+            for (int g = tid; g < G; g += kAttnThreads) {
+                float *rec = part_rec(a, t, kvh, c, g);
+                rec[0] = stat[2 * g];
+                rec[1] = stat[2 * g + 1];
+            }
+            __syncthreads();  // ps, stat and red are reused by the next chunk
         }
     } else {
         for (int g = tid; g < G; g += kAttnThreads) {
@@ -301,8 +331,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     __syncthreads();
     if (tid == 0) {
         int *cnt = a.counters + (int64_t)t * a.n_kv_heads + kvh;
-        const int prev = atomicAdd(cnt, 1);
-        const int last = (prev == nc - 1);
+        const int prev = atomicAdd(cnt, mine);
+        const int last = (prev + mine == nc);
         if (last) *cnt = 0;  // ready for the next call
         *flag = last;
     }
@@ -400,6 +430,32 @@ cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// CTAs of kernel fn resident on the whole GPU at `smem` bytes of dynamic shared
+// memory (cached: the first launch of each configuration asks the runtime).
+int resident_ctas(const void *fn, size_t smem)
+{
+    struct Entry {
+        const void *fn;
+        size_t smem;
+        int dev, n;
+    };
+    static Entry cache[16];
+    static int used = 0;
+    static std::mutex mu;
+    const int dev = dev_info().device;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].smem == smem && cache[i].dev == dev) return cache[i].n;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kAttnThreads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    const int n = std::max(1, per_sm) * dev_info().sm_count;
+    if (used < 16) cache[used++] = Entry{fn, smem, dev, n};
+    return n;
+}
+
 }  // namespace
 
 int attention_chunk_len(int, int, int) { return kChunk; }
@@ -437,8 +493,15 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
     }
-    return launch_ex(fn, dim3((unsigned)a.n_kv_heads, (unsigned)a.m, (unsigned)a.launch_chunks),
-                     dim3(kAttnThreads), smem, s, kargs);
+    // One wave: as many chunk slots per (kv head, token) as resident CTAs allow,
+    // the chunks spread evenly over them (each CTA streams its chunks in turn).
+    const int per_z = a.n_kv_heads * a.m;
+    const int zcap = std::max(1, resident_ctas(fn, smem) / per_z);
+    int Z = std::min(a.launch_chunks, zcap);
+    const int per_cta = (a.launch_chunks + Z - 1) / Z;
+    Z = (a.launch_chunks + per_cta - 1) / per_cta;
+    return launch_ex(fn, dim3((unsigned)a.n_kv_heads, (unsigned)a.m, (unsigned)Z), dim3(kAttnThreads), smem, s,
+                     kargs);
 }
 
 }  // namespace rz
