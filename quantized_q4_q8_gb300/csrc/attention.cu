@@ -340,47 +340,79 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     if (!*flag) return;
     __threadfence();
 
-    // chunk statistics in parallel (thread per (head, chunk)), then the weights
-    float *wts = ps;  // [G][kChunk] reused: chunk weights exp(m_c - M)
-    for (int g = warp; g < G; g += kAttnThreads / 32) {
-        float mc[2], lc[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = lane + 32 * h;
-            mc[h] = c < nc ? __ldcg(part_rec(a, t, kvh, c, g)) : -INFINITY;
-            lc[h] = c < nc ? __ldcg(part_rec(a, t, kvh, c, g) + 1) : 0.0f;
-        }
-        const float M = warp_max(fmaxf(mc[0], mc[1]));
-        float lsum = 0.0f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = lane + 32 * h;
-            const float w = (c < nc && lc[h] > 0.0f) ? expf(mc[h] - M) : 0.0f;
-            if (c < kChunk) wts[g * kChunk + c] = w;
-            lsum += w * lc[h];
-        }
-        lsum = warp_sum(lsum);
-        if (lane == 0) stat[2 * g] = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;  // 0 only after a bad position
-    }
-    __syncthreads();
+    // The records of (t, kvh) go to shared memory first (kbuf / vbuf are free
+    // now), every load of a batch in flight at once: one round trip to L2 instead
+    // of one per few chunks.  Records of a query head are rows of hd + 4 floats
+    // (max, sum, o[hd], pad); as many heads per batch as fit in 2 * 64 * hd floats
+    // (nc <= 64, so one head always fits).
+    float *wts = ps;   // [G][kChunk]: chunk weights exp(m_c - M)
     float *outv = red;  // merged output [G][hd]
-    for (int i = tid; i < G * hd; i += kAttnThreads) {
-        const int g = i / hd, dd = i % hd;
-        float acc = 0.0f;
-        // eight records' loads in flight at a time (every record c < nc is written and
-        // finite; a zero weight adds exactly nothing), summed in chunk order
-        int c = 0;
-        for (; c + 8 <= nc; c += 8) {
-            float v[8];
+    float *rs = kbuf;
+    const int rstride = hd + 4;
+    const int gb = max(1, min(G, (2 * kChunk * hd) / (nc * rstride)));
+    constexpr int kRecLanes = CPT + 1;  // 32 * kRecLanes >= hd + 2
+    constexpr int kRecsInFlight = 4;    // per warp
+    for (int g0 = 0; g0 < G; g0 += gb) {
+        const int ng = min(gb, G - g0), nrec = ng * nc;
+        for (int r0 = 0; r0 < nrec; r0 += kRecsInFlight * (kAttnThreads / 32)) {
+            float v[kRecsInFlight][kRecLanes];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(part_rec(a, t, kvh, c + u, g) + 2 + dd);
+            for (int u = 0; u < kRecsInFlight; ++u) {
+                const int r = r0 + warp + (kAttnThreads / 32) * u;
+                const float *src = part_rec(a, t, kvh, r < nrec ? r % nc : 0, g0 + (r < nrec ? r / nc : 0));
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc = fmaf(v[u], wts[g * kChunk + c + u], acc);
+                for (int k = 0; k < kRecLanes; ++k) {
+                    const int e = lane + 32 * k;
+                    v[u][k] = (r < nrec && e < hd + 2) ? __ldcg(src + e) : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRecsInFlight; ++u) {
+                const int r = r0 + warp + (kAttnThreads / 32) * u;
+                if (r < nrec) {
+#pragma unroll
+                    for (int k = 0; k < kRecLanes; ++k) {
+                        const int e = lane + 32 * k;
+                        if (e < hd + 2) rs[r * rstride + e] = v[u][k];
+                    }
+                }
+            }
         }
-        for (; c < nc; ++c) acc = fmaf(__ldcg(part_rec(a, t, kvh, c, g) + 2 + dd), wts[g * kChunk + c], acc);
-        outv[g * hd + dd] = acc * stat[2 * g];
+        __syncthreads();
+        // chunk statistics (warp per query head, lane per chunk), then the weights
+        for (int gl = warp; gl < ng; gl += kAttnThreads / 32) {
+            const int g = g0 + gl;
+            float mc[2], lc[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                mc[h] = c < nc ? rs[(gl * nc + c) * rstride] : -INFINITY;
+                lc[h] = c < nc ? rs[(gl * nc + c) * rstride + 1] : 0.0f;
+            }
+            const float M = warp_max(fmaxf(mc[0], mc[1]));
+            float lsum = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                const float w = (c < nc && lc[h] > 0.0f) ? expf(mc[h] - M) : 0.0f;
+                if (c < kChunk) wts[g * kChunk + c] = w;
+                lsum += w * lc[h];
+            }
+            lsum = warp_sum(lsum);
+            if (lane == 0) stat[2 * g] = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;  // 0 only after a bad position
+        }
+        __syncthreads();
+        // weighted sum over the chunks in chunk order (every record c < nc is
+        // written and finite; a zero weight adds exactly nothing)
+        for (int i = tid; i < ng * hd; i += kAttnThreads) {
+            const int gl = i / hd, dd = i % hd, g = g0 + gl;
+            const float *col = rs + gl * nc * rstride + 2 + dd;
+            float acc = 0.0f;
+            for (int c = 0; c < nc; ++c) acc = fmaf(col[c * rstride], wts[g * kChunk + c], acc);
+            outv[g * hd + dd] = acc * stat[2 * g];
+        }
+        __syncthreads();
     }
-    __syncthreads();
     const int64_t col0 = (int64_t)kvh * G * hd;
     if (a.att) {
         for (int i = tid; i < G * hd; i += kAttnThreads) a.att[(int64_t)t * a.q_dim + col0 + i] = outv[i];
