@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
             int64_t k = 0;
             bool ok = true;
             RingPos rp{0, 0u};
@@ -137,9 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                         const int nr = min(a.rpp, n - p * a.rpp);
                         const int64_t u = u0 + (int64_t)p * a.rpp;
                         uint8_t *pd = dst + (int64_t)p * 2 * pack_bytes;
-                        bulk_g2s(pd, a.w[0] + u * a.row_bytes, (unsigned)(nr * a.row_bytes), &full[s]);
-                        bulk_g2s(pd + pack_bytes, a.w[1] + u * a.row_bytes, (unsigned)(nr * a.row_bytes),
-                                 &full[s]);
+                        bulk_g2s_hint(pd, a.w[0] + u * a.row_bytes, (unsigned)(nr * a.row_bytes), &full[s], pol);
+                        bulk_g2s_hint(pd + pack_bytes, a.w[1] + u * a.row_bytes, (unsigned)(nr * a.row_bytes),
+                                 &full[s], pol);
                     }
                 } else {
                     int r = 0;
@@ -147,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                         const int64_t u = u0 + r;
                         const int kseg = seg_of(a, u);
                         const int run = (int)min((int64_t)(n - r), a.seg_begin[kseg + 1] - u);
-                        bulk_g2s(dst + (int64_t)r * a.row_bytes,
+                        bulk_g2s_hint(dst + (int64_t)r * a.row_bytes,
                                  a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
-                                 (unsigned)(run * a.row_bytes), &full[s]);
+                                 (unsigned)(run * a.row_bytes), &full[s], pol);
                         r += run;
                     }
                 }
