@@ -44,7 +44,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kCtaSmem = 200 * 1024;
 constexpr int kStageTarget = 16 * 1024;
 constexpr int kStageTargetFused = 32 * 1024;
-constexpr int kXSmemMax = 48 * 1024;
+constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
 constexpr int kMaxStages = 16;
 
 struct Args {
