@@ -484,7 +484,9 @@ __device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64
                                             int warp, int lane, Sync sync)
 {
     const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
-    if (kf <= 4)
+    if (kf <= 2)
+        stage_x_f32_kf<CG, NORM, 2, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else if (kf <= 4)
         stage_x_f32_kf<CG, NORM, 4, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
     else
         stage_x_f32_kf<CG, NORM, 8, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
