@@ -85,7 +85,9 @@ __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
     return k;
 }
 
-template <int MT, int EPI, bool XS, int XIN>
+// PR: several tokens with the rows in pairs (a separate instantiation, so that
+// its register allocation does not touch the one-row-per-warp path)
+template <int MT, int EPI, bool XS, int XIN, bool PR = false>
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -237,6 +239,37 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                     a.y[kseg][lr] = out;
                 }
             }
+        } else if constexpr (PR) {
+            // several tokens (at least four rows per consumer warp): rows in pairs as
+            // above, tokens in groups of TG, each activation load shared by the two
+            // rows
+            constexpr int TG = MT < 4 ? MT : 4;
+            const int npair = (end - first + 1) / 2;
+            for (int q = q0; q < npair; q += kConsumerWarps) {
+                const int iA = first + 2 * q;
+                const bool hasB = iA + 1 < end;
+                const uint32_t pkA = slot + (uint32_t)(2 * q * R * pack_bytes);
+                for (int t0 = 0; t0 < a.m; t0 += TG) {
+                    float acc[2][TG];
+                    pack_pair_accumulate_tg<TG>(x, pkA, pkA + (uint32_t)(R * pack_bytes), hasB, R,
+                                                (uint32_t)pack_bytes, a.nsb, t0, lane, acc);
+                    if (lane == 0 || (lane == 16 && hasB)) {
+                        const int64_t unit = r0 + iA + (lane >> 4);
+                        const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
+                        const int64_t lr = unit - a.seg_begin[kseg];
+#pragma unroll
+                        for (int i = 0; i < TG; ++i) {
+                            const int t = t0 + i;
+                            if (t < a.m) {
+                                float out = acc[0][i];
+                                if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                                if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][i], acc[1][i]);
+                                a.y[kseg][t * a.ldy[kseg] + lr] = out;
+                            }
+                        }
+                    }
+                }
+            }
         } else {
             for (int i = first + i0; i < end; i += kConsumerWarps) {
                 const int64_t pack0 = r0 + (int64_t)i * a.rpp;
@@ -294,14 +327,14 @@ size_t smem_bytes(const Args &a)
     return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 96 + 2 * 8 * (size_t)a.NS;
 }
 
-template <int MT, int EPI, bool XS, int XIN>
+template <int MT, int EPI, bool XS, int XIN, bool PR = false>
 cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
 {
     static bool attr_done[64] = {};
     const int dev = dev_info().device;
     const size_t smem = smem_bytes(a);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS, XIN>,
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS, XIN, PR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
@@ -317,31 +350,36 @@ cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS, XIN>, a);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS, XIN, PR>, a);
 }
 
-template <int MT, int EPI>
+template <int MT, int EPI, bool PR>
 cudaError_t launch_x(const Args &a, int grid, cudaStream_t s, int xin)
 {
     if (xin == XIN_NORM) {
-        if constexpr (EPI != EPI_RESID) return launch_t<MT, EPI, true, XIN_NORM>(a, grid, s);
+        if constexpr (EPI != EPI_RESID) return launch_t<MT, EPI, true, XIN_NORM, PR>(a, grid, s);
         return cudaErrorInvalidValue;
     }
     if (xin == XIN_F32) {
-        if constexpr (EPI == EPI_RESID) return launch_t<MT, EPI, true, XIN_F32>(a, grid, s);
+        if constexpr (EPI == EPI_RESID) return launch_t<MT, EPI, true, XIN_F32, PR>(a, grid, s);
         return cudaErrorInvalidValue;
     }
-    return a.x_smem ? launch_t<MT, EPI, true, XIN_Q8>(a, grid, s) : launch_t<MT, EPI, false, XIN_Q8>(a, grid, s);
+    if (a.x_smem) return launch_t<MT, EPI, true, XIN_Q8, PR>(a, grid, s);
+    if constexpr (PR) return cudaErrorInvalidValue;  // the pair path wants the activations staged
+    return launch_t<MT, EPI, false, XIN_Q8>(a, grid, s);
 }
 
+// Several tokens take the row-pair kernels when each consumer warp gets at least
+// four rows (with fewer rows per CTA the pairs would leave warps idle).
 template <int EPI>
 cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
 {
-    if (a.m <= 1) return launch_x<1, EPI>(a, grid, s, xin);
-    if (a.m <= 2) return launch_x<2, EPI>(a, grid, s, xin);
-    if (a.m <= 4) return launch_x<4, EPI>(a, grid, s, xin);
-    if (a.m <= 8) return launch_x<8, EPI>(a, grid, s, xin);
-    return launch_x<16, EPI>(a, grid, s, xin);
+    const bool pr = a.m > 1 && a.rpp == 1 && a.x_smem && a.units / grid >= 4 * kConsumerWarps;
+    if (a.m <= 1) return launch_x<1, EPI, false>(a, grid, s, xin);
+    if (a.m <= 2) return pr ? launch_x<2, EPI, true>(a, grid, s, xin) : launch_x<2, EPI, false>(a, grid, s, xin);
+    if (a.m <= 4) return pr ? launch_x<4, EPI, true>(a, grid, s, xin) : launch_x<4, EPI, false>(a, grid, s, xin);
+    if (a.m <= 8) return pr ? launch_x<8, EPI, true>(a, grid, s, xin) : launch_x<8, EPI, false>(a, grid, s, xin);
+    return pr ? launch_x<16, EPI, true>(a, grid, s, xin) : launch_x<16, EPI, false>(a, grid, s, xin);
 }
 
 static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
@@ -398,7 +436,7 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     // ring fills: larger stages there mean fewer barrier round trips.
     const int64_t tgt = (f32in || epilogue != EPI_STORE) ? kStageTargetFused : kStageTarget;
     a.PS = (int)std::max<int64_t>(1, tgt / pack);
-    if (m == 1 && a.rpp == 1 && (a.PS & 1)) {
+    if (a.rpp == 1 && (a.PS & 1)) {
         // row pairs: an even pack count per stage, so that no pair is cut short
         if ((a.PS + 1) * pack <= tgt * 5 / 4) a.PS += 1;
         else if (a.PS > 1) a.PS -= 1;

@@ -269,6 +269,62 @@ __device__ __forceinline__ void pack_pair_accumulate(const XSrc &x, uint32_t pkA
     }
 }
 
+// Two packs of one row each (rows with 8 or more super-blocks), tokens t0 ..
+// t0 + TG - 1 (those below x.m), activations in shared memory: each activation
+// load feeds both rows, so shared-memory traffic per token is about half that
+// of one row at a time.  On return acc[h][i] holds, for token t0 + i, the total
+// of row A in lanes 0-15 and that of row B in lanes 16-31 (the reduction of
+// pack_pair_accumulate, per token).
+template <int TG>
+__device__ __forceinline__ void pack_pair_accumulate_tg(const XSrc &x, uint32_t pkA, uint32_t pkB, bool hasB, int R,
+                                                        uint32_t pack_bytes, int nsb, int t0, int lane,
+                                                        float (&acc)[2][TG])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const LaneConst Lc = lane_const(c);
+    const int nt = min(TG, x.m - t0);
+    const int nsbx = (int)(x.in_dim / 256);
+    float a[2][2][TG];  // [half][row][token]
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < TG; ++i) a[h][0][i] = a[h][1][i] = 0.0f;
+#pragma unroll 1
+    for (int h = 0; h < R; ++h) {
+        const uint32_t hA = pkA + (uint32_t)h * pack_bytes;
+        const uint32_t hB = (hasB ? pkB : pkA) + (uint32_t)h * pack_bytes;
+        for (int sb = g; sb < nsb; sb += 8) {
+            SbLane wa, wb;
+            sb_lane_load(hA + sb * kSB, c, Lc, wa);
+            sb_lane_load(hB + sb * kSB, c, Lc, wb);
+#pragma unroll
+            for (int i = 0; i < TG; ++i) {
+                if (i < nt) {
+                    const int t = t0 + i;
+                    const uint32_t xa = x.q + (uint32_t)(t * nsbx + sb) * kXSlot + x_chunk_off(c);
+                    const int4 x0 = lds128(xa), x1 = lds128(xa + 16), x2 = lds128(xa + 32), x3 = lds128(xa + 48);
+                    const uint32_t da = x.ds + (uint32_t)(t * x.nb + sb * 8 + 2 * c) * 4u;
+                    const float2 d8 = lds64f(da), s8 = lds64f(da + (uint32_t)(x.m * x.nb) * 4u);
+                    sb_lane_dot(wa, x0, x1, x2, x3, d8, s8, a[h][0][i]);
+                    sb_lane_dot(wb, x0, x1, x2, x3, d8, s8, a[h][1][i]);
+                }
+            }
+        }
+    }
+    const bool upper = lane & 16;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < TG; ++i) {
+            const float rA = a[h][0][i], rB = a[h][1][i];
+            const float keep = upper ? rB : rA, send = upper ? rA : rB;
+            float v = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[h][i] = v;
+        }
+}
+
 // Rows per pack: a warp takes a whole pack; rows with fewer than 8 super-blocks
 // are packed 8 / nsb to a warp so that every lane group has a super-block.
 __host__ __device__ inline int pack_rows_for(int nsb) { return (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1; }

@@ -82,6 +82,9 @@ GEMV_CASES = [
     (300, 2048, 1), (1000, 4096, 1), (23, 4864, 1), (45, 11008, 1), (19, 14336, 1),
     (256, 1024, 2), (100, 1024, 3), (77, 4096, 4), (50, 2304, 5), (33, 4096, 8),
     (65, 1024, 16), (40, 4864, 16), (9, 14336, 16), (2000, 256, 7),
+    # >= 64 rows per CTA on 152 SMs: the multi-token row-pair path (token groups
+    # of 2, 3, 4 with a ragged last group; CTAs with an odd row count)
+    (10001, 512, 2), (10001, 1024, 3), (9999, 512, 6), (9729, 2048, 16),
 ]
 
 

@@ -162,7 +162,16 @@ def test_attention_bad_device_position_is_reported(rz):
 
 
 # ----------------------------------------------------------------------------- SwiGLU FFN
-@pytest.mark.parametrize("shape,m", [(S.QWEN2, 1), (S.QWEN2, 3), (S.LLAMA7B, 1), (S.LLAMA7B, 2)])
+# wide gate/up (9984 rows) and wide down (9984 rows): the multi-token row-pair
+# path with the SwiGLU and the residual epilogues
+WIDE_INTER = S.LayerShape(hidden=512, inter=9984, n_heads=8, n_kv_heads=8, head_dim=64,
+                          rope_theta=1e4, rope_mode=0)
+WIDE_HIDDEN = S.LayerShape(hidden=9984, inter=512, n_heads=8, n_kv_heads=8, head_dim=64,
+                           rope_theta=1e4, rope_mode=0)
+
+
+@pytest.mark.parametrize("shape,m", [(S.QWEN2, 1), (S.QWEN2, 3), (S.LLAMA7B, 1), (S.LLAMA7B, 2),
+                                     (WIDE_INTER, 5), (WIDE_HIDDEN, 3)])
 def test_swiglu_ffn_parity(rz, shape, m):
     L = S.layer(shape, f"gffn.{shape.hidden}")
     x = S.hidden_input(f"gffn.x.{shape.hidden}.{m}", m, shape.hidden, shape.hidden_pad)
