@@ -963,8 +963,8 @@ __global__ void __launch_bounds__(kPThreads, 1) decode_persistent_kernel(const _
                     // 1-3: RMSNorm -> Q8_1 -> Q|K|V; 6-7: O + residual; 8-9: RMSNorm ->
                     // Q8_1 -> gate/up, silu(gate) * up; 9-10: Q8_1 of h -> down + residual
                     if (kind == K_O) {
-                        stage_x_q8<true, kPWarps>(xsm, a.a8, reinterpret_cast<const float *>(a.a8 + a.q_pad), 1,
-                                                  a.q_pad, threadIdx.x, sync);
+                        const float *a8d = reinterpret_cast<const float *>(a.a8 + a.q_pad);
+                        stage_x_q8<true, kPWarps>(xsm, a.a8, a8d, a8d + a.q_pad / 32, 1, a.q_pad, threadIdx.x, sync);
                     } else {
                         const float *src = kind == K_QKV ? x_in : kind == K_GU ? a.res1 : a.h;
                         const int64_t n = kind == K_DN ? a.inter : a.hidden_pad;

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     x.gd = a.xd;
     x.gs = a.xs;
     auto csync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
-    if (XS && XIN == XIN_Q8) stage_x_q8<false>(xsm, a.xq, a.xd, a.m, a.in_dim, threadIdx.x, csync);
+    if (XS && XIN == XIN_Q8) stage_x_q8<false>(xsm, a.xq, a.xd, a.xs, a.m, a.in_dim, threadIdx.x, csync);
     if (XS && XIN != XIN_Q8) {
         // quantise the f32 input (RMS-normalised first for XIN_NORM) straight into
         // the padded slot layout
@@ -382,8 +382,14 @@ cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
     return pr ? launch_x<16, EPI, true>(a, grid, s, xin) : launch_x<16, EPI, false>(a, grid, s, xin);
 }
 
-static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
-                                 const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
+// Q8_1 activations of m tokens: codes [m][in_dim], then d [m][in_dim/32], then s.
+struct Q8Src {
+    const int8_t *q;
+    const float *d, *s;
+};
+
+static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, const Q8Src *q8,
+                               const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
 {
     Args a = {};
     int64_t units = 0;
@@ -414,9 +420,9 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     a.m = (int)m;
     a.in_dim = in_dim;
     if (q8) {
-        a.xq = static_cast<const int8_t *>(q8);
-        a.xd = reinterpret_cast<const float *>(static_cast<const uint8_t *>(q8) + m * in_dim);
-        a.xs = a.xd + m * (in_dim / 32);
+        a.xq = q8->q;
+        a.xd = q8->d;
+        a.xs = q8->s;
     }
     int xin = XIN_Q8;
     if (f32in) {
@@ -465,6 +471,45 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     case EPI_RESID: return launch_epi<EPI_RESID>(a, (int)grid, s, xin);
     default: return launch_epi<EPI_SWIGLU>(a, (int)grid, s, xin);
     }
+}
+
+static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
+                                 const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
+{
+    if (!q8) return launch_core(seg, nseg, epilogue, nullptr, f32in, m, in_dim, s);
+    const int64_t nb = in_dim / 32;
+    Q8Src x;
+    x.q = static_cast<const int8_t *>(q8);
+    x.d = reinterpret_cast<const float *>(x.q + m * in_dim);
+    x.s = x.d + m * nb;
+    if (m == 1 || x_smem_bytes(m, in_dim) <= kXSmemMax) return launch_core(seg, nseg, epilogue, &x, f32in, m, in_dim, s);
+    // Several tokens whose activations do not fit in shared memory: equal groups
+    // of tokens that do, one launch each.  The weights stream once per group,
+    // which beats reading every token's activations from L2 for every row.
+    int64_t mc = m;
+    while (mc > 1 && x_smem_bytes(mc, in_dim) > kXSmemMax) --mc;
+    const int64_t ng = (m + mc - 1) / mc;
+    mc = (m + ng - 1) / ng;
+    for (int64_t t0 = 0; t0 < m; t0 += mc) {
+        const int64_t n = std::min(mc, m - t0);
+        Q4kSegment part[3];
+        for (int k = 0; k < nseg; ++k) {
+            part[k] = seg[k];
+            const int64_t ldy = seg[k].ldy ? seg[k].ldy : seg[k].rows;
+            const int64_t ldr = seg[k].ldr ? seg[k].ldr : seg[k].rows;
+            part[k].ldy = ldy;
+            part[k].ldr = ldr;
+            part[k].y = seg[k].y + t0 * ldy;
+            part[k].res = seg[k].res ? seg[k].res + t0 * ldr : nullptr;
+        }
+        Q8Src xg;
+        xg.q = x.q + t0 * in_dim;
+        xg.d = x.d + t0 * nb;
+        xg.s = x.s + t0 * nb;
+        const cudaError_t e = launch_core(part, nseg, epilogue, &xg, f32in, n, in_dim, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace

@@ -387,10 +387,11 @@ __device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
 // Both helpers run on the 32 * NW threads of NW warps (thread index tid, warp,
 // lane) and end with `sync` over them.
 
-// Q8_1 codes of m rows of in_dim (SoA: codes, then d, then s) -> slot layout.
+// Q8_1 codes of m rows of in_dim ([m][in_dim]) and their d and s ([m][in_dim/32]
+// each) -> slot layout.
 template <bool CG, int NW = kRowWarps, typename Sync>
-__device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const float *xd, int m,
-                                           int64_t in_dim, int tid, Sync sync)
+__device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const float *xd, const float *xs,
+                                           int m, int64_t in_dim, int tid, Sync sync)
 {
     const int64_t nsbx = (int64_t)m * (in_dim / 256);
     const int4 *src = reinterpret_cast<const int4 *>(xq);
@@ -400,11 +401,15 @@ __device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const
         const int4 v = CG ? __ldcg(src + i) : src[i];
         *reinterpret_cast<int4 *>(xsm + sbg * kXSlot + x_chunk_off(cc) + 16 * (ch & 3)) = v;
     }
-    // d and s, unchanged
-    const int64_t nds = 2LL * m * (in_dim / 32) / 4;
+    // d, then s, unchanged
+    const int64_t nd = (int64_t)m * (in_dim / 32) / 4;  // int4 of each
     const int4 *dsrc = reinterpret_cast<const int4 *>(xd);
+    const int4 *ssrc = reinterpret_cast<const int4 *>(xs);
     int4 *ddst = reinterpret_cast<int4 *>(xsm + nsbx * kXSlot);
-    for (int64_t i = tid; i < nds; i += NW * 32) ddst[i] = CG ? __ldcg(dsrc + i) : dsrc[i];
+    for (int64_t i = tid; i < 2 * nd; i += NW * 32) {
+        const int4 *src = i < nd ? dsrc + i : ssrc + (i - nd);
+        ddst[i] = CG ? __ldcg(src) : *src;
+    }
     sync();
 }
 

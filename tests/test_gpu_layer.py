@@ -170,8 +170,10 @@ WIDE_HIDDEN = S.LayerShape(hidden=9984, inter=512, n_heads=8, n_kv_heads=8, head
                            rope_theta=1e4, rope_mode=0)
 
 
+# (LLAMA7B, 16): the activations of down (16 x 11008) exceed shared memory, so
+# down runs as token groups, each with its slice of the residual
 @pytest.mark.parametrize("shape,m", [(S.QWEN2, 1), (S.QWEN2, 3), (S.LLAMA7B, 1), (S.LLAMA7B, 2),
-                                     (WIDE_INTER, 5), (WIDE_HIDDEN, 3)])
+                                     (S.LLAMA7B, 16), (WIDE_INTER, 5), (WIDE_HIDDEN, 3)])
 def test_swiglu_ffn_parity(rz, shape, m):
     L = S.layer(shape, f"gffn.{shape.hidden}")
     x = S.hidden_input(f"gffn.x.{shape.hidden}.{m}", m, shape.hidden, shape.hidden_pad)
