@@ -382,6 +382,10 @@ cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
     return pr ? launch_x<16, EPI, true>(a, grid, s, xin) : launch_x<16, EPI, false>(a, grid, s, xin);
 }
 
+}  // namespace
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim);
+namespace {
+
 // Q8_1 activations of m tokens: codes [m][in_dim], then d [m][in_dim/32], then s.
 struct Q8Src {
     const int8_t *q;
@@ -486,10 +490,8 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
     // Several tokens whose activations do not fit in shared memory: equal groups
     // of tokens that do, one launch each.  The weights stream once per group,
     // which beats reading every token's activations from L2 for every row.
-    int64_t mc = m;
-    while (mc > 1 && x_smem_bytes(mc, in_dim) > kXSmemMax) --mc;
-    const int64_t ng = (m + mc - 1) / mc;
-    mc = (m + ng - 1) / ng;
+    const int64_t ng = q4k_gemv_launch_count(m, in_dim);
+    const int64_t mc = (m + ng - 1) / ng;
     for (int64_t t0 = 0; t0 < m; t0 += mc) {
         const int64_t n = std::min(mc, m - t0);
         Q4kSegment part[3];
@@ -518,6 +520,14 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
                             int64_t m, int64_t in_dim, cudaStream_t s)
 {
     return launch_common(seg, nseg, epilogue, q8, nullptr, m, in_dim, s);
+}
+
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim)
+{
+    if (m <= 1 || x_smem_bytes(m, in_dim) <= kXSmemMax) return 1;
+    int64_t mc = m;
+    while (mc > 1 && x_smem_bytes(mc, in_dim) > kXSmemMax) --mc;
+    return (int)((m + mc - 1) / mc);
 }
 
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)

@@ -277,10 +277,12 @@ int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int 
     const LayerDesc &L0 = layers[0];
     const int h = head ? 2 : 0;  // output RMSNorm, LM head
     if (persistent_decode_ok(L0, m, max_seq) && same_rope(layers, n_layers)) return (n_layers + 31) / 32 + h;
-    int per_layer = 1 /* attention */ + 1 /* O */;
-    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 2;  // Q|K|V (+ RMSNorm)
-    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 2;  // gate/up (+ RMSNorm)
-    per_layer += q4k_gemv_f32_input_ok(m, L0.inter) ? 1 : 2;       // down (+ Q8_1 of h)
+    const int q_pad = (L0.n_heads * L0.head_dim + 255) / 256 * 256;
+    const int gh = q4k_gemv_launch_count(m, L0.hidden_pad), gi = q4k_gemv_launch_count(m, L0.inter);
+    int per_layer = 1 /* attention */ + q4k_gemv_launch_count(m, q_pad) /* O */;
+    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 1 + gh;  // Q|K|V (or RMSNorm, then groups)
+    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 1 + gh;  // gate/up
+    per_layer += q4k_gemv_f32_input_ok(m, L0.inter) ? 1 : 1 + gi;       // down (or Q8_1 of h, then groups)
     return 1 /* RoPE table */ + n_layers * per_layer + h;
 }
 

@@ -64,6 +64,9 @@ struct F32Input {
     float eps;
 };
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim);
+// launches one Q8_1-input GEMV of m tokens takes (token groups when the
+// activations exceed shared memory)
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim);
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
                                 int64_t m, int64_t in_dim, cudaStream_t s);
 
