@@ -123,15 +123,19 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
 // heads in shared memory.
 // shared memory: kbuf [64][hd] | vbuf [64][hd] | qs [G][hd] | kn [hd] | vn [hd] |
 //                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | 2 mbarriers
+// With att_bufs == 1 (every chunk has a CTA of its own) vbuf is kbuf: the V rows
+// are copied in once the scores have read the K rows, and the smaller footprint
+// lets more CTAs share an SM.
 template <int CPT>
-__global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const AttnArgs a)
 {
     extern __shared__ __align__(16) float sm[];
     const int kvh = blockIdx.x, t = blockIdx.y, chunk = blockIdx.z;
     const int hd = a.head_dim, G = a.group;
+    const int nbuf = a.att_bufs;
     float *kbuf = sm;
-    float *vbuf = kbuf + kChunk * hd;
-    float *qs = vbuf + kChunk * hd;
+    float *vbuf = kbuf + (nbuf - 1) * kChunk * hd;
+    float *qs = kbuf + nbuf * kChunk * hd;
     float *kn = qs + G * hd;
     float *vn = kn + hd;
     float *ps = vn + hd;
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
         }
         __syncthreads();
         issue_k(chunk);
-        issue_v(chunk);
+        if (nbuf == 2) issue_v(chunk);
 
         // rotated query heads of this kv head, and (owner) the new row
         for (int g = 0; g < G; ++g)
@@ -249,7 +253,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
                 }
             }
             __syncthreads();
-            if (ok && it + 1 < mine) issue_k(c + Z);  // kbuf is free
+            if (nbuf == 1)
+                issue_v(c);  // the K rows are read: the buffer takes the V rows
+            else if (ok && it + 1 < mine)
+                issue_k(c + Z);  // kbuf is free
             // ---- chunk softmax statistics (warp per query head)
             for (int g = warp; g < G; g += kAttnThreads / 32) {
                 const float v0 = lane < n ? ps[g * kChunk + lane] : -INFINITY;
@@ -302,7 +309,12 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
                 }
             }
             __syncthreads();
-            if (ok && it + 1 < mine) issue_v(c + Z);  // vbuf is free
+            if (ok && it + 1 < mine) {
+                if (nbuf == 1)
+                    issue_k(c + Z);  // the buffer is free again
+                else
+                    issue_v(c + Z);  // vbuf is free
+            }
             // fixed-order sum over the 8 row groups -> partial record of chunk c
             for (int i = tid; i < G * hd; i += kAttnThreads) {
                 const int g = i / hd, dd = i % hd;
@@ -343,13 +355,13 @@ __global__ void __launch_bounds__(kAttnThreads) attention_chunk_kernel(const Att
     // The records of (t, kvh) go to shared memory first (kbuf / vbuf are free
     // now), every load of a batch in flight at once: one round trip to L2 instead
     // of one per few chunks.  Records of a query head are rows of hd + 4 floats
-    // (max, sum, o[hd], pad); as many heads per batch as fit in 2 * 64 * hd floats
-    // (nc <= 64, so one head always fits).
+    // (max, sum, o[hd], pad); as many heads per batch as fit in the K/V buffers
+    // (one head always fits: nc <= 64 with two buffers, checked at launch with one).
     float *wts = ps;   // [G][kChunk]: chunk weights exp(m_c - M)
     float *outv = red;  // merged output [G][hd]
     float *rs = kbuf;
     const int rstride = hd + 4;
-    const int gb = max(1, min(G, (2 * kChunk * hd) / (nc * rstride)));
+    const int gb = max(1, min(G, (nbuf * kChunk * hd) / (nc * rstride)));  // >= 1 head: checked at launch
     constexpr int kRecLanes = CPT + 1;  // 32 * kRecLanes >= hd + 2
     constexpr int kRecsInFlight = 4;    // per warp
     for (int g0 = 0; g0 < G; g0 += gb) {
@@ -492,13 +504,15 @@ int resident_ctas(const void *fn, size_t smem)
 
 int attention_chunk_len(int, int, int) { return kChunk; }
 
-size_t attention_smem_bytes(int group, int head_dim, int)
+size_t attention_smem_bytes_n(int group, int head_dim, int nbuf)
 {
-    return (2 * (size_t)kChunk * head_dim + (size_t)group * head_dim + 2 * (size_t)head_dim +
+    return ((size_t)nbuf * kChunk * head_dim + (size_t)group * head_dim + 2 * (size_t)head_dim +
             (size_t)group * kChunk + ((2 * (size_t)group + 2 + 3) & ~(size_t)3) + 8 * (size_t)group * head_dim) *
                sizeof(float) +
            16 + 16;  // flag (+ pad), two mbarriers
 }
+
+size_t attention_smem_bytes(int group, int head_dim, int) { return attention_smem_bytes_n(group, head_dim, 2); }
 
 cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s)
 {
@@ -515,19 +529,25 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
         cudaError_t e = launch_rope_table(a, s);
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = attention_smem_bytes(a.group, a.head_dim, kChunk);
     const void *fn = a.head_dim == 32    ? (const void *)attention_chunk_kernel<1>
                      : a.head_dim == 64  ? (const void *)attention_chunk_kernel<2>
                      : a.head_dim == 128 ? (const void *)attention_chunk_kernel<4>
                                          : (const void *)attention_chunk_kernel<8>;
-    if (smem > 48 * 1024) {
+    if (attention_smem_bytes_n(a.group, a.head_dim, 2) > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
     }
-    // One wave: as many chunk slots per (kv head, token) as resident CTAs allow,
+    // One wave.  When every chunk can have a resident CTA of its own with K and V
+    // through one buffer (and the merge's records fit in it), that; else as many
+    // chunk slots per (kv head, token) as resident CTAs allow with two buffers,
     // the chunks spread evenly over them (each CTA streams its chunks in turn).
     const int per_z = a.n_kv_heads * a.m;
+    const size_t smem1 = attention_smem_bytes_n(a.group, a.head_dim, 1);
+    const bool one = resident_ctas(fn, smem1) >= per_z * a.launch_chunks &&
+                     (size_t)a.n_chunks * (a.head_dim + 4) <= (size_t)kChunk * a.head_dim;
+    args.att_bufs = one ? 1 : 2;
+    const size_t smem = one ? smem1 : attention_smem_bytes_n(a.group, a.head_dim, 2);
     const int zcap = std::max(1, resident_ctas(fn, smem) / per_z);
     int Z = std::min(a.launch_chunks, zcap);
     const int per_cta = (a.launch_chunks + Z - 1) / Z;

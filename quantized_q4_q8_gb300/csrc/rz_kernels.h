@@ -93,6 +93,7 @@ struct AttnArgs {
     int rope_mode;
     int chunk_len, n_chunks;     // n_chunks covers max_seq (workspace layout)
     int launch_chunks;           // chunks launched: enough for the host position, else n_chunks
+    int att_bufs;                // set by launch_attention: 1 = K then V through one buffer, 2 = both
     float *part;                 // workspace: [m][n_kv_heads][n_chunks][group][head_dim + 2]
     int *counters;               // workspace: [m][n_kv_heads], zero before the first call
     float *att;                  // f32 [m][q_dim] output, or nullptr

@@ -74,6 +74,11 @@ ATT_CASES = [
     (4, 1, 32, 1e4, 0, 50, [49]),
     (8, 2, 64, 1e4, 1, 2056, [2048]),
     (8, 4, 64, 1e4, 0, 100, [5, 0, 99]),
+    # more (head, chunk) units than resident CTAs: two K/V buffers, several chunks
+    # streamed per CTA
+    (32, 32, 128, 1e4, 0, 2056, [2000]),
+    # 63 chunk records per head exceed one buffer: two buffers
+    (8, 8, 128, 1e4, 0, 4096, [4000]),
 ]
 
 
