@@ -345,3 +345,105 @@ def test_ffn_gates_with_silu_of_gate_times_up(orc):
     h_swapped = (u / (1.0 + np.exp(-u)) * g).astype(np.float32)
     dn_sw = orc.q4k_q8_gemv(L.w["wdown"], orc.q8_1_quantize(h_swapped), 1, sh.hidden, sh.inter)[0]
     assert np.abs(dn_sw - dn).max() > 1e-2 * np.abs(dn).max()
+
+
+# ----------------------------------------------------------------------------- layer at position >= 1
+def _k_of_layer(orc, L, x):
+    """The new token's un-rotated key: K GEMV of the Q8_1 of the normed input."""
+    sh = L.shape
+    x8 = orc.q8_1_quantize(orc.rmsnorm(x, L.attn_gamma, sh.hidden, sh.hidden_pad, sh.eps))
+    k = orc.q4k_q8_gemv(L.w["wk"], x8, 1, sh.kv_dim, sh.hidden_pad)[0]
+    v = orc.q4k_q8_gemv(L.w["wv"], x8, 1, sh.kv_dim, sh.hidden_pad)[0]
+    return k, v
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_writes_key_rotated_at_its_position(orc, mode):
+    """forward_single_full_cuda_with_cache rotates the new token's k by RoPE at the
+    token's position before it joins the cache: row pos of K holds rope(k, pos), row
+    pos of V the plain v, and no other row changes."""
+    sh = S.LayerShape(hidden=448, inter=512, n_heads=7, n_kv_heads=1, head_dim=64,
+                      rope_theta=1e4, rope_mode=mode)
+    L = S.layer(sh, f"pin.krow.{mode}")
+    lw = _orc_layer(orc, L)
+    x = S.hidden_input(f"pin.krow.x.{mode}", 1, sh.hidden, sh.hidden_pad)[0]
+    pos = 9
+    kc, vc = S.kv_prefill(sh, f"pin.krow.{mode}", 16, pos)
+    k0, v0 = kc[0].copy(), vc[0].copy()
+    orc.decode_layer(x, lw, kc[0], vc[0], pos)
+    k, v = _k_of_layer(orc, L, x)
+    assert np.array_equal(kc[0, pos], orc.rope(k, sh.n_kv_heads, sh.head_dim, pos, sh.rope_theta, mode))
+    assert np.array_equal(vc[0, pos], v)
+    others = np.arange(16) != pos
+    assert np.array_equal(kc[0][others], k0[others]) and np.array_equal(vc[0][others], v0[others])
+    # the rotation is not the identity here, nor the one of a neighbouring position
+    for wrong in (k, orc.rope(k, sh.n_kv_heads, sh.head_dim, pos + 1, sh.rope_theta, mode),
+                  orc.rope(k, sh.n_kv_heads, sh.head_dim, pos - 1, sh.rope_theta, mode)):
+        assert np.abs(kc[0, pos] - wrong).max() > 1e-3 * np.abs(k).max()
+
+
+def test_layer_uniform_attention_when_every_key_equals_the_new_one(orc):
+    """Position 6 with every earlier K row equal to the new token's rotated key:
+    all scores are the same number, the softmax is uniform and the attention output
+    is the plain mean of V rows 0..6 (the new token's v included).  The layer then
+    equals x + O(q8(mean v)) followed by the FFN, bit for bit."""
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.uni")
+    lw = _orc_layer(orc, L)
+    x = S.hidden_input("pin.uni.x", 1, sh.hidden, sh.hidden_pad)[0]
+    pos = 6
+    k, v = _k_of_layer(orc, L, x)
+    kr = orc.rope(k, sh.n_kv_heads, sh.head_dim, pos, sh.rope_theta, sh.rope_mode)
+    kc, vc = S.kv_prefill(sh, "pin.uni", 8, pos)
+    kc[0, :pos] = kr
+    out = orc.decode_layer(x, lw, kc[0], vc[0], pos)
+    mean = [0.0] * sh.kv_dim
+    for t in range(pos + 1):               # sequential f64 sum, rows in order
+        row = vc[0, t]
+        mean = [a + float(b) for a, b in zip(mean, row)]
+    mean = np.array(mean) / (pos + 1)
+    att = np.zeros(sh.q_pad, np.float32)
+    for h in range(sh.n_heads):
+        kvh = h // (sh.n_heads // sh.n_kv_heads)
+        att[h * sh.head_dim:(h + 1) * sh.head_dim] = mean[kvh * sh.head_dim:(kvh + 1) * sh.head_dim]
+    o = orc.q4k_q8_gemv(L.w["wo"], orc.q8_1_quantize(att), 1, sh.hidden, sh.q_pad)[0]
+    r1 = np.zeros(sh.hidden_pad, np.float32)
+    r1[:sh.hidden] = x[:sh.hidden] + o
+    expect = orc.swiglu_ffn(r1, L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
+                            sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
+    assert np.array_equal(out, expect)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_query_rotated_at_its_position(orc, mode):
+    """With W_q = W_k (so q = k before RoPE) and earlier K rows rope(k, j), the score
+    of row j is k . R((j - pos) theta) k / sqrt(hd), which depends on |j - pos| only
+    when the query is rotated at exactly `pos`.  Mirroring the rows about pos
+    (rope(k, 2 pos - j) in place of rope(k, j)) must then leave the layer output
+    unchanged up to f32 rounding, and mirroring about pos + 1 must not."""
+    sh = S.LayerShape(hidden=512, inter=512, n_heads=4, n_kv_heads=4, head_dim=64,
+                      rope_theta=1e4, rope_mode=mode)
+    L = S.layer(sh, f"pin.qpos.{mode}")
+    L.w["wq"] = L.w["wk"].copy()
+    L.attn_gamma = np.full(sh.hidden, 0.01, np.float32)   # moderate scores: a soft softmax
+    lw = _orc_layer(orc, L)
+    x = S.hidden_input(f"pin.qpos.x.{mode}", 1, sh.hidden, sh.hidden_pad)[0]
+    pos = 4
+    k, _ = _k_of_layer(orc, L, x)
+    rot = lambda p: orc.rope(k, sh.n_kv_heads, sh.head_dim, p, sh.rope_theta, mode)
+
+    def run(center2):
+        kc, vc = S.kv_prefill(sh, f"pin.qpos.{mode}", 8, pos)
+        for j in range(pos):
+            kc[0, j] = rot(center2 - j)
+        return orc.decode_layer(x, lw, kc[0], vc[0], pos).astype(np.float64)
+
+    kc, vc = S.kv_prefill(sh, f"pin.qpos.{mode}", 8, pos)
+    for j in range(pos):
+        kc[0, j] = rot(j)
+    base = orc.decode_layer(x, lw, kc[0], vc[0], pos).astype(np.float64)
+    mirrored = run(2 * pos)
+    shifted = run(2 * (pos + 1))
+    scale = np.abs(base).max()
+    assert np.abs(mirrored - base).max() <= 1e-3 * scale
+    assert np.abs(shifted - base).max() > 1e-2 * scale
