@@ -258,8 +258,8 @@ rz_status rz_decode_layers(const float *input, const rz_layer_weights *layers, c
 /*
  * rz_decode_stack_launches -- the number of librz kernels one rz_decode_stack call
  * (with_head != 0) or one rz_decode_layers call (with_head == 0) launches for
- * these layers, batch m and cache length max_seq, under the current settings
- * (rz_set_persistent).  Memset nodes are not kernels and are not counted.
+ * these layers, batch m and cache length max_seq.  Memset nodes are not kernels
+ * and are not counted.
  * Returns 0 for arguments the calls would reject.
  */
 int32_t rz_decode_stack_launches(const rz_layer_weights *layers, int32_t n_layers, int64_t m, int32_t max_seq,
@@ -296,20 +296,6 @@ rz_status rz_check_device_error(rz_stream stream, uint32_t *code_out);
  */
 rz_status rz_set_pdl(int enable);
 
-/*
- * rz_set_persistent -- enable or disable (default) the persistent decode kernel
- * used by rz_decode_layer and rz_decode_stack.  Enabled, a decode step of one
- * token (m == 1, head_dim 64 or 128, at most 8 query heads per kv head, rows up
- * to 16384 values, identical RoPE settings in every layer) runs as one
- * cooperative kernel per 32 layers: one CTA per SM streams all the step's
- * weights and cache rows through a shared-memory ring and meets the others at
- * grid barriers between dependent phases.  Disabled, or for any other shape,
- * the step runs as a sequence of kernels.  Both compute the same operations;
- * the results agree to f32 rounding (summation order inside the attention
- * differs).  The persistent kernel adds device error codes 0x103 (a ring wait
- * ran out) and 0x301 (a grid barrier ran out), both reported as RZ_ERR_TIMEOUT.
- */
-rz_status rz_set_persistent(int enable);
 
 #ifdef __cplusplus
 }

@@ -77,7 +77,6 @@ SIGNATURES = {
     "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
     "rz_set_pdl": [C.c_int],
-    "rz_set_persistent": [C.c_int],
     "rz_last_error": [],
     "rz_version": [],
 }

@@ -248,13 +248,6 @@ rz_status rz_set_pdl(int enable)
     return RZ_OK;
 }
 
-rz_status rz_set_persistent(int enable)
-{
-    t_last_error.clear();
-    g_use_persistent = enable != 0;
-    return RZ_OK;
-}
-
 }  // extern "C"
 
 // ---------------------------------------------------------------- layer-level helpers

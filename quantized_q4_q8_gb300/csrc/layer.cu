@@ -77,13 +77,10 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
 }
 
 // ---------------------------------------------------------------- decode layer
-// Workspace of one layer.  The attention merge counters and the grid-barrier
-// words of the persistent kernel come first, so that every path finds them at
-// the same place; the partial records are sized for the finer of the two
-// attention chunkings.
+// Workspace of one layer: the attention merge counters first, then the
+// intermediates of the step.
 struct LayerWs {
     int *counters;
-    unsigned *gbar;
     void *x8;
     float *qkv, *rope_tab, *part;
     void *a8;
@@ -99,7 +96,7 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int q_pad = (q_dim + 255) / 256 * 256;
     const int group = L.n_heads / L.n_kv_heads;
-    const int chunk = std::min(attention_chunk_len(max_seq, L.n_kv_heads, (int)m), persistent_chunk_len(L.head_dim));
+    const int chunk = attention_chunk_len(max_seq, L.n_kv_heads, (int)m);
     const int n_chunks = (max_seq + chunk - 1) / chunk;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -107,8 +104,7 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
         off += align256(bytes);
         return p;
     };
-    w.counters = reinterpret_cast<int *>(take(((size_t)m * L.n_kv_heads + 2) * 4));
-    w.gbar = base ? reinterpret_cast<unsigned *>(w.counters + m * L.n_kv_heads) : nullptr;
+    w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
     w.x8 = take(q8_bytes(m, L.hidden_pad));
     w.qkv = reinterpret_cast<float *>(take((size_t)m * (q_dim + 2 * kv_dim) * 4));
     w.rope_tab = reinterpret_cast<float *>(take((size_t)m * L.head_dim * 4));
@@ -126,19 +122,6 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
 size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
 {
     return layer_ws(L, m, max_seq, nullptr).total;
-}
-
-static PersistentWs persistent_ws(const LayerWs &w)
-{
-    PersistentWs p{};
-    p.qkv = w.qkv;
-    p.part = w.part;
-    p.res1 = w.res1;
-    p.h = w.h;
-    p.a8 = w.a8;
-    p.counters = w.counters;
-    p.gbar = w.gbar;
-    return p;
 }
 
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
@@ -185,8 +168,6 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
                                 void *workspace, cudaStream_t s, int make_table)
 {
     LayerWs w = layer_ws(L, m, kv.max_seq, static_cast<uint8_t *>(workspace));
-    if (persistent_decode_ok(L, m, kv.max_seq))
-        return launch_decode_persistent(input, &L, &kv, 1, positions, position, m, output, persistent_ws(w), s);
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int q_pad = (q_dim + 255) / 256 * 256;
     const int64_t ld_qkv = q_dim + 2 * kv_dim;
@@ -217,19 +198,11 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
 }
 
 // ---------------------------------------------------------------- stack
-// Workspace: two layer-output buffers, the normalised final hidden state, two
-// buffers for the outputs of all but the last persistent launch, then one layer
-// workspace shared by every layer.
+// Workspace: two layer-output buffers, the normalised final hidden state, then
+// one layer workspace shared by every layer.
 size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
 {
-    return 5 * align256((size_t)m * L.hidden_pad * 4) + layer_workspace_bytes(L, m, max_seq);
-}
-
-static bool same_rope(const LayerDesc *layers, int n_layers)
-{
-    for (int l = 1; l < n_layers; ++l)
-        if (layers[l].rope_theta != layers[0].rope_theta || layers[l].rope_mode != layers[0].rope_mode) return false;
-    return true;
+    return 3 * align256((size_t)m * L.hidden_pad * 4) + layer_workspace_bytes(L, m, max_seq);
 }
 
 cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
@@ -242,29 +215,15 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
     const size_t hbytes = align256((size_t)m * L0.hidden_pad * 4);
     float *buf[2] = {reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes)};
     float *normed = reinterpret_cast<float *>(ws + 2 * hbytes);
-    float *gbuf[2] = {reinterpret_cast<float *>(ws + 3 * hbytes), reinterpret_cast<float *>(ws + 4 * hbytes)};
-    void *lws = ws + 5 * hbytes;
+    void *lws = ws + 3 * hbytes;
     const float *cur = input;
     cudaError_t e = cudaSuccess;
-    if (persistent_decode_ok(L0, m, kvs[0].max_seq) && same_rope(layers, n_layers)) {
-        PersistentWs p = persistent_ws(layer_ws(L0, m, kvs[0].max_seq, static_cast<uint8_t *>(lws)));
-        p.xbuf[0] = buf[0];
-        p.xbuf[1] = buf[1];
-        p.gbuf[0] = gbuf[0];
-        p.gbuf[1] = gbuf[1];
-        const int launches = (n_layers + 31) / 32;
-        float *out = hidden_out ? hidden_out : gbuf[(launches - 1) & 1];
-        e = launch_decode_persistent(input, layers, kvs, n_layers, positions, position, m, out, p, s);
+    for (int l = 0; l < n_layers; ++l) {
+        float *out = (l == n_layers - 1 && hidden_out) ? hidden_out : buf[l & 1];
+        // the RoPE table depends only on the positions: built by the first layer
+        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s, l == 0);
         if (e != cudaSuccess) return e;
         cur = out;
-    } else {
-        for (int l = 0; l < n_layers; ++l) {
-            float *out = (l == n_layers - 1 && hidden_out) ? hidden_out : buf[l & 1];
-            // the RoPE table depends only on the positions: built by the first layer
-            e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s, l == 0);
-            if (e != cudaSuccess) return e;
-            cur = out;
-        }
     }
     if (!logits) return cudaSuccess;  // the layers only (rz_decode_layers)
     e = launch_rmsnorm(cur, out_gamma, normed, nullptr, m, L0.hidden, L0.hidden_pad, L0.eps, s);
@@ -274,9 +233,9 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
 
 int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head)
 {
+    (void)max_seq;
     const LayerDesc &L0 = layers[0];
     const int h = head ? 2 : 0;  // output RMSNorm, LM head
-    if (persistent_decode_ok(L0, m, max_seq) && same_rope(layers, n_layers)) return (n_layers + 31) / 32 + h;
     const int q_pad = (L0.n_heads * L0.head_dim + 255) / 256 * 256;
     const int gh = q4k_gemv_launch_count(m, L0.hidden_pad), gi = q4k_gemv_launch_count(m, L0.inter);
     int per_layer = 1 /* attention */ + q4k_gemv_launch_count(m, q_pad) /* O */;

@@ -1,8 +1,8 @@
-// q4k_dot.cuh -- the Q4_K x Q8_1 dot-product core shared by the stand-alone GEMV
-// kernel and the persistent decode kernel: the padded shared-memory layout of
-// the Q8_1 activations, the super-block accumulation of one lane, the packing of
-// rows into ring stages, and the staging of activations (copy of Q8_1 codes, or
-// quantisation of f32 values, optionally RMS-normalised first) into that layout.
+// q4k_dot.cuh -- the Q4_K x Q8_1 dot-product core of the GEMV kernels: the padded
+// shared-memory layout of the Q8_1 activations, the super-block accumulation of
+// one lane, the packing of rows into ring stages, and the staging of activations
+// (copy of Q8_1 codes, or quantisation of f32 values, optionally RMS-normalised
+// first) into that layout.
 //
 // Super-block layout (block_q4_K of GGML's k-quants): f16 d, f16 dmin, 12 bytes
 // of packed 6-bit scales and mins, 128 bytes of 4-bit codes; element e sits in

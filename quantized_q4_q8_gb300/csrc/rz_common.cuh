@@ -17,11 +17,9 @@ enum DevErr : unsigned {
     DEV_OK = 0,
     DEV_TIMEOUT_GEMV = 0x101,   // bulk-copy wait in a GEMV gave up
     DEV_TIMEOUT_Q40 = 0x102,
-    DEV_TIMEOUT_STEP = 0x103,   // a stage-ring wait of the persistent decode kernel gave up
     DEV_TIMEOUT_ATTN = 0x104,   // the V-row copy wait of the attention kernel gave up
     DEV_TIMEOUT_DRAIN = 0x1ff,  // draining outstanding copies gave up
     DEV_BAD_POSITION = 0x201,   // a device-resident position outside [0, max_seq)
-    DEV_TIMEOUT_GRID = 0x301,   // a grid barrier of the persistent decode kernel gave up
 };
 
 __device__ __forceinline__ void set_error(unsigned *err, unsigned code)

@@ -153,26 +153,4 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
 // kernels launched by one launch_decode_stack (with or without the head)
 int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head);
 
-// ---------------------------------------------------------------- persistent decode step
-// The decode step of a stack of identical layers as one cooperative kernel per
-// (up to) 32 layers (decode_persistent.cu).  Used by launch_decode_layer and
-// launch_decode_stack when persistent_decode_ok; the launch sequence above
-// serves every other case.
-extern bool g_use_persistent;
-
-struct PersistentWs {
-    float *xbuf[2];  // layer outputs inside one launch (ping-pong)
-    float *gbuf[2];  // outputs of the launches before the last one (ping-pong)
-    float *qkv, *part, *res1, *h;
-    void *a8;
-    int *counters;   // [m][n_kv_heads] merge counters, directly followed by
-    unsigned *gbar;  // the 2 grid-barrier words (zeroed before every launch)
-};
-
-int persistent_chunk_len(int head_dim);
-bool persistent_decode_ok(const LayerDesc &L, int64_t m, int max_seq);
-cudaError_t launch_decode_persistent(const float *input, const LayerDesc *layers, const KvDesc *kvs, int n_layers,
-                                     const int32_t *positions, int position, int64_t m, float *output,
-                                     const PersistentWs &ws, cudaStream_t s);
-
 }  // namespace rz

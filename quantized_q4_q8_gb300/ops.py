@@ -8,9 +8,9 @@ from ._lib import call, load, status
 __all__ = [
     "q8_1_size", "q4k_bytes", "q4_0_bytes",
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
-    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_set_persistent",
+    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
-    "rmsnorm", "residual_add", "check_device_error", "set_pdl", "set_persistent", "version",
+    "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
     "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
     "swiglu_ffn", "rz_swiglu_ffn_static", "attention_workspace_bytes", "attention_decode",
     "decode_layer_workspace_bytes", "decode_layer", "rz_decode_stack", "decode_stack",
@@ -84,10 +84,6 @@ def rz_check_device_error(stream=None):
 
 def rz_set_pdl(enable: bool):
     return call("rz_set_pdl", 1 if enable else 0)
-
-
-def rz_set_persistent(enable: bool):
-    return call("rz_set_persistent", 1 if enable else 0)
 
 
 # ------------------------------------------------------------------ tensor helpers
@@ -167,10 +163,6 @@ def check_device_error(stream=None):
 
 def set_pdl(enable: bool):
     rz_set_pdl(enable)
-
-
-def set_persistent(enable: bool):
-    rz_set_persistent(enable)
 
 
 def version() -> str:

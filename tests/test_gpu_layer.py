@@ -28,15 +28,6 @@ def rz():
     return rz
 
 
-@pytest.fixture(params=["persistent", "launches"])
-def step_path(request, rz):
-    """Run the test through the persistent decode kernel and through the launch
-    sequence (rz_set_persistent)."""
-    rz.set_persistent(request.param == "persistent")
-    yield request.param
-    rz.set_persistent(False)
-
-
 def assert_rel(gpu, ref, tol=1e-3, what=""):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
@@ -195,7 +186,7 @@ def test_swiglu_ffn_parity(rz, shape, m):
 
 # ----------------------------------------------------------------------------- decode layer
 @pytest.mark.parametrize("pos", [127, 0])
-def test_decode_layer_qwen2_parity(rz, step_path, pos):
+def test_decode_layer_qwen2_parity(rz, pos):
     """The Qwen2-0.5B-shaped layer at position 127 (and the first token)."""
     sh = S.QWEN2
     L = S.layer(sh, "qwen2.l0")
@@ -234,7 +225,7 @@ def test_decode_layer_batched_positions(rz):
         assert_rel(out[t], ref, what=f"token {t} at {p}")
 
 
-def test_decode_layer_llama_parity(rz, step_path):
+def test_decode_layer_llama_parity(rz):
     sh = S.LLAMA7B
     L = S.layer(sh, "llama.l0")
     pos, max_seq = 128, 256
@@ -247,7 +238,7 @@ def test_decode_layer_llama_parity(rz, step_path):
     assert_rel(out[0], ref, what="llama layer")
 
 
-def test_decode_layer_in_place(rz, step_path):
+def test_decode_layer_in_place(rz):
     import torch
     sh = S.QWEN2
     L = S.layer(sh, "qwen2.ip")
@@ -261,7 +252,7 @@ def test_decode_layer_in_place(rz, step_path):
 
 
 # ----------------------------------------------------------------------------- stack
-def test_decode_stack_qwen2_two_layers_and_lm_head(rz, step_path):
+def test_decode_stack_qwen2_two_layers_and_lm_head(rz):
     """Two Qwen2-shaped layers, output norm and the 151936 x 896 Q4_0 LM head."""
     sh = S.QWEN2
     vocab = 151936
