@@ -162,10 +162,72 @@ def max_over_ranks(pg, v: float, device) -> float:
 
 
 # ----------------------------------------------------------------------------- workloads
+def gemv_bytes(out_dim: int, in_dim: int, m: int) -> int:
+    """Algorithmic bytes of one Q4_K x Q8_1 GEMV: quantised weights + Q8_1
+    activations (1.25 B per value) + f32 outputs."""
+    return out_dim * (in_dim // 256) * S.Q4K_BYTES + m * in_dim * 5 // 4 + m * out_dim * 4
+
+
+def time_graph(graph, stream, reps: int) -> float:
+    """ms per replay of a captured graph, CUDA events on the launching stream."""
+    import torch
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def capture(fn, stream):
+    """fn() once eagerly (kernel attributes), then captured into a CUDA graph."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def measure_gemv(rz, out_dim: int, in_dim: int, m: int, dev, stream, launches: int = 64,
+                 reps: int = 30):
+    """One Q4_K x Q8_1 GEMV shape timed as back-to-back launches in a CUDA graph, the
+    weights rotated through distinct copies larger than twice the L2 together (no
+    launch finds its weights in L2).  Returns us per launch, GB/s, copies."""
+    import torch
+    wbytes = out_dim * (in_dim // 256) * S.Q4K_BYTES
+    ncopies = max(2, int(np.ceil(2 * L2_BYTES / wbytes)) + 1)
+    w0 = S.q4k_weight_device(f"sweep.{out_dim}.{in_dim}", out_dim, in_dim, dev)
+    ws = [w0] + [w0.clone() for _ in range(ncopies - 1)]
+    x = torch.randn((m, in_dim), device=dev, generator=S.torch_gen(f"sweep.x.{in_dim}.{m}", dev))
+    q8 = rz.q8_1_quantize(x)
+    y = torch.empty((m, out_dim), dtype=torch.float32, device=dev)
+
+    def launch():
+        for i in range(launches):
+            rz.rz_q4k_q8_gemv(ws[i % ncopies], q8, y, m, out_dim, in_dim, stream=stream)
+
+    g = capture(launch, stream)
+    ms = time_graph(g, stream, reps) / launches
+    del g, ws
+    us = ms * 1e3
+    return {"us": round(us, 3), "gbs": round(gemv_bytes(out_dim, in_dim, m) / (ms * 1e-3) / 1e9, 1),
+            "weight_copies": ncopies}
+
+
 class GemvWorkload:
-    """Q4_K x Q8_1 GEMV, out 4096 x in 14336 (the largest shape of the Llama sweep)."""
+    """Q4_K x Q8_1 GEMV, out 4096 x in 14336 (the largest shape of the Llama sweep),
+    launched back to back over weight copies larger than twice the L2."""
     out_dim, in_dim = 4096, 14336
     kernel_file = "gemv_q4k.cu"
+    launches = 64
 
     def __init__(self, m: int):
         self.m = m
@@ -175,71 +237,77 @@ class GemvWorkload:
         import torch
         import quantized_q4_q8_gb300 as rz
         self.rz = rz
-        self.w_host = S.q4k_weight(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim, self.in_dim)
-        self.wbytes = self.w_host.size
-        ncopies = max(2, int(np.ceil(2 * L2_BYTES / self.wbytes)) + 1)
-        w0 = torch.from_numpy(self.w_host).to(dev)
-        self.ws = [w0] + [w0.clone() for _ in range(ncopies - 1)]
-        self.x_host = S.normal(f"sweep.x.{self.in_dim}.{self.m}", (self.m, self.in_dim))
-        self.x = torch.from_numpy(self.x_host).to(dev)
+        self.wbytes = self.out_dim * (self.in_dim // 256) * S.Q4K_BYTES
+        self.ncopies = max(2, int(np.ceil(2 * L2_BYTES / self.wbytes)) + 1)
+        w0 = S.q4k_weight_device(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim, self.in_dim, dev)
+        self.ws = [w0] + [w0.clone() for _ in range(self.ncopies - 1)]
+        self.x = torch.randn((self.m, self.in_dim), device=dev,
+                             generator=S.torch_gen(f"sweep.x.{self.in_dim}.{self.m}", dev))
         self.q8 = rz.q8_1_quantize(self.x)
         self.y = torch.empty((self.m, self.out_dim), dtype=torch.float32, device=dev)
-        self.i = 0
+        self.graph = None
         # pinned host buffers for the end-to-end leg
-        self.x_pin = torch.from_numpy(self.x_host).pin_memory()
+        self.x_pin = self.x.cpu().pin_memory()
         self.y_pin = torch.empty((self.m, self.out_dim), dtype=torch.float32).pin_memory()
 
     def bytes_per_step(self):
-        return self.wbytes + S.Q4K_BYTES * 0 + self.m * self.in_dim * 5 // 4 + self.m * self.out_dim * 4
+        return self.launches * gemv_bytes(self.out_dim, self.in_dim, self.m)
 
     def launches_per_step(self):
-        return 1
+        return self.launches
+
+    def _launch(self, stream):
+        for i in range(self.launches):
+            self.rz.rz_q4k_q8_gemv(self.ws[i % self.ncopies], self.q8, self.y, self.m, self.out_dim,
+                                   self.in_dim, stream=stream)
 
     def step(self, stream):
-        w = self.ws[self.i % len(self.ws)]
-        self.i += 1
-        self.rz.rz_q4k_q8_gemv(w, self.q8, self.y, self.m, self.out_dim, self.in_dim, stream=stream)
+        if self.graph is None:
+            self.graph = capture(lambda: self._launch(stream), stream)
+        self.graph.replay()
 
     def e2e_step(self, stream):
-        """host x -> device, quantise, GEMV, device y -> host (through the C ABI)."""
+        """host x -> device, quantise, the GEMVs, device y -> host (through the C ABI)."""
         self.x.copy_(self.x_pin, non_blocking=True)
         self.rz.rz_q8_1_quantize(self.x, self.q8, self.m, self.in_dim, stream=stream)
-        self.step(stream)
+        self.graph.replay()
         self.y_pin.copy_(self.y, non_blocking=True)
 
     def e2e_bytes(self):
         return self.m * self.in_dim * 4, self.m * self.out_dim * 4
 
     def e2e_launches(self):
-        return 2
+        return self.launches + 1
 
     def dominant(self):
-        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.bytes_per_step(),
-                "launches_per_step": 1}
+        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": gemv_bytes(self.out_dim, self.in_dim, self.m),
+                "launches_per_step": self.launches}
+
+    def dominant_time(self, stream):
+        return None
 
     def cpu_sample(self, min_seconds: float = 0.0):
         """The oracle on the same GEMV (all rows), repeated until min_seconds."""
         import oracle
-        if not hasattr(self, "w_host"):
-            self.w_host = S.q4k_weight(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim,
-                                       self.in_dim)
-            self.x_host = S.normal(f"sweep.x.{self.in_dim}.{self.m}", (self.m, self.in_dim))
-            self.wbytes = self.w_host.size
-        x8 = oracle.q8_1_quantize(self.x_host)
+        cores = oracle.use_all_cores(True)
+        w = S.q4k_weight(f"sweep.{self.out_dim}.{self.in_dim}", self.out_dim, self.in_dim)
+        x8 = oracle.q8_1_quantize(S.normal(f"sweep.x.{self.in_dim}.{self.m}", (self.m, self.in_dim)))
         reps, t_total = 0, 0.0
         while reps == 0 or t_total < min_seconds:
             t0 = time.perf_counter()
-            oracle.q4k_q8_gemv(self.w_host, x8, self.m, self.out_dim, self.in_dim)
+            oracle.q4k_q8_gemv(w, x8, self.m, self.out_dim, self.in_dim)
             t_total += time.perf_counter() - t0
             reps += 1
         dt = t_total / reps
-        return {"value": self.bytes_per_step() / dt / 1e9, "unit": "GB/s", "cores": 1,
-                "kind": "oracle", "sample": f"the whole {self.out_dim}x{self.in_dim} GEMV "
-                f"(m={self.m}) x {reps}, single-threaded C oracle, {dt:.2f} s each"}
+        return {"value": gemv_bytes(self.out_dim, self.in_dim, self.m) / dt / 1e9, "unit": "GB/s",
+                "cores": cores, "kind": "oracle",
+                "sample": f"the whole {self.out_dim}x{self.in_dim} GEMV (m={self.m}) x {reps}, C oracle "
+                          f"on {cores} host threads (rows split over threads), {dt:.3f} s each"}
 
     def config(self):
         return {"workload": self.name, "out_dim": self.out_dim, "in_dim": self.in_dim,
-                "batch_tokens": self.m, "weight_copies": len(self.ws),
+                "batch_tokens": self.m, "launches_per_step": self.launches,
+                "weight_copies": self.ncopies,
                 "l2": "weights rotated through copies > 2x L2"}
 
     def config_ref(self):
@@ -249,15 +317,12 @@ class GemvWorkload:
     def cpu_baseline(self):
         return self.cpu_sample(min_seconds=10.0)
 
-    def dominant_time(self, stream):
-        return None
-
 
 class StackWorkload:
     """One decode step of the 32-layer Llama-7B-shaped Q4_K stack + Q4_0 LM head."""
-    n_layers = S.LLAMA_LAYERS
     vocab = S.LLAMA_VOCAB
     max_seq = S.LLAMA_MAX_SEQ
+    kernel_file = "gemv_q4k.cu"
 
     def __init__(self, m: int, position: int, n_layers: int = S.LLAMA_LAYERS):
         self.m = m
@@ -282,10 +347,19 @@ class StackWorkload:
         head = m * sh.hidden * 4 + m * self.vocab * 4
         return self.weight_bytes() + self.n_layers * per_layer + head
 
-    def gemv_bytes(self):
+    def fused_gemv_bytes(self):
+        """Algorithmic bytes of the step's four GEMV launches per layer, as they run
+        in the step: Q|K|V (f32 input normalised and quantised inside, gamma), O
+        (Q8_1 input, residual), gate/up (f32 input, gamma, h out), down (f32 h in,
+        residual)."""
         sh, m = self.shape, self.m
-        return self.n_layers * sum(o * (i // 256) * S.Q4K_BYTES + m * i * 5 // 4 + m * o * 4
-                                   for o, i in sh.weight_shapes().values())
+        W = {nm: o * (i // 256) * S.Q4K_BYTES for nm, (o, i) in sh.weight_shapes().items()}
+        hp, q, kv, inter = sh.hidden_pad, sh.q_dim, sh.kv_dim, sh.inter
+        qkv = W["wq"] + W["wk"] + W["wv"] + m * hp * 4 + sh.hidden * 4 + m * (q + 2 * kv) * 4
+        o = W["wo"] + m * sh.q_pad * 5 // 4 + 2 * m * hp * 4
+        gu = W["wgate"] + W["wup"] + m * hp * 4 + sh.hidden * 4 + m * inter * 4
+        dn = W["wdown"] + m * inter * 4 + 2 * m * hp * 4
+        return self.n_layers * (qkv + o + gu + dn)
 
     def head_bytes(self):
         sh, m = self.shape, self.m
@@ -293,17 +367,9 @@ class StackWorkload:
             m * self.vocab * 4
 
     def launches_per_step(self):
-        # the library's own count: the persistent kernel (one per 32 layers) + output
-        # norm + LM head, or RoPE table + 5 per layer + output norm + LM head
+        # the library's own count: RoPE table + the launches of every layer + output
+        # norm + LM head
         return self.stack.launches(self.m, with_head=True)
-
-    @property
-    def persistent(self):
-        return self.stack.launches(self.m, with_head=False) == (self.n_layers + 31) // 32
-
-    @property
-    def kernel_file(self):
-        return "decode_persistent.cu" if self.persistent else "gemv_q4k.cu"
 
     def setup(self, dev):
         import torch
@@ -333,24 +399,14 @@ class StackWorkload:
         self.logits_pin = torch.empty((self.m, self.vocab), dtype=torch.float32).pin_memory()
         self.graph = None
         self.gemv_graph = None
-        self.layers_graph = None
 
     def _launch(self, stream):
         self.rz.rz_decode_stack(self.x, self.stack, None, self.position, self.m, self.hid,
                                 self.logits, self.ws, stream=stream)
 
-    def capture(self, stream):
-        import torch
-        self._launch(stream)          # eager warm-up outside the graph (sets attributes)
-        torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=stream):
-            self._launch(stream)
-        torch.cuda.synchronize()
-
     def step(self, stream):
         if self.graph is None:
-            self.capture(stream)
+            self.graph = capture(lambda: self._launch(stream), stream)
         self.graph.replay()
 
     def e2e_step(self, stream):
@@ -366,76 +422,51 @@ class StackWorkload:
         return self.launches_per_step()
 
     def dominant(self):
-        if self.persistent:
-            n = (self.n_layers + 31) // 32
-            return {"kernel": "decode_persistent_kernel",
-                    "bytes_per_launch": (self.bytes_per_step() - self.head_bytes()) / n,
-                    "launches_per_step": n}
-        n = self.n_layers * 7
-        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.gemv_bytes() / n,
-                "launches_per_step": n}
-
-    def _time_graph(self, graph, stream, reps):
-        import torch
-        graph.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+        n = self.n_layers * 4
+        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.fused_gemv_bytes() / n,
+                "launches_per_step": n,
+                "what": "the step's own four GEMV launches per layer (Q|K|V with the RMSNorm/Q8_1 "
+                        "prologue, O + residual, gate/up with the norm prologue and SiLU*up, down "
+                        "with the Q8_1 prologue + residual), all layers back to back in one graph"}
 
     def dominant_time(self, stream, reps=20):
-        """Average launch duration of the dominant kernel, CUDA events on the stream.
-        Persistent path: the step's layers alone (rz_decode_layers: the persistent
-        kernel, after a memset of its 8 barrier bytes) replayed as a graph.  Launch
-        sequence: the 224 weight matrices of the 32 layers launched back to back
-        (CUDA graph) against the layer's Q8_1 activation."""
+        """Average launch duration of the dominant kernel inside the step: the four
+        GEMV launches of every layer, with the same fused prologues and epilogues the
+        step runs (rz_rmsnorm_q4k_gemv, rz_q4k_q8_gemv_ex with a residual,
+        rz_swiglu_ffn), replayed back to back as one CUDA graph (CUDA events on the
+        stream).  The attention, the RoPE table and the LM head are left out."""
         import torch
-        rz = self.rz
-        sh = self.shape
-        if self.persistent:
-            if self.layers_graph is None:
-                self.layers_out = torch.empty((self.m, sh.hidden_pad), dtype=torch.float32,
-                                              device=self.x.device)
-                def launch():
-                    rz.rz_decode_layers(self.x, self.stack, None, self.position, self.m,
-                                        self.layers_out, self.ws, stream=stream)
-                launch()
-                torch.cuda.synchronize()
-                self.layers_graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(self.layers_graph, stream=stream):
-                    launch()
-                torch.cuda.synchronize()
-            return self._time_graph(self.layers_graph, stream, reps) / self.dominant()["launches_per_step"]
+        rz, sh, m, dev = self.rz, self.shape, self.m, self.x.device
         if self.gemv_graph is None:
-            dev = self.x.device
-            self.gx = {i: rz.q8_1_quantize(torch.randn((self.m, i), device=dev,
-                                                        generator=S.torch_gen(f"gx{i}", dev)))
-                       for i in {i for _, i in sh.weight_shapes().values()}}
-            self.gy = torch.empty((self.m, max(o for o, _ in sh.weight_shapes().values())),
-                                  device=dev)
+            self.g_in = self.x
+            self.g_qkv = torch.empty((m, sh.q_dim + 2 * sh.kv_dim), dtype=torch.float32, device=dev)
+            self.g_a8 = rz.q8_1_quantize(torch.randn((m, sh.q_pad), device=dev,
+                                                      generator=S.torch_gen("dom.att", dev)))
+            self.g_res = torch.empty((m, sh.hidden_pad), dtype=torch.float32, device=dev)
+            self.g_out = torch.empty((m, sh.hidden_pad), dtype=torch.float32, device=dev)
+            self.g_ws = rz.workspace(rz.swiglu_ffn_workspace_bytes(m, sh.hidden_pad, sh.inter), dev)
+
             def launch():
                 for dl in self.dls:
-                    for nm, (o, i) in sh.weight_shapes().items():
-                        rz.rz_q4k_q8_gemv(dl.t[nm], self.gx[i], self.gy, self.m, o, i,
-                                          stream=stream)
-            launch()
-            torch.cuda.synchronize()
-            self.gemv_graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(self.gemv_graph, stream=stream):
-                launch()
-            torch.cuda.synchronize()
-        return self._time_graph(self.gemv_graph, stream, 5) / (self.n_layers * 7)
+                    t = dl.t
+                    rz.rz_rmsnorm_q4k_gemv(self.g_in, sh.hidden_pad, t["attn_gamma"], sh.hidden, sh.eps,
+                                           [t["wq"], t["wk"], t["wv"]], [sh.q_dim, sh.kv_dim, sh.kv_dim],
+                                           None, self.g_qkv, sh.q_dim + 2 * sh.kv_dim, m, sh.hidden_pad,
+                                           stream=stream)
+                    rz.rz_q4k_q8_gemv_ex(t["wo"], self.g_a8, None, self.g_in, self.g_res, sh.hidden_pad, m,
+                                         sh.hidden, sh.q_pad, stream=stream)
+                    rz.swiglu_ffn(self.g_res, t["ffn_gamma"], t["wgate"], t["wup"], t["wdown"], sh.hidden,
+                                  sh.hidden_pad, sh.inter, sh.eps, out=self.g_out, ws=self.g_ws,
+                                  stream=stream)
+
+            self.gemv_graph = capture(launch, stream)
+        return time_graph(self.gemv_graph, stream, reps) / self.dominant()["launches_per_step"]
 
     def cpu_sample(self, n_sample_layers: int = 1):
         """The oracle on n_sample_layers layers of the same shape plus the LM head, one
         token, timed on this host; the step time is extrapolated from the mean layer time."""
         import oracle
+        cores = oracle.use_all_cores(True)
         sh = self.shape
         kc, vc = S.kv_prefill(sh, "cpu.kv", self.position + 1, self.position, 1)
         x = S.hidden_input("cpu.x", 1, sh.hidden, sh.hidden_pad)[0]
@@ -458,15 +489,15 @@ class StackWorkload:
         t_step = (self.n_layers * t_layer + t_head) * self.m
         one_token = StackWorkload(1, self.position, self.n_layers)
         return {"value": one_token.bytes_per_step() * self.m / t_step / 1e9, "unit": "GB/s",
-                "cores": 1, "kind": "oracle",
+                "cores": cores, "kind": "oracle",
                 "tokens_per_s": self.m / t_step,
-                "sample": f"{n_sample_layers} of {self.n_layers} layers (single-threaded C "
-                          f"oracle, mean {t_layer:.2f} s per layer) + the Q4_0 LM head "
-                          f"({t_head:.2f} s), one token at position {self.position}; step time "
-                          f"extrapolated as {self.n_layers} x layer + head per token"}
+                "sample": f"{n_sample_layers} of {self.n_layers} layers (C oracle on {cores} host "
+                          f"threads, rows and heads split over threads; mean {t_layer:.3f} s per layer) "
+                          f"+ the Q4_0 LM head ({t_head:.3f} s), one token at position {self.position}; "
+                          f"step time extrapolated as {self.n_layers} x layer + head per token"}
 
     def cpu_baseline(self):
-        return self.cpu_sample(n_sample_layers=16)
+        return self.cpu_sample(n_sample_layers=8)
 
     def config_ref(self):
         return {"workload": self.name, "layers": self.n_layers, "hidden": self.shape.hidden,
@@ -479,9 +510,7 @@ class StackWorkload:
 
     def config(self):
         c = self.config_ref()
-        c["launch"] = ("one CUDA graph per step: the persistent decode kernel (cooperative, one CTA "
-                       "per SM, all layers) + output RMSNorm + LM head") if self.persistent else \
-            "one CUDA graph per step (PDL edges between kernels)"
+        c["launch"] = "one CUDA graph per step (PDL edges between kernels)"
         return c
 
 
@@ -495,13 +524,52 @@ def make_workload(args):
 
 
 # ----------------------------------------------------------------------------- arms
+# GEMV shapes reported beside every stack run: the target shape of the Llama sweep
+# at one token, and the widest batched-decode GEMV at 16 tokens.
+SUBRECORD_GEMVS = [(4096, 14336, 1), (14336, 4096, 16)]
+MIN_TIMED_S = 1.0
+
+
+def run_timed_blocks(wl, stream, steps, pg, dev):
+    """Blocks of exactly `steps` steps, each bracketed by a barrier and a device
+    synchronisation and timed with CUDA events on the launching stream, repeated
+    until the blocks add up to MIN_TIMED_S (so that the clock record covers a
+    steady stretch).  Returns the median block's ms per step (max over ranks) and
+    the number of blocks."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    per_step, total_s = [], 0.0
+    while True:
+        barrier(pg)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                wl.step(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = e0.elapsed_time(e1)
+        per_step.append(ms / steps)
+        total_s += ms * 1e-3
+        # every rank runs the same number of blocks: the decision is rank 0's
+        done = total_s >= MIN_TIMED_S or len(per_step) >= 10000
+        if pg is not None:
+            t = torch.tensor([1.0 if done else 0.0], device=dev)
+            pg.broadcast(t, 0)
+            done = bool(t.item())
+        if done:
+            break
+    return max_over_ranks(pg, statistics.median(per_step), dev), len(per_step)
+
+
 def run_rz(args, world, rank, local, pg):
     import torch
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     import quantized_q4_q8_gb300 as rz
     rz.load()
-    rz.set_persistent(args.persistent)
     wl = make_workload(args)
     wl.setup(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -521,31 +589,23 @@ def run_rz(args, world, rank, local, pg):
     # ---- device-timed region
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else local)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     barrier(pg)
     torch.cuda.synchronize()
     if rank == 0:
         clocks.start()
         time.sleep(0.3)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            wl.step(stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(pg)
+    ms, blocks = run_timed_blocks(wl, stream, args.steps, pg, dev)
     clk = clocks.stop() if rank == 0 else None
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(pg, ms, dev)
 
     # ---- dominant kernel: average launch duration over back-to-back launches
     dom = wl.dominant()
     dom_ms = wl.dominant_time(stream)
-    if dom_ms is None:   # the step is one launch of the dominant kernel
+    if dom_ms is None:   # the step is back-to-back launches of the dominant kernel
         dom_ms = ms / dom["launches_per_step"]
 
     # ---- end to end through the C ABI with host buffers
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             wl.e2e_step(stream)
@@ -559,34 +619,51 @@ def run_rz(args, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg)
     e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps, dev)
+
+    # ---- the GEMV shapes of the metric, reported beside the step
+    peak, peak_kind = measured_peaks()
+    gemvs = {}
+    if not args.no_subrecords:
+        for o, i, m in SUBRECORD_GEMVS:
+            r = measure_gemv(rz, o, i, m, dev, stream)
+            r["frac"] = round(r["gbs"] / peak, 4)
+            gemvs[f"{o}x{i}_m{m}"] = r
     st, code = rz.check_device_error(stream)
     if st != 0:
         raise RuntimeError(f"device error word after timing: 0x{code:x}")
 
     bytes_step = wl.bytes_per_step()
     value = world * bytes_step / (ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
     achieved = dom["bytes_per_launch"] / (dom_ms * 1e-3) / 1e9
     traffic = profile_traffic(wl.kernel_file, wl.name)
+    cfg = wl.config()
+    cfg["timed_blocks"] = blocks
+    cfg["timed_region"] = (f"{blocks} blocks of {args.steps} steps (median block), at least "
+                           f"{MIN_TIMED_S:g} s in total")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "q4k_x_q8_1_int8dot_f32",
         "data": "synthetic (seeded, distributions of the workload definition)",
-        "config": wl.config(),
+        "config": cfg,
         "pct_of_peak": round(100 * value / world / peak, 2),
         "tokens_per_s": round(world * wl.m / (ms * 1e-3), 2),
         "tokens_per_s_per_layer_stack": round(world * wl.m / (ms * 1e-3), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": dom["kernel"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     "kernel": dom["kernel"], "launch_us": round(dom_ms * 1e3, 3),
+                     "bytes_per_launch": int(dom["bytes_per_launch"]),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "gemv": gemvs,
         "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": wl.e2e_bytes()[0], "d2h_bytes_per_step": wl.e2e_bytes()[1],
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": args.steps * wl.launches_per_step(),
+        "gpu_launches": blocks * args.steps * wl.launches_per_step(),
         "clocks": clk,
     }
+    if "what" in dom:
+        line["roofline"]["what"] = dom["what"]
     if cpu_line is not None:
         line["cpu_baseline"] = cpu_line
     if rank == 0:
@@ -620,13 +697,13 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 1000 for the stack, 2000 for the GEMV)")
+                    help="steps per timed block (default: 200 for the stack, 50 for the GEMV)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="rz", choices=["rz", "reference"])
     ap.add_argument("--workload", default="stack", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--persistent", action="store_true",
-                    help="run the decode step as the persistent kernel instead of the launch sequence")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="skip the GEMV shapes reported beside the step")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--position", type=int, default=1024)
     ap.add_argument("--layers", type=int, default=S.LLAMA_LAYERS,
@@ -635,9 +712,9 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     if args.steps is None:
-        args.steps = 1000 if args.workload == "stack" else 2000
+        args.steps = 200 if args.workload == "stack" else 50
         if args.impl == "reference":
-            args.steps = 20
+            args.steps = 3
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks have no work
         world = int(os.environ.get("WORLD_SIZE", "1"))

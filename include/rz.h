@@ -112,6 +112,40 @@ rz_status rz_q4k_q8_subblock_dots(const void *w, const void *q8, int32_t *I, int
                                   int64_t in_dim, rz_stream stream);
 
 /*
+ * rz_q4k_q8_gemv_ex -- the same GEMV with an epilogue:
+ *     y[t][r] = (W x_t)_r + bias[r]           (bias != NULL; the QKV and head biases
+ *                                              of preload_qkv_bias in cached.rs)
+ *     y[t][r] = (W x_t)_r + residual[t][r]    (residual != NULL; steps 6-7 and 9-10 of
+ *                                              transformer_layer_gpu_true_dp4a)
+ *     y[t][r] = (W x_t)_r                     (both NULL)
+ *   bias f32 [out_dim] (4-byte aligned); residual, y f32 [m][ld] with row stride ld
+ *   (0 = out_dim; ld >= out_dim); y may alias residual.  A bias and a residual in
+ *   one call: RZ_ERR_UNSUPPORTED.  Other arguments and checks as rz_q4k_q8_gemv.
+ */
+rz_status rz_q4k_q8_gemv_ex(const void *w, const void *q8, const float *bias, const float *residual, float *y,
+                            int64_t ld, int64_t m, int64_t out_dim, int64_t in_dim, rz_stream stream);
+
+/*
+ * rz_rmsnorm_q4k_gemv -- steps 1-3 of transformer_layer_gpu_true_dp4a in one
+ * launch: RMSNorm of x over its first n values with gamma (zero padding after n),
+ * Q8_1 quantisation of the normed row (bit-identical to rz_rmsnorm's q8 output),
+ * then up to three Q4_K GEMVs against that one Q8_1 activation, their outputs
+ * side by side in y (the Q | K | V projections):
+ *     y[t][off_k + r] = (W_k q8(norm(x_t)))_r (+ bias[k][r]),  off_k = rows[0] + ... + rows[k-1]
+ *   x      f32 [m][ldx], in_dim values per row are read (ldx >= in_dim)
+ *   gamma  f32 [n]; n <= in_dim; in_dim % 256 == 0
+ *   w      host array of n_mats (1..3) device pointers to Q4_K [rows[k]][in_dim]
+ *   bias   host array of n_mats device pointers (each may be NULL), or NULL
+ *   y      f32 [m][ldy], ldy >= rows[0] + ... + rows[n_mats-1]
+ *   x, gamma, y 16-byte aligned, ldx and ldy multiples of 4.  Every CTA normalises and
+ *   quantises the whole row (m * in_dim * 1.25 B of shared memory must fit, else
+ *   RZ_ERR_UNSUPPORTED).
+ */
+rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, int64_t n, float eps, int32_t n_mats,
+                              const void *const *w, const int64_t *rows, const float *const *bias, float *y,
+                              int64_t ldy, int64_t m, int64_t in_dim, rz_stream stream);
+
+/*
  * rz_q4_0_gemv -- y = W x for Q4_0 weights and f32 activations (the LM head of
  * GpuModelQ4::forward, q4_0_gemv_into; step 5 of that function).
  *   w  Q4_0 [out_dim][in_dim]   x  f32 [m][in_dim]   y  f32 [m][out_dim]
@@ -162,13 +196,21 @@ rz_status rz_residual_add(const float *a, const float *b, float *out, int64_t n,
  * pad_and_upload_input), inter % 256 == 0, head_dim % 32 == 0 and <= 256,
  * n_heads % n_kv_heads == 0 with at most 16 query heads per kv head.
  * rope_mode 0 rotates adjacent pairs (2i, 2i+1), 1 rotates (i, i + head_dim/2);
- * the angle of pair i at position p is p * rope_theta^(-2i/head_dim). */
+ * the angle of pair i at position p is p * rope_theta^(-2i/head_dim).
+ * Fused Q|K|V layout (OwnedQKVWeights::Fused of realizar 0.8.4
+ * clone_layer_weights.rs): wk = wv = NULL and wq holds the one matrix
+ * [n_heads*head_dim + 2*n_kv_heads*head_dim][hidden_pad] (Q rows, then K, then V).
+ * Biases (the Qwen2 QKV bias of preload_qkv_bias in realizar 0.8.5 cached.rs):
+ * bq [n_heads*head_dim], bk, bv [n_kv_heads*head_dim] f32, each NULL for none,
+ * added to the projections before RoPE; with the fused layout bq holds the fused
+ * bias [q_dim + 2*kv_dim] and bk, bv must be NULL.  Biases need 4-byte alignment. */
 typedef struct {
     const void *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
     const float *attn_gamma, *ffn_gamma;
     int32_t hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter;
     float eps, rope_theta;
     int32_t rope_mode;
+    const float *bq, *bk, *bv;
 } rz_layer_weights;
 
 /* f32 KV cache of one layer.  Row p of sequence t (token t of a batch) is at
@@ -295,6 +337,21 @@ rz_status rz_check_device_error(rz_stream stream, uint32_t *code_out);
  * weights while the previous kernel finishes; results are identical either way.
  */
 rz_status rz_set_pdl(int enable);
+
+/*
+ * rz_debug_stall_next_gemv -- test aid for the bounded-wait error path (off by
+ * default).  The next Q4_K GEMV launch of this process leaves the first weight
+ * stage of its CTA 0 unissued and bounds every wait of that CTA by wait_limit
+ * polls (1024 <= wait_limit <= 2^22, else RZ_ERR_INVALID_ARG).  Its consumer warps
+ * then run out of their wait, record code 0x101 in the device error word and
+ * stop; the CTA still waits for every copy it did issue before it exits, so no
+ * copy outlives the kernel.  rz_check_device_error then returns RZ_ERR_TIMEOUT,
+ * and the output rows of CTA 0 of that launch are undefined.  One shot: the
+ * setting clears itself at that launch.  The pages return errors instead of
+ * panicking (GpuError in realizar 0.8.5 forward_utils.rs); this checks that a
+ * wait that cannot complete ends in such an error and not in a hung GPU.
+ */
+rz_status rz_debug_stall_next_gemv(uint32_t wait_limit);
 
 
 #ifdef __cplusplus

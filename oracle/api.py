@@ -16,7 +16,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = [
-    "lib", "f32_to_f16", "f16_to_f64",
+    "lib", "use_all_cores", "threads", "f32_to_f16", "f16_to_f64",
     "q4k_unpack", "q4k_pack", "q4k_dequantize",
     "q4_0_unpack", "q4_0_pack", "q4_0_dequantize",
     "q8_1_quantize", "q8_1_dequantize", "q8_1_fields", "q8_1_size",
@@ -29,15 +29,30 @@ __all__ = [
 Q4K_BYTES = 144
 Q4_0_BYTES = 18
 
-_lib = None
+_libs = {}
+_use_omp = False
 
 
 def lib():
-    global _lib
-    if _lib is None:
-        _lib = C.CDLL(_build.build())
-        _declare(_lib)
-    return _lib
+    """The oracle library: single-threaded, unless use_all_cores(True) was called."""
+    key = "omp" if _use_omp else "st"
+    if key not in _libs:
+        L = C.CDLL(_build.build(openmp=_use_omp))
+        _declare(L)
+        _libs[key] = L
+    return _libs[key]
+
+
+def use_all_cores(enable: bool) -> int:
+    """Switch every following call to the all-core build (OpenMP over output rows
+    and attention heads; identical results) or back; returns its thread count."""
+    global _use_omp
+    _use_omp = bool(enable)
+    return threads()
+
+
+def threads() -> int:
+    return int(lib().orc_threads())
 
 
 _u8p = C.POINTER(C.c_uint8)
@@ -56,11 +71,13 @@ class _OrcLayer(C.Structure):
         ("hidden", _i64), ("hidden_pad", _i64), ("n_heads", _i64),
         ("n_kv_heads", _i64), ("head_dim", _i64), ("inter", _i64),
         ("eps", C.c_float), ("rope_theta", C.c_double), ("rope_mode", C.c_int),
+        ("bq", _f32p), ("bk", _f32p), ("bv", _f32p),
     ]
 
 
 def _declare(L):
     sig = {
+        "orc_threads": (C.c_int, []),
         "orc_f32_to_f16": (C.c_uint16, [C.c_float]),
         "orc_f16_to_f64": (C.c_double, [C.c_uint16]),
         "orc_f32_to_f16_array": (None, [_f32p, _u16p, _i64]),
@@ -317,12 +334,18 @@ class LayerWeights:
     eps: float
     rope_theta: float
     rope_mode: int
+    bq: np.ndarray = None
+    bk: np.ndarray = None
+    bv: np.ndarray = None
 
     def _struct(self):
         keep = {k: np.ascontiguousarray(getattr(self, k)) for k in
                 ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown")}
         keep["attn_gamma"] = _f32(self.attn_gamma)
         keep["ffn_gamma"] = _f32(self.ffn_gamma)
+        for b in ("bq", "bk", "bv"):
+            if getattr(self, b) is not None:
+                keep[b] = _f32(getattr(self, b))
         s = _OrcLayer(
             wq=_p(keep["wq"], C.c_uint8), wk=_p(keep["wk"], C.c_uint8),
             wv=_p(keep["wv"], C.c_uint8), wo=_p(keep["wo"], C.c_uint8),
@@ -332,7 +355,10 @@ class LayerWeights:
             ffn_gamma=_p(keep["ffn_gamma"], C.c_float),
             hidden=self.hidden, hidden_pad=self.hidden_pad, n_heads=self.n_heads,
             n_kv_heads=self.n_kv_heads, head_dim=self.head_dim, inter=self.inter,
-            eps=self.eps, rope_theta=self.rope_theta, rope_mode=self.rope_mode)
+            eps=self.eps, rope_theta=self.rope_theta, rope_mode=self.rope_mode,
+            bq=_p(keep["bq"], C.c_float) if "bq" in keep else None,
+            bk=_p(keep["bk"], C.c_float) if "bk" in keep else None,
+            bv=_p(keep["bv"], C.c_float) if "bv" in keep else None)
         return s, keep
 
 

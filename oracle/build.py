@@ -15,24 +15,30 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "rz_oracle.c")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liborc.so")
+LIB_OMP = os.path.join(OUT_DIR, "liborc_omp.so")
 
 CFLAGS = ["-std=c11", "-O2", "-Wall", "-Wextra", "-ffp-contract=off",
           "-fno-fast-math", "-fPIC", "-shared"]
 
 
-def build(force: bool = False) -> str:
-    """Compile rz_oracle.c into _build/liborc.so; return the library path."""
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile rz_oracle.c into _build/liborc.so (single-threaded), or with
+    openmp=True into _build/liborc_omp.so: the same source with its independent
+    output rows split over all host cores (the all-core CPU baseline; every row is
+    still summed in the same order, so results are identical)."""
     os.makedirs(OUT_DIR, exist_ok=True)
+    lib = LIB_OMP if openmp else LIB
     deps = [SRC, os.path.join(HERE, "rz_oracle.h")]
-    if not force and os.path.exists(LIB):
-        if os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in deps):
-            return LIB
-    tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"]
+    if not force and os.path.exists(lib):
+        if os.path.getmtime(lib) >= max(os.path.getmtime(p) for p in deps):
+            return lib
+    tmp = lib + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", *CFLAGS, *(["-fopenmp"] if openmp else []), "-o", tmp, SRC, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv))
+    print(build(force="--force" in sys.argv, openmp=True))

@@ -24,6 +24,20 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the row loops use: 1 in the plain build, the OpenMP team size in the
+   all-core build that only the CPU baseline loads. */
+int orc_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------- */
 /* IEEE-754 binary16, written from the standard's definition:                 */
@@ -293,11 +307,14 @@ void orc_q4k_q8_gemv(const uint8_t *w, const uint8_t *x8, float *y,
     int64_t nb8 = in_dim / ORC_QK8;
     const float *xd = q8_d(x8, m, in_dim);
     const float *xs = q8_s(x8, m, in_dim);
-    uint16_t d, dmin;
-    uint8_t sc[8], mn[8], q[256];
     for (int64_t t = 0; t < m; ++t) {
         const int8_t *xq = (const int8_t *)x8 + t * in_dim;
+        /* rows are independent: the all-core build (-fopenmp, the CPU baseline)
+           splits them over threads; each row's sum keeps this order */
+#pragma omp parallel for schedule(static)
         for (int64_t r = 0; r < out_dim; ++r) {
+            uint16_t d, dmin;
+            uint8_t sc[8], mn[8], q[256];
             double acc = 0.0;
             for (int64_t b = 0; b < nsb; ++b) {
                 orc_q4k_unpack(w + (r * nsb + b) * ORC_Q4K_BYTES, &d, &dmin, sc, mn, q);
@@ -319,10 +336,11 @@ void orc_q4_0_gemv(const uint8_t *w, const float *x, float *y,
                    int64_t m, int64_t out_dim, int64_t in_dim)
 {
     int64_t nb = in_dim / ORC_QK4_0;
-    uint16_t d;
-    uint8_t q[32];
     for (int64_t t = 0; t < m; ++t)
+#pragma omp parallel for schedule(static)
         for (int64_t r = 0; r < out_dim; ++r) {
+            uint16_t d;
+            uint8_t q[32];
             double acc = 0.0;
             for (int64_t b = 0; b < nb; ++b) {
                 orc_q4_0_unpack(w + (r * nb + b) * ORC_Q4_0_BYTES, &d, q);
@@ -397,10 +415,11 @@ void orc_attention(const float *q, const float *kc, const float *vc, int64_t pos
     int64_t kv_dim = n_kv_heads * head_dim;
     int64_t group = n_heads / n_kv_heads;
     int64_t T = pos + 1;
-    double *sc = (double *)malloc((size_t)T * sizeof(double));
-    double *acc = (double *)malloc((size_t)head_dim * sizeof(double));
     double inv = 1.0 / sqrt((double)head_dim);
+#pragma omp parallel for schedule(static)
     for (int64_t h = 0; h < n_heads; ++h) {
+        double *sc = (double *)malloc((size_t)T * sizeof(double));
+        double *acc = (double *)malloc((size_t)head_dim * sizeof(double));
         int64_t kvh = h / group;
         const float *qh = q + h * head_dim;
         double mx = -INFINITY;
@@ -427,9 +446,9 @@ void orc_attention(const float *q, const float *kc, const float *vc, int64_t pos
         }
         for (int64_t d = 0; d < head_dim; ++d)
             out[h * head_dim + d] = (float)(acc[d] / z);
+        free(sc);
+        free(acc);
     }
-    free(sc);
-    free(acc);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -493,6 +512,14 @@ void orc_decode_layer(const float *input, const orc_layer *L, float *kc, float *
     orc_q4k_q8_gemv(L->wq, x8, q, 1, q_dim, hp);
     orc_q4k_q8_gemv(L->wk, x8, k, 1, kv_dim, hp);
     orc_q4k_q8_gemv(L->wv, x8, v, 1, kv_dim, hp);
+    /* projection biases (Qwen2's QKV bias, preload_qkv_bias in realizar 0.8.5
+       cached.rs): one f32 add per output, before RoPE */
+    if (L->bq)
+        orc_residual_add(q, L->bq, q, q_dim);
+    if (L->bk)
+        orc_residual_add(k, L->bk, k, kv_dim);
+    if (L->bv)
+        orc_residual_add(v, L->bv, v, kv_dim);
     orc_rope(q, L->n_heads, L->head_dim, pos, L->rope_theta, L->rope_mode);
     orc_rope(k, L->n_kv_heads, L->head_dim, pos, L->rope_theta, L->rope_mode);
     memcpy(kc + pos * kv_dim, k, (size_t)kv_dim * sizeof(float));

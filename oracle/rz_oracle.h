@@ -38,6 +38,9 @@ extern "C" {
 #define ORC_QK4_0 32
 #define ORC_Q4_0_BYTES 18
 
+/* Threads of the row loops: 1, or the OpenMP team size in the all-core build. */
+int orc_threads(void);
+
 /* ---- IEEE-754 binary16 <-> binary32/64 (round to nearest, ties to even) ---- */
 uint16_t orc_f32_to_f16(float x);
 double orc_f16_to_f64(uint16_t h);
@@ -97,6 +100,7 @@ typedef struct {
     float eps;
     double rope_theta;
     int rope_mode;
+    const float *bq, *bk, *bv; /* optional projection biases (NULL: none) */
 } orc_layer;
 
 /* out[hidden_pad] = x + down(q8(silu(gate.q8(norm x)) * up.q8(norm x))) */
@@ -104,7 +108,8 @@ void orc_swiglu_ffn(const float *x, const float *gamma, const uint8_t *wgate,
                     const uint8_t *wup, const uint8_t *wdown, float *out,
                     int64_t hidden, int64_t hidden_pad, int64_t inter, float eps);
 /* One decode step of one token at `pos` (0-based).  kc/vc: [max_seq][kv_dim]
-   f32, written at row pos, read at rows 0..pos. */
+   f32, written at row pos, read at rows 0..pos.  A non-NULL bias is added (f32)
+   to its projection's output before RoPE. */
 void orc_decode_layer(const float *input, const orc_layer *L, float *kc, float *vc,
                       int64_t pos, float *output);
 /* layers, then output RMSNorm, then Q4_0 LM head -> logits[vocab]. */

@@ -43,6 +43,7 @@ class LayerWeightsStruct(C.Structure):
         ("hidden", _i32), ("hidden_pad", _i32), ("n_heads", _i32), ("n_kv_heads", _i32),
         ("head_dim", _i32), ("inter", _i32),
         ("eps", _f32), ("rope_theta", _f32), ("rope_mode", _i32),
+        ("bq", _vp), ("bk", _vp), ("bv", _vp),
     ]
 
 
@@ -59,6 +60,9 @@ SIGNATURES = {
     "rz_q8_1_quantize": [_vp, _vp, _i64, _i64, _vp],
     "rz_q4k_q8_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "rz_q4k_q8_subblock_dots": [_vp, _vp, _vp, _i64, _i64, _vp],
+    "rz_q4k_q8_gemv_ex": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp],
+    "rz_rmsnorm_q4k_gemv": [_vp, _i64, _vp, _i64, _f32, _i32, C.POINTER(_vp), C.POINTER(_i64),
+                            C.POINTER(_vp), _vp, _i64, _i64, _i64, _vp],
     "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "rz_rmsnorm": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _vp],
     "rz_residual_add": [_vp, _vp, _vp, _i64, _vp],
@@ -77,6 +81,7 @@ SIGNATURES = {
     "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
     "rz_set_pdl": [C.c_int],
+    "rz_debug_stall_next_gemv": [C.c_uint32],
     "rz_last_error": [],
     "rz_version": [],
 }

@@ -15,6 +15,7 @@
 namespace rz {
 
 bool g_use_pdl = true;
+uint32_t g_stall_next_gemv = 0;
 
 namespace {
 
@@ -175,6 +176,71 @@ rz_status rz_q4k_q8_subblock_dots(const void *w, const void *q8, int32_t *I, int
     return RZ_OK;
 }
 
+rz_status rz_q4k_q8_gemv_ex(const void *w, const void *q8, const float *bias, const float *residual, float *y,
+                            int64_t ld, int64_t m, int64_t out_dim, int64_t in_dim, rz_stream stream)
+{
+    const char *fn = "rz_q4k_q8_gemv_ex";
+    t_last_error.clear();
+    if (!w || !q8 || !y) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (bias && residual) return fail(RZ_ERR_UNSUPPORTED, "%s: a bias and a residual in one call", fn);
+    if (m < 1 || out_dim < 1 || in_dim < 1)
+        return fail(RZ_ERR_INVALID_ARG, "%s: m=%lld out_dim=%lld in_dim=%lld", fn, (long long)m, (long long)out_dim,
+                    (long long)in_dim);
+    if (ld == 0) ld = out_dim;
+    if (ld < out_dim) return fail(RZ_ERR_SHAPE, "%s: ld=%lld < out_dim", fn, (long long)ld);
+    if (m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld > %d", fn, (long long)m, RZ_MAX_BATCH);
+    if (in_dim % 256) return fail(RZ_ERR_SHAPE, "%s: in_dim=%lld is not a multiple of 256", fn, (long long)in_dim);
+    if (in_dim / 256 > (1 << 20)) return fail(RZ_ERR_SHAPE, "%s: in_dim too large", fn);
+    if (!aligned16(w) || !aligned16(q8) || !aligned16(y) || (residual && !aligned16(residual)))
+        return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return fail(RZ_ERR_ALIGN, "%s: bias must be 4-byte aligned", fn);
+    RZ_TRY(check_device());
+    const int epi = residual ? EPI_RESID : EPI_STORE;
+    if (!q4k_gemv_supported(m, in_dim, epi))
+        return fail(RZ_ERR_UNSUPPORTED, "%s: in_dim=%lld exceeds the shared-memory stage ring", fn, (long long)in_dim);
+    Q4kSegment seg{w, y, residual, out_dim, ld, ld, bias};
+    RZ_CUDA(launch_q4k_gemv(&seg, 1, epi, q8, m, in_dim, static_cast<cudaStream_t>(stream)), "rz_q4k_q8_gemv_ex launch");
+    return RZ_OK;
+}
+
+rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, int64_t n, float eps, int32_t n_mats,
+                              const void *const *w, const int64_t *rows, const float *const *bias, float *y,
+                              int64_t ldy, int64_t m, int64_t in_dim, rz_stream stream)
+{
+    const char *fn = "rz_rmsnorm_q4k_gemv";
+    t_last_error.clear();
+    if (!x || !gamma || !w || !rows || !y) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (n_mats < 1 || n_mats > 3) return fail(RZ_ERR_INVALID_ARG, "%s: n_mats=%d not in [1, 3]", fn, n_mats);
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld", fn, (long long)m);
+    if (in_dim < 256 || in_dim % 256) return fail(RZ_ERR_SHAPE, "%s: in_dim=%lld is not a multiple of 256", fn,
+                                                  (long long)in_dim);
+    if (n < 1 || n > in_dim) return fail(RZ_ERR_SHAPE, "%s: n=%lld not in [1, in_dim]", fn, (long long)n);
+    if (ldx < in_dim) return fail(RZ_ERR_SHAPE, "%s: ldx < in_dim", fn);
+    if (!(eps >= 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps", fn);
+    int64_t total = 0;
+    Q4kSegment seg[3];
+    for (int k = 0; k < n_mats; ++k) {
+        if (!w[k] || rows[k] < 1) return fail(RZ_ERR_INVALID_ARG, "%s: matrix %d", fn, k);
+        if (!aligned16(w[k])) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
+        const float *b = bias ? bias[k] : nullptr;
+        if (b && (reinterpret_cast<uintptr_t>(b) & 3u)) return fail(RZ_ERR_ALIGN, "%s: bias alignment", fn);
+        seg[k] = Q4kSegment{w[k], y + total, nullptr, rows[k], ldy, 0, b};
+        total += rows[k];
+    }
+    if (ldy < total) return fail(RZ_ERR_SHAPE, "%s: ldy=%lld < the %lld rows of the matrices", fn, (long long)ldy,
+                                 (long long)total);
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(y) || (ldx % 4) || (ldy % 4))
+        return fail(RZ_ERR_ALIGN, "%s: x, gamma, y must be 16-byte aligned (ldx, ldy multiples of 4)", fn);
+    RZ_TRY(check_device());
+    if (!q4k_gemv_supported(m, in_dim, EPI_STORE) || !q4k_gemv_f32_input_ok(m, in_dim))
+        return fail(RZ_ERR_UNSUPPORTED, "%s: in_dim=%lld with m=%lld does not fit the fused prologue", fn,
+                    (long long)in_dim, (long long)m);
+    RZ_CUDA(launch_q4k_gemv_f32(seg, n_mats, EPI_STORE, F32Input{x, ldx, gamma, n, eps}, m, in_dim,
+                                static_cast<cudaStream_t>(stream)),
+            "rz_rmsnorm_q4k_gemv launch");
+    return RZ_OK;
+}
+
 rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                        int64_t in_dim, rz_stream stream)
 {
@@ -248,6 +314,15 @@ rz_status rz_set_pdl(int enable)
     return RZ_OK;
 }
 
+rz_status rz_debug_stall_next_gemv(uint32_t wait_limit)
+{
+    t_last_error.clear();
+    if (wait_limit < 1024 || wait_limit > (1u << 22))
+        return fail(RZ_ERR_INVALID_ARG, "rz_debug_stall_next_gemv: wait_limit=%u outside [1024, 2^22]", wait_limit);
+    g_stall_next_gemv = wait_limit;
+    return RZ_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------- layer-level helpers
@@ -258,11 +333,18 @@ rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, Laye
     if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
     // the shape limits below depend on the device's shared memory
     RZ_TRY(check_device());
-    const void *ptrs[] = {w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma};
+    const bool fused = !w->wk && !w->wv;
+    const void *ptrs[] = {w->wq, fused ? w->wq : w->wk, fused ? w->wq : w->wv, w->wo, w->wgate, w->wup, w->wdown,
+                          w->attn_gamma, w->ffn_gamma};
     for (const void *p : ptrs) {
-        if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer", fn);
+        if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer (wk and wv are both NULL or both set)", fn);
         if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
     }
+    if (fused && (w->bk || w->bv))
+        return fail(RZ_ERR_INVALID_ARG, "%s: a fused Q|K|V matrix takes its bias in bq alone", fn);
+    const float *biases[] = {w->bq, w->bk, w->bv};
+    for (const float *b : biases)
+        if (b && (reinterpret_cast<uintptr_t>(b) & 3u)) return fail(RZ_ERR_ALIGN, "%s: biases must be 4-byte aligned", fn);
     if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld not in [1, %d]", fn, (long long)m, RZ_MAX_BATCH);
     if (w->hidden < 1 || w->hidden_pad < w->hidden || w->hidden_pad % 256)
         return fail(RZ_ERR_SHAPE, "%s: hidden=%d hidden_pad=%d (hidden_pad must be a multiple of 256 >= hidden)", fn,
@@ -285,7 +367,7 @@ rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, Laye
         return fail(RZ_ERR_UNSUPPORTED, "%s: a GEMV row is too wide for the shared-memory stage ring", fn);
     LayerDesc d{w->wq, w->wk, w->wv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma,
                 w->hidden, w->hidden_pad, w->n_heads, w->n_kv_heads, w->head_dim, w->inter,
-                w->eps, w->rope_theta, w->rope_mode};
+                w->eps, w->rope_theta, w->rope_mode, w->bq, w->bk, w->bv};
     *out = d;
     return RZ_OK;
 }

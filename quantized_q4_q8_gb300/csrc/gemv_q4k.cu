@@ -50,7 +50,7 @@ constexpr int kMaxStages = 16;
 struct Args {
     const uint8_t *w[3];
     float *y[3];
-    const float *res[3];
+    const float *res[3];   // residual (EPI_RESID), or bias (EPI_STORE, ldr 0), or nullptr
     int64_t ldy[3], ldr[3];
     int64_t seg_begin[4];  // first unit of segment k; seg_begin[nseg] == units
     int nseg;
@@ -74,6 +74,10 @@ struct Args {
     int64_t norm_n;
     float eps;
     unsigned *err;
+    // test aid (rz_debug_stall_next_gemv): in CTA 0 the stage stall_stage is never
+    // issued and every wait polls at most wait_limit times; -1 / unused otherwise
+    int stall_stage;
+    uint32_t wait_limit;
 };
 
 enum XIn { XIN_Q8 = 0, XIN_NORM = 1, XIN_F32 = 2 };
@@ -116,6 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     // the next kernel may become resident now: its weights stream while we drain
     pdl_launch_dependents();
 
+    // the stall test aid applies to CTA 0 only; every other CTA runs as usual
+    const int stall = (blockIdx.x == 0) ? a.stall_stage : -1;
+    const uint32_t lim = (stall >= 0) ? a.wait_limit : kWaitLimit;
+
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -125,11 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
             RingPos rp{0, 0u};
             for (; k < nstages; ++k, ring_next(rp, a.NS)) {
                 const int s = rp.s;
-                if (k >= a.NS && !mbar_wait(&empty[s], rp.par ^ 1u)) {
+                if (k >= a.NS && !mbar_wait(&empty[s], rp.par ^ 1u, lim)) {
                     set_error(a.err, DEV_TIMEOUT_GEMV);
                     ok = false;
                     break;
                 }
+                if (k == stall) continue;  // never issued: the consumers' wait runs out
                 const int64_t u0 = r0 + k * a.PS * a.rpp;
                 const int n = (int)min((int64_t)a.PS * a.rpp, r1 - u0);  // rows in this stage
                 uint8_t *dst = ring + (int64_t)s * a.stage_bytes;
@@ -158,9 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                 }
             }
             // drain: stages issued but possibly not complete must land before exit
-            if (!ok) {
+            // (the consumers may have given up on them)
+            if (!ok || stall >= 0) {
                 for (int64_t q = (k > a.NS ? k - a.NS : 0); q < k; ++q)
-                    if (!mbar_wait(&full[q % a.NS], (unsigned)((q / a.NS) & 1)))
+                    if (q != stall && !mbar_wait(&full[q % a.NS], (unsigned)((q / a.NS) & 1)))
                         set_error(a.err, DEV_TIMEOUT_DRAIN);
             }
         }
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     int prot = 0, rot = 0;  // pairs / packs of the earlier stages, modulo the warp count
     for (int k = 0; k < (int)nstages; ++k, ring_next(rp, a.NS)) {
         const int s = rp.s;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], rp.par));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], rp.par, lim));
         if (!ok) {
             if (lane == 0) set_error(a.err, DEV_TIMEOUT_GEMV);
             return;
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                     const int kseg = (EPI == EPI_SWIGLU) ? 0 : seg_of(a, unit);
                     const int64_t lr = unit - a.seg_begin[kseg];
                     float out = acc[0][0];
-                    if (EPI == EPI_RESID) out = a.res[kseg][lr] + out;
+                    if (EPI == EPI_RESID || (EPI == EPI_STORE && a.res[kseg])) out = a.res[kseg][lr] + out;
                     if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][0], acc[1][0]);
                     a.y[kseg][lr] = out;
                 }
@@ -262,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                             const int t = t0 + i;
                             if (t < a.m) {
                                 float out = acc[0][i];
-                                if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                                if (EPI == EPI_RESID || (EPI == EPI_STORE && a.res[kseg]))
+                                    out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
                                 if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][i], acc[1][i]);
                                 a.y[kseg][t * a.ldy[kseg] + lr] = out;
                             }
@@ -286,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
                         // spread the token stores over the lanes of the row
                         if (t < a.m && ((seg_lanes == 32) ? lane == (t & 31) : leader)) {
                             float out = acc[0][t];
-                            if (EPI == EPI_RESID) out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
+                            if (EPI == EPI_RESID || (EPI == EPI_STORE && a.res[kseg]))
+                                out = a.res[kseg][t * a.ldr[kseg] + lr] + out;
                             if (EPI == EPI_SWIGLU) out = silu_mul(acc[0][t], acc[1][t]);
                             a.y[kseg][t * a.ldy[kseg] + lr] = out;
                         }
@@ -403,6 +415,10 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
         a.res[k] = seg[k].res;
         a.ldy[k] = seg[k].ldy ? seg[k].ldy : seg[k].rows;
         a.ldr[k] = seg[k].ldr ? seg[k].ldr : seg[k].rows;
+        if (epilogue == EPI_STORE) {
+            a.res[k] = seg[k].bias;  // the same bias row for every token
+            a.ldr[k] = 0;
+        }
         if (epilogue != EPI_SWIGLU) {
             a.seg_begin[k] = units;
             units += seg[k].rows;
@@ -438,6 +454,13 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
         xin = f32in->gamma ? XIN_NORM : XIN_F32;
     }
     a.err = dev_error_word();
+    a.stall_stage = -1;
+    a.wait_limit = kWaitLimit;
+    if (g_stall_next_gemv) {
+        a.stall_stage = 0;
+        a.wait_limit = g_stall_next_gemv;
+        g_stall_next_gemv = 0;  // one launch only
+    }
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
     // Small stages for the plain GEMV (Q8_1 in, store out): its consumers start

@@ -173,17 +173,23 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
     const int64_t ld_qkv = q_dim + 2 * kv_dim;
 
     cudaError_t e;
-    Q4kSegment qkv[3] = {{L.wq, w.qkv, nullptr, q_dim, ld_qkv, 0},
-                         {L.wk, w.qkv + q_dim, nullptr, kv_dim, ld_qkv, 0},
-                         {L.wv, w.qkv + q_dim + kv_dim, nullptr, kv_dim, ld_qkv, 0}};
+    Q4kSegment qkv[3] = {{L.wq, w.qkv, nullptr, q_dim, ld_qkv, 0, L.bq},
+                         {L.wk, w.qkv + q_dim, nullptr, kv_dim, ld_qkv, 0, L.bk},
+                         {L.wv, w.qkv + q_dim + kv_dim, nullptr, kv_dim, ld_qkv, 0, L.bv}};
+    int nseg = 3;
+    if (!L.wk) {
+        // fused Q|K|V matrix: one segment of q_dim + 2 kv_dim rows
+        qkv[0].rows = ld_qkv;
+        nseg = 1;
+    }
     if (q4k_gemv_f32_input_ok(m, L.hidden_pad)) {
         // RMSNorm -> Q8_1 inside the Q|K|V GEMV
-        e = launch_q4k_gemv_f32(qkv, 3, EPI_STORE,
+        e = launch_q4k_gemv_f32(qkv, nseg, EPI_STORE,
                                 F32Input{input, L.hidden_pad, L.attn_gamma, L.hidden, L.eps}, m, L.hidden_pad, s);
     } else {
         e = launch_rmsnorm(input, L.attn_gamma, nullptr, w.x8, m, L.hidden, L.hidden_pad, L.eps, s);
         if (e != cudaSuccess) return e;
-        e = launch_q4k_gemv(qkv, 3, EPI_STORE, w.x8, m, L.hidden_pad, s);
+        e = launch_q4k_gemv(qkv, nseg, EPI_STORE, w.x8, m, L.hidden_pad, s);
     }
     if (e != cudaSuccess) return e;
     AttnArgs a = make_attn_args(L, m, kv, positions, position, w.rope_tab, make_table, w.part, w.counters,

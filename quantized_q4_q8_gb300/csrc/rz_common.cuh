@@ -88,24 +88,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
 // Bounded wait for the phase with the given parity to complete.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, uint32_t limit = kWaitLimit)
 {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// Bounded wait that also gives up as soon as the error word is set by any CTA
-// (so that one failure ends every waiting CTA quickly instead of each running
-// into its own bound).  On running out of the bound it records `code`.
-__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, unsigned parity, unsigned *err,
-                                                    unsigned code)
-{
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && *reinterpret_cast<volatile unsigned *>(err) != 0u) return false;
-    }
-    set_error(err, code);
     return false;
 }
 

@@ -19,6 +19,10 @@ const DevInfo &dev_info();
 // Device error word of the current device (a file-scope __device__ variable).
 unsigned *dev_error_word();
 
+// Test aid: non-zero makes the next Q4_K GEMV launch leave its first stage in
+// CTA 0 unissued and bound that CTA's waits by this many polls (then reset to 0).
+extern uint32_t g_stall_next_gemv;
+
 // Launch with the programmatic-stream-serialization attribute (PDL) so that the
 // kernel's weight prefetch overlaps the tail of the previous kernel in the stream.
 extern bool g_use_pdl;
@@ -42,6 +46,7 @@ struct Q4kSegment {
     int64_t rows;
     int64_t ldy = 0;   // 0: rows
     int64_t ldr = 0;   // 0: rows
+    const float *bias = nullptr;  // [rows] added to every token's output (EPI_STORE only)
 };
 
 // Up to three weight matrices with the same in_dim read against one Q8_1
@@ -117,12 +122,15 @@ cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, floa
                                 int64_t out_dim, int64_t in_dim, cudaStream_t s);
 
 // ---------------------------------------------------------------- layer / stack
+// wk == wv == nullptr: wq is the fused [q_dim + 2 kv_dim][hidden_pad] matrix (and
+// bq, when given, its fused bias).  Biases are optional.
 struct LayerDesc {
     const void *wq, *wk, *wv, *wo, *wgate, *wup, *wdown;
     const float *attn_gamma, *ffn_gamma;
     int hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter;
     float eps, rope_theta;
     int rope_mode;
+    const float *bq, *bk, *bv;
 };
 
 struct KvDesc {

@@ -8,7 +8,8 @@ from ._lib import call, load, status
 __all__ = [
     "q8_1_size", "q4k_bytes", "q4_0_bytes",
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
-    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl",
+    "rz_q4k_q8_gemv_ex", "rz_rmsnorm_q4k_gemv", "q4k_q8_gemv_ex", "rmsnorm_q4k_gemv",
+    "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_debug_stall_next_gemv",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
     "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
     "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
@@ -62,6 +63,21 @@ def rz_q4k_q8_subblock_dots(w, q8, I, out_dim, in_dim, stream=None):
                 _stream(stream))
 
 
+def rz_q4k_q8_gemv_ex(w, q8, bias, residual, y, ld, m, out_dim, in_dim, stream=None):
+    return call("rz_q4k_q8_gemv_ex", _ptr(w), _ptr(q8), _ptr(bias), _ptr(residual), _ptr(y), ld, m,
+                out_dim, in_dim, _stream(stream))
+
+
+def rz_rmsnorm_q4k_gemv(x, ldx, gamma, n, eps, ws, rows, biases, y, ldy, m, in_dim, stream=None):
+    """ws, rows, biases: sequences of equal length (1..3); biases may be None."""
+    k = len(ws)
+    wp = (C.c_void_p * k)(*[_ptr(t) for t in ws])
+    rp = (C.c_int64 * k)(*rows)
+    bp = None if biases is None else (C.c_void_p * k)(*[_ptr(b) for b in biases])
+    return call("rz_rmsnorm_q4k_gemv", _ptr(x), ldx, _ptr(gamma), n, eps, k, wp, rp, bp, _ptr(y), ldy,
+                m, in_dim, _stream(stream))
+
+
 def rz_q4_0_gemv(w, x, y, m, out_dim, in_dim, stream=None):
     return call("rz_q4_0_gemv", _ptr(w), _ptr(x), _ptr(y), m, out_dim, in_dim, _stream(stream))
 
@@ -83,7 +99,12 @@ def rz_check_device_error(stream=None):
 
 
 def rz_set_pdl(enable: bool):
-    return call("rz_set_pdl", 1 if enable else 0)
+    return call("rz_set_pdl", "rz_debug_stall_next_gemv", 1 if enable else 0)
+
+
+def rz_debug_stall_next_gemv(wait_limit: int):
+    """Test aid: the next Q4_K GEMV launch runs out of a bounded wait (see rz.h)."""
+    return call("rz_debug_stall_next_gemv", int(wait_limit))
 
 
 # ------------------------------------------------------------------ tensor helpers
@@ -116,6 +137,27 @@ def q4k_q8_gemv(w, q8, m, out_dim, in_dim, out=None, stream=None):
     if out is None:
         out = torch.empty((m, out_dim), dtype=torch.float32, device=w.device)
     rz_q4k_q8_gemv(w, q8, out, m, out_dim, in_dim, stream)
+    return out
+
+
+def q4k_q8_gemv_ex(w, q8, m, out_dim, in_dim, bias=None, residual=None, out=None, ld=0,
+                   stream=None):
+    """y = W x (+ bias | + residual); y f32 [m, ld or out_dim]."""
+    import torch
+    if out is None:
+        out = torch.empty((m, ld or out_dim), dtype=torch.float32, device=w.device)
+    rz_q4k_q8_gemv_ex(w, q8, bias, residual, out, ld, m, out_dim, in_dim, stream)
+    return out
+
+
+def rmsnorm_q4k_gemv(x, gamma, n, eps, ws, rows, in_dim, biases=None, out=None, stream=None):
+    """RMSNorm -> Q8_1 -> GEMVs of 1..3 matrices; returns f32 [m, sum(rows)]."""
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    ldx = x.shape[-1]
+    if out is None:
+        out = torch.empty((m, sum(rows)), dtype=torch.float32, device=x.device)
+    rz_rmsnorm_q4k_gemv(x, ldx, gamma, n, eps, ws, rows, biases, out, out.shape[-1], m, in_dim, stream)
     return out
 
 
@@ -174,7 +216,9 @@ class DeviceLayer:
     """One Q4_K decode layer resident on the GPU (torch tensors) and its C descriptor.
 
     weights: dict with uint8 CUDA tensors wq, wk, wv, wo, wgate, wup, wdown and f32
-    CUDA tensors attn_gamma, ffn_gamma.  Shapes follow include/rz.h."""
+    CUDA tensors attn_gamma, ffn_gamma; optional f32 CUDA tensors bq, bk, bv (QKV
+    bias).  The fused Q|K|V layout leaves wk and wv out (or None) and holds the one
+    [q_dim + 2 kv_dim][hidden_pad] matrix in wq.  Shapes follow include/rz.h."""
 
     def __init__(self, weights: dict, hidden: int, hidden_pad: int, n_heads: int,
                  n_kv_heads: int, head_dim: int, inter: int, eps: float, rope_theta: float,
@@ -184,10 +228,15 @@ class DeviceLayer:
         self.hidden, self.hidden_pad, self.n_heads = hidden, hidden_pad, n_heads
         self.n_kv_heads, self.head_dim, self.inter = n_kv_heads, head_dim, inter
         self.eps, self.rope_theta, self.rope_mode = eps, rope_theta, rope_mode
+
+        def p(k):
+            t = weights.get(k)
+            return None if t is None else t.data_ptr()
+
         self.struct = LayerWeightsStruct(
-            *[weights[k].data_ptr() for k in ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown",
-                                             "attn_gamma", "ffn_gamma")],
-            hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter, eps, rope_theta, rope_mode)
+            *[p(k) for k in ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown", "attn_gamma", "ffn_gamma")],
+            hidden, hidden_pad, n_heads, n_kv_heads, head_dim, inter, eps, rope_theta, rope_mode,
+            p("bq"), p("bk"), p("bv"))
 
     @property
     def kv_dim(self):

@@ -110,20 +110,16 @@ def test_q4k_gemv_deterministic(rz):
 
 @pytest.mark.parametrize("out_dim,in_dim", S.LLAMA_SWEEP)
 @pytest.mark.parametrize("m", [1, 16])
-def test_q4k_gemv_full_size_sampled(rz, out_dim, in_dim, m):
+def test_q4k_gemv_full_size(rz, out_dim, in_dim, m):
     """Full Llama-shaped sweep in the launch configuration the benchmark times;
-    the oracle recomputes a sample of rows (first, last, random)."""
+    every output row of every token against the oracle."""
     w = S.q4k_weight(f"sweep.{out_dim}.{in_dim}", out_dim, in_dim)
     x = S.normal(f"sweep.x.{in_dim}.{m}", (m, in_dim))
     x8 = oracle.q8_1_quantize(x)
     y = rz.q4k_q8_gemv(to_dev(w), to_dev(x8), m, out_dim, in_dim).cpu().numpy()
     check_no_device_error()
-    g = np.random.default_rng(out_dim + in_dim + m)
-    rows = np.unique(np.concatenate([[0, 1, out_dim // 2, out_dim - 1],
-                                     g.integers(0, out_dim, 60)]))
-    y_ref = oracle.q4k_q8_gemv(w[rows], x8, m, len(rows), in_dim)
-    assert_gemv_close(y[:, rows], y_ref, row_norms_q4k(w[rows])[None, :], f"sweep {out_dim}x{in_dim}")
-    assert np.isfinite(y).all()
+    y_ref = oracle.q4k_q8_gemv(w, x8, m, out_dim, in_dim)
+    assert_gemv_close(y, y_ref, row_norms_q4k(w)[None, :], f"sweep {out_dim}x{in_dim} m={m}")
 
 
 def test_q4k_gemv_padding_invariance(rz):
@@ -154,15 +150,14 @@ def test_q4_0_gemv_parity(rz, out_dim, in_dim, m):
 
 
 @pytest.mark.parametrize("vocab,hidden", S.LM_HEADS)
-def test_q4_0_lm_head_full_size_sampled(rz, vocab, hidden):
+def test_q4_0_lm_head_full_size(rz, vocab, hidden):
+    """Both LM heads at full size; every logit against the oracle."""
     w = S.q4_0_weight(f"lm.{vocab}.{hidden}", vocab, hidden)
     x = S.normal(f"lm.x.{hidden}", (1, hidden))
     y = rz.q4_0_gemv(to_dev(w), to_dev(x), vocab, hidden).cpu().numpy()
     check_no_device_error()
-    g = np.random.default_rng(vocab)
-    rows = np.unique(np.concatenate([[0, vocab - 1], g.integers(0, vocab, 200)]))
-    y_ref = oracle.q4_0_gemv(w[rows], x, len(rows), hidden)
-    assert_gemv_close(y[:, rows], y_ref, row_norms_q4_0(w[rows])[None, :], f"lm head {vocab}")
+    y_ref = oracle.q4_0_gemv(w, x, vocab, hidden)
+    assert_gemv_close(y, y_ref, row_norms_q4_0(w)[None, :], f"lm head {vocab}")
 
 
 # ----------------------------------------------------------------------------- RMSNorm / residual

@@ -447,3 +447,51 @@ def test_layer_query_rotated_at_its_position(orc, mode):
     scale = np.abs(base).max()
     assert np.abs(mirrored - base).max() <= 1e-3 * scale
     assert np.abs(shifted - base).max() > 1e-2 * scale
+
+
+# ----------------------------------------------------------------------------- projection biases
+def test_zero_bias_is_no_bias(orc):
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.bias0")
+    x = S.hidden_input("pin.bias0.x", 1, sh.hidden, sh.hidden_pad)[0]
+    kc, vc = S.kv_prefill(sh, "pin.bias0", 8, 3)
+    ref = orc.decode_layer(x, _orc_layer(orc, L), kc[0].copy(), vc[0].copy(), 3)
+    lw = _orc_layer(orc, L)
+    lw.bq = np.zeros(sh.q_dim, np.float32)
+    lw.bk = np.zeros(sh.kv_dim, np.float32)
+    lw.bv = np.zeros(sh.kv_dim, np.float32)
+    assert np.array_equal(orc.decode_layer(x, lw, kc[0].copy(), vc[0].copy(), 3), ref)
+
+
+def test_bias_on_zero_projections_is_the_bias(orc):
+    """With W_q = W_k = W_v = 0 the projections are the biases themselves: the cache
+    row at pos holds bv and rope(bk, pos), and the attention of a first token is bv
+    expanded over the query heads."""
+    sh = _tiny_shape()
+    L = S.layer(sh, "pin.bias1")
+    for k in ("wq", "wk", "wv"):
+        L.w[k] = np.zeros_like(L.w[k])
+    lw = _orc_layer(orc, L)
+    lw.bq = S.normal("pin.bias1.bq", sh.q_dim)
+    lw.bk = S.normal("pin.bias1.bk", sh.kv_dim)
+    lw.bv = S.normal("pin.bias1.bv", sh.kv_dim)
+    x = S.hidden_input("pin.bias1.x", 1, sh.hidden, sh.hidden_pad)[0]
+    pos = 5
+    kc, vc = S.kv_prefill(sh, "pin.bias1", 8, pos)
+    orc.decode_layer(x, lw, kc[0], vc[0], pos)
+    assert np.array_equal(vc[0, pos], lw.bv)
+    assert np.array_equal(kc[0, pos], orc.rope(lw.bk, sh.n_kv_heads, sh.head_dim, pos, sh.rope_theta,
+                                               sh.rope_mode))
+    # first token: output = x + O(q8(bv expanded)) then the FFN
+    kc0, vc0 = S.kv_prefill(sh, "pin.bias1b", 4, 0)
+    out = orc.decode_layer(x, lw, kc0[0], vc0[0], 0)
+    att = np.zeros(sh.q_pad, np.float32)
+    for h in range(sh.n_heads):
+        kvh = h // (sh.n_heads // sh.n_kv_heads)
+        att[h * sh.head_dim:(h + 1) * sh.head_dim] = lw.bv[kvh * sh.head_dim:(kvh + 1) * sh.head_dim]
+    o = orc.q4k_q8_gemv(L.w["wo"], orc.q8_1_quantize(att), 1, sh.hidden, sh.q_pad)[0]
+    r1 = np.zeros(sh.hidden_pad, np.float32)
+    r1[:sh.hidden] = x[:sh.hidden] + o
+    expect = orc.swiglu_ffn(r1, L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
+                            sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
+    assert np.array_equal(out, expect)
