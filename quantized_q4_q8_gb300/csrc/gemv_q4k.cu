@@ -39,9 +39,16 @@
 namespace rz {
 namespace {
 
+// Consumer warps and shared-memory budget per CTA, for several tokens and for one
+// (a one-token CTA of 8 warps in <= 110 KB, two per SM so that the next kernel's
+// CTA streams its weights beside this one, measured slower: 9.8 us against 8.9
+// for 4096 x 14336, 2.32 ms against 1.71 for the decode step).
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarps1 = 16;
 constexpr int kCtaSmem = 200 * 1024;
+constexpr int kCtaSmem1 = 200 * 1024;
+__host__ __device__ constexpr int consumer_warps(int mt) { return mt == 1 ? kConsumerWarps1 : kConsumerWarps; }
+__host__ __device__ constexpr int cta_threads(int mt) { return (consumer_warps(mt) + 1) * 32; }
 constexpr int kStageTarget = 16 * 1024;
 constexpr int kStageTargetFused = 32 * 1024;
 constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
@@ -92,8 +99,9 @@ __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
 // PR: several tokens with the rows in pairs (a separate instantiation, so that
 // its register allocation does not touch the one-row-per-warp path)
 template <int MT, int EPI, bool XS, int XIN, bool PR = false>
-__global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
+__global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args a)
 {
+    constexpr int kConsumerWarps = consumer_warps(MT);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint8_t *xsm = smem + (int64_t)a.NS * a.stage_bytes;
@@ -187,13 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel(const Args a)
     x.gd = a.xd;
     x.gs = a.xs;
     auto csync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); };
-    if (XS && XIN == XIN_Q8) stage_x_q8<false>(xsm, a.xq, a.xd, a.xs, a.m, a.in_dim, threadIdx.x, csync);
+    if (XS && XIN == XIN_Q8)
+        stage_x_q8<false, kConsumerWarps>(xsm, a.xq, a.xd, a.xs, a.m, a.in_dim, threadIdx.x, csync);
     if (XS && XIN != XIN_Q8) {
         // quantise the f32 input (RMS-normalised first for XIN_NORM) straight into
         // the padded slot layout
         float *red = reinterpret_cast<float *>(full) - 24;  // 17 floats below the barriers
-        stage_x_f32<false, XIN == XIN_NORM>(xsm, a.xf, a.ldxf, a.gamma, a.norm_n, a.eps, a.m, a.in_dim, red,
-                                            warp, lane, csync);
+        stage_x_f32<false, XIN == XIN_NORM, kConsumerWarps>(xsm, a.xf, a.ldxf, a.gamma, a.norm_n, a.eps, a.m,
+                                                            a.in_dim, red, warp, lane, csync);
     }
     if (XS) {
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
@@ -354,7 +363,7 @@ cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(cta_threads(MT));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -381,21 +390,22 @@ cudaError_t launch_x(const Args &a, int grid, cudaStream_t s, int xin)
     return launch_t<MT, EPI, false, XIN_Q8>(a, grid, s);
 }
 
-// Several tokens take the row-pair kernels when each consumer warp gets at least
-// four rows (with fewer rows per CTA the pairs would leave warps idle).
+// One to three tokens (from kMmaMinTokens on, the tensor-core kernel of
+// gemv_q4k_mma.cu runs instead).  Several tokens take the row-pair kernels when
+// each consumer warp gets at least four rows.
 template <int EPI>
 cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
 {
-    const bool pr = a.m > 1 && a.rpp == 1 && a.x_smem && a.units / grid >= 4 * kConsumerWarps;
+    static_assert(kMmaMinTokens <= 4, "the dp4a kernels cover fewer than four tokens");
+    const bool pr = a.m > 1 && a.rpp == 1 && a.x_smem && a.units / grid >= 4 * consumer_warps(a.m);
     if (a.m <= 1) return launch_x<1, EPI, false>(a, grid, s, xin);
     if (a.m <= 2) return pr ? launch_x<2, EPI, true>(a, grid, s, xin) : launch_x<2, EPI, false>(a, grid, s, xin);
     if (a.m <= 4) return pr ? launch_x<4, EPI, true>(a, grid, s, xin) : launch_x<4, EPI, false>(a, grid, s, xin);
-    if (a.m <= 8) return pr ? launch_x<8, EPI, true>(a, grid, s, xin) : launch_x<8, EPI, false>(a, grid, s, xin);
-    return pr ? launch_x<16, EPI, true>(a, grid, s, xin) : launch_x<16, EPI, false>(a, grid, s, xin);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim);
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue);
 namespace {
 
 // Q8_1 activations of m tokens: codes [m][in_dim], then d [m][in_dim/32], then s.
@@ -477,7 +487,7 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
     a.stage_bytes = (int)(a.PS * pack);
     const int64_t xbytes = x_smem_bytes(m, in_dim);
     a.x_smem = (xbytes <= kXSmemMax || f32in) ? 1 : 0;
-    const int64_t budget = (int64_t)kCtaSmem - (a.x_smem ? xbytes : 0) - 1024;
+    const int64_t budget = (int64_t)(m == 1 ? kCtaSmem1 : kCtaSmem) - (a.x_smem ? xbytes : 0) - 1024;
     int64_t ns = budget / a.stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns < 2) {
@@ -500,21 +510,14 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
     }
 }
 
-static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
-                                 const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
+// Several tokens: the tensor-core kernel, in equal groups of tokens whose
+// activations fit in shared memory beside its stage ring (one launch each).
+static cudaError_t launch_mma_groups(const Q4kSegment *seg, int nseg, int epilogue, const Q8Src *x,
+                                     const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
 {
-    if (!q8) return launch_core(seg, nseg, epilogue, nullptr, f32in, m, in_dim, s);
-    const int64_t nb = in_dim / 32;
-    Q8Src x;
-    x.q = static_cast<const int8_t *>(q8);
-    x.d = reinterpret_cast<const float *>(x.q + m * in_dim);
-    x.s = x.d + m * nb;
-    if (m == 1 || x_smem_bytes(m, in_dim) <= kXSmemMax) return launch_core(seg, nseg, epilogue, &x, f32in, m, in_dim, s);
-    // Several tokens whose activations do not fit in shared memory: equal groups
-    // of tokens that do, one launch each.  The weights stream once per group,
-    // which beats reading every token's activations from L2 for every row.
-    const int64_t ng = q4k_gemv_launch_count(m, in_dim);
+    const int64_t ng = q4k_gemv_launch_count(m, in_dim, epilogue);
     const int64_t mc = (m + ng - 1) / ng;
+    const int64_t nb = in_dim / 32;
     for (int64_t t0 = 0; t0 < m; t0 += mc) {
         const int64_t n = std::min(mc, m - t0);
         Q4kSegment part[3];
@@ -527,14 +530,32 @@ static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, 
             part[k].y = seg[k].y + t0 * ldy;
             part[k].res = seg[k].res ? seg[k].res + t0 * ldr : nullptr;
         }
-        Q8Src xg;
-        xg.q = x.q + t0 * in_dim;
-        xg.d = x.d + t0 * nb;
-        xg.s = x.s + t0 * nb;
-        const cudaError_t e = launch_core(part, nseg, epilogue, &xg, f32in, n, in_dim, s);
+        cudaError_t e;
+        if (f32in) {
+            F32Input in = *f32in;
+            in.x = f32in->x + t0 * f32in->ldx;
+            e = launch_q4k_gemv_mma(part, nseg, epilogue, nullptr, nullptr, nullptr, &in, n, in_dim, s);
+        } else {
+            e = launch_q4k_gemv_mma(part, nseg, epilogue, x->q + t0 * in_dim, x->d + t0 * nb, x->s + t0 * nb,
+                                    nullptr, n, in_dim, s);
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+static cudaError_t launch_common(const Q4kSegment *seg, int nseg, int epilogue, const void *q8,
+                                 const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
+{
+    Q8Src x{};
+    if (q8) {
+        const int64_t nb = in_dim / 32;
+        x.q = static_cast<const int8_t *>(q8);
+        x.d = reinterpret_cast<const float *>(x.q + m * in_dim);
+        x.s = x.d + m * nb;
+    }
+    if (m >= kMmaMinTokens) return launch_mma_groups(seg, nseg, epilogue, q8 ? &x : nullptr, f32in, m, in_dim, s);
+    return launch_core(seg, nseg, epilogue, q8 ? &x : nullptr, f32in, m, in_dim, s);
 }
 
 }  // namespace
@@ -545,17 +566,20 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
     return launch_common(seg, nseg, epilogue, q8, nullptr, m, in_dim, s);
 }
 
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim)
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue)
 {
-    if (m <= 1 || x_smem_bytes(m, in_dim) <= kXSmemMax) return 1;
-    int64_t mc = m;
-    while (mc > 1 && x_smem_bytes(mc, in_dim) > kXSmemMax) --mc;
-    return (int)((m + mc - 1) / mc);
+    if (m < kMmaMinTokens) return 1;
+    const int64_t mt = q4k_gemv_mma_group(m, in_dim, epilogue);
+    return mt < 1 ? 0 : (int)((m + mt - 1) / mt);
 }
 
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)
 {
-    return x_smem_bytes(m, in_dim) <= kXSmemMax && in_dim <= 32LL * kRowWarps * kRowBlocksPerWarp;
+    if (in_dim > 32LL * kRowWarps * kRowBlocksPerWarp) return false;
+    // several tokens: each token group of the tensor-core kernel normalises and
+    // quantises its own tokens
+    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, EPI_SWIGLU) >= 1;
+    return x_smem_bytes(m, in_dim) <= kXSmemMax;
 }
 
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
@@ -570,12 +594,13 @@ cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, c
 
 bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue)
 {
+    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, epilogue) >= 1;
     const int R = (epilogue == EPI_SWIGLU) ? 2 : 1;
     const int64_t nsb = in_dim / 256;
     const int64_t rpp = (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1;
     const int64_t pack = R * rpp * nsb * kSB;
     const int64_t xbytes = x_smem_bytes(m, in_dim);
-    const int64_t budget = (int64_t)kCtaSmem - (xbytes <= kXSmemMax ? xbytes : 0) - 1024;
+    const int64_t budget = (int64_t)(m == 1 ? kCtaSmem1 : kCtaSmem) - (xbytes <= kXSmemMax ? xbytes : 0) - 1024;
     return budget / pack >= 2;
 }
 

@@ -243,11 +243,16 @@ int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int 
     const LayerDesc &L0 = layers[0];
     const int h = head ? 2 : 0;  // output RMSNorm, LM head
     const int q_pad = (L0.n_heads * L0.head_dim + 255) / 256 * 256;
-    const int gh = q4k_gemv_launch_count(m, L0.hidden_pad), gi = q4k_gemv_launch_count(m, L0.inter);
-    int per_layer = 1 /* attention */ + q4k_gemv_launch_count(m, q_pad) /* O */;
-    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 1 + gh;  // Q|K|V (or RMSNorm, then groups)
-    per_layer += q4k_gemv_f32_input_ok(m, L0.hidden_pad) ? 1 : 1 + gh;  // gate/up
-    per_layer += q4k_gemv_f32_input_ok(m, L0.inter) ? 1 : 1 + gi;       // down (or Q8_1 of h, then groups)
+    // a GEMV with its input normalised / quantised inside, or a separate kernel
+    // for that and then the Q8_1-input GEMV
+    auto gemv = [&](int64_t in_dim, int epi) {
+        const int n = q4k_gemv_launch_count(m, in_dim, epi);
+        return q4k_gemv_f32_input_ok(m, in_dim) ? n : 1 + n;
+    };
+    int per_layer = 1 /* attention */ + q4k_gemv_launch_count(m, q_pad, EPI_RESID) /* O */;
+    per_layer += gemv(L0.hidden_pad, EPI_STORE);   // RMSNorm -> Q|K|V
+    per_layer += gemv(L0.hidden_pad, EPI_SWIGLU);  // RMSNorm -> gate/up
+    per_layer += gemv(L0.inter, EPI_RESID);        // Q8_1 of h -> down
     return 1 /* RoPE table */ + n_layers * per_layer + h;
 }
 

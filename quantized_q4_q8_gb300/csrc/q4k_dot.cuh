@@ -423,15 +423,32 @@ __device__ __forceinline__ void stage_x_q8(uint8_t *xsm, const int8_t *xq, const
 // squares runs in a fixed order (per thread over its float4s in order, then the
 // xor butterfly of each warp, then the warp sums in order), so every CTA
 // computes the same bits.  `red`: NW + 1 floats of shared memory.
-template <bool CG, bool NORM, int KF, int NW, typename Sync>
-__device__ __forceinline__ void stage_x_f32_kf(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
+// Store functor of the padded-slot layout above: codes(t, b, e0, word) writes the
+// four codes e0..e0+3 of Q8_1 block b of token t, meta(t, b, d, s) its d and s.
+struct SlotStore {
+    uint8_t *xsm;
+    float *dsm, *ssm;
+    int64_t nb, nsb;
+    __device__ __forceinline__ void codes(int t, int64_t b, int e0, uint32_t word) const
+    {
+        const int j = (int)(b & 7);
+        *reinterpret_cast<uint32_t *>(xsm + (t * nsb + (b >> 3)) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) + e0) =
+            word;
+    }
+    __device__ __forceinline__ void meta(int t, int64_t b, float d, float s) const
+    {
+        dsm[t * nb + b] = d;
+        ssm[t * nb + b] = s;
+    }
+};
+
+template <bool CG, bool NORM, int KF, int NW, typename Store, typename Sync>
+__device__ __forceinline__ void stage_x_f32_kf(const Store &st, const float *xf, int64_t ldx, const float *gamma,
                                                int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
                                                int warp, int lane, Sync sync)
 {
     constexpr int NT = 32 * NW;
-    const int64_t nb = in_dim / 32, n4 = in_dim / 4, nsb = in_dim / 256;
-    float *dsm = reinterpret_cast<float *>(xsm + (int64_t)m * nsb * kXSlot);
-    float *ssm = dsm + (int64_t)m * nb;
+    const int64_t n4 = in_dim / 4;
     const int tid = warp * 32 + lane;
     for (int t = 0; t < m; ++t) {
         const float4 *xrow = reinterpret_cast<const float4 *>(xf + t * ldx);
@@ -524,33 +541,46 @@ __device__ __forceinline__ void stage_x_f32_kf(uint8_t *xsm, const float *xf, in
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             const int64_t b = f >> 3;  // Q8_1 block
             const int e0 = (int)(f & 7) * 4;
-            const int j = (int)(b & 7);
             const uint32_t word = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
                                   ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
-            *reinterpret_cast<uint32_t *>(xsm + (t * nsb + (b >> 3)) * kXSlot + x_chunk_off(j >> 1) + 32 * (j & 1) +
-                                          e0) = word;
-            if ((lane & 7) == 0) {
-                dsm[t * nb + b] = d;
-                ssm[t * nb + b] = __fmul_rn(d, (float)sum);
-            }
+            st.codes(t, b, e0, word);
+            if ((lane & 7) == 0) st.meta(t, b, d, __fmul_rn(d, (float)sum));
         }
     }
     sync();
 }
 
-// Dispatch on the float4s per thread the row needs (rows up to NW * 1024 values).
+// Dispatch on the float4s per thread the row needs (rows up to 16384 values:
+// 16 warps x 8 float4s, or 8 warps x 16).
+template <bool CG, bool NORM, int NW = kRowWarps, typename Store, typename Sync>
+__device__ __forceinline__ void stage_x_f32_to(const Store &st, const float *xf, int64_t ldx, const float *gamma,
+                                               int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
+                                               int warp, int lane, Sync sync)
+{
+    const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
+    if (kf <= 2)
+        stage_x_f32_kf<CG, NORM, 2, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else if (kf <= 4)
+        stage_x_f32_kf<CG, NORM, 4, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else if (kf <= 8 || NW >= 16)
+        stage_x_f32_kf<CG, NORM, 8, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    else
+        stage_x_f32_kf<CG, NORM, 16, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+}
+
+// The same into the padded-slot layout.
 template <bool CG, bool NORM, int NW = kRowWarps, typename Sync>
 __device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
                                             int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
                                             int warp, int lane, Sync sync)
 {
-    const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
-    if (kf <= 2)
-        stage_x_f32_kf<CG, NORM, 2, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
-    else if (kf <= 4)
-        stage_x_f32_kf<CG, NORM, 4, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
-    else
-        stage_x_f32_kf<CG, NORM, 8, NW>(xsm, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    SlotStore st;
+    st.xsm = xsm;
+    st.nb = in_dim / 32;
+    st.nsb = in_dim / 256;
+    st.dsm = reinterpret_cast<float *>(xsm + (int64_t)m * st.nsb * kXSlot);
+    st.ssm = st.dsm + (int64_t)m * st.nb;
+    stage_x_f32_to<CG, NORM, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
 }
 
 }  // namespace

@@ -6,6 +6,7 @@
 // code in the device error word and stops, it never traps.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -131,6 +132,25 @@ __device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsi
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 2-D tiled tensor copy (TMA) global -> shared: the box of the tensor map at
+// element coordinates (x inner, y outer), completion counted on `bar` in bytes
+// (the whole box, out-of-range parts zero-filled).  dst 128-byte aligned; the
+// map a __grid_constant__ kernel parameter (or in global / constant memory).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Position in a ring of n slots, advanced one stage at a time: the slot and the

@@ -2,10 +2,19 @@
 // Arguments are already validated by the C-ABI layer (abi.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace rz {
+
+// A 2-D tiled tensor map (TMA descriptor) over a row-major array of `rows` rows
+// whose rows are `row_stride` bytes apart and hold `inner` elements of
+// `elem_bytes` bytes (1, 2 or 4), copied in boxes of box_inner x box_rows
+// elements; out-of-range parts of a box read as zero.  Encoded through the
+// driver's cuTensorMapEncodeTiled (looked up once through the runtime).
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
+                                 uint64_t row_stride, uint32_t box_inner, uint32_t box_rows);
 
 // Device properties of the current device (cached per device).
 struct DevInfo {
@@ -69,9 +78,16 @@ struct F32Input {
     float eps;
 };
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim);
-// launches one Q8_1-input GEMV of m tokens takes (token groups when the
-// activations exceed shared memory)
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim);
+// launches one GEMV of m tokens takes (token groups when the activations exceed
+// shared memory)
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue);
+
+// From this many tokens on, the GEMV runs on the tensor cores (gemv_q4k_mma.cu).
+constexpr int kMmaMinTokens = 4;
+// Most tokens one tensor-core launch takes for this shape (0: none fit).
+int q4k_gemv_mma_group(int64_t m, int64_t in_dim, int epilogue);
+cudaError_t launch_q4k_gemv_mma(const Q4kSegment *seg, int nseg, int epilogue, const int8_t *xq, const float *xd,
+                                const float *xs, const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s);
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
                                 int64_t m, int64_t in_dim, cudaStream_t s);
 

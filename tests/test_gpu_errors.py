@@ -44,10 +44,12 @@ def test_stalled_gemv_reports_timeout_and_next_call_is_exact(rz, out_dim, in_dim
     rz.q4k_q8_gemv(wd, xd, m, out_dim, in_dim, out=y)      # the launch itself succeeds
     st, code = rz.check_device_error()                     # synchronises: the kernel ended
     assert st == 5 and code == 0x101, (st, hex(code))
-    # CTAs other than CTA 0 ran normally
+    # CTAs other than CTA 0 ran normally: only a prefix of rows (CTA 0's range, a
+    # few dozen at most) may differ
     yb = y.cpu().numpy()
-    rows0 = out_dim // torch.cuda.get_device_properties(0).multi_processor_count
-    assert np.array_equal(yb[:, rows0 + 1:].view(np.uint32), good[:, rows0 + 1:].view(np.uint32))
+    same = np.all(yb.view(np.uint32) == good.view(np.uint32), axis=0)
+    first_ok = int(np.argmax(same))
+    assert same[first_ok:].all() and first_ok <= 64, first_ok
     check_no_device_error()                                # the word was cleared
 
     again = rz.q4k_q8_gemv(wd, xd, m, out_dim, in_dim).cpu().numpy()
