@@ -215,7 +215,8 @@ typedef struct {
 
 /* f32 KV cache of one layer.  Row p of sequence t (token t of a batch) is at
  * k + t*seq_stride + p*kv_dim (same for v), kv_dim = n_kv_heads*head_dim.
- * seq_stride is ignored when m == 1; otherwise >= max_seq*kv_dim.  1 <= max_seq <= 4096. */
+ * seq_stride is ignored when m == 1; otherwise >= max_seq*kv_dim and a multiple of 4
+ * (every sequence starts 16-byte aligned).  1 <= max_seq <= 4096. */
 typedef struct {
     float *k, *v;
     int64_t seq_stride;

@@ -380,6 +380,9 @@ rz_status check_kv(const rz_kv_cache *kv, const char *fn, int64_t m, int kv_dim,
     if (kv->max_seq > 4096) return fail(RZ_ERR_UNSUPPORTED, "%s: max_seq=%d > 4096", fn, kv->max_seq);
     if (m > 1 && kv->seq_stride < (int64_t)kv->max_seq * kv_dim)
         return fail(RZ_ERR_SHAPE, "%s: seq_stride=%lld < max_seq*kv_dim", fn, (long long)kv->seq_stride);
+    if (m > 1 && kv->seq_stride % 4)
+        return fail(RZ_ERR_ALIGN, "%s: seq_stride=%lld is not a multiple of 4 (16-byte sequence starts)", fn,
+                    (long long)kv->seq_stride);
     *out = KvDesc{kv->k, kv->v, m > 1 ? kv->seq_stride : 0, kv->max_seq};
     return RZ_OK;
 }

@@ -19,11 +19,12 @@
 // z, z + Z, ... in turn, Z sized so that every CTA is resident at once and the
 // chunks are spread evenly.  It rotates its query heads once, and the CTA that
 // works the chunk holding the token's own row rotates k, writes k and v to the
-// cache and uses them from shared memory.  A chunk's K and V rows are bulk-
-// copied into shared memory (32 KB each at head_dim 128), and each buffer is
-// refilled with the CTA's next chunk as soon as it has been read, so the copies
-// of the next chunk overlap the work on this one and HBM rather than latency or
-// a second wave of CTAs bounds the kernel.  Each CTA leaves per chunk the max,
+// cache and uses them from shared memory.  A chunk's K and V rows arrive in
+// shared memory as one TMA tensor copy each (a box of one kv head's columns over
+// 64 cache rows, 32 KB at head_dim 128), and each buffer is refilled with the
+// CTA's next chunk as soon as it has been read, so the copies of the next chunk
+// overlap the work on this one and HBM rather than latency or a second wave of
+// CTAs bounds the kernel.  Each CTA leaves per chunk the max,
 // exp-sum and unnormalised weighted values; the CTA that completes the last
 // chunks of a (token, kv head) -- found with an atomic
 // counter, no spinning -- merges the chunks with the log-sum-exp rule and writes
@@ -127,9 +128,9 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
 // are copied in once the scores have read the K rows, and the smaller footprint
 // lets more CTAs share an SM.
 template <int CPT>
-__global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const __grid_constant__ AttnArgs a)
 {
-    extern __shared__ __align__(16) float sm[];
+    extern __shared__ __align__(128) float sm[];
     const int kvh = blockIdx.x, t = blockIdx.y, chunk = blockIdx.z;
     const int hd = a.head_dim, G = a.group;
     const int nbuf = a.att_bufs;
@@ -166,24 +167,23 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
     const bool own = pos_ok && own_chunk >= chunk && (own_chunk - chunk) % Z == 0;
 
     if (rows_of(chunk) > 0) {
-        // K and V rows of chunk c on their way into kbuf / vbuf, one bulk copy per
-        // row (the token's own row is taken from kn / vn: its cache copy is written
-        // by this CTA).  A buffer is refilled for the CTA's next chunk as soon as
-        // every thread is done with it, so the next chunk streams in meanwhile.
+        // K and V rows of chunk c on their way into kbuf / vbuf: one tensor copy each
+        // (a box of this kv head's columns over the chunk's 64 rows; rows past the
+        // cache read as zero, rows past the position are copied but unused; the
+        // token's own row is taken from kn / vn: its cache copy is written by this
+        // CTA).  A buffer is refilled for the CTA's next chunk as soon as every
+        // thread is done with it, so the next chunk streams in meanwhile.
         auto issue_k = [&](int c) {
-            const int nr = rows_of(c);
-            if (tid == 0) mbar_arrive_expect_tx(kbar, (unsigned)(nr * hd * 4));
-            if (tid < nr)
-                bulk_g2s(kbuf + tid * hd, a.kc + kv_base + (int64_t)(c * kChunk + tid) * a.kv_dim,
-                         (unsigned)(hd * 4), kbar);
+            if (tid == 0) {
+                mbar_arrive_expect_tx(kbar, (unsigned)(kChunk * hd * 4));
+                tma_load_3d(kbuf, &a.kmap, kvh * hd, c * kChunk, t, kbar);
+            }
         };
         auto issue_v = [&](int c) {
-            const int nr = rows_of(c);
-            if (tid == 0) mbar_arrive_expect_tx(vbar, (unsigned)(nr * hd * 4));
-            if (tid >= kChunk && tid - kChunk < nr)
-                bulk_g2s(vbuf + (tid - kChunk) * hd,
-                         a.vc + kv_base + (int64_t)(c * kChunk + tid - kChunk) * a.kv_dim, (unsigned)(hd * 4),
-                         vbar);
+            if (tid == 0) {
+                mbar_arrive_expect_tx(vbar, (unsigned)(kChunk * hd * 4));
+                tma_load_3d(vbuf, &a.vmap, kvh * hd, c * kChunk, t, vbar);
+            }
         };
         if (tid == 0) {
             mbar_init(kbar, 1);
@@ -525,6 +525,16 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
 {
     AttnArgs args = a;
     void *kargs[] = {&args};
+    {
+        // the caches as [m][max_seq][kv_dim] f32 tensors; a box is one head x 64 rows
+        const uint64_t seq = a.m > 1 ? (uint64_t)a.seq_stride * 4 : (uint64_t)a.max_seq * a.kv_dim * 4;
+        const uint64_t dims[3] = {(uint64_t)a.kv_dim, (uint64_t)a.max_seq, (uint64_t)a.m};
+        const uint64_t strides[2] = {(uint64_t)a.kv_dim * 4, seq};
+        const uint32_t box[3] = {(uint32_t)a.head_dim, (uint32_t)kChunk, 1u};
+        cudaError_t e = encode_tensor_map(&args.kmap, a.kc, 4, 3, dims, strides, box);
+        if (e == cudaSuccess) e = encode_tensor_map(&args.vmap, a.vc, 4, 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
     if (a.make_table) {
         cudaError_t e = launch_rope_table(a, s);
         if (e != cudaSuccess) return e;

@@ -15,6 +15,10 @@ namespace rz {
 // driver's cuTensorMapEncodeTiled (looked up once through the runtime).
 cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
                                  uint64_t row_stride, uint32_t box_inner, uint32_t box_rows);
+// The same for rank dimensions (dims[0] innermost; strides[i] = bytes between
+// consecutive indices of dimension i + 1).
+cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int elem_bytes, int rank, const uint64_t *dims,
+                              const uint64_t *strides, const uint32_t *box);
 
 // Device properties of the current device (cached per device).
 struct DevInfo {
@@ -100,6 +104,7 @@ cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, 
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
+    CUtensorMap kmap, vmap;      // the caches as [m][max_seq][kv_dim] f32, boxes of one head x 64 rows
     const float *q, *k, *v;      // pre-RoPE projections of token t at + t * ld_qkv
     int64_t ld_qkv;
     float *rope_tab;             // workspace f32 [m][head_dim/2][2]: cos, sin of each pair angle

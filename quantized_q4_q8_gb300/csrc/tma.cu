@@ -13,8 +13,7 @@ std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 }  // namespace
 
-cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
-                                 uint64_t row_stride, uint32_t box_inner, uint32_t box_rows)
+static PFN_cuTensorMapEncodeTiled_v12000 encoder()
 {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
@@ -24,7 +23,15 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_by
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return cudaErrorNotSupported;
+    return g_encode;
+}
+
+cudaError_t encode_tensor_map(CUtensorMap *map, const void *base, int elem_bytes, int rank, const uint64_t *dims,
+                              const uint64_t *strides, const uint32_t *box)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
     CUtensorMapDataType type;
     switch (elem_bytes) {
     case 1: type = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
@@ -32,14 +39,27 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_by
     case 4: type = CU_TENSOR_MAP_DATA_TYPE_UINT32; break;
     default: return cudaErrorInvalidValue;
     }
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {row_stride};
-    const cuuint32_t box[2] = {box_inner, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    const CUresult r = enc(map, type, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
+                                 uint64_t row_stride, uint32_t box_inner, uint32_t box_rows)
+{
+    const uint64_t dims[2] = {inner, rows};
+    const uint64_t strides[1] = {row_stride};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_tensor_map(map, base, elem_bytes, 2, dims, strides, box);
 }
 
 }  // namespace rz

@@ -198,3 +198,41 @@ def test_residual_add_bit_exact(rz, n):
 
 def test_device_errors_none_after_suite(rz):
     check_no_device_error()
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16])
+def test_q4k_gemv_integer_inputs_exact(rz, m):
+    """Integer-valued inputs make the GEMV exact in f32: d = 1, dmin = 0, scales and
+    codes below 4 (so every partial sum stays below 2^24), and activations that
+    are integers with a +-127 in every block (d8 = 1, q8 = x).  Then
+    y = sum_j sc_j I_j exactly, and every kernel path -- the dp4a forms for one to
+    three tokens and the tensor-core form from four on -- must return exactly
+    that: a wrong sub-block dot, scale or column mapping cannot hide in rounding."""
+    out_dim, in_dim = 1000, 512
+    g = np.random.default_rng(100 + m)
+    nsb = in_dim // 256
+    w = np.zeros((out_dim, nsb * 144), np.uint8)
+    blocks = []
+    for r in range(out_dim):
+        for b in range(nsb):
+            sc = g.integers(0, 4, 8).astype(np.uint8)
+            mn = g.integers(0, 64, 8).astype(np.uint8)
+            q = g.integers(0, 4, 256).astype(np.uint8)
+            w[r, b * 144:(b + 1) * 144] = oracle.q4k_pack(0x3C00, 0x0000, sc, mn, q)   # d = 1, dmin = 0
+            blocks.append((sc, q))
+    x = g.integers(-127, 128, (m, in_dim)).astype(np.float32)
+    x[:, ::32] = 127.0                                   # every block's max is 127: d8 = 1
+    x8 = oracle.q8_1_quantize(x)
+    d8, s8, q8 = oracle.q8_1_fields(x8, m, in_dim)
+    assert (d8 == 1.0).all() and np.array_equal(q8.reshape(m, in_dim), x.astype(np.int8))
+    expect = np.zeros((m, out_dim), np.int64)
+    qi = x.astype(np.int64).reshape(m, in_dim // 32, 32)
+    for r in range(out_dim):
+        for b in range(nsb):
+            sc, q = blocks[r * nsb + b]
+            I = (q.astype(np.int64).reshape(8, 32)[None] * qi[:, b * 8:(b + 1) * 8]).sum(-1)   # [m, 8]
+            expect[:, r] += (I * sc.astype(np.int64)[None]).sum(-1)
+    assert np.abs(expect).max() < 2 ** 24
+    y = rz.q4k_q8_gemv(to_dev(w), to_dev(x8), m, out_dim, in_dim).cpu().numpy()
+    check_no_device_error()
+    assert np.array_equal(y, expect.astype(np.float32))
