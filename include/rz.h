@@ -146,6 +146,19 @@ rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, i
                               int64_t ldy, int64_t m, int64_t in_dim, rz_stream stream);
 
 /*
+ * rz_q4k_f32_gemv -- y = W x (+ bias) for Q4_K weights and f32 activations, with no
+ * Q8_1 quantisation of x (q4k_gemv_cached_async in transformer_layer_gpu_cached,
+ * realizar 0.8.5 src/cuda/executor/cached.rs):
+ *     y[t][r] = sum_e (d * sc_j * q_e - dmin * m_j) x[t][e]   (+ bias[r])
+ *   w Q4_K [out_dim][in_dim]   x f32 [m][in_dim]   y f32 [m][out_dim]   bias f32 [out_dim] or NULL
+ *   1 <= m <= RZ_MAX_BATCH, in_dim % 256 == 0; w and x 16-byte aligned, y and bias
+ *   4-byte aligned.  f32 products and sums (order differs from a sequential sum;
+ *   deterministic run to run).
+ */
+rz_status rz_q4k_f32_gemv(const void *w, const float *x, const float *bias, float *y, int64_t m, int64_t out_dim,
+                          int64_t in_dim, rz_stream stream);
+
+/*
  * rz_q4_0_gemv -- y = W x for Q4_0 weights and f32 activations (the LM head of
  * GpuModelQ4::forward, q4_0_gemv_into; step 5 of that function).
  *   w  Q4_0 [out_dim][in_dim]   x  f32 [m][in_dim]   y  f32 [m][out_dim]
@@ -154,6 +167,15 @@ rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, i
  */
 rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                        int64_t in_dim, rz_stream stream);
+
+/*
+ * rz_q4_0_gemv_bias -- rz_q4_0_gemv plus a bias added to every token's output:
+ * y[t][r] = (W x_t)_r + bias[r] (the LM-head bias of preload_lm_head_bias,
+ * realizar 0.8.5 src/cuda/executor/cached.rs).  bias f32 [out_dim], 4-byte
+ * aligned; other arguments as rz_q4_0_gemv.
+ */
+rz_status rz_q4_0_gemv_bias(const void *w, const float *x, const float *bias, float *y, int64_t m, int64_t out_dim,
+                            int64_t in_dim, rz_stream stream);
 
 /*
  * rz_rmsnorm -- RMSNorm with optional fused Q8_1 quantisation (rms_norm_inplace in
@@ -276,6 +298,8 @@ rz_status rz_decode_layer(const float *input, const rz_layer_weights *w, const r
  *   layers, kvs   host arrays of n_layers descriptors (same hidden, hidden_pad,
  *                 eps and kv max_seq for every layer)
  *   out_gamma     f32 [hidden];  lm_head Q4_0 [vocab][hidden]
+ *   lm_bias       f32 [vocab] added to the logits (preload_lm_head_bias in realizar
+ *                 0.8.5 cached.rs), or NULL
  *   hidden_out    f32 [m][hidden_pad] final hidden state, or NULL
  *   logits        f32 [m][vocab]
  */
@@ -283,7 +307,7 @@ size_t rz_decode_stack_workspace_bytes(const rz_layer_weights *layers, int32_t n
                                        int32_t max_seq);
 rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
                           int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
-                          const float *out_gamma, const void *lm_head, int64_t vocab,
+                          const float *out_gamma, const void *lm_head, const float *lm_bias, int64_t vocab,
                           float *hidden_out, float *logits, void *workspace, size_t ws_bytes,
                           rz_stream stream);
 
@@ -297,6 +321,40 @@ rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, co
 rz_status rz_decode_layers(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
                            int32_t n_layers, const int32_t *positions, int32_t position, int64_t m, float *output,
                            void *workspace, size_t ws_bytes, rz_stream stream);
+
+/*
+ * The Q4_0 whole-model layer (GpuModelQ4::forward_layer of realizar 0.8.4
+ * src/gpu/adapters/using.rs): every projection Q4_0 against f32 activations.
+ *   wqkv   Q4_0 [n_heads*head_dim + 2*n_kv_heads*head_dim][hidden] (Q rows, then K, then V)
+ *   wo     Q4_0 [hidden][n_heads*head_dim]
+ *   wgate  Q4_0 [inter][hidden], or NULL for the GELU FFN
+ *   wup    Q4_0 [inter][hidden]      wdown  Q4_0 [hidden][inter]
+ *   attn_gamma, ffn_gamma f32 [hidden]
+ * hidden and inter multiples of 32 (hidden <= 16384), head_dim a multiple of 32 in
+ * [32, 256], rope as rz_layer_weights.
+ * Step order: RMSNorm -> QKV GEMV -> RoPE q, k at the position, KV append,
+ * attention over rows 0..position -> O GEMV -> + input -> RMSNorm -> FFN ->
+ * + residual.  FFN: silu(gate) * up then down (ffn_swiglu_gpu) with a gate,
+ * else GELU(up) then down (ffn_standard_gpu), GELU in its tanh form
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).  Intermediates are f32.
+ */
+typedef struct {
+    const void *wqkv, *wo, *wgate, *wup, *wdown;
+    const float *attn_gamma, *ffn_gamma;
+    int32_t hidden, n_heads, n_kv_heads, head_dim, inter;
+    float eps, rope_theta;
+    int32_t rope_mode;
+} rz_layer_weights_q4_0;
+
+/*
+ * rz_decode_layer_q4_0 -- one decode step of one Q4_0 layer for m tokens.
+ *   input, output f32 [m][hidden] (output may alias input); kv, positions,
+ *   position and the workspace (zero-filled once) as for rz_decode_layer.
+ */
+size_t rz_decode_layer_q4_0_workspace_bytes(const rz_layer_weights_q4_0 *w, int64_t m, int32_t max_seq);
+rz_status rz_decode_layer_q4_0(const float *input, const rz_layer_weights_q4_0 *w, const rz_kv_cache *kv,
+                               const int32_t *positions, int32_t position, int64_t m, float *output, void *workspace,
+                               size_t ws_bytes, rz_stream stream);
 
 /*
  * rz_decode_stack_launches -- the number of librz kernels one rz_decode_stack call

@@ -20,9 +20,10 @@ __all__ = [
     "q4k_unpack", "q4k_pack", "q4k_dequantize",
     "q4_0_unpack", "q4_0_pack", "q4_0_dequantize",
     "q8_1_quantize", "q8_1_dequantize", "q8_1_fields", "q8_1_size",
-    "q4k_q8_subblock_dots", "q4k_q8_gemv", "q4_0_gemv",
+    "q4k_q8_subblock_dots", "q4k_q8_gemv", "q4k_f32_gemv", "q4_0_gemv",
     "rmsnorm", "residual_add", "silu", "rope", "attention",
     "LayerWeights", "swiglu_ffn", "decode_layer", "decode_stack",
+    "gelu", "LayerWeightsQ40", "decode_layer_q4_0",
     "Q4K_BYTES", "Q4_0_BYTES",
 ]
 
@@ -75,6 +76,15 @@ class _OrcLayer(C.Structure):
     ]
 
 
+class _OrcLayerQ40(C.Structure):
+    _fields_ = [
+        ("wqkv", _u8p), ("wo", _u8p), ("wgate", _u8p), ("wup", _u8p), ("wdown", _u8p),
+        ("attn_gamma", _f32p), ("ffn_gamma", _f32p),
+        ("hidden", _i64), ("n_heads", _i64), ("n_kv_heads", _i64), ("head_dim", _i64), ("inter", _i64),
+        ("eps", C.c_float), ("rope_theta", C.c_double), ("rope_mode", C.c_int),
+    ]
+
+
 def _declare(L):
     sig = {
         "orc_threads": (C.c_int, []),
@@ -93,6 +103,7 @@ def _declare(L):
         "orc_q4k_q8_subblock_dots": (None, [_u8p, _u8p, _i32p, _i64, _i64]),
         "orc_q4k_q8_gemv": (None, [_u8p, _u8p, _f32p, _i64, _i64, _i64]),
         "orc_q4_0_gemv": (None, [_u8p, _f32p, _f32p, _i64, _i64, _i64]),
+        "orc_q4k_f32_gemv": (None, [_u8p, _f32p, _f32p, _i64, _i64, _i64]),
         "orc_rmsnorm": (None, [_f32p, _f32p, _f32p, _i64, _i64, _i64, C.c_float]),
         "orc_residual_add": (None, [_f32p, _f32p, _f32p, _i64]),
         "orc_silu": (C.c_double, [C.c_double]),
@@ -101,9 +112,11 @@ def _declare(L):
         "orc_swiglu_ffn": (None, [_f32p, _f32p, _u8p, _u8p, _u8p, _f32p,
                                   _i64, _i64, _i64, C.c_float]),
         "orc_decode_layer": (None, [_f32p, C.POINTER(_OrcLayer), _f32p, _f32p, _i64, _f32p]),
+        "orc_gelu": (C.c_double, [C.c_double]),
+        "orc_decode_layer_q4_0": (None, [_f32p, C.POINTER(_OrcLayerQ40), _f32p, _f32p, _i64, _f32p]),
         "orc_decode_stack": (None, [_f32p, C.POINTER(_OrcLayer), _i64,
                                     C.POINTER(_f32p), C.POINTER(_f32p), _i64,
-                                    _f32p, _u8p, _i64, _i64, _i64, C.c_float,
+                                    _f32p, _u8p, _f32p, _i64, _i64, _i64, C.c_float,
                                     _f32p, _f32p]),
     }
     for name, (res, args) in sig.items():
@@ -257,6 +270,19 @@ def q4k_q8_gemv(w, x8, m, out_dim, in_dim) -> np.ndarray:
     return y
 
 
+def q4k_f32_gemv(w, x, out_dim, in_dim) -> np.ndarray:
+    """Q4_K weights times f32 activations [m, in_dim] (no Q8_1) -> float32 [m, out_dim]."""
+    w = _u8(w)
+    x = _f32(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    m = x.shape[0]
+    assert x.shape[1] == in_dim and w.size == out_dim * (in_dim // 256) * Q4K_BYTES
+    y = np.empty((m, out_dim), np.float32)
+    lib().orc_q4k_f32_gemv(_p(w, C.c_uint8), _p(x, C.c_float), _p(y, C.c_float), m, out_dim, in_dim)
+    return y
+
+
 def q4_0_gemv(w, x, out_dim, in_dim) -> np.ndarray:
     w = _u8(w)
     x = _f32(x)
@@ -388,7 +414,7 @@ def decode_layer(x, lw: LayerWeights, kc: np.ndarray, vc: np.ndarray, pos: int) 
 
 
 def decode_stack(x, layers, kcs, vcs, pos, out_gamma, lm_head, vocab,
-                 hidden=None, hidden_pad=None, eps=None):
+                 hidden=None, hidden_pad=None, eps=None, lm_bias=None):
     """Layers, output RMSNorm and the Q4_0 LM head; returns (hidden, logits)."""
     x = _f32(x)
     n = len(layers)
@@ -407,8 +433,64 @@ def decode_stack(x, layers, kcs, vcs, pos, out_gamma, lm_head, vocab,
     lm = _u8(lm_head)
     hid = np.empty(hp, np.float32)
     logits = np.empty(vocab, np.float32)
+    lb = None if lm_bias is None else _f32(lm_bias)
     lib().orc_decode_stack(_p(x, C.c_float), structs, n, kp, vp, pos, _p(og, C.c_float),
-                           _p(lm, C.c_uint8), vocab, hidden, hp, eps,
+                           _p(lm, C.c_uint8), None if lb is None else _p(lb, C.c_float), vocab, hidden, hp, eps,
                            _p(hid, C.c_float), _p(logits, C.c_float))
     del keeps
     return hid, logits
+
+
+# ---------------------------------------------------------------- Q4_0 whole-model layer
+def gelu(x: float) -> float:
+    return lib().orc_gelu(float(x))
+
+
+@dataclass
+class LayerWeightsQ40:
+    """Host copy of one Q4_0 layer: fused QKV [q + 2 kv][hidden], O, optional gate,
+    up, down (uint8 Q4_0 blocks); gammas f32 [hidden]."""
+    wqkv: np.ndarray
+    wo: np.ndarray
+    wgate: np.ndarray   # or None: the GELU FFN
+    wup: np.ndarray
+    wdown: np.ndarray
+    attn_gamma: np.ndarray
+    ffn_gamma: np.ndarray
+    hidden: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    inter: int
+    eps: float
+    rope_theta: float
+    rope_mode: int
+
+    def _struct(self):
+        keep = {k: _u8(getattr(self, k)) for k in ("wqkv", "wo", "wup", "wdown")}
+        if self.wgate is not None:
+            keep["wgate"] = _u8(self.wgate)
+        keep["attn_gamma"] = _f32(self.attn_gamma)
+        keep["ffn_gamma"] = _f32(self.ffn_gamma)
+        s = _OrcLayerQ40(
+            wqkv=_p(keep["wqkv"], C.c_uint8), wo=_p(keep["wo"], C.c_uint8),
+            wgate=_p(keep["wgate"], C.c_uint8) if "wgate" in keep else None,
+            wup=_p(keep["wup"], C.c_uint8), wdown=_p(keep["wdown"], C.c_uint8),
+            attn_gamma=_p(keep["attn_gamma"], C.c_float), ffn_gamma=_p(keep["ffn_gamma"], C.c_float),
+            hidden=self.hidden, n_heads=self.n_heads, n_kv_heads=self.n_kv_heads,
+            head_dim=self.head_dim, inter=self.inter, eps=self.eps, rope_theta=self.rope_theta,
+            rope_mode=self.rope_mode)
+        return s, keep
+
+
+def decode_layer_q4_0(x, lw: LayerWeightsQ40, kc: np.ndarray, vc: np.ndarray, pos: int) -> np.ndarray:
+    """One token through one Q4_0 layer; kc, vc (float32 [max_seq, kv_dim]) updated at row pos."""
+    assert kc.dtype == np.float32 and kc.flags.c_contiguous
+    assert vc.dtype == np.float32 and vc.flags.c_contiguous
+    x = _f32(x)
+    s, keep = lw._struct()
+    out = np.empty(lw.hidden, np.float32)
+    lib().orc_decode_layer_q4_0(_p(x, C.c_float), C.byref(s), _p(kc, C.c_float), _p(vc, C.c_float), pos,
+                                _p(out, C.c_float))
+    del keep
+    return out

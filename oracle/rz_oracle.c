@@ -332,6 +332,34 @@ void orc_q4k_q8_gemv(const uint8_t *w, const uint8_t *x8, float *y,
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Q4_K x f32 (no activation quantisation; q4k_gemv_cached_async in          */
+/* transformer_layer_gpu_cached): y_r = sum_e w_re * x_e with the dequantised */
+/* weight w = d * sc_j * q - dmin * m_j, accumulated in f64.                  */
+/* ------------------------------------------------------------------------- */
+void orc_q4k_f32_gemv(const uint8_t *w, const float *x, float *y,
+                      int64_t m, int64_t out_dim, int64_t in_dim)
+{
+    int64_t nsb = in_dim / ORC_QK_K;
+    for (int64_t t = 0; t < m; ++t)
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < out_dim; ++r) {
+            uint16_t d, dmin;
+            uint8_t sc[8], mn[8], q[256];
+            double acc = 0.0;
+            for (int64_t b = 0; b < nsb; ++b) {
+                orc_q4k_unpack(w + (r * nsb + b) * ORC_Q4K_BYTES, &d, &dmin, sc, mn, q);
+                double dd = orc_f16_to_f64(d), dm = orc_f16_to_f64(dmin);
+                const float *xb = x + t * in_dim + b * ORC_QK_K;
+                for (int e = 0; e < 256; ++e) {
+                    int j = e / 32;
+                    acc += (dd * sc[j] * q[e] - dm * mn[j]) * (double)xb[e];
+                }
+            }
+            y[t * out_dim + r] = (float)acc;
+        }
+}
+
 void orc_q4_0_gemv(const uint8_t *w, const float *x, float *y,
                    int64_t m, int64_t out_dim, int64_t in_dim)
 {
@@ -546,7 +574,7 @@ void orc_decode_layer(const float *input, const orc_layer *L, float *kc, float *
 
 void orc_decode_stack(const float *input, const orc_layer *layers, int64_t n_layers,
                       float *const *kcs, float *const *vcs, int64_t pos,
-                      const float *out_gamma, const uint8_t *lm_head, int64_t vocab,
+                      const float *out_gamma, const uint8_t *lm_head, const float *lm_bias, int64_t vocab,
                       int64_t hidden, int64_t hidden_pad, float eps,
                       float *hidden_out, float *logits)
 {
@@ -562,6 +590,75 @@ void orc_decode_stack(const float *input, const orc_layer *layers, int64_t n_lay
     memcpy(hidden_out, a, (size_t)hidden_pad * sizeof(float));
     orc_rmsnorm(a, out_gamma, b, 1, hidden, hidden_pad, eps);
     orc_q4_0_gemv(lm_head, b, logits, 1, vocab, hidden);
+    if (lm_bias) /* the LM-head bias (preload_lm_head_bias in cached.rs): one f32 add */
+        orc_residual_add(logits, lm_bias, logits, vocab);
     free(a);
     free(b);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Q4_0 whole-model layer (GpuModelQ4::forward_layer, realizar 0.8.4          */
+/* src/gpu/adapters/using.rs): RMSNorm -> fused QKV Q4_0 GEMV -> RoPE q, k ->  */
+/* attention over the cache -> output Q4_0 GEMV -> residual -> RMSNorm ->     */
+/* FFN -> residual.  The FFN is ffn_swiglu_gpu (silu(gate) * up, then down)   */
+/* when a gate matrix is given, else ffn_standard_gpu (up, GELU, down).       */
+/* Every intermediate is an f32 buffer, as in the page.                       */
+/* ------------------------------------------------------------------------- */
+double orc_gelu(double x)
+{
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+void orc_decode_layer_q4_0(const float *input, const orc_layer_q4_0 *L, float *kc, float *vc,
+                           int64_t pos, float *output)
+{
+    int64_t hidden = L->hidden;
+    int64_t q_dim = L->n_heads * L->head_dim;
+    int64_t kv_dim = L->n_kv_heads * L->head_dim;
+    int64_t qkv_dim = q_dim + 2 * kv_dim;
+    float *normed = (float *)malloc((size_t)hidden * sizeof(float));
+    float *qkv = (float *)malloc((size_t)qkv_dim * sizeof(float));
+    float *att = (float *)malloc((size_t)q_dim * sizeof(float));
+    float *o = (float *)malloc((size_t)hidden * sizeof(float));
+    float *res1 = (float *)malloc((size_t)hidden * sizeof(float));
+    float *n2 = (float *)malloc((size_t)hidden * sizeof(float));
+    float *u = (float *)malloc((size_t)L->inter * sizeof(float));
+    float *g = (float *)malloc((size_t)L->inter * sizeof(float));
+    float *h = (float *)malloc((size_t)L->inter * sizeof(float));
+    float *dn = (float *)malloc((size_t)hidden * sizeof(float));
+
+    orc_rmsnorm(input, L->attn_gamma, normed, 1, hidden, hidden, L->eps);
+    orc_q4_0_gemv(L->wqkv, normed, qkv, 1, qkv_dim, hidden);
+    float *q = qkv, *k = qkv + q_dim, *v = qkv + q_dim + kv_dim;
+    orc_rope(q, L->n_heads, L->head_dim, pos, L->rope_theta, L->rope_mode);
+    orc_rope(k, L->n_kv_heads, L->head_dim, pos, L->rope_theta, L->rope_mode);
+    memcpy(kc + pos * kv_dim, k, (size_t)kv_dim * sizeof(float));
+    memcpy(vc + pos * kv_dim, v, (size_t)kv_dim * sizeof(float));
+    orc_attention(q, kc, vc, pos, L->n_heads, L->n_kv_heads, L->head_dim, att);
+    orc_q4_0_gemv(L->wo, att, o, 1, hidden, q_dim);
+    orc_residual_add(input, o, res1, hidden);
+    orc_rmsnorm(res1, L->ffn_gamma, n2, 1, hidden, hidden, L->eps);
+    orc_q4_0_gemv(L->wup, n2, u, 1, L->inter, hidden);
+    if (L->wgate) {
+        orc_q4_0_gemv(L->wgate, n2, g, 1, L->inter, hidden);
+        for (int64_t i = 0; i < L->inter; ++i)
+            h[i] = (float)(orc_silu((double)g[i]) * (double)u[i]);
+    } else {
+        for (int64_t i = 0; i < L->inter; ++i)
+            h[i] = (float)orc_gelu((double)u[i]);
+    }
+    orc_q4_0_gemv(L->wdown, h, dn, 1, hidden, L->inter);
+    orc_residual_add(res1, dn, output, hidden);
+
+    free(normed);
+    free(qkv);
+    free(att);
+    free(o);
+    free(res1);
+    free(n2);
+    free(u);
+    free(g);
+    free(h);
+    free(dn);
 }

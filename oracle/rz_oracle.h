@@ -74,6 +74,10 @@ void orc_q4k_q8_subblock_dots(const uint8_t *w, const uint8_t *x8, int32_t *I,
    x8 the Q8_1 buffer of m rows of in_dim. */
 void orc_q4k_q8_gemv(const uint8_t *w, const uint8_t *x8, float *y,
                      int64_t m, int64_t out_dim, int64_t in_dim);
+/* Q4_K weights against f32 activations (no Q8_1): y[t][r] = sum_e w[r][e] x[t][e]
+   with the dequantised weights, accumulated in f64. */
+void orc_q4k_f32_gemv(const uint8_t *w, const float *x, float *y,
+                      int64_t m, int64_t out_dim, int64_t in_dim);
 /* y[t][r] = sum_i w[r][i] * x[t][i]; w row-major [out_dim][in_dim/32] Q4_0 blocks */
 void orc_q4_0_gemv(const uint8_t *w, const float *x, float *y,
                    int64_t m, int64_t out_dim, int64_t in_dim);
@@ -112,12 +116,32 @@ void orc_swiglu_ffn(const float *x, const float *gamma, const uint8_t *wgate,
    to its projection's output before RoPE. */
 void orc_decode_layer(const float *input, const orc_layer *L, float *kc, float *vc,
                       int64_t pos, float *output);
-/* layers, then output RMSNorm, then Q4_0 LM head -> logits[vocab]. */
+/* layers, then output RMSNorm, then Q4_0 LM head (+ lm_bias, when not NULL) -> logits[vocab]. */
 void orc_decode_stack(const float *input, const orc_layer *layers, int64_t n_layers,
                       float *const *kcs, float *const *vcs, int64_t pos,
-                      const float *out_gamma, const uint8_t *lm_head, int64_t vocab,
+                      const float *out_gamma, const uint8_t *lm_head, const float *lm_bias, int64_t vocab,
                       int64_t hidden, int64_t hidden_pad, float eps,
                       float *hidden_out, float *logits);
+
+/* ---- Q4_0 whole-model layer (GpuModelQ4::forward_layer of realizar 0.8.4
+   src/gpu/adapters/using.rs): every projection Q4_0 against f32 activations. */
+/* GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+double orc_gelu(double x);
+typedef struct {
+    const uint8_t *wqkv;   /* Q4_0 [q_dim + 2 kv_dim][hidden]: Q rows, then K, then V */
+    const uint8_t *wo;     /* Q4_0 [hidden][q_dim] */
+    const uint8_t *wgate;  /* Q4_0 [inter][hidden], or NULL: the GELU FFN (up -> GELU -> down) */
+    const uint8_t *wup;    /* Q4_0 [inter][hidden] */
+    const uint8_t *wdown;  /* Q4_0 [hidden][inter] */
+    const float *attn_gamma, *ffn_gamma; /* [hidden] */
+    int64_t hidden, n_heads, n_kv_heads, head_dim, inter;
+    float eps;
+    double rope_theta;
+    int rope_mode;
+} orc_layer_q4_0;
+/* One decode step of one token at `pos`; kc/vc [max_seq][kv_dim], written at row pos. */
+void orc_decode_layer_q4_0(const float *input, const orc_layer_q4_0 *L, float *kc, float *vc,
+                           int64_t pos, float *output);
 
 #ifdef __cplusplus
 }

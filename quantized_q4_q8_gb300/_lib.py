@@ -52,7 +52,18 @@ class KvCacheStruct(C.Structure):
     _fields_ = [("k", _vp), ("v", _vp), ("seq_stride", _i64), ("max_seq", _i32)]
 
 
+class LayerWeightsQ40Struct(C.Structure):
+    """rz_layer_weights_q4_0 (device pointers and dims)."""
+    _fields_ = [
+        ("wqkv", _vp), ("wo", _vp), ("wgate", _vp), ("wup", _vp), ("wdown", _vp),
+        ("attn_gamma", _vp), ("ffn_gamma", _vp),
+        ("hidden", _i32), ("n_heads", _i32), ("n_kv_heads", _i32), ("head_dim", _i32), ("inter", _i32),
+        ("eps", _f32), ("rope_theta", _f32), ("rope_mode", _i32),
+    ]
+
+
 _LWP = C.POINTER(LayerWeightsStruct)
+_LQP = C.POINTER(LayerWeightsQ40Struct)
 _KVP = C.POINTER(KvCacheStruct)
 
 # name -> argtypes (restype is rz_status = int unless listed in _RESTYPES)
@@ -64,6 +75,7 @@ SIGNATURES = {
     "rz_rmsnorm_q4k_gemv": [_vp, _i64, _vp, _i64, _f32, _i32, C.POINTER(_vp), C.POINTER(_i64),
                             C.POINTER(_vp), _vp, _i64, _i64, _i64, _vp],
     "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "rz_q4k_f32_gemv": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "rz_rmsnorm": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _vp],
     "rz_residual_add": [_vp, _vp, _vp, _i64, _vp],
     "rz_swiglu_ffn_workspace_bytes": [_i64, _i64, _i64],
@@ -75,8 +87,11 @@ SIGNATURES = {
     "rz_decode_layer_workspace_bytes": [_LWP, _i64, _i32],
     "rz_decode_layer": [_vp, _LWP, _KVP, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
     "rz_decode_stack_workspace_bytes": [_LWP, _i32, _i64, _i32],
-    "rz_decode_stack": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp, _vp,
+    "rz_decode_stack": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
                         _sz, _vp],
+    "rz_q4_0_gemv_bias": [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp],
+    "rz_decode_layer_q4_0_workspace_bytes": [_LQP, _i64, _i32],
+    "rz_decode_layer_q4_0": [_vp, _LQP, _KVP, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
     "rz_decode_layers": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
     "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
@@ -88,6 +103,7 @@ SIGNATURES = {
 _RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p,
              "rz_swiglu_ffn_workspace_bytes": _sz, "rz_attention_workspace_bytes": _sz,
              "rz_decode_layer_workspace_bytes": _sz, "rz_decode_stack_workspace_bytes": _sz,
+             "rz_decode_layer_q4_0_workspace_bytes": _sz,
              "rz_decode_stack_launches": C.c_int32}
 
 _lib = None

@@ -241,6 +241,26 @@ rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, i
     return RZ_OK;
 }
 
+rz_status rz_q4k_f32_gemv(const void *w, const float *x, const float *bias, float *y, int64_t m, int64_t out_dim,
+                          int64_t in_dim, rz_stream stream)
+{
+    const char *fn = "rz_q4k_f32_gemv";
+    t_last_error.clear();
+    if (!w || !x || !y) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (m < 1 || out_dim < 1 || in_dim < 1) return fail(RZ_ERR_INVALID_ARG, "%s: bad sizes", fn);
+    if (m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld > %d", fn, (long long)m, RZ_MAX_BATCH);
+    if (in_dim % 256) return fail(RZ_ERR_SHAPE, "%s: in_dim=%lld is not a multiple of 256", fn, (long long)in_dim);
+    if (!aligned16(w) || !aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 3u) ||
+        (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)))
+        return fail(RZ_ERR_ALIGN, "%s: w and x must be 16-byte aligned, y and bias 4-byte aligned", fn);
+    RZ_TRY(check_device());
+    if (q4k_f32_gemv_group(in_dim) < 1)
+        return fail(RZ_ERR_UNSUPPORTED, "%s: in_dim=%lld does not fit in shared memory", fn, (long long)in_dim);
+    RZ_CUDA(launch_q4k_f32_gemv(w, x, in_dim, y, out_dim, bias, m, out_dim, in_dim, static_cast<cudaStream_t>(stream)),
+            "rz_q4k_f32_gemv launch");
+    return RZ_OK;
+}
+
 rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                        int64_t in_dim, rz_stream stream)
 {
@@ -254,6 +274,22 @@ rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64
     RZ_TRY(check_device());
     RZ_CUDA(launch_q4_0_gemv(w, x, y, m, out_dim, in_dim, static_cast<cudaStream_t>(stream)),
             "rz_q4_0_gemv launch");
+    return RZ_OK;
+}
+
+rz_status rz_q4_0_gemv_bias(const void *w, const float *x, const float *bias, float *y, int64_t m, int64_t out_dim,
+                            int64_t in_dim, rz_stream stream)
+{
+    t_last_error.clear();
+    if (!w || !x || !y || !bias) return fail(RZ_ERR_INVALID_ARG, "rz_q4_0_gemv_bias: null pointer");
+    if (m < 1 || out_dim < 1 || in_dim < 1) return fail(RZ_ERR_INVALID_ARG, "rz_q4_0_gemv_bias: bad sizes");
+    if (m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "rz_q4_0_gemv_bias: m=%lld > %d", (long long)m, RZ_MAX_BATCH);
+    if (in_dim % 32) return fail(RZ_ERR_SHAPE, "rz_q4_0_gemv_bias: in_dim %% 32 != 0");
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+        return fail(RZ_ERR_ALIGN, "rz_q4_0_gemv_bias: alignment");
+    RZ_TRY(check_device());
+    RZ_CUDA(launch_q4_0_gemv(w, x, y, m, out_dim, in_dim, static_cast<cudaStream_t>(stream), bias),
+            "rz_q4_0_gemv_bias launch");
     return RZ_OK;
 }
 
@@ -566,8 +602,8 @@ static rz_status check_stack(const char *fn, const float *input, const rz_layer_
 
 rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, const rz_kv_cache *kvs,
                           int32_t n_layers, const int32_t *positions, int32_t position, int64_t m,
-                          const float *out_gamma, const void *lm_head, int64_t vocab, float *hidden_out,
-                          float *logits, void *workspace, size_t ws_bytes, rz_stream stream)
+                          const float *out_gamma, const void *lm_head, const float *lm_bias, int64_t vocab,
+                          float *hidden_out, float *logits, void *workspace, size_t ws_bytes, rz_stream stream)
 {
     const char *fn = "rz_decode_stack";
     t_last_error.clear();
@@ -577,13 +613,14 @@ rz_status rz_decode_stack(const float *input, const rz_layer_weights *layers, co
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: buffers must be 16-byte aligned", fn);
     if (hidden_out && !aligned16(hidden_out)) return fail(RZ_ERR_ALIGN, "%s: hidden_out alignment", fn);
+    if (lm_bias && (reinterpret_cast<uintptr_t>(lm_bias) & 3u)) return fail(RZ_ERR_ALIGN, "%s: lm_bias alignment", fn);
     std::vector<LayerDesc> Ls;
     std::vector<KvDesc> Ks;
     RZ_TRY(check_stack(fn, input, layers, kvs, n_layers, positions, position, m, Ls, Ks));
     if (Ls[0].hidden % 32) return fail(RZ_ERR_SHAPE, "%s: hidden %% 32 != 0 (Q4_0 LM head blocks)", fn);
     RZ_TRY(check_ws(workspace, ws_bytes, stack_workspace_bytes(Ls[0], m, Ks[0].max_seq), fn));
     RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, out_gamma, lm_head,
-                                vocab, hidden_out, logits, workspace, static_cast<cudaStream_t>(stream)),
+                                lm_bias, vocab, hidden_out, logits, workspace, static_cast<cudaStream_t>(stream)),
             "rz_decode_stack launch");
     return RZ_OK;
 }
@@ -600,9 +637,63 @@ rz_status rz_decode_layers(const float *input, const rz_layer_weights *layers, c
     std::vector<KvDesc> Ks;
     RZ_TRY(check_stack(fn, input, layers, kvs, n_layers, positions, position, m, Ls, Ks));
     RZ_TRY(check_ws(workspace, ws_bytes, stack_workspace_bytes(Ls[0], m, Ks[0].max_seq), fn));
-    RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, nullptr, nullptr, 0,
-                                output, nullptr, workspace, static_cast<cudaStream_t>(stream)),
+    RZ_CUDA(launch_decode_stack(input, Ls.data(), n_layers, Ks.data(), positions, position, m, nullptr, nullptr,
+                                nullptr, 0, output, nullptr, workspace, static_cast<cudaStream_t>(stream)),
             "rz_decode_layers launch");
+    return RZ_OK;
+}
+
+static rz_status check_layer_q4_0(const rz_layer_weights_q4_0 *w, const char *fn, int64_t m, LayerQ40Desc *out)
+{
+    if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
+    RZ_TRY(check_device());
+    const void *ptrs[] = {w->wqkv, w->wo, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma};
+    for (const void *p : ptrs) {
+        if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer", fn);
+        if (!aligned16(p)) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
+    }
+    if (w->wgate && !aligned16(w->wgate)) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld not in [1, %d]", fn, (long long)m, RZ_MAX_BATCH);
+    if (w->hidden < 32 || w->hidden % 32 || w->hidden > 16384)
+        return fail(RZ_ERR_SHAPE, "%s: hidden=%d (a multiple of 32, at most 16384)", fn, w->hidden);
+    if (w->inter < 32 || w->inter % 32) return fail(RZ_ERR_SHAPE, "%s: inter=%d is not a multiple of 32", fn, w->inter);
+    if (w->n_heads < 1 || w->n_kv_heads < 1 || w->n_heads % w->n_kv_heads || w->n_heads / w->n_kv_heads > 16)
+        return fail(RZ_ERR_SHAPE, "%s: n_heads=%d n_kv_heads=%d", fn, w->n_heads, w->n_kv_heads);
+    if (w->head_dim < 32 || w->head_dim > 256 || w->head_dim % 32)
+        return fail(RZ_ERR_SHAPE, "%s: head_dim=%d (multiple of 32 in [32, 256])", fn, w->head_dim);
+    if (attention_smem_bytes(w->n_heads / w->n_kv_heads, w->head_dim, 0) > dev_info().smem_optin)
+        return fail(RZ_ERR_UNSUPPORTED, "%s: the attention of this head shape does not fit a CTA", fn);
+    if (!(w->eps >= 0.0f) || !(w->rope_theta > 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps/rope_theta", fn);
+    if (w->rope_mode != 0 && w->rope_mode != 1) return fail(RZ_ERR_INVALID_ARG, "%s: rope_mode=%d", fn, w->rope_mode);
+    *out = LayerQ40Desc{w->wqkv, w->wo, w->wgate, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma, w->hidden,
+                        w->n_heads, w->n_kv_heads, w->head_dim, w->inter, w->eps, w->rope_theta, w->rope_mode};
+    return RZ_OK;
+}
+
+size_t rz_decode_layer_q4_0_workspace_bytes(const rz_layer_weights_q4_0 *w, int64_t m, int32_t max_seq)
+{
+    LayerQ40Desc L;
+    if (max_seq < 1 || check_layer_q4_0(w, "rz_decode_layer_q4_0_workspace_bytes", m, &L) != RZ_OK) return 0;
+    return layer_q4_0_workspace_bytes(L, m, max_seq);
+}
+
+rz_status rz_decode_layer_q4_0(const float *input, const rz_layer_weights_q4_0 *w, const rz_kv_cache *kv,
+                               const int32_t *positions, int32_t position, int64_t m, float *output, void *workspace,
+                               size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_decode_layer_q4_0";
+    t_last_error.clear();
+    if (!input || !output) return fail(RZ_ERR_INVALID_ARG, "%s: null input/output", fn);
+    if (!aligned16(input) || !aligned16(output)) return fail(RZ_ERR_ALIGN, "%s: input/output alignment", fn);
+    LayerQ40Desc L;
+    RZ_TRY(check_layer_q4_0(w, fn, m, &L));
+    KvDesc kd;
+    RZ_TRY(check_kv(kv, fn, m, L.n_kv_heads * L.head_dim, &kd));
+    RZ_TRY(check_position(positions, position, kv->max_seq, fn));
+    RZ_TRY(check_ws(workspace, ws_bytes, layer_q4_0_workspace_bytes(L, m, kd.max_seq), fn));
+    RZ_CUDA(launch_decode_layer_q4_0(input, L, kd, positions, position, m, output, workspace,
+                                     static_cast<cudaStream_t>(stream)),
+            "rz_decode_layer_q4_0 launch");
     return RZ_OK;
 }
 

@@ -1,4 +1,5 @@
-// elementwise.cu -- Q8_1 quantisation, RMSNorm (with fused Q8_1) and residual add.
+// elementwise.cu -- Q8_1 quantisation, RMSNorm (with fused Q8_1), residual add and
+// the FFN activations of the Q4_0 layer.
 //
 // Q8_1 (q8_quantize_async in realizar 0.8.5 src/cuda/executor/cached.rs,
 // transformer_layer_gpu_true_dp4a steps 2 and 5): per block of 32 values,
@@ -101,7 +102,41 @@ __global__ void residual_add_kernel(const float *a, const float *b, float *out, 
     if (i < n - n4 * 4) out[n4 * 4 + i] = __fadd_rn(a[n4 * 4 + i], b[n4 * 4 + i]);
 }
 
+// FFN activation of the Q4_0 layer (GpuModelQ4::forward_layer): h = silu(g) * u
+// (ffn_swiglu_gpu's fused SwiGLU) when g is given, else h = GELU(u) in its tanh
+// form (ffn_standard_gpu's gelu_gpu).
+__global__ void ffn_act_kernel(const float *g, const float *u, float *h, int64_t n)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float x = u[i];
+    if (g) {
+        const float gv = g[i];
+        h[i] = gv / (1.0f + expf(-gv)) * x;
+    } else {
+        const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+        h[i] = 0.5f * x * (1.0f + tanhf(c * (x + 0.044715f * x * x * x)));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_ffn_act(const float *g, const float *u, float *h, int64_t n, cudaStream_t s)
+{
+    const int threads = 256;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n + threads - 1) / threads));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, ffn_act_kernel, g, u, h, n);
+}
 
 cudaError_t launch_q8_1_quantize(const float *x, void *q8, int64_t m, int64_t n, cudaStream_t s)
 {

@@ -35,6 +35,7 @@ struct Args {
     int m;
     int64_t ldx;   // elements between tokens' activation rows
     int64_t rows_per_cta_max;
+    const float *bias;  // [out_dim] added to every token's row, or nullptr (the LM-head bias)
 };
 
 __device__ __forceinline__ float nib_minus8(uint32_t word, int shift)
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
                         for (int t = 0; t < MT; ++t) {
                             if (t >= a.m) continue;
                             if (direct) {
-                                a.y[t * a.out_dim + rr] = res[u][t];
+                                a.y[t * a.out_dim + rr] = a.bias ? res[u][t] + a.bias[rr] : res[u][t];
                             } else {
                                 float *slot = &part[((rr - r0) * MT + t) * a.wg + wc];
                                 *slot = (cw == wc) ? res[u][t] : *slot + res[u][t];
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
         if (t >= a.m) continue;
         float sum = 0.0f;
         for (int k = 0; k < a.wg; ++k) sum += part[(rl * MT + t) * a.wg + k];
-        a.y[t * a.out_dim + r0 + rl] = sum;
+        a.y[t * a.out_dim + r0 + rl] = a.bias ? sum + a.bias[r0 + rl] : sum;
     }
 }
 
@@ -166,15 +167,16 @@ cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
-                             int64_t in_dim, cudaStream_t s)
+                             int64_t in_dim, cudaStream_t s, const float *bias)
 {
-    return launch_q4_0_gemv_ld(w, x, in_dim, y, m, out_dim, in_dim, s);
+    return launch_q4_0_gemv_ld(w, x, in_dim, y, m, out_dim, in_dim, s, bias);
 }
 
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
-                                int64_t out_dim, int64_t in_dim, cudaStream_t s)
+                                int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias)
 {
     Args a = {};
+    a.bias = bias;
     a.ldx = ldx;
     a.w = static_cast<const uint8_t *>(w);
     a.x = x;

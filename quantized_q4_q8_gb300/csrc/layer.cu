@@ -213,7 +213,7 @@ size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
 
 cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
                                 const KvDesc *kvs, const int32_t *positions, int position, int64_t m,
-                                const float *out_gamma, const void *lm_head, int64_t vocab,
+                                const float *out_gamma, const void *lm_head, const float *lm_bias, int64_t vocab,
                                 float *hidden_out, float *logits, void *workspace, cudaStream_t s)
 {
     const LayerDesc &L0 = layers[0];
@@ -234,7 +234,7 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
     if (!logits) return cudaSuccess;  // the layers only (rz_decode_layers)
     e = launch_rmsnorm(cur, out_gamma, normed, nullptr, m, L0.hidden, L0.hidden_pad, L0.eps, s);
     if (e != cudaSuccess) return e;
-    return launch_q4_0_gemv_ld(lm_head, normed, L0.hidden_pad, logits, m, vocab, L0.hidden, s);
+    return launch_q4_0_gemv_ld(lm_head, normed, L0.hidden_pad, logits, m, vocab, L0.hidden, s, lm_bias);
 }
 
 int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head)
@@ -254,6 +254,83 @@ int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int 
     per_layer += gemv(L0.hidden_pad, EPI_SWIGLU);  // RMSNorm -> gate/up
     per_layer += gemv(L0.inter, EPI_RESID);        // Q8_1 of h -> down
     return 1 /* RoPE table */ + n_layers * per_layer + h;
+}
+
+// ---------------------------------------------------------------- Q4_0 layer
+// GpuModelQ4::forward_layer (realizar 0.8.4 src/gpu/adapters/using.rs) for m
+// tokens: RMSNorm -> fused QKV Q4_0 GEMV -> attention (RoPE, KV append, as in the
+// Q4_K layer) -> O Q4_0 GEMV -> residual -> RMSNorm -> up (and gate) Q4_0 GEMVs
+// -> silu(gate) * up or GELU(up) -> down Q4_0 GEMV -> residual.  Every
+// intermediate is an f32 buffer, as on the page.
+struct LayerQ40Ws {
+    int *counters;
+    float *normed, *qkv, *rope_tab, *part, *att, *o, *res1, *n2, *u, *g, *h, *dn;
+    size_t total;
+};
+
+static LayerQ40Ws layer_q4_0_ws(const LayerQ40Desc &L, int64_t m, int max_seq, uint8_t *base)
+{
+    LayerQ40Ws w{};
+    const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
+    const int group = L.n_heads / L.n_kv_heads;
+    const int chunk = attention_chunk_len(max_seq, L.n_kv_heads, (int)m);
+    const int n_chunks = (max_seq + chunk - 1) / chunk;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return reinterpret_cast<float *>(p);
+    };
+    w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
+    w.normed = take((size_t)m * L.hidden * 4);
+    w.qkv = take((size_t)m * (q_dim + 2 * kv_dim) * 4);
+    w.rope_tab = take((size_t)m * L.head_dim * 4);
+    w.part = take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4);
+    w.att = take((size_t)m * q_dim * 4);
+    w.o = take((size_t)m * L.hidden * 4);
+    w.res1 = take((size_t)m * L.hidden * 4);
+    w.n2 = take((size_t)m * L.hidden * 4);
+    w.u = take((size_t)m * L.inter * 4);
+    w.g = take((size_t)m * L.inter * 4);
+    w.h = take((size_t)m * L.inter * 4);
+    w.dn = take((size_t)m * L.hidden * 4);
+    w.total = off;
+    return w;
+}
+
+size_t layer_q4_0_workspace_bytes(const LayerQ40Desc &L, int64_t m, int max_seq)
+{
+    return layer_q4_0_ws(L, m, max_seq, nullptr).total;
+}
+
+cudaError_t launch_decode_layer_q4_0(const float *input, const LayerQ40Desc &L, const KvDesc &kv,
+                                     const int32_t *positions, int position, int64_t m, float *output,
+                                     void *workspace, cudaStream_t s)
+{
+    LayerQ40Ws w = layer_q4_0_ws(L, m, kv.max_seq, static_cast<uint8_t *>(workspace));
+    const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
+    const int64_t ld_qkv = q_dim + 2 * kv_dim;
+    cudaError_t e = launch_rmsnorm(input, L.attn_gamma, w.normed, nullptr, m, L.hidden, L.hidden, L.eps, s);
+    if (e == cudaSuccess) e = launch_q4_0_gemv_ld(L.wqkv, w.normed, L.hidden, w.qkv, m, ld_qkv, L.hidden, s);
+    if (e != cudaSuccess) return e;
+    LayerDesc ld{};
+    ld.n_heads = L.n_heads;
+    ld.n_kv_heads = L.n_kv_heads;
+    ld.head_dim = L.head_dim;
+    ld.rope_theta = L.rope_theta;
+    ld.rope_mode = L.rope_mode;
+    AttnArgs a = make_attn_args(ld, m, kv, positions, position, w.rope_tab, 1, w.part, w.counters, w.qkv,
+                                w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, w.att, nullptr);
+    e = launch_attention(a, s);
+    if (e == cudaSuccess) e = launch_q4_0_gemv_ld(L.wo, w.att, q_dim, w.o, m, L.hidden, q_dim, s);
+    if (e == cudaSuccess) e = launch_residual_add(input, w.o, w.res1, m * L.hidden, s);
+    if (e == cudaSuccess) e = launch_rmsnorm(w.res1, L.ffn_gamma, w.n2, nullptr, m, L.hidden, L.hidden, L.eps, s);
+    if (e == cudaSuccess) e = launch_q4_0_gemv_ld(L.wup, w.n2, L.hidden, w.u, m, L.inter, L.hidden, s);
+    if (e == cudaSuccess && L.wgate) e = launch_q4_0_gemv_ld(L.wgate, w.n2, L.hidden, w.g, m, L.inter, L.hidden, s);
+    if (e == cudaSuccess) e = launch_ffn_act(L.wgate ? w.g : nullptr, w.u, w.h, m * L.inter, s);
+    if (e == cudaSuccess) e = launch_q4_0_gemv_ld(L.wdown, w.h, L.inter, w.dn, m, L.hidden, L.inter, s);
+    if (e == cudaSuccess) e = launch_residual_add(w.res1, w.dn, output, m * L.hidden, s);
+    return e;
 }
 
 }  // namespace rz

@@ -48,6 +48,8 @@ cudaError_t launch_rmsnorm(const float *x, const float *gamma, float *y, void *q
                            int64_t n, int64_t n_pad, float eps, cudaStream_t s);
 cudaError_t launch_residual_add(const float *a, const float *b, float *out, int64_t n,
                                 cudaStream_t s);
+// h = silu(g) * u (g != nullptr) or GELU(u), n values
+cudaError_t launch_ffn_act(const float *g, const float *u, float *h, int64_t n, cudaStream_t s);
 
 // ---------------------------------------------------------------- Q4_K x Q8_1 GEMV
 enum Q4kEpilogue { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
@@ -99,6 +101,12 @@ cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, c
 // (two stages of one pack: rows up to about 47000 wide at m = 1).
 bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue);
 
+// Q4_K weights times f32 activations without Q8_1 (gemv_q4k_f32.cu): x [m][ldx],
+// y [m][ldy], optional bias [out_dim]; tokens in groups that fit shared memory.
+int q4k_f32_gemv_group(int64_t in_dim);
+cudaError_t launch_q4k_f32_gemv(const void *w, const float *x, int64_t ldx, float *y, int64_t ldy, const float *bias,
+                                int64_t m, int64_t out_dim, int64_t in_dim, cudaStream_t s);
+
 cudaError_t launch_q4k_subblock_dots(const void *w, const void *q8, int32_t *I, int64_t out_dim,
                                      int64_t in_dim, cudaStream_t s);
 
@@ -136,11 +144,12 @@ cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- Q4_0 GEMV
+// bias (nullable) [out_dim] is added to every token's output row
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
-                             int64_t in_dim, cudaStream_t s);
+                             int64_t in_dim, cudaStream_t s, const float *bias = nullptr);
 // as above with activation row stride ldx (elements) between tokens
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
-                                int64_t out_dim, int64_t in_dim, cudaStream_t s);
+                                int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias = nullptr);
 
 // ---------------------------------------------------------------- layer / stack
 // wk == wv == nullptr: wq is the fused [q_dim + 2 kv_dim][hidden_pad] matrix (and
@@ -174,10 +183,23 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
                                 const int32_t *positions, int position, int64_t m, float *output,
                                 void *workspace, cudaStream_t s, int make_table = 1);
 size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
+
+// The Q4_0 whole-model layer (every projection Q4_0 against f32 activations).
+struct LayerQ40Desc {
+    const void *wqkv, *wo, *wgate, *wup, *wdown;  // wgate nullptr: GELU FFN
+    const float *attn_gamma, *ffn_gamma;
+    int hidden, n_heads, n_kv_heads, head_dim, inter;
+    float eps, rope_theta;
+    int rope_mode;
+};
+size_t layer_q4_0_workspace_bytes(const LayerQ40Desc &L, int64_t m, int max_seq);
+cudaError_t launch_decode_layer_q4_0(const float *input, const LayerQ40Desc &L, const KvDesc &kv,
+                                     const int32_t *positions, int position, int64_t m, float *output,
+                                     void *workspace, cudaStream_t s);
 // logits == nullptr: the layers only, the final hidden state in hidden_out.
 cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int n_layers,
                                 const KvDesc *kvs, const int32_t *positions, int position, int64_t m,
-                                const float *out_gamma, const void *lm_head, int64_t vocab,
+                                const float *out_gamma, const void *lm_head, const float *lm_bias, int64_t vocab,
                                 float *hidden_out, float *logits, void *workspace, cudaStream_t s);
 // kernels launched by one launch_decode_stack (with or without the head)
 int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head);

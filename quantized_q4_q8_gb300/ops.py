@@ -9,13 +9,14 @@ __all__ = [
     "q8_1_size", "q4k_bytes", "q4_0_bytes",
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
     "rz_q4k_q8_gemv_ex", "rz_rmsnorm_q4k_gemv", "q4k_q8_gemv_ex", "rmsnorm_q4k_gemv",
+    "rz_q4k_f32_gemv", "q4k_f32_gemv",
     "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_debug_stall_next_gemv",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
     "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
     "DeviceLayer", "DeviceKV", "DeviceStack", "workspace", "swiglu_ffn_workspace_bytes",
     "swiglu_ffn", "rz_swiglu_ffn_static", "attention_workspace_bytes", "attention_decode",
     "decode_layer_workspace_bytes", "decode_layer", "rz_decode_stack", "decode_stack",
-    "rz_decode_layers", "decode_layers",
+    "rz_decode_layers", "decode_layers", "DeviceLayerQ40", "decode_layer_q4_0",
 ]
 
 
@@ -76,6 +77,20 @@ def rz_rmsnorm_q4k_gemv(x, ldx, gamma, n, eps, ws, rows, biases, y, ldy, m, in_d
     bp = None if biases is None else (C.c_void_p * k)(*[_ptr(b) for b in biases])
     return call("rz_rmsnorm_q4k_gemv", _ptr(x), ldx, _ptr(gamma), n, eps, k, wp, rp, bp, _ptr(y), ldy,
                 m, in_dim, _stream(stream))
+
+
+def rz_q4k_f32_gemv(w, x, bias, y, m, out_dim, in_dim, stream=None):
+    return call("rz_q4k_f32_gemv", _ptr(w), _ptr(x), _ptr(bias), _ptr(y), m, out_dim, in_dim, _stream(stream))
+
+
+def q4k_f32_gemv(w, x, out_dim, in_dim, bias=None, out=None, stream=None):
+    """Q4_K weights times f32 activations x [m, in_dim] (no Q8_1) -> f32 [m, out_dim]."""
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    if out is None:
+        out = torch.empty((m, out_dim), dtype=torch.float32, device=w.device)
+    rz_q4k_f32_gemv(w, x, bias, out, m, out_dim, in_dim, stream)
+    return out
 
 
 def rz_q4_0_gemv(w, x, y, m, out_dim, in_dim, stream=None):
@@ -169,14 +184,17 @@ def q4k_q8_subblock_dots(w, q8, out_dim, in_dim, out=None, stream=None):
     return out
 
 
-def q4_0_gemv(w, x, out_dim, in_dim, out=None, stream=None):
+def q4_0_gemv(w, x, out_dim, in_dim, out=None, bias=None, stream=None):
     import torch
     _cuda_contig(w, torch.uint8, "w")
     _cuda_contig(x, torch.float32, "x")
     m = 1 if x.dim() == 1 else x.shape[0]
     if out is None:
         out = torch.empty((m, out_dim), dtype=torch.float32, device=w.device)
-    rz_q4_0_gemv(w, x, out, m, out_dim, in_dim, stream)
+    if bias is None:
+        rz_q4_0_gemv(w, x, out, m, out_dim, in_dim, stream)
+    else:
+        call("rz_q4_0_gemv_bias", _ptr(w), _ptr(x), _ptr(bias), _ptr(out), m, out_dim, in_dim, _stream(stream))
     return out
 
 
@@ -332,10 +350,10 @@ class DeviceStack:
     """Layers + per-layer KV caches + output norm + Q4_0 LM head, with the host
     descriptor arrays the C ABI takes."""
 
-    def __init__(self, layers, kvs, out_gamma, lm_head, vocab):
+    def __init__(self, layers, kvs, out_gamma, lm_head, vocab, lm_bias=None):
         from ._lib import KvCacheStruct, LayerWeightsStruct
         self.layers, self.kvs = layers, kvs
-        self.out_gamma, self.lm_head, self.vocab = out_gamma, lm_head, vocab
+        self.out_gamma, self.lm_head, self.vocab, self.lm_bias = out_gamma, lm_head, vocab, lm_bias
         n = len(layers)
         self.lw = (LayerWeightsStruct * n)(*[l.struct for l in layers])
         self.kv = (KvCacheStruct * n)(*[k.struct for k in kvs])
@@ -354,7 +372,8 @@ def rz_decode_stack(x, stack: "DeviceStack", positions, position, m, hidden_out,
                     stream=None):
     return call("rz_decode_stack", _ptr(x), stack.lw, stack.kv, len(stack.layers),
                 _ptr(positions), position, m, _ptr(stack.out_gamma), _ptr(stack.lm_head),
-                stack.vocab, _ptr(hidden_out), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream))
+                _ptr(stack.lm_bias), stack.vocab, _ptr(hidden_out), _ptr(logits), _ptr(ws), ws.numel(),
+                _stream(stream))
 
 
 def rz_decode_layers(x, stack: "DeviceStack", positions, position, m, out, ws, stream=None):
@@ -384,3 +403,37 @@ def decode_stack(x, stack: "DeviceStack", position=0, positions=None, ws=None, s
         ws = workspace(stack.workspace_bytes(m), x.device)
     rz_decode_stack(x, stack, positions, position, m, hid, logits, ws, stream)
     return hid, logits
+
+
+# ------------------------------------------------------------------ Q4_0 whole-model layer
+class DeviceLayerQ40:
+    """One Q4_0 layer on the GPU: uint8 CUDA tensors wqkv, wo, wup, wdown (and wgate
+    for SwiGLU, absent for the GELU FFN), f32 attn_gamma, ffn_gamma."""
+
+    def __init__(self, weights: dict, hidden: int, n_heads: int, n_kv_heads: int, head_dim: int, inter: int,
+                 eps: float, rope_theta: float, rope_mode: int):
+        from ._lib import LayerWeightsQ40Struct
+        self.t = weights
+        self.hidden, self.n_heads, self.n_kv_heads, self.head_dim, self.inter = hidden, n_heads, n_kv_heads, head_dim, inter
+
+        def p(k):
+            t = weights.get(k)
+            return None if t is None else t.data_ptr()
+
+        self.struct = LayerWeightsQ40Struct(
+            *[p(k) for k in ("wqkv", "wo", "wgate", "wup", "wdown", "attn_gamma", "ffn_gamma")],
+            hidden, n_heads, n_kv_heads, head_dim, inter, eps, rope_theta, rope_mode)
+
+
+def decode_layer_q4_0(x, layer: DeviceLayerQ40, kv: "DeviceKV", position=0, positions=None, out=None, ws=None,
+                      stream=None):
+    import ctypes as C
+    import torch
+    m = 1 if x.dim() == 1 else x.shape[0]
+    if out is None:
+        out = torch.empty((m, layer.hidden), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(load().rz_decode_layer_q4_0_workspace_bytes(C.byref(layer.struct), m, kv.max_seq), x.device)
+    call("rz_decode_layer_q4_0", _ptr(x), C.byref(layer.struct), C.byref(kv.struct), _ptr(positions), position, m,
+         _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+    return out

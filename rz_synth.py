@@ -228,3 +228,51 @@ def kv_prefill_device(shape: LayerShape, tag: str, max_seq: int, filled: int, m:
         v[:, :filled] = torch.randn((m, filled, shape.kv_dim), device=device,
                                     generator=torch_gen(f"{tag}.v", device, seed))
     return k, v
+
+
+# ----------------------------------------------------------------------------- Q4_0 whole-model layer
+@dataclass(frozen=True)
+class Q40Shape:
+    """A layer whose projections are all Q4_0 (f32 activations): fused QKV, O,
+    gate (SwiGLU) or none (GELU FFN), up, down."""
+    hidden: int
+    inter: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    rope_theta: float
+    rope_mode: int
+    gated: bool
+    eps: float = 1e-6
+
+    @property
+    def q_dim(self) -> int:
+        return self.n_heads * self.head_dim
+
+    @property
+    def kv_dim(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+    def weight_shapes(self):
+        s = {"wqkv": (self.q_dim + 2 * self.kv_dim, self.hidden), "wo": (self.hidden, self.q_dim),
+             "wup": (self.inter, self.hidden), "wdown": (self.hidden, self.inter)}
+        if self.gated:
+            s["wgate"] = (self.inter, self.hidden)
+        return s
+
+
+# a phi-2-sized GELU layer (hidden 2560, intermediate 10240; 40 heads of 64, the
+# attention kernels taking head dimensions that are multiples of 32) and a
+# TinyLlama-sized SwiGLU layer with grouped KV heads
+Q40_GELU = Q40Shape(hidden=2560, inter=10240, n_heads=40, n_kv_heads=40, head_dim=64,
+                    rope_theta=1e4, rope_mode=1, gated=False)
+Q40_SWIGLU = Q40Shape(hidden=2048, inter=5632, n_heads=32, n_kv_heads=4, head_dim=64,
+                      rope_theta=1e4, rope_mode=0, gated=True)
+
+
+def layer_q4_0(shape: Q40Shape, tag: str, seed: int = SEED) -> dict:
+    """Random Q4_0 layer: matrices as q4_0_weight, gammas ~ U[0.5, 1.5]."""
+    out = {nm: q4_0_weight(f"{tag}.{nm}", o, i, seed) for nm, (o, i) in shape.weight_shapes().items()}
+    out["attn_gamma"] = uniform(f"{tag}.attn_gamma", shape.hidden, 0.5, 1.5, seed)
+    out["ffn_gamma"] = uniform(f"{tag}.ffn_gamma", shape.hidden, 0.5, 1.5, seed)
+    return out

@@ -236,3 +236,27 @@ def test_q4k_gemv_integer_inputs_exact(rz, m):
     y = rz.q4k_q8_gemv(to_dev(w), to_dev(x8), m, out_dim, in_dim).cpu().numpy()
     check_no_device_error()
     assert np.array_equal(y, expect.astype(np.float32))
+
+
+# ----------------------------------------------------------------------------- Q4_K x f32
+@pytest.mark.parametrize("out_dim,in_dim,m", [(256, 1024, 1), (7, 256, 1), (129, 768, 2), (1000, 4096, 1),
+                                              (33, 4096, 3), (77, 11008, 5), (19, 14336, 1), (300, 2048, 16)])
+def test_q4k_f32_gemv_parity(rz, out_dim, in_dim, m):
+    w = S.q4k_weight(f"gf32.{out_dim}.{in_dim}", out_dim, in_dim)
+    x = S.normal(f"gf32.x.{in_dim}.{m}", (m, in_dim))
+    y = rz.q4k_f32_gemv(to_dev(w), to_dev(x), out_dim, in_dim).cpu().numpy()
+    check_no_device_error()
+    y_ref = oracle.q4k_f32_gemv(w, x, out_dim, in_dim)
+    assert_gemv_close(y, y_ref, row_norms_q4k(w)[None, :], f"q4k x f32 {out_dim}x{in_dim} m={m}")
+
+
+@pytest.mark.parametrize("out_dim,in_dim", S.LLAMA_SWEEP)
+def test_q4k_f32_gemv_full_size(rz, out_dim, in_dim):
+    """The Llama sweep at one token, every row, with a bias."""
+    w = S.q4k_weight(f"sweep.{out_dim}.{in_dim}", out_dim, in_dim)
+    x = S.normal(f"sweepf.x.{in_dim}", (1, in_dim))
+    b = S.normal(f"sweepf.b.{out_dim}", out_dim)
+    y = rz.q4k_f32_gemv(to_dev(w), to_dev(x), out_dim, in_dim, bias=to_dev(b)).cpu().numpy()
+    check_no_device_error()
+    y_ref = oracle.residual_add(oracle.q4k_f32_gemv(w, x, out_dim, in_dim)[0], b)[None, :]
+    assert_gemv_close(y, y_ref, row_norms_q4k(w)[None, :], f"q4k x f32 {out_dim}x{in_dim} + bias")

@@ -495,3 +495,126 @@ def test_bias_on_zero_projections_is_the_bias(orc):
     expect = orc.swiglu_ffn(r1, L.ffn_gamma, L.w["wgate"], L.w["wup"], L.w["wdown"],
                             sh.hidden, sh.hidden_pad, sh.inter, sh.eps)
     assert np.array_equal(out, expect)
+
+
+# ----------------------------------------------------------------------------- Q4_K x f32
+def test_q4k_f32_gemv_exact_integers(orc):
+    """d = 1, dmin = 0, integer activations: y = sum_j sc_j sum_k q_k x_k exactly."""
+    g = np.random.default_rng(7)
+    nsb, rows = 2, 5
+    w = np.zeros((rows, nsb * 144), np.uint8)
+    expect = np.zeros(rows, np.int64)
+    x = g.integers(-50, 51, 256 * nsb).astype(np.float32)
+    for r in range(rows):
+        for b in range(nsb):
+            sc = g.integers(0, 64, 8).astype(np.uint8)
+            q = g.integers(0, 16, 256).astype(np.uint8)
+            w[r, b * 144:(b + 1) * 144] = orc.q4k_pack(0x3C00, 0, sc, np.zeros(8, np.uint8), q)
+            xi = x[b * 256:(b + 1) * 256].astype(np.int64).reshape(8, 32)
+            expect[r] += int((sc.astype(np.int64) * (q.astype(np.int64).reshape(8, 32) * xi).sum(1)).sum())
+    y = orc.q4k_f32_gemv(w, x, rows, 256 * nsb)[0]
+    assert np.array_equal(y, expect.astype(np.float32))
+
+
+def test_q4k_f32_gemv_min_term_alone(orc):
+    """All codes zero: every weight is -dmin m_j, so y = -sum_b dmin_b sum_j m_j (sum of
+    sub-block j of x), the min term and nothing else."""
+    g = np.random.default_rng(8)
+    rows, nsb = 4, 3
+    w = np.zeros((rows, nsb * 144), np.uint8)
+    x = g.standard_normal(256 * nsb).astype(np.float32)
+    expect = np.zeros(rows)
+    for r in range(rows):
+        for b in range(nsb):
+            mn = g.integers(0, 64, 8).astype(np.uint8)
+            dmin = np.float16(g.uniform(1e-3, 1e-2))
+            w[r, b * 144:(b + 1) * 144] = orc.q4k_pack(0x3C00, dmin.view(np.uint16), g.integers(0, 64, 8),
+                                                     mn, np.zeros(256, np.uint8))
+            xs = x[b * 256:(b + 1) * 256].astype(np.float64).reshape(8, 32).sum(1)
+            expect[r] -= float(dmin) * (mn.astype(np.float64) * xs).sum()
+    y = orc.q4k_f32_gemv(w, x, rows, 256 * nsb)[0]
+    assert np.allclose(y, expect, rtol=1e-6, atol=1e-9)
+
+
+def test_q4k_f32_gemv_close_to_q8_1_path(orc):
+    """The Q8_1 path differs only by the activation rounding: |y_f32 - y_q8| <=
+    sum_k |w_k| d8_k / 2 (each code is within half a step of x / d8), per row."""
+    rows, in_dim = 64, 1024
+    w = S.q4k_weight("pin.f32vq8", rows, in_dim)
+    x = S.normal("pin.f32vq8.x", (1, in_dim))
+    x8 = orc.q8_1_quantize(x)
+    yf = orc.q4k_f32_gemv(w, x, rows, in_dim)[0].astype(np.float64)
+    yq = orc.q4k_q8_gemv(w, x8, 1, rows, in_dim)[0].astype(np.float64)
+    d8, _, _ = orc.q8_1_fields(x8, 1, in_dim)
+    wd = orc.q4k_dequantize(w)
+    bound = (np.abs(wd) * np.repeat(d8[0], 32)[None, :] / 2).sum(1) + 1e-5 * np.abs(yf)
+    assert (np.abs(yf - yq) <= bound).all()
+    assert np.abs(yf - yq).max() > 0   # the two paths are not the same computation
+
+
+# ----------------------------------------------------------------------------- Q4_0 whole-model layer
+def test_gelu_identities(orc):
+    """GELU (tanh form): gelu(0) = 0; the odd part is x/2, so gelu(x) - gelu(-x) = x;
+    gelu(x) -> x for large x and -> 0 for large negative x."""
+    assert orc.gelu(0.0) == 0.0
+    for x in (0.1, 0.5, 1.0, 2.5, 7.0):
+        assert abs(orc.gelu(x) - orc.gelu(-x) - x) < 1e-14 * max(1.0, x)
+    assert abs(orc.gelu(12.0) - 12.0) < 1e-12 and abs(orc.gelu(-12.0)) < 1e-12
+    # between x * sigmoid(1.5 x) - 0.02 and x (a crude bracket that a wrong constant breaks)
+    for x in (0.3, 1.0, 2.0):
+        assert x / (1 + np.exp(-1.5 * x)) - 0.03 < orc.gelu(x) < x
+
+
+def _q40_tiny(gated):
+    return S.Q40Shape(hidden=256, inter=384, n_heads=4, n_kv_heads=2, head_dim=64, rope_theta=1e4,
+                      rope_mode=0, gated=gated)
+
+
+def _orc_q40(orc, sh, w):
+    return orc.LayerWeightsQ40(wqkv=w["wqkv"], wo=w["wo"], wgate=w.get("wgate"), wup=w["wup"], wdown=w["wdown"],
+                               attn_gamma=w["attn_gamma"], ffn_gamma=w["ffn_gamma"], hidden=sh.hidden,
+                               n_heads=sh.n_heads, n_kv_heads=sh.n_kv_heads, head_dim=sh.head_dim,
+                               inter=sh.inter, eps=sh.eps, rope_theta=sh.rope_theta, rope_mode=sh.rope_mode)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_q4_0_layer_zero_weights_is_identity(orc, gated):
+    sh = _q40_tiny(gated)
+    w = S.layer_q4_0(sh, f"pin.q40z.{gated}")
+    for k in sh.weight_shapes():
+        w[k] = np.zeros_like(w[k])
+    x = S.normal(f"pin.q40z.x.{gated}", sh.hidden)
+    kc = S.normal("pin.q40z.k", (8, sh.kv_dim))
+    vc = S.normal("pin.q40z.v", (8, sh.kv_dim))
+    out = orc.decode_layer_q4_0(x, _orc_q40(orc, sh, w), kc, vc, 5)
+    assert np.array_equal(out, x)
+    assert not kc[5].any() and not vc[5].any()
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_q4_0_layer_first_token_composition(orc, gated):
+    """Position 0: the layer is x + O(v expanded) followed by the FFN of the page:
+    silu(gate) * up then down (ffn_swiglu_gpu) or GELU(up) then down
+    (ffn_standard_gpu), every step an f32 buffer."""
+    sh = _q40_tiny(gated)
+    w = S.layer_q4_0(sh, f"pin.q40f.{gated}")
+    x = S.normal(f"pin.q40f.x.{gated}", sh.hidden)
+    kc = np.zeros((4, sh.kv_dim), np.float32)
+    vc = np.zeros_like(kc)
+    out = orc.decode_layer_q4_0(x, _orc_q40(orc, sh, w), kc, vc, 0)
+    n = orc.rmsnorm(x, w["attn_gamma"], sh.hidden, sh.hidden, sh.eps)[0]
+    qkv = orc.q4_0_gemv(w["wqkv"], n, sh.q_dim + 2 * sh.kv_dim, sh.hidden)[0]
+    v = qkv[sh.q_dim + sh.kv_dim:]
+    att = np.concatenate([v[(h // (sh.n_heads // sh.n_kv_heads)) * sh.head_dim:][:sh.head_dim]
+                          for h in range(sh.n_heads)])
+    r1 = orc.residual_add(x, orc.q4_0_gemv(w["wo"], att, sh.hidden, sh.q_dim)[0])
+    n2 = orc.rmsnorm(r1, w["ffn_gamma"], sh.hidden, sh.hidden, sh.eps)[0]
+    u = orc.q4_0_gemv(w["wup"], n2, sh.inter, sh.hidden)[0].astype(np.float64)
+    if gated:
+        g = orc.q4_0_gemv(w["wgate"], n2, sh.inter, sh.hidden)[0].astype(np.float64)
+        h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+    else:
+        h = np.array([orc.gelu(t) for t in u], np.float32)
+    expect = orc.residual_add(r1, orc.q4_0_gemv(w["wdown"], h, sh.hidden, sh.inter)[0])
+    assert np.allclose(out, expect, rtol=0, atol=1e-6 * np.abs(expect).max())
+    assert np.array_equal(vc[0], v)
