@@ -106,8 +106,8 @@ def test_decode_layer_qwen2_with_qkv_bias(rz, fused):
     # the cache rows carry the biased projections (v + bv, rope(k + bk))
     kn, vn = kc[0].copy(), vc[0].copy()
     oracle.decode_layer(x[0], orc_layer(L), kn, vn, pos)
-    assert_rel(kv.v.cpu().numpy()[0, pos], vr[pos], tol=1e-4, what="v row")
-    assert_rel(kv.k.cpu().numpy()[0, pos], kr[pos], tol=1e-4, what="k row")
+    assert_rel(kv.v.cpu().numpy()[0, pos], vr[pos], what="v row")
+    assert_rel(kv.k.cpu().numpy()[0, pos], kr[pos], what="k row")
     assert np.abs(vr[pos] - vn[pos] - bv).max() <= 1e-3 * np.abs(bv).max()
 
 
