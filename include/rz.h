@@ -126,6 +126,27 @@ rz_status rz_q4k_q8_gemv_ex(const void *w, const void *q8, const float *bias, co
                             int64_t ld, int64_t m, int64_t out_dim, int64_t in_dim, rz_stream stream);
 
 /*
+ * rz_q4k_q8_gemm -- the same product for many tokens at once (a prompt's prefill:
+ * GpuModelQ4::forward of realizar 0.8.4 src/gpu/adapters/using.rs takes a sequence
+ * of token ids), on the tensor cores (tcgen05.mma):
+ *     y[t][r] = sum_b d_b * sum_j sc_bj * d8_tbj * I_tbrj - dmin_b * sum_j m_bj * s_tbj
+ *   for every token t < m, with the integer sub-block dots I exact, as
+ *   rz_q4k_q8_gemv.  Each 128 x 128 tile of (tokens, rows) reads its weights once.
+ *   w          Q4_K [out_dim][in_dim]         q8  Q8_1 of m rows of in_dim
+ *   y          f32 [m][ldy] (ldy 0 = out_dim; ldy >= out_dim), 4-byte aligned
+ *   workspace  device scratch of at least rz_q4k_q8_gemm_workspace_bytes(m, in_dim)
+ *              bytes, 16-byte aligned (the activations re-laid out as tensor-core
+ *              operands); contents need no initialisation and are not kept.
+ *   1 <= m (any; tokens beyond a multiple of 128 are padding inside the kernel),
+ *   in_dim % 256 == 0, out_dim >= 1.  Two launches.  f32 combination order
+ *   differs from rz_q4k_q8_gemv's (deterministic run to run).  A bounded wait that
+ *   runs out records RZ_ERR_TIMEOUT for rz_check_device_error.
+ */
+size_t rz_q4k_q8_gemm_workspace_bytes(int64_t m, int64_t in_dim);
+rz_status rz_q4k_q8_gemm(const void *w, const void *q8, float *y, int64_t ldy, int64_t m, int64_t out_dim,
+                         int64_t in_dim, void *workspace, size_t ws_bytes, rz_stream stream);
+
+/*
  * rz_rmsnorm_q4k_gemv -- steps 1-3 of transformer_layer_gpu_true_dp4a in one
  * launch: RMSNorm of x over its first n values with gamma (zero padding after n),
  * Q8_1 quantisation of the normed row (bit-identical to rz_rmsnorm's q8 output),

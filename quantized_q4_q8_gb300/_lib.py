@@ -72,6 +72,8 @@ SIGNATURES = {
     "rz_q4k_q8_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
     "rz_q4k_q8_subblock_dots": [_vp, _vp, _vp, _i64, _i64, _vp],
     "rz_q4k_q8_gemv_ex": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp],
+    "rz_q4k_q8_gemm_workspace_bytes": [_i64, _i64],
+    "rz_q4k_q8_gemm": [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp],
     "rz_rmsnorm_q4k_gemv": [_vp, _i64, _vp, _i64, _f32, _i32, C.POINTER(_vp), C.POINTER(_i64),
                             C.POINTER(_vp), _vp, _i64, _i64, _i64, _vp],
     "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
@@ -103,7 +105,7 @@ SIGNATURES = {
 _RESTYPES = {"rz_last_error": C.c_char_p, "rz_version": C.c_char_p,
              "rz_swiglu_ffn_workspace_bytes": _sz, "rz_attention_workspace_bytes": _sz,
              "rz_decode_layer_workspace_bytes": _sz, "rz_decode_stack_workspace_bytes": _sz,
-             "rz_decode_layer_q4_0_workspace_bytes": _sz,
+             "rz_decode_layer_q4_0_workspace_bytes": _sz, "rz_q4k_q8_gemm_workspace_bytes": _sz,
              "rz_decode_stack_launches": C.c_int32}
 
 _lib = None

@@ -203,6 +203,39 @@ rz_status rz_q4k_q8_gemv_ex(const void *w, const void *q8, const float *bias, co
     return RZ_OK;
 }
 
+size_t rz_q4k_q8_gemm_workspace_bytes(int64_t m, int64_t in_dim)
+{
+    if (m < 1 || in_dim < 256 || in_dim % 256) return 0;
+    return (size_t)q4k_gemm_tc_workspace_bytes(m, in_dim);
+}
+
+rz_status rz_q4k_q8_gemm(const void *w, const void *q8, float *y, int64_t ldy, int64_t m, int64_t out_dim,
+                         int64_t in_dim, void *workspace, size_t ws_bytes, rz_stream stream)
+{
+    const char *fn = "rz_q4k_q8_gemm";
+    t_last_error.clear();
+    if (!w || !q8 || !y || !workspace) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (m < 1 || out_dim < 1 || in_dim < 1)
+        return fail(RZ_ERR_INVALID_ARG, "%s: m=%lld out_dim=%lld in_dim=%lld", fn, (long long)m, (long long)out_dim,
+                    (long long)in_dim);
+    if (in_dim % 256) return fail(RZ_ERR_SHAPE, "%s: in_dim=%lld is not a multiple of 256", fn, (long long)in_dim);
+    if (ldy == 0) ldy = out_dim;
+    if (ldy < out_dim) return fail(RZ_ERR_SHAPE, "%s: ldy=%lld < out_dim", fn, (long long)ldy);
+    // grid limits: 128-token tiles in the second grid dimension; int32 indexing
+    if (m > 65535LL * 128 || out_dim > (1LL << 30) || in_dim > (1LL << 24) || m * in_dim > (1LL << 40))
+        return fail(RZ_ERR_SHAPE, "%s: m=%lld out_dim=%lld in_dim=%lld beyond the supported range", fn, (long long)m,
+                    (long long)out_dim, (long long)in_dim);
+    if (!aligned16(w) || !aligned16(q8) || !aligned16(workspace))
+        return fail(RZ_ERR_ALIGN, "%s: w, q8 and the workspace must be 16-byte aligned", fn);
+    if (reinterpret_cast<uintptr_t>(y) & 3u) return fail(RZ_ERR_ALIGN, "%s: y must be 4-byte aligned", fn);
+    const size_t need = (size_t)q4k_gemm_tc_workspace_bytes(m, in_dim);
+    if (ws_bytes < need) return fail(RZ_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+    RZ_TRY(check_device());
+    RZ_CUDA(launch_q4k_gemm_tc(w, q8, y, ldy, m, out_dim, in_dim, workspace, static_cast<cudaStream_t>(stream)),
+            "rz_q4k_q8_gemm launch");
+    return RZ_OK;
+}
+
 rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, int64_t n, float eps, int32_t n_mats,
                               const void *const *w, const int64_t *rows, const float *const *bias, float *y,
                               int64_t ldy, int64_t m, int64_t in_dim, rz_stream stream)

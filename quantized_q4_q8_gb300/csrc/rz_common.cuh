@@ -19,6 +19,7 @@ enum DevErr : unsigned {
     DEV_TIMEOUT_GEMV = 0x101,   // bulk-copy wait in a GEMV gave up
     DEV_TIMEOUT_Q40 = 0x102,
     DEV_TIMEOUT_ATTN = 0x104,   // the V-row copy wait of the attention kernel gave up
+    DEV_TIMEOUT_GEMM = 0x108,   // a wait of the tensor-core many-token GEMM gave up
     DEV_TIMEOUT_DRAIN = 0x1ff,  // draining outstanding copies gave up
     DEV_BAD_POSITION = 0x201,   // a device-resident position outside [0, max_seq)
 };

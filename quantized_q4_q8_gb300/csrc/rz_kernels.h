@@ -43,6 +43,15 @@ extern bool g_use_pdl;
 // ---------------------------------------------------------------- Q8_1
 cudaError_t launch_q8_1_quantize(const float *x, void *q8, int64_t m, int64_t n, cudaStream_t s);
 
+// ---------------------------------------------------------------- many-token Q4_K x Q8_1 (tensor cores)
+// y[t][r] for m tokens (any m >= 1) with tcgen05.mma: a packing kernel turns the
+// Q8_1 activations into tensor-core operands in `workspace`
+// (q4k_gemm_tc_workspace_bytes), then one CTA per 128 tokens x 128 rows.
+int64_t q4k_gemm_tc_workspace_bytes(int64_t m, int64_t in_dim);
+int q4k_gemm_tc_launch_count();
+cudaError_t launch_q4k_gemm_tc(const void *w, const void *q8, float *y, int64_t ldy, int64_t m, int64_t out_dim,
+                               int64_t in_dim, void *workspace, cudaStream_t s);
+
 // ---------------------------------------------------------------- norms / elementwise
 cudaError_t launch_rmsnorm(const float *x, const float *gamma, float *y, void *q8, int64_t m,
                            int64_t n, int64_t n_pad, float eps, cudaStream_t s);

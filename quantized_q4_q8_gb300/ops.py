@@ -10,6 +10,7 @@ __all__ = [
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
     "rz_q4k_q8_gemv_ex", "rz_rmsnorm_q4k_gemv", "q4k_q8_gemv_ex", "rmsnorm_q4k_gemv",
     "rz_q4k_f32_gemv", "q4k_f32_gemv",
+    "rz_q4k_q8_gemm", "q4k_q8_gemm_workspace_bytes", "q4k_q8_gemm",
     "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_debug_stall_next_gemv",
     "q8_1_quantize", "q4k_q8_gemv", "q4k_q8_subblock_dots", "q4_0_gemv",
     "rmsnorm", "residual_add", "check_device_error", "set_pdl", "version",
@@ -152,6 +153,29 @@ def q4k_q8_gemv(w, q8, m, out_dim, in_dim, out=None, stream=None):
     if out is None:
         out = torch.empty((m, out_dim), dtype=torch.float32, device=w.device)
     rz_q4k_q8_gemv(w, q8, out, m, out_dim, in_dim, stream)
+    return out
+
+
+def rz_q4k_q8_gemm(w, q8, y, ldy, m, out_dim, in_dim, ws, ws_bytes, stream=None):
+    return call("rz_q4k_q8_gemm", _ptr(w), _ptr(q8), _ptr(y), ldy, m, out_dim, in_dim, _ptr(ws), ws_bytes,
+                _stream(stream))
+
+
+def q4k_q8_gemm_workspace_bytes(m: int, in_dim: int) -> int:
+    return int(load().rz_q4k_q8_gemm_workspace_bytes(m, in_dim))
+
+
+def q4k_q8_gemm(w, q8, m, out_dim, in_dim, out=None, ws=None, stream=None):
+    """y = W x_t for m tokens on the tensor cores (any m >= 1); y f32 [m, out_dim]."""
+    import torch
+    _cuda_contig(w, torch.uint8, "w")
+    _cuda_contig(q8, torch.uint8, "q8")
+    if out is None:
+        out = torch.empty((m, out_dim), dtype=torch.float32, device=w.device)
+    need = q4k_q8_gemm_workspace_bytes(m, in_dim)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=w.device)
+    rz_q4k_q8_gemm(w, q8, out, out.shape[-1], m, out_dim, in_dim, ws, ws.numel(), stream)
     return out
 
 
