@@ -18,11 +18,19 @@
 // pieces (s = s1 + s2 + s3, 8 significant bits each).
 //
 // Tile: 128 tokens (MMA M = tensor-memory lanes) x 128 weight rows (MMA N =
-// columns); K walks the super-blocks, nine regions of K = 32 each.  The 21 warps:
-//   warp 0       allocates tensor memory; lane 0 issues the MMAs
-//   warps 1-4    convert the TMA-staged raw Q4_K tile into the B operand, one
-//                weight row per thread; warp 1 lane 0 also issues every copy
-//   warps 5-20   drain: region -> registers, times d8 (sub-block) and d, dmin
+// columns); K walks the super-blocks, nine regions of K = 32 each (region
+// g = 9 sb + j).  Every synchronising instruction (an mbarrier wait, an MMA
+// issue, a commit) costs a warp on the order of a hundred cycles here while one
+// region is 128 cycles of tensor work, so the work of a region is spread over
+// warps that run side by side, each region's steps on its own warp:
+//   warps 0-2    MMA: warp b issues the regions g = b mod 3 into tensor-memory
+//                buffer b and frees the region's operand slots by a commit
+//                (warp 0 also allocates tensor memory)
+//   warp 3       copies: the bulk copy of every region's activation operand and
+//                the TMA load of every raw Q4_K tile (one per super-block)
+//   warps 4-7    conversion: warp c converts the regions g = c mod 4 (all 128
+//                rows, four in flight per lane) into the B operand
+//   warps 8-23   drain: region -> registers, times d8 (sub-block) and d, dmin
 //                (super-block); the running sums stay in tensor memory
 // Shared-memory operand layout: K-major core matrices of 8 rows x 16 bytes, no
 // swizzle; the two core matrices along K 128 bytes apart, 8-row groups 512 bytes
@@ -30,9 +38,9 @@
 // operands hold elements (0, 2, 1, 3) of the sub-block: the order in which a
 // 32-bit word of packed nibbles unpacks into two f16 pairs; the dot is the same.
 //
-// Every wait is bounded; on a timeout the CTA records DEV_TIMEOUT_GEMM, stops
-// issuing, waits (bounded) for its copies and MMAs in flight, frees its tensor
-// memory and exits.
+// Every wait is bounded; on a timeout the CTA records DEV_TIMEOUT_GEMM, every
+// role stops, the copies and MMAs in flight are waited for (bounded), tensor
+// memory is freed and the CTA exits.
 #include <algorithm>
 
 #include "rz_common.cuh"
@@ -45,29 +53,31 @@ constexpr int kTM = 128;                  // tokens per tile
 constexpr int kTN = 128;                  // weight rows per tile
 constexpr int kRegions = 9;               // per super-block: 8 sub-blocks + the min term
 constexpr int kOpBytes = 8192;            // one 128 x 32 operand of 16-bit values
-constexpr int kStagesA = 8;               // activation operands (bulk copies)
-constexpr int kStagesB = 4;               // weight operands (converted)
-constexpr int kLookA = kStagesA - kStagesB;  // activation copies run this far ahead
+constexpr int kStages = 8;                // operand slots (A and B each), region g in slot g % 8
 constexpr int kStagesW = 3;               // raw Q4_K tiles
 constexpr int kStagesH = 2;               // d, dmin of the tile's rows
-constexpr int kTBufs = 3;                 // region buffers in tensor memory
+constexpr int kTBufs = 3;                 // region buffers in tensor memory = MMA warps
 constexpr int kAccCol = kTBufs * kTN;     // columns 384..511: the running sums
+constexpr int kMmaWarps = kTBufs;
+constexpr int kLoadWarp = kMmaWarps;      // warp 3
+constexpr int kFirstConv = kLoadWarp + 1; // warps 4-7
 constexpr int kConvWarps = 4;
+constexpr int kFirstDrain = kFirstConv + kConvWarps;  // warps 8-23
 constexpr int kDrainWarps = 16;
-constexpr int kFirstDrain = 1 + kConvWarps;
-constexpr int kThreads = 32 * (1 + kConvWarps + kDrainWarps);
+constexpr int kThreads = 32 * (kFirstDrain + kDrainWarps);
 constexpr int kWBytes = 144 * kTN;        // raw Q4_K of one super-block of the tile
 
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStagesA * kOpBytes;
-constexpr int kOffW = kOffB + kStagesB * kOpBytes;
+constexpr int kOffB = kOffA + kStages * kOpBytes;
+constexpr int kOffW = kOffB + kStages * kOpBytes;
 constexpr int kOffH = kOffW + kStagesW * kWBytes;
 constexpr int kOffBar = kOffH + kStagesH * kTN * 8;
-constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 * kStagesW + 2 * kTBufs + 2 * kStagesH + 1;
+constexpr int kNumBars = 3 * kStages + 2 * kStagesW + 2 * kTBufs + 2 * kStagesH + kMmaWarps;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
 static_assert(kOffW % 1024 == 0 && kWBytes % 128 == 0, "TMA destinations 128-byte aligned");
+static_assert(kStages % kConvWarps == 0, "a conversion warp's regions cycle through its own slots");
 
 // instruction descriptors (kind::f16): D f32 (bits 4-5 = 1), A and B K-major,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28; bf16 operands: bits 7-9 and 10-12 = 1
@@ -117,10 +127,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
     "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), \
         "=r"(r[b + 7]), "=r"(r[b + 8]), "=r"(r[b + 9]), "=r"(r[b + 10]), "=r"(r[b + 11]), "=r"(r[b + 12]),          \
         "=r"(r[b + 13]), "=r"(r[b + 14]), "=r"(r[b + 15])
-#define RZ_W16(b)                                                                                                  \
-    "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), "r"(r[b + 4]), "r"(r[b + 5]), "r"(r[b + 6]),       \
-        "r"(r[b + 7]), "r"(r[b + 8]), "r"(r[b + 9]), "r"(r[b + 10]), "r"(r[b + 11]), "r"(r[b + 12]), "r"(r[b + 13]), \
-        "r"(r[b + 14]), "r"(r[b + 15])
 
 // Consecutive columns of this warp's 32 lanes (one value per thread and column),
 // waited for inside the same statement so no use can move above the wait.
@@ -171,40 +177,55 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, float b0, float b1, f
         : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-// Warp-uniform bounded wait: lane 0 polls; every lane gets the verdict.  A
-// timeout, or an abort raised by another role, returns false.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, unsigned par, const GemmArgs &a, volatile int *abort_flag)
+// mbarrier wait that lets the thread sleep until the phase completes (or the
+// 20 us hint runs out), instead of spinning on the barrier
+__device__ __forceinline__ bool try_wait_sleep(uint64_t *bar, unsigned parity)
 {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        ok = 0;
-        for (uint32_t i = 0; i < a.wait_limit; ++i) {
-            if (mbar_try_wait(bar, par)) {
-                ok = 1;
-                break;
-            }
-            if (*abort_flag) break;
-        }
-        if (!ok && !*abort_flag) {
-            *abort_flag = 1;
-            set_error(a.err, DEV_TIMEOUT_GEMM);
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
 }
 
-// Single-thread bounded wait (the issuing lanes).
-__device__ __forceinline__ bool lane_wait(uint64_t *bar, unsigned par, const GemmArgs &a, volatile int *abort_flag)
+// Non-blocking test of a phase: issued early, its result is read later, so its
+// latency overlaps other work.
+__device__ __forceinline__ bool test_wait(uint64_t *bar, unsigned parity)
 {
-    for (uint32_t i = 0; i < a.wait_limit; ++i) {
-        if (mbar_try_wait(bar, par)) return true;
-        if (*abort_flag) return false;
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Warp-wide bounded wait: every lane waits, the verdict is made uniform.  A
+// timeout, or an abort raised by another role, returns false.  Each try lasts
+// at most the 20 us hint, so the bound is a 64th of the poll limit in tries.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, unsigned par, const GemmArgs &a, volatile int *abort_flag)
+{
+    bool ok = false;
+    for (uint32_t i = 0; i < (a.wait_limit >> 6); ++i) {
+        if (try_wait_sleep(bar, par)) {
+            ok = true;
+            break;
+        }
+        if (*abort_flag) break;
     }
-    if (!*abort_flag) {
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0 && !*abort_flag) {
         *abort_flag = 1;
         set_error(a.err, DEV_TIMEOUT_GEMM);
     }
-    return false;
+    return ok;
 }
 
 // byte offset of row `row`, 16-byte chunk `kk` (K slots 8 kk .. 8 kk + 7) of an operand
@@ -212,17 +233,31 @@ __device__ __forceinline__ int op_offset(int row, int kk) { return (row >> 3) * 
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
+// 6-bit scale / min of sub-block j from header bytes 4-15 (s0-3 in y, s4-7 in z,
+// s8-11 in w)
+__device__ __forceinline__ int q4k_scale(const uint4 &h, int j)
+{
+    const int k = j & 3;
+    const int b0 = (int)((h.y >> (8 * k)) & 0xFFu), b8 = (int)((h.w >> (8 * k)) & 0xFFu);
+    return j < 4 ? (b0 & 63) : ((b8 & 15) | ((b0 >> 6) << 4));
+}
+__device__ __forceinline__ int q4k_min(const uint4 &h, int j)
+{
+    const int k = j & 3;
+    const int b4 = (int)((h.z >> (8 * k)) & 0xFFu), b8 = (int)((h.w >> (8 * k)) & 0xFFu);
+    return j < 4 ? (b4 & 63) : ((b8 >> 4) | ((b4 >> 6) << 4));
+}
+
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_constant__ GemmArgs a)
 {
     extern __shared__ uint8_t gsm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-    uint64_t *full_a = bars, *empty_a = full_a + kStagesA;
-    uint64_t *full_b = empty_a + kStagesA, *empty_b = full_b + kStagesB;
-    uint64_t *full_w = empty_b + kStagesB, *empty_w = full_w + kStagesW;
+    uint64_t *full_a = bars, *full_b = full_a + kStages, *empty_ab = full_b + kStages;
+    uint64_t *full_w = empty_ab + kStages, *empty_w = full_w + kStagesW;
     uint64_t *full_t = empty_w + kStagesW, *empty_t = full_t + kTBufs;
     uint64_t *full_h = empty_t + kTBufs, *empty_h = full_h + kStagesH;
-    uint64_t *done_bar = empty_h + kStagesH;
+    uint64_t *done_bar = empty_h + kStagesH;  // one per MMA warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
     float *hdr = reinterpret_cast<float *>(sm + kOffH);
@@ -232,27 +267,24 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
     const int nsb = a.nsb, G = nsb * kRegions;
 
     if (tid == 0) {
-        for (int i = 0; i < kStagesA; ++i) {
-            mbar_init(&full_a[i], 1);
-            mbar_init(&empty_a[i], 1);
-        }
-        for (int i = 0; i < kStagesB; ++i) {
-            mbar_init(&full_b[i], kConvWarps);
-            mbar_init(&empty_b[i], 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full_a[i], 1);    // the bulk copy's arrive.expect_tx
+            mbar_init(&full_b[i], 1);    // the converting warp
+            mbar_init(&empty_ab[i], 1);  // the commit after the region's MMAs
         }
         for (int i = 0; i < kStagesW; ++i) {
             mbar_init(&full_w[i], 1);
-            mbar_init(&empty_w[i], kConvWarps);
+            mbar_init(&empty_w[i], kRegions);  // one arrival per region converted from it
         }
         for (int i = 0; i < kTBufs; ++i) {
             mbar_init(&full_t[i], 1);
             mbar_init(&empty_t[i], kDrainWarps);
         }
         for (int i = 0; i < kStagesH; ++i) {
-            mbar_init(&full_h[i], kConvWarps);
+            mbar_init(&full_h[i], 1);
             mbar_init(&empty_h[i], kDrainWarps);
         }
-        mbar_init(done_bar, 1);
+        for (int i = 0; i < kMmaWarps; ++i) mbar_init(&done_bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&a.wmap);
@@ -267,118 +299,116 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp < kMmaWarps) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            RingPos pa{0, 0}, pb{0, 0}, pt{0, 0};
-            int j = 0;
-            for (int g = 0; g < G; ++g) {
-                if (!lane_wait(&full_a[pa.s], pa.par, a, abort_flag)) break;
-                if (!lane_wait(&full_b[pb.s], pb.par, a, abort_flag)) break;
-                if (!lane_wait(&empty_t[pt.s], pt.par ^ 1u, a, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t sa = smem_u32(sm + kOffA + pa.s * kOpBytes);
-                const uint32_t sb_ = smem_u32(sm + kOffB + pb.s * kOpBytes);
-                const uint32_t idesc = (j == 8) ? kIdescBF16 : kIdescF16;
-                const uint32_t d = tmem + (uint32_t)(pt.s * kTN);
+        const int b = warp;
+        const uint32_t d = tmem + (uint32_t)(b * kTN);
+        int issued = 0;
+        for (int g = b; g < G; g += kTBufs) {
+            const RingPos ps = ring_pos(g, kStages);
+            const RingPos pt = ring_pos(g / kTBufs, 1);  // parity of this buffer's use
+            // the three phases tested together (one latency); only a phase not yet
+            // complete is waited for
+            const bool ra = test_wait(&full_a[ps.s], ps.par);
+            const bool rb = test_wait(&full_b[ps.s], ps.par);
+            const bool rt = test_wait(&empty_t[b], pt.par ^ 1u);
+            if (!__all_sync(0xffffffffu, ra && rb && rt)) {
+                if (!warp_wait(&full_a[ps.s], ps.par, a, abort_flag)) break;
+                if (!warp_wait(&full_b[ps.s], ps.par, a, abort_flag)) break;
+                if (!warp_wait(&empty_t[b], pt.par ^ 1u, a, abort_flag)) break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sa = smem_u32(sm + kOffA + ps.s * kOpBytes);
+                const uint32_t sb_ = smem_u32(sm + kOffB + ps.s * kOpBytes);
+                const uint32_t idesc = (g % kRegions == 8) ? kIdescBF16 : kIdescF16;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)  // K = 16 each: core matrices 2h, 2h + 1 along K
                     mma_issue(d, kmajor_desc(sa + 256u * h), kmajor_desc(sb_ + 256u * h), idesc, (uint32_t)h);
-                mma_commit(&empty_a[pa.s]);
-                mma_commit(&empty_b[pb.s]);
-                mma_commit(&full_t[pt.s]);
-                ring_next(pa, kStagesA);
-                ring_next(pb, kStagesB);
-                ring_next(pt, kTBufs);
-                if (++j == kRegions) j = 0;
+                mma_commit(&empty_ab[ps.s]);
+                mma_commit(&full_t[b]);
             }
-            // every MMA issued so far has completed once this arrives
-            mma_commit(done_bar);
-            mbar_wait(done_bar, 0, a.wait_limit);
+            __syncwarp();
+            ++issued;
+        }
+        // every MMA this warp issued has completed once this arrives
+        if (lane == 0) {
+            mma_commit(&done_bar[b]);
+            mbar_wait(&done_bar[b], 0, a.wait_limit);
         }
         __syncwarp();
-    } else if (warp < kFirstDrain) {
-        // ------------------------------------------------------------ conversion (+ copies)
-        const int cw = warp - 1;
-        const int row = cw * 32 + lane;
-        const bool issuer = (cw == 0 && lane == 0);
+    } else if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ copies
         const uint64_t pol = l2_evict_first_policy();
         const uint8_t *pack_tile = a.pack + (int64_t)tile_t * G * kOpBytes;
-        // issue bookkeeping (the issuing lane only)
-        int a_issued = 0;            // activation operands issued so far
-        int w_issued = 0;            // raw weight tiles issued so far
-        auto issue_a = [&](int g) {  // region g into its slot; waits for the slot to be free
-            const RingPos p = ring_pos(g, kStagesA);
-            if (!lane_wait(&empty_a[p.s], p.par ^ 1u, a, abort_flag)) return false;
-            mbar_arrive_expect_tx(&full_a[p.s], kOpBytes);
-            bulk_g2s(sm + kOffA + p.s * kOpBytes, pack_tile + (int64_t)g * kOpBytes, kOpBytes, &full_a[p.s]);
-            ++a_issued;
-            return true;
-        };
-        auto issue_w = [&](int sbk) {
+        int w_issued = 0, a_issued = 0;
+        auto issue_w = [&](int sbk) {  // raw tile sbk into slot sbk % 3 once its regions are converted
             const RingPos p = ring_pos(sbk, kStagesW);
-            if (!lane_wait(&empty_w[p.s], p.par ^ 1u, a, abort_flag)) return false;
-            mbar_arrive_expect_tx(&full_w[p.s], kWBytes);
-            tma_load_2d(sm + kOffW + p.s * kWBytes, &a.wmap, sbk * 144, r0, &full_w[p.s], pol);
+            if (!warp_wait(&empty_w[p.s], p.par ^ 1u, a, abort_flag)) return false;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full_w[p.s], kWBytes);
+                tma_load_2d(sm + kOffW + p.s * kWBytes, &a.wmap, sbk * 144, r0, &full_w[p.s], pol);
+            }
+            __syncwarp();
             ++w_issued;
             return true;
         };
         bool ok = true;
-        if (issuer) {
-            for (int k = 0; k < min(kStagesW, nsb) && ok; ++k) ok = issue_w(k);
-            for (int g = 0; g < min(kLookA, G) && ok; ++g) ok = issue_a(g);
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        RingPos pw{0, 0}, ph{0, 0}, pb{0, 0};
-        int g = 0;
-        for (int sbk = 0; sbk < nsb && ok; ++sbk) {
-            if (!warp_wait(&full_w[pw.s], pw.par, a, abort_flag)) break;
-            const uint8_t *raw = sm + kOffW + pw.s * kWBytes + row * 144;
-            const uint4 h0 = *reinterpret_cast<const uint4 *>(raw);
-            const float dsb = h2f((uint16_t)(h0.x & 0xffffu)), dminsb = h2f((uint16_t)(h0.x >> 16));
-            // 6-bit scales and mins: bytes 4-15 of the header (s0-3 in .y, s4-7 in .z,
-            // s8-11 in .w), decoded where they are used
-            auto scale_of = [&](int jj) {
-                const int k = jj & 3;
-                const int b0 = (int)((h0.y >> (8 * k)) & 0xFFu), b8 = (int)((h0.w >> (8 * k)) & 0xFFu);
-                return jj < 4 ? (b0 & 63) : ((b8 & 15) | ((b0 >> 6) << 4));
-            };
-            auto min_of = [&](int jj) {
-                const int k = jj & 3;
-                const int b0 = (int)((h0.y >> (8 * k)) & 0xFFu), b4 = (int)((h0.z >> (8 * k)) & 0xFFu);
-                const int b8 = (int)((h0.w >> (8 * k)) & 0xFFu);
-                return jj < 4 ? (b4 & 63) : ((b8 >> 4) | ((b4 >> 6) << 4));
-            };
-            // d and dmin of this row for the drain
-            if (!warp_wait(&empty_h[ph.s], ph.par ^ 1u, a, abort_flag)) break;
-            *reinterpret_cast<float2 *>(hdr + ph.s * kTN * 2 + row * 2) = make_float2(dsb, dminsb);
+        for (int k = 0; k < min(kStagesW - 1, nsb) && ok; ++k) ok = issue_w(k);
+        for (int g = 0; g < G && ok; ++g) {
+            // the raw tile two super-blocks ahead, at the first region of each super-block
+            if (g % kRegions == 0 && w_issued < nsb && !(ok = issue_w(w_issued))) break;
+            const RingPos p = ring_pos(g, kStages);
+            if (!warp_wait(&empty_ab[p.s], p.par ^ 1u, a, abort_flag)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full_a[p.s], kOpBytes);
+                bulk_g2s(sm + kOffA + p.s * kOpBytes, pack_tile + (int64_t)g * kOpBytes, kOpBytes, &full_a[p.s]);
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_h[ph.s]);
-            ring_next(ph, kStagesH);
-
+            ++a_issued;
+        }
+        // copies in flight must land before the CTA exits: the last phase issued
+        // into every slot
+        if (lane == 0) {
+            for (int k = max(0, w_issued - kStagesW); k < w_issued; ++k) {
+                const RingPos p = ring_pos(k, kStagesW);
+                mbar_wait(&full_w[p.s], p.par, a.wait_limit);
+            }
+            for (int k = max(0, a_issued - kStages); k < a_issued; ++k) {
+                const RingPos p = ring_pos(k, kStages);
+                mbar_wait(&full_a[p.s], p.par, a.wait_limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kFirstDrain) {
+        // ------------------------------------------------------------ conversion
+        const int c = warp - kFirstConv;
+        for (int g = c; g < G; g += kConvWarps) {
+            const int sbk = g / kRegions, j = g - kRegions * sbk;
+            const RingPos pw = ring_pos(sbk, kStagesW);
+            const RingPos ps = ring_pos(g, kStages);
+            if (!warp_wait(&full_w[pw.s], pw.par, a, abort_flag)) break;
+            if (!warp_wait(&empty_ab[ps.s], ps.par ^ 1u, a, abort_flag)) break;
+            const uint8_t *wtile = sm + kOffW + pw.s * kWBytes;
+            uint8_t *dst = sm + kOffB + ps.s * kOpBytes;
+            if (j < 8) {
+                // sub-block j: the low (j even) or high (j odd) nibbles of bytes
+                // 32 (j / 2) .. + 31; q * sc exactly as (1024 + q) * sc - 1024 * sc, or
+                // (1024 + 16 q) * (sc / 16) - 64 * sc, one rounding of an exact small
+                // integer
+                const int hi = j & 1;
+                const uint32_t mask = hi ? 0x00F000F0u : 0x000F000Fu;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (!ok) break;
-                // sub-blocks 2c (low nibbles) and 2c + 1 (high nibbles) of bytes 32c .. 32c + 31
-                const uint4 qa = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * c);
-                const uint4 qb = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * c);
-                const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int hi = 0; hi < 2; ++hi) {
-                    if (issuer && g + kLookA < G) ok = issue_a(g + kLookA);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok || !warp_wait(&empty_b[pb.s], pb.par ^ 1u, a, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    // q * sc exactly: (1024 + q) * sc - 1024 * sc (low nibbles), or
-                    // (1024 + 16 q) * (sc / 16) - 64 * sc (high nibbles), one rounding of
-                    // an exact small integer
-                    const int s6 = scale_of(2 * c + hi);
+                for (int rr = 0; rr < kTN / 32; ++rr) {
+                    const int row = 32 * rr + lane;
+                    const uint8_t *raw = wtile + row * 144;
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(raw);
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * (j >> 1));
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * (j >> 1));
+                    const int s6 = q4k_scale(h0, j);
                     const __half2 mul = __float2half2_rn(hi ? (float)s6 * 0.0625f : (float)s6);
                     const __half2 add = __float2half2_rn(hi ? -64.0f * (float)s6 : -1024.0f * (float)s6);
-                    const uint32_t mask = hi ? 0x00F000F0u : 0x000F000Fu;
-                    uint8_t *dst = sm + kOffB + pb.s * kOpBytes;
+                    const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         uint32_t o[4];
@@ -392,59 +422,39 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
                         }
                         *reinterpret_cast<uint4 *>(dst + op_offset(row, kk)) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[pb.s]);
-                    ring_next(pb, kStagesB);
-                    ++g;
                 }
-            }
-            if (!ok) break;
-            // the min-term operand: m_0..7 in K slots 0-7, 8-15 and 16-23 (against the
-            // three bf16 pieces of s), zeros in 24-31
-            {
-                if (issuer && g + kLookA < G) ok = issue_a(g + kLookA);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok || !warp_wait(&empty_b[pb.s], pb.par ^ 1u, a, abort_flag)) {
-                    ok = false;
-                    break;
+            } else {
+                // the min-term operand: m_0..7 in K slots 0-7, 8-15 and 16-23 (against
+                // the three bf16 pieces of s), zeros in 24-31; and d, dmin of every
+                // row for the drain
+                const RingPos ph = ring_pos(sbk, kStagesH);
+                if (!warp_wait(&empty_h[ph.s], ph.par ^ 1u, a, abort_flag)) break;
+#pragma unroll 1
+                for (int rr = 0; rr < kTN / 32; ++rr) {
+                    const int row = 32 * rr + lane;
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(wtile + row * 144);
+                    uint32_t mm[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)  // bf16 of a 6-bit integer: the top half of its f32
+                        mm[i] = (__float_as_uint((float)q4k_min(h0, 2 * i)) >> 16) |
+                                (__float_as_uint((float)q4k_min(h0, 2 * i + 1)) & 0xFFFF0000u);
+#pragma unroll
+                    for (int kk = 0; kk < 3; ++kk)
+                        *reinterpret_cast<uint4 *>(dst + op_offset(row, kk)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
+                    *reinterpret_cast<uint4 *>(dst + op_offset(row, 3)) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<float2 *>(hdr + ph.s * kTN * 2 + row * 2) =
+                        make_float2(h2f((uint16_t)(h0.x & 0xffffu)), h2f((uint16_t)(h0.x >> 16)));
                 }
-                uint32_t mm[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)  // bf16 of a 6-bit integer: the top half of its f32
-                    mm[i] = (__float_as_uint((float)min_of(2 * i)) >> 16) |
-                            (__float_as_uint((float)min_of(2 * i + 1)) & 0xFFFF0000u);
-                uint8_t *dst = sm + kOffB + pb.s * kOpBytes;
-#pragma unroll
-                for (int kk = 0; kk < 3; ++kk)
-                    *reinterpret_cast<uint4 *>(dst + op_offset(row, kk)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
-                *reinterpret_cast<uint4 *>(dst + op_offset(row, 3)) = make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_b[pb.s]);
-                ring_next(pb, kStagesB);
-                ++g;
+                if (lane == 0) mbar_arrive(&full_h[ph.s]);
             }
-            // release the raw tile; the issuer refills it with super-block sbk + kStagesW
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_w[pw.s]);
-            if (issuer && sbk + kStagesW < nsb) ok = issue_w(sbk + kStagesW);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            ring_next(pw, kStagesW);
-        }
-        // copies in flight must land before the CTA exits: wait (bounded) for the
-        // last phase issued into every slot
-        if (issuer) {
-            for (int k = max(0, a_issued - kStagesA); k < a_issued; ++k) {
-                const RingPos p = ring_pos(k, kStagesA);
-                mbar_wait(&full_a[p.s], p.par, a.wait_limit);
-            }
-            for (int k = max(0, w_issued - kStagesW); k < w_issued; ++k) {
-                const RingPos p = ring_pos(k, kStagesW);
-                mbar_wait(&full_w[p.s], p.par, a.wait_limit);
+            if (lane == 0) {
+                mbar_arrive(&full_b[ps.s]);
+                mbar_arrive(&empty_w[pw.s]);
             }
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ drain
         const int q = warp & 3;                      // tensor-memory lanes 32q .. 32q + 31
@@ -459,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc_sb[i] = 0.0f;
         RingPos pt{0, 0}, ph{0, 0};
-        bool ok = true;
+        bool ok = true, ready = false;  // ready: region g known complete
+        int g = 0;
         for (int sbk = 0; sbk < nsb && ok; ++sbk) {
             float4 dn0 = make_float4(0.f, 0.f, 0.f, 0.f), dn1 = dn0;
             if (tok) {
@@ -469,30 +480,35 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
             const float d8[8] = {dn0.x, dn0.y, dn0.z, dn0.w, dn1.x, dn1.y, dn1.z, dn1.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                if (!warp_wait(&full_t[pt.s], pt.par, a, abort_flag)) {
+                if (!ready && !warp_wait(&full_t[pt.s], pt.par, a, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t src = tmem + lane_base + (uint32_t)(pt.s * kTN + 32 * cg);
                 const float dj = d8[j];
+                RingPos pn = pt;
+                ring_next(pn, kTBufs);
+                float v[16];
+                tmem_ld16(src, v);
+                const bool nxt = test_wait(&full_t[pn.s], pn.par);  // region g + 1, read at the end
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[16];
-                    tmem_ld16(src + 16 * half, v);
+                for (int i = 0; i < 16; i += 2) fma2(acc_sb[i], acc_sb[i + 1], v[i], v[i + 1], dj, dj);
+                tmem_ld16(src + 16, v);
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2)
-                        fma2(acc_sb[16 * half + i], acc_sb[16 * half + i + 1], v[i], v[i + 1], dj, dj);
-                }
+                for (int i = 0; i < 16; i += 2) fma2(acc_sb[16 + i], acc_sb[16 + i + 1], v[i], v[i + 1], dj, dj);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_t[pt.s]);
-                ring_next(pt, kTBufs);
+                pt = pn;
+                ++g;
+                ready = __all_sync(0xffffffffu, nxt);
             }
             if (!ok) break;
             // the min-term region: acc += d * acc_sb - dmin * mins, the running sums in
             // tensor memory
-            if (!warp_wait(&full_t[pt.s], pt.par, a, abort_flag) || !warp_wait(&full_h[ph.s], ph.par, a, abort_flag)) {
+            if ((!ready && !warp_wait(&full_t[pt.s], pt.par, a, abort_flag)) ||
+                !warp_wait(&full_h[ph.s], ph.par, a, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -516,14 +532,19 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemm_tc_kernel(const __grid_c
                 }
                 tmem_st8(acc_addr + 8 * qq, accv);
             }
+            RingPos pn = pt;
+            ring_next(pn, kTBufs);
+            const bool nxt = test_wait(&full_t[pn.s], pn.par);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&empty_t[pt.s]);
                 mbar_arrive(&empty_h[ph.s]);
             }
-            ring_next(pt, kTBufs);
+            pt = pn;
             ring_next(ph, kStagesH);
+            ++g;
+            ready = __all_sync(0xffffffffu, nxt);
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc_sb[i] = 0.0f;
         }
@@ -666,3 +687,4 @@ cudaError_t launch_q4k_gemm_tc(const void *w, const void *q8, float *y, int64_t 
 }
 
 }  // namespace rz
+
