@@ -52,6 +52,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak() -> float:
+    """Dense 16-bit tensor peak in TFLOP/s: the measured bf16 burst figure (f16
+    runs at the same rate), else the fallback 1900."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def profile_traffic(kernel_file: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on the
     current source of the kernel (sha256 of the .cu file), else None."""
@@ -222,6 +232,34 @@ def measure_gemv(rz, out_dim: int, in_dim: int, m: int, dev, stream, launches: i
             "weight_copies": ncopies}
 
 
+def measure_gemm(rz, out_dim: int, in_dim: int, m: int, dev, stream, launches: int = 8, reps: int = 10):
+    """The many-token tensor-core product (rz_q4k_q8_gemm: operand packing + the
+    tcgen05 GEMM) for one shape, timed like measure_gemv.  Returns us per call and
+    TFLOP/s of the integer-dot work (2 m out in) and of what the tensor cores
+    execute (9/8 of it: the min-term product)."""
+    import torch
+    wbytes = out_dim * (in_dim // 256) * S.Q4K_BYTES
+    ncopies = max(2, int(np.ceil(2 * L2_BYTES / wbytes)) + 1)
+    w0 = S.q4k_weight_device(f"sweep.{out_dim}.{in_dim}", out_dim, in_dim, dev)
+    ws = [w0] + [w0.clone() for _ in range(ncopies - 1)]
+    x = torch.randn((m, in_dim), device=dev, generator=S.torch_gen(f"gemm.x.{in_dim}.{m}", dev))
+    q8 = rz.q8_1_quantize(x)
+    y = torch.empty((m, out_dim), dtype=torch.float32, device=dev)
+    wsb = rz.q4k_q8_gemm_workspace_bytes(m, in_dim)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def launch():
+        for i in range(launches):
+            rz.rz_q4k_q8_gemm(ws[i % ncopies], q8, y, out_dim, m, out_dim, in_dim, work, wsb, stream=stream)
+
+    g = capture(launch, stream)
+    ms = time_graph(g, stream, reps) / launches
+    del g, ws
+    flops = 2.0 * m * out_dim * in_dim
+    return {"us": round(ms * 1e3, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+            "tensor_tflops": round(1.125 * flops / (ms * 1e-3) / 1e12, 1), "weight_copies": ncopies}
+
+
 class GemvWorkload:
     """Q4_K x Q8_1 GEMV, out 4096 x in 14336 (the largest shape of the Llama sweep),
     launched back to back over weight copies larger than twice the L2."""
@@ -329,6 +367,9 @@ class StackWorkload:
         self.position = position
         self.n_layers = n_layers
         self.shape = S.LLAMA7B
+        # from four tokens on the step's GEMVs run on the tensor cores (mma.sync)
+        self.gemv_kernel = "q4k_gemv_mma_kernel" if m >= 4 else "q4k_gemv_kernel"
+        self.kernel_file = "gemv_q4k_mma.cu" if m >= 4 else "gemv_q4k.cu"
         self.name = f"llama7b_q4k_decode_stack_l{self.n_layers}_m{m}_pos{position}"
 
     # ---- algorithmic bytes of one step
@@ -423,7 +464,7 @@ class StackWorkload:
 
     def dominant(self):
         n = self.n_layers * 4
-        return {"kernel": "q4k_gemv_kernel", "bytes_per_launch": self.fused_gemv_bytes() / n,
+        return {"kernel": self.gemv_kernel, "bytes_per_launch": self.fused_gemv_bytes() / n,
                 "launches_per_step": n,
                 "what": "the step's own four GEMV launches per layer (Q|K|V with the RMSNorm/Q8_1 "
                         "prologue, O + residual, gate/up with the norm prologue and SiLU*up, down "
@@ -527,6 +568,9 @@ def make_workload(args):
 # GEMV shapes reported beside every stack run: the target shape of the Llama sweep
 # at one token, and the widest batched-decode GEMV at 16 tokens.
 SUBRECORD_GEMVS = [(4096, 14336, 1), (14336, 4096, 16)]
+# The many-token (prefill) product on the tensor cores: a 512-token prompt
+# against the widest Llama-sweep shapes.
+SUBRECORD_GEMMS = [(4096, 14336, 512), (14336, 4096, 512)]
 MIN_TIMED_S = 1.0
 
 
@@ -628,6 +672,13 @@ def run_rz(args, world, rank, local, pg):
             r = measure_gemv(rz, o, i, m, dev, stream)
             r["frac"] = round(r["gbs"] / peak, 4)
             gemvs[f"{o}x{i}_m{m}"] = r
+    gemms = {}
+    if not args.no_subrecords:
+        tc_peak = measured_tensor_peak()
+        for o, i, m in SUBRECORD_GEMMS:
+            r = measure_gemm(rz, o, i, m, dev, stream)
+            r["frac_of_f16_tensor_peak"] = round(r["tensor_tflops"] / tc_peak, 4)
+            gemms[f"{o}x{i}_m{m}"] = r
     st, code = rz.check_device_error(stream)
     if st != 0:
         raise RuntimeError(f"device error word after timing: 0x{code:x}")
@@ -656,6 +707,7 @@ def run_rz(args, world, rank, local, pg):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "gemv": gemvs,
+        "prefill_gemm": gemms,
         "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": wl.e2e_bytes()[0], "d2h_bytes_per_step": wl.e2e_bytes()[1],
                 "ms_per_step": round(e2e_ms, 5)},
