@@ -18,6 +18,7 @@
 // ordered by the caller.  Nothing in the FFN scratch needs to start at zero; the
 // array keeps whatever the last call left in it.
 #include <mutex>
+#include <string>
 
 #include "../../include/rz.h"
 #include "rz_common.cuh"
@@ -27,6 +28,15 @@ namespace rz {
 rz_status record_error(rz_status st, const char *msg);
 rz_status ensure_device();
 }  // namespace rz
+
+namespace {
+// RZ_ERR_CUDA with the CUDA error's name and text, like the other entry points
+rz_status cuda_error(const char *what, cudaError_t e)
+{
+    std::string msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return rz::record_error(RZ_ERR_CUDA, msg.c_str());
+}
+}  // namespace
 
 namespace {
 
@@ -69,8 +79,8 @@ extern "C" rz_status rz_swiglu_ffn_static(const float *x, const float *gamma, co
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64)
-        return record_error(RZ_ERR_CUDA, "rz_swiglu_ffn_static: cudaGetDevice failed");
+    if (e != cudaSuccess) return cuda_error("rz_swiglu_ffn_static: cudaGetDevice", e);
+    if (dev < 0 || dev >= 64) return record_error(RZ_ERR_UNSUPPORTED, "rz_swiglu_ffn_static: device index");
     void *scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_scratch_mu);
@@ -78,14 +88,13 @@ extern "C" rz_status rz_swiglu_ffn_static(const float *x, const float *gamma, co
             void *p = nullptr;
             e = cudaGetSymbolAddress(&p, g_ffn_scratch);
             if (e != cudaSuccess)
-                return record_error(RZ_ERR_CUDA, "rz_swiglu_ffn_static: cudaGetSymbolAddress of the static "
-                                                 "scratch failed");
+                return cuda_error("rz_swiglu_ffn_static: cudaGetSymbolAddress of the static scratch", e);
             g_scratch_dev[dev] = p;
         }
         scratch = g_scratch_dev[dev];
     }
     e = launch_swiglu_ffn(x, gamma, w_gate, w_up, w_down, out, m, hidden, hidden_pad, inter, eps, scratch,
                           static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return record_error(RZ_ERR_CUDA, "rz_swiglu_ffn_static: launch failed");
+    if (e != cudaSuccess) return cuda_error("rz_swiglu_ffn_static: launch", e);
     return RZ_OK;
 }
