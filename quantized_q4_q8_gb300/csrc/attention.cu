@@ -8,11 +8,13 @@
 // kv head h / (n_heads / n_kv_heads) with softmax(q.k / sqrt(head_dim)).
 //
 // RoPE pairs (2i, 2i + 1) for mode 0 and (i, i + head_dim/2) for mode 1 turn by
-// position * theta^(-2i/head_dim).  A small kernel builds, per token, the cosine
-// and sine of every pair's angle: the angle is formed and reduced modulo 2*pi in
+// position * theta^(-2i/head_dim).  Every CTA forms the cosine and sine of its
+// token's pair angles itself, one pair per thread: theta^(-2i/head_dim) is the
+// i-th power of r = theta^(-2/head_dim) (computed on the host), taken by binary
+// powering in double precision; the angle is formed and reduced modulo 2*pi in
 // double precision (positions reach thousands of radians), then sin/cos are taken
-// in single precision.  The table depends only on the positions, so the layer
-// stack builds it once per step and every layer reuses it.
+// in single precision.  A dozen double operations per thread, no table kernel and
+// no dependency on one.
 //
 // Attention is split over the sequence in chunks of 64 cache rows (flash-
 // decoding style).  The grid is one wave: CTA (z, kv head, token) works chunks
@@ -45,29 +47,30 @@ namespace {
 constexpr int kAttnThreads = 256;
 constexpr int kChunk = 64;  // cache rows per CTA
 constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 
 __device__ __forceinline__ int token_position(const AttnArgs &a, int t)
 {
     return a.positions ? a.positions[t] : a.position;
 }
 
-// cos/sin of every pair angle, per token: tab[t][i] = (cos, sin)
-__global__ void rope_table_kernel(const AttnArgs a)
+// cos/sin of the pair angles of position pos into tabs[i] = (cos, sin), one pair
+// per thread of the CTA
+__device__ __forceinline__ void rope_angles(const AttnArgs &a, int pos, float *tabs, int tid, int nthreads)
 {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int t = blockIdx.x;
     const int half = a.head_dim / 2;
-    const int pos = token_position(a, t);
-    const double l2t = log2((double)a.rope_theta);
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const double inv_freq = exp2(-(2.0 * i / a.head_dim) * l2t);
-        const double ang = (double)pos * inv_freq;
-        const double red = ang - kTwoPi * rint(ang / kTwoPi);
+    for (int i = tid; i < half; i += nthreads) {
+        double f = 1.0, b = a.rope_r;  // f = r^i
+        for (int e = i; e; e >>= 1) {
+            if (e & 1) f *= b;
+            b *= b;
+        }
+        const double ang = (double)pos * f;
+        const double red = ang - kTwoPi * rint(ang * kInvTwoPi);
         float sn, cs;
         sincosf((float)red, &sn, &cs);
-        a.rope_tab[((int64_t)t * half + i) * 2] = cs;
-        a.rope_tab[((int64_t)t * half + i) * 2 + 1] = sn;
+        tabs[2 * i] = cs;
+        tabs[2 * i + 1] = sn;
     }
 }
 
@@ -123,7 +126,8 @@ __device__ __forceinline__ void load_cols(const float *p, float (&r)[CNT])
 // w + 8, ..., lane l dims l + 32 e of each (conflict-free), with the rotated query
 // heads in shared memory.
 // shared memory: kbuf [64][hd] | vbuf [64][hd] | qs [G][hd] | kn [hd] | vn [hd] |
-//                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | 2 mbarriers
+//                ps [G][64] | stat [G][2] + 2 (padded to 4) | red [8][G][hd] | flag | 2 mbarriers |
+//                tabs [hd/2][2] (cos, sin of the token's pair angles)
 // With att_bufs == 1 (every chunk has a CTA of its own) vbuf is kbuf: the V rows
 // are copied in once the scores have read the K rows, and the smaller footprint
 // lets more CTAs share an SM.
@@ -145,9 +149,16 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
     int *flag = reinterpret_cast<int *>(red + 8 * G * hd);
     uint64_t *kbar = reinterpret_cast<uint64_t *>(flag + 2);
     uint64_t *vbar = kbar + 1;
+    float *tabs = reinterpret_cast<float *>(vbar + 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
-    pdl_wait();
+    // With the position a host value, nothing before the rotation of q depends on
+    // the previous kernel: the cache rows below the position were written by
+    // earlier steps, so their copies start before the wait for this step's q, k
+    // and v.  With device positions everything waits.  Every global write comes
+    // after the wait.
+    const bool early = a.positions == nullptr;
+    if (!early) pdl_wait();
 
     const int pos = token_position(a, t);
     const bool pos_ok = pos >= 0 && pos < a.max_seq;
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
     const int mine = chunk < nc ? (nc - 1 - chunk) / Z + 1 : 0;
     if (mine == 0) return;
     if (!pos_ok && chunk == 0 && kvh == 0 && tid == 0) set_error(a.err, DEV_BAD_POSITION);
-    const float *tab = a.rope_tab + (int64_t)t * (hd / 2) * 2;
+    const float *tab = tabs;
     const float scale = 1.0f / sqrtf((float)hd);
     const int64_t kv_base = (int64_t)t * a.seq_stride + (int64_t)kvh * hd;
     auto rows_of = [&](int c) { return pos_ok ? max(0, min(kChunk, pos + 1 - c * kChunk)) : 0; };
@@ -193,6 +204,9 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
         __syncthreads();
         issue_k(chunk);
         if (nbuf == 2) issue_v(chunk);
+        rope_angles(a, pos, tabs, tid, kAttnThreads);
+        if (early) pdl_wait();  // q, k and v of this step come from the previous kernel
+        __syncthreads();
 
         // rotated query heads of this kv head, and (owner) the new row
         for (int g = 0; g < G; ++g)
@@ -331,6 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) attention_chunk_kernel(const 
             __syncthreads();  // ps, stat and red are reused by the next chunk
         }
     } else {
+        if (early) pdl_wait();
         for (int g = tid; g < G; g += kAttnThreads) {
             float *rec = part_rec(a, t, kvh, chunk, g);
             rec[0] = -INFINITY;
@@ -509,17 +524,10 @@ size_t attention_smem_bytes_n(int group, int head_dim, int nbuf)
     return ((size_t)nbuf * kChunk * head_dim + (size_t)group * head_dim + 2 * (size_t)head_dim +
             (size_t)group * kChunk + ((2 * (size_t)group + 2 + 3) & ~(size_t)3) + 8 * (size_t)group * head_dim) *
                sizeof(float) +
-           16 + 16;  // flag (+ pad), two mbarriers
+           16 + 16 + (size_t)head_dim * sizeof(float);  // flag (+ pad), two mbarriers, the pair angles
 }
 
 size_t attention_smem_bytes(int group, int head_dim, int) { return attention_smem_bytes_n(group, head_dim, 2); }
-
-cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s)
-{
-    AttnArgs args = a;
-    void *kargs[] = {&args};
-    return launch_ex((const void *)rope_table_kernel, dim3((unsigned)a.m), dim3(64), 0, s, kargs);
-}
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
 {
@@ -535,10 +543,6 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
         if (e == cudaSuccess) e = encode_tensor_map(&args.vmap, a.vc, 4, 3, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
-    if (a.make_table) {
-        cudaError_t e = launch_rope_table(a, s);
-        if (e != cudaSuccess) return e;
-    }
     const void *fn = a.head_dim == 32    ? (const void *)attention_chunk_kernel<1>
                      : a.head_dim == 64  ? (const void *)attention_chunk_kernel<2>
                      : a.head_dim == 128 ? (const void *)attention_chunk_kernel<4>
@@ -548,13 +552,16 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s)
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
     }
-    // One wave.  When every chunk can have a resident CTA of its own with K and V
-    // through one buffer (and the merge's records fit in it), that; else as many
+    // One wave.  Else, when every chunk can have a resident CTA of its own with K
+    // and V through one buffer (and the merge's records fit in it), that; else as many
     // chunk slots per (kv head, token) as resident CTAs allow with two buffers,
     // the chunks spread evenly over them (each CTA streams its chunks in turn).
+    // With two buffers V streams in beside K; when every chunk can have a CTA of
+    // its own that way (short positions, small grids), that comes first.
     const int per_z = a.n_kv_heads * a.m;
     const size_t smem1 = attention_smem_bytes_n(a.group, a.head_dim, 1);
-    const bool one = resident_ctas(fn, smem1) >= per_z * a.launch_chunks &&
+    const bool two_all = resident_ctas(fn, attention_smem_bytes_n(a.group, a.head_dim, 2)) >= per_z * a.launch_chunks;
+    const bool one = !two_all && resident_ctas(fn, smem1) >= per_z * a.launch_chunks &&
                      (size_t)a.n_chunks * (a.head_dim + 4) <= (size_t)kChunk * a.head_dim;
     args.att_bufs = one ? 1 : 2;
     const size_t smem = one ? smem1 : attention_smem_bytes_n(a.group, a.head_dim, 2);

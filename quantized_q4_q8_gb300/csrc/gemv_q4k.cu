@@ -85,6 +85,10 @@ struct Args {
     // issued and every wait polls at most wait_limit times; -1 / unused otherwise
     int stall_stage;
     uint32_t wait_limit;
+    // zero padding of the output: y[0][t * zy_ld + zy_from + j] = 0 for j < zy_cnt,
+    // written by the last CTA (segment 0 only)
+    float *zy;
+    int64_t zy_ld, zy_from, zy_cnt;
 };
 
 enum XIn { XIN_Q8 = 0, XIN_NORM = 1, XIN_F32 = 2 };
@@ -187,6 +191,9 @@ __global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args
 
     // ---------------------------------------------------------------- consumers
     pdl_wait();  // activations and the output buffers belong to the previous kernel
+    if (a.zy && blockIdx.x == gridDim.x - 1)
+        for (int64_t i = threadIdx.x; i < (int64_t)a.m * a.zy_cnt; i += kConsumerWarps * 32)
+            a.zy[(i / a.zy_cnt) * a.zy_ld + a.zy_from + i % a.zy_cnt] = 0.0f;
     XSrc x;
     x.in_dim = a.in_dim;
     x.nb = a.in_dim / 32;
@@ -464,6 +471,12 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
         xin = f32in->gamma ? XIN_NORM : XIN_F32;
     }
     a.err = dev_error_word();
+    if (seg[0].zero_to > seg[0].rows) {
+        a.zy = seg[0].y;
+        a.zy_ld = seg[0].ldy ? seg[0].ldy : seg[0].rows;
+        a.zy_from = seg[0].rows;
+        a.zy_cnt = seg[0].zero_to - seg[0].rows;
+    }
     a.stall_stage = -1;
     a.wait_limit = kWaitLimit;
     if (g_stall_next_gemv) {

@@ -80,6 +80,8 @@ struct MArgs {
     unsigned *err;
     int stall_stage;      // test aid (rz_debug_stall_next_gemv), -1 otherwise
     uint32_t wait_limit;
+    float *zy;            // zero padding of segment 0's output (last CTA), or nullptr
+    int64_t zy_ld, zy_from, zy_cnt;
 };
 
 enum MXIn { MX_Q8 = 0, MX_NORM = 1, MX_F32 = 2 };
@@ -446,6 +448,9 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     pdl_wait();
     auto csync = [] { asm volatile("bar.sync 1, %0;" ::"r"(kMW * 32) : "memory"); };
     const int tid = threadIdx.x;
+    if (a.zy && blockIdx.x == gridDim.x - 1)
+        for (int64_t i = tid; i < (int64_t)a.m * a.zy_cnt; i += kMW * 32)
+            a.zy[(i / a.zy_cnt) * a.zy_ld + a.zy_from + i % a.zy_cnt] = 0.0f;
     {
         // the d8 table and the s pieces start at zero: token slots past m contribute 0
         const int64_t n16 = (mma_d8_bytes(a.in_dim, NT) + mma_spc_bytes(a.in_dim, NT)) / 16;
@@ -735,6 +740,12 @@ cudaError_t launch_q4k_gemv_mma(const Q4kSegment *seg, int nseg, int epilogue, c
         a.xs = xs;
     }
     a.err = dev_error_word();
+    if (seg[0].zero_to > seg[0].rows) {
+        a.zy = seg[0].y;
+        a.zy_ld = seg[0].ldy ? seg[0].ldy : seg[0].rows;
+        a.zy_from = seg[0].rows;
+        a.zy_cnt = seg[0].zero_to - seg[0].rows;
+    }
     a.stall_stage = -1;
     a.wait_limit = kWaitLimit;
     if (g_stall_next_gemv) {

@@ -10,7 +10,7 @@
 // Fusions here: 1+2+3 are one launch: every CTA of the Q|K|V GEMV normalises
 // and quantises the layer input into its shared memory, and the three matrices
 // are one GEMV; 4+5 are one split-sequence attention kernel that also applies
-// RoPE (from a cos/sin table built once per step), appends k and v to the cache,
+// RoPE, appends k and v to the cache,
 // and whose merging CTA quantises its heads; 6+7 are one GEMV with a residual
 // epilogue; in 9 the norm + Q8_1 live in the gate/up GEMV, whose epilogue
 // applies silu(gate) * up, and the Q8_1 of h lives in the down GEMV, whose
@@ -60,7 +60,9 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
         e = launch_q4k_gemv(gu, 2, EPI_SWIGLU, x8, m, hidden_pad, s);
     }
     if (e != cudaSuccess) return e;
-    Q4kSegment dn = {w_down, out, x, hidden, hidden_pad, hidden_pad};
+    // out's padding [hidden, hidden_pad) is zeroed by the down GEMV itself (a
+    // memset node would end the programmatic-dependent-launch chain)
+    Q4kSegment dn = {w_down, out, x, hidden, hidden_pad, hidden_pad, nullptr, hidden_pad};
     if (q4k_gemv_f32_input_ok(m, inter)) {
         // Q8_1 of h inside the down GEMV
         e = launch_q4k_gemv_f32(&dn, 1, EPI_RESID, F32Input{h, inter, nullptr, 0, 0.0f}, m, inter, s);
@@ -69,10 +71,6 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
         if (e != cudaSuccess) return e;
         e = launch_q4k_gemv(&dn, 1, EPI_RESID, h8, m, inter, s);
     }
-    if (e != cudaSuccess) return e;
-    if (hidden_pad > hidden)
-        e = cudaMemset2DAsync(out + hidden, (size_t)hidden_pad * 4, 0, (size_t)(hidden_pad - hidden) * 4,
-                              (size_t)m, s);
     return e;
 }
 
@@ -82,7 +80,7 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
 struct LayerWs {
     int *counters;
     void *x8;
-    float *qkv, *rope_tab, *part;
+    float *qkv, *part;
     void *a8;
     float *res1;
     void *ffn;
@@ -107,7 +105,6 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
     w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
     w.x8 = take(q8_bytes(m, L.hidden_pad));
     w.qkv = reinterpret_cast<float *>(take((size_t)m * (q_dim + 2 * kv_dim) * 4));
-    w.rope_tab = reinterpret_cast<float *>(take((size_t)m * L.head_dim * 4));
     w.part = reinterpret_cast<float *>(
         take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4));
     w.a8 = take(q8_bytes(m, q_pad));
@@ -125,7 +122,7 @@ size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq)
 }
 
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
-                        int position, float *rope_tab, int make_table, float *part, int *counters,
+                        int position, float *part, int *counters,
                         const float *q, const float *k, const float *v, int64_t ld_qkv, float *att,
                         void *att_q8)
 {
@@ -134,8 +131,7 @@ AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const i
     a.k = k;
     a.v = v;
     a.ld_qkv = ld_qkv;
-    a.rope_tab = rope_tab;
-    a.make_table = make_table;
+    a.rope_r = pow((double)L.rope_theta, -2.0 / (double)L.head_dim);
     a.kc = kv.k;
     a.vc = kv.v;
     a.seq_stride = kv.seq_stride;
@@ -165,7 +161,7 @@ AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const i
 
 cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
                                 const int32_t *positions, int position, int64_t m, float *output,
-                                void *workspace, cudaStream_t s, int make_table)
+                                void *workspace, cudaStream_t s)
 {
     LayerWs w = layer_ws(L, m, kv.max_seq, static_cast<uint8_t *>(workspace));
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
@@ -192,7 +188,7 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
         e = launch_q4k_gemv(qkv, nseg, EPI_STORE, w.x8, m, L.hidden_pad, s);
     }
     if (e != cudaSuccess) return e;
-    AttnArgs a = make_attn_args(L, m, kv, positions, position, w.rope_tab, make_table, w.part, w.counters,
+    AttnArgs a = make_attn_args(L, m, kv, positions, position, w.part, w.counters,
                                 w.qkv, w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, nullptr, w.a8);
     e = launch_attention(a, s);
     if (e != cudaSuccess) return e;
@@ -226,8 +222,7 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
     cudaError_t e = cudaSuccess;
     for (int l = 0; l < n_layers; ++l) {
         float *out = (l == n_layers - 1 && hidden_out) ? hidden_out : buf[l & 1];
-        // the RoPE table depends only on the positions: built by the first layer
-        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s, l == 0);
+        e = launch_decode_layer(cur, layers[l], kvs[l], positions, position, m, out, lws, s);
         if (e != cudaSuccess) return e;
         cur = out;
     }
@@ -253,7 +248,7 @@ int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int 
     per_layer += gemv(L0.hidden_pad, EPI_STORE);   // RMSNorm -> Q|K|V
     per_layer += gemv(L0.hidden_pad, EPI_SWIGLU);  // RMSNorm -> gate/up
     per_layer += gemv(L0.inter, EPI_RESID);        // Q8_1 of h -> down
-    return 1 /* RoPE table */ + n_layers * per_layer + h;
+    return n_layers * per_layer + h;
 }
 
 // ---------------------------------------------------------------- Q4_0 layer
@@ -264,7 +259,7 @@ int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int 
 // intermediate is an f32 buffer, as on the page.
 struct LayerQ40Ws {
     int *counters;
-    float *normed, *qkv, *rope_tab, *part, *att, *o, *res1, *n2, *u, *g, *h, *dn;
+    float *normed, *qkv, *part, *att, *o, *res1, *n2, *u, *g, *h, *dn;
     size_t total;
 };
 
@@ -284,7 +279,6 @@ static LayerQ40Ws layer_q4_0_ws(const LayerQ40Desc &L, int64_t m, int max_seq, u
     w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
     w.normed = take((size_t)m * L.hidden * 4);
     w.qkv = take((size_t)m * (q_dim + 2 * kv_dim) * 4);
-    w.rope_tab = take((size_t)m * L.head_dim * 4);
     w.part = take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4);
     w.att = take((size_t)m * q_dim * 4);
     w.o = take((size_t)m * L.hidden * 4);
@@ -319,7 +313,7 @@ cudaError_t launch_decode_layer_q4_0(const float *input, const LayerQ40Desc &L, 
     ld.head_dim = L.head_dim;
     ld.rope_theta = L.rope_theta;
     ld.rope_mode = L.rope_mode;
-    AttnArgs a = make_attn_args(ld, m, kv, positions, position, w.rope_tab, 1, w.part, w.counters, w.qkv,
+    AttnArgs a = make_attn_args(ld, m, kv, positions, position, w.part, w.counters, w.qkv,
                                 w.qkv + q_dim, w.qkv + q_dim + kv_dim, ld_qkv, w.att, nullptr);
     e = launch_attention(a, s);
     if (e == cudaSuccess) e = launch_q4_0_gemv_ld(L.wo, w.att, q_dim, w.o, m, L.hidden, q_dim, s);

@@ -71,6 +71,7 @@ struct Q4kSegment {
     int64_t ldy = 0;   // 0: rows
     int64_t ldr = 0;   // 0: rows
     const float *bias = nullptr;  // [rows] added to every token's output (EPI_STORE only)
+    int64_t zero_to = 0;          // > rows: y[t][rows .. zero_to) is set to 0 (a padded hidden state)
 };
 
 // Up to three weight matrices with the same in_dim read against one Q8_1
@@ -124,8 +125,7 @@ struct AttnArgs {
     CUtensorMap kmap, vmap;      // the caches as [m][max_seq][kv_dim] f32, boxes of one head x 64 rows
     const float *q, *k, *v;      // pre-RoPE projections of token t at + t * ld_qkv
     int64_t ld_qkv;
-    float *rope_tab;             // workspace f32 [m][head_dim/2][2]: cos, sin of each pair angle
-    int make_table;              // 1: build rope_tab first (else it holds this step's table)
+    double rope_r;               // theta^(-2 / head_dim): pair i turns by position * rope_r^i
     float *kc, *vc;              // caches: token t at + t * seq_stride, row p at + p * kv_dim
     int64_t seq_stride;
     int max_seq;
@@ -146,8 +146,6 @@ struct AttnArgs {
 
 int attention_chunk_len(int max_seq, int n_kv_heads, int m);
 size_t attention_smem_bytes(int group, int head_dim, int chunk_len);
-// the RoPE cos/sin table of every token (one small launch)
-cudaError_t launch_rope_table(const AttnArgs &a, cudaStream_t s);
 // (table,) then split-sequence attention with RoPE, the KV append, the merge and
 // the Q8_1 of the output.
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
@@ -185,12 +183,12 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
                               cudaStream_t s);
 size_t layer_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
 AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const int32_t *positions,
-                        int position, float *rope_tab, int make_table, float *part, int *counters,
+                        int position, float *part, int *counters,
                         const float *q, const float *k, const float *v, int64_t ld_qkv, float *att,
                         void *att_q8);
 cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const KvDesc &kv,
                                 const int32_t *positions, int position, int64_t m, float *output,
-                                void *workspace, cudaStream_t s, int make_table = 1);
+                                void *workspace, cudaStream_t s);
 size_t stack_workspace_bytes(const LayerDesc &L, int64_t m, int max_seq);
 
 // The Q4_0 whole-model layer (every projection Q4_0 against f32 activations).
