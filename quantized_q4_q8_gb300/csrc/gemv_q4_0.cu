@@ -13,6 +13,8 @@
 // (2^23 + 8), so the inner loop is one integer op, one add and one FMA per
 // weight.  Partial sums of the column warps of a row are combined in a fixed
 // order in shared memory (deterministic).
+#include <algorithm>
+
 #include "rz_common.cuh"
 #include "rz_kernels.h"
 
@@ -143,6 +145,280 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// One token (the LM head of a decode step): the weights stream through a ring of
+// shared-memory stages filled by bulk copies, as the Q4_K GEMV does.  A CTA per
+// SM owns a contiguous range of rows (a whole number of copy units: rows whose
+// bytes are a multiple of 16); a producer warp keeps the ring full, 16 consumer
+// warps are (nb / 32) column warps x row groups: lane L of column warp c owns
+// block 32 c + L of every row and keeps its 32 activations in registers,
+// pre-scaled by 2^-s for the bit position s its nibble has inside a 16-bit half
+// of the packed word.  A nibble then becomes an exact float with one LOP3
+// (0x4B000000 | (half & (0xF << s)) = 2^23 + q 2^s) and one subtraction of 2^23,
+// and the dot runs on fma.rn.f32x2 pairs:
+//   sum_i (q_i - 8) x_i = sum_i (q_i 2^s_i)(x_i 2^-s_i) - 8 sum_i x_i.
+// Per-row partial sums of the column warps are added in a fixed order at the end.
+constexpr int kRW = 16;                  // consumer warps
+constexpr int kRThreads = (kRW + 1) * 32;
+constexpr int kRingBytes = 160 * 1024;
+
+struct RArgs {
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    const float *bias;
+    int64_t out_dim, row_bytes;
+    int nb;          // blocks per row
+    int cw, rg;      // column warps per row, row groups (cw * rg == kRW)
+    int unit;        // rows per copy unit
+    int64_t units;   // copy units of the matrix
+    int stage_rows;  // rows per ring stage (a multiple of unit)
+    int NS;          // stages in the ring
+    int64_t rows_max;  // rows of the largest CTA range
+    unsigned *err;
+};
+
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr)
+{
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// 2^23 + v as a float (v < 2^23 in the mantissa bits)
+__device__ __forceinline__ float magic(uint32_t v) { return __uint_as_float(v | 0x4B000000u); }
+
+// bit position of element i's nibble inside its 16-bit half: byte k = i % 16,
+// nibble i / 16 (high), byte k % 2 inside the half
+__host__ __device__ constexpr int nib_shift(int i) { return 8 * ((i % 16) % 2) + 4 * (i / 16); }
+
+// sum_i q_i 2^s_i xs_i of one block whose 16 code bytes are q[0..3]
+__device__ __forceinline__ float block_dot_scaled(const uint32_t (&q)[4], const float (&xs)[32])
+{
+    const float2 off = make_float2(-8388608.0f, -8388608.0f);
+    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0;  // two chains
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t v = hh ? (q[wd] >> 16) : q[wd];
+            const int k0 = 4 * wd + 2 * hh;  // bytes k0 (bits 0-7) and k0 + 1 (bits 8-15)
+            // elements: k0 (s 0), k0 + 16 (s 4), k0 + 1 (s 8), k0 + 17 (s 12)
+            const float2 fa = f2_add(make_float2(magic(v & 0xFu), magic(v & 0xF0u)), off);
+            const float2 fb = f2_add(make_float2(magic(v & 0xF00u), magic(v & 0xF000u)), off);
+            acc0 = f2_fma(fa, make_float2(xs[k0], xs[k0 + 16]), acc0);
+            acc1 = f2_fma(fb, make_float2(xs[k0 + 1], xs[k0 + 17]), acc1);
+        }
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+__global__ void __launch_bounds__(kRThreads, 1) q4_0_gemv_ring_kernel(const RArgs a)
+{
+    extern __shared__ __align__(128) uint8_t rsm[];
+    const int64_t stage_bytes = (int64_t)a.stage_rows * a.row_bytes;
+    uint8_t *ring = rsm;
+    float *part = reinterpret_cast<float *>(rsm + (int64_t)a.NS * stage_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(
+        (reinterpret_cast<uintptr_t>(part + a.rows_max * a.cw) + 7) & ~uintptr_t(7));
+    uint64_t *empty = full + a.NS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
+    const int64_t r0 = (a.units * blockIdx.x / G) * a.unit;
+    const int64_t r1 = min((a.units * (blockIdx.x + 1) / G) * a.unit, a.out_dim);
+    const int64_t nrows = r1 > r0 ? r1 - r0 : 0;
+    const int64_t nstages = (nrows + a.stage_rows - 1) / a.stage_rows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kRW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kRW) {
+        // ---- producer: the weights do not depend on the previous kernel
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            RingPos rp{0, 0u};
+            for (int64_t k = 0; k < nstages; ++k, ring_next(rp, a.NS)) {
+                if (k >= a.NS && !mbar_wait(&empty[rp.s], rp.par ^ 1u)) {
+                    set_error(a.err, DEV_TIMEOUT_Q40);
+                    // copies issued before must land before the CTA exits
+                    for (int64_t q = (k > a.NS ? k - a.NS : 0); q < k; ++q)
+                        if (!mbar_wait(&full[q % a.NS], (unsigned)((q / a.NS) & 1))) set_error(a.err, DEV_TIMEOUT_DRAIN);
+                    break;
+                }
+                const int64_t u0 = r0 + k * a.stage_rows;
+                const int64_t n = min((int64_t)a.stage_rows, r1 - u0);
+                const unsigned bytes = (unsigned)(n * a.row_bytes);
+                mbar_arrive_expect_tx(&full[rp.s], bytes);
+                bulk_g2s_hint(ring + (int64_t)rp.s * stage_bytes, a.w + u0 * a.row_bytes, bytes, &full[rp.s], pol);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
+    pdl_wait();  // the activations come from the previous kernel
+    const int cwi = warp % a.cw, rgi = warp / a.cw;
+    const int b = 32 * cwi + lane;  // this lane's block
+    const bool active = b < a.nb;
+    float xs[32];
+    float sx = 0.0f;
+    {
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + (int64_t)(active ? b : 0) * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = active ? __ldg(xp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xs[4 * i] = v.x;
+            xs[4 * i + 1] = v.y;
+            xs[4 * i + 2] = v.z;
+            xs[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            sx += xs[i];
+            xs[i] = ldexpf(xs[i], -nib_shift(i));  // exact: a power-of-two scale
+        }
+    }
+    const uint32_t ring_s = smem_u32(ring);
+    RingPos rp{0, 0u};
+    bool ok = true;
+    for (int64_t k = 0; k < nstages; ++k, ring_next(rp, a.NS)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[rp.s], rp.par));
+        if (!ok) {
+            if (lane == 0) set_error(a.err, DEV_TIMEOUT_Q40);
+            break;
+        }
+        const int64_t u0 = r0 + k * a.stage_rows;
+        const int n = (int)min((int64_t)a.stage_rows, r1 - u0);
+        const uint32_t slot = ring_s + (uint32_t)((int64_t)rp.s * stage_bytes);
+        // two rows in flight per warp: independent loads, dots and reductions
+        for (int rr = rgi; rr < n; rr += 2 * a.rg) {
+            float v[2] = {0.0f, 0.0f};
+            const bool has1 = rr + a.rg < n;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (active && (u == 0 || has1)) {
+                    // the 18 bytes of the block: five aligned words, realigned by funnel shifts
+                    const uint32_t addr = slot + (uint32_t)((int64_t)(rr + u * a.rg) * a.row_bytes) + 18u * (uint32_t)b;
+                    const uint32_t base = addr & ~3u, off = addr & 3u;  // off is 0 or 2
+                    uint32_t w5[5];
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) w5[i] = lds_b32(base + 4u * i);
+                    const uint32_t sh = 16u - 8u * off;  // 16 (off 0) or 0 (off 2)
+                    uint32_t q[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t lo = off ? w5[i + 1] : w5[i];
+                        const uint32_t hi = off ? (i + 2 < 5 ? w5[i + 2] : 0u) : w5[i + 1];
+                        q[i] = __funnelshift_r(lo, hi, sh);
+                    }
+                    const float d = h2f((uint16_t)(off ? (w5[0] >> 16) : (w5[0] & 0xffffu)));
+                    v[u] = d * (block_dot_scaled(q, xs) - 8.0f * sx);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+                v[1] += __shfl_xor_sync(0xffffffffu, v[1], o);
+            }
+            if (lane == 0) {
+                part[(u0 - r0 + rr) * a.cw + cwi] = v[0];
+                if (has1) part[(u0 - r0 + rr + a.rg) * a.cw + cwi] = v[1];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[rp.s]);
+    }
+    // the column warps' partial sums of every row, in a fixed order
+    asm volatile("bar.sync 1, %0;" ::"r"(kRW * 32) : "memory");
+    if (!ok) return;
+    for (int64_t i = threadIdx.x; i < nrows; i += kRW * 32) {
+        float sum = 0.0f;
+        for (int c = 0; c < a.cw; ++c) sum += part[i * a.cw + c];
+        a.y[r0 + i] = a.bias ? sum + a.bias[r0 + i] : sum;
+    }
+}
+
+// One token through the ring kernel, when the shapes allow it (else false).
+cudaError_t launch_ring(const void *w, const float *x, float *y, int64_t out_dim, int64_t in_dim, const float *bias,
+                        cudaStream_t s, bool *used)
+{
+    *used = false;
+    RArgs a = {};
+    a.nb = (int)(in_dim / 32);
+    a.cw = (a.nb + 31) / 32;
+    if (a.cw > kRW || kRW % a.cw) return cudaSuccess;
+    a.rg = kRW / a.cw;
+    a.row_bytes = (int64_t)a.nb * 18;
+    int g = 16;
+    while (a.row_bytes % g) g >>= 1;
+    a.unit = 16 / g;  // rows whose bytes are a multiple of 16
+    if ((out_dim * a.row_bytes) % 16) return cudaSuccess;
+    a.units = (out_dim + a.unit - 1) / a.unit;
+    const int64_t per_stage = std::max<int64_t>(1, 32768 / (a.row_bytes * a.unit));
+    a.stage_rows = (int)(per_stage * a.unit);
+    const int64_t stage_bytes = (int64_t)a.stage_rows * a.row_bytes;
+    a.NS = (int)std::min<int64_t>(32, kRingBytes / stage_bytes);
+    if (a.NS < 2) return cudaSuccess;
+    const int64_t grid = std::min<int64_t>(dev_info().sm_count, a.units);
+    a.rows_max = ((a.units + grid - 1) / grid) * a.unit;
+    const size_t smem = (size_t)(a.NS * stage_bytes) + (size_t)a.rows_max * a.cw * 4 + 8 + 16 * (size_t)a.NS;
+    if (smem > dev_info().smem_optin) return cudaSuccess;
+    a.w = static_cast<const uint8_t *>(w);
+    a.x = x;
+    a.y = y;
+    a.bias = bias;
+    a.out_dim = out_dim;
+    a.err = dev_error_word();
+    static bool attr_done[64] = {};
+    const int dev = dev_info().device;
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(q4_0_gemv_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)dev_info().smem_optin);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kRThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_use_pdl ? 1 : 0;
+    *used = true;
+    return cudaLaunchKernelEx(&cfg, q4_0_gemv_ring_kernel, a);
+}
+
 template <int MT>
 cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t s)
 {
@@ -175,6 +451,11 @@ cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m,
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
                                 int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias)
 {
+    if (m == 1) {
+        bool used = false;
+        const cudaError_t e = launch_ring(w, x, y, out_dim, in_dim, bias, s, &used);
+        if (used || e != cudaSuccess) return e;
+    }
     Args a = {};
     a.bias = bias;
     a.ldx = ldx;
