@@ -160,7 +160,10 @@ __global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Args a)
 // Per-row partial sums of the column warps are added in a fixed order at the end.
 constexpr int kRW = 16;                  // consumer warps
 constexpr int kRThreads = (kRW + 1) * 32;
-constexpr int kRingBytes = 160 * 1024;
+constexpr int kRingBytes = 196 * 1024;
+// 64 KB stages: every mbarrier wait costs a warp a few hundred cycles here, so fewer,
+// larger stages keep more of the consumers' time on the dot products.
+constexpr int kStageBytes = 64 * 1024;
 
 struct RArgs {
     const uint8_t *w;
@@ -382,7 +385,7 @@ cudaError_t launch_ring(const void *w, const float *x, float *y, int64_t out_dim
     a.unit = 16 / g;  // rows whose bytes are a multiple of 16
     if ((out_dim * a.row_bytes) % 16) return cudaSuccess;
     a.units = (out_dim + a.unit - 1) / a.unit;
-    const int64_t per_stage = std::max<int64_t>(1, 32768 / (a.row_bytes * a.unit));
+    const int64_t per_stage = std::max<int64_t>(1, kStageBytes / (a.row_bytes * a.unit));
     a.stage_rows = (int)(per_stage * a.unit);
     const int64_t stage_bytes = (int64_t)a.stage_rows * a.row_bytes;
     a.NS = (int)std::min<int64_t>(32, kRingBytes / stage_bytes);

@@ -49,8 +49,6 @@ constexpr int kCtaSmem = 200 * 1024;
 constexpr int kCtaSmem1 = 200 * 1024;
 __host__ __device__ constexpr int consumer_warps(int mt) { return mt == 1 ? kConsumerWarps1 : kConsumerWarps; }
 __host__ __device__ constexpr int cta_threads(int mt) { return (consumer_warps(mt) + 1) * 32; }
-constexpr int kStageTarget = 16 * 1024;
-constexpr int kStageTargetFused = 32 * 1024;
 constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
 constexpr int kMaxStages = 16;
 
@@ -486,21 +484,18 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
     }
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
-    // Small stages for the plain GEMV (Q8_1 in, store out): its consumers start
-    // at once, so the first stage's arrival is on the critical path.  The fused
-    // kernels first wait for the previous kernel and stage their input, while the
-    // ring fills: larger stages there mean fewer barrier round trips.
-    const int64_t tgt = (f32in || epilogue != EPI_STORE) ? kStageTargetFused : kStageTarget;
-    a.PS = (int)std::max<int64_t>(1, tgt / pack);
-    if (a.rpp == 1 && (a.PS & 1)) {
-        // row pairs: an even pack count per stage, so that no pair is cut short
-        if ((a.PS + 1) * pack <= tgt * 5 / 4) a.PS += 1;
-        else if (a.PS > 1) a.PS -= 1;
-    }
-    a.stage_bytes = (int)(a.PS * pack);
+    // Two stages, each half of the shared memory left beside the activations.
+    // Every consumer warp waits on every stage (a few hundred cycles per wait on
+    // this GPU) and a small stage leaves most warps without a row pair in it, so
+    // fewer, larger stages win even though the first one lands later; the bytes
+    // in flight (one stage, ~90 KB per SM) still cover the HBM latency.
     const int64_t xbytes = x_smem_bytes(m, in_dim);
     a.x_smem = (xbytes <= kXSmemMax || f32in) ? 1 : 0;
     const int64_t budget = (int64_t)(m == 1 ? kCtaSmem1 : kCtaSmem) - (a.x_smem ? xbytes : 0) - 1024;
+    const int64_t tgt = budget / 2;
+    a.PS = (int)std::max<int64_t>(1, tgt / pack);
+    if (a.rpp == 1 && (a.PS & 1) && a.PS > 1) a.PS -= 1;  // row pairs: an even pack count per stage
+    a.stage_bytes = (int)(a.PS * pack);
     int64_t ns = budget / a.stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns < 2) {

@@ -85,6 +85,8 @@ GEMV_CASES = [
     # >= 64 rows per CTA on 152 SMs: the multi-token row-pair path (token groups
     # of 2, 3, 4 with a ragged last group; CTAs with an odd row count)
     (10001, 512, 2), (10001, 1024, 3), (9999, 512, 6), (9729, 2048, 16),
+    # several laps of the stage ring per CTA (263 and 198 rows per CTA)
+    (40000, 4096, 1), (30001, 2048, 3),
 ]
 
 
