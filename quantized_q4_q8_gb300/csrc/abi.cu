@@ -516,11 +516,9 @@ size_t rz_attention_workspace_bytes(int64_t m, int32_t n_heads, int32_t n_kv_hea
 {
     if (m < 1 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1 || max_seq < 1) return 0;
     if (check_device() != RZ_OK) return 0;
-    const int chunk = attention_chunk_len(max_seq, n_kv_heads, (int)m);
-    const int n_chunks = (max_seq + chunk - 1) / chunk;
-    const size_t group = (size_t)(n_heads / n_kv_heads);
     auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
-    return a256((size_t)m * n_kv_heads * n_chunks * group * (head_dim + 2) * 4) + a256((size_t)m * n_kv_heads * 4);
+    return a256(attention_part_bytes(m, n_kv_heads, n_heads / n_kv_heads, head_dim, max_seq)) +
+           a256((size_t)m * n_kv_heads * 4);
 }
 
 rz_status rz_attention_decode(const float *q, const float *k, const float *v, int64_t ld_qkv,
@@ -559,10 +557,8 @@ rz_status rz_attention_decode(const float *q, const float *k, const float *v, in
     L.rope_mode = rope_mode;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const int chunk = attention_chunk_len(kv->max_seq, n_kv_heads, (int)m);
-    const int n_chunks = (kv->max_seq + chunk - 1) / chunk;
     float *part = reinterpret_cast<float *>(ws);
-    ws += a256((size_t)m * n_kv_heads * n_chunks * (n_heads / n_kv_heads) * (head_dim + 2) * 4);
+    ws += a256(attention_part_bytes(m, n_kv_heads, n_heads / n_kv_heads, head_dim, kv->max_seq));
     int *counters = reinterpret_cast<int *>(ws);
     AttnArgs a = make_attn_args(L, m, kd, positions, position, part, counters, q, k, v, ld_qkv, att,
                                 att_q8);

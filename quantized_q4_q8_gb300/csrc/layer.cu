@@ -94,8 +94,6 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int q_pad = (q_dim + 255) / 256 * 256;
     const int group = L.n_heads / L.n_kv_heads;
-    const int chunk = attention_chunk_len(max_seq, L.n_kv_heads, (int)m);
-    const int n_chunks = (max_seq + chunk - 1) / chunk;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         uint8_t *p = base ? base + off : nullptr;
@@ -105,8 +103,7 @@ static LayerWs layer_ws(const LayerDesc &L, int64_t m, int max_seq, uint8_t *bas
     w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
     w.x8 = take(q8_bytes(m, L.hidden_pad));
     w.qkv = reinterpret_cast<float *>(take((size_t)m * (q_dim + 2 * kv_dim) * 4));
-    w.part = reinterpret_cast<float *>(
-        take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4));
+    w.part = reinterpret_cast<float *>(take(attention_part_bytes(m, L.n_kv_heads, group, L.head_dim, max_seq)));
     w.a8 = take(q8_bytes(m, q_pad));
     w.res1 = reinterpret_cast<float *>(take((size_t)m * L.hidden_pad * 4));
     w.ffn = take(ffn_workspace_bytes(m, L.hidden_pad, L.inter));
@@ -131,7 +128,16 @@ AttnArgs make_attn_args(const LayerDesc &L, int64_t m, const KvDesc &kv, const i
     a.k = k;
     a.v = v;
     a.ld_qkv = ld_qkv;
-    a.rope_r = pow((double)L.rope_theta, -2.0 / (double)L.head_dim);
+    // r^i by binary powering of r = theta^(-2 / head_dim), in double precision
+    const double r = pow((double)L.rope_theta, -2.0 / (double)L.head_dim);
+    for (int i = 0; i < L.head_dim / 2 && i < 128; ++i) {
+        double f = 1.0, b = r;
+        for (int e = i; e; e >>= 1) {
+            if (e & 1) f *= b;
+            b *= b;
+        }
+        a.rope_f[i] = f;
+    }
     a.kc = kv.k;
     a.vc = kv.v;
     a.seq_stride = kv.seq_stride;
@@ -268,8 +274,6 @@ static LayerQ40Ws layer_q4_0_ws(const LayerQ40Desc &L, int64_t m, int max_seq, u
     LayerQ40Ws w{};
     const int q_dim = L.n_heads * L.head_dim, kv_dim = L.n_kv_heads * L.head_dim;
     const int group = L.n_heads / L.n_kv_heads;
-    const int chunk = attention_chunk_len(max_seq, L.n_kv_heads, (int)m);
-    const int n_chunks = (max_seq + chunk - 1) / chunk;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         uint8_t *p = base ? base + off : nullptr;
@@ -279,7 +283,7 @@ static LayerQ40Ws layer_q4_0_ws(const LayerQ40Desc &L, int64_t m, int max_seq, u
     w.counters = reinterpret_cast<int *>(take((size_t)m * L.n_kv_heads * 4));
     w.normed = take((size_t)m * L.hidden * 4);
     w.qkv = take((size_t)m * (q_dim + 2 * kv_dim) * 4);
-    w.part = take((size_t)m * L.n_kv_heads * n_chunks * group * (L.head_dim + 2) * 4);
+    w.part = take(attention_part_bytes(m, L.n_kv_heads, group, L.head_dim, max_seq));
     w.att = take((size_t)m * q_dim * 4);
     w.o = take((size_t)m * L.hidden * 4);
     w.res1 = take((size_t)m * L.hidden * 4);

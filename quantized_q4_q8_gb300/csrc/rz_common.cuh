@@ -22,6 +22,7 @@ enum DevErr : unsigned {
     DEV_TIMEOUT_GEMM = 0x108,   // a wait of the tensor-core many-token GEMM gave up
     DEV_TIMEOUT_DRAIN = 0x1ff,  // draining outstanding copies gave up
     DEV_BAD_POSITION = 0x201,   // a device-resident position outside [0, max_seq)
+    DEV_ATTN_GEOMETRY = 0x202,  // an attention work split outgrew its records or tables (skipped)
 };
 
 __device__ __forceinline__ void set_error(unsigned *err, unsigned code)

@@ -125,7 +125,7 @@ struct AttnArgs {
     CUtensorMap kmap, vmap;      // the caches as [m][max_seq][kv_dim] f32, boxes of one head x 64 rows
     const float *q, *k, *v;      // pre-RoPE projections of token t at + t * ld_qkv
     int64_t ld_qkv;
-    double rope_r;               // theta^(-2 / head_dim): pair i turns by position * rope_r^i
+    double rope_f[128];          // rope_f[i] = (theta^(-2 / head_dim))^i: pair i turns by position * rope_f[i]
     float *kc, *vc;              // caches: token t at + t * seq_stride, row p at + p * kv_dim
     int64_t seq_stride;
     int max_seq;
@@ -137,7 +137,11 @@ struct AttnArgs {
     int chunk_len, n_chunks;     // n_chunks covers max_seq (workspace layout)
     int launch_chunks;           // chunks launched: enough for the host position, else n_chunks
     int att_bufs;                // set by launch_attention: 1 = K then V through one buffer, 2 = both
-    float *part;                 // workspace: [m][n_kv_heads][n_chunks][group][head_dim + 2]
+    int stream_slots;            // set by launch_attention for the streaming kernel: tiles in flight per warp,
+    int stream_tab_tokens;       //   tokens whose RoPE angles a CTA tabulates,
+    int stream_kmax;             //   record slots per (token, kv head)
+    int stream_cluster;          //   CTAs per cluster of the cluster kernel
+    float *part;                 // workspace of attention_part_bytes: the partial records
     int *counters;               // workspace: [m][n_kv_heads], zero before the first call
     float *att;                  // f32 [m][q_dim] output, or nullptr
     void *att_q8;                // Q8_1 of m rows of q_pad (output), or nullptr
@@ -145,6 +149,8 @@ struct AttnArgs {
 };
 
 int attention_chunk_len(int max_seq, int n_kv_heads, int m);
+// Bytes of the partial-record workspace (AttnArgs::part) for either attention kernel.
+size_t attention_part_bytes(int64_t m, int n_kv_heads, int group, int head_dim, int max_seq);
 size_t attention_smem_bytes(int group, int head_dim, int chunk_len);
 // (table,) then split-sequence attention with RoPE, the KV append, the merge and
 // the Q8_1 of the output.

@@ -80,6 +80,13 @@ ATT_CASES = [
     # the Llama-7B head layout with several tokens at distinct positions
     (32, 32, 128, 1e4, 0, 1100, [1024, 3, 517, 0]),
     (32, 32, 128, 1e4, 0, 300, [5, 299, 64, 65, 0, 128, 200, 1, 7, 250, 33, 190, 2, 299, 100, 63]),
+    # dispatch: more (token, kv head) segments than SMs (the flat tiled kernel);
+    # two tokens in clusters of CTAs per segment; 16 query heads per kv head and
+    # head_dim 256 (the chunk kernel)
+    (32, 32, 128, 1e4, 0, 200, [5, 199, 64, 0, 100, 150]),
+    (16, 16, 128, 1e4, 0, 700, [650, 11]),
+    (32, 2, 64, 1e4, 1, 600, [555]),
+    (4, 2, 256, 1e4, 0, 300, [200]),
 ]
 
 
