@@ -396,10 +396,14 @@ class StackWorkload:
         sh, m = self.shape, self.m
         W = {nm: o * (i // 256) * S.Q4K_BYTES for nm, (o, i) in sh.weight_shapes().items()}
         hp, q, kv, inter = sh.hidden_pad, sh.q_dim, sh.kv_dim, sh.inter
-        qkv = W["wq"] + W["wk"] + W["wv"] + m * hp * 4 + sh.hidden * 4 + m * (q + 2 * kv) * 4
+        # input of the norm-fed GEMVs: the f32 row and gamma (normalised inside), or
+        # from four tokens on the Q8_1 written by the separate norm / quantise launch
+        x_in = m * hp * 4 + sh.hidden * 4 if m < 4 else m * hp * 5 // 4
+        h_in = m * inter * 4 if m < 4 else m * inter * 5 // 4
+        qkv = W["wq"] + W["wk"] + W["wv"] + x_in + m * (q + 2 * kv) * 4
         o = W["wo"] + m * sh.q_pad * 5 // 4 + 2 * m * hp * 4
-        gu = W["wgate"] + W["wup"] + m * hp * 4 + sh.hidden * 4 + m * inter * 4
-        dn = W["wdown"] + m * inter * 4 + 2 * m * hp * 4
+        gu = W["wgate"] + W["wup"] + x_in + m * inter * 4
+        dn = W["wdown"] + h_in + 2 * m * hp * 4
         return self.n_layers * (qkv + o + gu + dn)
 
     def head_bytes(self):
@@ -466,9 +470,14 @@ class StackWorkload:
         n = self.n_layers * 4
         return {"kernel": self.gemv_kernel, "bytes_per_launch": self.fused_gemv_bytes() / n,
                 "launches_per_step": n,
-                "what": "the step's own four GEMV launches per layer (Q|K|V with the RMSNorm/Q8_1 "
-                        "prologue, O + residual, gate/up with the norm prologue and SiLU*up, down "
-                        "with the Q8_1 prologue + residual), all layers back to back in one graph"}
+                "what": ("the step's own four GEMV launches per layer (Q|K|V with the RMSNorm/Q8_1 "
+                         "prologue, O + residual, gate/up with the norm prologue and SiLU*up, down "
+                         "with the Q8_1 prologue + residual), all layers back to back in one graph"
+                         if self.m < 4 else
+                         "the step's own four GEMV launches per layer (Q|K|V, O + residual, gate/up with "
+                         "SiLU*up, down + residual) and the separate RMSNorm / Q8_1 launches that feed "
+                         "them at this batch, all layers back to back in one graph; the time of those "
+                         "small launches is counted into the GEMVs'")}
 
     def dominant_time(self, stream, reps=20):
         """Average launch duration of the dominant kernel inside the step: the four
@@ -487,13 +496,26 @@ class StackWorkload:
             self.g_out = torch.empty((m, sh.hidden_pad), dtype=torch.float32, device=dev)
             self.g_ws = rz.workspace(rz.swiglu_ffn_workspace_bytes(m, sh.hidden_pad, sh.inter), dev)
 
+            # from four tokens on the step quantises the normed input in a separate
+            # launch and feeds the GEMV Q8_1 (each CTA would stage the tokens one
+            # after another); the graph does what the step does
+            separate = m >= 4
+            self.g_x8 = torch.empty(rz.q8_1_size(m, sh.hidden_pad), dtype=torch.uint8, device=dev)
+
             def launch():
                 for dl in self.dls:
                     t = dl.t
-                    rz.rz_rmsnorm_q4k_gemv(self.g_in, sh.hidden_pad, t["attn_gamma"], sh.hidden, sh.eps,
-                                           [t["wq"], t["wk"], t["wv"]], [sh.q_dim, sh.kv_dim, sh.kv_dim],
-                                           None, self.g_qkv, sh.q_dim + 2 * sh.kv_dim, m, sh.hidden_pad,
-                                           stream=stream)
+                    if separate:
+                        rz.rz_rmsnorm(self.g_in, t["attn_gamma"], None, self.g_x8, m, sh.hidden, sh.hidden_pad,
+                                      sh.eps, stream=stream)
+                        rz.rz_q4k_q8_gemv_multi(self.g_x8, [t["wq"], t["wk"], t["wv"]],
+                                                [sh.q_dim, sh.kv_dim, sh.kv_dim], None, self.g_qkv,
+                                                sh.q_dim + 2 * sh.kv_dim, m, sh.hidden_pad, stream=stream)
+                    else:
+                        rz.rz_rmsnorm_q4k_gemv(self.g_in, sh.hidden_pad, t["attn_gamma"], sh.hidden, sh.eps,
+                                               [t["wq"], t["wk"], t["wv"]], [sh.q_dim, sh.kv_dim, sh.kv_dim],
+                                               None, self.g_qkv, sh.q_dim + 2 * sh.kv_dim, m, sh.hidden_pad,
+                                               stream=stream)
                     rz.rz_q4k_q8_gemv_ex(t["wo"], self.g_a8, None, self.g_in, self.g_res, sh.hidden_pad, m,
                                          sh.hidden, sh.q_pad, stream=stream)
                     rz.swiglu_ffn(self.g_res, t["ffn_gamma"], t["wgate"], t["wup"], t["wdown"], sh.hidden,

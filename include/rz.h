@@ -167,6 +167,23 @@ rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, i
                               int64_t ldy, int64_t m, int64_t in_dim, rz_stream stream);
 
 /*
+ * rz_q4k_q8_gemv_multi -- up to three Q4_K GEMVs against one Q8_1 activation in one
+ * launch (the Q | K | V projections of transformer_layer_gpu_true_dp4a, realizar
+ * 0.8.5 src/cuda/executor/cached.rs, with the activation quantised beforehand, as
+ * a layer does from four tokens on):
+ *     y[t][off_k + r] = (W_k q8_t)_r (+ bias[k][r]),  off_k = rows[0] + ... + rows[k-1]
+ *   q8     Q8_1 of m rows of in_dim values (the layout of rz_q8_1_quantize), 16-byte aligned
+ *   w      host array of n_mats (1..3) device pointers to Q4_K [rows[k]][in_dim], 16-byte aligned
+ *   bias   host array of n_mats device pointers (each may be NULL), or NULL
+ *   y      f32 [m][ldy], ldy >= rows[0] + ... + rows[n_mats-1], 4-byte aligned
+ *   1 <= m <= RZ_MAX_BATCH, in_dim % 256 == 0.  The same results as one
+ *   rz_q4k_q8_gemv_ex per matrix.
+ */
+rz_status rz_q4k_q8_gemv_multi(const void *q8, int32_t n_mats, const void *const *w, const int64_t *rows,
+                               const float *const *bias, float *y, int64_t ldy, int64_t m, int64_t in_dim,
+                               rz_stream stream);
+
+/*
  * rz_q4k_f32_gemv -- y = W x (+ bias) for Q4_K weights and f32 activations, with no
  * Q8_1 quantisation of x (q4k_gemv_cached_async in transformer_layer_gpu_cached,
  * realizar 0.8.5 src/cuda/executor/cached.rs):
@@ -379,13 +396,13 @@ rz_status rz_decode_layer_q4_0(const float *input, const rz_layer_weights_q4_0 *
 
 /*
  * rz_decode_stack_launches -- the number of librz kernels one rz_decode_stack call
- * (with_head != 0) or one rz_decode_layers call (with_head == 0) launches for
- * these layers, batch m and cache length max_seq.  Memset nodes are not kernels
- * and are not counted.
+ * (with_head != 0, an LM head of `vocab` rows) or one rz_decode_layers call
+ * (with_head == 0, vocab unused) launches for these layers, batch m and cache
+ * length max_seq.  Memset nodes are not kernels and are not counted.
  * Returns 0 for arguments the calls would reject.
  */
 int32_t rz_decode_stack_launches(const rz_layer_weights *layers, int32_t n_layers, int64_t m, int32_t max_seq,
-                                 int32_t with_head);
+                                 int32_t with_head, int64_t vocab);
 
 /*
  * rz_swiglu_ffn_static -- the same computation as rz_swiglu_ffn, for callers that

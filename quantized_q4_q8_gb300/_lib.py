@@ -74,6 +74,8 @@ SIGNATURES = {
     "rz_q4k_q8_gemv_ex": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp],
     "rz_q4k_q8_gemm_workspace_bytes": [_i64, _i64],
     "rz_q4k_q8_gemm": [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp],
+    "rz_q4k_q8_gemv_multi": [_vp, _i32, C.POINTER(_vp), C.POINTER(_i64), C.POINTER(_vp), _vp, _i64, _i64,
+                             _i64, _vp],
     "rz_rmsnorm_q4k_gemv": [_vp, _i64, _vp, _i64, _f32, _i32, C.POINTER(_vp), C.POINTER(_i64),
                             C.POINTER(_vp), _vp, _i64, _i64, _i64, _vp],
     "rz_q4_0_gemv": [_vp, _vp, _vp, _i64, _i64, _i64, _vp],
@@ -95,7 +97,7 @@ SIGNATURES = {
     "rz_decode_layer_q4_0_workspace_bytes": [_LQP, _i64, _i32],
     "rz_decode_layer_q4_0": [_vp, _LQP, _KVP, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
     "rz_decode_layers": [_vp, _LWP, _KVP, _i32, _vp, _i32, _i64, _vp, _vp, _sz, _vp],
-    "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32],
+    "rz_decode_stack_launches": [_LWP, _i32, _i64, _i32, _i32, _i64],
     "rz_check_device_error": [_vp, C.POINTER(C.c_uint32)],
     "rz_set_pdl": [C.c_int],
     "rz_debug_stall_next_gemv": [C.c_uint32],

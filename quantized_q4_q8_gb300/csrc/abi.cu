@@ -274,6 +274,40 @@ rz_status rz_rmsnorm_q4k_gemv(const float *x, int64_t ldx, const float *gamma, i
     return RZ_OK;
 }
 
+rz_status rz_q4k_q8_gemv_multi(const void *q8, int32_t n_mats, const void *const *w, const int64_t *rows,
+                               const float *const *bias, float *y, int64_t ldy, int64_t m, int64_t in_dim,
+                               rz_stream stream)
+{
+    const char *fn = "rz_q4k_q8_gemv_multi";
+    t_last_error.clear();
+    if (!q8 || !w || !rows || !y) return fail(RZ_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (n_mats < 1 || n_mats > 3) return fail(RZ_ERR_INVALID_ARG, "%s: n_mats=%d not in [1, 3]", fn, n_mats);
+    if (m < 1 || m > RZ_MAX_BATCH) return fail(RZ_ERR_SHAPE, "%s: m=%lld", fn, (long long)m);
+    if (in_dim < 256 || in_dim % 256) return fail(RZ_ERR_SHAPE, "%s: in_dim=%lld is not a multiple of 256", fn,
+                                                  (long long)in_dim);
+    int64_t total = 0;
+    Q4kSegment seg[3];
+    for (int k = 0; k < n_mats; ++k) {
+        if (!w[k] || rows[k] < 1) return fail(RZ_ERR_INVALID_ARG, "%s: matrix %d", fn, k);
+        if (!aligned16(w[k])) return fail(RZ_ERR_ALIGN, "%s: weights must be 16-byte aligned", fn);
+        const float *b = bias ? bias[k] : nullptr;
+        if (b && (reinterpret_cast<uintptr_t>(b) & 3u)) return fail(RZ_ERR_ALIGN, "%s: bias alignment", fn);
+        seg[k] = Q4kSegment{w[k], y + total, nullptr, rows[k], ldy, 0, b};
+        total += rows[k];
+    }
+    if (ldy < total) return fail(RZ_ERR_SHAPE, "%s: ldy=%lld < the %lld rows of the matrices", fn, (long long)ldy,
+                                 (long long)total);
+    if (!aligned16(q8) || (reinterpret_cast<uintptr_t>(y) & 3u))
+        return fail(RZ_ERR_ALIGN, "%s: q8 must be 16-byte aligned, y 4-byte aligned", fn);
+    RZ_TRY(check_device());
+    if (!q4k_gemv_supported(m, in_dim, EPI_STORE))
+        return fail(RZ_ERR_UNSUPPORTED, "%s: in_dim=%lld with m=%lld does not fit the stage ring", fn,
+                    (long long)in_dim, (long long)m);
+    RZ_CUDA(launch_q4k_gemv(seg, n_mats, EPI_STORE, q8, m, in_dim, static_cast<cudaStream_t>(stream)),
+            "rz_q4k_q8_gemv_multi launch");
+    return RZ_OK;
+}
+
 rz_status rz_q4k_f32_gemv(const void *w, const float *x, const float *bias, float *y, int64_t m, int64_t out_dim,
                           int64_t in_dim, rz_stream stream)
 {
@@ -724,14 +758,14 @@ rz_status rz_decode_layer_q4_0(const float *input, const rz_layer_weights_q4_0 *
 }
 
 int32_t rz_decode_stack_launches(const rz_layer_weights *layers, int32_t n_layers, int64_t m, int32_t max_seq,
-                                 int32_t with_head)
+                                 int32_t with_head, int64_t vocab)
 {
-    if (!layers || n_layers < 1 || n_layers > 4096 || max_seq < 1) return 0;
+    if (!layers || n_layers < 1 || n_layers > 4096 || max_seq < 1 || (with_head && vocab < 1)) return 0;
     std::vector<LayerDesc> Ls((size_t)n_layers);
     for (int l = 0; l < n_layers; ++l)
         if (check_layer(&layers[l], "rz_decode_stack_launches", m, &Ls[l]) != RZ_OK) return 0;
     if (check_device() != RZ_OK) return 0;
-    return stack_kernel_launches(Ls.data(), n_layers, m, max_seq, with_head != 0);
+    return stack_kernel_launches(Ls.data(), n_layers, m, max_seq, with_head != 0, vocab);
 }
 
 }  // extern "C"

@@ -369,31 +369,40 @@ __global__ void __launch_bounds__(kRThreads, 1) q4_0_gemv_ring_kernel(const RArg
     }
 }
 
-// One token through the ring kernel, when the shapes allow it (else false).
-cudaError_t launch_ring(const void *w, const float *x, float *y, int64_t out_dim, int64_t in_dim, const float *bias,
-                        cudaStream_t s, bool *used)
+// The ring kernel's geometry for these shapes; false when they do not suit it.
+bool ring_plan(int64_t out_dim, int64_t in_dim, RArgs &a, int64_t &grid, size_t &smem)
 {
-    *used = false;
-    RArgs a = {};
+    a = RArgs{};
     a.nb = (int)(in_dim / 32);
     a.cw = (a.nb + 31) / 32;
-    if (a.cw > kRW || kRW % a.cw) return cudaSuccess;
+    if (a.cw > kRW || kRW % a.cw) return false;
     a.rg = kRW / a.cw;
     a.row_bytes = (int64_t)a.nb * 18;
     int g = 16;
     while (a.row_bytes % g) g >>= 1;
     a.unit = 16 / g;  // rows whose bytes are a multiple of 16
-    if ((out_dim * a.row_bytes) % 16) return cudaSuccess;
+    if ((out_dim * a.row_bytes) % 16) return false;
     a.units = (out_dim + a.unit - 1) / a.unit;
     const int64_t per_stage = std::max<int64_t>(1, kStageBytes / (a.row_bytes * a.unit));
     a.stage_rows = (int)(per_stage * a.unit);
     const int64_t stage_bytes = (int64_t)a.stage_rows * a.row_bytes;
     a.NS = (int)std::min<int64_t>(32, kRingBytes / stage_bytes);
-    if (a.NS < 2) return cudaSuccess;
-    const int64_t grid = std::min<int64_t>(dev_info().sm_count, a.units);
+    if (a.NS < 2) return false;
+    grid = std::min<int64_t>(dev_info().sm_count, a.units);
     a.rows_max = ((a.units + grid - 1) / grid) * a.unit;
-    const size_t smem = (size_t)(a.NS * stage_bytes) + (size_t)a.rows_max * a.cw * 4 + 8 + 16 * (size_t)a.NS;
-    if (smem > dev_info().smem_optin) return cudaSuccess;
+    smem = (size_t)(a.NS * stage_bytes) + (size_t)a.rows_max * a.cw * 4 + 8 + 16 * (size_t)a.NS;
+    return smem <= dev_info().smem_optin;
+}
+
+// One token through the ring kernel, when the shapes allow it (else *used = false).
+cudaError_t launch_ring(const void *w, const float *x, float *y, int64_t out_dim, int64_t in_dim, const float *bias,
+                        cudaStream_t s, bool *used)
+{
+    *used = false;
+    RArgs a;
+    int64_t grid;
+    size_t smem;
+    if (!ring_plan(out_dim, in_dim, a, grid, smem)) return cudaSuccess;
     a.w = static_cast<const uint8_t *>(w);
     a.x = x;
     a.y = y;
@@ -445,6 +454,14 @@ cudaError_t launch_t(const Args &a, int grid, size_t smem, cudaStream_t s)
 
 }  // namespace
 
+int q4_0_gemv_launches(int64_t m, int64_t out_dim, int64_t in_dim)
+{
+    RArgs a;
+    int64_t grid;
+    size_t smem;
+    return ring_plan(out_dim, in_dim, a, grid, smem) ? (int)m : 1;
+}
+
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                              int64_t in_dim, cudaStream_t s, const float *bias)
 {
@@ -454,9 +471,14 @@ cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m,
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
                                 int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias)
 {
-    if (m == 1) {
+    {
+        // the ring kernel, once per token: each launch streams the weights at the
+        // bandwidth the one-token kernel reaches, where the multi-token kernel
+        // below re-reads every block per token from the cache hierarchy
         bool used = false;
-        const cudaError_t e = launch_ring(w, x, y, out_dim, in_dim, bias, s, &used);
+        cudaError_t e = launch_ring(w, x, y, out_dim, in_dim, bias, s, &used);
+        for (int64_t t = 1; used && e == cudaSuccess && t < m; ++t)
+            e = launch_ring(w, x + t * ldx, y + t * out_dim, out_dim, in_dim, bias, s, &used);
         if (used || e != cudaSuccess) return e;
     }
     Args a = {};

@@ -590,6 +590,16 @@ bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)
     return x_smem_bytes(m, in_dim) <= kXSmemMax;
 }
 
+bool q4k_gemv_f32_input_preferred(int64_t m, int64_t in_dim)
+{
+    // Several tokens (the tensor-core kernel) would stage their input one token
+    // after another in every CTA, each token a round trip and a block reduction: at
+    // 16 tokens that was most of the launch (Q|K|V 54 us, down 2 x 37 us).  The
+    // separate norm / quantise kernels do all tokens at once, so from
+    // kMmaMinTokens on a layer passes the GEMV its input as Q8_1.
+    return m < kMmaMinTokens && q4k_gemv_f32_input_ok(m, in_dim);
+}
+
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
                                 int64_t m, int64_t in_dim, cudaStream_t s)
 {

@@ -51,7 +51,7 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
 
     cudaError_t e;
     Q4kSegment gu[2] = {{w_gate, h, nullptr, inter, inter, 0}, {w_up, nullptr, nullptr, inter, 0, 0}};
-    if (q4k_gemv_f32_input_ok(m, hidden_pad)) {
+    if (q4k_gemv_f32_input_preferred(m, hidden_pad)) {
         // RMSNorm -> Q8_1 inside the gate/up GEMV (every CTA normalises the input)
         e = launch_q4k_gemv_f32(gu, 2, EPI_SWIGLU, F32Input{x, hidden_pad, gamma, hidden, eps}, m, hidden_pad, s);
     } else {
@@ -63,7 +63,7 @@ cudaError_t launch_swiglu_ffn(const float *x, const float *gamma, const void *w_
     // out's padding [hidden, hidden_pad) is zeroed by the down GEMV itself (a
     // memset node would end the programmatic-dependent-launch chain)
     Q4kSegment dn = {w_down, out, x, hidden, hidden_pad, hidden_pad, nullptr, hidden_pad};
-    if (q4k_gemv_f32_input_ok(m, inter)) {
+    if (q4k_gemv_f32_input_preferred(m, inter)) {
         // Q8_1 of h inside the down GEMV
         e = launch_q4k_gemv_f32(&dn, 1, EPI_RESID, F32Input{h, inter, nullptr, 0, 0.0f}, m, inter, s);
     } else {
@@ -184,7 +184,7 @@ cudaError_t launch_decode_layer(const float *input, const LayerDesc &L, const Kv
         qkv[0].rows = ld_qkv;
         nseg = 1;
     }
-    if (q4k_gemv_f32_input_ok(m, L.hidden_pad)) {
+    if (q4k_gemv_f32_input_preferred(m, L.hidden_pad)) {
         // RMSNorm -> Q8_1 inside the Q|K|V GEMV
         e = launch_q4k_gemv_f32(qkv, nseg, EPI_STORE,
                                 F32Input{input, L.hidden_pad, L.attn_gamma, L.hidden, L.eps}, m, L.hidden_pad, s);
@@ -238,17 +238,18 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
     return launch_q4_0_gemv_ld(lm_head, normed, L0.hidden_pad, logits, m, vocab, L0.hidden, s, lm_bias);
 }
 
-int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head)
+int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head,
+                          int64_t vocab)
 {
     (void)max_seq;
     const LayerDesc &L0 = layers[0];
-    const int h = head ? 2 : 0;  // output RMSNorm, LM head
+    const int h = head ? 1 + q4_0_gemv_launches(m, vocab, L0.hidden) : 0;  // output RMSNorm, LM head
     const int q_pad = (L0.n_heads * L0.head_dim + 255) / 256 * 256;
     // a GEMV with its input normalised / quantised inside, or a separate kernel
     // for that and then the Q8_1-input GEMV
     auto gemv = [&](int64_t in_dim, int epi) {
         const int n = q4k_gemv_launch_count(m, in_dim, epi);
-        return q4k_gemv_f32_input_ok(m, in_dim) ? n : 1 + n;
+        return q4k_gemv_f32_input_preferred(m, in_dim) ? n : 1 + n;
     };
     int per_layer = 1 /* attention */ + q4k_gemv_launch_count(m, q_pad, EPI_RESID) /* O */;
     per_layer += gemv(L0.hidden_pad, EPI_STORE);   // RMSNorm -> Q|K|V

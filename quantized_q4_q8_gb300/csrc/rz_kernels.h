@@ -94,6 +94,9 @@ struct F32Input {
     float eps;
 };
 bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim);
+// Whether a layer should let the GEMV quantise its f32 input (else a separate
+// norm / quantise launch first).
+bool q4k_gemv_f32_input_preferred(int64_t m, int64_t in_dim);
 // launches one GEMV of m tokens takes (token groups when the activations exceed
 // shared memory)
 int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue);
@@ -158,6 +161,9 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- Q4_0 GEMV
 // bias (nullable) [out_dim] is added to every token's output row
+// Kernels one launch_q4_0_gemv call starts for these shapes (the one-token ring
+// kernel once per token, else one multi-token launch).
+int q4_0_gemv_launches(int64_t m, int64_t out_dim, int64_t in_dim);
 cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                              int64_t in_dim, cudaStream_t s, const float *bias = nullptr);
 // as above with activation row stride ldx (elements) between tokens
@@ -215,6 +221,8 @@ cudaError_t launch_decode_stack(const float *input, const LayerDesc *layers, int
                                 const float *out_gamma, const void *lm_head, const float *lm_bias, int64_t vocab,
                                 float *hidden_out, float *logits, void *workspace, cudaStream_t s);
 // kernels launched by one launch_decode_stack (with or without the head)
-int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head);
+// vocab: rows of the LM head (with head only)
+int stack_kernel_launches(const LayerDesc *layers, int n_layers, int64_t m, int max_seq, bool head,
+                          int64_t vocab);
 
 }  // namespace rz

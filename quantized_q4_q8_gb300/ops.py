@@ -9,6 +9,7 @@ __all__ = [
     "q8_1_size", "q4k_bytes", "q4_0_bytes",
     "rz_q8_1_quantize", "rz_q4k_q8_gemv", "rz_q4k_q8_subblock_dots", "rz_q4_0_gemv",
     "rz_q4k_q8_gemv_ex", "rz_rmsnorm_q4k_gemv", "q4k_q8_gemv_ex", "rmsnorm_q4k_gemv",
+    "rz_q4k_q8_gemv_multi", "q4k_q8_gemv_multi",
     "rz_q4k_f32_gemv", "q4k_f32_gemv",
     "rz_q4k_q8_gemm", "q4k_q8_gemm_workspace_bytes", "q4k_q8_gemm",
     "rz_rmsnorm", "rz_residual_add", "rz_check_device_error", "rz_set_pdl", "rz_debug_stall_next_gemv",
@@ -78,6 +79,24 @@ def rz_rmsnorm_q4k_gemv(x, ldx, gamma, n, eps, ws, rows, biases, y, ldy, m, in_d
     bp = None if biases is None else (C.c_void_p * k)(*[_ptr(b) for b in biases])
     return call("rz_rmsnorm_q4k_gemv", _ptr(x), ldx, _ptr(gamma), n, eps, k, wp, rp, bp, _ptr(y), ldy,
                 m, in_dim, _stream(stream))
+
+
+def rz_q4k_q8_gemv_multi(q8, ws, rows, biases, y, ldy, m, in_dim, stream=None):
+    """ws, rows, biases: sequences of equal length (1..3); biases may be None."""
+    k = len(ws)
+    wp = (C.c_void_p * k)(*[_ptr(t) for t in ws])
+    rp = (C.c_int64 * k)(*rows)
+    bp = None if biases is None else (C.c_void_p * k)(*[_ptr(b) for b in biases])
+    return call("rz_q4k_q8_gemv_multi", _ptr(q8), k, wp, rp, bp, _ptr(y), ldy, m, in_dim, _stream(stream))
+
+
+def q4k_q8_gemv_multi(q8, ws, rows, m, in_dim, biases=None, out=None, stream=None):
+    """GEMVs of 1..3 matrices against one Q8_1 activation; returns f32 [m, sum(rows)]."""
+    import torch
+    if out is None:
+        out = torch.empty((m, sum(rows)), dtype=torch.float32, device=q8.device)
+    rz_q4k_q8_gemv_multi(q8, ws, rows, biases, out, out.shape[-1], m, in_dim, stream)
+    return out
 
 
 def rz_q4k_f32_gemv(w, x, bias, y, m, out_dim, in_dim, stream=None):
@@ -389,7 +408,7 @@ class DeviceStack:
     def launches(self, m, with_head=True):
         """librz kernels one rz_decode_stack (or rz_decode_layers) call launches."""
         return load().rz_decode_stack_launches(self.lw, len(self.layers), m, self.kvs[0].max_seq,
-                                               1 if with_head else 0)
+                                               1 if with_head else 0, self.vocab)
 
 
 def rz_decode_stack(x, stack: "DeviceStack", positions, position, m, hidden_out, logits, ws,

@@ -139,9 +139,10 @@ def test_q4k_gemv_padding_invariance(rz):
 
 
 # ----------------------------------------------------------------------------- Q4_0
-# m = 1 runs on the bulk-copy ring kernel when a whole number of rows fills 16
-# bytes (896: two rows, column warps 1; 2048: 2; 4096: 4; 8192: 8; 16384: 16),
-# else (in_dim 32, 992) on the register kernel, like m > 1
+# Every token runs on the bulk-copy ring kernel (one launch per token) when a whole
+# number of rows fills 16 bytes and the column warps divide 16 (896: two rows,
+# column warps 1; 2048: 2; 4096: 4; 8192: 8; 16384: 16), else (in_dim 32, 992,
+# 9216) on the multi-token register kernel
 @pytest.mark.parametrize("out_dim,in_dim,m", [(100, 896, 1), (33, 4096, 1), (7, 32, 1),
                                               (50, 1000 // 32 * 32, 1), (64, 8192, 1),
                                               (102, 2048, 1), (30, 16384, 1), (998, 896, 1),

@@ -73,6 +73,29 @@ def test_rmsnorm_qkv_fused_launch(rz, m):
         off += r
 
 
+@pytest.mark.parametrize("m", [1, 5, 16])
+def test_q8_gemv_multi_matches_single_gemvs(rz, m):
+    """Three matrices against one Q8_1 activation in one launch (how a layer runs
+    Q|K|V from four tokens on), a bias on K only: each matrix's rows against the
+    oracle's GEMV of the same Q8_1 codes, at the GEMV bar."""
+    sh = S.QWEN2
+    L = S.layer(sh, "gmq")
+    x = S.normal(f"gmq.x.{m}", (m, sh.hidden_pad))
+    x8 = oracle.q8_1_quantize(x)
+    bk = S.normal("gmq.bk", sh.kv_dim)
+    rows = [sh.q_dim, sh.kv_dim, sh.kv_dim]
+    y = rz.q4k_q8_gemv_multi(to_dev(x8), [to_dev(L.w["wq"]), to_dev(L.w["wk"]), to_dev(L.w["wv"])], rows, m,
+                             sh.hidden_pad, biases=[None, to_dev(bk), None]).cpu().numpy()
+    check_no_device_error()
+    off = 0
+    for nm, r in zip(("wq", "wk", "wv"), rows):
+        ref = oracle.q4k_q8_gemv(L.w[nm], x8, m, r, sh.hidden_pad)
+        if nm == "wk":
+            ref = np.stack([oracle.residual_add(ref[t], bk) for t in range(m)])
+        assert_gemv_close(y[:, off:off + r], ref, row_norms_q4k(L.w[nm])[None, :], f"multi {nm} m={m}")
+        off += r
+
+
 # ----------------------------------------------------------------------------- QKV bias, fused layout
 @pytest.mark.parametrize("fused", [False, True])
 def test_decode_layer_qwen2_with_qkv_bias(rz, fused):
