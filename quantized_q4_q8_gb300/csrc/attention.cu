@@ -1134,7 +1134,6 @@ __global__ void __launch_bounds__(kSW * 32, 1) attention_cluster_kernel(const __
     float *tabs = sm + (size_t)kSW * NS * slot_f;
     uint64_t *bar0 = reinterpret_cast<uint64_t *>(tabs + hd);
     uint64_t *bars = bar0 + warp * NS;
-    pdl_launch_dependents();
     const bool early = a.positions == nullptr;  // as in the flat kernel
     if (!early) pdl_wait();
 
@@ -1186,6 +1185,10 @@ __global__ void __launch_bounds__(kSW * 32, 1) attention_cluster_kernel(const __
                                 }
                             });
     }
+    // The next kernel may start only now: its CTAs would take the SMs this grid
+    // leaves free and stream their weights against the K/V tiles (measured: the
+    // step 1.568 -> 1.531 ms with the trigger here rather than at the start).
+    pdl_launch_dependents();
     __syncthreads();  // the rings are idle: their space holds the partials now
     float *pacc = sm;                      // [kSW][G][hd] the warps' weighted values
     float *pml = pacc + kSW * G * hd;      // [kSW][G][2] their max and exp-sum
