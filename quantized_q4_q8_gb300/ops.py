@@ -134,7 +134,7 @@ def rz_check_device_error(stream=None):
 
 
 def rz_set_pdl(enable: bool):
-    return call("rz_set_pdl", "rz_debug_stall_next_gemv", 1 if enable else 0)
+    return call("rz_set_pdl", 1 if enable else 0)
 
 
 def rz_debug_stall_next_gemv(wait_limit: int):

@@ -137,6 +137,39 @@ def test_attention_decode_parity(rz, H, Hkv, hd, theta, mode, max_seq, positions
         assert np.array_equal(kc_after[t][mask], kc[t][mask])
 
 
+def test_results_identical_without_pdl(rz):
+    """Programmatic dependent launch changes only when kernels may start: a Qwen2
+    layer (the cluster attention kernel) and 6-token attention over 32 kv heads
+    (192 segments: the flat kernel) give the same bits with it switched off."""
+    sh = S.QWEN2
+    L = S.layer(sh, "pdl.l")
+    dl = dev_layer(rz, L)
+    x = to_dev(S.hidden_input("pdl.x", 1, sh.hidden, sh.hidden_pad))
+    kc, vc = S.kv_prefill(sh, "pdl.kv", 160, 77)
+    H, Hkv, hd, max_seq = 32, 32, 128, 200
+    positions = [5, 199, 64, 0, 100, 150]
+    ash = S.LayerShape(hidden=H * hd, inter=256, n_heads=H, n_kv_heads=Hkv, head_dim=hd, rope_theta=1e4,
+                       rope_mode=0)
+    akc, avc = S.kv_prefill(ash, "pdl.att", max_seq, max(positions), len(positions))
+    qkv = to_dev(S.normal("pdl.qkv", (len(positions), (H + 2 * Hkv) * hd)))
+    pos_d = to_dev(np.array(positions, np.int32))
+    runs = []
+    try:
+        for pdl in (True, False):
+            rz.set_pdl(pdl)
+            kv = rz.DeviceKV(to_dev(kc), to_dev(vc))
+            out = rz.decode_layer(x, dl, kv, position=77).cpu().numpy()
+            akv = rz.DeviceKV(to_dev(akc), to_dev(avc))
+            att, a8 = rz.attention_decode(qkv, qkv[:, H * hd:], qkv[:, (H + Hkv) * hd:], (H + 2 * Hkv) * hd, akv,
+                                          H, Hkv, hd, 1e4, 0, positions=pos_d)
+            check_no_device_error()
+            runs.append((out, kv.k.cpu().numpy(), att.cpu().numpy(), a8.cpu().numpy(), akv.k.cpu().numpy()))
+    finally:
+        rz.set_pdl(True)
+    for a, b in zip(*runs):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
 def test_attention_first_token_is_v(rz):
     """Position 0: every query head returns the value of its kv head (the first-token
     case of forward_single_full_cuda_with_cache), to f32 rounding of the weights."""
