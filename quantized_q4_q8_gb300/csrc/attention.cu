@@ -136,7 +136,7 @@ __device__ __forceinline__ void write_outputs(const AttnArgs &a, int t, int kvh,
             const float v = outv[b * 32 + lane];
             const float amax = warp_max(fabsf(v));
             const float dq = __fdiv_rn(amax, 127.0f);
-            const int qi = q8_code(v, dq, rcp_approx(dq));
+            const int qi = q8_code(v, q8_scale(dq));
             const int sum = warp_sum_int(qi);
             const int64_t blk = (col0 / 32) + b;
             q[(int64_t)t * a.q_pad + blk * 32 + lane] = (int8_t)qi;

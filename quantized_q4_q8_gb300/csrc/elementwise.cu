@@ -25,7 +25,7 @@ __device__ __forceinline__ void q8_block_store(float v, int lane, int8_t *q, flo
 {
     const float amax = warp_max(fabsf(v));
     const float d = __fdiv_rn(amax, 127.0f);
-    const int qi = q8_code(v, d, rcp_approx(d));
+    const int qi = q8_code(v, q8_scale(d));
     const int sum = warp_sum_int(qi);
     q[lane] = (int8_t)qi;
     if (lane == 0) {

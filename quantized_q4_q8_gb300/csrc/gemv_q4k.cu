@@ -188,10 +188,10 @@ __global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args
     }
 
     // ---------------------------------------------------------------- consumers
-    pdl_wait();  // activations and the output buffers belong to the previous kernel
-    if (a.zy && blockIdx.x == gridDim.x - 1)
-        for (int64_t i = threadIdx.x; i < (int64_t)a.m * a.zy_cnt; i += kConsumerWarps * 32)
-            a.zy[(i / a.zy_cnt) * a.zy_ld + a.zy_from + i % a.zy_cnt] = 0.0f;
+    // activations and the output buffers belong to the previous kernel: wait for
+    // it (inside the f32 staging, after its loads of the weights it needs)
+    constexpr bool kF32Stage = XS && XIN != XIN_Q8;
+    if (!kF32Stage) pdl_wait();
     XSrc x;
     x.in_dim = a.in_dim;
     x.nb = a.in_dim / 32;
@@ -207,8 +207,11 @@ __global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args
         // the padded slot layout
         float *red = reinterpret_cast<float *>(full) - 24;  // 17 floats below the barriers
         stage_x_f32<false, XIN == XIN_NORM, kConsumerWarps>(xsm, a.xf, a.ldxf, a.gamma, a.norm_n, a.eps, a.m,
-                                                            a.in_dim, red, warp, lane, csync);
+                                                            a.in_dim, red, warp, lane, csync, [] { pdl_wait(); });
     }
+    if (a.zy && blockIdx.x == gridDim.x - 1)
+        for (int64_t i = threadIdx.x; i < (int64_t)a.m * a.zy_cnt; i += kConsumerWarps * 32)
+            a.zy[(i / a.zy_cnt) * a.zy_ld + a.zy_from + i % a.zy_cnt] = 0.0f;
     if (XS) {
         const int64_t nsbx = (int64_t)a.m * (a.in_dim / 256);
         x.q = smem_u32(xsm);

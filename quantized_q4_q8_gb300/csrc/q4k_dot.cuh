@@ -442,34 +442,49 @@ struct SlotStore {
     }
 };
 
-template <bool CG, bool NORM, int KF, int NW, typename Store, typename Sync>
+struct NoWait {
+    __device__ void operator()() const {}
+};
+
+template <bool CG, bool NORM, int KF, int NW, typename Store, typename Sync, typename PreWait>
 __device__ __forceinline__ void stage_x_f32_kf(const Store &st, const float *xf, int64_t ldx, const float *gamma,
                                                int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
-                                               int warp, int lane, Sync sync)
+                                               int warp, int lane, Sync sync, PreWait prewait)
 {
     constexpr int NT = 32 * NW;
     const int64_t n4 = in_dim / 4;
     const int tid = warp * 32 + lane;
+    auto load_gamma = [&](int64_t f) {
+        // gamma holds norm_n values (not padded): no read past them
+        const int64_t i0 = f * 4;
+        float4 g;
+        if (i0 + 3 < norm_n) {
+            g = __ldg(reinterpret_cast<const float4 *>(gamma) + f);
+        } else {
+            g.x = i0 < norm_n ? __ldg(gamma + i0) : 0.f;
+            g.y = i0 + 1 < norm_n ? __ldg(gamma + i0 + 1) : 0.f;
+            g.z = i0 + 2 < norm_n ? __ldg(gamma + i0 + 2) : 0.f;
+            g.w = 0.f;
+        }
+        return g;
+    };
+    // Short rows keep their gammas in registers, loaded once for every token and
+    // before `prewait` (the wait on the kernel that writes xf: gamma is a weight,
+    // and read cold it would otherwise arrive from HBM behind the weight stream
+    // after the values); long rows fetch them after the reduction.
+    constexpr bool kEarly = NORM && KF <= 4;
+    float4 gm[kEarly ? KF : 1];
+    if constexpr (kEarly) {
+#pragma unroll
+        for (int k = 0; k < KF; ++k) {
+            const int64_t f = (int64_t)k * NT + tid;
+            gm[k] = f < n4 ? load_gamma(f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    prewait();
     for (int t = 0; t < m; ++t) {
         const float4 *xrow = reinterpret_cast<const float4 *>(xf + t * ldx);
-        // gammas ride along with the values for short rows; for long rows they
-        // are fetched after the reduction (registers)
-        constexpr bool kEarly = NORM && KF <= 4;
-        auto load_gamma = [&](int64_t f) {
-            // gamma holds norm_n values (not padded): no read past them
-            const int64_t i0 = f * 4;
-            float4 g;
-            if (i0 + 3 < norm_n) {
-                g = __ldg(reinterpret_cast<const float4 *>(gamma) + f);
-            } else {
-                g.x = i0 < norm_n ? __ldg(gamma + i0) : 0.f;
-                g.y = i0 + 1 < norm_n ? __ldg(gamma + i0 + 1) : 0.f;
-                g.z = i0 + 2 < norm_n ? __ldg(gamma + i0 + 2) : 0.f;
-                g.w = 0.f;
-            }
-            return g;
-        };
-        float4 v[KF], gm[kEarly ? KF : 1];
+        float4 v[KF];
 #pragma unroll
         for (int k = 0; k < KF; ++k) {
             const int64_t f = (int64_t)k * NT + tid;  // validity is uniform over a warp
@@ -478,10 +493,8 @@ __device__ __forceinline__ void stage_x_f32_kf(const Store &st, const float *xf,
                     v[k] = __ldcg(xrow + f);
                 else
                     v[k] = __ldg(xrow + f);
-                if constexpr (kEarly) gm[k] = load_gamma(f);
             } else {
                 v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (kEarly) gm[k] = v[k];
             }
         }
         if constexpr (NORM) {
@@ -532,9 +545,9 @@ __device__ __forceinline__ void stage_x_f32_kf(const Store &st, const float *xf,
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
             am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
             const float d = __fdiv_rn(am, 127.0f);
-            const float rd = rcp_approx(d);
-            const int q0 = q8_code(v[k].x, d, rd), q1 = q8_code(v[k].y, d, rd);
-            const int q2 = q8_code(v[k].z, d, rd), q3 = q8_code(v[k].w, d, rd);
+            const Q8Scale sc = q8_scale(d);
+            const int q0 = q8_code(v[k].x, sc), q1 = q8_code(v[k].y, sc);
+            const int q2 = q8_code(v[k].z, sc), q3 = q8_code(v[k].w, sc);
             int sum = q0 + q1 + q2 + q3;
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -551,28 +564,29 @@ __device__ __forceinline__ void stage_x_f32_kf(const Store &st, const float *xf,
 }
 
 // Dispatch on the float4s per thread the row needs (rows up to 16384 values:
-// 16 warps x 8 float4s, or 8 warps x 16).
-template <bool CG, bool NORM, int NW = kRowWarps, typename Store, typename Sync>
+// 16 warps x 8 float4s, or 8 warps x 16).  `prewait` runs once, after the loads
+// that do not depend on xf and before the first load of xf.
+template <bool CG, bool NORM, int NW = kRowWarps, typename Store, typename Sync, typename PreWait = NoWait>
 __device__ __forceinline__ void stage_x_f32_to(const Store &st, const float *xf, int64_t ldx, const float *gamma,
                                                int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
-                                               int warp, int lane, Sync sync)
+                                               int warp, int lane, Sync sync, PreWait prewait = PreWait())
 {
     const int64_t kf = (in_dim / 4 + 32 * NW - 1) / (32 * NW);
     if (kf <= 2)
-        stage_x_f32_kf<CG, NORM, 2, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+        stage_x_f32_kf<CG, NORM, 2, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync, prewait);
     else if (kf <= 4)
-        stage_x_f32_kf<CG, NORM, 4, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+        stage_x_f32_kf<CG, NORM, 4, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync, prewait);
     else if (kf <= 8 || NW >= 16)
-        stage_x_f32_kf<CG, NORM, 8, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+        stage_x_f32_kf<CG, NORM, 8, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync, prewait);
     else
-        stage_x_f32_kf<CG, NORM, 16, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+        stage_x_f32_kf<CG, NORM, 16, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync, prewait);
 }
 
 // The same into the padded-slot layout.
-template <bool CG, bool NORM, int NW = kRowWarps, typename Sync>
+template <bool CG, bool NORM, int NW = kRowWarps, typename Sync, typename PreWait = NoWait>
 __device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64_t ldx, const float *gamma,
                                             int64_t norm_n, float eps, int m, int64_t in_dim, float *red,
-                                            int warp, int lane, Sync sync)
+                                            int warp, int lane, Sync sync, PreWait prewait = PreWait())
 {
     SlotStore st;
     st.xsm = xsm;
@@ -580,7 +594,7 @@ __device__ __forceinline__ void stage_x_f32(uint8_t *xsm, const float *xf, int64
     st.nsb = in_dim / 256;
     st.dsm = reinterpret_cast<float *>(xsm + (int64_t)m * st.nsb * kXSlot);
     st.ssm = st.dsm + (int64_t)m * st.nb;
-    stage_x_f32_to<CG, NORM, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync);
+    stage_x_f32_to<CG, NORM, NW>(st, xf, ldx, gamma, norm_n, eps, m, in_dim, red, warp, lane, sync, prewait);
 }
 
 }  // namespace

@@ -224,17 +224,26 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// Q8_1 code of one value given its block scale d and rd, an approximation of
-// 1/d with relative error below 2^-21 (rcp_approx): round half away from zero of
-// the IEEE f32 quotient x / d, clamped to [-127, 127]; 0 when d == 0.
-// y = x * rd is within 127 (2^-21 + 2^-23) < 8e-5 of the IEEE quotient (|x / d| <=
-// 127 (1 + 2^-24) because d = max|x| / 127; the product and the quotient each
-// carry at most 2^-24 relative rounding error).  Round-half-away is constant
-// between consecutive half-integers, so when y lies more than 2^-10 away from
-// one -- |y - rint(y)| < 1/2 - 2^-10 -- rint(y) is the code (no tie is near); next
-// to a half-integer (and for a non-finite y) the quotient itself is formed
-// (out of line: rare) and decides.
-static __device__ __noinline__ float q8_exact_quotient(float x, float d) { return __fdiv_rn(x, d); }
+// Q8_1 code of one value of a block with scale d: round half away from zero of
+// the IEEE f32 quotient fl(x / d), clamped to [-127, 127]; 0 when d == 0 --
+// exactly, without a division and without a branch.
+//   y = |x| * rd (rd = rcp_approx(d), within 1 ulp of 1/d) lies within
+//   127 (2^-22 + 2^-24) < 8e-5 of fl(|x| / d), because d = max|x| / 127 bounds the
+//   quotient by 127 (1 + 2^-24).  So with k = floor(y) the code is k or k + 1 (the
+//   quotient lies in (k - 1e-4, k + 1 + 1e-4)), and it is k + 1 exactly when
+//   fl(|x| / d) >= h = k + 1/2.  Rounding is monotonic and h is a float whose last
+//   significand bit is 0, so that holds exactly when |x| / d >= m = h - ulp(h) / 2
+//   (at |x| / d == m the even neighbour, h, is chosen), i.e. when
+//   t = |x| - h d >= -u, u = ulp(h) / 2 * d = d 2^(E - 24), E = floor(log2 h).
+//   h d has at most 8 + 24 significant bits, so whenever t lies within a few u of
+//   -u it is a small multiple of the grid of |x| and h d and the fused
+//   multiply-add computes it exactly; further away its rounding cannot move it
+//   across -u.  u is d scaled by a power of two (exact).
+// Blocks with d < 2^-64 (1/d could overflow) scale x and d by 2^64 first: exact,
+// and the quotient is unchanged.  Non-finite values give +-127.
+// (An earlier form took rint(y) and formed the IEEE quotient out of line for the
+// values next to a half-integer; the call in the loop cost the activation staging
+// of a decode layer about 1.5 us, and an inline branch cost more.)
 
 __device__ __forceinline__ float rcp_approx(float d)
 {
@@ -243,23 +252,31 @@ __device__ __forceinline__ float rcp_approx(float d)
     return r;
 }
 
-__device__ __forceinline__ int q8_code(float x, float d, float rd)
+struct Q8Scale {
+    float ds, rds, s;  // d * s, rcp_approx(d * s), s = 2^64 when d < 2^-64 else 1
+    bool live;         // d != 0
+};
+
+__device__ __forceinline__ Q8Scale q8_scale(float d)
 {
-    if (d == 0.0f) return 0;
-    const float y = __fmul_rn(x, rd);
-    float r = rintf(y);
-    if (!(fabsf(y - r) < 0.4990234375f)) r = roundf(q8_exact_quotient(x, d));  // 1/2 - 2^-10; NaN too
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int>(r);
+    Q8Scale q;
+    q.live = d != 0.0f;
+    q.s = d < 0x1p-64f ? 0x1p64f : 1.0f;
+    q.ds = d * q.s;
+    q.rds = rcp_approx(q.ds);
+    return q;
 }
 
-// The same from the quotient alone (call sites that quantise one value per scale).
-__device__ __forceinline__ int q8_code(float x, float d)
+__device__ __forceinline__ int q8_code(float x, const Q8Scale &q)
 {
-    if (d == 0.0f) return 0;
-    float r = roundf(__fdiv_rn(x, d));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int>(r);
+    const float ax = fabsf(x) * q.s;
+    const float k = floorf(__fmul_rn(ax, q.rds));
+    const float h = k + 0.5f;
+    const float pw = __int_as_float((__float_as_int(h) & 0x7f800000) - (24 << 23));  // 2^(E - 24)
+    const float u = __fmul_rn(q.ds, pw);
+    const float t = __fmaf_rn(-h, q.ds, ax);
+    const float c = fminf(t >= -u ? k + 1.0f : k, 127.0f);
+    return q.live ? static_cast<int>(copysignf(c, x)) : 0;
 }
 
 // One activation row walked by 16 warps (512 threads): warp w owns the Q8_1

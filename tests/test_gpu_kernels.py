@@ -40,13 +40,17 @@ def test_q8_1_bit_exact(rz, m, n):
     assert np.array_equal(q8, oracle.q8_1_quantize(x))
 
 
-def test_q8_1_boundary_quotients_bit_exact(rz):
+@pytest.mark.parametrize("lo,hi", [(-2.0, 2.0), (-44.0, -36.0), (-37.5, -30.0), (30.0, 37.0)])
+def test_q8_1_boundary_quotients_bit_exact(rz, lo, hi):
     """Every element next to a rounding boundary of x / d ((k + 1/2) d, nudged by at
-    most an ulp): the kernels decide these with the IEEE quotient, as the format
-    does, so the codes still match the oracle bit for bit."""
+    most an ulp): the kernels decide these as the IEEE quotient does, as the
+    format does, so the codes still match the oracle bit for bit.  Block maxima
+    10^lo .. 10^hi: ordinary scales, subnormal maxima and scales (1/d beyond the
+    f32 range), scales near the top of the range."""
     g = np.random.default_rng(11)
     nblk = 4096
-    amax = g.uniform(0.01, 100, nblk).astype(np.float32)
+    amax = (10.0 ** g.uniform(lo, hi, nblk)).astype(np.float32)
+    amax = np.where(amax > 0, amax, np.float32(1e-45)).astype(np.float32)
     d = amax / np.float32(127)
     k = g.integers(-126, 126, (nblk, 31)).astype(np.float32)
     x = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
