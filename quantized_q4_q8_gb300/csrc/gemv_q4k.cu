@@ -14,11 +14,11 @@
 // of the CTA's rows into L2 up front was measured slower: it queues ahead of
 // the ring's own copies and of the activation loads.)  A stage
 // holds whole "packs" (one row, or 8/nsb rows when a row has fewer than 8
-// super-blocks); pack i goes to consumer warp i % 16.  Every consumer warp
+// super-blocks); pack i goes to consumer warp i % 15.  Every consumer warp
 // passes every stage in order -- waits for it, works its own packs in it,
 // releases the slot with one arrival -- so no warp can get a ring length ahead
 // of a stage that has not been filled (the parity waits stay unambiguous), and
-// a stage is refilled once all sixteen have passed it.  Within a pack each
+// a stage is refilled once all fifteen have passed it.  Within a pack each
 // group of 4 lanes takes a super-block (two at a time for independent work) and
 // each lane one 32-byte chunk of its quants (two sub-blocks: low and high
 // nibbles), so every 32-element integer dot completes inside one lane (dp4a of
@@ -42,9 +42,12 @@ namespace {
 // Consumer warps and shared-memory budget per CTA, for several tokens and for one
 // (a one-token CTA of 8 warps in <= 110 KB, two per SM so that the next kernel's
 // CTA streams its weights beside this one, measured slower: 9.8 us against 8.9
-// for 4096 x 14336, 2.32 ms against 1.71 for the decode step).
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumerWarps1 = 16;
+// for 4096 x 14336, 2.32 ms against 1.71 for the decode step).  15 consumer warps
+// and the producer make 16 warps, four per SM sub-partition, so that a thread may
+// hold 128 registers; with 16 consumers one sub-partition holds five warps and
+// the limit is 96 (the staging loops spilled there; decode step 1.491 -> 1.478 ms).
+constexpr int kConsumerWarps = 15;
+constexpr int kConsumerWarps1 = 15;
 constexpr int kCtaSmem = 200 * 1024;
 constexpr int kCtaSmem1 = 200 * 1024;
 __host__ __device__ constexpr int consumer_warps(int mt) { return mt == 1 ? kConsumerWarps1 : kConsumerWarps; }
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args
     const uint32_t ring_s = smem_u32(ring);
 
     // Every consumer warp passes every stage in order (waits for it, takes its own
-    // packs -- pack i goes to warp i % 16 -- and releases the slot once), so no
+    // packs -- pack i goes to warp i % 15 -- and releases the slot once), so no
     // warp can run a ring length ahead of a stage that is not filled yet and the
     // parity waits stay unambiguous.
     RingPos rp{0, 0u};
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args
         while (rot >= kConsumerWarps) rot -= kConsumerWarps;
         if (MT == 1 && XS && a.rpp == 1) {
             // rows in pairs: pair q of the stage (packs first + 2q, first + 2q + 1)
-            // goes to warp (pairs of earlier stages + q) % 16
+            // goes to warp (pairs of earlier stages + q) % 15
             const int npair = (end - first + 1) / 2;
             for (int q = q0; q < npair; q += kConsumerWarps) {
                 const int iA = first + 2 * q;

@@ -27,7 +27,7 @@
 // rows.  A producer warp streams stages through a ring with the tensor-memory-
 // access engine: a stage is one 2-D box of a TMA tensor map -- the CTA's rpc rows
 // over a slice of S super-blocks (S = 6, 2 or 1 so that the tiles x S units of a
-// stage fill at most the 16 consumer warps; for the SwiGLU pair one box of gate
+// stage fill at most the 15 consumer warps; for the SwiGLU pair one box of gate
 // rows and one of up rows) -- landing densely with a row pitch of S x 144 bytes
 // (864 and 288 are 96 and 32 mod 128: conflict-free fragment loads).  One tensor
 // copy per stage keeps the copy engine streaming; copies of single rows cost
@@ -51,7 +51,10 @@
 namespace rz {
 namespace {
 
-constexpr int kMW = 16;                    // consumer warps
+// 15 consumer warps and the producer make 16 warps, four per SM sub-partition:
+// a thread may hold 128 registers (with 16 consumers, five warps on one
+// sub-partition cap it at 96).
+constexpr int kMW = 15;                    // consumer warps
 constexpr int kMThreads = (kMW + 1) * 32;  // + 1 producer warp
 constexpr int kMSmem = 224 * 1024;         // shared-memory budget of a CTA
 constexpr int kMTile = 16;                 // rows per MMA tile
@@ -107,11 +110,11 @@ __host__ __device__ inline int64_t mma_x_bytes(int m, int64_t in_dim, int nt)
 __host__ __device__ inline int64_t mma_red_bytes(int nt) { return (int64_t)kMW * 32 * 4 * nt * 4; }
 // Super-blocks per stage for a CTA of `tiles` tiles (R halves): 6 or 2 (row
 // pitches conflict-free for the fragment loads), else 1, so that the units of a
-// stage, R x tiles x S, fit the 16 consumer warps.
+// stage, R x tiles x S, fit the consumer warps.
 __host__ __device__ inline int mma_slice_sb(int tiles, int R, int nsb)
 {
     const int u = R * tiles;
-    const int S = u <= 2 ? 6 : (u <= 8 ? 2 : 1);
+    const int S = 6 * u <= kMW ? 6 : (2 * u <= kMW ? 2 : 1);
     return S < nsb ? S : nsb;
 }
 __host__ __device__ inline int mma_half_bytes(int tiles, int S) { return (tiles * 16 * S * 144 + 127) / 128 * 128; }
@@ -641,7 +644,7 @@ MmaPlan mma_plan(const int64_t *rows, int nseg, int R, int nsb)
     for (int k = 0; k < nseg; ++k) {
         int64_t c = std::max<int64_t>(1, rows[k] * sms / U);
         int64_t rpc = (rows[k] + c - 1) / c;
-        const int64_t cap = 256 / R;  // R x tiles <= 16
+        const int64_t cap = 16 * (kMW / R);  // R x tiles <= kMW
         if (rpc > cap) rpc = cap;
         c = (rows[k] + rpc - 1) / rpc;
         p.cta_begin[k] = c0;
