@@ -46,12 +46,12 @@ namespace {
 // and the producer make 16 warps, four per SM sub-partition, so that a thread may
 // hold 128 registers; with 16 consumers one sub-partition holds five warps and
 // the limit is 96 (the staging loops spilled there; decode step 1.491 -> 1.478 ms).
+// One token on CTAs whose work splits better over 16 warps (16 packs of short
+// rows: the Qwen2-shaped gate/up, 26.9 -> 25.8 us per layer) takes a 16-warp
+// instantiation instead (nw_for below).
 constexpr int kConsumerWarps = 15;
-constexpr int kConsumerWarps1 = 15;
 constexpr int kCtaSmem = 200 * 1024;
 constexpr int kCtaSmem1 = 200 * 1024;
-__host__ __device__ constexpr int consumer_warps(int mt) { return mt == 1 ? kConsumerWarps1 : kConsumerWarps; }
-__host__ __device__ constexpr int cta_threads(int mt) { return (consumer_warps(mt) + 1) * 32; }
 constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
 constexpr int kMaxStages = 16;
 
@@ -103,10 +103,10 @@ __device__ __forceinline__ int seg_of(const Args &a, int64_t unit)
 
 // PR: several tokens with the rows in pairs (a separate instantiation, so that
 // its register allocation does not touch the one-row-per-warp path)
-template <int MT, int EPI, bool XS, int XIN, bool PR = false>
-__global__ void __launch_bounds__(cta_threads(MT), 1) q4k_gemv_kernel(const Args a)
+template <int MT, int EPI, bool XS, int XIN, bool PR, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) q4k_gemv_kernel(const Args a)
 {
-    constexpr int kConsumerWarps = consumer_warps(MT);
+    constexpr int kConsumerWarps = NW;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     uint8_t *xsm = smem + (int64_t)a.NS * a.stage_bytes;
@@ -359,14 +359,14 @@ size_t smem_bytes(const Args &a)
     return (size_t)a.NS * a.stage_bytes + (size_t)xbytes + 96 + 2 * 8 * (size_t)a.NS;
 }
 
-template <int MT, int EPI, bool XS, int XIN, bool PR = false>
+template <int MT, int EPI, bool XS, int XIN, bool PR, int NW>
 cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
 {
     static bool attr_done[64] = {};
     const int dev = dev_info().device;
     const size_t smem = smem_bytes(a);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS, XIN, PR>,
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_kernel<MT, EPI, XS, XIN, PR, NW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
@@ -374,7 +374,7 @@ cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(cta_threads(MT));
+    cfg.blockDim = dim3((NW + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -382,23 +382,33 @@ cudaError_t launch_t(const Args &a, int grid, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS, XIN, PR>, a);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_kernel<MT, EPI, XS, XIN, PR, NW>, a);
 }
 
-template <int MT, int EPI, bool PR>
+template <int MT, int EPI, bool PR, int NW = kConsumerWarps>
 cudaError_t launch_x(const Args &a, int grid, cudaStream_t s, int xin)
 {
     if (xin == XIN_NORM) {
-        if constexpr (EPI != EPI_RESID) return launch_t<MT, EPI, true, XIN_NORM, PR>(a, grid, s);
+        if constexpr (EPI != EPI_RESID) return launch_t<MT, EPI, true, XIN_NORM, PR, NW>(a, grid, s);
         return cudaErrorInvalidValue;
     }
     if (xin == XIN_F32) {
-        if constexpr (EPI == EPI_RESID) return launch_t<MT, EPI, true, XIN_F32, PR>(a, grid, s);
+        if constexpr (EPI == EPI_RESID) return launch_t<MT, EPI, true, XIN_F32, PR, NW>(a, grid, s);
         return cudaErrorInvalidValue;
     }
-    if (a.x_smem) return launch_t<MT, EPI, true, XIN_Q8, PR>(a, grid, s);
+    if (a.x_smem) return launch_t<MT, EPI, true, XIN_Q8, PR, NW>(a, grid, s);
     if constexpr (PR) return cudaErrorInvalidValue;  // the pair path wants the activations staged
-    return launch_t<MT, EPI, false, XIN_Q8>(a, grid, s);
+    return launch_t<MT, EPI, false, XIN_Q8, false, NW>(a, grid, s);
+}
+
+// Consumer warps of a one-token launch: 16 when a CTA's work -- row pairs, or
+// packs of short rows -- gives some warp one unit fewer than over 15 warps, else
+// 15 (more registers a thread).
+int nw_for(const Args &a, int grid)
+{
+    const int64_t rows = (a.units + grid - 1) / grid;
+    const int64_t work = a.rpp > 1 ? (rows + a.rpp - 1) / a.rpp : (rows + 1) / 2;
+    return (work + 15) / 16 < (work + 14) / 15 ? 16 : 15;
 }
 
 // One to three tokens (from kMmaMinTokens on, the tensor-core kernel of
@@ -408,8 +418,9 @@ template <int EPI>
 cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
 {
     static_assert(kMmaMinTokens <= 4, "the dp4a kernels cover fewer than four tokens");
-    const bool pr = a.m > 1 && a.rpp == 1 && a.x_smem && a.units / grid >= 4 * consumer_warps(a.m);
-    if (a.m <= 1) return launch_x<1, EPI, false>(a, grid, s, xin);
+    const bool pr = a.m > 1 && a.rpp == 1 && a.x_smem && a.units / grid >= 4 * kConsumerWarps;
+    if (a.m <= 1)
+        return nw_for(a, grid) == 16 ? launch_x<1, EPI, false, 16>(a, grid, s, xin) : launch_x<1, EPI, false>(a, grid, s, xin);
     if (a.m <= 2) return pr ? launch_x<2, EPI, true>(a, grid, s, xin) : launch_x<2, EPI, false>(a, grid, s, xin);
     if (a.m <= 4) return pr ? launch_x<4, EPI, true>(a, grid, s, xin) : launch_x<4, EPI, false>(a, grid, s, xin);
     return cudaErrorInvalidValue;
