@@ -36,10 +36,12 @@
 // whole row in registers with no synchronisation but the ring's.  At the end the
 // warps add their partials through shared memory in a fixed order
 // (deterministic) and run the epilogue (store, + bias, + residual, or
-// silu(gate) * up).  Activations are staged once per CTA: the int8 codes of
-// every token (offset binary, token pitch 32 mod 128), and per sub-block and lane
-// group the d8 and s of the four tokens that lane group's accumulator columns
-// hold.  Every wait is bounded.
+// silu(gate) * up).  Activations are staged once per CTA: the codes of every
+// token -- as f16 already in B-fragment order when that still leaves two ring
+// stages (Q8_1 input; the warps' partial sums then reuse the idle ring), else as
+// int8 in offset binary that every warp converts per fragment -- and per
+// sub-block and lane group the d8 and s of the four tokens that lane group's
+// accumulator columns hold.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -96,16 +98,20 @@ enum MXIn { MX_Q8 = 0, MX_NORM = 1, MX_F32 = 2 };
 //   spc    uint32 [in_dim / 256][T][4 lane groups][4]: s of sub-blocks 2i, 2i + 1
 //          of a token in three bf16 pieces (hi, mid, lo pairs; then 0), the B
 //          fragments of the min-term MMA
-__host__ __device__ inline int64_t mma_code_pitch(int64_t in_dim) { return in_dim + 32; }
-__host__ __device__ inline int64_t mma_codes_bytes(int m, int64_t in_dim)
+// Token pitch of the codes in bytes: int8 codes, or (xh) the codes as f16 in
+// B-fragment order (each group of eight x0..x7 stored as x0 x2 x1 x3 x4 x6 x5 x7,
+// so that a lane's two fragments of a sub-block are one 16-byte load); 32 and 64
+// mod 128, so that the 8 lanes of a load phase (two tokens) hit distinct banks.
+__host__ __device__ inline int64_t mma_code_pitch(int64_t in_dim, bool xh) { return xh ? 2 * in_dim + 64 : in_dim + 32; }
+__host__ __device__ inline int64_t mma_codes_bytes(int m, int64_t in_dim, bool xh)
 {
-    return ((int64_t)m * mma_code_pitch(in_dim) + 127) & ~int64_t(127);
+    return ((int64_t)m * mma_code_pitch(in_dim, xh) + 127) & ~int64_t(127);
 }
 __host__ __device__ inline int64_t mma_d8_bytes(int64_t in_dim, int nt) { return (in_dim / 32) * 4 * 2 * nt * 4; }
 __host__ __device__ inline int64_t mma_spc_bytes(int64_t in_dim, int nt) { return (in_dim / 256) * 8 * nt * 4 * 16; }
-__host__ __device__ inline int64_t mma_x_bytes(int m, int64_t in_dim, int nt)
+__host__ __device__ inline int64_t mma_x_bytes(int m, int64_t in_dim, int nt, bool xh)
 {
-    return mma_codes_bytes(m, in_dim) + mma_d8_bytes(in_dim, nt) + mma_spc_bytes(in_dim, nt);
+    return mma_codes_bytes(m, in_dim, xh) + mma_d8_bytes(in_dim, nt) + mma_spc_bytes(in_dim, nt);
 }
 __host__ __device__ inline int64_t mma_red_bytes(int nt) { return (int64_t)kMW * 32 * 4 * nt * 4; }
 // Super-blocks per stage for a CTA of `tiles` tiles (R halves): 6 or 2 (row
@@ -262,7 +268,7 @@ __device__ __forceinline__ uint32_t smem_after(uint32_t a)
 // 2i, 2i + 1 (+ 8 nt); e = 2, 3 row g + 8.  xrow: this lane's B-fragment row of
 // codes for n-tile 0 (and + xstep for n-tile 1) at this super-block; d8a, spa:
 // this lane's entries of the d8 table and the s pieces at this super-block.
-template <int NT>
+template <int NT, bool XH>
 __device__ __forceinline__ void mma_superblock(uint32_t blkA, uint32_t blkB, uint32_t xrow, uint32_t xstep,
                                                uint32_t d8a, uint32_t spa, int i, float (&acc)[NT][4])
 {
@@ -302,10 +308,17 @@ __device__ __forceinline__ void mma_superblock(uint32_t blkA, uint32_t blkB, uin
             a1[3] = hfma2u(lop_and_or(wBy8, mask, kF16x2_1024), fB.m, fB.c);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint2 X = lds_u2(xrow + nt * xstep + 32 * j);
                 float d[4];
-                mma16816(d, a0, code_pair(X.x), code_pair(X.x >> 8), zero);
-                mma16816(d, a1, code_pair(X.y), code_pair(X.y >> 8), d);
+                if constexpr (XH) {
+                    // both fragments of the sub-block, staged as f16 in fragment order
+                    const uint4 X = lds_u4(xrow + nt * xstep + 64 * j);
+                    mma16816(d, a0, X.x, X.y, zero);
+                    mma16816(d, a1, X.z, X.w, d);
+                } else {
+                    const uint2 X = lds_u2(xrow + nt * xstep + 32 * j);
+                    mma16816(d, a0, code_pair(X.x), code_pair(X.x >> 8), zero);
+                    mma16816(d, a1, code_pair(X.y), code_pair(X.y >> 8), d);
+                }
                 // d8 of tokens 2i, 2i + 1 (+ 8 nt)
                 const float2 v = lds_f2(d8a + (j * 4 * 2 * NT + 2 * nt) * 4);
                 tb[nt][0] = fmaf(d[0], v.x, tb[nt][0]);
@@ -375,19 +388,23 @@ struct MmaStore {
     }
 };
 
-template <int EPI, int XIN, int NT>
+template <int EPI, int XIN, int NT, bool XH>
 __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid_constant__ MArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int R = (EPI == EPI_SWIGLU) ? 2 : 1;
     uint8_t *ring = smem;
     uint8_t *xcodes = ring + (int64_t)a.NS * a.stage_bytes;
-    const int64_t cpitch = mma_code_pitch(a.in_dim);
-    float *d8t = reinterpret_cast<float *>(xcodes + mma_codes_bytes(a.m, a.in_dim));
+    static_assert(!XH || XIN == MX_Q8, "f16 activations are staged from Q8_1 input only");
+    const int64_t cpitch = mma_code_pitch(a.in_dim, XH);
+    float *d8t = reinterpret_cast<float *>(xcodes + mma_codes_bytes(a.m, a.in_dim, XH));
     uint32_t *spc = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(d8t) + mma_d8_bytes(a.in_dim, NT));
     const int64_t nb = a.in_dim / 32;
-    float *red = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(spc) + mma_spc_bytes(a.in_dim, NT));
-    float *nred = red + mma_red_bytes(NT) / 4;  // 32 floats: the norm reduction
+    // the partial sums of the warps: after the tables, or (XH) in the ring, idle
+    // by then (every consumer warp has waited for every stage it reads)
+    uint8_t *tables_end = reinterpret_cast<uint8_t *>(spc) + mma_spc_bytes(a.in_dim, NT);
+    float *red = XH ? reinterpret_cast<float *>(ring) : reinterpret_cast<float *>(tables_end);
+    float *nred = XH ? reinterpret_cast<float *>(tables_end) : red + mma_red_bytes(NT) / 4;  // 32 floats: the norm reduction
     uint64_t *full = reinterpret_cast<uint64_t *>(nred + 32);
     uint64_t *empty = full + a.NS;
 
@@ -482,9 +499,19 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
                 const int q = q0 + u * kMW * 32 + tid;
                 if (q < nq) {
                     const int t = q / n16;
-                    const int4 w = make_int4(v[u].x ^ 0x80808080, v[u].y ^ 0x80808080, v[u].z ^ 0x80808080,
-                                             v[u].w ^ 0x80808080);
-                    *reinterpret_cast<int4 *>(xcodes + t * cpitch + (int64_t)(q - t * n16) * 16) = w;
+                    const uint32_t w0 = (uint32_t)v[u].x ^ 0x80808080u, w1 = (uint32_t)v[u].y ^ 0x80808080u;
+                    const uint32_t w2 = (uint32_t)v[u].z ^ 0x80808080u, w3 = (uint32_t)v[u].w ^ 0x80808080u;
+                    if constexpr (XH) {
+                        // 16 codes -> two groups of eight f16 in fragment order
+                        uint8_t *dst = xcodes + t * cpitch + (int64_t)(q - t * n16) * 32;
+                        *reinterpret_cast<uint4 *>(dst) =
+                            make_uint4(code_pair(w0), code_pair(w0 >> 8), code_pair(w1), code_pair(w1 >> 8));
+                        *reinterpret_cast<uint4 *>(dst + 16) =
+                            make_uint4(code_pair(w2), code_pair(w2 >> 8), code_pair(w3), code_pair(w3 >> 8));
+                    } else {
+                        *reinterpret_cast<uint4 *>(xcodes + t * cpitch + (int64_t)(q - t * n16) * 16) =
+                            make_uint4(w0, w1, w2, w3);
+                    }
                 }
             }
         }
@@ -514,7 +541,7 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     // (token g, clamped into the staged tokens; n-tile 1 is xstep further), its
     // d8 entries and its s pieces
     const uint32_t ring_s = smem_u32(ring);
-    const uint32_t xrow0 = smem_u32(xcodes) + (uint32_t)(min(g, a.m - 1) * cpitch) + 8u * i;
+    const uint32_t xrow0 = smem_u32(xcodes) + (uint32_t)(min(g, a.m - 1) * cpitch) + (XH ? 16u : 8u) * i;
     const uint32_t xstep = (uint32_t)((min(g + 8, a.m - 1) - min(g, a.m - 1)) * cpitch);
     const uint32_t d8a0 = smem_u32(d8t) + (uint32_t)i * (2 * NT * 4);
     const uint32_t spa0 = smem_u32(spc) + (uint32_t)(g * 4 + i) * 16u;
@@ -544,7 +571,7 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
             const uint32_t t0 = base + (uint32_t)(s * a.stage_bytes + h * hs + (tl * kMTile) * pitch + js * 144);
             const int sbg = sl * S + js;
             const uint32_t off = base - ring_s;  // 0, carries the ordering to the other tables
-            mma_superblock<NT>(t0 + g * pitch, t0 + (g + 8) * pitch, xrow0 + off + (uint32_t)sbg * 256u, xstep,
+            mma_superblock<NT, XH>(t0 + g * pitch, t0 + (g + 8) * pitch, xrow0 + off + (uint32_t)sbg * (XH ? 512u : 256u), xstep,
                                d8a0 + off + (uint32_t)sbg * (8 * 4 * 2 * NT * 4),
                                spa0 + off + (uint32_t)sbg * (8 * NT * 4 * 16), i, acc);
         }
@@ -552,6 +579,7 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
         if (lane == 0 && !failed) mbar_arrive(&empty[s]);
     }
     // every unit done: partials -> fixed-order sums -> epilogue
+    if constexpr (XH) csync();  // the partials overwrite the ring: every warp is past its last stage
     float *rw = red + (warp * 32 + lane) * 4 * NT;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -580,18 +608,19 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     }
 }
 
-int64_t mma_smem_bytes(int m, int64_t in_dim, int nt, int NS, int stage_bytes)
+int64_t mma_smem_bytes(int m, int64_t in_dim, int nt, int NS, int stage_bytes, bool xh)
 {
-    return (int64_t)NS * stage_bytes + mma_x_bytes(m, in_dim, nt) + mma_red_bytes(nt) + 32 * 4 + 2 * 8 * NS;
+    return (int64_t)NS * stage_bytes + mma_x_bytes(m, in_dim, nt, xh) + (xh ? 0 : mma_red_bytes(nt)) + 32 * 4 +
+           2 * 8 * NS;
 }
 
-template <int EPI, int XIN, int NT>
+template <int EPI, int XIN, int NT, bool XH = false>
 cudaError_t mma_launch_t(const MArgs &a, int grid, cudaStream_t s, size_t smem)
 {
     static bool attr_done[64] = {};
     const int dev = dev_info().device;
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_mma_kernel<EPI, XIN, NT>,
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_mma_kernel<EPI, XIN, NT, XH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev_info().smem_optin);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
@@ -606,12 +635,13 @@ cudaError_t mma_launch_t(const MArgs &a, int grid, cudaStream_t s, size_t smem)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, q4k_gemv_mma_kernel<EPI, XIN, NT>, a);
+    return cudaLaunchKernelEx(&cfg, q4k_gemv_mma_kernel<EPI, XIN, NT, XH>, a);
 }
 
 template <int EPI, int NT>
-cudaError_t mma_launch_x(const MArgs &a, int grid, cudaStream_t s, size_t smem, int xin)
+cudaError_t mma_launch_x(const MArgs &a, int grid, cudaStream_t s, size_t smem, int xin, bool xh)
 {
+    if (xh) return xin == MX_Q8 ? mma_launch_t<EPI, MX_Q8, NT, true>(a, grid, s, smem) : cudaErrorInvalidValue;
     if (xin == MX_NORM) {
         if constexpr (EPI != EPI_RESID) return mma_launch_t<EPI, MX_NORM, NT>(a, grid, s, smem);
         return cudaErrorInvalidValue;
@@ -658,13 +688,15 @@ MmaPlan mma_plan(const int64_t *rows, int nseg, int R, int nsb)
     return p;
 }
 
-// Ring stages that fit next to the activations of mt tokens (0 if fewer than two).
-int mma_stages(int mt, int64_t in_dim, int stage_bytes)
+// Ring stages that fit next to the activations of mt tokens (0 if fewer than
+// two).  xh: the codes as f16, the partial sums in the ring (which must hold them).
+int mma_stages(int mt, int64_t in_dim, int stage_bytes, bool xh = false)
 {
     const int nt = mt > 8 ? 2 : 1;
-    const int64_t fixed = mma_x_bytes(mt, in_dim, nt) + mma_red_bytes(nt) + 32 * 4 + 1024;
+    const int64_t fixed = mma_x_bytes(mt, in_dim, nt, xh) + (xh ? 0 : mma_red_bytes(nt)) + 32 * 4 + 1024;
     const int64_t ns = ((int64_t)std::min<int64_t>(kMSmem, dev_info().smem_optin) - fixed) / (stage_bytes + 16);
-    return ns >= 2 ? (int)std::min<int64_t>(ns, 8) : 0;
+    if (ns < 2 || (xh && ns * stage_bytes < mma_red_bytes(nt))) return 0;
+    return (int)std::min<int64_t>(ns, 8);
 }
 
 // The largest ring slot any plan can need: R x the largest half over tile counts.
@@ -758,18 +790,21 @@ cudaError_t launch_q4k_gemv_mma(const Q4kSegment *seg, int nseg, int epilogue, c
     }
     a.stage_bytes = plan.stage_bytes;
     const int nt = m > 8 ? 2 : 1;
-    a.NS = mma_stages((int)m, in_dim, a.stage_bytes);
+    // Q8_1 input: the codes staged as f16 in fragment order when two stages still fit
+    // beside them (each warp then loads its B fragments instead of converting them)
+    const bool xh = !f32in && mma_stages((int)m, in_dim, a.stage_bytes, true) >= 2;
+    a.NS = mma_stages((int)m, in_dim, a.stage_bytes, xh);
     if (a.NS < 2) return cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)mma_smem_bytes((int)m, in_dim, nt, a.NS, a.stage_bytes);
+    const size_t smem = (size_t)mma_smem_bytes((int)m, in_dim, nt, a.NS, a.stage_bytes, xh);
     if (smem > dev_info().smem_optin) return cudaErrorInvalidConfiguration;
     const int grid = plan.cta_begin[nplan];
     switch (epilogue) {
-    case EPI_STORE: return nt == 1 ? mma_launch_x<EPI_STORE, 1>(a, grid, s, smem, xin)
-                                   : mma_launch_x<EPI_STORE, 2>(a, grid, s, smem, xin);
-    case EPI_RESID: return nt == 1 ? mma_launch_x<EPI_RESID, 1>(a, grid, s, smem, xin)
-                                   : mma_launch_x<EPI_RESID, 2>(a, grid, s, smem, xin);
-    default: return nt == 1 ? mma_launch_x<EPI_SWIGLU, 1>(a, grid, s, smem, xin)
-                            : mma_launch_x<EPI_SWIGLU, 2>(a, grid, s, smem, xin);
+    case EPI_STORE: return nt == 1 ? mma_launch_x<EPI_STORE, 1>(a, grid, s, smem, xin, xh)
+                                   : mma_launch_x<EPI_STORE, 2>(a, grid, s, smem, xin, xh);
+    case EPI_RESID: return nt == 1 ? mma_launch_x<EPI_RESID, 1>(a, grid, s, smem, xin, xh)
+                                   : mma_launch_x<EPI_RESID, 2>(a, grid, s, smem, xin, xh);
+    default: return nt == 1 ? mma_launch_x<EPI_SWIGLU, 1>(a, grid, s, smem, xin, xh)
+                            : mma_launch_x<EPI_SWIGLU, 2>(a, grid, s, smem, xin, xh);
     }
 }
 

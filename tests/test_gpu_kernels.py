@@ -91,6 +91,9 @@ GEMV_CASES = [
     (10001, 512, 2), (10001, 1024, 3), (9999, 512, 6), (9729, 2048, 16),
     # several laps of the stage ring per CTA (263 and 198 rows per CTA)
     (40000, 4096, 1), (30001, 2048, 3),
+    # 16 units per CTA on 152 SMs (16 row pairs; 16 packs of two short rows): the
+    # one-token launch takes its 16-warp instantiation
+    (4864, 2048, 1), (4800, 1024, 1),
 ]
 
 
