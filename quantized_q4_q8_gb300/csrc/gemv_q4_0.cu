@@ -459,6 +459,7 @@ int q4_0_gemv_launches(int64_t m, int64_t out_dim, int64_t in_dim)
     RArgs a;
     int64_t grid;
     size_t smem;
+    if (q4_0_head_mma_ok(m, out_dim, in_dim, nullptr, in_dim)) return q4_0_head_mma_launches(m);
     return ring_plan(out_dim, in_dim, a, grid, smem) ? (int)m : 1;
 }
 
@@ -471,6 +472,9 @@ cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m,
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
                                 int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias)
 {
+    // two or more tokens: the tensor-core kernel reads the weights once per eight
+    if (q4_0_head_mma_ok(m, out_dim, in_dim, x, ldx))
+        return launch_q4_0_head_mma(w, x, ldx, y, m, out_dim, in_dim, bias, s);
     {
         // the ring kernel, once per token: each launch streams the weights at the
         // bandwidth the one-token kernel reaches, where the multi-token kernel

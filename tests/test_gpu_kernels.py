@@ -146,14 +146,19 @@ def test_q4k_gemv_padding_invariance(rz):
 
 
 # ----------------------------------------------------------------------------- Q4_0
-# Every token runs on the bulk-copy ring kernel (one launch per token) when a whole
-# number of rows fills 16 bytes and the column warps divide 16 (896: two rows,
-# column warps 1; 2048: 2; 4096: 4; 8192: 8; 16384: 16), else (in_dim 32, 992,
-# 9216) on the multi-token register kernel
+# Two or more tokens with in_dim a multiple of 256 run on the tensor-core kernel
+# (token groups of at most eight; 17 rows: one row per CTA; 5000 x 512: ragged
+# last tile; 40000 x 256: 240 rows per CTA, 167 CTAs; 9 tokens: groups of 5 and
+# 4).  Otherwise every token runs on the bulk-copy ring kernel (one launch per
+# token) when a whole number of rows fills 16 bytes and the column warps divide 16
+# (896: two rows, column warps 1; 2048: 2; 4096: 4; 8192: 8; 16384: 16), else (in_dim
+# 32, 992) on the multi-token register kernel
 @pytest.mark.parametrize("out_dim,in_dim,m", [(100, 896, 1), (33, 4096, 1), (7, 32, 1),
                                               (50, 1000 // 32 * 32, 1), (64, 8192, 1),
                                               (102, 2048, 1), (30, 16384, 1), (998, 896, 1),
-                                              (40, 896, 3), (17, 4096, 16), (300, 9216, 2)])
+                                              (40, 896, 3), (17, 4096, 16), (300, 9216, 2),
+                                              (1000, 4096, 8), (5000, 512, 5), (40000, 256, 4),
+                                              (2048, 4096, 9), (64, 992, 4)])
 def test_q4_0_gemv_parity(rz, out_dim, in_dim, m):
     w = S.q4_0_weight(f"gq40.{out_dim}.{in_dim}", out_dim, in_dim)
     x = S.normal(f"gq40.x.{in_dim}.{m}", (m, in_dim))
@@ -163,11 +168,26 @@ def test_q4_0_gemv_parity(rz, out_dim, in_dim, m):
     assert_gemv_close(y, y_ref, row_norms_q4_0(w)[None, :], f"q4_0 {out_dim}x{in_dim} m={m}")
 
 
-@pytest.mark.parametrize("vocab,hidden", S.LM_HEADS)
-def test_q4_0_lm_head_full_size(rz, vocab, hidden):
-    """Both LM heads at full size; every logit against the oracle."""
+def test_q4_0_gemv_tensor_core_bias_and_range(rz):
+    """The tensor-core head with a bias, activations up to +-300 (the two f16
+    pieces still carry x to about 2^-22) and exact zeros."""
+    out_dim, in_dim, m = 3000, 1024, 6
+    w = S.q4_0_weight("gq40b.w", out_dim, in_dim)
+    x = (S.normal("gq40b.x", (m, in_dim)) * np.float32(100.0)).astype(np.float32)
+    x[1, :300] = 0.0
+    b = S.normal("gq40b.b", (out_dim,))
+    y = rz.q4_0_gemv(to_dev(w), to_dev(x), out_dim, in_dim, bias=to_dev(b)).cpu().numpy()
+    check_no_device_error()
+    y_ref = oracle.q4_0_gemv(w, x, out_dim, in_dim) + b[None, :].astype(np.float64)
+    assert_gemv_close(y, y_ref, row_norms_q4_0(w)[None, :] * np.abs(x).max(), "q4_0 + bias")
+
+
+@pytest.mark.parametrize("vocab,hidden,m", [(v, h, 1) for v, h in S.LM_HEADS] + [(32000, 4096, 16)])
+def test_q4_0_lm_head_full_size(rz, vocab, hidden, m):
+    """Both LM heads at full size, and the Llama head at 16 tokens (the
+    tensor-core kernel, two groups of eight); every logit against the oracle."""
     w = S.q4_0_weight(f"lm.{vocab}.{hidden}", vocab, hidden)
-    x = S.normal(f"lm.x.{hidden}", (1, hidden))
+    x = S.normal(f"lm.x.{hidden}.{m}" if m > 1 else f"lm.x.{hidden}", (m, hidden))
     y = rz.q4_0_gemv(to_dev(w), to_dev(x), vocab, hidden).cpu().numpy()
     check_no_device_error()
     y_ref = oracle.q4_0_gemv(w, x, vocab, hidden)
