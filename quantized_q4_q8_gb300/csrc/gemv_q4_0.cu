@@ -472,7 +472,9 @@ cudaError_t launch_q4_0_gemv(const void *w, const float *x, float *y, int64_t m,
 cudaError_t launch_q4_0_gemv_ld(const void *w, const float *x, int64_t ldx, float *y, int64_t m,
                                 int64_t out_dim, int64_t in_dim, cudaStream_t s, const float *bias)
 {
-    // two or more tokens: the tensor-core kernel reads the weights once per eight
+    // the tensor-core kernel (rows of a whole number of 144-byte slices): it reads
+    // the weights once per eight tokens, and even for one token it is faster
+    // than the ring kernel below (32000 x 4096: 22.8 against 30.1 us)
     if (q4_0_head_mma_ok(m, out_dim, in_dim, x, ldx))
         return launch_q4_0_head_mma(w, x, ldx, y, m, out_dim, in_dim, bias, s);
     {

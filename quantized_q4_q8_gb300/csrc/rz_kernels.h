@@ -163,8 +163,8 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s);
 // bias (nullable) [out_dim] is added to every token's output row
 // Kernels one launch_q4_0_gemv call starts for these shapes (the one-token ring
 // kernel once per token, else one multi-token launch).
-// The Q4_0 GEMV of two to eight tokens per launch on the tensor cores (the LM
-// head of batched decode; gemv_q4_0_mma.cu): rows with in_dim % 256 == 0, x
+// The Q4_0 GEMV of one to eight tokens per launch on the tensor cores (the LM
+// head; gemv_q4_0_mma.cu): rows with in_dim % 256 == 0, x
 // 16-byte aligned, ldx % 4 == 0.  Tokens in equal groups of at most eight.
 bool q4_0_head_mma_ok(int64_t m, int64_t out_dim, int64_t in_dim, const float *x, int64_t ldx);
 int q4_0_head_mma_launches(int64_t m);

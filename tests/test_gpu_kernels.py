@@ -146,14 +146,14 @@ def test_q4k_gemv_padding_invariance(rz):
 
 
 # ----------------------------------------------------------------------------- Q4_0
-# Two or more tokens with in_dim a multiple of 256 run on the tensor-core kernel
-# (token groups of at most eight; 17 rows: one row per CTA; 5000 x 512: ragged
-# last tile; 40000 x 256: 240 rows per CTA, 167 CTAs; 9 tokens: groups of 5 and
-# 4).  Otherwise every token runs on the bulk-copy ring kernel (one launch per
-# token) when a whole number of rows fills 16 bytes and the column warps divide 16
-# (896: two rows, column warps 1; 2048: 2; 4096: 4; 8192: 8; 16384: 16), else (in_dim
-# 32, 992) on the multi-token register kernel
-@pytest.mark.parametrize("out_dim,in_dim,m", [(100, 896, 1), (33, 4096, 1), (7, 32, 1),
+# in_dim a multiple of 256 runs on the tensor-core kernel (token groups of at
+# most eight; 17 rows: one row per CTA; 5000 x 512: ragged last tile; 40000 x 256:
+# 240 rows per CTA, 167 CTAs; 9 tokens: groups of 5 and 4).  Otherwise every token
+# runs on the bulk-copy ring kernel (one launch per token) when a whole number of
+# rows fills 16 bytes and the column warps divide 16 (896: two rows, column warps 1;
+# 1408: two rows, column warps 2), else (in_dim 32, 992) on the multi-token
+# register kernel
+@pytest.mark.parametrize("out_dim,in_dim,m", [(100, 896, 1), (33, 4096, 1), (7, 32, 1), (40, 1408, 1),
                                               (50, 1000 // 32 * 32, 1), (64, 8192, 1),
                                               (102, 2048, 1), (30, 16384, 1), (998, 896, 1),
                                               (40, 896, 3), (17, 4096, 16), (300, 9216, 2),
@@ -184,8 +184,9 @@ def test_q4_0_gemv_tensor_core_bias_and_range(rz):
 
 @pytest.mark.parametrize("vocab,hidden,m", [(v, h, 1) for v, h in S.LM_HEADS] + [(32000, 4096, 16)])
 def test_q4_0_lm_head_full_size(rz, vocab, hidden, m):
-    """Both LM heads at full size, and the Llama head at 16 tokens (the
-    tensor-core kernel, two groups of eight); every logit against the oracle."""
+    """Both LM heads at full size (32000 x 4096 on the tensor-core kernel,
+    151936 x 896 on the ring kernel), and the Llama head at 16 tokens (two groups
+    of eight); every logit against the oracle."""
     w = S.q4_0_weight(f"lm.{vocab}.{hidden}", vocab, hidden)
     x = S.normal(f"lm.x.{hidden}.{m}" if m > 1 else f"lm.x.{hidden}", (m, hidden))
     y = rz.q4_0_gemv(to_dev(w), to_dev(x), vocab, hidden).cpu().numpy()
