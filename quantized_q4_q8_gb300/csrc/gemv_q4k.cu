@@ -427,7 +427,6 @@ cudaError_t launch_epi(const Args &a, int grid, cudaStream_t s, int xin)
 }
 
 }  // namespace
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue);
 namespace {
 
 // Q8_1 activations of m tokens: codes [m][in_dim], then d [m][in_dim/32], then s.
@@ -540,7 +539,7 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
 static cudaError_t launch_mma_groups(const Q4kSegment *seg, int nseg, int epilogue, const Q8Src *x,
                                      const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s)
 {
-    const int64_t ng = q4k_gemv_launch_count(m, in_dim, epilogue);
+    const int64_t ng = q4k_gemv_launch_count(m, in_dim, epilogue, f32in == nullptr);
     const int64_t mc = (m + ng - 1) / ng;
     const int64_t nb = in_dim / 32;
     for (int64_t t0 = 0; t0 < m; t0 += mc) {
@@ -591,10 +590,10 @@ cudaError_t launch_q4k_gemv(const Q4kSegment *seg, int nseg, int epilogue, const
     return launch_common(seg, nseg, epilogue, q8, nullptr, m, in_dim, s);
 }
 
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue)
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue, bool q8_input)
 {
     if (m < kMmaMinTokens) return 1;
-    const int64_t mt = q4k_gemv_mma_group(m, in_dim, epilogue);
+    const int64_t mt = q4k_gemv_mma_group(m, in_dim, epilogue, q8_input);
     return mt < 1 ? 0 : (int)((m + mt - 1) / mt);
 }
 
@@ -603,7 +602,7 @@ bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim)
     if (in_dim > 32LL * kRowWarps * kRowBlocksPerWarp) return false;
     // several tokens: each token group of the tensor-core kernel normalises and
     // quantises its own tokens
-    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, EPI_SWIGLU) >= 1;
+    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, EPI_SWIGLU, false) >= 1;
     return x_smem_bytes(m, in_dim) <= kXSmemMax;
 }
 
@@ -629,7 +628,7 @@ cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, c
 
 bool q4k_gemv_supported(int64_t m, int64_t in_dim, int epilogue)
 {
-    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, epilogue) >= 1;
+    if (m >= kMmaMinTokens) return q4k_gemv_mma_group(m, in_dim, epilogue, true) >= 1;
     const int R = (epilogue == EPI_SWIGLU) ? 2 : 1;
     const int64_t nsb = in_dim / 256;
     const int64_t rpp = (nsb < 8 && 8 % nsb == 0) ? 8 / nsb : 1;

@@ -83,6 +83,7 @@ struct MArgs {
     float eps;
     int NS;               // stages in the ring
     int stage_bytes;      // bytes of a ring slot (the largest stage of any CTA)
+    int xph;              // super-blocks of codes staged at a time (a multiple of 6, or nsb)
     unsigned *err;
     int stall_stage;      // test aid (rz_debug_stall_next_gemv), -1 otherwise
     uint32_t wait_limit;
@@ -110,9 +111,10 @@ __host__ __device__ inline int64_t mma_codes_bytes(int m, int64_t in_dim, bool x
 }
 __host__ __device__ inline int64_t mma_d8_bytes(int64_t in_dim, int nt) { return (in_dim / 32) * 4 * 2 * nt * 4; }
 __host__ __device__ inline int64_t mma_spc_bytes(int64_t in_dim, int nt) { return (in_dim / 256) * 8 * nt * 4 * 16; }
-__host__ __device__ inline int64_t mma_x_bytes(int m, int64_t in_dim, int nt, bool xh)
+// kdim: values of each token's codes staged at a time (in_dim, or a phase of it)
+__host__ __device__ inline int64_t mma_x_bytes(int m, int64_t in_dim, int nt, bool xh, int64_t kdim)
 {
-    return mma_codes_bytes(m, in_dim, xh) + mma_d8_bytes(in_dim, nt) + mma_spc_bytes(in_dim, nt);
+    return mma_codes_bytes(m, kdim, xh) + mma_d8_bytes(in_dim, nt) + mma_spc_bytes(in_dim, nt);
 }
 __host__ __device__ inline int64_t mma_red_bytes(int nt) { return (int64_t)kMW * 32 * 4 * nt * 4; }
 // Super-blocks per stage for a CTA of `tiles` tiles (R halves): 6 or 2 (row
@@ -324,8 +326,12 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     uint8_t *ring = smem;
     uint8_t *xcodes = ring + (int64_t)a.NS * a.stage_bytes;
     static_assert(!XH || XIN == MX_Q8, "f16 activations are staged from Q8_1 input only");
-    const int64_t cpitch = mma_code_pitch(a.in_dim, XH);
-    float *d8t = reinterpret_cast<float *>(xcodes + mma_codes_bytes(a.m, a.in_dim, XH));
+    // Q8_1 input whose codes do not fit beside the ring is staged in phases of
+    // a.xph super-blocks (the d8 and s tables for the whole row stay resident)
+    const bool phased = !XH && XIN == MX_Q8 && a.xph < a.nsb;
+    const int64_t kdim = phased ? (int64_t)a.xph * 256 : a.in_dim;
+    const int64_t cpitch = mma_code_pitch(kdim, XH);
+    float *d8t = reinterpret_cast<float *>(xcodes + mma_codes_bytes(a.m, kdim, XH));
     uint32_t *spc = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(d8t) + mma_d8_bytes(a.in_dim, NT));
     const int64_t nb = a.in_dim / 32;
     // the partial sums of the warps: after the tables, or (XH) in the ring, idle
@@ -406,12 +412,12 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
         csync();
     }
     MmaStore<NT> st{xcodes, d8t, spc, cpitch};
-    if (XIN == MX_Q8) {
-        // codes (offset binary), 16 bytes at a time; d and s into the table.  Each
-        // thread issues all its loads before its first store (one round trip to
-        // L2 rather than one per element).
-        constexpr int kQ = 8;  // int4s per thread and round (16 tokens x 4096 codes: one round)
-        const int n16 = (int)(a.in_dim / 16), nq = a.m * n16;
+    // codes of super-blocks [sb0, sb1) of every token (offset binary, or f16 in
+    // fragment order), 16 bytes at a time.  Each thread issues all its loads
+    // before its first store (one round trip to L2 rather than one per element).
+    constexpr int kQ = 8;  // int4s per thread and round (16 tokens x 4096 codes: one round)
+    auto stage_codes = [&](int sb0, int sb1) {
+        const int n16 = (sb1 - sb0) * 16, nq = a.m * n16;
         for (int q0 = 0; q0 < nq; q0 += kQ * kMW * 32) {
             int4 v[kQ];
 #pragma unroll
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
                 const int q = q0 + u * kMW * 32 + tid;
                 if (q < nq) {
                     const int t = q / n16;
-                    v[u] = __ldg(reinterpret_cast<const int4 *>(a.xq + t * a.in_dim) + (q - t * n16));
+                    v[u] = __ldg(reinterpret_cast<const int4 *>(a.xq + t * a.in_dim + (int64_t)sb0 * 256) + (q - t * n16));
                 }
             }
 #pragma unroll
@@ -443,6 +449,10 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
                 }
             }
         }
+    };
+    if (XIN == MX_Q8) {
+        stage_codes(0, phased ? a.xph : a.nsb);
+        // d and s of the whole row into the tables
         const int nbi = (int)nb, nm = a.m * nbi;
         for (int q0 = 0; q0 < nm; q0 += kQ * kMW * 32) {
             float dv[kQ], sv[kQ];
@@ -489,6 +499,13 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     RingPos rp{0, 0u};
     for (int sl = 0; sl < nslice; ++sl, ring_next(rp, a.NS)) {
         const int s = rp.s;
+        if (phased && sl > 0 && (sl * S) % a.xph == 0) {
+            // the next phase of the codes: every warp is past the slices of the
+            // last one (a.xph is a multiple of S, so no slice straddles two)
+            csync();
+            stage_codes(sl * S, min(a.nsb, sl * S + a.xph));
+            csync();
+        }
         if (!failed && !__all_sync(0xffffffffu, mbar_wait(&full[s], rp.par, lim))) {
             if (lane == 0) set_error(a.err, DEV_TIMEOUT_GEMV);
             failed = true;
@@ -498,8 +515,9 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
             const uint32_t base = smem_after(ring_s);  // ordered after the wait
             const uint32_t t0 = base + (uint32_t)(s * a.stage_bytes + h * hs + (tl * kMTile) * pitch + js * 144);
             const int sbg = sl * S + js;
+            const int sbx = phased ? sbg - (sl * S / a.xph) * a.xph : sbg;  // super-block within the staged codes
             const uint32_t off = base - ring_s;  // 0, carries the ordering to the other tables
-            mma_superblock<NT, XH>(t0 + g * pitch, t0 + (g + 8) * pitch, xrow0 + off + (uint32_t)sbg * (XH ? 512u : 256u), xstep,
+            mma_superblock<NT, XH>(t0 + g * pitch, t0 + (g + 8) * pitch, xrow0 + off + (uint32_t)sbx * (XH ? 512u : 256u), xstep,
                                d8a0 + off + (uint32_t)sbg * (8 * 4 * 2 * NT * 4),
                                spa0 + off + (uint32_t)sbg * (8 * NT * 4 * 16), i, acc);
         }
@@ -536,9 +554,9 @@ __global__ void __launch_bounds__(kMThreads, 1) q4k_gemv_mma_kernel(const __grid
     }
 }
 
-int64_t mma_smem_bytes(int m, int64_t in_dim, int nt, int NS, int stage_bytes, bool xh)
+int64_t mma_smem_bytes(int m, int64_t in_dim, int nt, int NS, int stage_bytes, bool xh, int64_t kdim)
 {
-    return (int64_t)NS * stage_bytes + mma_x_bytes(m, in_dim, nt, xh) + (xh ? 0 : mma_red_bytes(nt)) + 32 * 4 +
+    return (int64_t)NS * stage_bytes + mma_x_bytes(m, in_dim, nt, xh, kdim) + (xh ? 0 : mma_red_bytes(nt)) + 32 * 4 +
            2 * 8 * NS;
 }
 
@@ -618,13 +636,30 @@ MmaPlan mma_plan(const int64_t *rows, int nseg, int R, int nsb)
 
 // Ring stages that fit next to the activations of mt tokens (0 if fewer than
 // two).  xh: the codes as f16, the partial sums in the ring (which must hold them).
-int mma_stages(int mt, int64_t in_dim, int stage_bytes, bool xh = false)
+int mma_stages(int mt, int64_t in_dim, int stage_bytes, bool xh = false, int64_t kdim = 0)
 {
     const int nt = mt > 8 ? 2 : 1;
-    const int64_t fixed = mma_x_bytes(mt, in_dim, nt, xh) + (xh ? 0 : mma_red_bytes(nt)) + 32 * 4 + 1024;
+    const int64_t fixed = mma_x_bytes(mt, in_dim, nt, xh, kdim ? kdim : in_dim) + (xh ? 0 : mma_red_bytes(nt)) +
+                          32 * 4 + 1024;
     const int64_t ns = ((int64_t)std::min<int64_t>(kMSmem, dev_info().smem_optin) - fixed) / (stage_bytes + 16);
     if (ns < 2 || (xh && ns * stage_bytes < mma_red_bytes(nt))) return 0;
     return (int)std::min<int64_t>(ns, 8);
+}
+
+// Super-blocks of int8 codes per phase for mt tokens of Q8_1 input: nsb when the
+// whole row fits beside two stages, else the first of nsb / 2, nsb / 3, ... (up
+// to eight phases, rounded up to a multiple of 6 -- of every slice length) that
+// does; 0 when none does.
+int mma_phase_sb(int mt, int64_t in_dim, int stage_bytes)
+{
+    const int nsb = (int)(in_dim / 256);
+    if (mma_stages(mt, in_dim, stage_bytes) >= 2) return nsb;
+    for (int P = 2; P <= 8; ++P) {
+        const int ph = ((nsb + P - 1) / P + 5) / 6 * 6;
+        if (ph >= nsb) continue;
+        if (mma_stages(mt, in_dim, stage_bytes, false, (int64_t)ph * 256) >= 2) return ph;
+    }
+    return 0;
 }
 
 // The largest ring slot any plan can need: R x the largest half over tile counts.
@@ -639,13 +674,14 @@ int mma_stage_bound(int R, int nsb)
 }  // namespace
 
 // Largest token count per launch whose activations leave room for two stages
-// (of the largest stage any CTA can have).
-int q4k_gemv_mma_group(int64_t m, int64_t in_dim, int epilogue)
+// (of the largest stage any CTA can have); Q8_1 input may stage its codes in
+// phases, f32 input stages the whole row.
+int q4k_gemv_mma_group(int64_t m, int64_t in_dim, int epilogue, bool q8_input)
 {
     const int R = (epilogue == EPI_SWIGLU) ? 2 : 1;
     const int sb = mma_stage_bound(R, (int)(in_dim / 256));
     int64_t mt = std::min<int64_t>(m, 16);
-    while (mt > 0 && mma_stages((int)mt, in_dim, sb) == 0) --mt;
+    while (mt > 0 && (q8_input ? mma_phase_sb((int)mt, in_dim, sb) : mma_stages((int)mt, in_dim, sb)) == 0) --mt;
     return (int)mt;
 }
 
@@ -721,9 +757,12 @@ cudaError_t launch_q4k_gemv_mma(const Q4kSegment *seg, int nseg, int epilogue, c
     // Q8_1 input: the codes staged as f16 in fragment order when two stages still fit
     // beside them (each warp then loads its B fragments instead of converting them)
     const bool xh = !f32in && mma_stages((int)m, in_dim, a.stage_bytes, true) >= 2;
-    a.NS = mma_stages((int)m, in_dim, a.stage_bytes, xh);
+    a.xph = (xh || f32in) ? nsb : mma_phase_sb((int)m, in_dim, a.stage_bytes);
+    if (a.xph < 1) return cudaErrorInvalidConfiguration;
+    const int64_t kdim = (int64_t)a.xph * 256;
+    a.NS = mma_stages((int)m, in_dim, a.stage_bytes, xh, kdim);
     if (a.NS < 2) return cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)mma_smem_bytes((int)m, in_dim, nt, a.NS, a.stage_bytes, xh);
+    const size_t smem = (size_t)mma_smem_bytes((int)m, in_dim, nt, a.NS, a.stage_bytes, xh, kdim);
     if (smem > dev_info().smem_optin) return cudaErrorInvalidConfiguration;
     const int grid = plan.cta_begin[nplan];
     switch (epilogue) {

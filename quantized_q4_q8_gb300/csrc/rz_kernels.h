@@ -98,13 +98,13 @@ bool q4k_gemv_f32_input_ok(int64_t m, int64_t in_dim);
 // norm / quantise launch first).
 bool q4k_gemv_f32_input_preferred(int64_t m, int64_t in_dim);
 // launches one GEMV of m tokens takes (token groups when the activations exceed
-// shared memory)
-int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue);
+// shared memory; Q8_1 input stages its codes in phases first)
+int q4k_gemv_launch_count(int64_t m, int64_t in_dim, int epilogue, bool q8_input = true);
 
 // From this many tokens on, the GEMV runs on the tensor cores (gemv_q4k_mma.cu).
 constexpr int kMmaMinTokens = 4;
 // Most tokens one tensor-core launch takes for this shape (0: none fit).
-int q4k_gemv_mma_group(int64_t m, int64_t in_dim, int epilogue);
+int q4k_gemv_mma_group(int64_t m, int64_t in_dim, int epilogue, bool q8_input);
 cudaError_t launch_q4k_gemv_mma(const Q4kSegment *seg, int nseg, int epilogue, const int8_t *xq, const float *xd,
                                 const float *xs, const F32Input *f32in, int64_t m, int64_t in_dim, cudaStream_t s);
 cudaError_t launch_q4k_gemv_f32(const Q4kSegment *seg, int nseg, int epilogue, const F32Input &in,
