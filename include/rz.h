@@ -201,7 +201,11 @@ rz_status rz_q4k_f32_gemv(const void *w, const float *x, const float *bias, floa
  * GpuModelQ4::forward, q4_0_gemv_into; step 5 of that function).
  *   w  Q4_0 [out_dim][in_dim]   x  f32 [m][in_dim]   y  f32 [m][out_dim]
  *   in_dim % 32 == 0, 1 <= m <= RZ_MAX_BATCH.  Only w needs 16-byte alignment of
- *   its base; rows of 18-byte blocks may start anywhere.
+ *   its base; rows of 18-byte blocks may start anywhere.  When in_dim % 256 == 0
+ *   and x is 16-byte aligned the products run on the tensor cores with x split
+ *   into two f16 pieces (x to about 2^-22 relative; |x| must stay below 65504);
+ *   otherwise in f32 FMAs.  f32 accumulation either way (order differs from a
+ *   sequential sum; deterministic run to run).
  */
 rz_status rz_q4_0_gemv(const void *w, const float *x, float *y, int64_t m, int64_t out_dim,
                        int64_t in_dim, rz_stream stream);
