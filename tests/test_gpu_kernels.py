@@ -94,6 +94,9 @@ GEMV_CASES = [
     # 16 units per CTA on 152 SMs (16 row pairs; 16 packs of two short rows): the
     # one-token launch takes its 16-warp instantiation
     (4864, 2048, 1), (4800, 1024, 1),
+    # tensor-core GEMV whose int8 codes do not fit at once: staged in phases of K
+    # (11008 and 14336 at 12 and 16 tokens; 22528: more phases)
+    (300, 11008, 16), (100, 14336, 12), (64, 22528, 16),
 ]
 
 
