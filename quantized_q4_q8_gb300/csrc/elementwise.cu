@@ -14,6 +14,8 @@
 // realizar 0.8.5 src/cuda/executor/layers/forward_utils.rs).  One CTA per row;
 // the sum of squares is reduced in a fixed order (deterministic).  When a Q8_1
 // output is requested the same kernel quantises the f32 y it just produced.
+#include <algorithm>
+
 #include "rz_common.cuh"
 #include "rz_kernels.h"
 
@@ -52,30 +54,42 @@ constexpr int kNormThreads = 32 * kRowWarps;  // 512: the register-row layout
 
 // Rows up to kRowWarps * kRowBlocksPerWarp * 32 values, reduced in the same
 // fixed order as the GEMV prologue, so the fused and the separate paths give
-// identical bits.
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
+// identical bits.  `parts` CTAs share a row: each reduces the whole row (the
+// same order, so the same scale) and writes its share of the blocks -- block
+// warp + 16 k goes to part k % parts -- so that a warp's quantisations, a chain
+// of shuffles each, are few (one CTA per row took about 8 us for four rows of
+// 4096 values, most of it eight blocks in turn per warp).
+__global__ void __launch_bounds__(kNormThreads, 1) rmsnorm_kernel(
     const float *__restrict__ x, const float *__restrict__ gamma, float *__restrict__ y,
     int8_t *__restrict__ q, float *__restrict__ qd, float *__restrict__ qs, int64_t n,
-    int64_t n_pad, float eps)
+    int64_t n_pad, float eps, int parts)
 {
     __shared__ float red[kRowWarps + 1];
-    const int64_t row = blockIdx.x;
+    const int64_t row = blockIdx.x / parts;
+    const int part = (int)(blockIdx.x % parts);
     const float *xr = x + row * n_pad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();
     pdl_wait();
     const int64_t nb = (n_pad + 31) / 32;
     const float scale = rms_scale(row_sumsq(xr, nb, n, warp, lane, red, [] { __syncthreads(); }), n, eps);
-    for (int k0 = 0; k0 < kRowBlocksPerWarp; k0 += 8) {
+    for (int k0 = part; k0 < kRowBlocksPerWarp; k0 += 8 * parts) {
         if (warp + (int64_t)kRowWarps * k0 >= nb) break;
-        RowBatch rb;
-        row_batch(xr, gamma, nb, n, warp, lane, k0, rb);
+        float rv[8], rg[8];  // values and gammas of 8 blocks, loaded before any use
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
+            const int64_t b = warp + (int64_t)kRowWarps * (k0 + u * parts);
+            const int64_t i = b * 32 + lane;
+            const bool in = b < nb && i < n;
+            rv[u] = in ? __ldg(xr + i) : 0.0f;
+            rg[u] = (in && gamma) ? __ldg(gamma + i) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t b = warp + (int64_t)kRowWarps * (k0 + u * parts);
             if (b >= nb) break;
             const int64_t i = b * 32 + lane;
-            const float v = (i < n) ? __fmul_rn(__fmul_rn(rb.v[u], scale), rb.g[u]) : 0.0f;
+            const float v = (i < n) ? __fmul_rn(__fmul_rn(rv[u], scale), rg[u]) : 0.0f;
             if (y && i < n_pad) y[row * n_pad + i] = v;
             if (q) q8_block_store(v, lane, q + row * n_pad + b * 32, qd + row * (n_pad / 32) + b,
                                   qs + row * (n_pad / 32) + b);
@@ -164,8 +178,12 @@ cudaError_t launch_rmsnorm(const float *x, const float *gamma, float *y, void *q
     int8_t *q = static_cast<int8_t *>(q8);
     float *qd = q ? reinterpret_cast<float *>(q + m * n_pad) : nullptr;
     float *qs = q ? qd + m * (n_pad / 32) : nullptr;
+    // CTAs per row: about one block per warp (16 blocks a CTA), bounded by the SMs
+    const int64_t nb = (n_pad + 31) / 32;
+    int parts = (int)std::max<int64_t>(1, std::min<int64_t>((nb + kRowWarps - 1) / kRowWarps, 8));
+    while (parts > 1 && m * parts > dev_info().sm_count) --parts;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)m);
+    cfg.gridDim = dim3((unsigned)(m * parts));
     cfg.blockDim = dim3(kNormThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -173,7 +191,7 @@ cudaError_t launch_rmsnorm(const float *x, const float *gamma, float *y, void *q
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, gamma, y, q, qd, qs, n, n_pad, eps);
+    return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, gamma, y, q, qd, qs, n, n_pad, eps, parts);
 }
 
 cudaError_t launch_residual_add(const float *a, const float *b, float *out, int64_t n,

@@ -307,27 +307,6 @@ __device__ __forceinline__ float row_value(const float *x, int64_t nb, int64_t n
     return (b < nb && i < n_valid) ? ld_act<CG>(x + i) : 0.0f;
 }
 
-// The values (and gammas, when given) of 8 consecutive blocks k0 .. k0+7 of this
-// warp, loaded before any use so that stores to shared memory between them
-// cannot hold the loads back.  Gammas are weights: always the read-only path.
-struct RowBatch {
-    float v[8], g[8];
-};
-
-template <bool CG = false>
-__device__ __forceinline__ void row_batch(const float *x, const float *gamma, int64_t nb, int64_t n_valid,
-                                          int warp, int lane, int k0, RowBatch &r)
-{
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int64_t b = warp + (int64_t)kRowWarps * (k0 + u);
-        const int64_t i = b * 32 + lane;
-        const bool in = b < nb && i < n_valid;
-        r.v[u] = in ? ld_act<CG>(x + i) : 0.0f;
-        r.g[u] = (in && gamma) ? __ldg(gamma + i) : 0.0f;
-    }
-}
-
 // Sum of squares of the row in a fixed order: per thread over its blocks in
 // ascending block order, then the xor butterfly of each warp, then the butterfly
 // over the 16 warp sums.  `red` holds 17 floats of shared memory; `sync`
