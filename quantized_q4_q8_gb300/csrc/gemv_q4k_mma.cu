@@ -1,5 +1,5 @@
 // gemv_q4k_mma.cu -- Q4_K weight x Q8_1 activation GEMV for several tokens
-// (batched decode, 2..16 tokens per launch) on the tensor cores.
+// (batched decode, 4..16 tokens per launch) on the tensor cores.
 //
 // Operation: the one of gemv_q4k.cu (q4k_q8_gemv_async of realizar 0.8.5
 // src/cuda/executor/cached.rs, transformer_layer_gpu_true_dp4a), for every row r
@@ -41,7 +41,12 @@
 // stages (Q8_1 input; the warps' partial sums then reuse the idle ring), else as
 // int8 in offset binary that every warp converts per fragment -- and per
 // sub-block and lane group the d8 and s of the four tokens that lane group's
-// accumulator columns hold.  Every wait is bounded.
+// accumulator columns hold.  When even the int8 codes of a Q8_1 input do not fit
+// beside two stages (16 tokens at in_dim 11008 or 14336), they are staged one
+// phase of K at a time (a multiple of 6 super-blocks, so no slice straddles two
+// phases; the tables of the whole row stay resident): at each boundary the
+// consumer warps meet, restage, and go on while the producer keeps the ring
+// full.  f32 input runs in token groups instead.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include <algorithm>
