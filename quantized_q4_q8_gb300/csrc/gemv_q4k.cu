@@ -8,9 +8,10 @@
 //
 // GB300 design.  The kernel streams 144-byte super-blocks from HBM; compute is
 // a few dp4a per byte.  One CTA per SM owns a contiguous range of rows.  A
-// producer warp keeps a ring of 16-32 KB shared-memory stages full with the 1-D
-// bulk copy engine (cp.async.bulk, completion counted on an mbarrier), so the
-// bytes in flight live in shared memory, not registers.  (Prefetching the rest
+// producer warp keeps a ring of two shared-memory stages (each about half of
+// what the activations leave) full with the 1-D bulk copy engine
+// (cp.async.bulk in copies of at most 12 KB, completion counted on an
+// mbarrier), so the bytes in flight live in shared memory, not registers.  (Prefetching the rest
 // of the CTA's rows into L2 up front was measured slower: it queues ahead of
 // the ring's own copies and of the activation loads.)  A stage
 // holds whole "packs" (one row, or 8/nsb rows when a row has fewer than 8
@@ -54,6 +55,16 @@ constexpr int kCtaSmem = 200 * 1024;
 constexpr int kCtaSmem1 = 200 * 1024;
 constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
 constexpr int kMaxStages = 16;
+// Bytes per bulk copy of a stage's rows (whole rows, at least one).  Measured
+// on the 32-layer decode step against one copy per contiguous run of rows
+// (about 90 KB per stage): rows of 2304 bytes copied 5 at a time and rows of
+// 6192 bytes one at a time, 1.471 -> 1.406 ms; 2, 3 or 4 rows of 2304 bytes at
+// a time (the 6192-byte rows one at a time): +5.2%, -0.4%, -3.7%; 6192-byte
+// rows two or three at a time (the short rows five at a time): -0.2%, +0.8%.
+// The SwiGLU pair keeps a copy per row and half: its gate and up rows
+// interleaved pack by pack beat both halves laid out in blocks of rows, copied
+// whole (+1.7%) or 8-16 KB at a time (+2.8%).
+constexpr int64_t kCopyBytes = 12 * 1024;
 
 struct Args {
     const uint8_t *w[3];
@@ -171,7 +182,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) q4k_gemv_kernel(const Args a
                     while (r < n) {
                         const int64_t u = u0 + r;
                         const int kseg = seg_of(a, u);
-                        const int run = (int)min((int64_t)(n - r), a.seg_begin[kseg + 1] - u);
+                        // whole rows, at most kCopyBytes per copy
+                        const int run = (int)min(min((int64_t)(n - r), a.seg_begin[kseg + 1] - u),
+                                                 (int64_t)max(1, (int)(kCopyBytes / a.row_bytes)));
                         bulk_g2s_hint(dst + (int64_t)r * a.row_bytes,
                                  a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
                                  (unsigned)(run * a.row_bytes), &full[s], pol);
