@@ -55,12 +55,15 @@ constexpr int kCtaSmem = 200 * 1024;
 constexpr int kCtaSmem1 = 200 * 1024;
 constexpr int kXSmemMax = 128 * 1024;  // activations staged up to this size (the ring keeps >= 70 KB)
 constexpr int kMaxStages = 16;
-// Bytes per bulk copy of a stage's rows (whole rows, at least one).  Measured
-// on the 32-layer decode step against one copy per contiguous run of rows
-// (about 90 KB per stage): rows of 2304 bytes copied 5 at a time and rows of
-// 6192 bytes one at a time, 1.471 -> 1.406 ms; 2, 3 or 4 rows of 2304 bytes at
-// a time (the 6192-byte rows one at a time): +5.2%, -0.4%, -3.7%; 6192-byte
-// rows two or three at a time (the short rows five at a time): -0.2%, +0.8%.
+// Bytes per bulk copy of a stage's rows (whole rows, at least one; the row
+// count is worked out on the host: left as a 64-bit division inside the
+// producer loop, it slowed the step by 9%).  Measured on the 32-layer decode step against
+// one copy per contiguous run of rows (about 90 KB per stage): rows of 2304
+// bytes copied 5 at a time and rows of 6192 bytes one at a time, 1.471 -> 1.406
+// ms; 2, 3 or 4 rows of 2304 bytes at a time (the 6192-byte rows one at a
+// time): +5.2%, -0.4%, -3.7%; 6192-byte rows two or three at a time (the short
+// rows five at a time): -0.2%, +0.8%.  A CTA whose rows fit one stage (the
+// 4096 x 4096 projection: 27 rows) copies them whole: 1.408 -> 1.402 ms.
 // The SwiGLU pair keeps a copy per row and half: its gate and up rows
 // interleaved pack by pack beat both halves laid out in blocks of rows, copied
 // whole (+1.7%) or 8-16 KB at a time (+2.8%).
@@ -85,6 +88,7 @@ struct Args {
     int PS;                // packs per stage
     int NS;                // stages in the ring
     int stage_bytes;       // PS * rpp * R * row_bytes
+    int copy_rows;         // rows per bulk copy (kCopyBytes of whole rows, at least one)
     int x_smem;            // activations staged (swizzled) in shared memory
     // f32 input quantised in the kernel (XIN_NORM / XIN_F32)
     const float *xf;
@@ -155,6 +159,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) q4k_gemv_kernel(const Args a
             int64_t k = 0;
             bool ok = true;
             RingPos rp{0, 0u};
+            // rows per copy; a CTA whose rows fit one stage copies each run whole
+            const int crows = nstages == 1 ? 0x7fffffff : a.copy_rows;
             for (; k < nstages; ++k, ring_next(rp, a.NS)) {
                 const int s = rp.s;
                 if (k >= a.NS && !mbar_wait(&empty[s], rp.par ^ 1u, lim)) {
@@ -182,9 +188,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) q4k_gemv_kernel(const Args a
                     while (r < n) {
                         const int64_t u = u0 + r;
                         const int kseg = seg_of(a, u);
-                        // whole rows, at most kCopyBytes per copy
-                        const int run = (int)min(min((int64_t)(n - r), a.seg_begin[kseg + 1] - u),
-                                                 (int64_t)max(1, (int)(kCopyBytes / a.row_bytes)));
+                        const int run = (int)min((int64_t)min(n - r, crows), a.seg_begin[kseg + 1] - u);
                         bulk_g2s_hint(dst + (int64_t)r * a.row_bytes,
                                  a.w[kseg] + (u - a.seg_begin[kseg]) * a.row_bytes,
                                  (unsigned)(run * a.row_bytes), &full[s], pol);
@@ -512,6 +516,7 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
         g_stall_next_gemv = 0;  // one launch only
     }
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
+    a.copy_rows = (int)std::max<int64_t>(1, kCopyBytes / a.row_bytes);
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
     // Two stages, each half of the shared memory left beside the activations.
     // Every consumer warp waits on every stage (a few hundred cycles per wait on
