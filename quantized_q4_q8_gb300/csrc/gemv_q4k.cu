@@ -518,15 +518,22 @@ static cudaError_t launch_core(const Q4kSegment *seg, int nseg, int epilogue, co
     a.rpp = (a.nsb < 8 && 8 % a.nsb == 0) ? 8 / a.nsb : 1;
     a.copy_rows = (int)std::max<int64_t>(1, kCopyBytes / a.row_bytes);
     const int64_t pack = (int64_t)R * a.rpp * a.row_bytes;
-    // Two stages, each half of the shared memory left beside the activations.
-    // Every consumer warp waits on every stage (a few hundred cycles per wait on
+    // Two stages (four in one case, below), each half of the shared memory left
+    // beside the activations.  Every consumer warp waits on every stage (a few hundred cycles per wait on
     // this GPU) and a small stage leaves most warps without a row pair in it, so
     // fewer, larger stages win even though the first one lands later; the bytes
     // in flight (one stage, ~90 KB per SM) still cover the HBM latency.
     const int64_t xbytes = x_smem_bytes(m, in_dim);
     a.x_smem = (xbytes <= kXSmemMax || f32in) ? 1 : 0;
     const int64_t budget = (int64_t)(m == 1 ? kCtaSmem1 : kCtaSmem) - (a.x_smem ? xbytes : 0) - 1024;
-    const int64_t tgt = budget / 2;
+    // The stand-alone product of one token (Q8_1 in, plain store out) streams
+    // best through four stages when a CTA's rows do not fit the ring at once
+    // (4096 x 14336: 8.85 -> 8.16 us, 14336 x 4096: 8.46 -> 7.89 us); the fused
+    // launches of the decode step keep two (four there: O +0.45%, gate/up
+    // +0.7%, down +1.8% per step).
+    const int64_t cta_rows = (units + dev_info().sm_count - 1) / dev_info().sm_count;
+    const bool four = m == 1 && xin == XIN_Q8 && epilogue == EPI_STORE && cta_rows * R * a.row_bytes > budget;
+    const int64_t tgt = budget / (four ? 4 : 2);
     a.PS = (int)std::max<int64_t>(1, tgt / pack);
     if (a.rpp == 1 && (a.PS & 1) && a.PS > 1) a.PS -= 1;  // row pairs: an even pack count per stage
     a.stage_bytes = (int)(a.PS * pack);
