@@ -87,6 +87,68 @@ def test_argument_checks_fail_before_launch(lib, call, args, status):
     assert _lib.last_error()
 
 
+@pytest.mark.parametrize("call,args,status", [
+    ("rz_q4k_q8_subblock_dots", (16, 16, 16, 1, 300, None), 2),           # in_dim % 256
+    ("rz_q4k_q8_subblock_dots", (16, 16, 0, 1, 256, None), 1),            # null output
+    ("rz_q4k_q8_subblock_dots", (16, 16, 20, 1, 256, None), 3),           # misaligned output
+    ("rz_q4k_q8_gemv_ex", (16, 16, 16, 16, 16, 0, 1, 4, 256, None), 6),   # bias and residual
+    ("rz_q4k_q8_gemv_ex", (16, 16, None, None, 16, 3, 1, 4, 256, None), 2),   # ld < out_dim
+    ("rz_q4k_q8_gemv_ex", (16, 16, 18, None, 16, 0, 1, 4, 256, None), 3),     # bias not 4-byte aligned
+    ("rz_q4k_q8_gemv_ex", (16, 16, None, 24, 16, 0, 1, 4, 256, None), 3),     # residual misaligned
+    ("rz_q4k_q8_gemm", (16, 16, 16, 0, 1, 4, 300, 16, 1 << 20, None), 2),     # in_dim % 256
+    ("rz_q4k_q8_gemm", (16, 16, 16, 3, 1, 4, 256, 16, 1 << 20, None), 2),     # ldy < out_dim
+    ("rz_q4k_q8_gemm", (16, 16, 16, 0, 1, 4, 256, None, 1 << 20, None), 1),   # no workspace
+    ("rz_q4k_q8_gemm", (16, 16, 16, 0, 1, 4, 256, 16, 16, None), 1),          # workspace too small
+    ("rz_q4k_q8_gemm", (16, 16, 18, 0, 1, 4, 256, 16, 1 << 20, None), 3),     # y not 4-byte aligned
+    ("rz_q4k_f32_gemv", (16, 16, None, 16, 17, 4, 256, None), 2),         # m > 16
+    ("rz_q4k_f32_gemv", (16, 16, None, 16, 1, 4, 300, None), 2),          # in_dim % 256
+    ("rz_q4k_f32_gemv", (16, 20, None, 16, 1, 4, 256, None), 3),          # x misaligned
+    ("rz_q4k_f32_gemv", (16, 16, 18, 16, 1, 4, 256, None), 3),            # bias not 4-byte aligned
+    ("rz_q4_0_gemv_bias", (16, 16, None, 16, 1, 4, 32, None), 1),         # no bias
+    ("rz_q4_0_gemv_bias", (16, 16, 16, 16, 1, 4, 48, None), 2),           # in_dim % 32
+    ("rz_debug_stall_next_gemv", (100,), 1),                              # limit below 1024
+    ("rz_debug_stall_next_gemv", ((1 << 22) + 1,), 1),                    # limit above 2^22
+])
+def test_more_argument_checks_fail_before_launch(lib, call, args, status):
+    """The same for the other GEMV, GEMM and test-aid entry points."""
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    st = _lib.status(call, *args)
+    assert st == status, (st, _lib.last_error())
+    assert _lib.last_error()
+
+
+def test_multi_matrix_argument_checks(lib):
+    """rz_q4k_q8_gemv_multi and rz_rmsnorm_q4k_gemv take arrays of matrices: their
+    count, rows, alignment and output stride are checked on the host."""
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    w = (C.c_void_p * 3)(16, 32, 48)
+    rows = (C.c_int64 * 3)(4, 4, 4)
+    bad_w = (C.c_void_p * 3)(16, 40, 48)       # second matrix misaligned
+    bad_rows = (C.c_int64 * 3)(4, 0, 4)        # empty second matrix
+    bias = (C.c_void_p * 3)(16, 18, 16)        # second bias not 4-byte aligned
+    cases = [
+        (("rz_q4k_q8_gemv_multi", 16, 4, w, rows, None, 16, 12, 1, 256, None), 1),       # n_mats > 3
+        (("rz_q4k_q8_gemv_multi", 16, 3, w, rows, None, 16, 12, 17, 256, None), 2),     # m > 16
+        (("rz_q4k_q8_gemv_multi", 16, 3, w, rows, None, 16, 12, 1, 300, None), 2),      # in_dim % 256
+        (("rz_q4k_q8_gemv_multi", 16, 3, bad_w, rows, None, 16, 12, 1, 256, None), 3),
+        (("rz_q4k_q8_gemv_multi", 16, 3, w, bad_rows, None, 16, 12, 1, 256, None), 1),
+        (("rz_q4k_q8_gemv_multi", 16, 3, w, rows, bias, 16, 12, 1, 256, None), 3),
+        (("rz_q4k_q8_gemv_multi", 16, 3, w, rows, None, 16, 11, 1, 256, None), 2),      # ldy < 12 rows
+        (("rz_rmsnorm_q4k_gemv", 16, 256, 16, 256, 1e-6, 0, w, rows, None, 16, 12, 1, 256, None), 1),
+        (("rz_rmsnorm_q4k_gemv", 16, 256, 16, 300, 1e-6, 3, w, rows, None, 16, 12, 1, 256, None), 2),  # n > in_dim
+        (("rz_rmsnorm_q4k_gemv", 16, 128, 16, 256, 1e-6, 3, w, rows, None, 16, 12, 1, 256, None), 2),  # ldx < in_dim
+        (("rz_rmsnorm_q4k_gemv", 16, 256, 16, 256, -1.0, 3, w, rows, None, 16, 12, 1, 256, None), 1),  # eps < 0
+        (("rz_rmsnorm_q4k_gemv", 16, 256, 16, 256, 1e-6, 3, bad_w, rows, None, 16, 12, 1, 256, None), 3),
+        (("rz_rmsnorm_q4k_gemv", 16, 256, 16, 256, 1e-6, 3, w, rows, None, 16, 8, 1, 256, None), 2),  # ldy
+    ]
+    for args, status in cases:
+        st = _lib.status(*args)
+        assert st == status, (args[0], st, _lib.last_error())
+        assert _lib.last_error()
+
+
 def test_package_fails_loudly_without_library(tmp_path):
     from quantized_q4_q8_gb300 import _lib
     with pytest.raises(ImportError):
