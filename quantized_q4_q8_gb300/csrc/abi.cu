@@ -434,8 +434,6 @@ namespace {
 rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, LayerDesc *out)
 {
     if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
-    // the shape limits below depend on the device's shared memory
-    RZ_TRY(check_device());
     const bool fused = !w->wk && !w->wv;
     const void *ptrs[] = {w->wq, fused ? w->wq : w->wk, fused ? w->wq : w->wv, w->wo, w->wgate, w->wup, w->wdown,
                           w->attn_gamma, w->ffn_gamma};
@@ -457,6 +455,8 @@ rz_status check_layer(const rz_layer_weights *w, const char *fn, int64_t m, Laye
     if (w->n_heads / w->n_kv_heads > 16) return fail(RZ_ERR_UNSUPPORTED, "%s: more than 16 query heads per kv head", fn);
     if (w->head_dim < 32 || w->head_dim > 256 || w->head_dim % 32)
         return fail(RZ_ERR_SHAPE, "%s: head_dim=%d (multiple of 32 in [32, 256])", fn, w->head_dim);
+    // the limits from here on depend on the device's shared memory
+    RZ_TRY(check_device());
     if (attention_smem_bytes(w->n_heads / w->n_kv_heads, w->head_dim, 0) > dev_info().smem_optin)
         return fail(RZ_ERR_UNSUPPORTED, "%s: head_dim=%d with %d query heads per kv head needs more shared memory "
                     "than a CTA has", fn, w->head_dim, w->n_heads / w->n_kv_heads);
@@ -706,7 +706,6 @@ rz_status rz_decode_layers(const float *input, const rz_layer_weights *layers, c
 static rz_status check_layer_q4_0(const rz_layer_weights_q4_0 *w, const char *fn, int64_t m, LayerQ40Desc *out)
 {
     if (!w) return fail(RZ_ERR_INVALID_ARG, "%s: null layer descriptor", fn);
-    RZ_TRY(check_device());
     const void *ptrs[] = {w->wqkv, w->wo, w->wup, w->wdown, w->attn_gamma, w->ffn_gamma};
     for (const void *p : ptrs) {
         if (!p) return fail(RZ_ERR_INVALID_ARG, "%s: null weight pointer", fn);
@@ -721,6 +720,8 @@ static rz_status check_layer_q4_0(const rz_layer_weights_q4_0 *w, const char *fn
         return fail(RZ_ERR_SHAPE, "%s: n_heads=%d n_kv_heads=%d", fn, w->n_heads, w->n_kv_heads);
     if (w->head_dim < 32 || w->head_dim > 256 || w->head_dim % 32)
         return fail(RZ_ERR_SHAPE, "%s: head_dim=%d (multiple of 32 in [32, 256])", fn, w->head_dim);
+    // the limits from here on depend on the device's shared memory
+    RZ_TRY(check_device());
     if (attention_smem_bytes(w->n_heads / w->n_kv_heads, w->head_dim, 0) > dev_info().smem_optin)
         return fail(RZ_ERR_UNSUPPORTED, "%s: the attention of this head shape does not fit a CTA", fn);
     if (!(w->eps >= 0.0f) || !(w->rope_theta > 0.0f)) return fail(RZ_ERR_INVALID_ARG, "%s: eps/rope_theta", fn);

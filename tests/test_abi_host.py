@@ -149,6 +149,64 @@ def test_multi_matrix_argument_checks(lib):
         assert _lib.last_error()
 
 
+def _llama_like_layer(_lib, **over):
+    f = dict(wq=16, wk=32, wv=48, wo=64, wgate=80, wup=96, wdown=112, attn_gamma=128, ffn_gamma=144,
+             hidden=4096, hidden_pad=4096, n_heads=32, n_kv_heads=32, head_dim=128, inter=11008,
+             eps=1e-6, rope_theta=1e4, rope_mode=0, bq=None, bk=None, bv=None)
+    f.update(over)
+    return _lib.LayerWeightsStruct(**f)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(wo=72), 3),                          # a weight not 16-byte aligned
+    (dict(wup=None), 1),                       # a weight missing
+    (dict(wk=None, wv=None, bk=16), 1),        # fused Q|K|V with its K bias apart
+    (dict(bq=18), 3),                          # bias not 4-byte aligned
+    (dict(hidden_pad=4000), 2),                # hidden_pad not a multiple of 256
+    (dict(hidden_pad=3840), 2),                # hidden_pad < hidden
+    (dict(n_kv_heads=5), 2),                   # n_heads % n_kv_heads
+    (dict(n_kv_heads=1), 6),                   # 32 query heads per kv head
+    (dict(head_dim=48), 2),                    # head_dim not a multiple of 32
+    (dict(head_dim=512), 2),                   # head_dim beyond 256
+])
+def test_layer_descriptor_checks_fail_before_the_device(lib, over, status):
+    """rz_decode_layer validates the layer descriptor on the host before it
+    queries the device (whose shared memory bounds the remaining checks)."""
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    L = _llama_like_layer(_lib, **over)
+    st = _lib.status("rz_decode_layer", 16, C.byref(L), None, None, 0, 1, 16, None, 0, None)
+    assert st == status, (st, _lib.last_error())
+    assert _lib.last_error()
+    # the batch size is checked with the descriptor
+    st = _lib.status("rz_decode_layer", 16, C.byref(_llama_like_layer(_lib)), None, None, 0, 17, 16, None, 0, None)
+    assert st == 2, (st, _lib.last_error())
+
+
+def test_valid_layer_descriptor_reaches_the_device_check(lib):
+    """A descriptor that passes the host checks is next refused for what is
+    missing: here no sm_103a device (or, on a GPU machine, the missing KV cache)."""
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    st = _lib.status("rz_decode_layer", 16, C.byref(_llama_like_layer(_lib)), None, None, 0, 1, 16, None, 0, None)
+    assert st != 0 and _lib.last_error()
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(wo=24), 3), (dict(wdown=None), 1), (dict(hidden=100), 2), (dict(inter=1000), 2),
+    (dict(n_kv_heads=3), 2), (dict(head_dim=40), 2),
+])
+def test_q4_0_layer_descriptor_checks(lib, over, status):
+    from quantized_q4_q8_gb300 import _lib
+    _lib.load()
+    f = dict(wqkv=16, wo=32, wgate=48, wup=64, wdown=80, attn_gamma=96, ffn_gamma=112, hidden=896,
+             n_heads=14, n_kv_heads=2, head_dim=64, inter=4864, eps=1e-6, rope_theta=1e6, rope_mode=1)
+    f.update(over)
+    L = _lib.LayerWeightsQ40Struct(**f)
+    st = _lib.status("rz_decode_layer_q4_0", 16, C.byref(L), None, None, 0, 1, 16, None, 0, None)
+    assert st == status, (st, _lib.last_error())
+
+
 def test_package_fails_loudly_without_library(tmp_path):
     from quantized_q4_q8_gb300 import _lib
     with pytest.raises(ImportError):
